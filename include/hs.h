@@ -1,0 +1,172 @@
+/*
+ * hs.h -- C ABI of libhs: activation-sparse decode and prefill of a ReLU^2
+ * mixture-of-experts layer with 4-bit weights, for NVIDIA GB300 (sm_103a).
+ *
+ * The method is the one described on "Skipping dead neurons: a faster
+ * Nemotron 3.5 Lightning on Apple silicon" (sevren.ai, "Heimr Sparse Down").
+ * Each declaration below cites the section of that page that defines the
+ * operation.
+ *
+ * Conventions (all entry points):
+ *  - Every pointer argument named *_dev, and every pointer inside hs_w4,
+ *    hs_expert, hs_decode_debug, is a DEVICE pointer owned by the caller.
+ *    Descriptor structs themselves (hs_w4, hs_expert, hs_moe_layer) are read
+ *    on the host during the call and may be freed when it returns.
+ *  - The library allocates no memory.  Scratch comes from a caller-supplied
+ *    device workspace whose size the matching *_workspace_size call returns.
+ *  - Calls are asynchronous on the given stream (NULL = legacy default
+ *    stream): a return of HS_OK means the work was enqueued.  Outputs are
+ *    valid once the stream reaches that point.
+ *  - Weight, activation and output pointers must be 16-byte aligned; offsets
+ *    and logits 4-byte aligned.  Violations return HS_ERR_MISALIGNED.
+ *  - Errors are returned, never aborted on.  Nothing is enqueued when an
+ *    entry point returns an argument error.
+ *  - fp16 and bf16 values are passed as raw 16-bit patterns (uint16_t).
+ *
+ * 4-bit weight format (section "The whole decode step": one scale for every
+ * group of 64 along the input axis of the projection):
+ *   w = scale * q + bias,  q in 0..15,  scale and bias fp16.
+ * Codes are packed two per byte; the element with the even index along the
+ * packed axis sits in the low nibble.
+ *
+ * Layouts used by the library:
+ *   up projection (rows = neurons, packed along hidden; groups along hidden):
+ *     codes  [neurons][hidden/2] bytes
+ *     sb     [neurons][hidden/64] pairs (scale, bias) of fp16 (4 bytes)
+ *   neuron-major down projection (section "Transposing to skip the zeros":
+ *   the down weights stored transposed, one row per neuron, so that a dead
+ *   neuron's row is skipped in one piece):
+ *     codes  [neurons][hidden/2] bytes, packed along the outputs
+ *     sb     [neurons/64][hidden] pairs (scale, bias) of fp16 (4 bytes):
+ *            one slab of hidden pairs per group of 64 neurons
+ *   checkpoint (output-major) down projection, the repacker's input
+ *   (section "Two layouts, one problem": one row per output):
+ *     codes  [hidden][neurons/2], scale/bias [hidden][neurons/64] fp16
+ */
+#ifndef HS_H_
+#define HS_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Opaque CUDA stream (binary compatible with cudaStream_t). */
+typedef struct CUstream_st* hs_stream_t;
+
+/* Status codes. */
+#define HS_OK                     0
+#define HS_ERR_INVALID_ARG       -1  /* NULL where required, negative size, ... */
+#define HS_ERR_MISALIGNED        -2  /* a pointer breaks the alignment rule     */
+#define HS_ERR_UNSUPPORTED_SHAPE -3  /* sizes outside what the kernels support */
+#define HS_ERR_WORKSPACE         -4  /* workspace NULL or smaller than needed  */
+#define HS_ERR_CUDA              -5  /* a CUDA launch or query failed          */
+#define HS_ERR_TIMEOUT           -6  /* a bounded device wait gave up          */
+
+/* Flags. */
+#define HS_FORCE_DENSE  0x1u  /* read every neuron row and every scale group:
+                                 the dense comparison path through the same
+                                 kernels (section "The standard way reads
+                                 everything"); results equal the sparse path */
+
+/* One 4-bit projection in one of the layouts above. */
+typedef struct {
+    const uint8_t* codes;  /* device */
+    const void*    sb;     /* device, interleaved fp16 (scale, bias) pairs */
+} hs_w4;
+
+/* One expert: up projection, neuron-major down projection, offsets. */
+typedef struct {
+    hs_w4        up;         /* codes [neurons][hidden/2], sb [neurons][hidden/64] */
+    hs_w4        down_nm;    /* codes [neurons][hidden/2], sb [neurons/64][hidden] */
+    const float* up_offset;  /* device [neurons] pre-activation offsets, or NULL (= 0) */
+    int          neurons;    /* multiple of 64 */
+} hs_expert;
+
+/* One MoE layer (section "Inside a MoE layer": a router picks top_k of
+ * n_routed experts; a shared expert runs for every token). */
+typedef struct {
+    const hs_expert* routed;    /* host array [n_routed] */
+    int              n_routed;  /* 1..128 */
+    const hs_expert* shared;    /* host pointer, or NULL for no shared expert */
+    int              hidden;    /* multiple of 64, 64..3072 */
+    int              top_k;     /* 1..8, <= n_routed */
+} hs_moe_layer;
+
+/* Optional debug outputs of the decode and prefill calls (device pointers,
+ * each may be NULL). */
+typedef struct {
+    int*   topk_idx;   /* [batch][top_k] chosen experts, descending logit   */
+    float* topk_w;     /* [batch][top_k] router weights                     */
+    float* h;          /* batch 1 only: [shared neurons + top_k * routed
+                          neurons] fp32 ReLU^2 outputs in slot order (shared
+                          first, then the chosen experts in topk order)      */
+    int*   live_rows;  /* int: live down rows read by the call, summed over
+                          all (token group, expert) pairs                    */
+} hs_decode_debug;
+
+/* Human-readable text of a status code (static storage). */
+const char* hs_status_string(int status);
+
+/* Reads and clears the library's device-side error word (set when a bounded
+ * wait inside a kernel gives up).  Synchronises the current device.
+ * *status receives HS_OK or HS_ERR_TIMEOUT. */
+int hs_device_status(int* status);
+
+/* ------------------------------------------------------------------ repack
+ * Output-major (checkpoint) down projection -> neuron-major layout.
+ * Section "Transposing to skip the zeros" and "Two layouts, one problem":
+ * the same numbers, one row per neuron instead of one row per output.
+ *   codes_om_dev  [out_dim][neurons/2]     scale_om_dev, bias_om_dev [out_dim][neurons/64]
+ *   codes_nm_dev  [neurons][out_dim/2]     sb_nm_dev [neurons/64][out_dim] (scale, bias)
+ * out_dim and neurons multiples of 64.  Outputs must not overlap inputs. */
+int hs_repack_down_nm(const uint8_t* codes_om_dev, const uint16_t* scale_om_dev,
+                      const uint16_t* bias_om_dev, int out_dim, int neurons,
+                      uint8_t* codes_nm_dev, void* sb_nm_dev, hs_stream_t stream);
+
+/* Interleave separate fp16 scale and bias arrays [rows][groups] into the
+ * (scale, bias) pair array [rows][groups] the up projection reads. */
+int hs_pack_sb(const uint16_t* scale_dev, const uint16_t* bias_dev, int rows, int groups,
+               void* sb_dev, hs_stream_t stream);
+
+/* --------------------------------------------------------- sparse down
+ * One expert's activation-sparse down projection, one token.
+ * Section "Our way reads only the rows that fired": only neurons with
+ * h_n > 0 are read (one neuron-major row each); the (scale, bias) slab of a
+ * group of 64 is read only if one of its neurons fired (section "The whole
+ * decode step").  y_o = sum_n h_n * (scale_{g(n),o} * q_{n,o} + bias_{g(n),o}).
+ *   h_dev        [neurons] fp32, h >= 0 (ReLU^2 outputs); h_n > 0 means live
+ *   y_bf16_dev   [out_dim] bf16 (round to nearest even), required
+ *   y_f32_dev    [out_dim] fp32 pre-rounding sums, or NULL
+ *   live_count_dev  int: number of live rows read, or NULL
+ * Deterministic: the same inputs give bit-identical outputs. */
+size_t hs_expert_down_sparse_workspace_size(int neurons, int out_dim);
+int hs_expert_down_sparse(const float* h_dev, const hs_w4* down_nm, int neurons, int out_dim,
+                          uint16_t* y_bf16_dev, float* y_f32_dev, int* live_count_dev,
+                          unsigned flags, void* workspace_dev, size_t workspace_bytes,
+                          hs_stream_t stream);
+
+/* ---------------------------------------------------------- layer decode
+ * One MoE layer at decode for `batch` tokens (sections "Inside a MoE layer",
+ * "Two projections and a switch", "Our way reads only the rows that fired"):
+ *   idx, w   = top_k of logits (ties -> lower index), softmax over the chosen
+ *   z_e      = W_up,e x + offset_e;  h_e = max(z_e, 0)^2
+ *   y_e      = sparse down projection of h_e (live rows only)
+ *   y        = y_shared + sum_j w_j y_{idx_j}
+ *   x_bf16_dev       [batch][hidden] bf16
+ *   logits_dev       [batch][n_routed] fp32 (finite)
+ *   y_bf16_dev       [batch][hidden] bf16, required;  y_f32_dev fp32 or NULL
+ *   debug            host pointer to device debug outputs, or NULL
+ * batch 1..64.  Deterministic. */
+size_t hs_moe_layer_decode_workspace_size(const hs_moe_layer* layer, int batch);
+int hs_moe_layer_decode(const hs_moe_layer* layer, const uint16_t* x_bf16_dev,
+                        const float* logits_dev, int batch, uint16_t* y_bf16_dev,
+                        float* y_f32_dev, unsigned flags, const hs_decode_debug* debug,
+                        void* workspace_dev, size_t workspace_bytes, hs_stream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* HS_H_ */

@@ -43,7 +43,7 @@ from scipy.special import ndtri
 __all__ = [
     "HIDDEN", "N_ROUTED", "N_SHARED", "N_EXPERTS", "TOP_K", "GROUP",
     "stream_key", "hash_u32", "random_code_bytes", "random_scales",
-    "W4Proj", "Expert", "gen_proj", "gen_expert", "gen_routed_stack",
+    "W4Proj", "Expert", "gen_proj", "gen_expert", "gen_routed_stack", "stack_offsets",
     "code_group_sq_sums", "calibrated_offsets", "dead_mask",
     "normal_f32", "normal_bf16", "config1_h", "shared_live_fraction",
     "uniform_f64",
@@ -205,14 +205,28 @@ def gen_routed_stack(key_parts: tuple, n_experts: int, neurons: int, hidden: int
     """All routed experts' projections of one layer as stacked tensors.
 
     Returns (up, down) W4Proj whose tensors carry a leading expert axis; expert e
-    is bit-identical to gen_proj(..., index=e) of the same stream."""
-    ups, downs = [], []
-    for e in range(n_experts):
-        ups.append(gen_proj(neurons, hidden, (*key_parts, "up"), device, e))
-        downs.append(gen_proj(hidden, neurons, (*key_parts, "down"), device, e))
-    st = lambda xs, f: torch.stack([getattr(x, f) for x in xs])
-    return (W4Proj(st(ups, "codes"), st(ups, "scale"), st(ups, "bias")),
-            W4Proj(st(downs, "codes"), st(downs, "scale"), st(downs, "bias")))
+    is bit-identical to gen_proj(..., index=e) of the same stream (the stream
+    position of expert e starts where expert e-1's ends)."""
+    out = []
+    for name, rows, cols in (("up", neurons, hidden), ("down", hidden, neurons)):
+        kp = (*key_parts, name)
+        nb = rows * cols // 2
+        ng = rows * cols // 64
+        codes = random_code_bytes(n_experts * nb, stream_key(*kp, "codes"), device, 0)
+        scale = random_scales(n_experts * ng, stream_key(*kp, "scale"), device, 0)
+        bias = -(scale * 8)
+        out.append(W4Proj(codes.reshape(n_experts, rows, cols // 2), scale.reshape(n_experts, rows, cols // 64),
+                          bias.reshape(n_experts, rows, cols // 64)))
+    return out[0], out[1]
+
+
+def stack_offsets(up: W4Proj, p, dead: np.ndarray | None = None) -> torch.Tensor:
+    """calibrated_offsets for a stacked [E][N] up projection (CPU fp32 [E][N]);
+    row for row identical to calibrated_offsets of each expert alone."""
+    E, N = up.codes.shape[0], up.codes.shape[1]
+    flat = W4Proj(up.codes.reshape(E * N, -1), up.scale.reshape(E * N, -1), up.bias.reshape(E * N, -1))
+    d = None if dead is None else np.asarray(dead).reshape(E * N)
+    return calibrated_offsets(flat, p, d).reshape(E, N)
 
 
 def _rng(*parts) -> np.random.Generator:

@@ -1,0 +1,87 @@
+"""The C ABI (CPU): libhs.so builds, loads, exports every declared symbol, and
+rejects bad arguments with the documented status codes before any GPU work."""
+import ctypes as C
+
+import pytest
+
+from activation_sparse_moe_gb300 import build as hsbuild
+from activation_sparse_moe_gb300 import hs
+
+
+@pytest.fixture(scope="module")
+def lib():
+    hsbuild.build()
+    return hs.lib()
+
+
+def test_exports_every_declared_symbol(lib):
+    names = hs.declared_functions()
+    assert len(names) >= 8
+    for n in ("hs_repack_down_nm", "hs_expert_down_sparse", "hs_moe_layer_decode", "hs_status_string"):
+        assert n in names
+    missing = [n for n in names if not hasattr(lib, n)]
+    assert not missing, missing
+
+
+def test_status_strings(lib):
+    for code in (0, -1, -2, -3, -4, -5, -6):
+        s = hs.hs_status_string(code)
+        assert s and s != "unknown status"
+    assert hs.hs_status_string(-99) == "unknown status"
+
+
+def test_down_sparse_argument_errors(lib):
+    f = lib.hs_expert_down_sparse
+    w = hs.hs_w4(0x10000, 0x20000)
+    W = C.byref(w)
+    A = 0x100000  # fake, 16-byte aligned; validation fails before it is touched
+    assert f(None, W, 1856, 2688, A, None, None, 0, A, 1 << 30, None) == hs.HS_ERR_INVALID_ARG
+    assert f(A, W, 1856, 2688, None, None, None, 0, A, 1 << 30, None) == hs.HS_ERR_INVALID_ARG
+    assert f(A, W, 1800, 2688, A, None, None, 0, A, 1 << 30, None) == hs.HS_ERR_UNSUPPORTED_SHAPE
+    assert f(A, W, 1856, 2690, A, None, None, 0, A, 1 << 30, None) == hs.HS_ERR_UNSUPPORTED_SHAPE
+    assert f(A, W, -64, 2688, A, None, None, 0, A, 1 << 30, None) == hs.HS_ERR_INVALID_ARG
+    assert f(A + 4, W, 1856, 2688, A, None, None, 0, A, 1 << 30, None) == hs.HS_ERR_MISALIGNED
+    assert f(A, W, 1856, 2688, A + 2, None, None, 0, A, 1 << 30, None) == hs.HS_ERR_MISALIGNED
+    need = hs.hs_expert_down_sparse_workspace_size(1856, 2688)
+    assert need >= 29 * 2688 * 4
+    assert f(A, W, 1856, 2688, A, None, None, 0, A, need - 1, None) == hs.HS_ERR_WORKSPACE
+    assert f(A, W, 1856, 2688, A, None, None, 0, None, need, None) == hs.HS_ERR_WORKSPACE
+    assert hs.hs_expert_down_sparse_workspace_size(100, 2688) == 0
+
+
+def _layer(n_routed=4, top_k=2, hidden=256, neurons=128, shared=True, base=0x1000000):
+    ex = [hs.make_expert(base, base, base, base, None, neurons) for _ in range(n_routed)]
+    sh = hs.make_expert(base, base, base, base, None, 256) if shared else None
+    return hs.Layer(ex, sh, hidden, top_k)
+
+
+def test_layer_decode_argument_errors(lib):
+    f = lib.hs_moe_layer_decode
+    A = 0x200000
+    L = _layer()
+    need = hs.hs_moe_layer_decode_workspace_size(L, 1)
+    assert need == ((4 + 2 * 2) * 256 * 4 + 255) // 256 * 256 + 256
+    assert f(L.ref, A, A, 1, A, None, 0, None, A, need - 1, None) == hs.HS_ERR_WORKSPACE
+    assert f(L.ref, None, A, 1, A, None, 0, None, A, need, None) == hs.HS_ERR_INVALID_ARG
+    assert f(L.ref, A, A, 0, A, None, 0, None, A, need, None) == hs.HS_ERR_INVALID_ARG
+    assert f(L.ref, A + 8, A, 1, A, None, 0, None, A, need, None) == hs.HS_ERR_MISALIGNED
+    assert f(_layer(top_k=5).ref, A, A, 1, A, None, 0, None, A, need, None) == hs.HS_ERR_UNSUPPORTED_SHAPE
+    assert f(_layer(hidden=200).ref, A, A, 1, A, None, 0, None, A, need, None) == hs.HS_ERR_UNSUPPORTED_SHAPE
+    assert f(_layer(hidden=4096).ref, A, A, 1, A, None, 0, None, A, need, None) == hs.HS_ERR_UNSUPPORTED_SHAPE
+    assert f(_layer(neurons=100).ref, A, A, 1, A, None, 0, None, A, need, None) == hs.HS_ERR_UNSUPPORTED_SHAPE
+    assert f(_layer(base=0x1000008).ref, A, A, 1, A, None, 0, None, A, need, None) == hs.HS_ERR_MISALIGNED
+    assert f(None, A, A, 1, A, None, 0, None, A, need, None) == hs.HS_ERR_INVALID_ARG
+    # mixed routed sizes are rejected
+    ex = [hs.make_expert(A, A, A, A, None, 128), hs.make_expert(A, A, A, A, None, 192)]
+    assert f(hs.Layer(ex, None, 256, 1).ref, A, A, 1, A, None, 0, None, A, need, None) == \
+        hs.HS_ERR_UNSUPPORTED_SHAPE
+
+
+def test_repack_argument_errors(lib):
+    f = lib.hs_repack_down_nm
+    A = 0x300000
+    assert f(None, A, A, 2688, 1856, A, A, None) == hs.HS_ERR_INVALID_ARG
+    assert f(A, A, A, 2688, 1800, A, A, None) == hs.HS_ERR_UNSUPPORTED_SHAPE
+    assert f(A + 1, A, A, 2688, 1856, A, A, None) == hs.HS_ERR_MISALIGNED
+    assert lib.hs_pack_sb(A, A, 0, 42, A, None) == hs.HS_ERR_INVALID_ARG
+    assert lib.hs_pack_sb(A, A, 10, 42, A + 2, None) == hs.HS_ERR_MISALIGNED

@@ -1,0 +1,131 @@
+"""GPU parity of hs_moe_layer_decode (batch 1) against the oracle.
+
+"Skipping dead neurons..." sections "Inside a MoE layer" (top-6 of 128 plus a
+shared expert), "Two projections and a switch" (up, ReLU^2, down) and "Our
+way reads only the rows that fired".  Calls go through the C ABI.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import synth
+from _util import check_bf16_within_one_ulp, check_close, live_flip_bound
+from activation_sparse_moe_gb300 import hs
+from activation_sparse_moe_gb300.layer import DeviceLayer, from_synth_expert, from_synth_stack
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    from activation_sparse_moe_gb300 import build
+    build.build()
+    hs.lib()
+
+
+def make_layer(L: synth.LayerInputs, top_k):
+    routed = from_synth_stack(L.up, L.down, L.offsets)
+    shared = from_synth_expert(L.shared) if L.shared is not None else None
+    return DeviceLayer(routed, shared, top_k)
+
+
+def run_layer(dl: DeviceLayer, x, lg, flags=0):
+    H = dl.hidden
+    NS = dl.shared.N if dl.shared is not None else 0
+    ws = torch.empty(dl.workspace_size(1), dtype=torch.uint8, device="cuda")
+    y = torch.empty(H, dtype=torch.bfloat16, device="cuda")
+    yf = torch.empty(H, dtype=torch.float32, device="cuda")
+    dbg = {"topk_idx": torch.full((dl.top_k,), -1, dtype=torch.int32, device="cuda"),
+           "topk_w": torch.zeros(dl.top_k, dtype=torch.float32, device="cuda"),
+           "h": torch.full((NS + dl.top_k * dl.routed.N,), -1.0, dtype=torch.float32, device="cuda"),
+           "live_rows": torch.full((1,), -1, dtype=torch.int32, device="cuda")}
+    hs.hs_moe_layer_decode(dl.c, x.reshape(-1).cuda(), lg.reshape(-1).cuda(), 1, y, yf, flags, dbg, ws)
+    torch.cuda.synchronize()
+    assert hs.hs_device_status() == hs.HS_OK
+    return y.cpu(), yf.cpu().double().numpy(), {k: v.cpu() for k, v in dbg.items()}
+
+
+def check_layer(L: synth.LayerInputs, dl, x, lg, top_k, what):
+    y, yf, dbg = run_layer(dl, x, lg)
+    ref = oracle.moe_layer(x.reshape(-1), lg.reshape(-1), L.routed_expert, L.shared, k=top_k)
+    # router: indices exact, weights to fp32 precision
+    assert dbg["topk_idx"].tolist() == ref["idx"].tolist(), what
+    np.testing.assert_allclose(dbg["topk_w"].double().numpy(), ref["w"], rtol=2e-6, atol=1e-7)
+    # live sets: the kernel's own h > 0 equals the oracle's, except where the
+    # oracle's |z| is within fp32 accumulation error of 0
+    hk = dbg["h"].double().numpy()
+    NS = L.shared.neurons if L.shared is not None else 0
+    slots = ([(L.shared, ref["shared"], 0)] if L.shared is not None else []) + [
+        (L.routed_expert(int(e)), ref["experts"][int(e)], NS + j * L.up.codes.shape[1])
+        for j, e in enumerate(ref["idx"])]
+    flips = 0
+    live_total = 0
+    for ex, r, base in slots:
+        n = ex.neurons
+        hg = hk[base:base + n]
+        assert (hg >= 0).all()
+        live_total += int((hg > 0).sum())
+        mism = (hg > 0) != (r["h"] > 0)
+        if mism.any():
+            bound = live_flip_bound(x.reshape(-1), ex.up)
+            zmag = np.abs(r["z"])
+            assert (zmag[mism] <= bound[mism]).all(), f"{what}: live-set mismatch beyond fp32 bound"
+            flips += int(mism.sum())
+        check_close(hg, r["h"], f"{what} h")
+    assert int(dbg["live_rows"].item()) == live_total
+    check_close(yf, ref["out"], f"{what} y_f32")
+    check_bf16_within_one_ulp(y, ref["out"], f"{what} y_bf16", yf)
+    return y, yf, flips
+
+
+def test_small_layer():
+    H, E, NR, NS, K = 512, 8, 128, 256, 3
+    L = synth.layer_inputs(0, "t-small", 0, E, NR, NS, H, p=0.2, p_shared=0.3)
+    x, lg = synth.tokens(0, "t-small", 0, 1, H, E)
+    dl = make_layer(L, K)
+    check_layer(L, dl, x, lg, K, "small")
+
+
+def test_no_shared_top1_and_extreme_hidden():
+    for H, E, NR, K in ((64, 4, 64, 1), (3072, 6, 192, 2)):
+        L = synth.layer_inputs(1, "t-edge", H, E, NR, 0, H, p=0.3)
+        x, lg = synth.tokens(1, "t-edge", H, 1, H, E)
+        dl = make_layer(L, K)
+        check_layer(L, dl, x, lg, K, f"edge H={H}")
+
+
+@pytest.fixture(scope="module")
+def full_layer():
+    """One full-size MoE layer at live fraction 0.1 (weights generated on the GPU)."""
+    L = synth.layer_inputs(0, "cfg2", 0, device="cuda")
+    dl = make_layer(L, 6)
+    x, lg = synth.tokens(0, "cfg2", 0, 1)
+    return L, dl, x, lg
+
+
+def test_full_layer_parity(full_layer):
+    L, dl, x, lg = full_layer
+    y, yf, flips = check_layer(L, dl, x, lg, 6, "full layer")
+    assert flips <= 2
+
+
+def test_full_layer_dense_flag_and_determinism(full_layer):
+    L, dl, x, lg = full_layer
+    y1, yf1, d1 = run_layer(dl, x, lg)
+    y2, yf2, d2 = run_layer(dl, x, lg)
+    yd, yfd, dd = run_layer(dl, x, lg, flags=hs.HS_FORCE_DENSE)
+    assert np.array_equal(yf1, yf2) and torch.equal(y1, y2)
+    assert np.array_equal(yf1, yfd) and torch.equal(y1, yd)
+    assert int(dd["live_rows"].item()) == 3712 + 6 * 1856
+    frac = int(d1["live_rows"].item()) / (3712 + 6 * 1856)
+    assert 0.07 < frac < 0.13
+
+
+def test_generator_device_independent(full_layer):
+    """The GPU-generated stack equals the CPU generator for a sampled expert."""
+    L, dl, x, lg = full_layer
+    e = 77
+    cpu = synth.gen_expert((0, "cfg2", 0, "routed"), synth.N_ROUTED, index=e)
+    assert torch.equal(cpu.up.codes, L.up.codes[e].cpu()) and torch.equal(cpu.down.scale, L.down.scale[e].cpu())
+    assert torch.equal(cpu.offset, L.offsets[e])
