@@ -29,6 +29,9 @@
 //    products); the 128 * sum(x) term is removed per 32-code chunk.
 #include "hs_common.cuh"
 
+#include <cstring>
+#include <mutex>
+
 namespace hs {
 
 struct ExpertPtrs {
@@ -42,12 +45,29 @@ struct ExpertPtrs {
 struct LayerParams {
     ExpertPtrs routed[kMaxRouted];
     ExpertPtrs shared;
+    long long stride[5];  // when uniform: byte strides of the 5 fields between experts
+    int uniform;          // routed[e] = routed[0] + e * stride (no table lookup)
     int n_routed;
     int routed_neurons;
     int shared_neurons;   // 0 if no shared expert
     int hidden;
     int top_k;
 };
+
+// Pointers of routed expert e: by arithmetic when the experts are stacked at
+// uniform strides (no dependent load), else from the table.
+__device__ __forceinline__ ExpertPtrs routed_ptrs(const LayerParams& P, int e) {
+    if (P.uniform) {
+        ExpertPtrs b = P.routed[0];
+        b.up_codes += e * P.stride[0];
+        b.up_sb = reinterpret_cast<const uint32_t*>(reinterpret_cast<const char*>(b.up_sb) + e * P.stride[1]);
+        b.dn_codes += e * P.stride[2];
+        b.dn_sb = reinterpret_cast<const uint32_t*>(reinterpret_cast<const char*>(b.dn_sb) + e * P.stride[3]);
+        if (b.up_off) b.up_off = reinterpret_cast<const float*>(reinterpret_cast<const char*>(b.up_off) + e * P.stride[4]);
+        return b;
+    }
+    return P.routed[e];
+}
 
 struct DecodeIO {
     const uint16_t* x;       // [hidden] bf16
@@ -60,133 +80,246 @@ struct DecodeIO {
     int* live_counts;        // [units] live rows per unit (workspace)
 };
 
-// Dynamic shared memory layout of one decode CTA.
+// Dynamic shared memory layout of one decode CTA (offsets in bytes).
 struct SmemLayout {
-    static constexpr int kBars = 6;  // 4 up chunks, 1 down, spare
+    static constexpr int kBars = 6;  // 4 up chunks, 1 down, 1 activations
     __host__ __device__ static int codes_bytes(int hidden) { return 64 * hidden / 2; }
     __host__ __device__ static int sb_bytes(int hidden) { return hidden * 4; }
-    __host__ __device__ static int total(int hidden) {
-        return codes_bytes(hidden) + sb_bytes(hidden) + 64 * 4 /*h*/ + 64 /*bars*/ + 128 /*misc*/;
-    }
+    __host__ __device__ static int misc_off(int hidden) { return codes_bytes(hidden) + sb_bytes(hidden); }
+    // misc: h[64] f32, off[64] f32, logits[kMaxRouted] f32, rank parts[256] i32, sel_v[8] f32,
+    //       sel_i[8] i32, topk_i[8], topk_w[8], bars[8] u64, live u64, hsum f32,
+    // then x[hidden] bf16 (staging), the fixed-point x table [G][144 B] and its
+    // per-group (2^(E-15), sum x) pairs [G][2] f32.
+    static constexpr int kH = 0, kOff = 256, kLg = 512, kRank = kLg + 4 * kMaxRouted, kSelV = kRank + 1024,
+                         kSelI = kSelV + 32, kTopI = kSelI + 32, kTopW = kTopI + 32, kBarsOff = kTopW + 32,
+                         kLive = kBarsOff + 64, kHsum = kLive + 8, kX = kHsum + 24;
+    static constexpr int kXfStride = 144;  // 128 B of bytes + 16 B pad: conflict-free 128-bit loads
+    __host__ __device__ static int x_off(int hidden) { return misc_off(hidden) + kX; }
+    __host__ __device__ static int xf_off(int hidden) { return x_off(hidden) + 2 * hidden; }
+    __host__ __device__ static int xs_off(int hidden) { return xf_off(hidden) + (hidden / 64) * kXfStride; }
+    __host__ __device__ static int total(int hidden) { return xs_off(hidden) + (hidden / 64) * 8; }
 };
 
 // ------------------------------------------------------------------ router
-// Top-k of n logits (ties -> lower index) and softmax over the chosen k.
-// Executed by one full warp; results in idx[k], w[k] (shared memory).
+// Top-k of n <= 128 logits (ties -> lower index) and a softmax over the chosen
+// k <= 8, by one warp in registers.  Lane l sorts logits l, l+32, l+64, l+96
+// (value descending, index ascending) into a list of 8 padded with losers.
+// Five butterfly levels merge each lane's list with its xor partner's: the
+// elementwise best of L[j] and R[7-j] is the top 8 of the union as a bitonic
+// sequence, which a 3-stage bitonic merger sorts.  After the last level every
+// lane holds the overall top 8.  Lane 0 writes idx[k], w[k] (shared memory).
+__device__ __forceinline__ bool topk_better(float a, int ia, float b, int ib) {
+    return a > b || (a == b && ia < ib);
+}
+
+__device__ __forceinline__ void topk_cx(float (&v)[8], int (&id)[8], int a, int b) {
+    // order positions a < b best-first
+    const bool sw = topk_better(v[b], id[b], v[a], id[a]);
+    const float va = v[a], vb = v[b];
+    const int ia = id[a], ib = id[b];
+    v[a] = sw ? vb : va; v[b] = sw ? va : vb;
+    id[a] = sw ? ib : ia; id[b] = sw ? ia : ib;
+}
+
 __device__ void warp_topk_softmax(const float* __restrict__ logits, int n, int k, int* idx, float* w) {
     const int lane = threadIdx.x & 31;
-    float v[kMaxRouted / 32];
+    float v[8];
+    int id[8];
 #pragma unroll
-    for (int i = 0; i < kMaxRouted / 32; ++i) {
+    for (int i = 0; i < 8; ++i) {
         const int e = lane + 32 * i;
-        v[i] = (e < n) ? logits[e] : -INFINITY;
+        const bool real = i < 4 && e < n;
+        id[i] = real ? e : 1024 + 32 * i + lane;  // padding loses every comparison
+        v[i] = real ? logits[e] : -INFINITY;
     }
-    unsigned taken = 0;  // bit i: element lane+32i already chosen
-    float sel[kMaxTopK];
-    int seli[kMaxTopK];
-    for (int j = 0; j < k; ++j) {
-        float bv = -INFINITY;
-        int bi = 0x7fffffff;
+    topk_cx(v, id, 0, 1); topk_cx(v, id, 2, 3); topk_cx(v, id, 0, 2); topk_cx(v, id, 1, 3); topk_cx(v, id, 1, 2);
 #pragma unroll
-        for (int i = 0; i < kMaxRouted / 32; ++i) {
-            const int e = lane + 32 * i;
-            if (e < n && !((taken >> i) & 1u)) {
-                if (v[i] > bv || (v[i] == bv && e < bi)) { bv = v[i]; bi = e; }
-            }
+    for (int off = 16; off; off >>= 1) {
+        float rv[8];
+        int ri[8];
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+            rv[j] = __shfl_xor_sync(0xffffffffu, v[j], off);
+            ri[j] = __shfl_xor_sync(0xffffffffu, id[j], off);
         }
 #pragma unroll
-        for (int off = 16; off; off >>= 1) {
-            const float ov = __shfl_xor_sync(0xffffffffu, bv, off);
-            const int oi = __shfl_xor_sync(0xffffffffu, bi, off);
-            if (ov > bv || (ov == bv && oi < bi)) { bv = ov; bi = oi; }
+        for (int j = 0; j < 8; ++j) {
+            if (topk_better(rv[7 - j], ri[7 - j], v[j], id[j])) { v[j] = rv[7 - j]; id[j] = ri[7 - j]; }
         }
-        if ((bi & 31) == lane) taken |= 1u << (bi >> 5);
-        sel[j] = bv;
-        seli[j] = bi;
+#pragma unroll
+        for (int d = 4; d; d >>= 1) {
+#pragma unroll
+            for (int j = 0; j < 8; ++j)
+                if (!(j & d)) topk_cx(v, id, j, j + d);
+        }
     }
     if (lane == 0) {
-        const float m = sel[0];
-        float den = 0.f;
         float ex[kMaxTopK];
-        for (int j = 0; j < k; ++j) { ex[j] = expf(sel[j] - m); den += ex[j]; }
-        for (int j = 0; j < k; ++j) { idx[j] = seli[j]; w[j] = ex[j] / den; }
+        float den = 0.f;
+#pragma unroll
+        for (int j = 0; j < kMaxTopK; ++j) ex[j] = (j < k) ? expf(v[j] - v[0]) : 0.f;
+#pragma unroll
+        for (int j = 0; j < kMaxTopK; ++j) den += ex[j];
+        const float inv = 1.f / den;
+#pragma unroll
+        for (int j = 0; j < kMaxTopK; ++j)
+            if (j < k) { idx[j] = id[j]; w[j] = ex[j] * inv; }
     }
-    __syncwarp();
 }
 
 // ------------------------------------------------------------- up phase
-// Dot products of the CTA's 64 up rows with x.  Thread (c, r0) owns the
-// 32-code chunk c of every row r = r0 + S*i; its 32 activations stay in
-// registers as bf16 pairs matched to the nibble order of the code words.
-// Per-(row, chunk) partial dot products are written over the first 4 bytes of
-// the chunk they were computed from (each chunk has exactly one reader).
-__device__ __forceinline__ float chunk_dot(const uint4 cw, const uint32_t (&xp)[16]) {
-    float a0 = 0.f, a1 = 0.f;
-    const uint32_t w[4] = {cw.x, cw.y, cw.z, cw.w};
-#pragma unroll
-    for (int j = 0; j < 4; ++j) {
-#pragma unroll
-        for (int s = 0; s < 4; ++s) {
-            uint32_t q;
-            const uint32_t ws = w[j] >> (4 * s);
-            asm("lop3.b32 %0, %1, 0x000F000F, 0x43004300, 0xea;" : "=r"(q) : "r"(ws));
-            asm("{ .reg .b16 ql, qh, xl, xh;\n"
-                "  mov.b32 {ql, qh}, %2;\n"
-                "  mov.b32 {xl, xh}, %3;\n"
-                "  fma.rn.f32.bf16 %0, ql, xl, %0;\n"
-                "  fma.rn.f32.bf16 %1, qh, xh, %1;\n"
-                "}"
-                : "+f"(a0), "+f"(a1)
-                : "r"(q), "r"(xp[4 * j + s]));
-        }
-    }
-    return a0 + a1;  // = sum_k (128 + q_k) x_k
-}
-
-struct UpThread {
-    int c;       // chunk index (32 codes)
-    int r0;      // first row
-    int S;       // row stride
-    bool active;
+// Dot products of the CTA's 64 up rows with x on the integer pipes.
+// Thread (gc, r0) owns scale group gc (64 codes, 32 bytes) of every row
+// r = r0 + S*i.  Its 64 activations are held as a 16-bit fixed-point copy
+// with one exponent for the group, X_k = round(x_k * 2^(15-E)) with
+// max|x_k| < 2^E, split into a signed high byte and an unsigned low byte
+// (X = 256*H + L).  A bf16 x with |x| >= 2^(E-8) is represented exactly (its
+// 8 significant bits fit); smaller ones are off by at most 2^(E-16).  Per
+// group and row:
+//   sum_k q_k X_k = 256 * dp4a(q, H) + dp4a(q, L)    (exact in int32)
+// with the codes split into even/odd nibble bytes by one mask each.
+struct XFixed {
+    int hE[8], hO[8];          // high bytes of X for even / odd codes of word j
+    unsigned lE[8], lO[8];     // low bytes
+    float inv;                 // 2^(E-15) / 16 (the group dot products carry a factor 16)
+    float xsum;                // sum of the 64 x values (fp32)
 };
 
-__device__ __forceinline__ void load_x_chunk(const uint16_t* __restrict__ x, int c, uint32_t (&xp)[16],
-                                             float& xsum) {
-    const uint4* p = reinterpret_cast<const uint4*>(x + 32 * c);
-    uint32_t xw[16];
+// Cooperative conversion of x into the fixed-point table: 4 threads per
+// group of 64, thread q covering x[16q..16q+15] (code words 2q, 2q+1).  The
+// group maximum and sum combine the 4 partials by a fixed 2-level tree.
+// Threads first..first+4G-1 take part; returns after writing the table.
+__device__ __forceinline__ void convert_x_fixed(const uint16_t* x_s, int G, uint8_t* xf_s, float* xs_s, int first) {
+    const int i = threadIdx.x - first;
+    if (i < 0 || i >= 4 * G) return;
+    const int grp = i >> 2, q = i & 3;
+    const uint4 r0 = reinterpret_cast<const uint4*>(x_s + 64 * grp + 16 * q)[0];
+    const uint4 r1 = reinterpret_cast<const uint4*>(x_s + 64 * grp + 16 * q)[1];
+    const uint32_t w[8] = {r0.x, r0.y, r0.z, r0.w, r1.x, r1.y, r1.z, r1.w};
+    float xv[16];
 #pragma unroll
-    for (int i = 0; i < 4; ++i) {
-        const uint4 v = __ldg(p + i);
-        xw[4 * i] = v.x; xw[4 * i + 1] = v.y; xw[4 * i + 2] = v.z; xw[4 * i + 3] = v.w;
+    for (int m = 0; m < 8; ++m) {
+        xv[2 * m] = __uint_as_float(w[m] << 16);
+        xv[2 * m + 1] = __uint_as_float(w[m] & 0xffff0000u);
     }
-    float s = 0.f;
+    float mx = 0.f, sa = 0.f, sb = 0.f;
 #pragma unroll
-    for (int j = 0; j < 4; ++j) {
-        const uint32_t w0 = xw[4 * j], w1 = xw[4 * j + 1], w2 = xw[4 * j + 2], w3 = xw[4 * j + 3];
-        xp[4 * j + 0] = __byte_perm(w0, w2, 0x5410);
-        xp[4 * j + 1] = __byte_perm(w0, w2, 0x7632);
-        xp[4 * j + 2] = __byte_perm(w1, w3, 0x5410);
-        xp[4 * j + 3] = __byte_perm(w1, w3, 0x7632);
+    for (int m = 0; m < 16; m += 2) {
+        mx = fmaxf(mx, fmaxf(fabsf(xv[m]), fabsf(xv[m + 1])));
+        sa += xv[m];
+        sb += xv[m + 1];
     }
+    float sm = sa + sb;
+    // the 4 threads of a group are adjacent lanes (first is a multiple of 4):
+    // a fixed xor tree among exactly those lanes
+    const unsigned m4 = 0xFu << (threadIdx.x & 28);
+    mx = fmaxf(mx, __shfl_xor_sync(m4, mx, 1));
+    sm += __shfl_xor_sync(m4, sm, 1);
+    mx = fmaxf(mx, __shfl_xor_sync(m4, mx, 2));
+    sm += __shfl_xor_sync(m4, sm, 2);
+    int e = 0;
+    if (mx > 0.f) frexpf(mx, &e);   // mx < 2^e
+    e = max(e, -100);               // keeps 2^(15-e) and 2^(e-19) normal floats
+    const float scale = __int_as_float((127 + 15 - e) << 23);   // 2^(15-e)
+    // words 2q, 2q+1: bytes b of word j <-> x[8j + 2b] (even) and x[8j + 2b + 1] (odd)
+    uint32_t hE[2], hO[2], lE[2], lO[2];
 #pragma unroll
-    for (int i = 0; i < 16; ++i) {
-        s += __uint_as_float(xw[i] << 16);
-        s += __uint_as_float(xw[i] & 0xffff0000u);
+    for (int jj = 0; jj < 2; ++jj) {
+        hE[jj] = hO[jj] = lE[jj] = lO[jj] = 0;
+#pragma unroll
+        for (int b = 0; b < 4; ++b) {
+            const int X0 = __float2int_rn(xv[8 * jj + 2 * b] * scale);
+            const int X1 = __float2int_rn(xv[8 * jj + 2 * b + 1] * scale);
+            hE[jj] |= (uint32_t)((X0 >> 8) & 0xff) << (8 * b);
+            lE[jj] |= (uint32_t)(X0 & 0xff) << (8 * b);
+            hO[jj] |= (uint32_t)((X1 >> 8) & 0xff) << (8 * b);
+            lO[jj] |= (uint32_t)(X1 & 0xff) << (8 * b);
+        }
     }
-    xsum = s;
+    uint8_t* tb = xf_s + grp * SmemLayout::kXfStride + 8 * q;
+    *reinterpret_cast<uint2*>(tb) = make_uint2(hE[0], hE[1]);
+    *reinterpret_cast<uint2*>(tb + 32) = make_uint2(hO[0], hO[1]);
+    *reinterpret_cast<uint2*>(tb + 64) = make_uint2(lE[0], lE[1]);
+    *reinterpret_cast<uint2*>(tb + 96) = make_uint2(lO[0], lO[1]);
+    if (q == 0) {
+        xs_s[2 * grp] = __int_as_float((127 + e - 19) << 23);   // 2^(E-15) / 16
+        xs_s[2 * grp + 1] = sm;
+    }
+}
+
+__device__ __forceinline__ void load_x_fixed(const uint8_t* xf_s, const float* xs_s, int gc, XFixed& xf) {
+    const uint4* p = reinterpret_cast<const uint4*>(xf_s + gc * SmemLayout::kXfStride);
+    uint4 v[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) v[i] = p[i];
+#pragma unroll
+    for (int i = 0; i < 2; ++i) {
+        xf.hE[4 * i] = (int)v[i].x; xf.hE[4 * i + 1] = (int)v[i].y; xf.hE[4 * i + 2] = (int)v[i].z; xf.hE[4 * i + 3] = (int)v[i].w;
+        xf.hO[4 * i] = (int)v[2 + i].x; xf.hO[4 * i + 1] = (int)v[2 + i].y; xf.hO[4 * i + 2] = (int)v[2 + i].z; xf.hO[4 * i + 3] = (int)v[2 + i].w;
+        xf.lE[4 * i] = v[4 + i].x; xf.lE[4 * i + 1] = v[4 + i].y; xf.lE[4 * i + 2] = v[4 + i].z; xf.lE[4 * i + 3] = v[4 + i].w;
+        xf.lO[4 * i] = v[6 + i].x; xf.lO[4 * i + 1] = v[6 + i].y; xf.lO[4 * i + 2] = v[6 + i].z; xf.lO[4 * i + 3] = v[6 + i].w;
+    }
+    xf.inv = xs_s[2 * gc];
+    xf.xsum = xs_s[2 * gc + 1];
+}
+
+// Where the up phase leaves the partial dot product of (row r, group gc): the
+// 4 bytes at word (gc/4 + r)%8 of the group's 32-byte code block.  A warp's
+// stores (consecutive gc, one row) and the row sums' loads (8 rows x 4
+// threads, groups q + 4i) then hit 32 distinct banks (for rows of
+// 1344 bytes; other widths stay correct, with some conflicts).
+__device__ __forceinline__ float* part_slot(uint8_t* codes_buf, int rowb, int r, int gc) {
+    return reinterpret_cast<float*>(codes_buf + r * rowb + 32 * gc + 4 * (((gc >> 2) + r) & 7));
+}
+
+// 16 * sum_k q_k X_k over one scale group: 32 code bytes in two 16-byte
+// halves (codes 8j+i in nibble i of word j; half 1 holds words 4..7).  Even
+// codes are masked in place (q), odd codes too (16 q): no shifts; the factor
+// 16 is carried by the even sums instead.  |16 T| < 2^28: exact in int32.
+__device__ __forceinline__ int group_dot_fixed16(const uint4 c0, const uint4 c1, const XFixed& xf) {
+    const uint32_t w[8] = {c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w};
+    int hE = 0, hO = 0;
+    unsigned lE = 0, lO = 0;
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+        const uint32_t ev = w[j] & 0x0F0F0F0Fu;   // q of codes 8j, 8j+2, 8j+4, 8j+6
+        const uint32_t od = w[j] & 0xF0F0F0F0u;   // 16 q of codes 8j+1, ..., 8j+7
+        asm("dp4a.u32.s32 %0, %1, %2, %0;" : "+r"(hE) : "r"(ev), "r"(xf.hE[j]));
+        asm("dp4a.u32.s32 %0, %1, %2, %0;" : "+r"(hO) : "r"(od), "r"(xf.hO[j]));
+        lE = __dp4a(ev, xf.lE[j], lE);
+        lO = __dp4a(od, xf.lO[j], lO);
+    }
+    // 16 T = 16 (256 hE + lE) + (256 hO + lO), hO and lO already carrying 16
+    return (hE * 256 + (int)lE) * 16 + hO * 256 + (int)lO;
+}
+
+// Reads the two 16-byte halves of group gc of a row, in an order that makes
+// the 8-lane phases of a warp's 128-bit shared loads hit distinct banks.
+__device__ __forceinline__ void load_group_codes(const uint8_t* row, int gc, uint4& c0, uint4& c1) {
+    const int f = (gc >> 2) & 1;
+    const uint4 a = *reinterpret_cast<const uint4*>(row + 32 * gc + 16 * f);
+    const uint4 b = *reinterpret_cast<const uint4*>(row + 32 * gc + 16 * (f ^ 1));
+    c0 = f ? b : a;
+    c1 = f ? a : b;
 }
 
 // ------------------------------------------------------------ down phase
 // Given h[64] and the live mask in shared memory, accumulate
 //   partial_o = wgt * (sum_{n live} h_n * (s_o q_{n,o} + b_o))
 // for the CTA's group, with the live rows at their row slot in codes_buf and
-// the slab (s_o, b_o) in sb_buf.  Thread (c, r3) sums the live rows n with
-// n % S == r3 in ascending order; the S sums are added in order r3 = 0..S-1.
+// the slab (s_o, b_o) in sb_buf.  Thread (c, r3) owns outputs 32c..32c+31 and
+// sums the live rows n with n % S == r3 in ascending order; the S sums are
+// added in order r3 = 0..S-1 by all threads, one output each (the result does
+// not depend on which rows are live beyond the +0 terms, so the dense flag
+// gives identical bits).
+// A nibble at bit 4i of a code word becomes a float by masking it in place
+// under the exponent of 2^23 and subtracting 2^23 (exact: q * 16^i < 2^23);
+// the row's h is pre-scaled by 16^-i to undo the position.
 __device__ void down_accumulate_and_store(const uint8_t* codes_buf, const uint32_t* sb_buf, float* red_buf,
                                           const float* h_s, uint64_t live, float Hsum, float wgt, int hidden,
                                           float* __restrict__ out_row) {
     const int C = hidden / 32;
-    const int S = min(256 / C, 8);
+    const int S = min(256 / C, 7);  // S * C * 33 floats fit in the 64-row code buffer
     const int t = threadIdx.x;
     const int c = t % C, r3 = t / C;
     const int rowb = hidden / 2;
@@ -201,46 +334,51 @@ __device__ void down_accumulate_and_store(const uint8_t* codes_buf, const uint32
             const int n = __ffsll((long long)m) - 1;
             m &= m - 1;
             const float hn = h_s[n];
+            const float hs[5] = {hn, hn * 0.0625f, hn * 0.00390625f, hn * 0.000244140625f, hn * 1.52587890625e-05f};
             const uint4 cw = *reinterpret_cast<const uint4*>(codes_buf + n * rowb + 16 * c);
             const uint32_t w[4] = {cw.x, cw.y, cw.z, cw.w};
 #pragma unroll
             for (int j = 0; j < 4; ++j) {
+                const uint32_t hi = w[j] >> 12;  // nibbles 5, 6, 7 at positions 2, 3, 4
 #pragma unroll
                 for (int i = 0; i < 8; ++i) {
-                    const float q = __uint_as_float(0x4B000000u | ((w[j] >> (4 * i)) & 15u)) - 8388608.f;
-                    acc[8 * j + i] = fmaf(hn, q, acc[8 * j + i]);
+                    const uint32_t src = i < 5 ? w[j] : hi;
+                    const int pos = i < 5 ? i : i - 3;
+                    const float q = __uint_as_float((src & (15u << (4 * pos))) | 0x4B000000u) - 8388608.f;
+                    acc[8 * j + i] = fmaf(hs[pos], q, acc[8 * j + i]);
                 }
             }
         }
     }
     __syncthreads();  // all reads of codes_buf done: reuse it for the cross-subset sum
-    if (r3 >= 1 && r3 < S) {
-        float4* dst = reinterpret_cast<float4*>(red_buf + (size_t)(r3 - 1) * hidden + 32 * c);
+    // red[s][c][k] with rows of 33 floats: the 32-float stores of a warp
+    // (consecutive c) and the combine's loads (consecutive outputs) are
+    // both free of bank conflicts
+    if (r3 < S) {
+        float* dst = red_buf + ((size_t)r3 * C + c) * 33;
 #pragma unroll
-        for (int k = 0; k < 8; ++k) dst[k] = make_float4(acc[4 * k], acc[4 * k + 1], acc[4 * k + 2], acc[4 * k + 3]);
+        for (int k = 0; k < 32; ++k) dst[k] = acc[k];
     }
     __syncthreads();
-    if (r3 == 0) {
+    // every thread finishes a strided set of 4-output quads: subsets added in order 0..S-1
+    for (int o4 = t; o4 < hidden / 4; o4 += blockDim.x) {
+        const int o = 4 * o4, oc = o >> 5, ok = o & 31;
+        float a[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) a[e] = red_buf[(size_t)oc * 33 + ok + e];
         for (int s = 1; s < S; ++s) {
-            const float4* src = reinterpret_cast<const float4*>(red_buf + (size_t)(s - 1) * hidden + 32 * c);
 #pragma unroll
-            for (int k = 0; k < 8; ++k) {
-                const float4 v = src[k];
-                acc[4 * k] += v.x; acc[4 * k + 1] += v.y; acc[4 * k + 2] += v.z; acc[4 * k + 3] += v.w;
-            }
+            for (int e = 0; e < 4; ++e) a[e] += red_buf[((size_t)s * C + oc) * 33 + ok + e];
         }
-        float4* dst = reinterpret_cast<float4*>(out_row + 32 * c);
+        const uint4 sb4 = reinterpret_cast<const uint4*>(sb_buf)[o4];
+        const uint32_t sbw[4] = {sb4.x, sb4.y, sb4.z, sb4.w};
+        float r[4];
 #pragma unroll
-        for (int k = 0; k < 8; ++k) {
-            float r[4];
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-                const int o = 32 * c + 4 * k + e;
-                const float2 sb = half2_to_float2(sb_buf[o]);
-                r[e] = wgt * fmaf(sb.x, acc[4 * k + e], sb.y * Hsum);
-            }
-            dst[k] = make_float4(r[0], r[1], r[2], r[3]);
+        for (int e = 0; e < 4; ++e) {
+            const float2 sb = half2_to_float2(sbw[e]);
+            r[e] = wgt * fmaf(sb.x, a[e], sb.y * Hsum);
         }
+        reinterpret_cast<float4*>(out_row)[o4] = make_float4(r[0], r[1], r[2], r[3]);
     }
 }
 
@@ -261,9 +399,6 @@ __device__ __forceinline__ void warp0_mask_and_issue(const float* h_s, bool dens
     const unsigned b0 = __ballot_sync(0xffffffffu, h0 > 0.f);
     const unsigned b1 = __ballot_sync(0xffffffffu, h1 > 0.f);
     uint64_t live = dense ? ~0ull : ((uint64_t)b1 << 32 | b0);
-    float s = h0 + h1;
-#pragma unroll
-    for (int off = 16; off; off >>= 1) s += __shfl_xor_sync(0xffffffffu, s, off);
     const int rowb = hidden / 2;
     if (live) {
         if (lane == 0) mbar_arrive_expect_tx(bar, (uint32_t)(__popcll(live) * rowb + hidden * 4));
@@ -273,6 +408,10 @@ __device__ __forceinline__ void warp0_mask_and_issue(const float* h_s, bool dens
         if ((live >> (lane + 32)) & 1)
             bulk_g2s(codes_buf + (lane + 32) * rowb, dn_codes_g + (size_t)(lane + 32) * rowb, rowb, bar, policy);
     }
+    // the fixed-order sum of h is needed only at the end: after the copies
+    float s = h0 + h1;
+#pragma unroll
+    for (int off = 16; off; off >>= 1) s += __shfl_xor_sync(0xffffffffu, s, off);
     if (lane == 0) { *mask_out = live; *hsum_out = s; }
 }
 
@@ -283,12 +422,15 @@ moe_decode_b1_kernel(const __grid_constant__ LayerParams P, const DecodeIO io) {
     const int hidden = P.hidden;
     uint8_t* codes_buf = smem;
     uint32_t* sb_buf = reinterpret_cast<uint32_t*>(smem + SmemLayout::codes_bytes(hidden));
-    float* h_s = reinterpret_cast<float*>(smem + SmemLayout::codes_bytes(hidden) + SmemLayout::sb_bytes(hidden));
-    uint64_t* bars = reinterpret_cast<uint64_t*>(h_s + 64);
-    int* topk_i = reinterpret_cast<int*>(bars + 8);
-    float* topk_w = reinterpret_cast<float*>(topk_i + kMaxTopK);
-    uint64_t* live_s = reinterpret_cast<uint64_t*>(topk_w + kMaxTopK);
-    float* hsum_s = reinterpret_cast<float*>(live_s + 1);
+    uint8_t* misc = smem + SmemLayout::misc_off(hidden);
+    float* h_s = reinterpret_cast<float*>(misc + SmemLayout::kH);
+    float* off_s = reinterpret_cast<float*>(misc + SmemLayout::kOff);
+    int* topk_i = reinterpret_cast<int*>(misc + SmemLayout::kTopI);
+    float* topk_w = reinterpret_cast<float*>(misc + SmemLayout::kTopW);
+    uint64_t* bars = reinterpret_cast<uint64_t*>(misc + SmemLayout::kBarsOff);
+    uint64_t* live_s = reinterpret_cast<uint64_t*>(misc + SmemLayout::kLive);
+    float* hsum_s = reinterpret_cast<float*>(misc + SmemLayout::kHsum);
+    uint16_t* x_s = reinterpret_cast<uint16_t*>(smem + SmemLayout::x_off(hidden));
 
     const int t = threadIdx.x;
     const int u = blockIdx.x;
@@ -297,6 +439,7 @@ moe_decode_b1_kernel(const __grid_constant__ LayerParams P, const DecodeIO io) {
     const int slot = is_shared ? 0 : 1 + (u - sg) / rg;
     const int g = is_shared ? u : (u - sg) % rg;
     const int rowb = hidden / 2;
+    const int G = hidden / 64;  // scale groups per up row
     const bool dense = (io.flags & HS_FORCE_DENSE) != 0;
     const uint64_t pol = policy_evict_first();
 
@@ -306,13 +449,12 @@ moe_decode_b1_kernel(const __grid_constant__ LayerParams P, const DecodeIO io) {
     }
     __syncthreads();
 
-    const ExpertPtrs* ep = nullptr;
     auto issue_up = [&](const ExpertPtrs& e) {
         // 4 chunks of 16 rows; the up scales ride on the first chunk
         const uint8_t* src = e.up_codes + (size_t)g * 64 * rowb;
         const uint32_t chunk = 16 * rowb;
         mbar_arrive_expect_tx(&bars[0], chunk + hidden * 4);
-        bulk_g2s(sb_buf, e.up_sb + (size_t)g * 64 * (hidden / 64), hidden * 4, &bars[0], pol);
+        bulk_g2s(sb_buf, e.up_sb + (size_t)g * 64 * G, hidden * 4, &bars[0], pol);
         bulk_g2s(codes_buf, src, chunk, &bars[0], pol);
         for (int k = 1; k < 4; ++k) {
             mbar_arrive_expect_tx(&bars[k], chunk);
@@ -320,65 +462,104 @@ moe_decode_b1_kernel(const __grid_constant__ LayerParams P, const DecodeIO io) {
         }
     };
 
+    ExpertPtrs ep;
     if (is_shared) {
-        ep = &P.shared;
-        if (t == 0) issue_up(*ep);  // weights do not depend on the previous kernel
+        ep = P.shared;
+        if (t == 0) issue_up(ep);  // weights do not depend on the previous kernel
     }
     pdl_wait();
     pdl_trigger();
-    if (!is_shared || (u == 0 && io.dbg_topk_idx)) {
-        if (t < 32) warp_topk_softmax(io.logits, P.n_routed, P.top_k, topk_i, topk_w);
-        __syncthreads();
-        if (u == 0 && io.dbg_topk_idx && t < P.top_k) {
-            io.dbg_topk_idx[t] = topk_i[t];
-            io.dbg_topk_w[t] = topk_w[t];
-        }
+
+    // activations and logits (may be produced by the previous kernel)
+    if (t == 0) {
+        mbar_arrive_expect_tx(&bars[5], hidden * 2);
+        bulk_g2s(x_s, io.x, hidden * 2, &bars[5], policy_evict_last());
+    }
+    const bool need_topk = !is_shared || (u == 0 && io.dbg_topk_idx);
+    // warp 0 routes (if this CTA needs it); the other warps convert x meanwhile
+    const int S = 256 / G;
+    const int gc = t % G, r0 = t / G;
+    const bool up_active = r0 < S;
+    uint8_t* xf_s = smem + SmemLayout::xf_off(hidden);
+    float* xs_s = reinterpret_cast<float*>(smem + SmemLayout::xs_off(hidden));
+    bool ok = true;
+    if (need_topk && t < 32) {
+        warp_topk_softmax(io.logits, P.n_routed, P.top_k, topk_i, topk_w);
+    } else {
+        ok = mbar_wait(&bars[5], 0);
+        if (ok) convert_x_fixed(x_s, G, xf_s, xs_s, need_topk ? 32 : 0);
+    }
+    if (!__syncthreads_and(ok)) return;
+    if (u == 0 && io.dbg_topk_idx && t < P.top_k) {
+        io.dbg_topk_idx[t] = topk_i[t];
+        io.dbg_topk_w[t] = topk_w[t];
     }
     float wgt = 1.f;
     if (!is_shared) {
         const int e = topk_i[slot - 1];
         wgt = topk_w[slot - 1];
-        ep = &P.routed[e];
-        if (t == 0) issue_up(*ep);
+        ep = routed_ptrs(P, e);
+        if (t == 0) issue_up(ep);
     }
+    float off_r = 0.f;
+    if (t < 64 && ep.up_off) off_r = ep.up_off[g * 64 + t];
 
     // ---- up projection for 64 rows
-    const int C = hidden / 32;
-    const int S = 256 / C;
-    const int c = t % C, r0 = t / C;
-    const bool up_active = r0 < S;
-    uint32_t xp[16];
-    float xsum = 0.f;
-    if (up_active) load_x_chunk(io.x, c, xp, xsum);
-    bool ok = true;
+    XFixed xf;
     if (up_active) {
+        load_x_fixed(xf_s, xs_s, gc, xf);
         int waited = -1;
-        for (int r = r0; r < 64; r += S) {
-            const int k = r >> 4;
+        const uint8_t* base = codes_buf;
+        int r = r0;
+        for (; r + S < 64; r += 2 * S) {  // two rows at a time
+            const int k = (r + S) >> 4;
             while (waited < k) { ++waited; ok &= mbar_wait(&bars[waited], 0); }
             if (!ok) break;
-            const uint4 cw = *reinterpret_cast<const uint4*>(codes_buf + r * rowb + 16 * c);
-            const float2 sb = half2_to_float2(sb_buf[r * (hidden / 64) + (c >> 1)]);
-            const float acc = chunk_dot(cw, xp);
-            const float part = fmaf(sb.x, acc, fmaf(-128.f, sb.x, sb.y) * xsum);
-            *reinterpret_cast<float*>(codes_buf + r * rowb + 16 * c) = part;
+            uint4 a0, a1, b0, b1;
+            load_group_codes(base + r * rowb, gc, a0, a1);
+            load_group_codes(base + (r + S) * rowb, gc, b0, b1);
+            const float2 sa = half2_to_float2(sb_buf[r * G + gc]);
+            const float2 sbb = half2_to_float2(sb_buf[(r + S) * G + gc]);
+            const int da = group_dot_fixed16(a0, a1, xf);
+            const int db = group_dot_fixed16(b0, b1, xf);
+            // part = s * sum_k q_k x_k + b * sum_k x_k
+            *part_slot(codes_buf, rowb, r, gc) = fmaf(sa.x * xf.inv, (float)da, sa.y * xf.xsum);
+            *part_slot(codes_buf, rowb, r + S, gc) = fmaf(sbb.x * xf.inv, (float)db, sbb.y * xf.xsum);
         }
+        if (ok && r < 64) {
+            const int k = r >> 4;
+            while (waited < k) { ++waited; ok &= mbar_wait(&bars[waited], 0); }
+            if (ok) {
+                uint4 a0, a1;
+                load_group_codes(base + r * rowb, gc, a0, a1);
+                const float2 sa = half2_to_float2(sb_buf[r * G + gc]);
+                const int da = group_dot_fixed16(a0, a1, xf);
+                *part_slot(codes_buf, rowb, r, gc) = fmaf(sa.x * xf.inv, (float)da, sa.y * xf.xsum);
+            }
+        }
+        while (ok && waited < 3) { ++waited; ok &= mbar_wait(&bars[waited], 0); }
     } else {
         for (int k = 0; k < 4; ++k) ok &= mbar_wait(&bars[k], 0);
     }
+    if (t < 64) off_s[t] = off_r;
     if (!__syncthreads_and(ok)) return;
 
-    // ---- row sums: thread (r, q) adds chunks q, q+4, ... then a fixed 4-way tree
+    // ---- row sums: thread (r, q) adds groups q, q+4, ... then a fixed 4-way tree
     {
         const int r = t >> 2, q = t & 3;
-        float s = 0.f;
-        for (int cc = q; cc < C; cc += 4) s += *reinterpret_cast<const float*>(codes_buf + r * rowb + 16 * cc);
+        float s0 = 0.f, s1 = 0.f;
+        int cc = q;
+        for (; cc + 4 < G; cc += 8) {
+            s0 += *part_slot(codes_buf, rowb, r, cc);
+            s1 += *part_slot(codes_buf, rowb, r, cc + 4);
+        }
+        if (cc < G) s0 += *part_slot(codes_buf, rowb, r, cc);
+        float s = s0 + s1;
         s += __shfl_xor_sync(0xffffffffu, s, 1);
         s += __shfl_xor_sync(0xffffffffu, s, 2);
         if (q == 0) {
             const int n = g * 64 + r;
-            const float off = ep->up_off ? ep->up_off[n] : 0.f;
-            const float z = s + off;
+            const float z = s + off_s[r];
             const float h = z > 0.f ? z * z : 0.f;
             h_s[r] = h;
             if (io.dbg_h) {
@@ -392,7 +573,7 @@ moe_decode_b1_kernel(const __grid_constant__ LayerParams P, const DecodeIO io) {
 
     // ---- live mask, fixed-order sum of h, down copies
     if (t < 32)
-        warp0_mask_and_issue(h_s, dense, ep->dn_codes + (size_t)g * 64 * rowb, ep->dn_sb + (size_t)g * hidden, hidden,
+        warp0_mask_and_issue(h_s, dense, ep.dn_codes + (size_t)g * 64 * rowb, ep.dn_sb + (size_t)g * hidden, hidden,
                              codes_buf, sb_buf, &bars[4], live_s, hsum_s, pol);
     __syncthreads();
     const uint64_t live = *live_s;
@@ -415,10 +596,11 @@ down_sparse_kernel(const float* __restrict__ h, const uint8_t* __restrict__ dn_c
     extern __shared__ __align__(128) uint8_t smem[];
     uint8_t* codes_buf = smem;
     uint32_t* sb_buf = reinterpret_cast<uint32_t*>(smem + SmemLayout::codes_bytes(hidden));
-    float* h_s = reinterpret_cast<float*>(smem + SmemLayout::codes_bytes(hidden) + SmemLayout::sb_bytes(hidden));
-    uint64_t* bars = reinterpret_cast<uint64_t*>(h_s + 64);
-    uint64_t* live_s = bars + 8;
-    float* hsum_s = reinterpret_cast<float*>(live_s + 1);
+    uint8_t* misc = smem + SmemLayout::misc_off(hidden);
+    float* h_s = reinterpret_cast<float*>(misc + SmemLayout::kH);
+    uint64_t* bars = reinterpret_cast<uint64_t*>(misc + SmemLayout::kBarsOff);
+    uint64_t* live_s = reinterpret_cast<uint64_t*>(misc + SmemLayout::kLive);
+    float* hsum_s = reinterpret_cast<float*>(misc + SmemLayout::kHsum);
     const int t = threadIdx.x, g = blockIdx.x;
     const int rowb = hidden / 2;
     if (t == 0) { mbar_init(&bars[0], 1); fence_mbar_init(); }
@@ -442,14 +624,16 @@ down_sparse_kernel(const float* __restrict__ h, const uint8_t* __restrict__ dn_c
 
 // ------------------------------------------------ fixed-order partial sum
 // y[o] = sum_{u=0..U-1} partial[u][o] (u ascending within each of 32 strided
-// subsets, then the 32 subset sums in order); bf16 round to nearest even.
+// subsets, then a fixed tree over the 32 subset sums); bf16 round to nearest
+// even.
 // Also sums the per-unit live counts into *live_total (if non-null).
 __global__ void __launch_bounds__(256)
 reduce_partials_kernel(const float* __restrict__ partial, int U, int hidden, uint16_t* __restrict__ y_bf16,
                        float* __restrict__ y_f32, const int* __restrict__ live_counts, int* __restrict__ live_total) {
     __shared__ float4 red[32][8];
+    __shared__ float4 red2[8][8];
+    pdl_trigger();  // the next kernel may start its weight prefetch now
     pdl_wait();
-    pdl_trigger();
     const int t = threadIdx.x;
     const int col = blockIdx.x * 8 + (t & 7);  // float4 column
     const int uc = t >> 3;
@@ -457,17 +641,39 @@ reduce_partials_kernel(const float* __restrict__ partial, int U, int hidden, uin
     float4 s = make_float4(0.f, 0.f, 0.f, 0.f);
     if (col < ncol) {
         const float4* p = reinterpret_cast<const float4*>(partial) + col;
-        for (int u = uc; u < U; u += 32) {
+        int u = uc;
+        // batches of 8 independent loads, then the adds in unit order
+        for (; u + 7 * 32 < U; u += 8 * 32) {
+            float4 v[8];
+#pragma unroll
+            for (int i = 0; i < 8; ++i) v[i] = __ldcg(p + (size_t)(u + 32 * i) * ncol);
+#pragma unroll
+            for (int i = 0; i < 8; ++i) { s.x += v[i].x; s.y += v[i].y; s.z += v[i].z; s.w += v[i].w; }
+        }
+        for (; u < U; u += 32) {
             const float4 v = __ldcg(p + (size_t)u * ncol);
             s.x += v.x; s.y += v.y; s.z += v.z; s.w += v.w;
         }
     }
     red[uc][t & 7] = s;
     __syncthreads();
+    // fixed tree: 32 unit chunks -> 8 (4 each, in order) -> 1 (8, in order)
+    if (t < 64) {
+        const int c8 = t & 7, p = t >> 3;
+        float4 a = red[4 * p][c8];
+#pragma unroll
+        for (int i = 1; i < 4; ++i) {
+            const float4 v = red[4 * p + i][c8];
+            a.x += v.x; a.y += v.y; a.z += v.z; a.w += v.w;
+        }
+        red2[p][c8] = a;
+    }
+    __syncthreads();
     if (t < 8 && col < ncol) {
-        float4 a = red[0][t];
-        for (int i = 1; i < 32; ++i) {
-            const float4 v = red[i][t];
+        float4 a = red2[0][t];
+#pragma unroll
+        for (int i = 1; i < 8; ++i) {
+            const float4 v = red2[i][t];
             a.x += v.x; a.y += v.y; a.z += v.z; a.w += v.w;
         }
         if (y_f32) reinterpret_cast<float4*>(y_f32)[col] = a;
@@ -509,9 +715,22 @@ cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t sme
     return cudaLaunchKernelEx(&cfg, kern, args...);
 }
 
+// Raises a kernel's dynamic shared memory limit once per (kernel, device, size):
+// the attribute call is kept out of the per-call path (and out of stream capture
+// after the first eager call).
 int set_smem_attr(const void* fn, int bytes) {
+    struct Entry { const void* fn; int dev; int bytes; };
+    static Entry done[64];
+    static int n_done = 0;
+    static std::mutex mu;
+    std::lock_guard<std::mutex> lock(mu);
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return HS_ERR_CUDA;
+    for (int i = 0; i < n_done; ++i)
+        if (done[i].fn == fn && done[i].dev == dev && done[i].bytes >= bytes) return HS_OK;
     if (cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes) != cudaSuccess)
         return HS_ERR_CUDA;
+    if (n_done < 64) done[n_done++] = Entry{fn, dev, bytes};
     return HS_OK;
 }
 
@@ -636,6 +855,22 @@ extern "C" int hs_moe_layer_decode(const hs_moe_layer* L, const uint16_t* x, con
     };
     for (int e = 0; e < L->n_routed; ++e) fill(P.routed[e], L->routed[e]);
     if (L->shared) fill(P.shared, *L->shared);
+    // experts stacked at uniform strides: the kernel computes their pointers
+    {
+        auto fld = [&](int e, int f) -> long long {
+            const hs::ExpertPtrs& d = P.routed[e];
+            const void* v[5] = {d.up_codes, d.up_sb, d.dn_codes, d.dn_sb, d.up_off};
+            return (long long)(uintptr_t)v[f];
+        };
+        bool uni = true;
+        for (int f = 0; f < 5; ++f) {
+            const long long st = L->n_routed > 1 ? fld(1, f) - fld(0, f) : 0;
+            P.stride[f] = st;
+            for (int e = 0; e < L->n_routed && uni; ++e) uni = (fld(e, f) == fld(0, f) + e * st);
+            if (f == 4) for (int e = 0; e < L->n_routed && uni; ++e) uni = ((fld(e, 4) == 0) == (fld(0, 4) == 0));
+        }
+        P.uniform = uni ? 1 : 0;
+    }
     P.n_routed = L->n_routed;
     P.routed_neurons = L->routed[0].neurons;
     P.shared_neurons = L->shared ? L->shared->neurons : 0;

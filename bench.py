@@ -1,0 +1,405 @@
+#!/usr/bin/env python
+"""Benchmark of the activation-sparse MoE decode path on GB300.
+
+Workload (one step): batch-1 decode through 23 distinct MoE layers (hidden
+2688, 128 routed experts of 1856 neurons, top-6, a 3712-neuron shared expert,
+4-bit affine group-64 weights, 16.8 GB of weights in total), routed live
+fraction 0.1, shared live fraction U(0.05, 0.15) per layer.  One step is 23
+calls of hs_moe_layer_decode, captured in one CUDA graph.  The weights are far
+larger than L2, so no L2 flush is needed between steps.
+
+Metric: MoE-layer decode time in microseconds per layer per token (lower is
+better), with the achieved HBM bandwidth on the bytes the method must move.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl hs|reference]
+
+--impl reference times the CPU fp64 oracle on the host cores on the same
+workload (a bounded sample of layers per step).  Under torchrun each rank
+runs an independent replica (the path has no cross-GPU exchange).
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "MoE-layer decode us/token (batch 1, per layer) and achieved HBM GB/s at live frac 0.1"
+UNIT = "us/layer"
+LAYERS = 23
+WORKLOAD = "moe_decode_b1_23layers_p0.1"
+
+
+def _args():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", choices=["hs", "reference"], default="hs")
+    ap.add_argument("--p", type=float, default=0.1)
+    ap.add_argument("--layers", type=int, default=LAYERS)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--profile", action="store_true",
+                    help="minimal run for profilers: no clock soak, dense, end-to-end or CPU legs")
+    return ap.parse_args()
+
+
+def _dist():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+def _config(args, extra=None):
+    c = {"workload": WORKLOAD if args.p == 0.1 and args.layers == LAYERS else
+         f"moe_decode_b1_{args.layers}layers_p{args.p}",
+         "layers": args.layers, "batch": 1, "hidden": 2688, "routed_experts": 128, "top_k": 6,
+         "routed_neurons": 1856, "shared_neurons": 3712, "weights": "W4 affine group-64, fp16 scale+bias",
+         "p_routed": args.p, "p_shared": "U(0.05,0.15) per layer",
+         "l2": "weights 16.8 GB > L2, no flush", "parallelism": "replicas" if _dist()[0] > 1 else "single"}
+    if extra:
+        c.update(extra)
+    return c
+
+
+# ------------------------------------------------------------------ clocks
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_id: str):
+        self.gpu_id = gpu_id
+        self.lines = []
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits", "-lms", "200",
+                 "-i", self.gpu_id], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self._t = threading.Thread(target=self._read, daemon=True)
+            self._t.start()
+        except OSError:
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *a):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self):
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            f = [x.strip() for x in ln.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                mx.append(float(f[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, f[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ----------------------------------------------------------- ncu traffic
+def _recorded_traffic(kernel: str, src: str):
+    """DRAM bytes per launch recorded under profiles/ for `kernel`, if the
+    recorded source hash still matches the kernel's source file."""
+    path = os.path.join(ROOT, "profiles", f"{kernel}.txt")
+    if not os.path.exists(path):
+        return None
+    sha = hashlib.sha256(open(src, "rb").read()).hexdigest()
+    rec = {}
+    for ln in open(path):
+        if ":" in ln:
+            k, v = ln.split(":", 1)
+            rec[k.strip()] = v.strip()
+    if rec.get("source_sha256") != sha:
+        return None
+    try:
+        return float(rec["dram_bytes_per_launch"])
+    except (KeyError, ValueError):
+        return None
+
+
+# ------------------------------------------------------------- workload
+def build_layers(n_layers, p, device):
+    import synth
+    from activation_sparse_moe_gb300.layer import DeviceLayer, from_synth_expert, from_synth_stack
+    layers = []
+    for l in range(n_layers):
+        L = synth.layer_inputs(0, "cfg3", l, p=p, p_shared=synth.shared_live_fraction(0, l), device=device)
+        dl = DeviceLayer(from_synth_stack(L.up, L.down, L.offsets, device),
+                         from_synth_expert(L.shared, device), top_k=6)
+        layers.append(dl)
+        del L
+    return layers
+
+
+def oracle_layer_expert_source(l, p):
+    """Checkpoint-layout experts of layer l regenerated on the CPU (for the oracle)."""
+    import synth
+    cache = {}
+
+    def routed(e):
+        if e not in cache:
+            cache[e] = synth.gen_expert((0, "cfg3", l, "routed"), synth.N_ROUTED, p=p, index=e)
+        return cache[e]
+
+    shared = synth.gen_expert((0, "cfg3", l, "shared"), synth.N_SHARED, p=synth.shared_live_fraction(0, l))
+    return routed, shared
+
+
+def time_oracle(n_layers_max, p, budget_s, steps=None):
+    """Times the oracle per layer on the host; returns (us per layer, layers done, threads)."""
+    import oracle
+    import synth
+    prepared = []
+    for l in range(n_layers_max):
+        x, lg = synth.tokens(0, "cfg3", l, 1)
+        routed, shared = oracle_layer_expert_source(l, p)
+        idx, _ = oracle.router_topk(lg[0], 6)
+        for e in idx:
+            routed(int(e))  # generate outside the timed region
+        prepared.append((x[0], lg[0], routed, shared))
+    times = []
+    t_all = time.perf_counter()
+    i = 0
+    while True:
+        x, lg, routed, shared = prepared[i % len(prepared)]
+        t0 = time.perf_counter()
+        oracle.moe_layer(x, lg, routed, shared, k=6)
+        times.append(time.perf_counter() - t0)
+        i += 1
+        if steps is not None:
+            if i >= steps:
+                break
+        elif time.perf_counter() - t_all > budget_s:
+            break
+    return times
+
+
+def main():
+    args = _args()
+    ws, rank, local = _dist()
+    if args.impl == "reference":
+        return run_reference(args, ws, rank)
+
+    import numpy as np
+    import torch
+    from activation_sparse_moe_gb300 import build as hsbuild
+    from activation_sparse_moe_gb300 import bytemodel, hs
+
+    if not torch.cuda.is_available():
+        raise SystemExit("bench.py needs a CUDA GPU")
+    torch.cuda.set_device(local)
+    if ws > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    hsbuild.build()
+    hs.lib()
+    dev = torch.device("cuda", local)
+
+    import synth
+    n = args.layers
+    layers = build_layers(n, args.p, dev)
+    xs, lgs = [], []
+    for l in range(n):
+        x, lg = synth.tokens(0, "cfg3", l, 1)
+        xs.append(x[0])
+        lgs.append(lg[0])
+    X = torch.stack(xs).to(dev)
+    LG = torch.stack(lgs).to(dev)
+    Y = torch.empty((n, 2688), dtype=torch.bfloat16, device=dev)
+    wsz = max(dl.workspace_size(1) for dl in layers)
+    WS = torch.empty(wsz, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.Stream(device=dev)
+
+    # untimed pass with debug outputs: live rows and live groups per layer
+    live_rows, live_groups = [], []
+    NS, NR = 3712, 1856
+    with torch.cuda.stream(stream):
+        for l, dl in enumerate(layers):
+            dbg = {"h": torch.empty(NS + 6 * NR, dtype=torch.float32, device=dev),
+                   "live_rows": torch.empty(1, dtype=torch.int32, device=dev)}
+            hs.hs_moe_layer_decode(dl.c, X[l], LG[l], 1, Y[l], None, 0, dbg, WS, stream=stream)
+            stream.synchronize()
+            h = dbg["h"].cpu().numpy()
+            live_rows.append(int(dbg["live_rows"].item()))
+            live_groups.append(int((h.reshape(-1, 64) > 0).any(axis=1).sum()))
+            assert live_rows[-1] == int((h > 0).sum())
+    assert hs.hs_device_status() == hs.HS_OK
+    req_bytes = [bytemodel.decode_layer_bytes(2688, [NS] + [NR] * 6, r, g, 128)
+                 for r, g in zip(live_rows, live_groups)]
+    dense_bytes = bytemodel.decode_layer_bytes(2688, [NS] + [NR] * 6, NS + 6 * NR, (NS + 6 * NR) // 64, 128)
+    step_bytes = sum(req_bytes)
+
+    def capture(flags):
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            for l, dl in enumerate(layers):
+                hs.hs_moe_layer_decode(dl.c, X[l], LG[l], 1, Y[l], None, flags, None, WS, stream=stream)
+        return g
+
+    # eager warm call (sets kernel attributes outside capture)
+    with torch.cuda.stream(stream):
+        for l, dl in enumerate(layers):
+            hs.hs_moe_layer_decode(dl.c, X[l], LG[l], 1, Y[l], None, 0, None, WS, stream=stream)
+    stream.synchronize()
+    g_sparse = capture(0)
+    g_dense = capture(hs.HS_FORCE_DENSE)
+
+    def barrier():
+        if ws > 1:
+            torch.distributed.barrier()
+
+    def timed(graph, K, W):
+        for _ in range(W):
+            graph.replay()
+        stream.synchronize()
+        barrier()
+        torch.cuda.synchronize()
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(stream):
+            e0.record(stream)
+            for _ in range(K):
+                graph.replay()
+            e1.record(stream)
+        stream.synchronize()
+        torch.cuda.synchronize()
+        barrier()
+        ms = e0.elapsed_time(e1)
+        if ws > 1:
+            t = torch.tensor([ms], device=dev)
+            torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+            ms = float(t.item())
+        return ms
+
+    K, W = args.steps, max(3, args.warmup)
+    props = torch.cuda.get_device_properties(dev)
+    gpu_id = getattr(props, "uuid", None)
+    gpu_id = f"GPU-{gpu_id}" if gpu_id is not None and not str(gpu_id).startswith("GPU-") else str(gpu_id or local)
+    with ClockSampler(gpu_id) as clk:
+        # keep the GPU under this load long enough for the sampler (~1.5 s)
+        t_end = time.time() + (0.0 if args.profile else 1.5)
+        while time.time() < t_end:
+            g_sparse.replay()
+        stream.synchronize()
+        ms = timed(g_sparse, K, W)
+    clocks = clk.summary()
+    ms_dense = ms if args.profile else timed(g_dense, K, W)
+
+    us_layer = ms * 1e3 / (K * n)
+    us_layer_dense = ms_dense * 1e3 / (K * n)
+    achieved = step_bytes / (ms * 1e-3 / K) / 1e9  # GB/s on required bytes
+    peaks_path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(peaks_path):
+        peak = float(json.load(open(peaks_path))["hbm_gbs"])
+        peak_src = "measured"
+    else:
+        peak, peak_src = 6800.0, "fallback"
+
+    # end to end through the C ABI: pinned host inputs in, result out, every step
+    Xh = X.cpu().pin_memory()
+    LGh = LG.cpu().pin_memory()
+    Yh = torch.empty((n, 2688), dtype=torch.bfloat16).pin_memory()
+    g_e2e = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g_e2e, stream=stream):
+        X.copy_(Xh, non_blocking=True)
+        LG.copy_(LGh, non_blocking=True)
+        for l, dl in enumerate(layers):
+            hs.hs_moe_layer_decode(dl.c, X[l], LG[l], 1, Y[l], None, 0, None, WS, stream=stream)
+        Yh.copy_(Y, non_blocking=True)
+    ms_e2e = ms if args.profile else timed(g_e2e, K, W)
+    us_e2e = ms_e2e * 1e3 / (K * n)
+    h2d = X.numel() * X.element_size() + LG.numel() * LG.element_size()
+    d2h = Y.numel() * Y.element_size()
+
+    cpu = None
+    if rank == 0 and ws == 1 and not (args.no_cpu_baseline or args.profile):
+        times = time_oracle(3, args.p, budget_s=12.0)
+        cpu = {"value": statistics.median(times) * 1e6, "unit": UNIT, "cores": 1, "kind": "oracle",
+               "sample": f"{len(times)} layer decodes of layers 0-2 of the same workload (fp64 numpy, "
+                         "single-threaded BLAS), median per layer"}
+
+    if rank == 0:
+        src = os.path.join(ROOT, "activation_sparse_moe_gb300", "csrc", "hs_decode.cu")
+        out = {
+            "metric": METRIC, "value": round(us_layer, 4), "unit": UNIT, "n_gpus": ws, "steps": K, "warmup": W,
+            "ms_per_step": round(ms / K, 6), "higher_is_better": False, "scaling": "weak", "vs_baseline": None,
+            "dtype": "f32", "data": "synthetic (seeded; random W4 weights of the page's shapes)",
+            "config": _config(args, {"operands": "W4 weights, bf16 activations, fp32 accumulate, bf16 out"}),
+            "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
+                         "frac": round(achieved / peak, 4), "peak_source": peak_src,
+                         "kernel": "hs_moe_layer_decode (moe_decode_b1_kernel + reduce_partials_kernel)",
+                         "bytes_per_launch": round(step_bytes / n),
+                         "traffic": _recorded_traffic("moe_decode_b1_kernel", src),
+                         "frac_of_8TBs": round(achieved / 8000.0, 4)},
+            "e2e": {"value": round(us_e2e, 4), "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+            "gpu_launches": 2 * n * K,
+            "clocks": clocks,
+            "dense_path": {"value": round(us_layer_dense, 4), "unit": UNIT, "flag": "HS_FORCE_DENSE",
+                           "speedup_sparse_vs_dense": round(us_layer_dense / us_layer, 3),
+                           "bytes_per_layer": dense_bytes},
+            "live": {"rows_per_layer": round(float(np.mean(live_rows)), 1),
+                     "groups_per_layer": round(float(np.mean(live_groups)), 1),
+                     "required_MB_per_step": round(step_bytes / 1e6, 2)},
+            "cpu_baseline": cpu,
+        }
+        print(json.dumps(out), flush=True)
+    if ws > 1:
+        torch.distributed.destroy_process_group()
+
+
+def run_reference(args, ws, rank):
+    """The reference arm: the CPU oracle on the host cores, same workload."""
+    if rank != 0:
+        return
+    K, W = args.steps, max(3, args.warmup)
+    # bound the run: the oracle takes about a second per layer
+    K_eff = min(K, 20)
+    W_eff = min(W, 3)
+    times = time_oracle(min(4, args.layers), args.p, budget_s=None, steps=K_eff + W_eff)
+    t = times[W_eff:]
+    v = statistics.median(t) * 1e6
+    out = {"metric": METRIC, "value": round(v, 1), "unit": UNIT, "n_gpus": ws, "steps": len(t), "warmup": W_eff,
+           "ms_per_step": round(statistics.median(t) * 1e3, 3), "higher_is_better": False, "scaling": "weak",
+           "vs_baseline": None, "dtype": "f64", "data": "synthetic", "impl": "reference",
+           "config": _config(args),
+           "cpu_baseline": {"value": round(v, 1), "unit": UNIT, "cores": 1, "kind": "oracle",
+                            "sample": f"one layer decode per step cycling over layers 0-3, {len(t)} timed steps "
+                                      f"(requested {K}), fp64 numpy"},
+           "e2e": {"value": round(v, 1), "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(out), flush=True)
+
+
+if __name__ == "__main__":
+    for v in ("OPENBLAS_NUM_THREADS", "OMP_NUM_THREADS", "MKL_NUM_THREADS"):
+        os.environ.setdefault(v, "1")
+    main()
