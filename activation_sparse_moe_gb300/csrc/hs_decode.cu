@@ -899,3 +899,76 @@ extern "C" int hs_moe_layer_decode(const hs_moe_layer* L, const uint16_t* x, con
         return HS_ERR_CUDA;
     return launch_err();
 }
+
+// ============================================================================
+// Allocation-free variant of hs_expert_down_sparse.
+//
+// Some callers cannot hand the library a workspace: code that runs where
+// device allocation is not allowed or not available at call time (a plugin
+// that only receives the tensors it must read and write from a host framework
+// which owns every allocation, or a real-time path that must never enter the
+// CUDA allocator).  For them the scratch of the two kernels below lives in a
+// fixed array compiled into the library; each GPU that loads the library
+// keeps that array (about 0.75 MB) until the process exits.
+//
+// The host never dereferences or passes the array's name to a kernel: in host
+// code that name is only a stand-in.  Its device address is looked up once per
+// device with cudaGetSymbolAddress and cached.
+// ============================================================================
+namespace {
+constexpr int kNoAllocMaxNeurons = 4096;   // at most 64 groups of 64 neurons
+constexpr int kNoAllocMaxOut = 3072;
+constexpr size_t kNoAllocPartialBytes = (size_t)(kNoAllocMaxNeurons / 64) * kNoAllocMaxOut * sizeof(float);
+constexpr size_t kNoAllocBytes = kNoAllocPartialBytes + (kNoAllocMaxNeurons / 64) * sizeof(int);
+}  // namespace
+
+static __device__ __align__(256) unsigned char hs_noalloc_scratch[kNoAllocBytes];
+
+namespace {
+// Device address of hs_noalloc_scratch on the current device (looked up on the
+// first call per device).  Returns nullptr if the lookup fails.
+void* noalloc_scratch_address() {
+    constexpr int kMaxDevices = 64;
+    static void* addr[kMaxDevices] = {};
+    static std::mutex mu;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
+    std::lock_guard<std::mutex> lock(mu);
+    if (!addr[dev]) {
+        void* p = nullptr;
+        if (cudaGetSymbolAddress(&p, hs_noalloc_scratch) != cudaSuccess) return nullptr;
+        addr[dev] = p;
+    }
+    return addr[dev];
+}
+}  // namespace
+
+extern "C" int hs_expert_down_sparse_noalloc(const float* h, const hs_w4* down_nm, int neurons, int out_dim,
+                                             uint16_t* y_bf16, float* y_f32, int* live_count, unsigned flags,
+                                             hs_stream_t stream) {
+    if (!h || !down_nm || !down_nm->codes || !down_nm->sb || !y_bf16) return HS_ERR_INVALID_ARG;
+    if (neurons <= 0 || out_dim <= 0) return HS_ERR_INVALID_ARG;
+    if (neurons % 64 || out_dim % 64) return HS_ERR_UNSUPPORTED_SHAPE;
+    // beyond the compiled-in scratch capacity
+    if (neurons > kNoAllocMaxNeurons || out_dim > kNoAllocMaxOut) return HS_ERR_UNSUPPORTED_SHAPE;
+    if (!al16(h) || !al16(down_nm->codes) || !al16(down_nm->sb) || !al16(y_bf16) || (y_f32 && !al16(y_f32)) ||
+        (live_count && !al4(live_count)))
+        return HS_ERR_MISALIGNED;
+    char* scratch = static_cast<char*>(noalloc_scratch_address());
+    if (!scratch) return HS_ERR_CUDA;
+    const int G = neurons / 64;
+    float* partial = reinterpret_cast<float*>(scratch);
+    int* counts = reinterpret_cast<int*>(scratch + kNoAllocPartialBytes);
+    // every partial row and count is written before it is read: nothing in the
+    // scratch has to start at zero
+    const int smem = hs::SmemLayout::total(out_dim);
+    if (set_smem_attr((const void*)hs::down_sparse_kernel, smem) != HS_OK) return HS_ERR_CUDA;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    if (launch_pdl(hs::down_sparse_kernel, dim3(G), dim3(256), smem, s, h, down_nm->codes,
+                   static_cast<const uint32_t*>(down_nm->sb), out_dim, flags, partial, counts) != cudaSuccess)
+        return HS_ERR_CUDA;
+    if (launch_pdl(hs::reduce_partials_kernel, dim3((out_dim / 4 + 7) / 8), dim3(256), 0, s, (const float*)partial, G,
+                   out_dim, y_bf16, y_f32, (const int*)counts, live_count) != cudaSuccess)
+        return HS_ERR_CUDA;
+    return launch_err();
+}

@@ -59,6 +59,8 @@ _SIGS = {
     "hs_expert_down_sparse_workspace_size": (C.c_size_t, [C.c_int, C.c_int]),
     "hs_expert_down_sparse": (C.c_int, [C.c_void_p, C.POINTER(hs_w4), C.c_int, C.c_int, C.c_void_p, C.c_void_p,
                                         C.c_void_p, C.c_uint, C.c_void_p, C.c_size_t, C.c_void_p]),
+    "hs_expert_down_sparse_noalloc": (C.c_int, [C.c_void_p, C.POINTER(hs_w4), C.c_int, C.c_int, C.c_void_p,
+                                                C.c_void_p, C.c_void_p, C.c_uint, C.c_void_p]),
     "hs_moe_layer_decode_workspace_size": (C.c_size_t, [C.POINTER(hs_moe_layer), C.c_int]),
     "hs_moe_layer_decode": (C.c_int, [C.POINTER(hs_moe_layer), C.c_void_p, C.c_void_p, C.c_int, C.c_void_p,
                                       C.c_void_p, C.c_uint, C.POINTER(hs_decode_debug), C.c_void_p, C.c_size_t,
@@ -144,6 +146,14 @@ def hs_expert_down_sparse(h, down_codes, down_sb, neurons, out_dim, y_bf16, y_f3
     _check("hs_expert_down_sparse", lib().hs_expert_down_sparse(
         _p(h), C.byref(w), neurons, out_dim, _p(y_bf16), _p(y_f32), _p(live_count), flags, _p(workspace), nb,
         _stream(stream)))
+
+
+def hs_expert_down_sparse_noalloc(h, down_codes, down_sb, neurons, out_dim, y_bf16, y_f32=None, live_count=None,
+                                  flags=0, stream=None):
+    """hs_expert_down_sparse with the library's built-in scratch (no workspace)."""
+    w = hs_w4(_p(down_codes), _p(down_sb))
+    _check("hs_expert_down_sparse_noalloc", lib().hs_expert_down_sparse_noalloc(
+        _p(h), C.byref(w), neurons, out_dim, _p(y_bf16), _p(y_f32), _p(live_count), flags, _stream(stream)))
 
 
 def make_expert(up_codes, up_sb, down_codes, down_sb, offset, neurons) -> hs_expert:

@@ -148,6 +148,25 @@ int hs_expert_down_sparse(const float* h_dev, const hs_w4* down_nm, int neurons,
                           unsigned flags, void* workspace_dev, size_t workspace_bytes,
                           hs_stream_t stream);
 
+/* The same single-expert sparse down projection as hs_expert_down_sparse,
+ * for callers that cannot allocate device memory: a host framework that owns
+ * every allocation and hands a plugin only the tensors it reads and writes,
+ * or a path that must never enter the CUDA allocator.  The page has no
+ * counterpart; this is an interface convenience of this library.
+ *   Same arguments and results as hs_expert_down_sparse, minus the workspace.
+ *   Scratch: a fixed array inside the library (about 0.75 MB on every GPU
+ *   that loads it, held until the process exits), sized for at most 4096
+ *   neurons and out_dim 3072; larger shapes return HS_ERR_UNSUPPORTED_SHAPE.
+ *   Allocates nothing (no cudaMalloc, no allocating library routine).
+ *   The first call on each device looks up the array's device address once
+ *   (cudaGetSymbolAddress); make that first call before any stream capture.
+ *   Every call shares the one array and overwrites it (nothing in it needs to
+ *   start at zero): calls that can overlap on the GPU, on different streams,
+ *   race with each other; order them on one stream or with events. */
+int hs_expert_down_sparse_noalloc(const float* h_dev, const hs_w4* down_nm, int neurons, int out_dim,
+                                  uint16_t* y_bf16_dev, float* y_f32_dev, int* live_count_dev,
+                                  unsigned flags, hs_stream_t stream);
+
 /* ---------------------------------------------------------- layer decode
  * One MoE layer at decode for `batch` tokens (sections "Inside a MoE layer",
  * "Two projections and a switch", "Our way reads only the rows that fired"):
