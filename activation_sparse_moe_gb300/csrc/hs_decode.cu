@@ -78,6 +78,7 @@ struct DecodeIO {
     float* dbg_topk_w;
     float* dbg_h;
     int* live_counts;        // [units] live rows per unit (workspace)
+    int units;
 };
 
 // Dynamic shared memory layout of one decode CTA (offsets in bytes).
@@ -303,6 +304,18 @@ __device__ __forceinline__ void load_group_codes(const uint8_t* row, int gc, uin
     c1 = f ? a : b;
 }
 
+// Partial rows are stored column-block-major: the 32 outputs of block cb of
+// unit u sit at partial[(cb * U + u) * 32 ...], so one reduce CTA reads the
+// contiguous slice of its block for every unit with a single bulk copy.
+struct PartialOut {
+    float* base;  // [hidden/32][U][32]
+    int U;
+    int u;
+    __device__ __forceinline__ float4* quad(int o4) const {  // outputs 4*o4 .. 4*o4+3
+        return reinterpret_cast<float4*>(base + ((size_t)(o4 >> 3) * U + u) * 32) + (o4 & 7);
+    }
+};
+
 // ------------------------------------------------------------ down phase
 // Given h[64] and the live mask in shared memory, accumulate
 //   partial_o = wgt * (sum_{n live} h_n * (s_o q_{n,o} + b_o))
@@ -317,7 +330,7 @@ __device__ __forceinline__ void load_group_codes(const uint8_t* row, int gc, uin
 // the row's h is pre-scaled by 16^-i to undo the position.
 __device__ void down_accumulate_and_store(const uint8_t* codes_buf, const uint32_t* sb_buf, float* red_buf,
                                           const float* h_s, uint64_t live, float Hsum, float wgt, int hidden,
-                                          float* __restrict__ out_row) {
+                                          const PartialOut out) {
     const int C = hidden / 32;
     const int S = min(256 / C, 7);  // S * C * 33 floats fit in the 64-row code buffer
     const int t = threadIdx.x;
@@ -378,13 +391,12 @@ __device__ void down_accumulate_and_store(const uint8_t* codes_buf, const uint32
             const float2 sb = half2_to_float2(sbw[e]);
             r[e] = wgt * fmaf(sb.x, a[e], sb.y * Hsum);
         }
-        reinterpret_cast<float4*>(out_row)[o4] = make_float4(r[0], r[1], r[2], r[3]);
+        *out.quad(o4) = make_float4(r[0], r[1], r[2], r[3]);
     }
 }
 
-__device__ __forceinline__ void store_zero_row(float* __restrict__ out_row, int hidden) {
-    for (int i = threadIdx.x; i < hidden / 4; i += blockDim.x)
-        reinterpret_cast<float4*>(out_row)[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+__device__ __forceinline__ void store_zero_row(const PartialOut out, int hidden) {
+    for (int i = threadIdx.x; i < hidden / 4; i += blockDim.x) *out.quad(i) = make_float4(0.f, 0.f, 0.f, 0.f);
 }
 
 // Live mask of h_s[0..63] (warp 0), the fixed-order sum of h, and the issue
@@ -577,7 +589,7 @@ moe_decode_b1_kernel(const __grid_constant__ LayerParams P, const DecodeIO io) {
                              codes_buf, sb_buf, &bars[4], live_s, hsum_s, pol);
     __syncthreads();
     const uint64_t live = *live_s;
-    float* out_row = io.partial + (size_t)u * hidden;
+    const PartialOut out_row{io.partial, io.units, u};
     if (t == 0) io.live_counts[u] = __popcll(live);
     if (!live) {
         store_zero_row(out_row, hidden);
@@ -614,7 +626,7 @@ down_sparse_kernel(const float* __restrict__ h, const uint8_t* __restrict__ dn_c
                              policy_evict_first());
     __syncthreads();
     const uint64_t live = *live_s;
-    float* out_row = partial + (size_t)g * hidden;
+    const PartialOut out_row{partial, (int)gridDim.x, g};
     if (t == 0) live_counts[g] = __popcll(live);
     if (!live) { store_zero_row(out_row, hidden); return; }
     if (!__syncthreads_and(mbar_wait(&bars[0], 0))) return;
@@ -623,65 +635,53 @@ down_sparse_kernel(const float* __restrict__ h, const uint8_t* __restrict__ dn_c
 }
 
 // ------------------------------------------------ fixed-order partial sum
-// y[o] = sum_{u=0..U-1} partial[u][o] (u ascending within each of 32 strided
-// subsets, then a fixed tree over the 32 subset sums); bf16 round to nearest
-// even.
-// Also sums the per-unit live counts into *live_total (if non-null).
+// y[o] = sum over the U partial rows, for the 32 outputs of block blockIdx.x:
+// one bulk copy brings the block's [U][32] slice into shared memory; thread
+// (lane, p) adds rows p, p+8, p+16, ... in ascending order, then the 8 sums
+// are added in order p = 0..7; bf16 round to nearest even.  Block 0 also sums
+// the per-unit live counts into *live_total (if non-null).
 __global__ void __launch_bounds__(256)
 reduce_partials_kernel(const float* __restrict__ partial, int U, int hidden, uint16_t* __restrict__ y_bf16,
                        float* __restrict__ y_f32, const int* __restrict__ live_counts, int* __restrict__ live_total) {
-    __shared__ float4 red[32][8];
-    __shared__ float4 red2[8][8];
+    extern __shared__ __align__(128) float slice[];  // [U][32]
+    __shared__ float part[8][33];
+    __shared__ __align__(8) uint64_t bar;
+    const int t = threadIdx.x;
+    const int cb = blockIdx.x;
+    if (t == 0) { mbar_init(&bar, 1); fence_mbar_init(); }
+    __syncthreads();
     pdl_trigger();  // the next kernel may start its weight prefetch now
     pdl_wait();
-    const int t = threadIdx.x;
-    const int col = blockIdx.x * 8 + (t & 7);  // float4 column
-    const int uc = t >> 3;
-    const int ncol = hidden / 4;
-    float4 s = make_float4(0.f, 0.f, 0.f, 0.f);
-    if (col < ncol) {
-        const float4* p = reinterpret_cast<const float4*>(partial) + col;
-        int u = uc;
-        // batches of 8 independent loads, then the adds in unit order
-        for (; u + 7 * 32 < U; u += 8 * 32) {
-            float4 v[8];
-#pragma unroll
-            for (int i = 0; i < 8; ++i) v[i] = __ldcg(p + (size_t)(u + 32 * i) * ncol);
-#pragma unroll
-            for (int i = 0; i < 8; ++i) { s.x += v[i].x; s.y += v[i].y; s.z += v[i].z; s.w += v[i].w; }
-        }
-        for (; u < U; u += 32) {
-            const float4 v = __ldcg(p + (size_t)u * ncol);
-            s.x += v.x; s.y += v.y; s.z += v.z; s.w += v.w;
+    if (t == 0) {
+        mbar_arrive_expect_tx(&bar, (uint32_t)U * 128u);
+        const float* src = partial + (size_t)cb * U * 32;
+        // pieces of at most 32 KB, 16-byte aligned (rows are 128 B)
+        for (int r0 = 0; r0 < U; r0 += 256) {
+            const int rows = min(256, U - r0);
+            bulk_g2s(slice + (size_t)r0 * 32, src + (size_t)r0 * 32, (uint32_t)rows * 128u, &bar, policy_evict_first());
         }
     }
-    red[uc][t & 7] = s;
+    const bool ok = mbar_wait(&bar, 0);
+    if (!__syncthreads_and(ok)) return;
+    const int lane = t & 31, p = t >> 5;
+    float a0 = 0.f, a1 = 0.f;
+    int r = p;
+    for (; r + 8 < U; r += 16) {
+        a0 += slice[r * 32 + lane];
+        a1 += slice[(r + 8) * 32 + lane];
+    }
+    if (r < U) a0 += slice[r * 32 + lane];
+    part[p][lane] = a0 + a1;
     __syncthreads();
-    // fixed tree: 32 unit chunks -> 8 (4 each, in order) -> 1 (8, in order)
-    if (t < 64) {
-        const int c8 = t & 7, p = t >> 3;
-        float4 a = red[4 * p][c8];
+    if (t < 32) {
+        float y = part[0][t];
 #pragma unroll
-        for (int i = 1; i < 4; ++i) {
-            const float4 v = red[4 * p + i][c8];
-            a.x += v.x; a.y += v.y; a.z += v.z; a.w += v.w;
-        }
-        red2[p][c8] = a;
+        for (int i = 1; i < 8; ++i) y += part[i][t];
+        const int o = cb * 32 + t;
+        if (y_f32) y_f32[o] = y;
+        y_bf16[o] = f32_to_bf16_bits(y);
     }
-    __syncthreads();
-    if (t < 8 && col < ncol) {
-        float4 a = red2[0][t];
-#pragma unroll
-        for (int i = 1; i < 8; ++i) {
-            const float4 v = red2[i][t];
-            a.x += v.x; a.y += v.y; a.z += v.z; a.w += v.w;
-        }
-        if (y_f32) reinterpret_cast<float4*>(y_f32)[col] = a;
-        const uint32_t lo = (uint32_t)f32_to_bf16_bits(a.x) | ((uint32_t)f32_to_bf16_bits(a.y) << 16);
-        const uint32_t hi = (uint32_t)f32_to_bf16_bits(a.z) | ((uint32_t)f32_to_bf16_bits(a.w) << 16);
-        reinterpret_cast<uint2*>(y_bf16)[col] = make_uint2(lo, hi);
-    }
-    if (live_total && blockIdx.x == 0 && t == 0) {
+    if (live_total && cb == 0 && t == 0) {
         int n = 0;
         for (int u = 0; u < U; ++u) n += live_counts[u];
         *live_total = n;
@@ -743,6 +743,9 @@ int check_expert(const hs_expert& e, int hidden, int neurons_expected) {
     return HS_OK;
 }
 
+// The reduce pass holds one 128-byte row per unit in shared memory.
+constexpr int kMaxUnits = 1536;
+
 int check_layer(const hs_moe_layer* L) {
     if (!L || !L->routed) return HS_ERR_INVALID_ARG;
     if (L->n_routed < 1 || L->n_routed > hs::kMaxRouted) return HS_ERR_UNSUPPORTED_SHAPE;
@@ -759,6 +762,7 @@ int check_layer(const hs_moe_layer* L) {
         const int st = check_expert(*L->shared, L->hidden, L->shared->neurons);
         if (st != HS_OK) return st;
     }
+    if ((L->shared ? L->shared->neurons / 64 : 0) + L->top_k * (rn / 64) > kMaxUnits) return HS_ERR_UNSUPPORTED_SHAPE;
     return HS_OK;
 }
 
@@ -818,8 +822,9 @@ extern "C" int hs_expert_down_sparse(const float* h, const hs_w4* down_nm, int n
     if (launch_pdl(hs::down_sparse_kernel, dim3(G), dim3(256), smem, s, h, down_nm->codes,
                    static_cast<const uint32_t*>(down_nm->sb), out_dim, flags, partial, counts) != cudaSuccess)
         return HS_ERR_CUDA;
-    if (launch_pdl(hs::reduce_partials_kernel, dim3((out_dim / 4 + 7) / 8), dim3(256), 0, s, (const float*)partial, G,
-                   out_dim, y_bf16, y_f32, (const int*)counts, live_count) != cudaSuccess)
+    if (set_smem_attr((const void*)hs::reduce_partials_kernel, G * 128) != HS_OK) return HS_ERR_CUDA;
+    if (launch_pdl(hs::reduce_partials_kernel, dim3(out_dim / 32), dim3(256), (size_t)G * 128, s,
+                   (const float*)partial, G, out_dim, y_bf16, y_f32, (const int*)counts, live_count) != cudaSuccess)
         return HS_ERR_CUDA;
     return launch_err();
 }
@@ -883,6 +888,7 @@ extern "C" int hs_moe_layer_decode(const hs_moe_layer* L, const uint16_t* x, con
     io.logits = logits;
     io.partial = static_cast<float*>(ws);
     io.live_counts = reinterpret_cast<int*>(static_cast<char*>(ws) + round_up((size_t)U * L->hidden * sizeof(float), 256));
+    io.units = U;
     io.flags = flags;
     io.dbg_topk_idx = dbg ? dbg->topk_idx : nullptr;
     io.dbg_topk_w = dbg ? dbg->topk_w : nullptr;
@@ -893,7 +899,8 @@ extern "C" int hs_moe_layer_decode(const hs_moe_layer* L, const uint16_t* x, con
     if (set_smem_attr((const void*)hs::moe_decode_b1_kernel, smem) != HS_OK) return HS_ERR_CUDA;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     if (launch_pdl(hs::moe_decode_b1_kernel, dim3(U), dim3(256), smem, s, P, io) != cudaSuccess) return HS_ERR_CUDA;
-    if (launch_pdl(hs::reduce_partials_kernel, dim3((L->hidden / 4 + 7) / 8), dim3(256), 0, s,
+    if (set_smem_attr((const void*)hs::reduce_partials_kernel, U * 128) != HS_OK) return HS_ERR_CUDA;
+    if (launch_pdl(hs::reduce_partials_kernel, dim3(L->hidden / 32), dim3(256), (size_t)U * 128, s,
                    (const float*)io.partial, U, L->hidden, y_bf16, y_f32, (const int*)io.live_counts,
                    live_out) != cudaSuccess)
         return HS_ERR_CUDA;
@@ -967,8 +974,9 @@ extern "C" int hs_expert_down_sparse_noalloc(const float* h, const hs_w4* down_n
     if (launch_pdl(hs::down_sparse_kernel, dim3(G), dim3(256), smem, s, h, down_nm->codes,
                    static_cast<const uint32_t*>(down_nm->sb), out_dim, flags, partial, counts) != cudaSuccess)
         return HS_ERR_CUDA;
-    if (launch_pdl(hs::reduce_partials_kernel, dim3((out_dim / 4 + 7) / 8), dim3(256), 0, s, (const float*)partial, G,
-                   out_dim, y_bf16, y_f32, (const int*)counts, live_count) != cudaSuccess)
+    if (set_smem_attr((const void*)hs::reduce_partials_kernel, G * 128) != HS_OK) return HS_ERR_CUDA;
+    if (launch_pdl(hs::reduce_partials_kernel, dim3(out_dim / 32), dim3(256), (size_t)G * 128, s,
+                   (const float*)partial, G, out_dim, y_bf16, y_f32, (const int*)counts, live_count) != cudaSuccess)
         return HS_ERR_CUDA;
     return launch_err();
 }

@@ -237,7 +237,7 @@ def main():
     LG = torch.stack(lgs).to(dev)
     Y = torch.empty((n, 2688), dtype=torch.bfloat16, device=dev)
     wsz = max(dl.workspace_size(1) for dl in layers)
-    WS = torch.empty(wsz, dtype=torch.uint8, device=dev)
+    WS = torch.zeros(wsz, dtype=torch.uint8, device=dev)  # zero before first use (control words)
     stream = torch.cuda.Stream(device=dev)
 
     # untimed pass with debug outputs: live rows and live groups per layer
@@ -278,28 +278,33 @@ def main():
         if ws > 1:
             torch.distributed.barrier()
 
-    def timed(graph, K, W):
+    def timed(graph, K, W, repeats=1):
+        """Median over `repeats` timed regions of K steps (each bracketed by a
+        barrier and device synchronisation); returns (median ms, all ms)."""
         for _ in range(W):
             graph.replay()
         stream.synchronize()
-        barrier()
-        torch.cuda.synchronize()
-        e0 = torch.cuda.Event(enable_timing=True)
-        e1 = torch.cuda.Event(enable_timing=True)
-        with torch.cuda.stream(stream):
-            e0.record(stream)
-            for _ in range(K):
-                graph.replay()
-            e1.record(stream)
-        stream.synchronize()
-        torch.cuda.synchronize()
-        barrier()
-        ms = e0.elapsed_time(e1)
-        if ws > 1:
-            t = torch.tensor([ms], device=dev)
-            torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-            ms = float(t.item())
-        return ms
+        runs = []
+        for _ in range(repeats):
+            barrier()
+            torch.cuda.synchronize()
+            e0 = torch.cuda.Event(enable_timing=True)
+            e1 = torch.cuda.Event(enable_timing=True)
+            with torch.cuda.stream(stream):
+                e0.record(stream)
+                for _ in range(K):
+                    graph.replay()
+                e1.record(stream)
+            stream.synchronize()
+            torch.cuda.synchronize()
+            barrier()
+            ms = e0.elapsed_time(e1)
+            if ws > 1:
+                t = torch.tensor([ms], device=dev)
+                torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+                ms = float(t.item())
+            runs.append(ms)
+        return statistics.median(runs), runs
 
     K, W = args.steps, max(3, args.warmup)
     props = torch.cuda.get_device_properties(dev)
@@ -311,9 +316,9 @@ def main():
         while time.time() < t_end:
             g_sparse.replay()
         stream.synchronize()
-        ms = timed(g_sparse, K, W)
+        ms, ms_runs = timed(g_sparse, K, W, repeats=1 if args.profile else 5)
     clocks = clk.summary()
-    ms_dense = ms if args.profile else timed(g_dense, K, W)
+    ms_dense = ms if args.profile else timed(g_dense, K, W, repeats=3)[0]
 
     us_layer = ms * 1e3 / (K * n)
     us_layer_dense = ms_dense * 1e3 / (K * n)
@@ -336,7 +341,7 @@ def main():
         for l, dl in enumerate(layers):
             hs.hs_moe_layer_decode(dl.c, X[l], LG[l], 1, Y[l], None, 0, None, WS, stream=stream)
         Yh.copy_(Y, non_blocking=True)
-    ms_e2e = ms if args.profile else timed(g_e2e, K, W)
+    ms_e2e = ms if args.profile else timed(g_e2e, K, W, repeats=3)[0]
     us_e2e = ms_e2e * 1e3 / (K * n)
     h2d = X.numel() * X.element_size() + LG.numel() * LG.element_size()
     d2h = Y.numel() * Y.element_size()
@@ -352,7 +357,8 @@ def main():
         src = os.path.join(ROOT, "activation_sparse_moe_gb300", "csrc", "hs_decode.cu")
         out = {
             "metric": METRIC, "value": round(us_layer, 4), "unit": UNIT, "n_gpus": ws, "steps": K, "warmup": W,
-            "ms_per_step": round(ms / K, 6), "higher_is_better": False, "scaling": "weak", "vs_baseline": None,
+            "ms_per_step": round(ms / K, 6), "repeats_us_per_layer": [round(r * 1e3 / (K * n), 3) for r in ms_runs],
+            "higher_is_better": False, "scaling": "weak", "vs_baseline": None,
             "dtype": "f32", "data": "synthetic (seeded; random W4 weights of the page's shapes)",
             "config": _config(args, {"operands": "W4 weights, bf16 activations, fp32 accumulate, bf16 out"}),
             "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",

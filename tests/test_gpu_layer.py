@@ -33,7 +33,7 @@ def make_layer(L: synth.LayerInputs, top_k):
 def run_layer(dl: DeviceLayer, x, lg, flags=0):
     H = dl.hidden
     NS = dl.shared.N if dl.shared is not None else 0
-    ws = torch.empty(dl.workspace_size(1), dtype=torch.uint8, device="cuda")
+    ws = torch.zeros(dl.workspace_size(1), dtype=torch.uint8, device="cuda")
     y = torch.empty(H, dtype=torch.bfloat16, device="cuda")
     yf = torch.empty(H, dtype=torch.float32, device="cuda")
     dbg = {"topk_idx": torch.full((dl.top_k,), -1, dtype=torch.int32, device="cuda"),
