@@ -109,6 +109,7 @@ struct SmemLayout {
 // elementwise best of L[j] and R[7-j] is the top 8 of the union as a bitonic
 // sequence, which a 3-stage bitonic merger sorts.  After the last level every
 // lane holds the overall top 8.  Lane 0 writes idx[k], w[k] (shared memory).
+
 __device__ __forceinline__ bool topk_better(float a, int ia, float b, int ib) {
     return a > b || (a == b && ia < ib);
 }
@@ -189,62 +190,67 @@ struct XFixed {
 // Cooperative conversion of x into the fixed-point table: 4 threads per
 // group of 64, thread q covering x[16q..16q+15] (code words 2q, 2q+1).  The
 // group maximum and sum combine the 4 partials by a fixed 2-level tree.
-// Threads first..first+4G-1 take part; returns after writing the table.
+// Threads first..blockDim-1 (whole warps) take the work items round-robin.
+// E comes from the exponent field of the maximum (max < 2^E); rounding to the
+// integer grid uses the 1.5 * 2^23 magic constant (exact: |x * 2^(15-E)| < 2^15).
 __device__ __forceinline__ void convert_x_fixed(const uint16_t* x_s, int G, uint8_t* xf_s, float* xs_s, int first) {
-    const int i = threadIdx.x - first;
-    if (i < 0 || i >= 4 * G) return;
-    const int grp = i >> 2, q = i & 3;
-    const uint4 r0 = reinterpret_cast<const uint4*>(x_s + 64 * grp + 16 * q)[0];
-    const uint4 r1 = reinterpret_cast<const uint4*>(x_s + 64 * grp + 16 * q)[1];
-    const uint32_t w[8] = {r0.x, r0.y, r0.z, r0.w, r1.x, r1.y, r1.z, r1.w};
-    float xv[16];
+    const int nthr = blockDim.x - first;
+    for (int i0 = threadIdx.x - first; i0 - (int)(threadIdx.x & 31) < 4 * G; i0 += nthr) {
+        // whole warps iterate together (the shuffles need all lanes); idle lanes work on item 0
+        const bool act = i0 < 4 * G;
+        const int i = act ? i0 : 0;
+        const int grp = i >> 2, q = i & 3;
+        const uint4 r0 = reinterpret_cast<const uint4*>(x_s + 64 * grp + 16 * q)[0];
+        const uint4 r1 = reinterpret_cast<const uint4*>(x_s + 64 * grp + 16 * q)[1];
+        const uint32_t w[8] = {r0.x, r0.y, r0.z, r0.w, r1.x, r1.y, r1.z, r1.w};
+        float xv[16];
 #pragma unroll
-    for (int m = 0; m < 8; ++m) {
-        xv[2 * m] = __uint_as_float(w[m] << 16);
-        xv[2 * m + 1] = __uint_as_float(w[m] & 0xffff0000u);
-    }
-    float mx = 0.f, sa = 0.f, sb = 0.f;
-#pragma unroll
-    for (int m = 0; m < 16; m += 2) {
-        mx = fmaxf(mx, fmaxf(fabsf(xv[m]), fabsf(xv[m + 1])));
-        sa += xv[m];
-        sb += xv[m + 1];
-    }
-    float sm = sa + sb;
-    // the 4 threads of a group are adjacent lanes (first is a multiple of 4):
-    // a fixed xor tree among exactly those lanes
-    const unsigned m4 = 0xFu << (threadIdx.x & 28);
-    mx = fmaxf(mx, __shfl_xor_sync(m4, mx, 1));
-    sm += __shfl_xor_sync(m4, sm, 1);
-    mx = fmaxf(mx, __shfl_xor_sync(m4, mx, 2));
-    sm += __shfl_xor_sync(m4, sm, 2);
-    int e = 0;
-    if (mx > 0.f) frexpf(mx, &e);   // mx < 2^e
-    e = max(e, -100);               // keeps 2^(15-e) and 2^(e-19) normal floats
-    const float scale = __int_as_float((127 + 15 - e) << 23);   // 2^(15-e)
-    // words 2q, 2q+1: bytes b of word j <-> x[8j + 2b] (even) and x[8j + 2b + 1] (odd)
-    uint32_t hE[2], hO[2], lE[2], lO[2];
-#pragma unroll
-    for (int jj = 0; jj < 2; ++jj) {
-        hE[jj] = hO[jj] = lE[jj] = lO[jj] = 0;
-#pragma unroll
-        for (int b = 0; b < 4; ++b) {
-            const int X0 = __float2int_rn(xv[8 * jj + 2 * b] * scale);
-            const int X1 = __float2int_rn(xv[8 * jj + 2 * b + 1] * scale);
-            hE[jj] |= (uint32_t)((X0 >> 8) & 0xff) << (8 * b);
-            lE[jj] |= (uint32_t)(X0 & 0xff) << (8 * b);
-            hO[jj] |= (uint32_t)((X1 >> 8) & 0xff) << (8 * b);
-            lO[jj] |= (uint32_t)(X1 & 0xff) << (8 * b);
+        for (int m = 0; m < 8; ++m) {
+            xv[2 * m] = __uint_as_float(w[m] << 16);
+            xv[2 * m + 1] = __uint_as_float(w[m] & 0xffff0000u);
         }
-    }
-    uint8_t* tb = xf_s + grp * SmemLayout::kXfStride + 8 * q;
-    *reinterpret_cast<uint2*>(tb) = make_uint2(hE[0], hE[1]);
-    *reinterpret_cast<uint2*>(tb + 32) = make_uint2(hO[0], hO[1]);
-    *reinterpret_cast<uint2*>(tb + 64) = make_uint2(lE[0], lE[1]);
-    *reinterpret_cast<uint2*>(tb + 96) = make_uint2(lO[0], lO[1]);
-    if (q == 0) {
-        xs_s[2 * grp] = __int_as_float((127 + e - 19) << 23);   // 2^(E-15) / 16
-        xs_s[2 * grp + 1] = sm;
+        float mx = 0.f, sa = 0.f, sb = 0.f;
+#pragma unroll
+        for (int m = 0; m < 16; m += 2) {
+            mx = fmaxf(mx, fmaxf(fabsf(xv[m]), fabsf(xv[m + 1])));
+            sa += xv[m];
+            sb += xv[m + 1];
+        }
+        float sm = sa + sb;
+        // the 4 threads of a group are adjacent lanes: fixed xor tree
+        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
+        sm += __shfl_xor_sync(0xffffffffu, sm, 1);
+        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
+        sm += __shfl_xor_sync(0xffffffffu, sm, 2);
+        int e = (int)((__float_as_uint(mx) >> 23) & 0xff) - 126;  // mx < 2^e (mx normal)
+        e = max(e, -100);                                          // zero / subnormal maxima
+        const float scale = __int_as_float((127 + 15 - e) << 23);  // 2^(15-e)
+        // words 2q, 2q+1: byte b of word j <-> x[8j + 2b] (even) and x[8j + 2b + 1] (odd)
+        uint32_t hE[2], hO[2], lE[2], lO[2];
+#pragma unroll
+        for (int jj = 0; jj < 2; ++jj) {
+            hE[jj] = hO[jj] = lE[jj] = lO[jj] = 0;
+#pragma unroll
+            for (int b = 0; b < 4; ++b) {
+                const int X0 = __float_as_int(fmaf(xv[8 * jj + 2 * b], scale, 12582912.f)) - 0x4B400000;
+                const int X1 = __float_as_int(fmaf(xv[8 * jj + 2 * b + 1], scale, 12582912.f)) - 0x4B400000;
+                hE[jj] |= (uint32_t)((X0 >> 8) & 0xff) << (8 * b);
+                lE[jj] |= (uint32_t)(X0 & 0xff) << (8 * b);
+                hO[jj] |= (uint32_t)((X1 >> 8) & 0xff) << (8 * b);
+                lO[jj] |= (uint32_t)(X1 & 0xff) << (8 * b);
+            }
+        }
+        if (act) {
+            uint8_t* tb = xf_s + grp * SmemLayout::kXfStride + 8 * q;
+            *reinterpret_cast<uint2*>(tb) = make_uint2(hE[0], hE[1]);
+            *reinterpret_cast<uint2*>(tb + 32) = make_uint2(hO[0], hO[1]);
+            *reinterpret_cast<uint2*>(tb + 64) = make_uint2(lE[0], lE[1]);
+            *reinterpret_cast<uint2*>(tb + 96) = make_uint2(lO[0], lO[1]);
+            if (q == 0) {
+                xs_s[2 * grp] = __int_as_float((127 + e - 19) << 23);   // 2^(E-15) / 16
+                xs_s[2 * grp + 1] = sm;
+            }
+        }
     }
 }
 
@@ -494,17 +500,16 @@ moe_decode_b1_kernel(const __grid_constant__ LayerParams P, const DecodeIO io) {
     const bool up_active = r0 < S;
     uint8_t* xf_s = smem + SmemLayout::xf_off(hidden);
     float* xs_s = reinterpret_cast<float*>(smem + SmemLayout::xs_off(hidden));
-    bool ok = true;
-    if (need_topk && t < 32) {
-        warp_topk_softmax(io.logits, P.n_routed, P.top_k, topk_i, topk_w);
-    } else {
-        ok = mbar_wait(&bars[5], 0);
-        if (ok) convert_x_fixed(x_s, G, xf_s, xs_s, need_topk ? 32 : 0);
-    }
-    if (!__syncthreads_and(ok)) return;
-    if (u == 0 && io.dbg_topk_idx && t < P.top_k) {
-        io.dbg_topk_idx[t] = topk_i[t];
-        io.dbg_topk_w[t] = topk_w[t];
+    // routing first, with the rest of the CTA idle (a latency-bound chain);
+    // the routed weight copies go out before x is converted, so the
+    // conversion overlaps their latency
+    if (need_topk) {
+        if (t < 32) warp_topk_softmax(io.logits, P.n_routed, P.top_k, topk_i, topk_w);
+        __syncthreads();
+        if (u == 0 && io.dbg_topk_idx && t < P.top_k) {
+            io.dbg_topk_idx[t] = topk_i[t];
+            io.dbg_topk_w[t] = topk_w[t];
+        }
     }
     float wgt = 1.f;
     if (!is_shared) {
@@ -515,6 +520,9 @@ moe_decode_b1_kernel(const __grid_constant__ LayerParams P, const DecodeIO io) {
     }
     float off_r = 0.f;
     if (t < 64 && ep.up_off) off_r = ep.up_off[g * 64 + t];
+    bool ok = mbar_wait(&bars[5], 0);
+    if (ok) convert_x_fixed(x_s, G, xf_s, xs_s, 0);
+    if (!__syncthreads_and(ok)) return;
 
     // ---- up projection for 64 rows
     XFixed xf;
