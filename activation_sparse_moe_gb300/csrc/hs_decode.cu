@@ -27,47 +27,13 @@
 //    turned into bf16 (128 + q) with one LOP3 per two codes and multiplied
 //    with the bf16 activations by mixed-precision FMA into fp32 (exact
 //    products); the 128 * sum(x) term is removed per 32-code chunk.
-#include "hs_common.cuh"
+#include "hs_kernels.cuh"
+#include "hs_host.h"
 
 #include <cstring>
 #include <mutex>
 
 namespace hs {
-
-struct ExpertPtrs {
-    const uint8_t* up_codes;   // [neurons][hidden/2]
-    const uint32_t* up_sb;     // [neurons][hidden/64] (scale, bias)
-    const uint8_t* dn_codes;   // [neurons][hidden/2] neuron-major
-    const uint32_t* dn_sb;     // [neurons/64][hidden] (scale, bias)
-    const float* up_off;       // [neurons] or null
-};
-
-struct LayerParams {
-    ExpertPtrs routed[kMaxRouted];
-    ExpertPtrs shared;
-    long long stride[5];  // when uniform: byte strides of the 5 fields between experts
-    int uniform;          // routed[e] = routed[0] + e * stride (no table lookup)
-    int n_routed;
-    int routed_neurons;
-    int shared_neurons;   // 0 if no shared expert
-    int hidden;
-    int top_k;
-};
-
-// Pointers of routed expert e: by arithmetic when the experts are stacked at
-// uniform strides (no dependent load), else from the table.
-__device__ __forceinline__ ExpertPtrs routed_ptrs(const LayerParams& P, int e) {
-    if (P.uniform) {
-        ExpertPtrs b = P.routed[0];
-        b.up_codes += e * P.stride[0];
-        b.up_sb = reinterpret_cast<const uint32_t*>(reinterpret_cast<const char*>(b.up_sb) + e * P.stride[1]);
-        b.dn_codes += e * P.stride[2];
-        b.dn_sb = reinterpret_cast<const uint32_t*>(reinterpret_cast<const char*>(b.dn_sb) + e * P.stride[3]);
-        if (b.up_off) b.up_off = reinterpret_cast<const float*>(reinterpret_cast<const char*>(b.up_off) + e * P.stride[4]);
-        return b;
-    }
-    return P.routed[e];
-}
 
 struct DecodeIO {
     const uint16_t* x;       // [hidden] bf16
@@ -94,221 +60,11 @@ struct SmemLayout {
     static constexpr int kH = 0, kOff = 256, kLg = 512, kRank = kLg + 4 * kMaxRouted, kSelV = kRank + 1024,
                          kSelI = kSelV + 32, kTopI = kSelI + 32, kTopW = kTopI + 32, kBarsOff = kTopW + 32,
                          kLive = kBarsOff + 64, kHsum = kLive + 8, kX = kHsum + 24;
-    static constexpr int kXfStride = 144;  // 128 B of bytes + 16 B pad: conflict-free 128-bit loads
     __host__ __device__ static int x_off(int hidden) { return misc_off(hidden) + kX; }
     __host__ __device__ static int xf_off(int hidden) { return x_off(hidden) + 2 * hidden; }
-    __host__ __device__ static int xs_off(int hidden) { return xf_off(hidden) + (hidden / 64) * kXfStride; }
+    __host__ __device__ static int xs_off(int hidden) { return xf_off(hidden) + (hidden / 64) * hs::kXfStride; }
     __host__ __device__ static int total(int hidden) { return xs_off(hidden) + (hidden / 64) * 8; }
 };
-
-// ------------------------------------------------------------------ router
-// Top-k of n <= 128 logits (ties -> lower index) and a softmax over the chosen
-// k <= 8, by one warp in registers.  Lane l sorts logits l, l+32, l+64, l+96
-// (value descending, index ascending) into a list of 8 padded with losers.
-// Five butterfly levels merge each lane's list with its xor partner's: the
-// elementwise best of L[j] and R[7-j] is the top 8 of the union as a bitonic
-// sequence, which a 3-stage bitonic merger sorts.  After the last level every
-// lane holds the overall top 8.  Lane 0 writes idx[k], w[k] (shared memory).
-
-__device__ __forceinline__ bool topk_better(float a, int ia, float b, int ib) {
-    return a > b || (a == b && ia < ib);
-}
-
-__device__ __forceinline__ void topk_cx(float (&v)[8], int (&id)[8], int a, int b) {
-    // order positions a < b best-first
-    const bool sw = topk_better(v[b], id[b], v[a], id[a]);
-    const float va = v[a], vb = v[b];
-    const int ia = id[a], ib = id[b];
-    v[a] = sw ? vb : va; v[b] = sw ? va : vb;
-    id[a] = sw ? ib : ia; id[b] = sw ? ia : ib;
-}
-
-__device__ void warp_topk_softmax(const float* __restrict__ logits, int n, int k, int* idx, float* w) {
-    const int lane = threadIdx.x & 31;
-    float v[8];
-    int id[8];
-#pragma unroll
-    for (int i = 0; i < 8; ++i) {
-        const int e = lane + 32 * i;
-        const bool real = i < 4 && e < n;
-        id[i] = real ? e : 1024 + 32 * i + lane;  // padding loses every comparison
-        v[i] = real ? logits[e] : -INFINITY;
-    }
-    topk_cx(v, id, 0, 1); topk_cx(v, id, 2, 3); topk_cx(v, id, 0, 2); topk_cx(v, id, 1, 3); topk_cx(v, id, 1, 2);
-#pragma unroll
-    for (int off = 16; off; off >>= 1) {
-        float rv[8];
-        int ri[8];
-#pragma unroll
-        for (int j = 0; j < 8; ++j) {
-            rv[j] = __shfl_xor_sync(0xffffffffu, v[j], off);
-            ri[j] = __shfl_xor_sync(0xffffffffu, id[j], off);
-        }
-#pragma unroll
-        for (int j = 0; j < 8; ++j) {
-            if (topk_better(rv[7 - j], ri[7 - j], v[j], id[j])) { v[j] = rv[7 - j]; id[j] = ri[7 - j]; }
-        }
-#pragma unroll
-        for (int d = 4; d; d >>= 1) {
-#pragma unroll
-            for (int j = 0; j < 8; ++j)
-                if (!(j & d)) topk_cx(v, id, j, j + d);
-        }
-    }
-    if (lane == 0) {
-        float ex[kMaxTopK];
-        float den = 0.f;
-#pragma unroll
-        for (int j = 0; j < kMaxTopK; ++j) ex[j] = (j < k) ? expf(v[j] - v[0]) : 0.f;
-#pragma unroll
-        for (int j = 0; j < kMaxTopK; ++j) den += ex[j];
-        const float inv = 1.f / den;
-#pragma unroll
-        for (int j = 0; j < kMaxTopK; ++j)
-            if (j < k) { idx[j] = id[j]; w[j] = ex[j] * inv; }
-    }
-}
-
-// ------------------------------------------------------------- up phase
-// Dot products of the CTA's 64 up rows with x on the integer pipes.
-// Thread (gc, r0) owns scale group gc (64 codes, 32 bytes) of every row
-// r = r0 + S*i.  Its 64 activations are held as a 16-bit fixed-point copy
-// with one exponent for the group, X_k = round(x_k * 2^(15-E)) with
-// max|x_k| < 2^E, split into a signed high byte and an unsigned low byte
-// (X = 256*H + L).  A bf16 x with |x| >= 2^(E-8) is represented exactly (its
-// 8 significant bits fit); smaller ones are off by at most 2^(E-16).  Per
-// group and row:
-//   sum_k q_k X_k = 256 * dp4a(q, H) + dp4a(q, L)    (exact in int32)
-// with the codes split into even/odd nibble bytes by one mask each.
-struct XFixed {
-    int hE[8], hO[8];          // high bytes of X for even / odd codes of word j
-    unsigned lE[8], lO[8];     // low bytes
-    float inv;                 // 2^(E-15) / 16 (the group dot products carry a factor 16)
-    float xsum;                // sum of the 64 x values (fp32)
-};
-
-// Cooperative conversion of x into the fixed-point table: 4 threads per
-// group of 64, thread q covering x[16q..16q+15] (code words 2q, 2q+1).  The
-// group maximum and sum combine the 4 partials by a fixed 2-level tree.
-// Threads first..blockDim-1 (whole warps) take the work items round-robin.
-// E comes from the exponent field of the maximum (max < 2^E); rounding to the
-// integer grid uses the 1.5 * 2^23 magic constant (exact: |x * 2^(15-E)| < 2^15).
-__device__ __forceinline__ void convert_x_fixed(const uint16_t* x_s, int G, uint8_t* xf_s, float* xs_s, int first) {
-    const int nthr = blockDim.x - first;
-    for (int i0 = threadIdx.x - first; i0 - (int)(threadIdx.x & 31) < 4 * G; i0 += nthr) {
-        // whole warps iterate together (the shuffles need all lanes); idle lanes work on item 0
-        const bool act = i0 < 4 * G;
-        const int i = act ? i0 : 0;
-        const int grp = i >> 2, q = i & 3;
-        const uint4 r0 = reinterpret_cast<const uint4*>(x_s + 64 * grp + 16 * q)[0];
-        const uint4 r1 = reinterpret_cast<const uint4*>(x_s + 64 * grp + 16 * q)[1];
-        const uint32_t w[8] = {r0.x, r0.y, r0.z, r0.w, r1.x, r1.y, r1.z, r1.w};
-        float xv[16];
-#pragma unroll
-        for (int m = 0; m < 8; ++m) {
-            xv[2 * m] = __uint_as_float(w[m] << 16);
-            xv[2 * m + 1] = __uint_as_float(w[m] & 0xffff0000u);
-        }
-        float mx = 0.f, sa = 0.f, sb = 0.f;
-#pragma unroll
-        for (int m = 0; m < 16; m += 2) {
-            mx = fmaxf(mx, fmaxf(fabsf(xv[m]), fabsf(xv[m + 1])));
-            sa += xv[m];
-            sb += xv[m + 1];
-        }
-        float sm = sa + sb;
-        // the 4 threads of a group are adjacent lanes: fixed xor tree
-        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
-        sm += __shfl_xor_sync(0xffffffffu, sm, 1);
-        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
-        sm += __shfl_xor_sync(0xffffffffu, sm, 2);
-        int e = (int)((__float_as_uint(mx) >> 23) & 0xff) - 126;  // mx < 2^e (mx normal)
-        e = max(e, -100);                                          // zero / subnormal maxima
-        const float scale = __int_as_float((127 + 15 - e) << 23);  // 2^(15-e)
-        // words 2q, 2q+1: byte b of word j <-> x[8j + 2b] (even) and x[8j + 2b + 1] (odd)
-        uint32_t hE[2], hO[2], lE[2], lO[2];
-#pragma unroll
-        for (int jj = 0; jj < 2; ++jj) {
-            hE[jj] = hO[jj] = lE[jj] = lO[jj] = 0;
-#pragma unroll
-            for (int b = 0; b < 4; ++b) {
-                const int X0 = __float_as_int(fmaf(xv[8 * jj + 2 * b], scale, 12582912.f)) - 0x4B400000;
-                const int X1 = __float_as_int(fmaf(xv[8 * jj + 2 * b + 1], scale, 12582912.f)) - 0x4B400000;
-                hE[jj] |= (uint32_t)((X0 >> 8) & 0xff) << (8 * b);
-                lE[jj] |= (uint32_t)(X0 & 0xff) << (8 * b);
-                hO[jj] |= (uint32_t)((X1 >> 8) & 0xff) << (8 * b);
-                lO[jj] |= (uint32_t)(X1 & 0xff) << (8 * b);
-            }
-        }
-        if (act) {
-            uint8_t* tb = xf_s + grp * SmemLayout::kXfStride + 8 * q;
-            *reinterpret_cast<uint2*>(tb) = make_uint2(hE[0], hE[1]);
-            *reinterpret_cast<uint2*>(tb + 32) = make_uint2(hO[0], hO[1]);
-            *reinterpret_cast<uint2*>(tb + 64) = make_uint2(lE[0], lE[1]);
-            *reinterpret_cast<uint2*>(tb + 96) = make_uint2(lO[0], lO[1]);
-            if (q == 0) {
-                xs_s[2 * grp] = __int_as_float((127 + e - 19) << 23);   // 2^(E-15) / 16
-                xs_s[2 * grp + 1] = sm;
-            }
-        }
-    }
-}
-
-__device__ __forceinline__ void load_x_fixed(const uint8_t* xf_s, const float* xs_s, int gc, XFixed& xf) {
-    const uint4* p = reinterpret_cast<const uint4*>(xf_s + gc * SmemLayout::kXfStride);
-    uint4 v[8];
-#pragma unroll
-    for (int i = 0; i < 8; ++i) v[i] = p[i];
-#pragma unroll
-    for (int i = 0; i < 2; ++i) {
-        xf.hE[4 * i] = (int)v[i].x; xf.hE[4 * i + 1] = (int)v[i].y; xf.hE[4 * i + 2] = (int)v[i].z; xf.hE[4 * i + 3] = (int)v[i].w;
-        xf.hO[4 * i] = (int)v[2 + i].x; xf.hO[4 * i + 1] = (int)v[2 + i].y; xf.hO[4 * i + 2] = (int)v[2 + i].z; xf.hO[4 * i + 3] = (int)v[2 + i].w;
-        xf.lE[4 * i] = v[4 + i].x; xf.lE[4 * i + 1] = v[4 + i].y; xf.lE[4 * i + 2] = v[4 + i].z; xf.lE[4 * i + 3] = v[4 + i].w;
-        xf.lO[4 * i] = v[6 + i].x; xf.lO[4 * i + 1] = v[6 + i].y; xf.lO[4 * i + 2] = v[6 + i].z; xf.lO[4 * i + 3] = v[6 + i].w;
-    }
-    xf.inv = xs_s[2 * gc];
-    xf.xsum = xs_s[2 * gc + 1];
-}
-
-// Where the up phase leaves the partial dot product of (row r, group gc): the
-// 4 bytes at word (gc/4 + r)%8 of the group's 32-byte code block.  A warp's
-// stores (consecutive gc, one row) and the row sums' loads (8 rows x 4
-// threads, groups q + 4i) then hit 32 distinct banks (for rows of
-// 1344 bytes; other widths stay correct, with some conflicts).
-__device__ __forceinline__ float* part_slot(uint8_t* codes_buf, int rowb, int r, int gc) {
-    return reinterpret_cast<float*>(codes_buf + r * rowb + 32 * gc + 4 * (((gc >> 2) + r) & 7));
-}
-
-// 16 * sum_k q_k X_k over one scale group: 32 code bytes in two 16-byte
-// halves (codes 8j+i in nibble i of word j; half 1 holds words 4..7).  Even
-// codes are masked in place (q), odd codes too (16 q): no shifts; the factor
-// 16 is carried by the even sums instead.  |16 T| < 2^28: exact in int32.
-__device__ __forceinline__ int group_dot_fixed16(const uint4 c0, const uint4 c1, const XFixed& xf) {
-    const uint32_t w[8] = {c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w};
-    int hE = 0, hO = 0;
-    unsigned lE = 0, lO = 0;
-#pragma unroll
-    for (int j = 0; j < 8; ++j) {
-        const uint32_t ev = w[j] & 0x0F0F0F0Fu;   // q of codes 8j, 8j+2, 8j+4, 8j+6
-        const uint32_t od = w[j] & 0xF0F0F0F0u;   // 16 q of codes 8j+1, ..., 8j+7
-        asm("dp4a.u32.s32 %0, %1, %2, %0;" : "+r"(hE) : "r"(ev), "r"(xf.hE[j]));
-        asm("dp4a.u32.s32 %0, %1, %2, %0;" : "+r"(hO) : "r"(od), "r"(xf.hO[j]));
-        lE = __dp4a(ev, xf.lE[j], lE);
-        lO = __dp4a(od, xf.lO[j], lO);
-    }
-    // 16 T = 16 (256 hE + lE) + (256 hO + lO), hO and lO already carrying 16
-    return (hE * 256 + (int)lE) * 16 + hO * 256 + (int)lO;
-}
-
-// Reads the two 16-byte halves of group gc of a row, in an order that makes
-// the 8-lane phases of a warp's 128-bit shared loads hit distinct banks.
-__device__ __forceinline__ void load_group_codes(const uint8_t* row, int gc, uint4& c0, uint4& c1) {
-    const int f = (gc >> 2) & 1;
-    const uint4 a = *reinterpret_cast<const uint4*>(row + 32 * gc + 16 * f);
-    const uint4 b = *reinterpret_cast<const uint4*>(row + 32 * gc + 16 * (f ^ 1));
-    c0 = f ? b : a;
-    c1 = f ? a : b;
-}
 
 // Partial rows are stored column-block-major: the 32 outputs of block cb of
 // unit u sit at partial[(cb * U + u) * 32 ...], so one reduce CTA reads the
@@ -699,86 +455,8 @@ reduce_partials_kernel(const float* __restrict__ partial, int U, int hidden, uin
 }  // namespace hs
 
 // ===================================================================== host
-namespace {
 
-bool al16(const void* p) { return ((uintptr_t)p & 15u) == 0; }
-bool al4(const void* p) { return ((uintptr_t)p & 3u) == 0; }
-
-size_t round_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
-
-int launch_err() { return cudaGetLastError() == cudaSuccess ? HS_OK : HS_ERR_CUDA; }
-
-template <typename... KArgs, typename... Args>
-cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t s, Args... args) {
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = grid;
-    cfg.blockDim = block;
-    cfg.dynamicSmemBytes = smem;
-    cfg.stream = s;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr[0].val.programmaticStreamSerializationAllowed = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, kern, args...);
-}
-
-// Raises a kernel's dynamic shared memory limit once per (kernel, device, size):
-// the attribute call is kept out of the per-call path (and out of stream capture
-// after the first eager call).
-int set_smem_attr(const void* fn, int bytes) {
-    struct Entry { const void* fn; int dev; int bytes; };
-    static Entry done[64];
-    static int n_done = 0;
-    static std::mutex mu;
-    std::lock_guard<std::mutex> lock(mu);
-    int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess) return HS_ERR_CUDA;
-    for (int i = 0; i < n_done; ++i)
-        if (done[i].fn == fn && done[i].dev == dev && done[i].bytes >= bytes) return HS_OK;
-    if (cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes) != cudaSuccess)
-        return HS_ERR_CUDA;
-    if (n_done < 64) done[n_done++] = Entry{fn, dev, bytes};
-    return HS_OK;
-}
-
-int check_expert(const hs_expert& e, int hidden, int neurons_expected) {
-    if (!e.up.codes || !e.up.sb || !e.down_nm.codes || !e.down_nm.sb) return HS_ERR_INVALID_ARG;
-    if (e.neurons != neurons_expected) return HS_ERR_UNSUPPORTED_SHAPE;
-    if (!al16(e.up.codes) || !al16(e.up.sb) || !al16(e.down_nm.codes) || !al16(e.down_nm.sb)) return HS_ERR_MISALIGNED;
-    if (e.up_offset && !al4(e.up_offset)) return HS_ERR_MISALIGNED;
-    (void)hidden;
-    return HS_OK;
-}
-
-// The reduce pass holds one 128-byte row per unit in shared memory.
-constexpr int kMaxUnits = 1536;
-
-int check_layer(const hs_moe_layer* L) {
-    if (!L || !L->routed) return HS_ERR_INVALID_ARG;
-    if (L->n_routed < 1 || L->n_routed > hs::kMaxRouted) return HS_ERR_UNSUPPORTED_SHAPE;
-    if (L->top_k < 1 || L->top_k > hs::kMaxTopK || L->top_k > L->n_routed) return HS_ERR_UNSUPPORTED_SHAPE;
-    if (L->hidden < 64 || L->hidden > hs::kMaxHidden || L->hidden % 64) return HS_ERR_UNSUPPORTED_SHAPE;
-    const int rn = L->routed[0].neurons;
-    if (rn < 64 || rn % 64) return HS_ERR_UNSUPPORTED_SHAPE;
-    for (int e = 0; e < L->n_routed; ++e) {
-        const int st = check_expert(L->routed[e], L->hidden, rn);
-        if (st != HS_OK) return st;
-    }
-    if (L->shared) {
-        if (L->shared->neurons < 64 || L->shared->neurons % 64) return HS_ERR_UNSUPPORTED_SHAPE;
-        const int st = check_expert(*L->shared, L->hidden, L->shared->neurons);
-        if (st != HS_OK) return st;
-    }
-    if ((L->shared ? L->shared->neurons / 64 : 0) + L->top_k * (rn / 64) > kMaxUnits) return HS_ERR_UNSUPPORTED_SHAPE;
-    return HS_OK;
-}
-
-int decode_units(const hs_moe_layer* L) {
-    return (L->shared ? L->shared->neurons / 64 : 0) + L->top_k * (L->routed[0].neurons / 64);
-}
-
-}  // namespace
+using namespace hs_host;
 
 extern "C" const char* hs_status_string(int status) {
     switch (status) {
@@ -799,6 +477,7 @@ extern "C" int hs_device_status(int* status) {
     unsigned v = 0, zero = 0;
     if (cudaMemcpyFromSymbol(&v, hs::g_status, sizeof(v)) != cudaSuccess) return HS_ERR_CUDA;
     if (cudaMemcpyToSymbol(hs::g_status, &zero, sizeof(zero)) != cudaSuccess) return HS_ERR_CUDA;
+    v |= hs_batch_take_status();
     *status = v ? HS_ERR_TIMEOUT : HS_OK;
     return HS_OK;
 }
@@ -839,6 +518,7 @@ extern "C" int hs_expert_down_sparse(const float* h, const hs_w4* down_nm, int n
 
 // ---------------------------------------------------------- layer decode
 extern "C" size_t hs_moe_layer_decode_workspace_size(const hs_moe_layer* L, int batch) {
+    if (batch > 1) return hs_batch_decode_workspace_size(L, batch);
     if (check_layer(L) != HS_OK || batch != 1) return 0;
     const size_t U = decode_units(L);
     return round_up(U * L->hidden * sizeof(float), 256) + round_up(U * sizeof(int), 256);
@@ -851,44 +531,17 @@ extern "C" int hs_moe_layer_decode(const hs_moe_layer* L, const uint16_t* x, con
     if (st != HS_OK) return st;
     if (!x || !logits || !y_bf16) return HS_ERR_INVALID_ARG;
     if (batch < 1) return HS_ERR_INVALID_ARG;
-    if (batch != 1) return HS_ERR_UNSUPPORTED_SHAPE;
     if (!al16(x) || !al4(logits) || !al16(y_bf16) || (y_f32 && !al16(y_f32)) || !al16(ws)) return HS_ERR_MISALIGNED;
+    if (dbg && ((dbg->topk_idx == nullptr) != (dbg->topk_w == nullptr))) return HS_ERR_INVALID_ARG;
+    if (batch > 1)
+        return hs_batch_decode(L, x, logits, batch, y_bf16, y_f32, flags, dbg, ws, ws_bytes,
+                               reinterpret_cast<cudaStream_t>(stream));
     const size_t need = hs_moe_layer_decode_workspace_size(L, batch);
     if (!ws || ws_bytes < need) return HS_ERR_WORKSPACE;
     if (dbg && ((dbg->topk_idx == nullptr) != (dbg->topk_w == nullptr))) return HS_ERR_INVALID_ARG;
 
     hs::LayerParams P;
-    memset(&P, 0, sizeof(P));
-    auto fill = [](hs::ExpertPtrs& d, const hs_expert& e) {
-        d.up_codes = e.up.codes;
-        d.up_sb = static_cast<const uint32_t*>(e.up.sb);
-        d.dn_codes = e.down_nm.codes;
-        d.dn_sb = static_cast<const uint32_t*>(e.down_nm.sb);
-        d.up_off = e.up_offset;
-    };
-    for (int e = 0; e < L->n_routed; ++e) fill(P.routed[e], L->routed[e]);
-    if (L->shared) fill(P.shared, *L->shared);
-    // experts stacked at uniform strides: the kernel computes their pointers
-    {
-        auto fld = [&](int e, int f) -> long long {
-            const hs::ExpertPtrs& d = P.routed[e];
-            const void* v[5] = {d.up_codes, d.up_sb, d.dn_codes, d.dn_sb, d.up_off};
-            return (long long)(uintptr_t)v[f];
-        };
-        bool uni = true;
-        for (int f = 0; f < 5; ++f) {
-            const long long st = L->n_routed > 1 ? fld(1, f) - fld(0, f) : 0;
-            P.stride[f] = st;
-            for (int e = 0; e < L->n_routed && uni; ++e) uni = (fld(e, f) == fld(0, f) + e * st);
-            if (f == 4) for (int e = 0; e < L->n_routed && uni; ++e) uni = ((fld(e, 4) == 0) == (fld(0, 4) == 0));
-        }
-        P.uniform = uni ? 1 : 0;
-    }
-    P.n_routed = L->n_routed;
-    P.routed_neurons = L->routed[0].neurons;
-    P.shared_neurons = L->shared ? L->shared->neurons : 0;
-    P.hidden = L->hidden;
-    P.top_k = L->top_k;
+    fill_layer_params(L, P);
 
     const int U = decode_units(L);
     hs::DecodeIO io;

@@ -178,7 +178,10 @@ int hs_expert_down_sparse_noalloc(const float* h_dev, const hs_w4* down_nm, int 
  *   logits_dev       [batch][n_routed] fp32 (finite)
  *   y_bf16_dev       [batch][hidden] bf16, required;  y_f32_dev fp32 or NULL
  *   debug            host pointer to device debug outputs, or NULL
- * batch 1 (larger batches return HS_ERR_UNSUPPORTED_SHAPE).  Deterministic.
+ * batch 1..64.  For batch > 1 the tokens are grouped by expert (section
+ * "Sorted by expert") and each expert reads the union of its tokens' live
+ * rows once; hidden must then be a multiple of 128, neurons <= 3712, and the
+ * debug h dump is not available (HS_ERR_INVALID_ARG).  Deterministic.
  * Calls sharing one workspace must not overlap on the GPU. */
 size_t hs_moe_layer_decode_workspace_size(const hs_moe_layer* layer, int batch);
 int hs_moe_layer_decode(const hs_moe_layer* layer, const uint16_t* x_bf16_dev,

@@ -1,0 +1,112 @@
+"""GPU parity of hs_moe_layer_decode with batch > 1 against the oracle.
+
+"Skipping dead neurons..." sections "Inside a MoE layer" and "Sorted by
+expert": each token routes on its own; the tokens are grouped by expert and
+each expert reads the union of its tokens' live rows.  Configuration 4: batch
+2..64, 30% of every expert's neurons permanently dead, p = 0.1 on the rest.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import synth
+from _util import check_bf16_within_one_ulp, check_close
+from activation_sparse_moe_gb300 import hs
+from activation_sparse_moe_gb300.layer import DeviceLayer, from_synth_expert, from_synth_stack
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    from activation_sparse_moe_gb300 import build
+    build.build()
+    hs.lib()
+
+
+def make_layer(L, top_k):
+    routed = from_synth_stack(L.up, L.down, L.offsets)
+    shared = from_synth_expert(L.shared) if L.shared is not None else None
+    return DeviceLayer(routed, shared, top_k)
+
+
+def run_batch(dl, X, LG, flags=0):
+    B, H = X.shape
+    ws = torch.zeros(dl.workspace_size(B), dtype=torch.uint8, device="cuda")
+    assert ws.numel() > 0
+    y = torch.empty((B, H), dtype=torch.bfloat16, device="cuda")
+    yf = torch.empty((B, H), dtype=torch.float32, device="cuda")
+    dbg = {"topk_idx": torch.full((B, dl.top_k), -1, dtype=torch.int32, device="cuda"),
+           "topk_w": torch.zeros((B, dl.top_k), dtype=torch.float32, device="cuda"),
+           "live_rows": torch.full((1,), -1, dtype=torch.int32, device="cuda")}
+    hs.hs_moe_layer_decode(dl.c, X.cuda(), LG.cuda(), B, y, yf, flags, dbg, ws)
+    torch.cuda.synchronize()
+    assert hs.hs_device_status() == hs.HS_OK
+    return y.cpu(), yf.cpu().double().numpy(), {k: v.cpu() for k, v in dbg.items()}
+
+
+def union_rows(ref, L):
+    """Sum over touched experts (and the shared one) of the union live rows."""
+    n = 0
+    for e, (toks, h) in ref["h"].items():
+        n += int((h > 0).any(axis=0).sum())
+    if ref["h_shared"] is not None:
+        n += int((ref["h_shared"] > 0).any(axis=0).sum())
+    return n
+
+
+def check_batch(L, dl, X, LG, K, what, flips_allowed=4):
+    y, yf, dbg = run_batch(dl, X, LG)
+    ref = oracle.moe_tokens(X, LG, L.routed_expert, L.shared, k=K)
+    assert np.array_equal(dbg["topk_idx"].numpy(), ref["idx"]), what
+    np.testing.assert_allclose(dbg["topk_w"].double().numpy(), ref["w"], rtol=2e-6, atol=1e-7)
+    check_close(yf, ref["out"], f"{what} y_f32")
+    for b in range(X.shape[0]):
+        check_bf16_within_one_ulp(y[b], ref["out"][b], f"{what} token {b}", yf[b])
+    # rows read = union live rows (neurons within fp32 error of 0 may flip)
+    assert abs(int(dbg["live_rows"].item()) - union_rows(ref, L)) <= flips_allowed
+    return y, yf, dbg
+
+
+@pytest.mark.parametrize("B", [2, 5, 8])
+def test_small_batch(B):
+    H, E, NR, NS, K = 512, 8, 128, 256, 3
+    L = synth.layer_inputs(0, "t-batch", 0, E, NR, NS, H, p=0.2, p_shared=0.3)
+    X, LG = synth.tokens(0, "t-batch", B, B, H, E)
+    check_batch(L, make_layer(L, K), X, LG, K, f"small B={B}")
+
+
+def test_small_batch_no_shared_with_ties():
+    H, E, NR, K = 256, 6, 64, 2
+    L = synth.layer_inputs(1, "t-batch-ns", 0, E, NR, 0, H, p=0.3, dead_frac=0.3)
+    X, LG = synth.tokens(1, "t-batch-ns", 0, 4, H, E)
+    LG[1, :] = 0.5  # all tied: experts 0 and 1 by the index rule
+    check_batch(L, make_layer(L, K), X, LG, K, "no shared, ties")
+
+
+@pytest.fixture(scope="module")
+def cfg4_layer():
+    """Configuration 4: full-size layer, 30% permanently dead, p = 0.1 on the rest."""
+    L = synth.layer_inputs(0, "cfg4", 0, p=0.1, p_shared=0.1, dead_frac=0.3, device="cuda")
+    return L, make_layer(L, 6)
+
+
+@pytest.mark.parametrize("B", [2, 8, 32, 64])
+def test_config4_parity(cfg4_layer, B):
+    L, dl = cfg4_layer
+    X, LG = synth.tokens(0, "cfg4", B, B)
+    check_batch(L, dl, X, LG, 6, f"config 4 B={B}", flips_allowed=8)
+
+
+def test_config4_dense_flag_and_determinism(cfg4_layer):
+    L, dl = cfg4_layer
+    X, LG = synth.tokens(0, "cfg4", 8, 8)
+    y1, yf1, d1 = run_batch(dl, X, LG)
+    y2, yf2, d2 = run_batch(dl, X, LG)
+    yd, yfd, dd = run_batch(dl, X, LG, flags=hs.HS_FORCE_DENSE)
+    assert np.array_equal(yf1, yf2) and torch.equal(y1, y2)
+    assert np.array_equal(yf1, yfd) and torch.equal(y1, yd)
+    ntouched = len(np.unique(d1["topk_idx"].numpy()))
+    assert int(dd["live_rows"].item()) == ntouched * synth.N_ROUTED + synth.N_SHARED
+    assert int(d1["live_rows"].item()) < int(dd["live_rows"].item())
