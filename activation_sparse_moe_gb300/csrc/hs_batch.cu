@@ -34,6 +34,7 @@ struct BatchMeta {
     int e_off[kMaxRouted + 1];      // grouped pair offsets per expert id
     int up_off[kMaxRouted + 2];     // up unit offsets per touched index (+ shared)
     int live_cnt[kMaxRouted + 1];   // union live rows per touched index (+ shared)
+    int live_grp[kMaxRouted + 1];   // groups with a union live row, same indexing
 };
 
 struct BatchIO {
@@ -57,6 +58,7 @@ struct BatchIO {
     int* dbg_topk_idx;
     float* dbg_topk_w;
     int* live_total;
+    int* live_groups;
 };
 
 // ------------------------------------------------------------------ route
@@ -315,11 +317,16 @@ __global__ void __launch_bounds__(256) batch_down_kernel(const __grid_constant__
         }
         // prefix sums of live counts per mask word (thread 0, NW <= 116)
         if (t == 0) {
-            int acc = 0;
-            for (int w = 0; w < NW; ++w) { wpre[w] = acc; acc += __popc(__ldcg(mask + w)); }
+            int acc = 0, ng = 0;
+            for (int w = 0; w < NW; ++w) {
+                const uint32_t mw = __ldcg(mask + w);
+                wpre[w] = acc;
+                acc += __popc(mw);
+                if ((w & 1) && (mw | __ldcg(mask + w - 1))) ++ng;  // words 2g, 2g+1 cover group g
+            }
             wpre[NW] = acc;
             misc[0] = acc;
-            if (band == 0) io.meta->live_cnt[i] = acc;
+            if (band == 0) { io.meta->live_cnt[i] = acc; io.meta->live_grp[i] = ng; }
         }
         __syncthreads();
         const int nlive = misc[0];
@@ -422,11 +429,12 @@ __global__ void __launch_bounds__(256) batch_reduce_kernel(const __grid_constant
         const uint32_t hi = (uint32_t)f32_to_bf16_bits(a.z) | ((uint32_t)f32_to_bf16_bits(a.w) << 16);
         reinterpret_cast<uint2*>(io.y_bf16)[idx] = make_uint2(lo, hi);
     }
-    if (io.live_total && blockIdx.x == 0 && threadIdx.x == 0) {
+    if ((io.live_total || io.live_groups) && blockIdx.x == 0 && threadIdx.x == 0) {
         const BatchMeta* m = io.meta;
-        int n = 0;
-        for (int i = 0; i < m->n_touched + (P.shared_neurons ? 1 : 0); ++i) n += m->live_cnt[i];
-        *io.live_total = n;
+        int n = 0, ng = 0;
+        for (int i = 0; i < m->n_touched + (P.shared_neurons ? 1 : 0); ++i) { n += m->live_cnt[i]; ng += m->live_grp[i]; }
+        if (io.live_total) *io.live_total = n;
+        if (io.live_groups) *io.live_groups = ng;
     }
 }
 
@@ -514,6 +522,7 @@ int hs_batch_decode(const hs_moe_layer* L, const uint16_t* x, const float* logit
     io.dbg_topk_idx = dbg ? dbg->topk_idx : nullptr;
     io.dbg_topk_w = dbg ? dbg->topk_w : nullptr;
     io.live_total = dbg ? dbg->live_rows : nullptr;
+    io.live_groups = dbg ? dbg->live_groups : nullptr;
 
     int dev = 0, sms = 148;
     if (cudaGetDevice(&dev) != cudaSuccess) return HS_ERR_CUDA;

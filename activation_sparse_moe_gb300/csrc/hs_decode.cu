@@ -406,7 +406,8 @@ down_sparse_kernel(const float* __restrict__ h, const uint8_t* __restrict__ dn_c
 // the per-unit live counts into *live_total (if non-null).
 __global__ void __launch_bounds__(256)
 reduce_partials_kernel(const float* __restrict__ partial, int U, int hidden, uint16_t* __restrict__ y_bf16,
-                       float* __restrict__ y_f32, const int* __restrict__ live_counts, int* __restrict__ live_total) {
+                       float* __restrict__ y_f32, const int* __restrict__ live_counts, int* __restrict__ live_total,
+                       int* __restrict__ live_groups) {
     extern __shared__ __align__(128) float slice[];  // [U][32]
     __shared__ float part[8][33];
     __shared__ __align__(8) uint64_t bar;
@@ -445,10 +446,11 @@ reduce_partials_kernel(const float* __restrict__ partial, int U, int hidden, uin
         if (y_f32) y_f32[o] = y;
         y_bf16[o] = f32_to_bf16_bits(y);
     }
-    if (live_total && cb == 0 && t == 0) {
-        int n = 0;
-        for (int u = 0; u < U; ++u) n += live_counts[u];
-        *live_total = n;
+    if ((live_total || live_groups) && cb == 0 && t == 0) {
+        int n = 0, ng = 0;
+        for (int u = 0; u < U; ++u) { n += live_counts[u]; ng += live_counts[u] > 0; }
+        if (live_total) *live_total = n;
+        if (live_groups) *live_groups = ng;
     }
 }
 
@@ -511,7 +513,8 @@ extern "C" int hs_expert_down_sparse(const float* h, const hs_w4* down_nm, int n
         return HS_ERR_CUDA;
     if (set_smem_attr((const void*)hs::reduce_partials_kernel, G * 128) != HS_OK) return HS_ERR_CUDA;
     if (launch_pdl(hs::reduce_partials_kernel, dim3(out_dim / 32), dim3(256), (size_t)G * 128, s,
-                   (const float*)partial, G, out_dim, y_bf16, y_f32, (const int*)counts, live_count) != cudaSuccess)
+                   (const float*)partial, G, out_dim, y_bf16, y_f32, (const int*)counts, live_count,
+                   (int*)nullptr) != cudaSuccess)
         return HS_ERR_CUDA;
     return launch_err();
 }
@@ -563,7 +566,7 @@ extern "C" int hs_moe_layer_decode(const hs_moe_layer* L, const uint16_t* x, con
     if (set_smem_attr((const void*)hs::reduce_partials_kernel, U * 128) != HS_OK) return HS_ERR_CUDA;
     if (launch_pdl(hs::reduce_partials_kernel, dim3(L->hidden / 32), dim3(256), (size_t)U * 128, s,
                    (const float*)io.partial, U, L->hidden, y_bf16, y_f32, (const int*)io.live_counts,
-                   live_out) != cudaSuccess)
+                   live_out, dbg ? dbg->live_groups : (int*)nullptr) != cudaSuccess)
         return HS_ERR_CUDA;
     return launch_err();
 }
@@ -637,7 +640,8 @@ extern "C" int hs_expert_down_sparse_noalloc(const float* h, const hs_w4* down_n
         return HS_ERR_CUDA;
     if (set_smem_attr((const void*)hs::reduce_partials_kernel, G * 128) != HS_OK) return HS_ERR_CUDA;
     if (launch_pdl(hs::reduce_partials_kernel, dim3(out_dim / 32), dim3(256), (size_t)G * 128, s,
-                   (const float*)partial, G, out_dim, y_bf16, y_f32, (const int*)counts, live_count) != cudaSuccess)
+                   (const float*)partial, G, out_dim, y_bf16, y_f32, (const int*)counts, live_count,
+                   (int*)nullptr) != cudaSuccess)
         return HS_ERR_CUDA;
     return launch_err();
 }

@@ -45,7 +45,8 @@ class hs_moe_layer(C.Structure):
 
 
 class hs_decode_debug(C.Structure):
-    _fields_ = [("topk_idx", C.c_void_p), ("topk_w", C.c_void_p), ("h", C.c_void_p), ("live_rows", C.c_void_p)]
+    _fields_ = [("topk_idx", C.c_void_p), ("topk_w", C.c_void_p), ("h", C.c_void_p), ("live_rows", C.c_void_p),
+                ("live_groups", C.c_void_p)]
 
 
 _lib = None
@@ -188,7 +189,7 @@ def hs_moe_layer_decode(layer: Layer, x_bf16, logits, batch, y_bf16, y_f32=None,
     dbg = None
     if debug is not None:
         dbg = C.byref(hs_decode_debug(_p(debug.get("topk_idx")), _p(debug.get("topk_w")), _p(debug.get("h")),
-                                      _p(debug.get("live_rows"))))
+                                      _p(debug.get("live_rows")), _p(debug.get("live_groups"))))
     _check("hs_moe_layer_decode", lib().hs_moe_layer_decode(
         layer.ref, _p(x_bf16), _p(logits), batch, _p(y_bf16), _p(y_f32), flags, dbg, _p(workspace), nb,
         _stream(stream)))

@@ -47,6 +47,8 @@ def _args():
     ap.add_argument("--p", type=float, default=0.1)
     ap.add_argument("--layers", type=int, default=LAYERS)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--batch-sizes", type=str, default="2,8,32,64",
+                    help="batch decode leg (one MoE layer, 30%% dead neurons); empty to skip")
     ap.add_argument("--profile", action="store_true",
                     help="minimal run for profilers: no clock soak, dense, end-to-end or CPU legs")
     return ap.parse_args()
@@ -204,6 +206,54 @@ def time_oracle(n_layers_max, p, budget_s, steps=None):
     return times
 
 
+def bench_batch(args, dev, stream, timed, bytemodel, hs):
+    """Batch decode through one MoE layer: 8 distinct layers with 30% of every
+    expert's neurons permanently dead and p = 0.1 on the rest, cycled so that
+    the weights a call reads are not left in L2 by the previous call."""
+    import torch
+    import synth
+    from activation_sparse_moe_gb300.layer import DeviceLayer, from_synth_expert, from_synth_stack
+    n_layers = 8
+    layers = []
+    for l in range(n_layers):
+        L = synth.layer_inputs(0, "cfg4", l, p=0.1, p_shared=0.1, dead_frac=0.3, device=dev)
+        layers.append(DeviceLayer(from_synth_stack(L.up, L.down, L.offsets, dev), from_synth_expert(L.shared, dev), 6))
+        del L
+    out = {"workload": "moe_decode_batch_1layer_dead0.3_p0.1 (8 distinct layers cycled)", "unit": "us/layer"}
+    for B in [int(b) for b in args.batch_sizes.split(",") if b]:
+        xs, lgs = zip(*[synth.tokens(0, "cfg4", 100 * B + l, B) for l in range(n_layers)])
+        X = torch.stack(xs).to(dev)
+        LG = torch.stack(lgs).to(dev)
+        Y = torch.empty((n_layers, B, 2688), dtype=torch.bfloat16, device=dev)
+        WS = torch.zeros(max(d.workspace_size(B) for d in layers), dtype=torch.uint8, device=dev)
+        req = 0
+        with torch.cuda.stream(stream):
+            for l, dl in enumerate(layers):
+                dbg = {"topk_idx": torch.empty((B, 6), dtype=torch.int32, device=dev),
+                       "topk_w": torch.empty((B, 6), dtype=torch.float32, device=dev),
+                       "live_rows": torch.empty(1, dtype=torch.int32, device=dev),
+                       "live_groups": torch.empty(1, dtype=torch.int32, device=dev)}
+                hs.hs_moe_layer_decode(dl.c, X[l], LG[l], B, Y[l], None, 0, dbg, WS, stream=stream)
+                stream.synchronize()
+                touched = len(set(dbg["topk_idx"].cpu().numpy().ravel().tolist()))
+                req += bytemodel.decode_layer_bytes(2688, [3712] + [1856] * touched, int(dbg["live_rows"].item()),
+                                                    int(dbg["live_groups"].item()), 128, batch=B)
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            for l, dl in enumerate(layers):
+                hs.hs_moe_layer_decode(dl.c, X[l], LG[l], B, Y[l], None, 0, None, WS, stream=stream)
+        K = max(10, args.steps // 4)
+        ms, _ = timed(g, K, 3, repeats=3)
+        us = ms * 1e3 / (K * n_layers)
+        out[f"B{B}"] = {"us_per_layer": round(us, 3), "us_per_token_layer": round(us / B, 4),
+                        "required_MB_per_layer": round(req / n_layers / 1e6, 2),
+                        "achieved_GBs": round(req / n_layers / (us * 1e-6) / 1e9, 1)}
+        del g, WS
+    del layers
+    torch.cuda.empty_cache()
+    return out
+
+
 def main():
     args = _args()
     ws, rank, local = _dist()
@@ -246,13 +296,15 @@ def main():
     with torch.cuda.stream(stream):
         for l, dl in enumerate(layers):
             dbg = {"h": torch.empty(NS + 6 * NR, dtype=torch.float32, device=dev),
-                   "live_rows": torch.empty(1, dtype=torch.int32, device=dev)}
+                   "live_rows": torch.empty(1, dtype=torch.int32, device=dev),
+                   "live_groups": torch.empty(1, dtype=torch.int32, device=dev)}
             hs.hs_moe_layer_decode(dl.c, X[l], LG[l], 1, Y[l], None, 0, dbg, WS, stream=stream)
             stream.synchronize()
             h = dbg["h"].cpu().numpy()
             live_rows.append(int(dbg["live_rows"].item()))
-            live_groups.append(int((h.reshape(-1, 64) > 0).any(axis=1).sum()))
+            live_groups.append(int(dbg["live_groups"].item()))
             assert live_rows[-1] == int((h > 0).sum())
+            assert live_groups[-1] == int((h.reshape(-1, 64) > 0).any(axis=1).sum())
     assert hs.hs_device_status() == hs.HS_OK
     req_bytes = [bytemodel.decode_layer_bytes(2688, [NS] + [NR] * 6, r, g, 128)
                  for r, g in zip(live_rows, live_groups)]
@@ -346,6 +398,10 @@ def main():
     h2d = X.numel() * X.element_size() + LG.numel() * LG.element_size()
     d2h = Y.numel() * Y.element_size()
 
+    batch = None
+    if not args.profile and args.batch_sizes:
+        batch = bench_batch(args, dev, stream, timed, bytemodel, hs)
+
     cpu = None
     if rank == 0 and ws == 1 and not (args.no_cpu_baseline or args.profile):
         times = time_oracle(3, args.p, budget_s=12.0)
@@ -376,6 +432,7 @@ def main():
             "live": {"rows_per_layer": round(float(np.mean(live_rows)), 1),
                      "groups_per_layer": round(float(np.mean(live_groups)), 1),
                      "required_MB_per_step": round(step_bytes / 1e6, 2)},
+            "batch_decode": batch,
             "cpu_baseline": cpu,
         }
         print(json.dumps(out), flush=True)

@@ -105,6 +105,8 @@ typedef struct {
                           first, then the chosen experts in topk order)      */
     int*   live_rows;  /* int: live down rows read by the call, summed over
                           all (token group, expert) pairs                    */
+    int*   live_groups;/* int: 64-neuron groups whose (scale, bias) slab the
+                          call read, summed the same way                     */
 } hs_decode_debug;
 
 /* Human-readable text of a status code (static storage). */

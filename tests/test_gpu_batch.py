@@ -39,7 +39,8 @@ def run_batch(dl, X, LG, flags=0):
     yf = torch.empty((B, H), dtype=torch.float32, device="cuda")
     dbg = {"topk_idx": torch.full((B, dl.top_k), -1, dtype=torch.int32, device="cuda"),
            "topk_w": torch.zeros((B, dl.top_k), dtype=torch.float32, device="cuda"),
-           "live_rows": torch.full((1,), -1, dtype=torch.int32, device="cuda")}
+           "live_rows": torch.full((1,), -1, dtype=torch.int32, device="cuda"),
+           "live_groups": torch.full((1,), -1, dtype=torch.int32, device="cuda")}
     hs.hs_moe_layer_decode(dl.c, X.cuda(), LG.cuda(), B, y, yf, flags, dbg, ws)
     torch.cuda.synchronize()
     assert hs.hs_device_status() == hs.HS_OK
@@ -47,13 +48,17 @@ def run_batch(dl, X, LG, flags=0):
 
 
 def union_rows(ref, L):
-    """Sum over touched experts (and the shared one) of the union live rows."""
-    n = 0
-    for e, (toks, h) in ref["h"].items():
-        n += int((h > 0).any(axis=0).sum())
+    """Sum over touched experts (and the shared one) of the union live rows
+    and of the 64-neuron groups holding one."""
+    n = ng = 0
+    hs_ = [h for (toks, h) in ref["h"].values()]
     if ref["h_shared"] is not None:
-        n += int((ref["h_shared"] > 0).any(axis=0).sum())
-    return n
+        hs_.append(ref["h_shared"])
+    for h in hs_:
+        u = (h > 0).any(axis=0)
+        n += int(u.sum())
+        ng += int(u.reshape(-1, 64).any(axis=1).sum())
+    return n, ng
 
 
 def check_batch(L, dl, X, LG, K, what, flips_allowed=4):
@@ -65,7 +70,9 @@ def check_batch(L, dl, X, LG, K, what, flips_allowed=4):
     for b in range(X.shape[0]):
         check_bf16_within_one_ulp(y[b], ref["out"][b], f"{what} token {b}", yf[b])
     # rows read = union live rows (neurons within fp32 error of 0 may flip)
-    assert abs(int(dbg["live_rows"].item()) - union_rows(ref, L)) <= flips_allowed
+    n, ng = union_rows(ref, L)
+    assert abs(int(dbg["live_rows"].item()) - n) <= flips_allowed
+    assert abs(int(dbg["live_groups"].item()) - ng) <= flips_allowed
     return y, yf, dbg
 
 

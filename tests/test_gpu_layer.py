@@ -39,7 +39,8 @@ def run_layer(dl: DeviceLayer, x, lg, flags=0):
     dbg = {"topk_idx": torch.full((dl.top_k,), -1, dtype=torch.int32, device="cuda"),
            "topk_w": torch.zeros(dl.top_k, dtype=torch.float32, device="cuda"),
            "h": torch.full((NS + dl.top_k * dl.routed.N,), -1.0, dtype=torch.float32, device="cuda"),
-           "live_rows": torch.full((1,), -1, dtype=torch.int32, device="cuda")}
+           "live_rows": torch.full((1,), -1, dtype=torch.int32, device="cuda"),
+           "live_groups": torch.full((1,), -1, dtype=torch.int32, device="cuda")}
     hs.hs_moe_layer_decode(dl.c, x.reshape(-1).cuda(), lg.reshape(-1).cuda(), 1, y, yf, flags, dbg, ws)
     torch.cuda.synchronize()
     assert hs.hs_device_status() == hs.HS_OK
@@ -61,11 +62,13 @@ def check_layer(L: synth.LayerInputs, dl, x, lg, top_k, what):
         for j, e in enumerate(ref["idx"])]
     flips = 0
     live_total = 0
+    live_groups = 0
     for ex, r, base in slots:
         n = ex.neurons
         hg = hk[base:base + n]
         assert (hg >= 0).all()
         live_total += int((hg > 0).sum())
+        live_groups += int((hg.reshape(-1, 64) > 0).any(axis=1).sum())
         mism = (hg > 0) != (r["h"] > 0)
         if mism.any():
             bound = live_flip_bound(x.reshape(-1), ex.up)
@@ -74,6 +77,7 @@ def check_layer(L: synth.LayerInputs, dl, x, lg, top_k, what):
             flips += int(mism.sum())
         check_close(hg, r["h"], f"{what} h")
     assert int(dbg["live_rows"].item()) == live_total
+    assert int(dbg["live_groups"].item()) == live_groups
     check_close(yf, ref["out"], f"{what} y_f32")
     check_bf16_within_one_ulp(y, ref["out"], f"{what} y_bf16", yf)
     return y, yf, flips
