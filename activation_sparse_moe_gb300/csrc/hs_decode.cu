@@ -480,6 +480,7 @@ extern "C" int hs_device_status(int* status) {
     if (cudaMemcpyFromSymbol(&v, hs::g_status, sizeof(v)) != cudaSuccess) return HS_ERR_CUDA;
     if (cudaMemcpyToSymbol(hs::g_status, &zero, sizeof(zero)) != cudaSuccess) return HS_ERR_CUDA;
     v |= hs_batch_take_status();
+    v |= hs_prefill_take_status();
     *status = v ? HS_ERR_TIMEOUT : HS_OK;
     return HS_OK;
 }

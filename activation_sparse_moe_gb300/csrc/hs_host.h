@@ -131,3 +131,5 @@ int hs_batch_decode(const hs_moe_layer* L, const uint16_t* x, const float* logit
                     cudaStream_t stream);
 // Reads and clears the batch translation unit's device error word.
 unsigned hs_batch_take_status();
+// Reads and clears the prefill translation unit's device error word.
+unsigned hs_prefill_take_status();

@@ -49,6 +49,10 @@ class hs_decode_debug(C.Structure):
                 ("live_groups", C.c_void_p)]
 
 
+class hs_prefill_debug(C.Structure):
+    _fields_ = [("topk_idx", C.c_void_p), ("topk_w", C.c_void_p), ("tiles", C.c_void_p), ("work", C.c_void_p)]
+
+
 _lib = None
 
 _SIGS = {
@@ -66,6 +70,9 @@ _SIGS = {
     "hs_moe_layer_decode": (C.c_int, [C.POINTER(hs_moe_layer), C.c_void_p, C.c_void_p, C.c_int, C.c_void_p,
                                       C.c_void_p, C.c_uint, C.POINTER(hs_decode_debug), C.c_void_p, C.c_size_t,
                                       C.c_void_p]),
+    "hs_moe_prefill_workspace_size": (C.c_size_t, [C.POINTER(hs_moe_layer), C.c_int]),
+    "hs_moe_prefill": (C.c_int, [C.POINTER(hs_moe_layer), C.c_void_p, C.c_void_p, C.c_int, C.c_void_p, C.c_void_p,
+                                 C.c_uint, C.POINTER(hs_prefill_debug), C.c_void_p, C.c_size_t, C.c_void_p]),
 }
 
 
@@ -192,4 +199,21 @@ def hs_moe_layer_decode(layer: Layer, x_bf16, logits, batch, y_bf16, y_f32=None,
                                       _p(debug.get("live_rows")), _p(debug.get("live_groups"))))
     _check("hs_moe_layer_decode", lib().hs_moe_layer_decode(
         layer.ref, _p(x_bf16), _p(logits), batch, _p(y_bf16), _p(y_f32), flags, dbg, _p(workspace), nb,
+        _stream(stream)))
+
+
+def hs_moe_prefill_workspace_size(layer: Layer, tokens: int) -> int:
+    return lib().hs_moe_prefill_workspace_size(layer.ref, tokens)
+
+
+def hs_moe_prefill(layer: Layer, x_bf16, logits, tokens, y_bf16, y_f32=None, flags=0, debug=None, workspace=None,
+                   workspace_bytes=None, stream=None):
+    nb = workspace_bytes if workspace_bytes is not None else (workspace.numel() * workspace.element_size()
+                                                              if workspace is not None else 0)
+    dbg = None
+    if debug is not None:
+        dbg = C.byref(hs_prefill_debug(_p(debug.get("topk_idx")), _p(debug.get("topk_w")), _p(debug.get("tiles")),
+                                       _p(debug.get("work"))))
+    _check("hs_moe_prefill", lib().hs_moe_prefill(
+        layer.ref, _p(x_bf16), _p(logits), tokens, _p(y_bf16), _p(y_f32), flags, dbg, _p(workspace), nb,
         _stream(stream)))

@@ -76,5 +76,8 @@ class DeviceLayer:
     def workspace_size(self, batch: int = 1) -> int:
         return hs.hs_moe_layer_decode_workspace_size(self.c, batch)
 
+    def prefill_workspace_size(self, tokens: int) -> int:
+        return hs.hs_moe_prefill_workspace_size(self.c, tokens)
+
     def nbytes(self) -> int:
         return self.routed.nbytes() + (self.shared.nbytes() if self.shared is not None else 0)

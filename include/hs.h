@@ -191,6 +191,43 @@ int hs_moe_layer_decode(const hs_moe_layer* layer, const uint16_t* x_bf16_dev,
                         float* y_f32_dev, unsigned flags, const hs_decode_debug* debug,
                         void* workspace_dev, size_t workspace_bytes, hs_stream_t stream);
 
+/* --------------------------------------------------------------- prefill
+ * One MoE layer over a prompt chunk of `tokens` tokens (sections "A whole
+ * prompt at once", "Sorted by expert", "Per token sparse, per prompt dense",
+ * "What we do instead"): every token is routed as in decode, the tokens are
+ * grouped by expert, and each expert runs its up projection, ReLU^2 and
+ * down projection as matrix products on the tensor cores, the down product
+ * reading the neuron-major copy directly.  A 64-neuron tile of the down
+ * product is skipped for a tile of up to 256 of the expert's tokens when h is
+ * zero for all of them (the skip does not change the result).
+ *   x_bf16_dev   [tokens][hidden] bf16;  logits_dev [tokens][n_routed] fp32
+ *   y_bf16_dev   [tokens][hidden] bf16, required;  y_f32_dev fp32 or NULL
+ * Arithmetic: x and the dequantised weights as fp16, products accumulated in
+ * fp32, h = max(z, 0)^2 rounded to fp16; h that rounds to 0 counts as dead.
+ * tokens 1..4096; hidden a multiple of 128 (<= 3072); the routed experts'
+ * up and down codes must each be stacked back to back in one buffer (expert
+ * e at base + e * neurons * hidden/2), else HS_ERR_UNSUPPORTED_SHAPE.
+ * Deterministic: the same inputs give bit-identical outputs.  Calls sharing
+ * one workspace must not overlap on the GPU. */
+typedef struct {
+    int*   topk_idx;  /* [tokens][top_k] chosen experts, descending logit  */
+    float* topk_w;    /* [tokens][top_k] router weights                    */
+    int*   tiles;     /* int[2]: 64-neuron down tiles skipped, considered,
+                         summed over (expert, token tile) pairs            */
+    long long* work;  /* int64[3], each summed over (expert, token tile)
+                         pairs of the tile's tokens times: [0] the neurons
+                         live for at least one of them (the union), [1] the
+                         neurons the down product multiplied (64 per tile
+                         not skipped), [2] all of the expert's neurons.
+                         Down-product flops = 2 * hidden * each entry.     */
+} hs_prefill_debug;
+
+size_t hs_moe_prefill_workspace_size(const hs_moe_layer* layer, int tokens);
+int hs_moe_prefill(const hs_moe_layer* layer, const uint16_t* x_bf16_dev, const float* logits_dev,
+                   int tokens, uint16_t* y_bf16_dev, float* y_f32_dev, unsigned flags,
+                   const hs_prefill_debug* debug, void* workspace_dev, size_t workspace_bytes,
+                   hs_stream_t stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -78,3 +78,21 @@ def live_flip_bound(x, up, n_rows=None) -> np.ndarray:
     w = oracle.dequant(up)
     xa = np.abs(oracle.as_f64(x))
     return (w.shape[1] * 2.0 ** -24) * (np.abs(w) @ xa)
+
+
+def check_bf16_rounding(y_bf16: torch.Tensor, y_f32, ref: np.ndarray, what=""):
+    """bf16 output contract when the arithmetic itself uses 16-bit operands
+    (prefill): y_bf16 == RNE(y_f32) bit for bit, and every element within the
+    max-abs bar of the oracle plus half a bf16 ulp (the final rounding).
+    Returns the largest distance in bf16 ulps from RNE(ref)."""
+    own = torch.from_numpy(np.asarray(y_f32, dtype=np.float32)).to(torch.bfloat16)
+    assert torch.equal(own.view(torch.int16), y_bf16.detach().cpu().view(torch.int16)), \
+        f"{what}: bf16 output is not RNE of the kernel's fp32 sums"
+    ref = np.asarray(ref, dtype=np.float64)
+    yb = y_bf16.detach().cpu().float().numpy().astype(np.float64)
+    _, e = np.frexp(np.where(ref != 0, ref, 1.0))
+    half_ulp = np.ldexp(1.0, np.maximum(e - 1, -126) - 8)
+    bound = MAX_ABS * np.abs(ref).max() + half_ulp * 1.001
+    err = np.abs(yb - ref)
+    assert (err <= bound).all(), f"{what}: bf16 error {err.max():.3e} above the bar"
+    return float((np.abs(yb - oracle.bf16_rne(ref)) / (2 * half_ulp)).max())

@@ -85,3 +85,34 @@ def test_repack_argument_errors(lib):
     assert f(A + 1, A, A, 2688, 1856, A, A, None) == hs.HS_ERR_MISALIGNED
     assert lib.hs_pack_sb(A, A, 0, 42, A, None) == hs.HS_ERR_INVALID_ARG
     assert lib.hs_pack_sb(A, A, 10, 42, A + 2, None) == hs.HS_ERR_MISALIGNED
+
+
+def _stacked_layer(n_routed=4, top_k=2, hidden=256, neurons=128, shared=True, base=0x1000000):
+    """Fake descriptors with the routed codes stacked back to back (expert e at
+    base + e * neurons * hidden / 2), as the prefill requires."""
+    step = neurons * hidden // 2
+    ex = [hs.make_expert(base + e * step, base + e * step, base + e * step, base + e * step, None, neurons)
+          for e in range(n_routed)]
+    sh = hs.make_expert(base, base, base, base, None, 256) if shared else None
+    return hs.Layer(ex, sh, hidden, top_k)
+
+
+def test_prefill_argument_errors(lib):
+    f = lib.hs_moe_prefill
+    A = 0x400000
+    L = _stacked_layer()
+    need = hs.hs_moe_prefill_workspace_size(L, 100)
+    assert need > 100 * 256 * (2 + 2 * 2)
+    assert f(L.ref, A, A, 100, A, None, 0, None, A, need - 1, None) == hs.HS_ERR_WORKSPACE
+    assert f(L.ref, A, A, 100, A, None, 0, None, None, need, None) == hs.HS_ERR_WORKSPACE
+    assert f(L.ref, None, A, 100, A, None, 0, None, A, need, None) == hs.HS_ERR_INVALID_ARG
+    assert f(L.ref, A, A, 100, None, None, 0, None, A, need, None) == hs.HS_ERR_INVALID_ARG
+    assert f(L.ref, A, A, 0, A, None, 0, None, A, need, None) == hs.HS_ERR_INVALID_ARG
+    assert f(L.ref, A + 2, A, 100, A, None, 0, None, A, need, None) == hs.HS_ERR_MISALIGNED
+    assert f(L.ref, A, A, 4097, A, None, 0, None, A, need, None) == hs.HS_ERR_UNSUPPORTED_SHAPE
+    assert hs.hs_moe_prefill_workspace_size(L, 4097) == 0
+    # routed experts not stacked back to back, and hidden not a multiple of 128
+    assert hs.hs_moe_prefill_workspace_size(_layer(), 100) == 0
+    assert hs.hs_moe_prefill_workspace_size(_stacked_layer(hidden=192), 100) == 0
+    # the workspace grows with the token count
+    assert hs.hs_moe_prefill_workspace_size(L, 200) > need

@@ -1,0 +1,210 @@
+"""GPU parity of hs_moe_prefill against the oracle.
+
+"Skipping dead neurons..." sections "A whole prompt at once", "Sorted by
+expert", "Per token sparse, per prompt dense" and "What we do instead": the
+prompt's tokens are routed one by one, grouped by expert, and each expert's
+up projection, ReLU^2 and down projection run as matrix products; the result
+is the per-token MoE layer (oracle.moe_tokens).  Configuration 5: 2048
+tokens, top-6 of 128 plus the shared expert, 30% of every expert's neurons
+permanently dead, p = 0.1 on the rest.
+
+The tile skip must not change the result: the sparse call equals the
+HS_FORCE_DENSE call bit for bit, and the number of skipped 64-neuron tiles
+matches the oracle's count of tiles whose h is zero for every token of the
+tile (up to neurons within rounding of zero).
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import synth
+from _util import check_bf16_rounding, check_close
+from activation_sparse_moe_gb300 import hs
+from activation_sparse_moe_gb300.layer import DeviceLayer, from_synth_expert, from_synth_stack
+
+pytestmark = pytest.mark.gpu
+
+TILE = 256   # tokens per token tile of the library's prefill
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    from activation_sparse_moe_gb300 import build
+    build.build()
+    hs.lib()
+
+
+def make_layer(L, top_k):
+    routed = from_synth_stack(L.up, L.down, L.offsets)
+    shared = from_synth_expert(L.shared) if L.shared is not None else None
+    return DeviceLayer(routed, shared, top_k)
+
+
+def run_prefill(dl, X, LG, flags=0):
+    T, H = X.shape
+    ws = torch.zeros(dl.prefill_workspace_size(T), dtype=torch.uint8, device="cuda")
+    assert ws.numel() > 0
+    y = torch.empty((T, H), dtype=torch.bfloat16, device="cuda")
+    yf = torch.empty((T, H), dtype=torch.float32, device="cuda")
+    dbg = {"topk_idx": torch.full((T, dl.top_k), -1, dtype=torch.int32, device="cuda"),
+           "topk_w": torch.zeros((T, dl.top_k), dtype=torch.float32, device="cuda"),
+           "tiles": torch.full((2,), -1, dtype=torch.int32, device="cuda"),
+           "work": torch.full((3,), -1, dtype=torch.int64, device="cuda")}
+    hs.hs_moe_prefill(dl.c, X.cuda(), LG.cuda(), T, y, yf, flags, dbg, ws)
+    torch.cuda.synchronize()
+    assert hs.hs_device_status() == hs.HS_OK
+    return y.cpu(), yf.cpu().double().numpy(), {k: v.cpu() for k, v in dbg.items()}
+
+
+def oracle_tiles(ref, n_routed_neurons, n_shared_neurons, T):
+    """Over (expert, token tile) pairs (an expert's tokens in ascending order,
+    cut into tiles of TILE tokens): 64-neuron down tiles skipped and
+    considered, and the tokens x (union-live, multiplied, all) neurons sums."""
+    skipped = total = union = execd = dense = 0
+    mats = [h for (_toks, h) in ref["h"].values()]
+    if ref["h_shared"] is not None:
+        mats.append(ref["h_shared"])
+    for h in mats:
+        for r in range(0, h.shape[0], TILE):
+            ht = h[r:r + TILE]
+            rows = (ht > 0).any(axis=0)
+            live = rows.reshape(-1, 64).any(axis=1)
+            total += live.size
+            skipped += int((~live).sum())
+            union += ht.shape[0] * int(rows.sum())
+            execd += ht.shape[0] * 64 * int(live.sum())
+            dense += ht.shape[0] * ht.shape[1]
+    return skipped, total, union, execd, dense
+
+
+def check_prefill(L, dl, X, LG, K, what, tile_slack=2):
+    y, yf, dbg = run_prefill(dl, X, LG)
+    ref = oracle.moe_tokens(X, LG, L.routed_expert, L.shared, k=K)
+    assert np.array_equal(dbg["topk_idx"].numpy(), ref["idx"]), what
+    np.testing.assert_allclose(dbg["topk_w"].double().numpy(), ref["w"], rtol=2e-6, atol=1e-7)
+    rel, mx = check_close(yf, ref["out"], f"{what} y_f32")
+    ulps = check_bf16_rounding(y, yf, ref["out"], what)
+    print(f"{what}: rel-L2 {rel:.2e} max-abs/max {mx:.2e} bf16 max ulps from RNE(oracle) {ulps:.0f}")
+    NS = L.shared.neurons if L.shared is not None else 0
+    sk, tot, union, execd, dense = oracle_tiles(ref, L.up.codes.shape[1], NS, X.shape[0])
+    assert int(dbg["tiles"][1]) == tot, what
+    assert abs(int(dbg["tiles"][0]) - sk) <= tile_slack, (what, int(dbg["tiles"][0]), sk)
+    w = [int(v) for v in dbg["work"]]
+    assert w[2] == dense, what
+    # a neuron whose h rounds differently near 0 moves the union by at most one tile's tokens
+    assert abs(w[0] - union) <= tile_slack * TILE, (what, w[0], union)
+    assert abs(w[1] - execd) <= tile_slack * TILE * 64, (what, w[1], execd)
+    assert w[0] <= w[1] <= w[2]
+    return y, yf, dbg
+
+
+def cluster_dead(L, n_groups, seed=0):
+    """Kill whole 64-neuron groups of every routed expert (offset -inf) so that
+    the tile skip has work to do (the oracle reads the same offsets)."""
+    rng = np.random.default_rng(seed)
+    E, N = L.offsets.shape
+    for e in range(E):
+        for g in rng.choice(N // 64, size=n_groups, replace=False):
+            L.offsets[e, 64 * g:64 * (g + 1)] = -np.inf
+
+
+@pytest.mark.parametrize("T", [1, 37, 300])
+def test_small_prefill(T):
+    H, E, NR, NS, K = 512, 8, 128, 256, 3
+    L = synth.layer_inputs(0, "t-prefill", 0, E, NR, NS, H, p=0.2, p_shared=0.3)
+    X, LG = synth.tokens(0, "t-prefill", T, T, H, E)
+    check_prefill(L, make_layer(L, K), X, LG, K, f"small T={T}")
+
+
+def test_multi_tile_experts_and_clustered_dead():
+    """More than 256 tokens per expert (several token tiles), the shared expert
+    over 4 tiles, and whole dead 64-neuron groups that the skip must find."""
+    H, E, NR, NS, K = 256, 4, 256, 192, 2
+    L = synth.layer_inputs(2, "t-prefill-mt", 0, E, NR, NS, H, p=0.05, p_shared=0.2)
+    cluster_dead(L, 2, seed=2)
+    T = 900
+    X, LG = synth.tokens(2, "t-prefill-mt", 0, T, H, E)
+    y, yf, dbg = check_prefill(L, make_layer(L, K), X, LG, K, "multi-tile")
+    assert int(dbg["tiles"][0]) >= 2 * E * 2   # every routed tile skips at least the dead groups
+
+
+def test_no_shared_with_ties_and_ragged_neurons():
+    """No shared expert, tied logits, a neuron count that is not a multiple of
+    128 (the last 128-neuron block is half empty)."""
+    H, E, NR, K = 128, 6, 192, 2
+    L = synth.layer_inputs(1, "t-prefill-ns", 0, E, NR, 0, H, p=0.3, dead_frac=0.3)
+    X, LG = synth.tokens(1, "t-prefill-ns", 0, 50, H, E)
+    LG[3, :] = 0.5
+    check_prefill(L, make_layer(L, K), X, LG, K, "no shared, ties")
+
+
+def test_dense_flag_bit_identical_and_deterministic():
+    H, E, NR, NS, K = 256, 4, 256, 192, 2
+    L = synth.layer_inputs(3, "t-prefill-d", 0, E, NR, NS, H, p=0.05, p_shared=0.2)
+    cluster_dead(L, 1, seed=3)
+    dl = make_layer(L, K)
+    X, LG = synth.tokens(3, "t-prefill-d", 0, 400, H, E)
+    y1, yf1, d1 = run_prefill(dl, X, LG)
+    y2, yf2, d2 = run_prefill(dl, X, LG)
+    yd, yfd, dd = run_prefill(dl, X, LG, flags=hs.HS_FORCE_DENSE)
+    assert np.array_equal(yf1, yf2) and torch.equal(y1, y2)
+    assert np.array_equal(yf1, yfd) and torch.equal(y1, yd)
+    assert int(dd["tiles"][0]) == 0 and int(d1["tiles"][0]) > 0
+    assert int(dd["tiles"][1]) == int(d1["tiles"][1])
+
+
+def test_prefill_argument_errors():
+    H, E, NR, NS, K = 256, 4, 128, 128, 2
+    L = synth.layer_inputs(4, "t-prefill-err", 0, E, NR, NS, H)
+    dl = make_layer(L, K)
+    X, LG = synth.tokens(4, "t-prefill-err", 0, 8, H, E)
+    x, lg = X.cuda(), LG.cuda()
+    y = torch.empty((8, H), dtype=torch.bfloat16, device="cuda")
+    ws = torch.zeros(dl.prefill_workspace_size(8), dtype=torch.uint8, device="cuda")
+    with pytest.raises(hs.HsError) as e:
+        hs.hs_moe_prefill(dl.c, x, lg, 8, y, workspace=ws, workspace_bytes=ws.numel() - 1)
+    assert e.value.status == hs.HS_ERR_WORKSPACE
+    with pytest.raises(hs.HsError) as e:
+        hs.hs_moe_prefill(dl.c, x, lg, 0, y, workspace=ws)
+    assert e.value.status == hs.HS_ERR_INVALID_ARG
+    assert dl.prefill_workspace_size(4097) == 0
+    torch.cuda.synchronize()
+    assert hs.hs_device_status() == hs.HS_OK
+
+
+@pytest.fixture(scope="module")
+def cfg5():
+    """Configuration 5: full-size layer, 30% permanently dead, p = 0.1 on the rest, 2048 tokens."""
+    L = synth.layer_inputs(0, "cfg5", 0, p=0.1, p_shared=0.1, dead_frac=0.3, device="cuda")
+    X, LG = synth.tokens(0, "cfg5", 0, 2048)
+    return L, make_layer(L, 6), X, LG
+
+
+def test_config5_sampled_parity(cfg5):
+    """Full size, in the launch configuration the bench times; the oracle
+    evaluates a sample of tokens one by one (each token's output depends on
+    that token alone)."""
+    L, dl, X, LG = cfg5
+    y, yf, dbg = run_prefill(dl, X, LG)
+    rng = np.random.default_rng(5)
+    sample = np.sort(rng.choice(X.shape[0], size=16, replace=False))
+    ref = oracle.moe_tokens(X[sample], LG[sample], L.routed_expert, L.shared, k=6)
+    assert np.array_equal(dbg["topk_idx"].numpy()[sample], ref["idx"])
+    rel, mx = check_close(yf[sample], ref["out"], "config 5 sampled y_f32")
+    ulps = check_bf16_rounding(y[sample], yf[sample], ref["out"], "config 5 sampled")
+    print(f"config 5 sampled: rel-L2 {rel:.2e} max-abs/max {mx:.2e} bf16 max ulps {ulps:.0f}")
+    # every (expert, token tile) pair is counted once: 58-tile shared expert + 29 tiles per routed tile
+    counts = np.bincount(dbg["topk_idx"].numpy().ravel(), minlength=128)
+    tiles = int(sum((c + TILE - 1) // TILE for c in counts)) * (synth.N_ROUTED // 64)
+    tiles += ((2048 + TILE - 1) // TILE) * (synth.N_SHARED // 64)
+    assert int(dbg["tiles"][1]) == tiles
+    assert np.isfinite(yf).all()
+
+
+def test_config5_dense_flag_equal(cfg5):
+    L, dl, X, LG = cfg5
+    y1, yf1, d1 = run_prefill(dl, X, LG)
+    yd, yfd, dd = run_prefill(dl, X, LG, flags=hs.HS_FORCE_DENSE)
+    assert np.array_equal(yf1, yfd) and torch.equal(y1, yd)
+    assert int(dd["tiles"][0]) == 0
