@@ -30,10 +30,9 @@
 
 namespace hs {
 
-constexpr int kNt = 256;          // max tokens per tile (MMA N)
-constexpr int kStages = 3;        // up / down pipeline depth
+constexpr int kNt = 128;          // max tokens per tile (MMA N)
 constexpr int kMaxTokens = 4096;
-constexpr int kMaxKTiles = 1024;  // 64-neuron tiles per expert (neurons <= 65536)
+constexpr int kMaxKTiles = 64;    // 64-neuron tiles per expert (neurons <= 4096): one 64-bit mask
 
 struct PrefillMeta {
     int n_tiles;                  // token tiles (routed experts first, then shared)
@@ -84,131 +83,97 @@ struct PrefillIO {
 // product use it, so the product is unchanged.
 
 // ------------------------------------------------------------ routing
+// One warp per token: top-k + softmax, and the per-expert pair counts
+// (integer atomics: the counts, hence everything after, do not depend on the
+// order of the additions).  The meta block is zeroed before this kernel runs.
 __global__ void __launch_bounds__(256) prefill_route_kernel(const __grid_constant__ LayerParams P, const PrefillIO io) {
     pdl_wait();
     pdl_trigger();
-    const int tok = blockIdx.x * 8 + (threadIdx.x >> 5);
+    const int tok = blockIdx.x * 8 + (threadIdx.x >> 5), lane = threadIdx.x & 31;
     if (tok < io.T) {
         const int K = P.top_k;
         warp_topk_softmax(io.logits + (size_t)tok * P.n_routed, P.n_routed, K, io.idx + (size_t)tok * K,
                           io.w + (size_t)tok * K);
         __syncwarp();
-        if ((threadIdx.x & 31) < K && io.dbg_idx) {
-            const int j = threadIdx.x & 31;
-            io.dbg_idx[(size_t)tok * K + j] = io.idx[(size_t)tok * K + j];
-            io.dbg_w[(size_t)tok * K + j] = io.w[(size_t)tok * K + j];
+        if (lane < K) {
+            const int e = io.idx[(size_t)tok * K + lane];
+            atomicAdd(&io.meta->cnt[e], 1);
+            if (io.dbg_idx) {
+                io.dbg_idx[(size_t)tok * K + lane] = e;
+                io.dbg_w[(size_t)tok * K + lane] = io.w[(size_t)tok * K + lane];
+            }
         }
     }
 }
 
-// CTA e counts the (token, slot) pairs routed to expert e.
-__global__ void __launch_bounds__(256) prefill_count_kernel(const __grid_constant__ LayerParams P, const PrefillIO io) {
-    __shared__ int part[8];
-    pdl_wait();
-    pdl_trigger();
-    const int e = blockIdx.x, n = io.T * P.top_k;
-    int c = 0;
-    for (int p = threadIdx.x; p < n; p += blockDim.x) c += (io.idx[p] == e);
+// Inclusive sum over the 256 threads of a CTA (8 warps); `tmp` holds 8 ints.
+__device__ __forceinline__ int block_inclusive_sum(int v, int* tmp) {
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
 #pragma unroll
-    for (int off = 16; off; off >>= 1) c += __shfl_xor_sync(0xffffffffu, c, off);
-    if ((threadIdx.x & 31) == 0) part[threadIdx.x >> 5] = c;
-    __syncthreads();
-    if (threadIdx.x == 0) {
-        int s = 0;
-        for (int i = 0; i < 8; ++i) s += part[i];
-        io.meta->cnt[e] = s;
+    for (int off = 1; off < 32; off <<= 1) {
+        const int o = __shfl_up_sync(0xffffffffu, v, off);
+        if (lane >= off) v += o;
     }
+    if (lane == 31) tmp[warp] = v;
+    __syncthreads();
+    int before = 0;
+    for (int i = 0; i < warp; ++i) before += tmp[i];
+    __syncthreads();
+    return v + before;
 }
 
-// One CTA: pair offsets, token tiles, work-unit counts, cleared flags.
+// One CTA: pair offsets, token tiles (an expert's pairs cut into tiles of up
+// to kNt), work-unit counts, cleared live flags.
 __global__ void __launch_bounds__(256) prefill_tiles_kernel(const __grid_constant__ LayerParams P, const PrefillIO io) {
+    __shared__ int tmp[8];
     pdl_wait();
     pdl_trigger();
     PrefillMeta* m = io.meta;
-    const int E = P.n_routed;
-    if (threadIdx.x == 0) {
-        int acc = 0, nt = 0;
-        for (int e = 0; e < E; ++e) {
-            m->off[e] = acc;
-            m->tile_off[e] = nt;
-            const int c = m->cnt[e];
-            for (int r = 0; r < c; r += kNt) {
-                io.tiles[nt] = TileInfo{e, acc + r, min(kNt, c - r), 0};
-                ++nt;
-            }
-            acc += c;
-        }
-        m->off[E] = acc;
-        m->tile_off[E] = nt;
-        if (P.shared_neurons) {
-            for (int r = 0; r < io.T; r += kNt) {
-                io.tiles[nt] = TileInfo{E, r, min(kNt, io.T - r), 0};
-                ++nt;
-            }
-        }
-        m->tile_off[E + 1] = nt;
-        m->n_tiles = nt;
-        const int mr = (P.routed_neurons + 127) / 128, ms = (P.shared_neurons + 127) / 128;
-        m->up_units = (m->tile_off[E]) * mr + (nt - m->tile_off[E]) * ms;
-        m->dn_units = nt * (P.hidden / 128);
-        m->skipped = 0;
-        m->total = 0;
-        m->union_rt = 0;
-        m->exec_rt = 0;
-        m->dense_rt = 0;
+    const int E = P.n_routed, e = threadIdx.x;
+    const int c = e < E ? __ldcg(&m->cnt[e]) : 0;
+    const int nt_e = (c + kNt - 1) / kNt;
+    const int c_incl = block_inclusive_sum(c, tmp);
+    const int t_incl = block_inclusive_sum(nt_e, tmp);
+    const int off = c_incl - c, toff = t_incl - nt_e;
+    if (e < E) {
+        m->off[e] = off;
+        m->tile_off[e] = toff;
+        for (int i = 0; i < nt_e; ++i) io.tiles[toff + i] = TileInfo{e, off + kNt * i, min(kNt, c - kNt * i), 0};
     }
-    // live flags: one word per (tile, 32 k-tiles); up to max_tiles * words
+    __shared__ int tot_s[2];
+    if (e == E - 1) { tot_s[0] = c_incl; tot_s[1] = t_incl; }
+    __syncthreads();
+    const int npairs = tot_s[0], nrt = tot_s[1];
+    const int nst = P.shared_neurons ? (io.T + kNt - 1) / kNt : 0;
+    for (int i = threadIdx.x; i < nst; i += blockDim.x)
+        io.tiles[nrt + i] = TileInfo{E, kNt * i, min(kNt, io.T - kNt * i), 0};
+    if (threadIdx.x == 0) {
+        m->off[E] = npairs;
+        m->tile_off[E] = nrt;
+        m->tile_off[E + 1] = nrt + nst;
+        m->n_tiles = nrt + nst;
+        const int mr = (P.routed_neurons + 127) / 128, ms = (P.shared_neurons + 127) / 128;
+        m->up_units = nrt * mr + nst * ms;
+        m->dn_units = (nrt + nst) * (P.hidden / 128);
+    }
+    // live flags: one word per (tile, 32 k-tiles)
     const int words = io.max_tiles * ((max(P.routed_neurons, P.shared_neurons) / 64 + 31) / 32);
     for (int i = threadIdx.x; i < words; i += blockDim.x) io.flag_r[i] = 0u;
 }
 
-// CTA e lists its pairs in token order (ballot compaction over the token-major
-// pair order) and records each pair's grouped position.
-__global__ void __launch_bounds__(256) prefill_list_kernel(const __grid_constant__ LayerParams P, const PrefillIO io) {
-    __shared__ int wsum[8];
-    __shared__ int base_s;
-    pdl_wait();
-    pdl_trigger();
-    const int e = blockIdx.x, K = P.top_k, n = io.T * K;
-    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    if (threadIdx.x == 0) base_s = io.meta->off[e];
-    __syncthreads();
-    for (int p0 = 0; p0 < n; p0 += blockDim.x) {
-        const int p = p0 + threadIdx.x;
-        const bool hit = p < n && io.idx[p] == e;
-        const unsigned b = __ballot_sync(0xffffffffu, hit);
-        if (lane == 0) wsum[warp] = __popc(b);
-        __syncthreads();
-        int before = 0;
-        for (int i = 0; i < warp; ++i) before += wsum[i];
-        if (hit) {
-            const int pos = base_s + before + __popc(b & ((1u << lane) - 1u));
-            io.pair_tok[pos] = p / K;
-            io.pair_w[pos] = io.w[p];
-            io.pos_of[p] = pos;
-        }
-        __syncthreads();
-        if (threadIdx.x == 0) {
-            int tot = 0;
-            for (int i = 0; i < 8; ++i) tot += wsum[i];
-            base_s += tot;
-        }
-        __syncthreads();
-    }
-}
+// CTA e < E: lists the pairs routed to expert e in token order (a block-wide
+// scan over contiguous chunks of the token-major pair list), records their
+// grouped positions and router weights, and gathers their tokens' x rows.
+// CTAs >= E gather the rows of the shared expert (every token).  Gathered
+// rows are fp16; inside each group of 8 inputs (one word of codes) the order
+// is e0 e4 e1 e5 e2 e6 e3 e7, the order in which the dequantiser emits nibble
+// pairs (both operands of the up product use it).
+constexpr int kListThreads = 256;
 
-// Gathered fp16 rows: row r < T*K is pair r (its token's x), row T*K + t is token t.
-__global__ void __launch_bounds__(256) prefill_gather_kernel(const __grid_constant__ LayerParams P, const PrefillIO io) {
-    pdl_wait();
-    pdl_trigger();
-    const int H = P.hidden, npairs = io.T * P.top_k;
-    const int rows = npairs + (P.shared_neurons ? io.T : 0);
-    const int per_row = H / 8;  // 8 elements per thread-chunk
-    for (size_t q = (size_t)blockIdx.x * blockDim.x + threadIdx.x; q < (size_t)rows * per_row;
-         q += (size_t)gridDim.x * blockDim.x) {
-        const int r = (int)(q / per_row), c8 = (int)(q % per_row);
-        const int tok = r < npairs ? io.pair_tok[r] : r - npairs;
-        const uint4 v = __ldg(reinterpret_cast<const uint4*>(io.x + (size_t)tok * H) + c8);
+__device__ __forceinline__ void gather_row(const uint16_t* __restrict__ xrow, uint16_t* __restrict__ dst, int H,
+                                           int first, int stride) {
+    for (int c8 = first; c8 < H / 8; c8 += stride) {
+        const uint4 v = __ldg(reinterpret_cast<const uint4*>(xrow) + c8);
         const uint32_t wv[4] = {v.x, v.y, v.z, v.w};
         __half hv[8];
 #pragma unroll
@@ -216,94 +181,192 @@ __global__ void __launch_bounds__(256) prefill_gather_kernel(const __grid_consta
             hv[2 * i] = __float2half_rn(__uint_as_float(wv[i] << 16));
             hv[2 * i + 1] = __float2half_rn(__uint_as_float(wv[i] & 0xffff0000u));
         }
-        // elements 8*c8 .. 8*c8+7 are one code word: stored in the dequantiser's order
         const __half2 p0 = __halves2half2(hv[0], hv[4]), p1 = __halves2half2(hv[1], hv[5]);
         const __half2 p2 = __halves2half2(hv[2], hv[6]), p3 = __halves2half2(hv[3], hv[7]);
-        *reinterpret_cast<uint4*>(io.xg + (size_t)r * H + 8 * c8) =
+        reinterpret_cast<uint4*>(dst)[c8] =
             make_uint4(*reinterpret_cast<const uint32_t*>(&p0), *reinterpret_cast<const uint32_t*>(&p1),
                        *reinterpret_cast<const uint32_t*>(&p2), *reinterpret_cast<const uint32_t*>(&p3));
     }
 }
 
-// ------------------------------------------------------------ shared memory
-struct UpSmem {
-    static constexpr int kA = 128 * 128;          // fp16 A tile 128 x 64
-    static constexpr int kB = kNt * 128;          // fp16 B tile up to 256 x 64
-    static constexpr int kC = 128 * 32;           // raw codes 128 rows x 32 B
-    static constexpr int kStage = kA + kB + kC;   // multiple of 1024
-    __host__ __device__ static int sb(int H) { return 128 * (H / 64) * 4; }
-    __host__ __device__ static int total(int H) { return 1024 + kStages * kStage + sb(H) + 128 * 4 + 256; }
-};
-
-struct DownSmem {
-    static constexpr int kA = 128 * 128;          // fp16 A tile 128 outputs x 64 neurons
-    static constexpr int kB = kNt * 128;          // H tile up to 256 tokens x 64 neurons
-    static constexpr int kC = 64 * 64;            // codes 64 neurons x 64 B (128 outputs)
-    static constexpr int kSB = 128 * 4;           // slab slice
-    static constexpr int kStage = kA + kB + kC + 1024;  // keep 1024 alignment
-    __host__ __device__ static int total() { return 1024 + kStages * kStage + 64 + 4 * kMaxKTiles; }
-};
+__global__ void __launch_bounds__(kListThreads) prefill_list_kernel(const __grid_constant__ LayerParams P,
+                                                                    const PrefillIO io) {
+    __shared__ int tmp[8];
+    __shared__ int toks[kMaxTokens];
+    pdl_wait();
+    pdl_trigger();
+    const int E = P.n_routed, K = P.top_k, H = P.hidden, n = io.T * K;
+    if ((int)blockIdx.x >= E) {
+        // shared expert rows: token t -> row T*K + t
+        const int nb = gridDim.x - E, b = blockIdx.x - E;
+        if (!P.shared_neurons) return;
+        for (int t = b; t < io.T; t += nb) gather_row(io.x + (size_t)t * H, io.xg + ((size_t)n + t) * H, H, threadIdx.x, kListThreads);
+        return;
+    }
+    const int e = blockIdx.x;
+    const int chunk = (n + kListThreads - 1) / kListThreads;
+    const int p0 = threadIdx.x * chunk, p1 = min(n, p0 + chunk);
+    int hits = 0;
+    for (int p = p0; p < p1; ++p) hits += (io.idx[p] == e);
+    const int incl = block_inclusive_sum(hits, tmp);
+    const int base = __ldcg(&io.meta->off[e]);
+    int pos = incl - hits;
+    for (int p = p0; p < p1; ++p) {
+        if (io.idx[p] == e) {
+            io.pair_tok[base + pos] = p / K;
+            io.pair_w[base + pos] = io.w[p];
+            io.pos_of[p] = base + pos;
+            toks[pos] = p / K;
+            ++pos;
+        }
+    }
+    __syncthreads();
+    const int cnt = __ldcg(&io.meta->cnt[e]);
+    // gather: one warp per row
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    for (int i = warp; i < cnt; i += kListThreads / 32)
+        gather_row(io.x + (size_t)toks[i] * H, io.xg + (size_t)(base + i) * H, H, lane, 32);
+}
 
 struct TMaps {
-    CUtensorMap up_codes_r, up_codes_s;      // [rows][H/2] bytes, box 32 x 128
+    CUtensorMap up_codes_r, up_codes_s;      // [rows][H/2] bytes, box 64 x 128
     CUtensorMap dn_codes_r, dn_codes_s;      // [rows][H/2] bytes, box 64 x 64
-    CUtensorMap xg[3];                       // fp16 [rows][H], box 64 x {64,128,256}, 128B swizzle
-    CUtensorMap hr[3], hsh[3];               // fp16 H, box 64 x {64,128,256}
+    CUtensorMap xg[2];                       // fp16 [rows][H], box 64 x {64, 128}, 128-byte swizzle
+    CUtensorMap hr[2], hsh[2];               // fp16 h, box 64 x {64, 128}
 };
 
-__device__ __forceinline__ int box_index(int ntok) { return ntok <= 64 ? 0 : (ntok <= 128 ? 1 : 2); }
+// ------------------------------------------------------------ GEMM kernels
+// Both products run as persistent, warp-specialised kernels, one CTA per SM:
+//   warps 0-3    epilogue: read the accumulator from TMEM (lanes 0-127)
+//   warps 4-19   dequantise the 4-bit operand into fp16, in two groups of 8
+//                warps that take alternate k-steps
+//   warp 20      loads the 4-bit codes (and scales) by TMA: weight ring
+//   warp 21      loads the 16-bit operand (x or h) by TMA: activation ring
+//   warp 23      issues the tcgen05 MMAs (one thread); warp 22 idles
+// Every ring slot has a "full" and an "empty" mbarrier; each role counts its
+// own uses, so slot = q % depth and parity = (q / depth) & 1 (producers wait
+// for the previous use of the slot to be released).  The accumulator is
+// double-buffered in TMEM (two 128-column buffers), so the epilogue of one
+// unit overlaps the main loop of the next.  Every wait is bounded; a role
+// that gives up leaves its loop, and the others then give up in turn.
+constexpr int kEpiWarps = 4;
+constexpr int kDqGroup = 8;             // warps per dequantising group
+constexpr int kDqWarps = 2 * kDqGroup;
+constexpr int kWarpW = kEpiWarps + kDqWarps;   // 20
+constexpr int kWarpX = kWarpW + 1;             // 21
+constexpr int kWarpMma = kWarpX + 2;           // 23: sub-partition 3, which hosts the fewest other warps
+constexpr int kGemmThreads = 32 * (kWarpMma + 1);
+constexpr int kTileA = 128 * 128;       // 128 rows x 64 fp16
+constexpr int kTileX = kNt * 128;       // up to 128 rows x 64 fp16
+constexpr unsigned kProducerSleepNs = 64;
+constexpr unsigned kEpilogueSleepNs = 256;
 
-// ------------------------------------------------------------ pipeline
-// Stage ring shared by the two GEMM kernels.  Step q of the CTA (counted
-// across its units) uses stage q % kStages; full[s] completes when the
-// step's operands have landed, done[s] when the MMAs that read them have
-// completed.  Thread 0 issues the loads; every thread dequantises; thread 0
-// issues the MMAs.
-struct Ring {
-    uint64_t* full;
-    uint64_t* done;
-    uint32_t issued = 0;     // steps whose loads were issued (thread 0)
-    uint32_t committed = 0;  // steps whose MMAs were committed (thread 0)
-    // Thread 0: waits until the stage of step `issued` is free.  False on timeout.
-    __device__ bool acquire() {
-        const uint32_t q = issued;
-        return q < kStages || mbar_wait(&done[q % kStages], ((q / kStages) - 1) & 1);
+// Ring depths: weight codes (WD), 16-bit operand (XD), dequantised tiles (AD).
+template <int WD, int XD, int AD>
+struct GemmBars {
+    uint64_t *wfull, *wempty, *xfull, *xempty, *afull, *aempty, *sbfull, *sbempty, *tfull, *tempty;
+    uint32_t* tmem_slot;
+    static constexpr int kCount = 2 * WD + 2 * XD + 2 * AD + 2 * 2 + 2 * 2;
+    __device__ GemmBars(uint8_t* p) {
+        uint64_t* b = reinterpret_cast<uint64_t*>(p);
+        wfull = b; wempty = wfull + WD; xfull = wempty + WD; xempty = xfull + XD;
+        afull = xempty + XD; aempty = afull + AD; sbfull = aempty + AD; sbempty = sbfull + 2;
+        tfull = sbempty + 2; tempty = tfull + 2;
+        tmem_slot = reinterpret_cast<uint32_t*>(tempty + 2);
     }
-    // Thread 0, on the way out: waits (bounded) for the loads still in flight
-    // and for the last committed MMAs, so that no copy lands and no MMA reads
-    // after the CTA leaves.
-    __device__ void drain() {
-        const uint32_t lo = issued > (uint32_t)kStages ? issued - kStages : 0;
-        for (uint32_t q = lo; q < issued; ++q) mbar_wait(&full[q % kStages], (q / kStages) & 1);
-        if (committed) mbar_wait(&done[(committed - 1) % kStages], ((committed - 1) / kStages) & 1);
+    __device__ void init() {
+        for (int i = 0; i < WD; ++i) { mbar_init(&wfull[i], 1); mbar_init(&wempty[i], kDqGroup); }
+        for (int i = 0; i < XD; ++i) { mbar_init(&xfull[i], 1); mbar_init(&xempty[i], 1); }
+        for (int i = 0; i < AD; ++i) { mbar_init(&afull[i], kDqGroup); mbar_init(&aempty[i], 1); }
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(&sbfull[i], 1); mbar_init(&sbempty[i], kDqWarps);
+            mbar_init(&tfull[i], 1); mbar_init(&tempty[i], kEpiWarps);
+        }
+        fence_mbar_init();
     }
 };
 
-// ------------------------------------------------------------ up GEMM
-__global__ void __launch_bounds__(256, 1)
+// Producer-side wait for slot q of a ring of depth d to be free.
+__device__ __forceinline__ bool wait_free(uint64_t* empty, int d, uint32_t q) {
+    return mbar_wait(&empty[q % d], ((q / d) & 1u) ^ 1u);
+}
+__device__ __forceinline__ bool wait_full(uint64_t* full, int d, uint32_t q) {
+    return mbar_wait(&full[q % d], (q / d) & 1u);
+}
+// The same with a sleep between polls (producers, epilogue).
+__device__ __forceinline__ bool wait_free_sleep(uint64_t* empty, int d, uint32_t q, unsigned ns) {
+    return mbar_wait_sleep(&empty[q % d], ((q / d) & 1u) ^ 1u, ns);
+}
+__device__ __forceinline__ bool wait_full_sleep(uint64_t* full, int d, uint32_t q, unsigned ns) {
+    return mbar_wait_sleep(&full[q % d], (q / d) & 1u, ns);
+}
+// A producer on its way out: waits (bounded) for its last loads to land.
+__device__ __forceinline__ void drain_loads(uint64_t* full, int d, uint32_t issued) {
+    for (uint32_t q = issued > (uint32_t)d ? issued - d : 0; q < issued; ++q) wait_full(full, d, q);
+}
+
+// ---- up GEMM: unit = (token tile, 128-neuron block); D[neuron][token].  One k-step covers
+// 128 inputs (two scale groups).  TMEM: columns 0-255 the two accumulators, 256-511 four
+// dequantised A tiles (128 lanes x 64 columns = 128 rows x 128 fp16 each).
+constexpr int kUpWD = 5, kUpXD = 4, kUpAD = 4;
+using UpBars = GemmBars<kUpWD, kUpXD, kUpAD>;
+constexpr int kUpK = 128;                  // inputs per k-step
+
+struct UpLayout {
+    static constexpr int kXSlot = 2 * kTileX;           // two 64-input swizzled sub-tiles
+    static constexpr int kX = 0;
+    static constexpr int kW = kX + kUpXD * kXSlot;
+    static constexpr int kWSlot = 128 * kUpK / 2;       // 128 rows x 128 codes
+    static constexpr int kSB = kW + kUpWD * kWSlot;
+    __host__ __device__ static int sb_words(int H) { return 128 * (H / 64); }
+    __host__ __device__ static int bars(int H) { return kSB + 2 * 4 * sb_words(H); }
+    __host__ __device__ static int total(int H) { return 1024 + bars(H) + 8 * UpBars::kCount + 64; }
+};
+
+struct UpUnit {
+    int tile, row0, rows, ntok, nt16, bi, cy, xrow, N, row_out;
+    bool shared;
+    ExpertPtrs ep;
+};
+
+__device__ __forceinline__ UpUnit up_unit(const LayerParams& P, const PrefillIO& io, int ntr, int mr, int ms, int u) {
+    UpUnit d;
+    int mb;
+    if (u < ntr * mr) { d.tile = u / mr; mb = u % mr; }
+    else { d.tile = ntr + (u - ntr * mr) / ms; mb = (u - ntr * mr) % ms; }
+    const TileInfo ti = io.tiles[d.tile];
+    d.shared = ti.e == P.n_routed;
+    d.N = d.shared ? P.shared_neurons : P.routed_neurons;
+    d.ep = d.shared ? P.shared : routed_ptrs(P, ti.e);
+    d.row0 = 128 * mb;
+    d.rows = min(128, d.N - d.row0);
+    d.ntok = ti.ntok;
+    d.nt16 = (ti.ntok + 15) & ~15;
+    d.bi = ti.ntok <= 64 ? 0 : 1;
+    d.cy = d.shared ? d.row0 : ti.e * P.routed_neurons + d.row0;
+    d.xrow = d.shared ? io.T * P.top_k + ti.row0 : ti.row0;
+    d.row_out = ti.row0;
+    return d;
+}
+
+__global__ void __launch_bounds__(kGemmThreads, 1)
 prefill_up_kernel(const __grid_constant__ LayerParams P, const PrefillIO io, const __grid_constant__ TMaps tm) {
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    const int H = P.hidden, G = H / 64;
-    uint8_t* stage0 = smem;
-    uint32_t* sb_s = reinterpret_cast<uint32_t*>(smem + kStages * UpSmem::kStage);
-    float* off_s = reinterpret_cast<float*>(reinterpret_cast<uint8_t*>(sb_s) + UpSmem::sb(H));
-    uint64_t* bars = reinterpret_cast<uint64_t*>(off_s + 128);   // full[kStages], done[kStages], sb
-    uint32_t* tmem_s = reinterpret_cast<uint32_t*>(bars + 2 * kStages + 1);
-    uint64_t* sbbar = bars + 2 * kStages;
-    Ring ring;
-    ring.full = bars;
-    ring.done = bars + kStages;
+    const int H = P.hidden, G = H / 64, KS = H / kUpK;
+    uint8_t* sX = smem + UpLayout::kX;
+    uint8_t* sW = smem + UpLayout::kW;
+    uint32_t* sSB = reinterpret_cast<uint32_t*>(smem + UpLayout::kSB);
+    const int sbw = UpLayout::sb_words(H);
+    UpBars br(smem + UpLayout::bars(H));
     const int t = threadIdx.x, warp = t >> 5, lane = t & 31;
-    if (t == 0) {
-        for (int i = 0; i < 2 * kStages + 1; ++i) mbar_init(&bars[i], 1);
-        fence_mbar_init();
-    }
-    if (warp == 0) tmem_alloc(tmem_s, 256);
+    if (t == 0) br.init();
+    if (warp == 0) tmem_alloc(br.tmem_slot, 512);
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
-    const uint32_t tmem = *tmem_s;
+    const uint32_t tmem = *br.tmem_slot;
+    const uint32_t tmem_a = tmem + 256;
     pdl_wait();
     pdl_trigger();
     const PrefillMeta* m = io.meta;
@@ -312,285 +375,421 @@ prefill_up_kernel(const __grid_constant__ LayerParams P, const PrefillIO io, con
     const int mr = (NR + 127) / 128, ms = (NS + 127) / 128;
     const int U = m->up_units;
     const int words = (max(NR, NS) / 64 + 31) / 32;
-    uint32_t it = 0;  // steps consumed
-    uint32_t sbphase = 0;
     bool ok = true;
-    for (int u = blockIdx.x; u < U && ok; u += gridDim.x) {
-        // ---- unit: token tile x 128-neuron block
-        int tile, mb;
-        if (u < ntr * mr) { tile = u / mr; mb = u % mr; }
-        else { tile = ntr + (u - ntr * mr) / ms; mb = (u - ntr * mr) % ms; }
-        const TileInfo ti = io.tiles[tile];
-        const bool shared = ti.e == E;
-        const int N = shared ? NS : NR;
-        const ExpertPtrs ep = shared ? P.shared : routed_ptrs(P, ti.e);
-        const int row0 = 128 * mb;
-        const int rows = min(128, N - row0);
-        const int nt16 = (ti.ntok + 15) & ~15;
-        const int bi = box_index(ti.ntok);
-        const uint32_t bbytes = (uint32_t)(64 << bi) * 128;
-        const CUtensorMap* cmap = shared ? &tm.up_codes_s : &tm.up_codes_r;
-        const CUtensorMap* xmap = &tm.xg[bi];
-        const int cy = shared ? row0 : ti.e * NR + row0;
-        const int xrow = shared ? io.T * P.top_k + ti.row0 : ti.row0;
-        auto issue = [&](int k) -> bool {
-            if (!ring.acquire()) return false;
-            const int s = ring.issued % kStages;
-            uint8_t* st = stage0 + s * UpSmem::kStage;
-            mbar_arrive_expect_tx(&ring.full[s], (uint32_t)UpSmem::kC + bbytes);
-            tma_load_2d(st + UpSmem::kA + UpSmem::kB, cmap, 32 * k, cy, &ring.full[s]);
-            tma_load_2d(st + UpSmem::kA, xmap, 64 * k, xrow, &ring.full[s]);
-            ++ring.issued;
-            return true;
-        };
-        if (t == 0) {
-            // scales and biases of the block's rows (the previous unit is done with them)
-            mbar_arrive_expect_tx(sbbar, (uint32_t)rows * G * 4);
-            bulk_g2s(sb_s, ep.up_sb + (size_t)row0 * G, (uint32_t)rows * G * 4, sbbar, policy_evict_first());
-            for (int k = 0; k < kStages - 1 && k < G && ok; ++k) ok = issue(k);
+
+    if (warp == kWarpW) {
+        // ---- weight codes and (scale, bias) of each unit's rows
+        if (lane == 0) {
+            const uint64_t pol_stream = policy_evict_first(), pol_keep = policy_evict_last();
+            uint32_t wq = 0, nsb = 0;
+            for (int u = blockIdx.x; u < U && ok; u += gridDim.x) {
+                const UpUnit d = up_unit(P, io, ntr, mr, ms, u);
+                const int b = nsb & 1;
+                if (!(ok = wait_free_sleep(br.sbempty, 2, nsb, kProducerSleepNs))) break;
+                mbar_arrive_expect_tx(&br.sbfull[b], (uint32_t)d.rows * G * 4);
+                bulk_g2s(sSB + b * sbw, d.ep.up_sb + (size_t)d.row0 * G, (uint32_t)d.rows * G * 4, &br.sbfull[b],
+                         d.shared ? pol_keep : pol_stream);
+                ++nsb;
+                const CUtensorMap* cmap = d.shared ? &tm.up_codes_s : &tm.up_codes_r;
+                for (int k = 0; k < KS; ++k) {
+                    if (!(ok = wait_free_sleep(br.wempty, kUpWD, wq, kProducerSleepNs))) break;
+                    const int s = wq % kUpWD;
+                    mbar_arrive_expect_tx(&br.wfull[s], UpLayout::kWSlot);
+                    tma_load_2d_hint(sW + s * UpLayout::kWSlot, cmap, (kUpK / 2) * k, d.cy, &br.wfull[s],
+                                     d.shared ? pol_keep : pol_stream);
+                    ++wq;
+                }
+            }
+            drain_loads(br.wfull, kUpWD, wq);
+            drain_loads(br.sbfull, 2, nsb);
         }
-        if (t < 128) off_s[t] = (t < rows && ep.up_off) ? ep.up_off[row0 + t] : 0.f;
-        ok = ok && mbar_wait(sbbar, sbphase);
-        sbphase ^= 1u;
-        ok = __syncthreads_and(ok);
-        const uint32_t idesc = umma_idesc_f16_f32(128, nt16);
-        for (int k = 0; k < G && ok; ++k) {
-            const uint32_t q = it + k;
-            const int s = q % kStages;
-            uint8_t* st = stage0 + s * UpSmem::kStage;
-            if (t == 0 && k + kStages - 1 < G) ok = issue(k + kStages - 1);
-            ok = ok && mbar_wait(&ring.full[s], (q / kStages) & 1);
-            if (ok) {
-                // thread (row r, half hf): 32 codes -> chunks 4hf..4hf+3 of the swizzled fp16 row;
-                // chunk c holds, for its 8 codes c0..c7, the order c0 c4 c1 c5 c2 c6 c3 c7
-                const int r = t >> 1, hf = t & 1;
-                uint8_t* A = st;
-                if (r < rows) {
-                    const uint4 cw = *reinterpret_cast<const uint4*>(st + UpSmem::kA + UpSmem::kB + r * 32 + 16 * hf);
-                    const float2 sbv = half2_to_float2(sb_s[r * G + k]);
+        __syncwarp();
+    } else if (warp == kWarpX) {
+        // ---- gathered tokens (B operand): two 64-input sub-tiles per k-step
+        if (lane == 0) {
+            const uint64_t pol = policy_evict_last();
+            uint32_t xq = 0;
+            for (int u = blockIdx.x; u < U && ok; u += gridDim.x) {
+                const UpUnit d = up_unit(P, io, ntr, mr, ms, u);
+                const uint32_t bytes = (uint32_t)(64 << d.bi) * 128;
+                for (int k = 0; k < KS; ++k) {
+                    if (!(ok = wait_free_sleep(br.xempty, kUpXD, xq, kProducerSleepNs))) break;
+                    const int x = xq % kUpXD;
+                    uint8_t* dst = sX + x * UpLayout::kXSlot;
+                    mbar_arrive_expect_tx(&br.xfull[x], 2 * bytes);
+                    tma_load_2d_hint(dst, &tm.xg[d.bi], kUpK * k, d.xrow, &br.xfull[x], pol);
+                    tma_load_2d_hint(dst + kTileX, &tm.xg[d.bi], kUpK * k + 64, d.xrow, &br.xfull[x], pol);
+                    ++xq;
+                }
+            }
+            drain_loads(br.xfull, kUpXD, xq);
+        }
+        __syncwarp();
+    } else if (warp == kWarpMma) {
+        // ---- MMA issue: A (weights) from TMEM, B (tokens) from shared memory
+        if (lane == 0) {
+            uint32_t aq = 0, xq = 0, nu = 0;
+            for (int u = blockIdx.x; u < U && ok; u += gridDim.x, ++nu) {
+                const UpUnit d = up_unit(P, io, ntr, mr, ms, u);
+                const int acc = nu & 1;
+                if (!(ok = wait_free(br.tempty, 2, nu))) break;
+                tc_fence_after();
+                const uint32_t idesc = umma_idesc_f16_f32(128, d.nt16);
+                const uint32_t dt = tmem + (uint32_t)(acc * 128);
+                for (int k = 0; k < KS; ++k) {
+                    if (!(ok = wait_full(br.afull, kUpAD, aq) && wait_full(br.xfull, kUpXD, xq))) break;
+                    tc_fence_after();
+                    const int a = aq % kUpAD, x = xq % kUpXD;
+                    const uint64_t bd0 = umma_desc_sw128(smem_u32(sX + x * UpLayout::kXSlot));
+                    const uint64_t bd1 = umma_desc_sw128(smem_u32(sX + x * UpLayout::kXSlot + kTileX));
+#pragma unroll
+                    for (int j = 0; j < 8; ++j)
+                        umma_f16_tmem_a(dt, tmem_a + 64 * a + 8 * j, (j < 4 ? bd0 : bd1) + 2 * (j & 3), idesc,
+                                        (k | j) != 0);
+                    umma_commit(&br.aempty[a]);
+                    umma_commit(&br.xempty[x]);
+                    ++aq;
+                    ++xq;
+                }
+                if (ok) umma_commit(&br.tfull[acc]);
+            }
+            // every MMA issued has completed once the last commit has arrived
+            if (aq) wait_full(br.aempty, kUpAD, aq - 1);
+        }
+        __syncwarp();
+    } else if (warp >= kEpiWarps && warp < kWarpW) {
+        // ---- dequantise into TMEM: group g takes the k-steps q with q % 2 == g.  Thread (row r,
+        // half h) converts the 64 codes of scale group 2k+h and writes columns 32h..32h+31 of row r;
+        // each column holds two codes of one word in the order (c0 c4) (c1 c5) (c2 c6) (c3 c7)
+        const int dw = warp - kEpiWarps, g = dw / kDqGroup, h = (dw % kDqGroup) >> 2;
+        const int r = 32 * (warp & 3) + lane;
+        const uint32_t trow = tmem_a + ((uint32_t)(32 * (warp & 3)) << 16) + 32 * h;
+        uint32_t q = 0, nsb = 0;
+        const __half2 k1024 = __floats2half2_rn(1024.f, 1024.f);
+        for (int u = blockIdx.x; u < U && ok; u += gridDim.x) {
+            const UpUnit d = up_unit(P, io, ntr, mr, ms, u);
+            const int b = nsb & 1;
+            ok = __all_sync(0xffffffffu, wait_full(br.sbfull, 2, nsb));
+            if (!ok) break;
+            const uint32_t* sbr = sSB + b * sbw + r * G + h;
+            for (int k = (int)((q & 1u) != (uint32_t)g); k < KS; k += 2) {
+                const uint32_t qk = q + k;
+                ok = __all_sync(0xffffffffu, wait_full(br.wfull, kUpWD, qk) && wait_free(br.aempty, kUpAD, qk));
+                if (!ok) break;
+                tc_fence_after();
+                const int s = qk % kUpWD;
+                uint32_t o[32];
+                if (r < d.rows) {
+                    const uint4* cp = reinterpret_cast<const uint4*>(sW + s * UpLayout::kWSlot + r * (kUpK / 2) + 32 * h);
+                    const uint4 c0 = cp[0], c1 = cp[1];
+                    const float2 sbv = half2_to_float2(sbr[2 * k]);
                     const __half2 s1 = __floats2half2_rn(sbv.x, sbv.x);
                     const __half2 s16 = __floats2half2_rn(sbv.x * 0.0625f, sbv.x * 0.0625f);
                     const __half2 b2 = __floats2half2_rn(sbv.y, sbv.y);
-                    const __half2 k1024 = __floats2half2_rn(1024.f, 1024.f);
-                    const uint32_t w[4] = {cw.x, cw.y, cw.z, cw.w};
+                    const uint32_t w[8] = {c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w};
 #pragma unroll
-                    for (int j = 0; j < 4; ++j) {
+                    for (int j = 0; j < 8; ++j) {
                         const uint32_t lo = w[j], hi = w[j] >> 8;
-                        // fp16 1024 + c (or 1024 + 16c): the code in the low mantissa bits
+                        // fp16 1024 + c (or 1024 + 16c): the code sits in the low mantissa bits
                         const uint32_t pr[4] = {(lo & 0x000F000Fu) | 0x64006400u, (lo & 0x00F000F0u) | 0x64006400u,
                                                 (hi & 0x000F000Fu) | 0x64006400u, (hi & 0x00F000F0u) | 0x64006400u};
-                        uint32_t o[4];
 #pragma unroll
                         for (int p = 0; p < 4; ++p) {
                             const __half2 qv = __hsub2(*reinterpret_cast<const __half2*>(&pr[p]), k1024);
                             const __half2 v = __hfma2(qv, (p & 1) ? s16 : s1, b2);
-                            o[p] = *reinterpret_cast<const uint32_t*>(&v);
+                            o[4 * j + p] = *reinterpret_cast<const uint32_t*>(&v);
                         }
-                        *reinterpret_cast<uint4*>(A + sw128_offset(r, 4 * hf + j)) = make_uint4(o[0], o[1], o[2], o[3]);
                     }
                 } else {
 #pragma unroll
-                    for (int j = 0; j < 4; ++j)
-                        *reinterpret_cast<uint4*>(A + sw128_offset(r, 4 * hf + j)) = make_uint4(0, 0, 0, 0);
+                    for (int i = 0; i < 32; ++i) o[i] = 0u;
+                }
+                __syncwarp();
+                tmem_st32(trow + 64 * (qk % kUpAD), o);
+                tmem_st_wait();
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) {
+                    mbar_arrive(&br.wempty[s]);
+                    mbar_arrive(&br.afull[qk % kUpAD]);
                 }
             }
-            fence_proxy_async_smem();
-            tc_fence_before();
-            ok = __syncthreads_and(ok);
-            if (t == 0 && ok) {
-                tc_fence_after();
-                const uint64_t ad = umma_desc_sw128(smem_u32(st));
-                const uint64_t bd = umma_desc_sw128(smem_u32(st + UpSmem::kA));
-#pragma unroll
-                for (int j = 0; j < 4; ++j) umma_f16(tmem, ad + 2 * j, bd + 2 * j, idesc, (k | j) != 0);
-                umma_commit(&ring.done[s]);
-                ++ring.committed;
-            }
+            if (!ok) break;
+            q += KS;
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&br.sbempty[b]);
+            ++nsb;
         }
-        if (ok) {
-            const uint32_t ql = it + G - 1;
-            ok = mbar_wait(&ring.done[ql % kStages], (ql / kStages) & 1);
-        }
-        ok = __syncthreads_and(ok);
-        tc_fence_after();
-        it += G;
+    } else if (warp < kEpiWarps) {
         // ---- epilogue: + offset, ReLU^2, H (fp16) and the live flags of the block's 64-neuron tiles
-        if (warp < 4 && ok) {
-            const int r = 32 * warp + lane;
-            const int n = row0 + r;
-            const float off = off_s[r];
-            uint16_t* hb = shared ? io.h_s : io.h_r;
-            unsigned anylive = 0;
-            for (int c0 = 0; c0 < nt16; c0 += 16) {
-                float v[16];
-                tmem_ld16(tmem + ((uint32_t)(32 * warp) << 16) + (uint32_t)c0, v);
+        uint32_t nu = 0;
+        for (int u = blockIdx.x; u < U && ok; u += gridDim.x, ++nu) {
+            const UpUnit d = up_unit(P, io, ntr, mr, ms, u);
+            const int acc = nu & 1;
+            const int r = 32 * warp + lane, n = d.row0 + r;
+            const bool rowok = r < d.rows;
+            const float off = (rowok && d.ep.up_off) ? __ldg(d.ep.up_off + n) : 0.f;
+            uint16_t* hcol = (d.shared ? io.h_s : io.h_r) + (size_t)d.row_out * d.N + n;
+            ok = __all_sync(0xffffffffu, wait_full_sleep(br.tfull, 2, nu, kEpilogueSleepNs));
+            if (!ok) break;
+            tc_fence_after();
+            uint32_t live = 0;
+            for (int c0 = 0; c0 < d.nt16; c0 += 32) {
+                float v[32];
+                tmem_ld32(tmem + ((uint32_t)(32 * warp) << 16) + (uint32_t)(acc * 128 + c0), v);
 #pragma unroll
-                for (int i = 0; i < 16; ++i) {
+                for (int i = 0; i < 32; ++i) {
                     const int c = c0 + i;
                     const float z = v[i] + off;
-                    const __half hh = __float2half_rn(z > 0.f ? z * z : 0.f);
-                    const bool in = c < ti.ntok && r < rows;
-                    anylive |= __ballot_sync(0xffffffffu, in && __half2float(hh) > 0.f);
-                    if (in) hb[(size_t)(ti.row0 + c) * N + n] = __half_as_ushort(hh);
+                    const uint16_t hb = __half_as_ushort(__float2half_rn(z > 0.f ? z * z : 0.f));
+                    if (rowok && c < d.ntok) {
+                        hcol[(size_t)c * d.N] = hb;
+                        live |= hb;
+                    }
                 }
             }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&br.tempty[acc]);
+            const unsigned anylive = __ballot_sync(0xffffffffu, live != 0);
             const bool force = (io.flags & HS_FORCE_DENSE) != 0;
-            if (lane == 0 && 32 * warp < rows && (anylive || force)) {
-                const int kt = n / 64;
-                atomicOr(io.flag_r + (size_t)tile * words + kt / 32, 1u << (kt % 32));
+            if (lane == 0 && 32 * warp < d.rows && (anylive || force)) {
+                const int kt = (d.row0 + 32 * warp) / 64;
+                atomicOr(io.flag_r + (size_t)d.tile * words + kt / 32, 1u << (kt % 32));
             }
             if (lane == 0 && anylive)
-                atomicAdd(&io.meta->union_rt, (unsigned long long)__popc(anylive) * (unsigned long long)ti.ntok);
+                atomicAdd(&io.meta->union_rt, (unsigned long long)__popc(anylive) * (unsigned long long)d.ntok);
         }
-        tc_fence_before();
-        __syncthreads();
-        tc_fence_after();
     }
-    if (t == 0) ring.drain();
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
-    if (warp == 0) tmem_dealloc(tmem, 256);
+    if (warp == 0) tmem_dealloc(tmem, 512);
 }
 
-// ------------------------------------------------------------ down GEMM
-__global__ void __launch_bounds__(256, 1)
+// ---- down GEMM: unit = (token tile, 128-output band); D[output][token] over the live 64-neuron tiles.
+// The dequantised tiles stay in shared memory (the transpose from neuron-major codes needs
+// every thread to write several rows).
+constexpr int kDnWD = 10, kDnXD = 7, kDnAD = 4;
+using DnBars = GemmBars<kDnWD, kDnXD, kDnAD>;
+
+struct DownLayout {
+    static constexpr int kA = 0;
+    static constexpr int kX = kA + kDnAD * kTileA;
+    static constexpr int kW = kX + kDnXD * kTileX;
+    static constexpr int kCodes = 64 * 64;                 // 64 neurons x 128 outputs
+    static constexpr int kWSlot = kCodes + 128 * 4;        // + (scale, bias) of 128 outputs
+    static constexpr int kBars = kW + kDnWD * kWSlot;
+    __host__ __device__ static int total() { return 1024 + kBars + 8 * DnBars::kCount + 64; }
+};
+
+struct DownUnit {
+    int tile, ob, ntok, nt16, bi, cy0, NK, row0;
+    bool shared;
+    ExpertPtrs ep;
+    uint64_t live;   // bit j: 64-neuron tile j is multiplied
+};
+
+__device__ __forceinline__ DownUnit down_unit(const LayerParams& P, const PrefillIO& io, int nb, int words, bool dense,
+                                              int u) {
+    DownUnit d;
+    d.tile = u / nb;
+    d.ob = u % nb;
+    const TileInfo ti = io.tiles[d.tile];
+    d.shared = ti.e == P.n_routed;
+    d.NK = (d.shared ? P.shared_neurons : P.routed_neurons) / 64;
+    d.ep = d.shared ? P.shared : routed_ptrs(P, ti.e);
+    d.ntok = ti.ntok;
+    d.nt16 = (ti.ntok + 15) & ~15;
+    d.bi = ti.ntok <= 64 ? 0 : 1;
+    d.cy0 = d.shared ? 0 : ti.e * P.routed_neurons;
+    d.row0 = ti.row0;
+    const uint32_t* f = io.flag_r + (size_t)d.tile * words;
+    const uint64_t all = d.NK == 64 ? ~0ull : ((1ull << d.NK) - 1ull);
+    d.live = dense ? all : ((uint64_t)__ldcg(f) | (words > 1 ? (uint64_t)__ldcg(f + 1) << 32 : 0ull)) & all;
+    return d;
+}
+
+// Iterates the live tiles of a unit in ascending order.
+__device__ __forceinline__ int pop_live(uint64_t& m) {
+    const int j = __ffsll((long long)m) - 1;
+    m &= m - 1;
+    return j;
+}
+
+__global__ void __launch_bounds__(kGemmThreads, 1)
 prefill_down_kernel(const __grid_constant__ LayerParams P, const PrefillIO io, const __grid_constant__ TMaps tm) {
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const int H = P.hidden;
-    uint8_t* stage0 = smem;
-    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kStages * DownSmem::kStage);
-    uint32_t* tmem_s = reinterpret_cast<uint32_t*>(bars + 2 * kStages);
-    int* nk_s = reinterpret_cast<int*>(tmem_s + 2);
-    int* klist = nk_s + 2;   // live k-tiles of the unit, ascending (<= kMaxKTiles)
-    Ring ring;
-    ring.full = bars;
-    ring.done = bars + kStages;
+    uint8_t* sA = smem + DownLayout::kA;
+    uint8_t* sX = smem + DownLayout::kX;
+    uint8_t* sW = smem + DownLayout::kW;
+    DnBars br(smem + DownLayout::kBars);
     const int t = threadIdx.x, warp = t >> 5, lane = t & 31;
-    if (t == 0) {
-        for (int i = 0; i < 2 * kStages; ++i) mbar_init(&bars[i], 1);
-        fence_mbar_init();
-    }
-    if (warp == 0) tmem_alloc(tmem_s, 256);
+    if (t == 0) br.init();
+    if (warp == 0) tmem_alloc(br.tmem_slot, 256);
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
-    const uint32_t tmem = *tmem_s;
+    const uint32_t tmem = *br.tmem_slot;
     pdl_wait();
     pdl_trigger();
     PrefillMeta* m = io.meta;
-    const int E = P.n_routed, NR = P.routed_neurons, NS = P.shared_neurons, K = P.top_k;
+    const int NR = P.routed_neurons, NS = P.shared_neurons, K = P.top_k;
     const int nb = H / 128;
     const int U = m->dn_units;
     const int words = (max(NR, NS) / 64 + 31) / 32;
     const bool dense = (io.flags & HS_FORCE_DENSE) != 0;
-    uint32_t it = 0;
     bool ok = true;
-    for (int u = blockIdx.x; u < U && ok; u += gridDim.x) {
-        // ---- unit: token tile x 128-output band
-        const int tile = u / nb, ob = u % nb;
-        const TileInfo ti = io.tiles[tile];
-        const bool shared = ti.e == E;
-        const int N = shared ? NS : NR;
-        const int NK = N / 64;
-        const ExpertPtrs ep = shared ? P.shared : routed_ptrs(P, ti.e);
-        const int nt16 = (ti.ntok + 15) & ~15;
-        const int bi = box_index(ti.ntok);
-        const uint32_t bbytes = (uint32_t)(64 << bi) * 128;
-        const CUtensorMap* cmap = shared ? &tm.dn_codes_s : &tm.dn_codes_r;
-        const CUtensorMap* hmap = shared ? &tm.hsh[bi] : &tm.hr[bi];
-        const int cy0 = shared ? 0 : ti.e * NR;
-        auto issue = [&](int kk) -> bool {
-            if (!ring.acquire()) return false;
-            const int s = ring.issued % kStages;
-            uint8_t* st = stage0 + s * DownSmem::kStage;
-            const int j = klist[kk];
-            mbar_arrive_expect_tx(&ring.full[s], (uint32_t)(DownSmem::kC + DownSmem::kSB) + bbytes);
-            tma_load_2d(st + DownSmem::kA + DownSmem::kB, cmap, 64 * ob, cy0 + 64 * j, &ring.full[s]);
-            bulk_g2s(st + DownSmem::kA + DownSmem::kB + DownSmem::kC, ep.dn_sb + (size_t)j * H + 128 * ob,
-                     DownSmem::kSB, &ring.full[s], policy_evict_first());
-            tma_load_2d(st + DownSmem::kA, hmap, 64 * j, ti.row0, &ring.full[s]);
-            ++ring.issued;
-            return true;
-        };
-        if (t == 0) {
-            int nk = 0;
-            for (int j = 0; j < NK; ++j) {
-                const uint32_t fw = __ldcg(io.flag_r + (size_t)tile * words + j / 32);
-                if (dense || ((fw >> (j % 32)) & 1u)) klist[nk++] = j;
+
+    if (warp == kWarpW) {
+        // ---- codes + (scale, bias) slab slice of each live 64-neuron tile, this band
+        if (lane == 0) {
+            const uint64_t pol_stream = policy_evict_first(), pol_keep = policy_evict_last();
+            uint32_t wq = 0;
+            for (int u = blockIdx.x; u < U && ok; u += gridDim.x) {
+                const DownUnit d = down_unit(P, io, nb, words, dense, u);
+                const CUtensorMap* cmap = d.shared ? &tm.dn_codes_s : &tm.dn_codes_r;
+                const uint64_t pol = d.shared ? pol_keep : pol_stream;
+                const int nk = __popcll(d.live);
+                for (uint64_t lm = d.live; lm && ok;) {
+                    const int j = pop_live(lm);
+                    if (!(ok = wait_free_sleep(br.wempty, kDnWD, wq, kProducerSleepNs))) break;
+                    const int s = wq % kDnWD;
+                    uint8_t* slot = sW + s * DownLayout::kWSlot;
+                    mbar_arrive_expect_tx(&br.wfull[s], DownLayout::kWSlot);
+                    tma_load_2d_hint(slot, cmap, 64 * d.ob, d.cy0 + 64 * j, &br.wfull[s], pol);
+                    bulk_g2s(slot + DownLayout::kCodes, d.ep.dn_sb + (size_t)j * H + 128 * d.ob, 128 * 4,
+                             &br.wfull[s], pol);
+                    ++wq;
+                }
+                if (ok && d.ob == 0) {
+                    atomicAdd(&m->total, d.NK);
+                    atomicAdd(&m->skipped, d.NK - nk);
+                    atomicAdd(&m->exec_rt, (unsigned long long)d.ntok * 64ull * (unsigned long long)nk);
+                    atomicAdd(&m->dense_rt, (unsigned long long)d.ntok * 64ull * (unsigned long long)d.NK);
+                }
             }
-            *nk_s = nk;
-            if (ob == 0) {
-                atomicAdd(&m->total, NK);
-                atomicAdd(&m->skipped, NK - nk);
-                atomicAdd(&m->exec_rt, (unsigned long long)ti.ntok * 64ull * (unsigned long long)nk);
-                atomicAdd(&m->dense_rt, (unsigned long long)ti.ntok * (unsigned long long)N);
-            }
-            for (int kk = 0; kk < kStages - 1 && kk < nk && ok; ++kk) ok = issue(kk);
+            drain_loads(br.wfull, kDnWD, wq);
         }
-        ok = __syncthreads_and(ok);
-        const int nk = *nk_s;
-        const uint32_t idesc = umma_idesc_f16_f32(128, nt16);
-        for (int kk = 0; kk < nk && ok; ++kk) {
-            const uint32_t q = it + kk;
-            const int s = q % kStages;
-            uint8_t* st = stage0 + s * DownSmem::kStage;
-            if (t == 0 && kk + kStages - 1 < nk) ok = issue(kk + kStages - 1);
-            ok = ok && mbar_wait(&ring.full[s], (q / kStages) & 1);
-            if (ok) {
-                // thread (output pair p, neuron quarter qn): neurons 16qn..16qn+15 of outputs 2p, 2p+1,
-                // written as K-major fp16 rows (one output per row) of the swizzled tile
-                const int p = t & 63, qn = t >> 6;
-                const uint8_t* cs = st + DownSmem::kA + DownSmem::kB;
-                const uint32_t* sbs = reinterpret_cast<const uint32_t*>(cs + DownSmem::kC);
+        __syncwarp();
+    } else if (warp == kWarpX) {
+        // ---- h of the tile's tokens (B operand), live tiles only
+        if (lane == 0) {
+            const uint64_t pol = policy_evict_last();
+            uint32_t xq = 0;
+            for (int u = blockIdx.x; u < U && ok; u += gridDim.x) {
+                const DownUnit d = down_unit(P, io, nb, words, dense, u);
+                const CUtensorMap* hmap = d.shared ? &tm.hsh[d.bi] : &tm.hr[d.bi];
+                for (uint64_t lm = d.live; lm && ok;) {
+                    const int j = pop_live(lm);
+                    if (!(ok = wait_free_sleep(br.xempty, kDnXD, xq, kProducerSleepNs))) break;
+                    const int x = xq % kDnXD;
+                    mbar_arrive_expect_tx(&br.xfull[x], (uint32_t)(64 << d.bi) * 128);
+                    tma_load_2d_hint(sX + x * kTileX, hmap, 64 * j, d.row0, &br.xfull[x], pol);
+                    ++xq;
+                }
+            }
+            drain_loads(br.xfull, kDnXD, xq);
+        }
+        __syncwarp();
+    } else if (warp == kWarpMma) {
+        if (lane == 0) {
+            uint32_t aq = 0, xq = 0, nu = 0;
+            for (int u = blockIdx.x; u < U && ok; u += gridDim.x, ++nu) {
+                const DownUnit d = down_unit(P, io, nb, words, dense, u);
+                const int acc = nu & 1;
+                if (!(ok = wait_free(br.tempty, 2, nu))) break;
+                tc_fence_after();
+                const uint32_t idesc = umma_idesc_f16_f32(128, d.nt16);
+                const uint32_t dt = tmem + (uint32_t)(acc * 128);
+                const int nk = __popcll(d.live);
+                for (int kk = 0; kk < nk; ++kk) {
+                    if (!(ok = wait_full(br.afull, kDnAD, aq) && wait_full(br.xfull, kDnXD, xq))) break;
+                    tc_fence_after();
+                    const int a = aq % kDnAD, x = xq % kDnXD;
+                    const uint64_t ad = umma_desc_sw128(smem_u32(sA + a * kTileA));
+                    const uint64_t bd = umma_desc_sw128(smem_u32(sX + x * kTileX));
+#pragma unroll
+                    for (int q = 0; q < 4; ++q) umma_f16(dt, ad + 2 * q, bd + 2 * q, idesc, (kk | q) != 0);
+                    umma_commit(&br.aempty[a]);
+                    umma_commit(&br.xempty[x]);
+                    ++aq;
+                    ++xq;
+                }
+                if (ok) umma_commit(&br.tfull[acc]);   // also when no tile was live
+            }
+            if (aq) wait_full(br.aempty, kDnAD, aq - 1);
+        }
+        __syncwarp();
+    } else if (warp >= kEpiWarps && warp < kWarpW) {
+        // ---- dequantise + transpose, group g taking the k-steps q with q % 2 == g: thread
+        // (output pair p, neuron quarter qn) writes neurons 16qn..16qn+15 of outputs 2p and 2p+1
+        // as K-major fp16 rows (one output per row).  The codes of neurons n, n+1 for output pair p
+        // are bytes n*64+p and (n+1)*64+p; their four nibbles become two fp16 pairs 1024 + c.
+        const int dw = warp - kEpiWarps, g = dw / kDqGroup;
+        const int dt = t - 32 * (kEpiWarps + g * kDqGroup), p = dt & 63, qn = dt >> 6;
+        const __half2 k1024 = __floats2half2_rn(1024.f, 1024.f);
+        uint32_t q = 0;
+        for (int u = blockIdx.x; u < U && ok; u += gridDim.x) {
+            const DownUnit d = down_unit(P, io, nb, words, dense, u);
+            const int nk = __popcll(d.live);
+            for (int kk = (int)((q & 1u) != (uint32_t)g); kk < nk; kk += 2) {
+                const uint32_t qk = q + kk;
+                ok = __all_sync(0xffffffffu, wait_full(br.wfull, kDnWD, qk) && wait_free(br.aempty, kDnAD, qk));
+                if (!ok) break;
+                const int s = qk % kDnWD;
+                const uint8_t* cs = sW + s * DownLayout::kWSlot;
+                const uint32_t* sbs = reinterpret_cast<const uint32_t*>(cs + DownLayout::kCodes);
                 const float2 sb0 = half2_to_float2(sbs[2 * p]), sb1 = half2_to_float2(sbs[2 * p + 1]);
+                const __half2 s0 = __floats2half2_rn(sb0.x, sb0.x), b0 = __floats2half2_rn(sb0.y, sb0.y);
+                const __half2 s1 = __floats2half2_rn(sb1.x * 0.0625f, sb1.x * 0.0625f);
+                const __half2 b1 = __floats2half2_rn(sb1.y, sb1.y);
                 uint32_t o0[8], o1[8];
 #pragma unroll
                 for (int i = 0; i < 8; ++i) {
                     const uint32_t ba = cs[(16 * qn + 2 * i) * 64 + p];
                     const uint32_t bb = cs[(16 * qn + 2 * i + 1) * 64 + p];
-                    const __half2 v0 = __floats2half2_rn(fmaf(sb0.x, (float)(ba & 15u), sb0.y),
-                                                         fmaf(sb0.x, (float)(bb & 15u), sb0.y));
-                    const __half2 v1 = __floats2half2_rn(fmaf(sb1.x, (float)(ba >> 4), sb1.y),
-                                                         fmaf(sb1.x, (float)(bb >> 4), sb1.y));
+                    const uint32_t pair = ba | (bb << 16);
+                    const uint32_t lo = (pair & 0x000F000Fu) | 0x64006400u;   // output 2p: (1024 + c, 1024 + c')
+                    const uint32_t hi = (pair & 0x00F000F0u) | 0x64006400u;   // output 2p+1: (1024 + 16c, ...)
+                    const __half2 v0 = __hfma2(__hsub2(*reinterpret_cast<const __half2*>(&lo), k1024), s0, b0);
+                    const __half2 v1 = __hfma2(__hsub2(*reinterpret_cast<const __half2*>(&hi), k1024), s1, b1);
                     o0[i] = *reinterpret_cast<const uint32_t*>(&v0);
                     o1[i] = *reinterpret_cast<const uint32_t*>(&v1);
                 }
-                uint8_t* A = st;
+                uint8_t* A = sA + (qk % kDnAD) * kTileA;
                 *reinterpret_cast<uint4*>(A + sw128_offset(2 * p, 2 * qn)) = make_uint4(o0[0], o0[1], o0[2], o0[3]);
                 *reinterpret_cast<uint4*>(A + sw128_offset(2 * p, 2 * qn + 1)) = make_uint4(o0[4], o0[5], o0[6], o0[7]);
                 *reinterpret_cast<uint4*>(A + sw128_offset(2 * p + 1, 2 * qn)) = make_uint4(o1[0], o1[1], o1[2], o1[3]);
                 *reinterpret_cast<uint4*>(A + sw128_offset(2 * p + 1, 2 * qn + 1)) =
                     make_uint4(o1[4], o1[5], o1[6], o1[7]);
+                fence_proxy_async_smem();
+                __syncwarp();
+                if (lane == 0) {
+                    mbar_arrive(&br.wempty[s]);
+                    mbar_arrive(&br.afull[qk % kDnAD]);
+                }
             }
-            fence_proxy_async_smem();
-            tc_fence_before();
-            ok = __syncthreads_and(ok);
-            if (t == 0 && ok) {
-                tc_fence_after();
-                const uint64_t ad = umma_desc_sw128(smem_u32(st));
-                const uint64_t bd = umma_desc_sw128(smem_u32(st + DownSmem::kA));
-#pragma unroll
-                for (int j = 0; j < 4; ++j) umma_f16(tmem, ad + 2 * j, bd + 2 * j, idesc, (kk | j) != 0);
-                umma_commit(&ring.done[s]);
-                ++ring.committed;
-            }
+            if (!ok) break;
+            q += nk;
         }
-        if (ok && nk > 0) {
-            const uint32_t ql = it + nk - 1;
-            ok = mbar_wait(&ring.done[ql % kStages], (ql / kStages) & 1);
-        }
-        ok = __syncthreads_and(ok);
-        tc_fence_after();
-        it += nk;
+    } else if (warp < kEpiWarps) {
         // ---- epilogue: router-weighted partial rows of the tile's tokens for this band
-        if (warp < 4 && ok) {
-            const int o = 128 * ob + 32 * warp + lane;
-            for (int c0 = 0; c0 < nt16; c0 += 16) {
+        uint32_t nu = 0;
+        for (int u = blockIdx.x; u < U && ok; u += gridDim.x, ++nu) {
+            const DownUnit d = down_unit(P, io, nb, words, dense, u);
+            const int acc = nu & 1;
+            const bool any = d.live != 0;
+            ok = __all_sync(0xffffffffu, wait_full_sleep(br.tfull, 2, nu, kEpilogueSleepNs));
+            if (!ok) break;
+            tc_fence_after();
+            const int o = 128 * d.ob + 32 * warp + lane;
+            for (int c0 = 0; c0 < d.nt16; c0 += 16) {
                 float v[16];
-                if (nk > 0) {
-                    tmem_ld16(tmem + ((uint32_t)(32 * warp) << 16) + (uint32_t)c0, v);
+                if (any) {
+                    tmem_ld16(tmem + ((uint32_t)(32 * warp) << 16) + (uint32_t)(acc * 128 + c0), v);
                 } else {
 #pragma unroll
                     for (int i = 0; i < 16; ++i) v[i] = 0.f;
@@ -598,20 +797,19 @@ prefill_down_kernel(const __grid_constant__ LayerParams P, const PrefillIO io, c
 #pragma unroll
                 for (int i = 0; i < 16; ++i) {
                     const int c = c0 + i;
-                    if (c < ti.ntok) {
-                        const int row = ti.row0 + c;  // grouped pair (routed) or token (shared)
-                        const float wgt = shared ? 1.f : io.pair_w[row];
-                        const size_t prow = shared ? (size_t)io.T * K + row : (size_t)row;
+                    if (c < d.ntok) {
+                        const int row = d.row0 + c;  // grouped pair (routed) or token (shared)
+                        const float wgt = d.shared ? 1.f : __ldg(io.pair_w + row);
+                        const size_t prow = d.shared ? (size_t)io.T * K + row : (size_t)row;
                         io.partial[prow * H + o] = wgt * v[i];
                     }
                 }
             }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&br.tempty[acc]);
         }
-        tc_fence_before();
-        __syncthreads();
-        tc_fence_after();
     }
-    if (t == 0) ring.drain();
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
@@ -794,16 +992,16 @@ extern "C" int hs_moe_prefill(const hs_moe_layer* L, const uint16_t* x, const fl
     const uint64_t rows_x = (uint64_t)T * K + (NS ? T : 0);
     bool okm = true;
     okm &= make_map(enc, &tm.up_codes_r, CU_TENSOR_MAP_DATA_TYPE_UINT8, L->routed[0].up.codes, H / 2, (uint64_t)E * NR,
-                    H / 2, 32, 128, CU_TENSOR_MAP_SWIZZLE_NONE);
+                    H / 2, hs::kUpK / 2, 128, CU_TENSOR_MAP_SWIZZLE_NONE);
     okm &= make_map(enc, &tm.dn_codes_r, CU_TENSOR_MAP_DATA_TYPE_UINT8, L->routed[0].down_nm.codes, H / 2,
                     (uint64_t)E * NR, H / 2, 64, 64, CU_TENSOR_MAP_SWIZZLE_NONE);
     if (NS) {
-        okm &= make_map(enc, &tm.up_codes_s, CU_TENSOR_MAP_DATA_TYPE_UINT8, L->shared->up.codes, H / 2, NS, H / 2, 32,
-                        128, CU_TENSOR_MAP_SWIZZLE_NONE);
+        okm &= make_map(enc, &tm.up_codes_s, CU_TENSOR_MAP_DATA_TYPE_UINT8, L->shared->up.codes, H / 2, NS, H / 2,
+                        hs::kUpK / 2, 128, CU_TENSOR_MAP_SWIZZLE_NONE);
         okm &= make_map(enc, &tm.dn_codes_s, CU_TENSOR_MAP_DATA_TYPE_UINT8, L->shared->down_nm.codes, H / 2, NS, H / 2,
                         64, 64, CU_TENSOR_MAP_SWIZZLE_NONE);
     }
-    for (int b = 0; b < 3; ++b) {
+    for (int b = 0; b < 2; ++b) {
         const uint32_t br = 64u << b;
         okm &= make_map(enc, &tm.xg[b], CU_TENSOR_MAP_DATA_TYPE_FLOAT16, io.xg, H, rows_x, (uint64_t)H * 2, 64, br,
                         CU_TENSOR_MAP_SWIZZLE_128B);
@@ -818,19 +1016,22 @@ extern "C" int hs_moe_prefill(const hs_moe_layer* L, const uint16_t* x, const fl
     int dev = 0, sms = 148;
     if (cudaGetDevice(&dev) != cudaSuccess) return HS_ERR_CUDA;
     if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return HS_ERR_CUDA;
-    const int up_smem = hs::UpSmem::total(H);
-    const int dn_smem = hs::DownSmem::total();
+    const int up_smem = hs::UpLayout::total(H);
+    const int dn_smem = hs::DownLayout::total();
     if (set_smem_attr((const void*)hs::prefill_up_kernel, up_smem) != HS_OK) return HS_ERR_CUDA;
     if (set_smem_attr((const void*)hs::prefill_down_kernel, dn_smem) != HS_OK) return HS_ERR_CUDA;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-    if (launch_pdl(hs::prefill_route_kernel, dim3((T + 7) / 8), dim3(256), 0, s, P, io) != cudaSuccess) return HS_ERR_CUDA;
-    if (launch_pdl(hs::prefill_count_kernel, dim3(E), dim3(256), 0, s, P, io) != cudaSuccess) return HS_ERR_CUDA;
+    if (cudaMemsetAsync(io.meta, 0, sizeof(hs::PrefillMeta), s) != cudaSuccess) return HS_ERR_CUDA;
+    // the first kernel follows the memset with ordinary stream ordering
+    hs::prefill_route_kernel<<<dim3((T + 7) / 8), dim3(256), 0, s>>>(P, io);
+    if (cudaGetLastError() != cudaSuccess) return HS_ERR_CUDA;
     if (launch_pdl(hs::prefill_tiles_kernel, dim3(1), dim3(256), 0, s, P, io) != cudaSuccess) return HS_ERR_CUDA;
-    if (launch_pdl(hs::prefill_list_kernel, dim3(E), dim3(256), 0, s, P, io) != cudaSuccess) return HS_ERR_CUDA;
-    if (launch_pdl(hs::prefill_gather_kernel, dim3(4 * sms), dim3(256), 0, s, P, io) != cudaSuccess) return HS_ERR_CUDA;
-    if (launch_pdl(hs::prefill_up_kernel, dim3(sms), dim3(256), up_smem, s, P, io, tm) != cudaSuccess)
+    if (launch_pdl(hs::prefill_list_kernel, dim3(E + (NS ? 2 * sms - E % sms : 0)), dim3(hs::kListThreads), 0, s, P, io) !=
+        cudaSuccess)
         return HS_ERR_CUDA;
-    if (launch_pdl(hs::prefill_down_kernel, dim3(sms), dim3(256), dn_smem, s, P, io, tm) != cudaSuccess)
+    if (launch_pdl(hs::prefill_up_kernel, dim3(sms), dim3(hs::kGemmThreads), up_smem, s, P, io, tm) != cudaSuccess)
+        return HS_ERR_CUDA;
+    if (launch_pdl(hs::prefill_down_kernel, dim3(sms), dim3(hs::kGemmThreads), dn_smem, s, P, io, tm) != cudaSuccess)
         return HS_ERR_CUDA;
     if (launch_pdl(hs::prefill_combine_kernel, dim3(4 * sms), dim3(256), 0, s, P, io) != cudaSuccess)
         return HS_ERR_CUDA;

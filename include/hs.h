@@ -198,7 +198,7 @@ int hs_moe_layer_decode(const hs_moe_layer* layer, const uint16_t* x_bf16_dev,
  * grouped by expert, and each expert runs its up projection, ReLU^2 and
  * down projection as matrix products on the tensor cores, the down product
  * reading the neuron-major copy directly.  A 64-neuron tile of the down
- * product is skipped for a tile of up to 256 of the expert's tokens when h is
+ * product is skipped for a tile of up to 128 of the expert's tokens when h is
  * zero for all of them (the skip does not change the result).
  *   x_bf16_dev   [tokens][hidden] bf16;  logits_dev [tokens][n_routed] fp32
  *   y_bf16_dev   [tokens][hidden] bf16, required;  y_f32_dev fp32 or NULL

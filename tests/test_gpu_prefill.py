@@ -25,7 +25,7 @@ from activation_sparse_moe_gb300.layer import DeviceLayer, from_synth_expert, fr
 
 pytestmark = pytest.mark.gpu
 
-TILE = 256   # tokens per token tile of the library's prefill
+TILE = 128   # tokens per token tile of the library's prefill
 
 
 @pytest.fixture(scope="module", autouse=True)
