@@ -34,6 +34,9 @@ constexpr int kNt = 128;          // max tokens per tile (MMA N)
 constexpr int kMaxTokens = 4096;
 constexpr int kMaxKTiles = 64;    // 64-neuron tiles per expert (neurons <= 4096): one 64-bit mask
 
+// Output band width of the down product: 192 when it divides the hidden size, else 128.
+__host__ __device__ inline int down_band(int H) { return H % 192 == 0 ? 192 : 128; }
+
 struct PrefillMeta {
     int n_tiles;                  // token tiles (routed experts first, then shared)
     int up_units, dn_units;
@@ -154,7 +157,7 @@ __global__ void __launch_bounds__(256) prefill_tiles_kernel(const __grid_constan
         m->n_tiles = nrt + nst;
         const int mr = (P.routed_neurons + 127) / 128, ms = (P.shared_neurons + 127) / 128;
         m->up_units = nrt * mr + nst * ms;
-        m->dn_units = (nrt + nst) * (P.hidden / 128);
+        m->dn_units = (nrt + nst) * (P.hidden / down_band(P.hidden));
     }
     // live flags: one word per (tile, 32 k-tiles)
     const int words = io.max_tiles * ((max(P.routed_neurons, P.shared_neurons) / 64 + 31) / 32);
@@ -230,7 +233,7 @@ __global__ void __launch_bounds__(kListThreads) prefill_list_kernel(const __grid
 
 struct TMaps {
     CUtensorMap up_codes_r, up_codes_s;      // [rows][H/2] bytes, box 64 x 128
-    CUtensorMap dn_codes_r, dn_codes_s;      // [rows][H/2] bytes, box 64 x 64
+    CUtensorMap dn_codes_r, dn_codes_s;      // [rows][H/2] bytes, box (band / 2) x 64
     CUtensorMap xg[2];                       // fp16 [rows][H], box 64 x {64, 128}, 128-byte swizzle
     CUtensorMap hr[2], hsh[2];               // fp16 h, box 64 x {64, 128}
 };
@@ -261,23 +264,24 @@ constexpr int kTileX = kNt * 128;       // up to 128 rows x 64 fp16
 constexpr unsigned kProducerSleepNs = 64;
 constexpr unsigned kEpilogueSleepNs = 256;
 
-// Ring depths: weight codes (WD), 16-bit operand (XD), dequantised tiles (AD).
-template <int WD, int XD, int AD>
+// Ring depths: weight codes (WD) and stages (SD).  A stage is one k-step's
+// 16-bit operand (loaded by TMA) together with its dequantised tile: its
+// "full" barrier completes when the TMA bytes have landed and the 8 warps of
+// the dequantising group have arrived; one MMA commit releases both.
+template <int WD, int SD>
 struct GemmBars {
-    uint64_t *wfull, *wempty, *xfull, *xempty, *afull, *aempty, *sbfull, *sbempty, *tfull, *tempty;
+    uint64_t *wfull, *wempty, *sfull, *sempty, *sbfull, *sbempty, *tfull, *tempty;
     uint32_t* tmem_slot;
-    static constexpr int kCount = 2 * WD + 2 * XD + 2 * AD + 2 * 2 + 2 * 2;
+    static constexpr int kCount = 2 * WD + 2 * SD + 2 * 2 + 2 * 2;
     __device__ GemmBars(uint8_t* p) {
         uint64_t* b = reinterpret_cast<uint64_t*>(p);
-        wfull = b; wempty = wfull + WD; xfull = wempty + WD; xempty = xfull + XD;
-        afull = xempty + XD; aempty = afull + AD; sbfull = aempty + AD; sbempty = sbfull + 2;
-        tfull = sbempty + 2; tempty = tfull + 2;
+        wfull = b; wempty = wfull + WD; sfull = wempty + WD; sempty = sfull + SD;
+        sbfull = sempty + SD; sbempty = sbfull + 2; tfull = sbempty + 2; tempty = tfull + 2;
         tmem_slot = reinterpret_cast<uint32_t*>(tempty + 2);
     }
     __device__ void init() {
         for (int i = 0; i < WD; ++i) { mbar_init(&wfull[i], 1); mbar_init(&wempty[i], kDqGroup); }
-        for (int i = 0; i < XD; ++i) { mbar_init(&xfull[i], 1); mbar_init(&xempty[i], 1); }
-        for (int i = 0; i < AD; ++i) { mbar_init(&afull[i], kDqGroup); mbar_init(&aempty[i], 1); }
+        for (int i = 0; i < SD; ++i) { mbar_init(&sfull[i], kDqGroup + 1); mbar_init(&sempty[i], 1); }
         for (int i = 0; i < 2; ++i) {
             mbar_init(&sbfull[i], 1); mbar_init(&sbempty[i], kDqWarps);
             mbar_init(&tfull[i], 1); mbar_init(&tempty[i], kEpiWarps);
@@ -308,14 +312,14 @@ __device__ __forceinline__ void drain_loads(uint64_t* full, int d, uint32_t issu
 // ---- up GEMM: unit = (token tile, 128-neuron block); D[neuron][token].  One k-step covers
 // 128 inputs (two scale groups).  TMEM: columns 0-255 the two accumulators, 256-511 four
 // dequantised A tiles (128 lanes x 64 columns = 128 rows x 128 fp16 each).
-constexpr int kUpWD = 5, kUpXD = 4, kUpAD = 4;
-using UpBars = GemmBars<kUpWD, kUpXD, kUpAD>;
+constexpr int kUpWD = 5, kUpSD = 4;
+using UpBars = GemmBars<kUpWD, kUpSD>;
 constexpr int kUpK = 128;                  // inputs per k-step
 
 struct UpLayout {
     static constexpr int kXSlot = 2 * kTileX;           // two 64-input swizzled sub-tiles
     static constexpr int kX = 0;
-    static constexpr int kW = kX + kUpXD * kXSlot;
+    static constexpr int kW = kX + kUpSD * kXSlot;
     static constexpr int kWSlot = 128 * kUpK / 2;       // 128 rows x 128 codes
     static constexpr int kSB = kW + kUpWD * kWSlot;
     __host__ __device__ static int sb_words(int H) { return 128 * (H / 64); }
@@ -413,22 +417,22 @@ prefill_up_kernel(const __grid_constant__ LayerParams P, const PrefillIO io, con
                 const UpUnit d = up_unit(P, io, ntr, mr, ms, u);
                 const uint32_t bytes = (uint32_t)(64 << d.bi) * 128;
                 for (int k = 0; k < KS; ++k) {
-                    if (!(ok = wait_free_sleep(br.xempty, kUpXD, xq, kProducerSleepNs))) break;
-                    const int x = xq % kUpXD;
+                    if (!(ok = wait_free_sleep(br.sempty, kUpSD, xq, kProducerSleepNs))) break;
+                    const int x = xq % kUpSD;
                     uint8_t* dst = sX + x * UpLayout::kXSlot;
-                    mbar_arrive_expect_tx(&br.xfull[x], 2 * bytes);
-                    tma_load_2d_hint(dst, &tm.xg[d.bi], kUpK * k, d.xrow, &br.xfull[x], pol);
-                    tma_load_2d_hint(dst + kTileX, &tm.xg[d.bi], kUpK * k + 64, d.xrow, &br.xfull[x], pol);
+                    mbar_arrive_expect_tx(&br.sfull[x], 2 * bytes);
+                    tma_load_2d_hint(dst, &tm.xg[d.bi], kUpK * k, d.xrow, &br.sfull[x], pol);
+                    tma_load_2d_hint(dst + kTileX, &tm.xg[d.bi], kUpK * k + 64, d.xrow, &br.sfull[x], pol);
                     ++xq;
                 }
             }
-            drain_loads(br.xfull, kUpXD, xq);
+            drain_loads(br.sfull, kUpSD, xq);
         }
         __syncwarp();
     } else if (warp == kWarpMma) {
         // ---- MMA issue: A (weights) from TMEM, B (tokens) from shared memory
         if (lane == 0) {
-            uint32_t aq = 0, xq = 0, nu = 0;
+            uint32_t sq = 0, nu = 0;
             for (int u = blockIdx.x; u < U && ok; u += gridDim.x, ++nu) {
                 const UpUnit d = up_unit(P, io, ntr, mr, ms, u);
                 const int acc = nu & 1;
@@ -437,24 +441,22 @@ prefill_up_kernel(const __grid_constant__ LayerParams P, const PrefillIO io, con
                 const uint32_t idesc = umma_idesc_f16_f32(128, d.nt16);
                 const uint32_t dt = tmem + (uint32_t)(acc * 128);
                 for (int k = 0; k < KS; ++k) {
-                    if (!(ok = wait_full(br.afull, kUpAD, aq) && wait_full(br.xfull, kUpXD, xq))) break;
+                    if (!(ok = wait_full(br.sfull, kUpSD, sq))) break;
                     tc_fence_after();
-                    const int a = aq % kUpAD, x = xq % kUpXD;
-                    const uint64_t bd0 = umma_desc_sw128(smem_u32(sX + x * UpLayout::kXSlot));
-                    const uint64_t bd1 = umma_desc_sw128(smem_u32(sX + x * UpLayout::kXSlot + kTileX));
+                    const int a = sq % kUpSD;
+                    const uint64_t bd0 = umma_desc_sw128(smem_u32(sX + a * UpLayout::kXSlot));
+                    const uint64_t bd1 = umma_desc_sw128(smem_u32(sX + a * UpLayout::kXSlot + kTileX));
 #pragma unroll
                     for (int j = 0; j < 8; ++j)
                         umma_f16_tmem_a(dt, tmem_a + 64 * a + 8 * j, (j < 4 ? bd0 : bd1) + 2 * (j & 3), idesc,
                                         (k | j) != 0);
-                    umma_commit(&br.aempty[a]);
-                    umma_commit(&br.xempty[x]);
-                    ++aq;
-                    ++xq;
+                    umma_commit(&br.sempty[a]);
+                    ++sq;
                 }
                 if (ok) umma_commit(&br.tfull[acc]);
             }
             // every MMA issued has completed once the last commit has arrived
-            if (aq) wait_full(br.aempty, kUpAD, aq - 1);
+            if (sq) wait_full(br.sempty, kUpSD, sq - 1);
         }
         __syncwarp();
     } else if (warp >= kEpiWarps && warp < kWarpW) {
@@ -474,7 +476,7 @@ prefill_up_kernel(const __grid_constant__ LayerParams P, const PrefillIO io, con
             const uint32_t* sbr = sSB + b * sbw + r * G + h;
             for (int k = (int)((q & 1u) != (uint32_t)g); k < KS; k += 2) {
                 const uint32_t qk = q + k;
-                ok = __all_sync(0xffffffffu, wait_full(br.wfull, kUpWD, qk) && wait_free(br.aempty, kUpAD, qk));
+                ok = __all_sync(0xffffffffu, wait_full(br.wfull, kUpWD, qk) && wait_free(br.sempty, kUpSD, qk));
                 if (!ok) break;
                 tc_fence_after();
                 const int s = qk % kUpWD;
@@ -505,13 +507,13 @@ prefill_up_kernel(const __grid_constant__ LayerParams P, const PrefillIO io, con
                     for (int i = 0; i < 32; ++i) o[i] = 0u;
                 }
                 __syncwarp();
-                tmem_st32(trow + 64 * (qk % kUpAD), o);
+                tmem_st32(trow + 64 * (qk % kUpSD), o);
                 tmem_st_wait();
                 tc_fence_before();
                 __syncwarp();
                 if (lane == 0) {
                     mbar_arrive(&br.wempty[s]);
-                    mbar_arrive(&br.afull[qk % kUpAD]);
+                    mbar_arrive(&br.sfull[qk % kUpSD]);
                 }
             }
             if (!ok) break;
@@ -567,24 +569,32 @@ prefill_up_kernel(const __grid_constant__ LayerParams P, const PrefillIO io, con
     if (warp == 0) tmem_dealloc(tmem, 512);
 }
 
-// ---- down GEMM: unit = (token tile, 128-output band); D[output][token] over the live 64-neuron tiles.
-// The dequantised tiles stay in shared memory (the transpose from neuron-major codes needs
-// every thread to write several rows).
-constexpr int kDnWD = 10, kDnXD = 7, kDnAD = 4;
-using DnBars = GemmBars<kDnWD, kDnXD, kDnAD>;
+// ---- down GEMM: unit = (token tile, band of BN outputs); D[token][output] over the live
+// 64-neuron tiles of the expert.  A = h of the tile's tokens (K-major, by TMA); B = the
+// neuron-major codes of one 64-neuron tile dequantised in place into an MN-major fp16 tile
+// (64 neurons x BN outputs: 128-byte rows of 64 outputs, 8-neuron x 64-output swizzle atoms),
+// so no transpose is needed.  Within each group of 8 outputs (one word of codes) the tile
+// holds the order o0 o4 o1 o5 o2 o6 o3 o7; the epilogue undoes it when it writes a row.
+constexpr int kDnWD = 6, kDnSD = 4;
+using DnBars = GemmBars<kDnWD, kDnSD>;
 
 struct DownLayout {
-    static constexpr int kA = 0;
-    static constexpr int kX = kA + kDnAD * kTileA;
-    static constexpr int kW = kX + kDnXD * kTileX;
-    static constexpr int kCodes = 64 * 64;                 // 64 neurons x 128 outputs
-    static constexpr int kWSlot = kCodes + 128 * 4;        // + (scale, bias) of 128 outputs
-    static constexpr int kBars = kW + kDnWD * kWSlot;
-    __host__ __device__ static int total() { return 1024 + kBars + 8 * DnBars::kCount + 64; }
+    int bn, sbo, tile_b, wslot, codes, x, w, bars, total;
+    __host__ __device__ explicit DownLayout(int BN) {
+        bn = BN;
+        sbo = (BN / 64) * 1024;                 // bytes between 8-neuron groups of the B tile
+        tile_b = 8 * sbo;                       // 64 neurons x BN outputs
+        codes = 64 * (BN / 2);                  // 64 neurons x BN/2 bytes
+        wslot = (codes + BN * 4 + 127) / 128 * 128;
+        x = kDnSD * tile_b;
+        w = x + kDnSD * kTileX;
+        bars = w + kDnWD * wslot;
+        total = 1024 + bars + 8 * DnBars::kCount + 64;
+    }
 };
 
 struct DownUnit {
-    int tile, ob, ntok, nt16, bi, cy0, NK, row0;
+    int tile, ob, ntok, cy0, NK, row0;
     bool shared;
     ExpertPtrs ep;
     uint64_t live;   // bit j: 64-neuron tile j is multiplied
@@ -600,8 +610,6 @@ __device__ __forceinline__ DownUnit down_unit(const LayerParams& P, const Prefil
     d.NK = (d.shared ? P.shared_neurons : P.routed_neurons) / 64;
     d.ep = d.shared ? P.shared : routed_ptrs(P, ti.e);
     d.ntok = ti.ntok;
-    d.nt16 = (ti.ntok + 15) & ~15;
-    d.bi = ti.ntok <= 64 ? 0 : 1;
     d.cy0 = d.shared ? 0 : ti.e * P.routed_neurons;
     d.row0 = ti.row0;
     const uint32_t* f = io.flag_r + (size_t)d.tile * words;
@@ -617,18 +625,32 @@ __device__ __forceinline__ int pop_live(uint64_t& m) {
     return j;
 }
 
+// Shared-memory descriptor of an MN-major operand in the 128-byte swizzle layout: leading
+// byte offset = 1024 (next 64-wide block along MN), stride byte offset = between 8-row groups
+// along K.
+__device__ __forceinline__ uint64_t umma_desc_sw128_mn(uint32_t smem_addr, uint32_t sbo) {
+    uint64_t d = 0;
+    d |= (uint64_t)((smem_addr & 0x3FFFFu) >> 4);
+    d |= (uint64_t)(1024u >> 4) << 16;
+    d |= (uint64_t)((sbo >> 4) & 0x3FFFu) << 32;
+    d |= (uint64_t)1u << 46;
+    d |= (uint64_t)2u << 61;
+    return d;
+}
+
 __global__ void __launch_bounds__(kGemmThreads, 1)
 prefill_down_kernel(const __grid_constant__ LayerParams P, const PrefillIO io, const __grid_constant__ TMaps tm) {
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    const int H = P.hidden;
-    uint8_t* sA = smem + DownLayout::kA;
-    uint8_t* sX = smem + DownLayout::kX;
-    uint8_t* sW = smem + DownLayout::kW;
-    DnBars br(smem + DownLayout::kBars);
+    const int H = P.hidden, BN = down_band(H);
+    const DownLayout lay(BN);
+    uint8_t* sB = smem;
+    uint8_t* sX = smem + lay.x;
+    uint8_t* sW = smem + lay.w;
+    DnBars br(smem + lay.bars);
     const int t = threadIdx.x, warp = t >> 5, lane = t & 31;
     if (t == 0) br.init();
-    if (warp == 0) tmem_alloc(br.tmem_slot, 256);
+    if (warp == 0) tmem_alloc(br.tmem_slot, 512);
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
@@ -637,7 +659,7 @@ prefill_down_kernel(const __grid_constant__ LayerParams P, const PrefillIO io, c
     pdl_trigger();
     PrefillMeta* m = io.meta;
     const int NR = P.routed_neurons, NS = P.shared_neurons, K = P.top_k;
-    const int nb = H / 128;
+    const int nb = H / BN;
     const int U = m->dn_units;
     const int words = (max(NR, NS) / 64 + 31) / 32;
     const bool dense = (io.flags & HS_FORCE_DENSE) != 0;
@@ -657,11 +679,10 @@ prefill_down_kernel(const __grid_constant__ LayerParams P, const PrefillIO io, c
                     const int j = pop_live(lm);
                     if (!(ok = wait_free_sleep(br.wempty, kDnWD, wq, kProducerSleepNs))) break;
                     const int s = wq % kDnWD;
-                    uint8_t* slot = sW + s * DownLayout::kWSlot;
-                    mbar_arrive_expect_tx(&br.wfull[s], DownLayout::kWSlot);
-                    tma_load_2d_hint(slot, cmap, 64 * d.ob, d.cy0 + 64 * j, &br.wfull[s], pol);
-                    bulk_g2s(slot + DownLayout::kCodes, d.ep.dn_sb + (size_t)j * H + 128 * d.ob, 128 * 4,
-                             &br.wfull[s], pol);
+                    uint8_t* slot = sW + s * lay.wslot;
+                    mbar_arrive_expect_tx(&br.wfull[s], (uint32_t)(lay.codes + BN * 4));
+                    tma_load_2d_hint(slot, cmap, (BN / 2) * d.ob, d.cy0 + 64 * j, &br.wfull[s], pol);
+                    bulk_g2s(slot + lay.codes, d.ep.dn_sb + (size_t)j * H + BN * d.ob, BN * 4, &br.wfull[s], pol);
                     ++wq;
                 }
                 if (ok && d.ob == 0) {
@@ -675,133 +696,143 @@ prefill_down_kernel(const __grid_constant__ LayerParams P, const PrefillIO io, c
         }
         __syncwarp();
     } else if (warp == kWarpX) {
-        // ---- h of the tile's tokens (B operand), live tiles only
+        // ---- h of the tile's tokens (A operand: 128 rows, the rows past the tile are ignored)
         if (lane == 0) {
             const uint64_t pol = policy_evict_last();
             uint32_t xq = 0;
             for (int u = blockIdx.x; u < U && ok; u += gridDim.x) {
                 const DownUnit d = down_unit(P, io, nb, words, dense, u);
-                const CUtensorMap* hmap = d.shared ? &tm.hsh[d.bi] : &tm.hr[d.bi];
+                const CUtensorMap* hmap = d.shared ? &tm.hsh[1] : &tm.hr[1];
                 for (uint64_t lm = d.live; lm && ok;) {
                     const int j = pop_live(lm);
-                    if (!(ok = wait_free_sleep(br.xempty, kDnXD, xq, kProducerSleepNs))) break;
-                    const int x = xq % kDnXD;
-                    mbar_arrive_expect_tx(&br.xfull[x], (uint32_t)(64 << d.bi) * 128);
-                    tma_load_2d_hint(sX + x * kTileX, hmap, 64 * j, d.row0, &br.xfull[x], pol);
+                    if (!(ok = wait_free_sleep(br.sempty, kDnSD, xq, kProducerSleepNs))) break;
+                    const int x = xq % kDnSD;
+                    mbar_arrive_expect_tx(&br.sfull[x], (uint32_t)kTileX);
+                    tma_load_2d_hint(sX + x * kTileX, hmap, 64 * j, d.row0, &br.sfull[x], pol);
                     ++xq;
                 }
             }
-            drain_loads(br.xfull, kDnXD, xq);
+            drain_loads(br.sfull, kDnSD, xq);
         }
         __syncwarp();
     } else if (warp == kWarpMma) {
         if (lane == 0) {
-            uint32_t aq = 0, xq = 0, nu = 0;
+            uint32_t sq = 0, nu = 0;
+            const uint32_t idesc = umma_idesc_f16_f32(128, BN) | (1u << 16);   // B is MN-major
             for (int u = blockIdx.x; u < U && ok; u += gridDim.x, ++nu) {
                 const DownUnit d = down_unit(P, io, nb, words, dense, u);
                 const int acc = nu & 1;
                 if (!(ok = wait_free(br.tempty, 2, nu))) break;
                 tc_fence_after();
-                const uint32_t idesc = umma_idesc_f16_f32(128, d.nt16);
-                const uint32_t dt = tmem + (uint32_t)(acc * 128);
+                const uint32_t dt = tmem + (uint32_t)(acc * 256);
                 const int nk = __popcll(d.live);
                 for (int kk = 0; kk < nk; ++kk) {
-                    if (!(ok = wait_full(br.afull, kDnAD, aq) && wait_full(br.xfull, kDnXD, xq))) break;
+                    if (!(ok = wait_full(br.sfull, kDnSD, sq))) break;
                     tc_fence_after();
-                    const int a = aq % kDnAD, x = xq % kDnXD;
-                    const uint64_t ad = umma_desc_sw128(smem_u32(sA + a * kTileA));
-                    const uint64_t bd = umma_desc_sw128(smem_u32(sX + x * kTileX));
+                    const int a = sq % kDnSD;
+                    const uint64_t ad = umma_desc_sw128(smem_u32(sX + a * kTileX));
+                    const uint32_t b0 = smem_u32(sB + a * lay.tile_b);
 #pragma unroll
-                    for (int q = 0; q < 4; ++q) umma_f16(dt, ad + 2 * q, bd + 2 * q, idesc, (kk | q) != 0);
-                    umma_commit(&br.aempty[a]);
-                    umma_commit(&br.xempty[x]);
-                    ++aq;
-                    ++xq;
+                    for (int q = 0; q < 4; ++q)
+                        umma_f16(dt, ad + 2 * q, umma_desc_sw128_mn(b0 + q * 2 * lay.sbo, lay.sbo), idesc,
+                                 (kk | q) != 0);
+                    umma_commit(&br.sempty[a]);
+                    ++sq;
                 }
                 if (ok) umma_commit(&br.tfull[acc]);   // also when no tile was live
             }
-            if (aq) wait_full(br.aempty, kDnAD, aq - 1);
+            if (sq) wait_full(br.sempty, kDnSD, sq - 1);
         }
         __syncwarp();
     } else if (warp >= kEpiWarps && warp < kWarpW) {
-        // ---- dequantise + transpose, group g taking the k-steps q with q % 2 == g: thread
-        // (output pair p, neuron quarter qn) writes neurons 16qn..16qn+15 of outputs 2p and 2p+1
-        // as K-major fp16 rows (one output per row).  The codes of neurons n, n+1 for output pair p
-        // are bytes n*64+p and (n+1)*64+p; their four nibbles become two fp16 pairs 1024 + c.
+        // ---- dequantise: group g takes the k-steps q with q % 2 == g.  Item (word w, neuron
+        // octet v): outputs 8w..8w+7 of neurons 8v..8v+7, one 16-byte chunk per neuron.
         const int dw = warp - kEpiWarps, g = dw / kDqGroup;
-        const int dt = t - 32 * (kEpiWarps + g * kDqGroup), p = dt & 63, qn = dt >> 6;
+        const int it = t - 32 * (kEpiWarps + g * kDqGroup);
+        const int nw = BN / 8, w = it % nw, v = it / nw;
+        const bool active = v < 8;
         const __half2 k1024 = __floats2half2_rn(1024.f, 1024.f);
+        const __half2 sixteenth = __floats2half2_rn(0.0625f, 0.0625f);
         uint32_t q = 0;
         for (int u = blockIdx.x; u < U && ok; u += gridDim.x) {
             const DownUnit d = down_unit(P, io, nb, words, dense, u);
             const int nk = __popcll(d.live);
             for (int kk = (int)((q & 1u) != (uint32_t)g); kk < nk; kk += 2) {
                 const uint32_t qk = q + kk;
-                ok = __all_sync(0xffffffffu, wait_full(br.wfull, kDnWD, qk) && wait_free(br.aempty, kDnAD, qk));
+                ok = __all_sync(0xffffffffu, wait_full(br.wfull, kDnWD, qk) && wait_free(br.sempty, kDnSD, qk));
                 if (!ok) break;
                 const int s = qk % kDnWD;
-                const uint8_t* cs = sW + s * DownLayout::kWSlot;
-                const uint32_t* sbs = reinterpret_cast<const uint32_t*>(cs + DownLayout::kCodes);
-                const float2 sb0 = half2_to_float2(sbs[2 * p]), sb1 = half2_to_float2(sbs[2 * p + 1]);
-                const __half2 s0 = __floats2half2_rn(sb0.x, sb0.x), b0 = __floats2half2_rn(sb0.y, sb0.y);
-                const __half2 s1 = __floats2half2_rn(sb1.x * 0.0625f, sb1.x * 0.0625f);
-                const __half2 b1 = __floats2half2_rn(sb1.y, sb1.y);
-                uint32_t o0[8], o1[8];
+                if (active) {
+                    const uint8_t* cs = sW + s * lay.wslot;
+                    const uint4* sbq = reinterpret_cast<const uint4*>(cs + lay.codes) + 2 * w;
+                    const uint4 sa = sbq[0], sb = sbq[1];                 // (s, b) of outputs 8w..8w+3, 8w+4..8w+7
+                    const uint32_t lo[4] = {sa.x, sa.y, sa.z, sa.w}, hi[4] = {sb.x, sb.y, sb.z, sb.w};
+                    __half2 sc[4], bi[4];
 #pragma unroll
-                for (int i = 0; i < 8; ++i) {
-                    const uint32_t ba = cs[(16 * qn + 2 * i) * 64 + p];
-                    const uint32_t bb = cs[(16 * qn + 2 * i + 1) * 64 + p];
-                    const uint32_t pair = ba | (bb << 16);
-                    const uint32_t lo = (pair & 0x000F000Fu) | 0x64006400u;   // output 2p: (1024 + c, 1024 + c')
-                    const uint32_t hi = (pair & 0x00F000F0u) | 0x64006400u;   // output 2p+1: (1024 + 16c, ...)
-                    const __half2 v0 = __hfma2(__hsub2(*reinterpret_cast<const __half2*>(&lo), k1024), s0, b0);
-                    const __half2 v1 = __hfma2(__hsub2(*reinterpret_cast<const __half2*>(&hi), k1024), s1, b1);
-                    o0[i] = *reinterpret_cast<const uint32_t*>(&v0);
-                    o1[i] = *reinterpret_cast<const uint32_t*>(&v1);
+                    for (int p = 0; p < 4; ++p) {
+                        // pair p holds outputs (p, p+4); odd p arrive as 16 * code
+                        const uint32_t s2 = __byte_perm(lo[p], hi[p], 0x5410), b2 = __byte_perm(lo[p], hi[p], 0x7632);
+                        sc[p] = *reinterpret_cast<const __half2*>(&s2);
+                        if (p & 1) sc[p] = __hmul2(sc[p], sixteenth);
+                        bi[p] = *reinterpret_cast<const __half2*>(&b2);
+                    }
+                    uint8_t* B = sB + (qk % kDnSD) * lay.tile_b + (w >> 3) * 1024;
+#pragma unroll
+                    for (int i = 0; i < 8; ++i) {
+                        const int k = 8 * v + i;
+                        const uint32_t W = *reinterpret_cast<const uint32_t*>(cs + k * (BN / 2) + 4 * w);
+                        const uint32_t lw = W, hw = W >> 8;
+                        const uint32_t pr[4] = {(lw & 0x000F000Fu) | 0x64006400u, (lw & 0x00F000F0u) | 0x64006400u,
+                                                (hw & 0x000F000Fu) | 0x64006400u, (hw & 0x00F000F0u) | 0x64006400u};
+                        uint32_t o[4];
+#pragma unroll
+                        for (int p = 0; p < 4; ++p) {
+                            const __half2 r = __hfma2(__hsub2(*reinterpret_cast<const __half2*>(&pr[p]), k1024), sc[p], bi[p]);
+                            o[p] = *reinterpret_cast<const uint32_t*>(&r);
+                        }
+                        *reinterpret_cast<uint4*>(B + (k >> 3) * lay.sbo + (k & 7) * 128 + (((w & 7) ^ (k & 7)) << 4)) =
+                            make_uint4(o[0], o[1], o[2], o[3]);
+                    }
                 }
-                uint8_t* A = sA + (qk % kDnAD) * kTileA;
-                *reinterpret_cast<uint4*>(A + sw128_offset(2 * p, 2 * qn)) = make_uint4(o0[0], o0[1], o0[2], o0[3]);
-                *reinterpret_cast<uint4*>(A + sw128_offset(2 * p, 2 * qn + 1)) = make_uint4(o0[4], o0[5], o0[6], o0[7]);
-                *reinterpret_cast<uint4*>(A + sw128_offset(2 * p + 1, 2 * qn)) = make_uint4(o1[0], o1[1], o1[2], o1[3]);
-                *reinterpret_cast<uint4*>(A + sw128_offset(2 * p + 1, 2 * qn + 1)) =
-                    make_uint4(o1[4], o1[5], o1[6], o1[7]);
                 fence_proxy_async_smem();
                 __syncwarp();
                 if (lane == 0) {
                     mbar_arrive(&br.wempty[s]);
-                    mbar_arrive(&br.afull[qk % kDnAD]);
+                    mbar_arrive(&br.sfull[qk % kDnSD]);
                 }
             }
             if (!ok) break;
             q += nk;
         }
     } else if (warp < kEpiWarps) {
-        // ---- epilogue: router-weighted partial rows of the tile's tokens for this band
+        // ---- epilogue: thread = token row of the tile; router-weighted partial row for this band
         uint32_t nu = 0;
         for (int u = blockIdx.x; u < U && ok; u += gridDim.x, ++nu) {
             const DownUnit d = down_unit(P, io, nb, words, dense, u);
             const int acc = nu & 1;
-            const bool any = d.live != 0;
+            const int c = 32 * warp + lane;               // row of the tile
+            const bool rowok = c < d.ntok;
+            const int row = d.row0 + c;
+            const float wgt = (rowok && !d.shared) ? __ldg(io.pair_w + row) : 1.f;
+            float* prow = io.partial + (d.shared ? (size_t)io.T * K + row : (size_t)row) * H + BN * d.ob;
             ok = __all_sync(0xffffffffu, wait_full_sleep(br.tfull, 2, nu, kEpilogueSleepNs));
             if (!ok) break;
             tc_fence_after();
-            const int o = 128 * d.ob + 32 * warp + lane;
-            for (int c0 = 0; c0 < d.nt16; c0 += 16) {
-                float v[16];
-                if (any) {
-                    tmem_ld16(tmem + ((uint32_t)(32 * warp) << 16) + (uint32_t)(acc * 128 + c0), v);
+            for (int c0 = 0; c0 < BN; c0 += 32) {
+                float v[32];
+                if (d.live) {
+                    tmem_ld32(tmem + ((uint32_t)(32 * warp) << 16) + (uint32_t)(acc * 256 + c0), v);
                 } else {
 #pragma unroll
-                    for (int i = 0; i < 16; ++i) v[i] = 0.f;
+                    for (int i = 0; i < 32; ++i) v[i] = 0.f;
                 }
+                if (rowok) {
 #pragma unroll
-                for (int i = 0; i < 16; ++i) {
-                    const int c = c0 + i;
-                    if (c < d.ntok) {
-                        const int row = d.row0 + c;  // grouped pair (routed) or token (shared)
-                        const float wgt = d.shared ? 1.f : __ldg(io.pair_w + row);
-                        const size_t prow = d.shared ? (size_t)io.T * K + row : (size_t)row;
-                        io.partial[prow * H + o] = wgt * v[i];
+                    for (int g8 = 0; g8 < 4; ++g8) {
+                        const float* e = v + 8 * g8;   // o0 o4 o1 o5 o2 o6 o3 o7
+                        float4* dst = reinterpret_cast<float4*>(prow + c0 + 8 * g8);
+                        dst[0] = make_float4(wgt * e[0], wgt * e[2], wgt * e[4], wgt * e[6]);
+                        dst[1] = make_float4(wgt * e[1], wgt * e[3], wgt * e[5], wgt * e[7]);
                     }
                 }
             }
@@ -813,7 +844,7 @@ prefill_down_kernel(const __grid_constant__ LayerParams P, const PrefillIO io, c
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
-    if (warp == 0) tmem_dealloc(tmem, 256);
+    if (warp == 0) tmem_dealloc(tmem, 512);
 }
 
 // y[t] = shared partial + sum over slots j of the pair partials, in order; bf16 RNE.
@@ -993,13 +1024,14 @@ extern "C" int hs_moe_prefill(const hs_moe_layer* L, const uint16_t* x, const fl
     bool okm = true;
     okm &= make_map(enc, &tm.up_codes_r, CU_TENSOR_MAP_DATA_TYPE_UINT8, L->routed[0].up.codes, H / 2, (uint64_t)E * NR,
                     H / 2, hs::kUpK / 2, 128, CU_TENSOR_MAP_SWIZZLE_NONE);
+    const int BN = hs::down_band(H);
     okm &= make_map(enc, &tm.dn_codes_r, CU_TENSOR_MAP_DATA_TYPE_UINT8, L->routed[0].down_nm.codes, H / 2,
-                    (uint64_t)E * NR, H / 2, 64, 64, CU_TENSOR_MAP_SWIZZLE_NONE);
+                    (uint64_t)E * NR, H / 2, BN / 2, 64, CU_TENSOR_MAP_SWIZZLE_NONE);
     if (NS) {
         okm &= make_map(enc, &tm.up_codes_s, CU_TENSOR_MAP_DATA_TYPE_UINT8, L->shared->up.codes, H / 2, NS, H / 2,
                         hs::kUpK / 2, 128, CU_TENSOR_MAP_SWIZZLE_NONE);
         okm &= make_map(enc, &tm.dn_codes_s, CU_TENSOR_MAP_DATA_TYPE_UINT8, L->shared->down_nm.codes, H / 2, NS, H / 2,
-                        64, 64, CU_TENSOR_MAP_SWIZZLE_NONE);
+                        BN / 2, 64, CU_TENSOR_MAP_SWIZZLE_NONE);
     }
     for (int b = 0; b < 2; ++b) {
         const uint32_t br = 64u << b;
@@ -1017,7 +1049,7 @@ extern "C" int hs_moe_prefill(const hs_moe_layer* L, const uint16_t* x, const fl
     if (cudaGetDevice(&dev) != cudaSuccess) return HS_ERR_CUDA;
     if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return HS_ERR_CUDA;
     const int up_smem = hs::UpLayout::total(H);
-    const int dn_smem = hs::DownLayout::total();
+    const int dn_smem = hs::DownLayout(hs::down_band(H)).total;
     if (set_smem_attr((const void*)hs::prefill_up_kernel, up_smem) != HS_OK) return HS_ERR_CUDA;
     if (set_smem_attr((const void*)hs::prefill_down_kernel, dn_smem) != HS_OK) return HS_ERR_CUDA;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
