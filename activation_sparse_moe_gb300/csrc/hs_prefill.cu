@@ -232,9 +232,9 @@ __global__ void __launch_bounds__(kListThreads) prefill_list_kernel(const __grid
 }
 
 struct TMaps {
-    CUtensorMap up_codes_r, up_codes_s;      // [rows][H/2] bytes, box 64 x 128
+    CUtensorMap up_codes_r, up_codes_s;      // [rows][H/2] bytes, box 64 x 128, 64-byte swizzle
     CUtensorMap dn_codes_r, dn_codes_s;      // [rows][H/2] bytes, box (band / 2) x 64
-    CUtensorMap xg[2];                       // fp16 [rows][H], box 64 x {64, 128}, 128-byte swizzle
+    CUtensorMap xg[8];                       // fp16 [rows][H], box 64 x 16(i+1), 128-byte swizzle
     CUtensorMap hr[2], hsh[2];               // fp16 h, box 64 x {64, 128}
 };
 
@@ -328,7 +328,7 @@ struct UpLayout {
 };
 
 struct UpUnit {
-    int tile, row0, rows, ntok, nt16, bi, cy, xrow, N, row_out;
+    int tile, row0, rows, ntok, nt16, cy, xrow, N, row_out;
     bool shared;
     ExpertPtrs ep;
 };
@@ -346,7 +346,6 @@ __device__ __forceinline__ UpUnit up_unit(const LayerParams& P, const PrefillIO&
     d.rows = min(128, d.N - d.row0);
     d.ntok = ti.ntok;
     d.nt16 = (ti.ntok + 15) & ~15;
-    d.bi = ti.ntok <= 64 ? 0 : 1;
     d.cy = d.shared ? d.row0 : ti.e * P.routed_neurons + d.row0;
     d.xrow = d.shared ? io.T * P.top_k + ti.row0 : ti.row0;
     d.row_out = ti.row0;
@@ -415,14 +414,16 @@ prefill_up_kernel(const __grid_constant__ LayerParams P, const PrefillIO io, con
             uint32_t xq = 0;
             for (int u = blockIdx.x; u < U && ok; u += gridDim.x) {
                 const UpUnit d = up_unit(P, io, ntr, mr, ms, u);
-                const uint32_t bytes = (uint32_t)(64 << d.bi) * 128;
+                // a box of exactly the tile's rows rounded up to 16 (the MMA's N)
+                const CUtensorMap* xmap = &tm.xg[d.nt16 / 16 - 1];
+                const uint32_t bytes = (uint32_t)d.nt16 * 128;
                 for (int k = 0; k < KS; ++k) {
                     if (!(ok = wait_free_sleep(br.sempty, kUpSD, xq, kProducerSleepNs))) break;
                     const int x = xq % kUpSD;
                     uint8_t* dst = sX + x * UpLayout::kXSlot;
                     mbar_arrive_expect_tx(&br.sfull[x], 2 * bytes);
-                    tma_load_2d_hint(dst, &tm.xg[d.bi], kUpK * k, d.xrow, &br.sfull[x], pol);
-                    tma_load_2d_hint(dst + kTileX, &tm.xg[d.bi], kUpK * k + 64, d.xrow, &br.sfull[x], pol);
+                    tma_load_2d_hint(dst, xmap, kUpK * k, d.xrow, &br.sfull[x], pol);
+                    tma_load_2d_hint(dst + kTileX, xmap, kUpK * k + 64, d.xrow, &br.sfull[x], pol);
                     ++xq;
                 }
             }
@@ -482,8 +483,12 @@ prefill_up_kernel(const __grid_constant__ LayerParams P, const PrefillIO io, con
                 const int s = qk % kUpWD;
                 uint32_t o[32];
                 if (r < d.rows) {
-                    const uint4* cp = reinterpret_cast<const uint4*>(sW + s * UpLayout::kWSlot + r * (kUpK / 2) + 32 * h);
-                    const uint4 c0 = cp[0], c1 = cp[1];
+                    // the codes tile arrives with the 64-byte swizzle: 16-byte chunk c of row r sits at
+                    // chunk c ^ ((r >> 1) & 3), so the 32 rows a warp reads cover all banks
+                    const uint8_t* crow = sW + s * UpLayout::kWSlot + r * (kUpK / 2);
+                    const int sw = (r >> 1) & 3;
+                    const uint4 c0 = *reinterpret_cast<const uint4*>(crow + (((2 * h) ^ sw) << 4));
+                    const uint4 c1 = *reinterpret_cast<const uint4*>(crow + (((2 * h + 1) ^ sw) << 4));
                     const float2 sbv = half2_to_float2(sbr[2 * k]);
                     const __half2 s1 = __floats2half2_rn(sbv.x, sbv.x);
                     const __half2 s16 = __floats2half2_rn(sbv.x * 0.0625f, sbv.x * 0.0625f);
@@ -1023,20 +1028,21 @@ extern "C" int hs_moe_prefill(const hs_moe_layer* L, const uint16_t* x, const fl
     const uint64_t rows_x = (uint64_t)T * K + (NS ? T : 0);
     bool okm = true;
     okm &= make_map(enc, &tm.up_codes_r, CU_TENSOR_MAP_DATA_TYPE_UINT8, L->routed[0].up.codes, H / 2, (uint64_t)E * NR,
-                    H / 2, hs::kUpK / 2, 128, CU_TENSOR_MAP_SWIZZLE_NONE);
+                    H / 2, hs::kUpK / 2, 128, CU_TENSOR_MAP_SWIZZLE_64B);
     const int BN = hs::down_band(H);
     okm &= make_map(enc, &tm.dn_codes_r, CU_TENSOR_MAP_DATA_TYPE_UINT8, L->routed[0].down_nm.codes, H / 2,
                     (uint64_t)E * NR, H / 2, BN / 2, 64, CU_TENSOR_MAP_SWIZZLE_NONE);
     if (NS) {
         okm &= make_map(enc, &tm.up_codes_s, CU_TENSOR_MAP_DATA_TYPE_UINT8, L->shared->up.codes, H / 2, NS, H / 2,
-                        hs::kUpK / 2, 128, CU_TENSOR_MAP_SWIZZLE_NONE);
+                        hs::kUpK / 2, 128, CU_TENSOR_MAP_SWIZZLE_64B);
         okm &= make_map(enc, &tm.dn_codes_s, CU_TENSOR_MAP_DATA_TYPE_UINT8, L->shared->down_nm.codes, H / 2, NS, H / 2,
                         BN / 2, 64, CU_TENSOR_MAP_SWIZZLE_NONE);
     }
+    for (int b = 0; b < 8; ++b)
+        okm &= make_map(enc, &tm.xg[b], CU_TENSOR_MAP_DATA_TYPE_FLOAT16, io.xg, H, rows_x, (uint64_t)H * 2, 64,
+                        16u * (b + 1), CU_TENSOR_MAP_SWIZZLE_128B);
     for (int b = 0; b < 2; ++b) {
         const uint32_t br = 64u << b;
-        okm &= make_map(enc, &tm.xg[b], CU_TENSOR_MAP_DATA_TYPE_FLOAT16, io.xg, H, rows_x, (uint64_t)H * 2, 64, br,
-                        CU_TENSOR_MAP_SWIZZLE_128B);
         okm &= make_map(enc, &tm.hr[b], CU_TENSOR_MAP_DATA_TYPE_FLOAT16, io.h_r, NR, (uint64_t)T * K, (uint64_t)NR * 2,
                         64, br, CU_TENSOR_MAP_SWIZZLE_128B);
         if (NS)
