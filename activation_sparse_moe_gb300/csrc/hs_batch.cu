@@ -9,17 +9,23 @@
 // live rows once (the verify step of section "Speculative decoding." reads
 // three rows' activations through the same weights this way).
 //
-// Kernels (one stream, programmatic dependent launch between them):
-//  1. route:  top-k + softmax per token, counting sort of (token, slot) pairs
-//             by expert (tokens ascending), work-unit tables, zeroed masks.
-//  2. up:     persistent CTAs over units (expert, 32 neuron rows, <= 4 tokens):
-//             bulk copies of the rows, DP4A fixed-point GEMV per token, ReLU^2,
-//             h to global, union live bits OR-ed into a per-(expert, 32 rows)
-//             mask word.
-//  3. down:   persistent CTAs over units (expert, 128-output band): the union
-//             live rows' band slices, dequantised once per row, times each
-//             token's h; one partial row per (token, slot).
-//  4. reduce: y[t] = shared + sum_j (partial of slot j) in slot order; bf16.
+// Kernels (one stream; the meta block is zeroed first, then programmatic
+// dependent launch between the kernels):
+//  1. route:  one CTA per token: top-k + softmax (warp 0), per-expert pair
+//             counts (integer atomics), and the token's fixed-point x table
+//             for the integer-pipe GEMV (all threads).
+//  2. plan:   one CTA: pair offsets, (token, slot) pairs grouped by expert in
+//             token order, work-unit tables, zeroed union masks.
+//  3. up:     persistent CTAs over units (expert, 32 neuron rows, <= 4 tokens),
+//             the next unit's bulk copies in flight while the current one is
+//             computed: DP4A fixed-point GEMV per token, ReLU^2, h to global,
+//             union live bits OR-ed into a per-(expert, 32 rows) mask word.
+//  4. down:   persistent CTAs over units (expert or shared-expert row chunk,
+//             128-output band): the union live rows' band slices (and the
+//             scale slabs of their groups) staged by asynchronous copies, two
+//             passes in flight; each live row's weights dequantised once and
+//             multiplied by every token's h; one partial row per (token, slot).
+//  5. reduce: y[t] = sum of the token's partial rows in slot order; bf16.
 #include "hs_host.h"
 
 namespace hs {
@@ -27,9 +33,15 @@ namespace hs {
 constexpr int kTC = 4;          // tokens per up unit
 constexpr int kMaxBatch = 64;
 constexpr int kBand = 128;      // outputs per down unit
+constexpr int kMaxShChunks = 8; // shared-expert row chunks in the down pass
+
+// Row chunks of the shared expert's down product: the shared expert has every
+// token of the batch, so its work is split into ranges of rows.
+__host__ __device__ inline int shared_chunks(int B) { return min(kMaxShChunks, (B + 7) / 8); }
 
 struct BatchMeta {
-    int n_pairs, n_touched, up_units, dn_units;
+    int cnt[kMaxRouted];            // pairs per expert (route kernel, atomics)
+    int n_pairs, n_touched, up_units, dn_units, n_items;
     int touched[kMaxRouted];        // routed experts with tokens, ascending
     int e_off[kMaxRouted + 1];      // grouped pair offsets per expert id
     int up_off[kMaxRouted + 2];     // up unit offsets per touched index (+ shared)
@@ -48,11 +60,13 @@ struct BatchIO {
     int* pair_tok;          // [B*K] grouped by expert
     float* pair_w;
     int* pair_slot;         // 1..K
+    uint8_t* xt;            // [B][G][kXfStride] fixed-point x tables
+    float* xsc;             // [B][G][2] (scale, sum) per group
     float* h_pair;          // [B*K][NR] by grouped pair index
     float* h_sh;            // [B][NS]
     uint32_t* mask_r;       // [E][NR/32]
     uint32_t* mask_s;       // [NS/32]
-    float* partial;         // [B][K+1][H]
+    float* partial;         // [B][S][H], S = shared chunks + K slots
     uint16_t* y_bf16;
     float* y_f32;
     int* dbg_topk_idx;
@@ -63,49 +77,87 @@ struct BatchIO {
 
 // ------------------------------------------------------------------ route
 __global__ void __launch_bounds__(256) batch_route_kernel(const __grid_constant__ LayerParams P, const BatchIO io) {
-    __shared__ int s_idx[kMaxBatch * kMaxTopK];
-    __shared__ float s_w[kMaxBatch * kMaxTopK];
-    __shared__ int s_cnt[kMaxRouted];
-    __shared__ int s_off[kMaxRouted + 1];
+    __shared__ __align__(16) int s_idx[kMaxTopK];
+    __shared__ __align__(16) float s_w[kMaxTopK];
     pdl_wait();
     pdl_trigger();
-    const int t = threadIdx.x, warp = t >> 5;
-    const int B = io.batch, K = P.top_k, E = P.n_routed;
-    for (int b = warp; b < B; b += 8) warp_topk_softmax(io.logits + (size_t)b * E, E, K, s_idx + b * K, s_w + b * K);
-    if (t < kMaxRouted) s_cnt[t] = 0;
-    __syncthreads();
-    const int npair = B * K;
-    for (int p = t; p < npair; p += blockDim.x) {
-        atomicAdd(&s_cnt[s_idx[p]], 1);
-        io.topk_idx[p] = s_idx[p];
-        io.topk_w[p] = s_w[p];
-        if (io.dbg_topk_idx) { io.dbg_topk_idx[p] = s_idx[p]; io.dbg_topk_w[p] = s_w[p]; }
-    }
-    __syncthreads();
-    BatchMeta* m = io.meta;
-    if (t == 0) {
-        int acc = 0, nt = 0, units = 0;
-        const int HGr = P.routed_neurons / 32;
-        for (int e = 0; e < E; ++e) {
-            s_off[e] = acc;
-            m->e_off[e] = acc;
-            acc += s_cnt[e];
-            if (s_cnt[e]) {
-                m->touched[nt] = e;
-                m->up_off[nt] = units;
-                units += ((s_cnt[e] + kTC - 1) / kTC) * HGr;
-                ++nt;
-            }
+    const int b = blockIdx.x, t = threadIdx.x;
+    const int K = P.top_k, E = P.n_routed, H = P.hidden, G = H / 64;
+    if (t < 32) {
+        warp_topk_softmax(io.logits + (size_t)b * E, E, K, s_idx, s_w);
+        __syncwarp();
+        if (t < K) {
+            const int p = b * K + t;
+            io.topk_idx[p] = s_idx[t];
+            io.topk_w[p] = s_w[t];
+            atomicAdd(&io.meta->cnt[s_idx[t]], 1);
+            if (io.dbg_topk_idx) { io.dbg_topk_idx[p] = s_idx[t]; io.dbg_topk_w[p] = s_w[t]; }
         }
-        s_off[E] = acc;
-        m->e_off[E] = acc;
-        m->up_off[nt] = units;
-        if (P.shared_neurons) units += ((B + kTC - 1) / kTC) * (P.shared_neurons / 32);
-        m->up_off[nt + 1] = units;
+    }
+    // the token's fixed-point x table (read by every up unit that has this token)
+    convert_x_fixed(io.x + (size_t)b * H, G, io.xt + (size_t)b * G * kXfStride, io.xsc + (size_t)b * G * 2, 0);
+}
+
+// ------------------------------------------------------------------ plan
+// Inclusive sum over the threads of a CTA of at most 32 warps; `tmp` holds 32 ints.
+__device__ __forceinline__ int block_incl_sum(int v, int* tmp) {
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+        const int o = __shfl_up_sync(0xffffffffu, v, off);
+        if (lane >= off) v += o;
+    }
+    if (lane == 31) tmp[warp] = v;
+    __syncthreads();
+    int before = 0;
+    for (int i = 0; i < warp && i < nw; ++i) before += tmp[i];
+    __syncthreads();
+    return v + before;
+}
+
+__global__ void __launch_bounds__(512) batch_plan_kernel(const __grid_constant__ LayerParams P, const BatchIO io) {
+    __shared__ int s_idx[kMaxBatch * kMaxTopK];
+    __shared__ int s_off[kMaxRouted + 1];
+    __shared__ int tmp[32];
+    __shared__ int tot[3];
+    pdl_wait();
+    pdl_trigger();
+    const int t = threadIdx.x;
+    const int B = io.batch, K = P.top_k, E = P.n_routed;
+    const int npair = B * K;
+    BatchMeta* m = io.meta;
+    for (int p = t; p < npair; p += blockDim.x) s_idx[p] = io.topk_idx[p];
+    // offsets, touched experts and unit offsets: block scans over the experts (thread e)
+    const int HGr = P.routed_neurons / 32;
+    const int c = t < E ? __ldcg(&m->cnt[t]) : 0;
+    const int touched = c > 0 ? 1 : 0;
+    const int units = ((c + kTC - 1) / kTC) * HGr;
+    const int c_in = block_incl_sum(c, tmp);
+    const int t_in = block_incl_sum(touched, tmp);
+    const int u_in = block_incl_sum(units, tmp);
+    if (t < E) {
+        s_off[t] = c_in - c;
+        m->e_off[t] = c_in - c;
+        if (touched) {
+            m->touched[t_in - 1] = t;
+            m->up_off[t_in - 1] = u_in - units;
+        }
+    }
+    if (t == E - 1) { tot[0] = c_in; tot[1] = t_in; tot[2] = u_in; }
+    __syncthreads();
+    if (t == 0) {
+        const int nt = tot[1];
+        int un = tot[2];
+        s_off[E] = tot[0];
+        m->e_off[E] = tot[0];
+        m->up_off[nt] = un;
+        if (P.shared_neurons) un += ((B + kTC - 1) / kTC) * (P.shared_neurons / 32);
+        m->up_off[nt + 1] = un;
         m->n_pairs = npair;
         m->n_touched = nt;
-        m->up_units = units;
-        m->dn_units = (nt + (P.shared_neurons ? 1 : 0)) * (P.hidden / kBand);
+        m->up_units = un;
+        m->n_items = nt + (P.shared_neurons ? shared_chunks(B) : 0);
+        m->dn_units = m->n_items * (P.hidden / kBand);
     }
     __syncthreads();
     // place pairs: tokens ascending within an expert (pair order is token-major)
@@ -115,7 +167,7 @@ __global__ void __launch_bounds__(256) batch_route_kernel(const __grid_constant_
         for (int q = 0; q < p; ++q) rank += (s_idx[q] == e);
         const int pos = s_off[e] + rank;
         io.pair_tok[pos] = p / K;
-        io.pair_w[pos] = s_w[p];
+        io.pair_w[pos] = io.topk_w[p];
         io.pair_slot[pos] = p % K + 1;
     }
     // clear the union masks
@@ -125,20 +177,40 @@ __global__ void __launch_bounds__(256) batch_route_kernel(const __grid_constant_
 }
 
 // ------------------------------------------------------------------ up
+// Double-buffered unit stage: 32 rows of codes and (scale, bias) pairs, the
+// x tables of up to kTC tokens, and the offsets of the rows.
 struct BatchUpSmem {
     __host__ __device__ static int codes(int H) { return 32 * (H / 2); }
     __host__ __device__ static int sb(int H) { return 32 * (H / 64) * 4; }
     __host__ __device__ static int xf(int H) { return kTC * (H / 64) * kXfStride; }
     __host__ __device__ static int xs(int H) { return kTC * (H / 64) * 8; }
+    __host__ __device__ static int stage(int H) { return codes(H) + sb(H) + xf(H) + xs(H) + 128; }
     // parts row stride: 1 mod 32 words, so row-sum loads (lane = row) are conflict-free
     __host__ __device__ static int pstride(int H) { return ((H / 64 + 31) / 32) * 32 + 1; }
-    // x staging (bf16) and the dot-product parts share one region
-    __host__ __device__ static int stage(int H) {
-        const int a = kTC * H * 2, b = kTC * 32 * pstride(H) * 4;
-        return a > b ? a : b;
-    }
-    __host__ __device__ static int total(int H) { return codes(H) + sb(H) + xf(H) + xs(H) + stage(H) + 256 + 128; }
+    __host__ __device__ static int parts(int H) { return kTC * 32 * pstride(H) * 4; }
+    __host__ __device__ static int total(int H);
 };
+
+struct UpUnitDesc {
+    bool shared;
+    int e, c, hg, T, pbase, N, HG;
+    ExpertPtrs ep;
+};
+
+// The unit tables of the meta block, copied into shared memory once per CTA.
+struct MetaTables {
+    int up_off[kMaxRouted + 2];
+    int touched[kMaxRouted];
+    int e_off[kMaxRouted + 1];
+};
+
+__host__ __device__ inline int BatchUpSmem::total(int H) { return 2 * stage(H) + parts(H) + 64 + (int)sizeof(MetaTables); }
+
+__device__ __forceinline__ void load_tables(const BatchMeta* m, int nt, int E, MetaTables* s) {
+    for (int i = threadIdx.x; i < nt + 2; i += blockDim.x) s->up_off[i] = __ldcg(&m->up_off[i]);
+    for (int i = threadIdx.x; i < nt; i += blockDim.x) s->touched[i] = __ldcg(&m->touched[i]);
+    for (int i = threadIdx.x; i <= E; i += blockDim.x) s->e_off[i] = __ldcg(&m->e_off[i]);
+}
 
 __device__ __forceinline__ int unit_owner(const int* off, int n, int u) {
     // largest i in [0, n) with off[i] <= u
@@ -150,155 +222,211 @@ __device__ __forceinline__ int unit_owner(const int* off, int n, int u) {
     return lo;
 }
 
-__global__ void __launch_bounds__(256, 2) batch_up_kernel(const __grid_constant__ LayerParams P, const BatchIO io) {
+__device__ __forceinline__ UpUnitDesc up_unit_desc(const LayerParams& P, const BatchIO& io, const MetaTables* tb, int nt,
+                                                   int u) {
+    UpUnitDesc d;
+    const int i = unit_owner(tb->up_off, nt + 1, u);
+    d.shared = (i == nt);
+    d.N = d.shared ? P.shared_neurons : P.routed_neurons;
+    d.HG = d.N / 32;
+    const int local = u - tb->up_off[i];
+    d.c = local / d.HG;
+    d.hg = local % d.HG;
+    if (d.shared) {
+        d.e = -1;
+        d.ep = P.shared;
+        d.pbase = d.c * kTC;
+        d.T = min(kTC, io.batch - d.c * kTC);
+    } else {
+        d.e = tb->touched[i];
+        d.ep = routed_ptrs(P, d.e);
+        d.pbase = tb->e_off[d.e] + d.c * kTC;
+        d.T = min(kTC, tb->e_off[d.e + 1] - d.pbase);
+    }
+    return d;
+}
+
+__global__ void __launch_bounds__(256, 1) batch_up_kernel(const __grid_constant__ LayerParams P, const BatchIO io) {
     extern __shared__ __align__(128) uint8_t smem[];
     const int H = P.hidden, G = H / 64, rowb = H / 2;
-    uint8_t* codes = smem;
-    uint32_t* sbuf = reinterpret_cast<uint32_t*>(smem + BatchUpSmem::codes(H));
-    uint8_t* xf_s = smem + BatchUpSmem::codes(H) + BatchUpSmem::sb(H);
-    float* xs_s = reinterpret_cast<float*>(xf_s + BatchUpSmem::xf(H));
-    uint8_t* stage = reinterpret_cast<uint8_t*>(xs_s) + BatchUpSmem::xs(H);
-    float* parts = reinterpret_cast<float*>(stage);                      // [kTC][32][pstride]
-    uint16_t* xstage = reinterpret_cast<uint16_t*>(stage);               // [kTC][H]
-    float* off_s = reinterpret_cast<float*>(stage + BatchUpSmem::stage(H));  // [32]
-    int* tok_s = reinterpret_cast<int*>(off_s + 32);                     // [kTC] token ids
-    int* hrow_s = tok_s + kTC;                                           // [kTC] h rows
-    uint64_t* bars = reinterpret_cast<uint64_t*>(off_s + 64);            // 3 barriers
+    const int stage_bytes = BatchUpSmem::stage(H);
+    float* parts = reinterpret_cast<float*>(smem + 2 * stage_bytes);     // [kTC][32][pstride]
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + 2 * stage_bytes + BatchUpSmem::parts(H));  // [2]
+    MetaTables* tb = reinterpret_cast<MetaTables*>(bars + 8);
     const int t = threadIdx.x;
     const bool dense = (io.flags & HS_FORCE_DENSE) != 0;
-    const uint64_t pol = policy_evict_first();
     if (t == 0) {
-        for (int i = 0; i < 3; ++i) mbar_init(&bars[i], 1);
+        mbar_init(&bars[0], 1);
+        mbar_init(&bars[1], 1);
         fence_mbar_init();
     }
     __syncthreads();
     pdl_wait();
     pdl_trigger();
     const BatchMeta* m = io.meta;
-    const int U = m->up_units, nt = m->n_touched;
+    const int U = __ldcg(&m->up_units), nt = __ldcg(&m->n_touched);
     const int pstride = BatchUpSmem::pstride(H);
-    uint32_t phase = 0;
-    for (int u = blockIdx.x; u < U; u += gridDim.x, phase ^= 1u) {
-        // ---- which expert, rows and tokens
-        const int i = unit_owner(m->up_off, nt + 1, u);
-        const bool shared = (i == nt);
-        const int N = shared ? P.shared_neurons : P.routed_neurons;
-        const int HG = N / 32;
-        const int local = u - m->up_off[i];
-        const int c = local / HG, hg = local % HG;
-        ExpertPtrs ep;
-        int T, pbase = 0, e = -1;
-        if (shared) {
-            ep = P.shared;
-            T = min(kTC, io.batch - c * kTC);
-        } else {
-            e = m->touched[i];
-            ep = routed_ptrs(P, e);
-            pbase = m->e_off[e] + c * kTC;
-            T = min(kTC, m->e_off[e + 1] - pbase);
+    load_tables(m, nt, P.n_routed, tb);
+    __syncthreads();
+
+    // stage buffer layout
+    auto codes_of = [&](int b) { return smem + b * stage_bytes; };
+    auto sb_of = [&](int b) { return reinterpret_cast<uint32_t*>(smem + b * stage_bytes + BatchUpSmem::codes(H)); };
+    auto xf_of = [&](int b) { return smem + b * stage_bytes + BatchUpSmem::codes(H) + BatchUpSmem::sb(H); };
+    auto xs_of = [&](int b) {
+        return reinterpret_cast<float*>(smem + b * stage_bytes + BatchUpSmem::codes(H) + BatchUpSmem::sb(H) +
+                                        BatchUpSmem::xf(H));
+    };
+    auto off_of = [&](int b) {
+        return reinterpret_cast<float*>(smem + b * stage_bytes + BatchUpSmem::codes(H) + BatchUpSmem::sb(H) +
+                                        BatchUpSmem::xf(H) + BatchUpSmem::xs(H));
+    };
+    // thread 0 issues one unit's copies into stage b
+    auto issue = [&](const UpUnitDesc& d, int b) {
+        const uint64_t pol = policy_evict_first(), polx = policy_evict_last();
+        const uint32_t bytes = 32 * rowb + 32 * G * 4 + d.T * (G * kXfStride + G * 8);
+        mbar_arrive_expect_tx(&bars[b], bytes);
+        bulk_g2s(codes_of(b), d.ep.up_codes + (size_t)(32 * d.hg) * rowb, 32 * rowb, &bars[b], pol);
+        bulk_g2s(sb_of(b), d.ep.up_sb + (size_t)(32 * d.hg) * G, 32 * G * 4, &bars[b], pol);
+        for (int k = 0; k < d.T; ++k) {
+            const int tok = d.shared ? d.pbase + k : __ldcg(io.pair_tok + d.pbase + k);
+            bulk_g2s(xf_of(b) + (size_t)k * G * kXfStride, io.xt + (size_t)tok * G * kXfStride, G * kXfStride,
+                     &bars[b], polx);
+            bulk_g2s(xs_of(b) + (size_t)k * G * 2, io.xsc + (size_t)tok * G * 2, G * 8, &bars[b], polx);
         }
-        if (t < T) {
-            tok_s[t] = shared ? c * kTC + t : io.pair_tok[pbase + t];
-            hrow_s[t] = shared ? c * kTC + t : pbase + t;
+    };
+    int u = blockIdx.x;
+    UpUnitDesc cur;
+    if (u < U) {
+        cur = up_unit_desc(P, io, tb, nt, u);
+        if (t == 0) issue(cur, 0);
+    }
+    uint32_t phases = 0u;  // bit b: parity of stage b's next phase
+    for (int it = 0; u < U; ++it, u += gridDim.x) {
+        const int b = it & 1;
+        // offsets of the rows (plain loads; read after the barrier below)
+        if (t < 32) off_of(b)[t] = cur.ep.up_off ? __ldg(cur.ep.up_off + 32 * cur.hg + t) : 0.f;
+        // the next unit's copies go into the other stage (its previous unit finished last iteration)
+        const int un = u + gridDim.x;
+        UpUnitDesc nxt;
+        if (un < U) {
+            nxt = up_unit_desc(P, io, tb, nt, un);
+            if (t == 0) issue(nxt, b ^ 1);
         }
-        if (t < 32) off_s[t] = ep.up_off ? ep.up_off[32 * hg + t] : 0.f;
-        fence_proxy_async_smem();
-        __syncthreads();
-        if (t == 0) {
-            const uint8_t* src = ep.up_codes + (size_t)(32 * hg) * rowb;
-            mbar_arrive_expect_tx(&bars[0], 16 * rowb + 32 * G * 4);
-            bulk_g2s(sbuf, ep.up_sb + (size_t)(32 * hg) * G, 32 * G * 4, &bars[0], pol);
-            bulk_g2s(codes, src, 16 * rowb, &bars[0], pol);
-            mbar_arrive_expect_tx(&bars[1], 16 * rowb);
-            bulk_g2s(codes + 16 * rowb, src + (size_t)16 * rowb, 16 * rowb, &bars[1], pol);
-            mbar_arrive_expect_tx(&bars[2], T * H * 2);
-            for (int k = 0; k < T; ++k)
-                bulk_g2s(xstage + (size_t)k * H, io.x + (size_t)tok_s[k] * H, H * 2, &bars[2], policy_evict_last());
-        }
-        bool ok = __syncthreads_and(mbar_wait(&bars[2], phase));
-        // ---- fixed-point x tables for the T tokens (4 threads per group)
-        for (int k = 0; k < T && ok; ++k)
-            convert_x_fixed(xstage + (size_t)k * H, G, xf_s + (size_t)k * G * kXfStride, xs_s + (size_t)k * G * 2, 0);
-        if (!__syncthreads_and(ok)) return;  // x staging is free: parts may overwrite it
-        // ---- dot products: thread (gc, tk) over the 32 rows
-        const int gc = t % G, tk = t / G;
-        if (tk < T) {
-            XFixed xf;
-            load_x_fixed(xf_s + (size_t)tk * G * kXfStride, xs_s + (size_t)tk * G * 2, gc, xf);
-            float* pp = parts + (size_t)tk * 32 * pstride;
-            int waited = -1;
-            for (int r = 0; r < 32; ++r) {
-                const int kb = r >> 4;
-                while (waited < kb) { ++waited; ok &= mbar_wait(&bars[waited], phase); }
-                if (!ok) break;
-                uint4 a0, a1;
-                load_group_codes(codes + r * rowb, gc, a0, a1);
-                const float2 sb = half2_to_float2(sbuf[r * G + gc]);
-                const int d = group_dot_fixed16(a0, a1, xf);
-                pp[r * pstride + gc] = fmaf(sb.x * xf.inv, (float)d, sb.y * xf.xsum);
-            }
-            while (ok && waited < 1) { ++waited; ok &= mbar_wait(&bars[waited], phase); }
-        } else {
-            for (int k = 0; k < 2; ++k) ok &= mbar_wait(&bars[k], phase);
-        }
+        const bool ok = mbar_wait(&bars[b], (phases >> b) & 1u);
+        phases ^= 1u << b;
         if (!__syncthreads_and(ok)) return;
-        // ---- row sums, ReLU^2, h out, union live bits (warp w: token w/... rows)
+        // ---- dot products: thread (gc, tk, rs) over rows rs, rs + RS, ...
+        const int T = cur.T;
+        const int RS = 6 / T;  // 6, 3, 2, 1 row slices for 1..4 tokens: up to 252 threads busy
+        const int gc = t % G, rest = t / G, tk = rest % T, rs = rest / T;
+        if (rest < T * RS) {
+            XFixed xf;
+            load_x_fixed(xf_of(b) + (size_t)tk * G * kXfStride, xs_of(b) + (size_t)tk * G * 2, gc, xf);
+            float* pp = parts + (size_t)tk * 32 * pstride;
+            const uint8_t* cb = codes_of(b);
+            const uint32_t* sbb = sb_of(b);
+            for (int r = rs; r < 32; r += RS) {
+                uint4 a0, a1;
+                load_group_codes(cb + r * rowb, gc, a0, a1);
+                const float2 sbv = half2_to_float2(sbb[r * G + gc]);
+                const int dd = group_dot_fixed16(a0, a1, xf);
+                pp[r * pstride + gc] = fmaf(sbv.x * xf.inv, (float)dd, sbv.y * xf.xsum);
+            }
+        }
+        __syncthreads();
+        // ---- row sums, ReLU^2, h out, union live bits (warp w: token w)
         {
             const int lane = t & 31, w = t >> 5;
-            uint32_t anyl = 0;
-            for (int k = w; k < T; k += 8) {
-                const float* pp = parts + (size_t)k * 32 * pstride + lane * pstride;
+            if (w < T) {
+                const float* pp = parts + (size_t)w * 32 * pstride + lane * pstride;
                 float s0 = 0.f, s1 = 0.f;
                 int g = 0;
                 for (; g + 1 < G; g += 2) { s0 += pp[g]; s1 += pp[g + 1]; }
                 if (g < G) s0 += pp[g];
-                const float z = (s0 + s1) + off_s[lane];
+                const float z = (s0 + s1) + off_of(b)[lane];
                 const float h = z > 0.f ? z * z : 0.f;
-                const int n = 32 * hg + lane;
-                if (shared) io.h_sh[(size_t)hrow_s[k] * N + n] = h;
-                else io.h_pair[(size_t)hrow_s[k] * N + n] = h;
-                anyl |= __ballot_sync(0xffffffffu, h > 0.f);
-            }
-            if (lane == 0 && (anyl || dense)) {
-                uint32_t* mw = shared ? io.mask_s + hg : io.mask_r + (size_t)e * HG + hg;
-                atomicOr(mw, dense ? 0xffffffffu : anyl);
+                const int n = 32 * cur.hg + lane;
+                if (cur.shared) io.h_sh[(size_t)(cur.pbase + w) * cur.N + n] = h;
+                else io.h_pair[(size_t)(cur.pbase + w) * cur.N + n] = h;
+                const uint32_t anyl = __ballot_sync(0xffffffffu, h > 0.f);
+                if (lane == 0 && (anyl || dense)) {
+                    uint32_t* mw = cur.shared ? io.mask_s + cur.hg : io.mask_r + (size_t)cur.e * cur.HG + cur.hg;
+                    atomicOr(mw, dense ? 0xffffffffu : anyl);
+                }
             }
         }
-        __syncthreads();  // parts, codes and tables are reused by the next unit
+        __syncthreads();  // parts and this stage are reused
+        cur = nxt;
     }
 }
 
 // ------------------------------------------------------------------ down
-// Unit (expert i, band of 128 outputs).  Thread (oq, tl): outputs
-// 4*oq .. 4*oq+3 of the band, tokens tl, tl+8, ... of the expert.  Rows are
-// taken in ascending order; each live row's weights are dequantised once
-// (w = s*q + b, exact in fp32) and multiplied into every token's sum.
+// Unit (item i, band of 128 outputs); an item is a touched routed expert or a
+// row chunk of the shared expert.  The live rows come from the union mask
+// (parallel prefix over the mask words); their band code bytes and their
+// tokens' h are staged by cp.async, two passes of kRows rows in flight; the
+// (scale, bias) slab slices of the live groups are staged once per unit.
+// Thread (oq, warp): outputs 4*oq .. 4*oq+3 of the band.  With more than 8
+// tokens, warp w takes tokens w, w+8, ... over all rows; with at most 8, warp
+// w takes a fixed eighth of the rows (by mask word) for every token, streams
+// its live rows through its own buffer, and the 8 warps' sums are added in a
+// fixed order at the end.  Every split is by row index, never by position in
+// the live list, so the sparse and the dense (all rows live) results are
+// bit-identical: a dead row adds exact zeros.
 struct BatchDownSmem {
-    static constexpr int kRows = 64;  // live rows staged per pass
-    __host__ __device__ static int total() {
-        return kRows * 64 /*codes*/ + kRows * kMaxBatch * 4 /*h*/ + kRows * 2 /*ids*/ + 3712 / 32 * 4 + 256;
-    }
+    static constexpr int kRows = 64;                  // live rows per pass
+    static constexpr int kMaxWords = 3712 / 32;       // mask words of the widest expert
+    static constexpr int kMaxGroups = 3712 / 64;
+    static constexpr int kCodes = kRows * 64;         // band bytes of the rows of a pass
+    static constexpr int kH = kRows * kMaxBatch * 4;  // h of the rows of a pass
+    static constexpr int kPass = kCodes + kH;
+    static constexpr int kSlab = kMaxGroups * kBand * 4;
+    static constexpr int kIds = 3712 * 2;
+    static int total();
 };
+constexpr int kWarpRows = 16;                                  // rows per chunk of a warp's own pipeline
+constexpr int kWarpBuf = 2 * (kWarpRows * 64 + kWarpRows * 8 * 4);  // two stages: codes + h of <= 8 tokens
+static_assert(8 * kWarpBuf <= 2 * BatchDownSmem::kPass, "per-warp buffers fit in the pass buffers");
+
+inline int BatchDownSmem::total() { return 2 * kPass + kSlab + kIds + (kMaxWords + 1) * 4 * 2 + (int)sizeof(MetaTables) + 64; }
+
+__device__ __forceinline__ void cp_async16(void* dst, const void* src) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_u32(dst)), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async4(void* dst, const void* src) {
+    asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(smem_u32(dst)), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory"); }
 
 __global__ void __launch_bounds__(256) batch_down_kernel(const __grid_constant__ LayerParams P, const BatchIO io) {
     extern __shared__ __align__(128) uint8_t smem[];
-    constexpr int R = BatchDownSmem::kRows;
-    uint8_t* cs = smem;                                               // [R][64] band code bytes
-    float* hs = reinterpret_cast<float*>(smem + R * 64);              // [R][kMaxBatch]
-    uint16_t* ids = reinterpret_cast<uint16_t*>(hs + R * kMaxBatch);  // [R]
-    int* wpre = reinterpret_cast<int*>(ids + R);                      // prefix of live counts per mask word
-    int* misc = wpre + 3712 / 32 + 2;
-    const int t = threadIdx.x;
-    const int H = P.hidden, K = P.top_k;
+    using S = BatchDownSmem;
+    constexpr int R = S::kRows;
+    uint8_t* pass_buf = smem;                                             // [2][kPass]
+    uint32_t* slab = reinterpret_cast<uint32_t*>(smem + 2 * S::kPass);    // [group][128] (scale, bias)
+    uint16_t* ids = reinterpret_cast<uint16_t*>(smem + 2 * S::kPass + S::kSlab);
+    uint32_t* words = reinterpret_cast<uint32_t*>(ids + 3712);            // [kMaxWords + 1]
+    int* wpre = reinterpret_cast<int*>(words + S::kMaxWords + 1);         // [kMaxWords + 1]
+    MetaTables* tb = reinterpret_cast<MetaTables*>(wpre + S::kMaxWords + 1);
+    const int t = threadIdx.x, lane = t & 31, warp = t >> 5;
+    const int H = P.hidden, B = io.batch;
+    const int SC = P.shared_neurons ? shared_chunks(B) : 0;
+    const int NSl = SC + P.top_k;
     pdl_wait();
     pdl_trigger();
     const BatchMeta* m = io.meta;
-    const int nt = m->n_touched, nb = H / kBand;
-    const int U = m->dn_units;
-    const int oq = t & 31, tl = t >> 5;
+    const int nt = __ldcg(&m->n_touched), nb = H / kBand;
+    const int U = __ldcg(&m->dn_units);
+    const int oq = lane;
+    load_tables(m, nt, P.n_routed, tb);
+    __syncthreads();
     for (int u = blockIdx.x; u < U; u += gridDim.x) {
         const int i = u / nb, band = u % nb;
-        const bool shared = (i == nt);
+        const bool shared = (i >= nt);
+        const int chunk = shared ? i - nt : 0;
         const int N = shared ? P.shared_neurons : P.routed_neurons;
         const int NW = N / 32;
         ExpertPtrs ep;
@@ -306,101 +434,235 @@ __global__ void __launch_bounds__(256) batch_down_kernel(const __grid_constant__
         const uint32_t* mask;
         if (shared) {
             ep = P.shared;
-            T = io.batch;
+            T = B;
             mask = io.mask_s;
         } else {
-            const int e = m->touched[i];
+            const int e = tb->touched[i];
             ep = routed_ptrs(P, e);
-            pbase = m->e_off[e];
-            T = m->e_off[e + 1] - pbase;
+            pbase = tb->e_off[e];
+            T = tb->e_off[e + 1] - pbase;
             mask = io.mask_r + (size_t)e * NW;
         }
-        // prefix sums of live counts per mask word (thread 0, NW <= 116)
-        if (t == 0) {
-            int acc = 0, ng = 0;
-            for (int w = 0; w < NW; ++w) {
-                const uint32_t mw = __ldcg(mask + w);
-                wpre[w] = acc;
-                acc += __popc(mw);
-                if ((w & 1) && (mw | __ldcg(mask + w - 1))) ++ng;  // words 2g, 2g+1 cover group g
+        // ---- union live rows: mask words, prefix counts (warp 0), row ids
+        if (t < NW) words[t] = __ldcg(mask + t);
+        __syncthreads();
+        if (warp == 0) {
+            int c[4], s = 0;
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                const int w = 4 * lane + j;
+                c[j] = w < NW ? __popc(words[w]) : 0;
+                s += c[j];
             }
-            wpre[NW] = acc;
-            misc[0] = acc;
-            if (band == 0) { io.meta->live_cnt[i] = acc; io.meta->live_grp[i] = ng; }
+            int incl = s;
+#pragma unroll
+            for (int off = 1; off < 32; off <<= 1) {
+                const int o = __shfl_up_sync(0xffffffffu, incl, off);
+                if (lane >= off) incl += o;
+            }
+            int run = incl - s;
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                const int w = 4 * lane + j;
+                if (w < NW) wpre[w] = run;
+                run += c[j];
+            }
+            if (lane == 31) wpre[NW] = incl;
         }
         __syncthreads();
-        const int nlive = misc[0];
+        const int nlive = wpre[NW];
+        // this item's live rows: a shared-expert chunk owns the rows of a fixed range of mask
+        // words (by row index, so that the summation order does not depend on which rows are live)
+        const int w_lo = shared ? NW * chunk / SC : 0, w_hi = shared ? NW * (chunk + 1) / SC : NW;
+        const int lo = wpre[w_lo], hi = wpre[w_hi];
+        if (t >= w_lo && t < w_hi) {
+            uint32_t bits = words[t];
+            int pos = wpre[t] - lo;
+            while (bits) {
+                const int bb = __ffs(bits) - 1;
+                bits &= bits - 1;
+                ids[pos++] = (uint16_t)(32 * t + bb);
+            }
+        }
+        if (t == 0 && band == 0 && chunk == 0) {
+            int ng = 0;
+            for (int g = 0; g < NW / 2; ++g) ng += (words[2 * g] | words[2 * g + 1]) != 0u;
+            io.meta->live_cnt[shared ? nt : i] = nlive;
+            io.meta->live_grp[shared ? nt : i] = ng;
+        }
+        // slab slices of the groups holding a live row
+        for (int q = t; q < (N / 64) * 32; q += blockDim.x) {
+            const int g = q >> 5, part = q & 31;
+            if (words[2 * g] | words[2 * g + 1])
+                cp_async16(slab + g * kBand + 4 * part, ep.dn_sb + (size_t)g * H + band * kBand + 4 * part);
+        }
+        cp_async_commit();
+        __syncthreads();
+        const int nrows = hi - lo;
         float acc[4][kMaxBatch / 8];
 #pragma unroll
         for (int a = 0; a < 4; ++a)
 #pragma unroll
             for (int b = 0; b < kMaxBatch / 8; ++b) acc[a][b] = 0.f;
+        const bool rows_split = T <= 8;
+        // dequantise row n's 4 weights of this thread's outputs (group scales from the slab)
         int cur_g = -1;
         float2 sbv[4] = {};
-        for (int base = 0; base < nlive; base += R) {
-            const int nr = min(R, nlive - base);
-            // live row ids of this pass: each thread expands one mask word
-            for (int w = t; w < NW; w += blockDim.x) {
-                uint32_t bits = __ldcg(mask + w);
-                int pos = wpre[w];
-                while (bits) {
-                    const int b = __ffs(bits) - 1;
-                    bits &= bits - 1;
-                    if (pos >= base && pos < base + nr) ids[pos - base] = (uint16_t)(32 * w + b);
-                    ++pos;
+        auto weights = [&](int n, uint32_t cw, float (&wv)[4]) {
+            const int g = n >> 6;
+            if (g != cur_g) {
+                cur_g = g;
+                const uint4 s4 = *reinterpret_cast<const uint4*>(slab + g * kBand + 4 * oq);
+                sbv[0] = half2_to_float2(s4.x); sbv[1] = half2_to_float2(s4.y);
+                sbv[2] = half2_to_float2(s4.z); sbv[3] = half2_to_float2(s4.w);
+            }
+#pragma unroll
+            for (int a = 0; a < 4; ++a) {
+                // the code as an exact float: (2^23 + q) - 2^23
+                const float qf = __uint_as_float(0x4B000000u | ((cw >> (4 * a)) & 15u)) - 8388608.f;
+                wv[a] = fmaf(sbv[a].x, qf, sbv[a].y);
+            }
+        };
+        if (rows_split) {
+            // ---- few tokens: warp w owns a fixed range of rows (mask words) and streams its own
+            // live rows through a private double buffer of kWarpRows rows
+            constexpr int WR = kWarpRows;
+            uint8_t* wb = pass_buf + warp * kWarpBuf;
+            const int ww_lo = w_lo + (w_hi - w_lo) * warp / 8, ww_hi = w_lo + (w_hi - w_lo) * (warp + 1) / 8;
+            const int r_lo = wpre[ww_lo] - lo, r_hi = wpre[ww_hi] - lo;
+            const int nchunk = (r_hi - r_lo + WR - 1) / WR;
+            auto prefetch_w = [&](int c) {
+                uint8_t* st = wb + (c & 1) * (kWarpBuf / 2);
+                float* hbw = reinterpret_cast<float*>(st + WR * 64);
+                const int r0 = r_lo + c * WR, nr = min(WR, r_hi - r0);
+                for (int q = lane; q < nr * 4; q += 32) {
+                    const int r = q >> 2, part = q & 3;
+                    cp_async16(st + r * 64 + 16 * part,
+                               ep.dn_codes + (size_t)ids[r0 + r] * (H / 2) + band * (kBand / 2) + 16 * part);
                 }
-            }
-            __syncthreads();
-            // band code bytes of the rows (64 B each) and h of every token
-            for (int q = t; q < nr * 4; q += blockDim.x) {
-                const int r = q >> 2, part = q & 3;
-                const uint4 v = __ldg(reinterpret_cast<const uint4*>(ep.dn_codes + (size_t)ids[r] * (H / 2) +
-                                                                     band * (kBand / 2)) + part);
-                reinterpret_cast<uint4*>(cs + r * 64)[part] = v;
-            }
-            for (int q = t; q < nr * T; q += blockDim.x) {
-                const int r = q % nr, k = q / nr;
-                const int n = ids[r];
-                hs[r * kMaxBatch + k] = shared ? __ldcg(io.h_sh + (size_t)k * N + n)
-                                               : __ldcg(io.h_pair + (size_t)(pbase + k) * N + n);
-            }
-            __syncthreads();
-            for (int r = 0; r < nr; ++r) {
-                const int n = ids[r];
-                const int g = n >> 6;
-                if (g != cur_g) {
-                    cur_g = g;
-                    const uint4 s4 = __ldg(reinterpret_cast<const uint4*>(ep.dn_sb + (size_t)g * H + band * kBand) + oq);
-                    sbv[0] = half2_to_float2(s4.x); sbv[1] = half2_to_float2(s4.y);
-                    sbv[2] = half2_to_float2(s4.z); sbv[3] = half2_to_float2(s4.w);
+                for (int q = lane; q < nr * T; q += 32) {
+                    const int r = q % nr, k = q / nr;
+                    const int n = ids[r0 + r];
+                    cp_async4(hbw + r * 8 + k,
+                              shared ? io.h_sh + (size_t)k * N + n : io.h_pair + (size_t)(pbase + k) * N + n);
                 }
-                const uint32_t cw = reinterpret_cast<const uint16_t*>(cs + r * 64)[oq];  // 4 codes
-                float wv[4];
+                cp_async_commit();
+            };
+            if (nchunk > 0) prefetch_w(0);
+            // the slab copies (every thread's first group) are complete and visible to all warps
+            if (nchunk > 0) cp_async_wait<1>(); else cp_async_wait<0>();
+            __syncthreads();
+            for (int c = 0; c < nchunk; ++c) {
+                if (c + 1 < nchunk) {
+                    prefetch_w(c + 1);
+                    cp_async_wait<1>();
+                } else {
+                    cp_async_wait<0>();
+                }
+                __syncwarp();
+                const uint8_t* st = wb + (c & 1) * (kWarpBuf / 2);
+                const float* hbw = reinterpret_cast<const float*>(st + WR * 64);
+                const int r0 = r_lo + c * WR, nr = min(WR, r_hi - r0);
+                for (int r = 0; r < nr; ++r) {
+                    float wv[4];
+                    weights(ids[r0 + r], reinterpret_cast<const uint16_t*>(st + r * 64)[oq], wv);
 #pragma unroll
-                for (int a = 0; a < 4; ++a) wv[a] = fmaf(sbv[a].x, (float)((cw >> (4 * a)) & 15u), sbv[a].y);
+                    for (int k = 0; k < 8; ++k) {
+                        if (k < T) {
+                            const float hv = hbw[r * 8 + k];
 #pragma unroll
-                for (int b = 0; b < kMaxBatch / 8; ++b) {
-                    const int k = tl + 8 * b;
-                    if (k < T) {
-                        const float hv = hs[r * kMaxBatch + k];
-#pragma unroll
-                        for (int a = 0; a < 4; ++a) acc[a][b] = fmaf(hv, wv[a], acc[a][b]);
+                            for (int a = 0; a < 4; ++a) acc[a][k] = fmaf(hv, wv[a], acc[a][k]);
+                        }
                     }
                 }
+                __syncwarp();
             }
-            __syncthreads();
-        }
-        // partial rows: (token, slot) of this expert, outputs of this band
+            __syncthreads();  // every warp is done with its buffer before the reduction reuses them
+        } else {
+            // ---- many tokens: CTA-wide passes of R rows, warp w takes tokens w, w + 8, ...
+            const int npass = (nrows + R - 1) / R;
+            auto prefetch = [&](int p) {
+                uint8_t* pb = pass_buf + (p & 1) * S::kPass;
+                float* hb = reinterpret_cast<float*>(pb + S::kCodes);
+                const int r0 = p * R, nr = min(R, nrows - r0);
+                for (int q = t; q < nr * 4; q += blockDim.x) {
+                    const int r = q >> 2, part = q & 3;
+                    cp_async16(pb + r * 64 + 16 * part,
+                               ep.dn_codes + (size_t)ids[r0 + r] * (H / 2) + band * (kBand / 2) + 16 * part);
+                }
+                for (int q = t; q < nr * T; q += blockDim.x) {
+                    const int r = q % nr, k = q / nr;
+                    const int n = ids[r0 + r];
+                    cp_async4(hb + r * kMaxBatch + k,
+                              shared ? io.h_sh + (size_t)k * N + n : io.h_pair + (size_t)(pbase + k) * N + n);
+                }
+                cp_async_commit();
+            };
+            if (npass > 0) prefetch(0);
+            for (int p = 0; p < npass; ++p) {
+                if (p + 1 < npass) {
+                    prefetch(p + 1);
+                    cp_async_wait<1>();
+                } else {
+                    cp_async_wait<0>();
+                }
+                __syncthreads();
+                const uint8_t* pb = pass_buf + (p & 1) * S::kPass;
+                const float* hb = reinterpret_cast<const float*>(pb + S::kCodes);
+                const int nr = min(R, nrows - p * R);
+                for (int r = 0; r < nr; ++r) {
+                    float wv[4];
+                    weights(ids[p * R + r], reinterpret_cast<const uint16_t*>(pb + r * 64)[oq], wv);
 #pragma unroll
-        for (int b = 0; b < kMaxBatch / 8; ++b) {
-            const int k = tl + 8 * b;
-            if (k < T) {
-                const int tok = shared ? k : io.pair_tok[pbase + k];
-                const int slot = shared ? 0 : io.pair_slot[pbase + k];
-                const float wgt = shared ? 1.f : io.pair_w[pbase + k];
-                float* dst = io.partial + ((size_t)tok * (K + 1) + slot) * H + band * kBand + 4 * oq;
-                *reinterpret_cast<float4*>(dst) =
-                    make_float4(wgt * acc[0][b], wgt * acc[1][b], wgt * acc[2][b], wgt * acc[3][b]);
+                    for (int b = 0; b < kMaxBatch / 8; ++b) {
+                        const int k = warp + 8 * b;
+                        if (k < T) {
+                            const float hv = hb[r * kMaxBatch + k];
+#pragma unroll
+                            for (int a = 0; a < 4; ++a) acc[a][b] = fmaf(hv, wv[a], acc[a][b]);
+                        }
+                    }
+                }
+                __syncthreads();
+            }
+            if (npass == 0) {
+                cp_async_wait<0>();
+                __syncthreads();
+            }
+        }
+        // ---- partial rows: (token, slot) of this item, outputs of this band
+        auto store = [&](int k, const float (&v)[4]) {
+            const int tok = shared ? k : __ldcg(io.pair_tok + pbase + k);
+            const int slot = shared ? chunk : SC + __ldcg(io.pair_slot + pbase + k) - 1;
+            const float wgt = shared ? 1.f : __ldcg(io.pair_w + pbase + k);
+            float* dst = io.partial + ((size_t)tok * NSl + slot) * H + band * kBand + 4 * oq;
+            *reinterpret_cast<float4*>(dst) = make_float4(wgt * v[0], wgt * v[1], wgt * v[2], wgt * v[3]);
+        };
+        if (rows_split) {
+            // fixed-order sum of the 8 warps' sums: red[warp][k][128] over the (now idle) pass buffers
+            float* red = reinterpret_cast<float*>(pass_buf);
+#pragma unroll
+            for (int k = 0; k < 8; ++k)
+                if (k < T)
+                    *reinterpret_cast<float4*>(red + ((size_t)warp * 8 + k) * kBand + 4 * oq) =
+                        make_float4(acc[0][k], acc[1][k], acc[2][k], acc[3][k]);
+            __syncthreads();
+            if (warp < T) {
+                float v[4] = {0.f, 0.f, 0.f, 0.f};
+                for (int w = 0; w < 8; ++w) {
+                    const float4 s4 = *reinterpret_cast<const float4*>(red + ((size_t)w * 8 + warp) * kBand + 4 * oq);
+                    v[0] += s4.x; v[1] += s4.y; v[2] += s4.z; v[3] += s4.w;
+                }
+                store(warp, v);
+            }
+        } else {
+#pragma unroll
+            for (int b = 0; b < kMaxBatch / 8; ++b) {
+                const int k = warp + 8 * b;
+                if (k < T) {
+                    const float v[4] = {acc[0][b], acc[1][b], acc[2][b], acc[3][b]};
+                    store(k, v);
+                }
             }
         }
         __syncthreads();
@@ -408,19 +670,19 @@ __global__ void __launch_bounds__(256) batch_down_kernel(const __grid_constant__
 }
 
 // ------------------------------------------------------------------ reduce
-// y[t][o] = sum over slots 0..K of partial[t][slot][o], slots ascending
-// (slot 0 = shared expert, skipped without one); bf16 RNE.
+// y[t][o] = sum over the token's partial rows in slot order (shared-expert
+// chunks first, then the routed slots 1..K); bf16 RNE.
 __global__ void __launch_bounds__(256) batch_reduce_kernel(const __grid_constant__ LayerParams P, const BatchIO io) {
     pdl_wait();
     pdl_trigger();
-    const int H = P.hidden, K = P.top_k;
+    const int H = P.hidden, B = io.batch;
+    const int NSl = (P.shared_neurons ? shared_chunks(B) : 0) + P.top_k;
     const int idx = blockIdx.x * blockDim.x + threadIdx.x;  // float4 index over [B][H/4]
-    const int B = io.batch;
     if (idx < B * (H / 4)) {
         const int tok = idx / (H / 4), c4 = idx % (H / 4);
-        const float4* p = reinterpret_cast<const float4*>(io.partial + (size_t)tok * (K + 1) * H) + c4;
+        const float4* p = reinterpret_cast<const float4*>(io.partial + (size_t)tok * NSl * H) + c4;
         float4 a = make_float4(0.f, 0.f, 0.f, 0.f);
-        for (int s = P.shared_neurons ? 0 : 1; s <= K; ++s) {
+        for (int s = 0; s < NSl; ++s) {
             const float4 v = __ldcg(p + (size_t)s * (H / 4));
             a.x += v.x; a.y += v.y; a.z += v.z; a.w += v.w;
         }
@@ -445,12 +707,13 @@ using namespace hs_host;
 
 namespace {
 struct BatchLayout {
-    size_t meta, topk_idx, topk_w, pair_tok, pair_w, pair_slot, h_pair, h_sh, mask_r, mask_s, partial, total;
+    size_t meta, topk_idx, topk_w, pair_tok, pair_w, pair_slot, xt, xsc, h_pair, h_sh, mask_r, mask_s, partial, total;
 };
 
 BatchLayout batch_layout(const hs_moe_layer* L, int B) {
     const int K = L->top_k, E = L->n_routed, NR = L->routed[0].neurons;
-    const int NS = L->shared ? L->shared->neurons : 0, H = L->hidden;
+    const int NS = L->shared ? L->shared->neurons : 0, H = L->hidden, G = H / 64;
+    const int SC = NS ? hs::shared_chunks(B) : 0;
     BatchLayout l{};
     size_t o = 0;
     auto take = [&](size_t bytes) { const size_t at = o; o += round_up(bytes, 256); return at; };
@@ -460,11 +723,13 @@ BatchLayout batch_layout(const hs_moe_layer* L, int B) {
     l.pair_tok = take((size_t)B * K * 4);
     l.pair_w = take((size_t)B * K * 4);
     l.pair_slot = take((size_t)B * K * 4);
+    l.xt = take((size_t)B * G * hs::kXfStride);
+    l.xsc = take((size_t)B * G * 8);
     l.h_pair = take((size_t)B * K * NR * 4);
     l.h_sh = take((size_t)B * (NS ? NS : 1) * 4);
     l.mask_r = take((size_t)E * (NR / 32) * 4);
     l.mask_s = take((size_t)(NS ? NS / 32 : 1) * 4);
-    l.partial = take((size_t)B * (K + 1) * H * 4);
+    l.partial = take((size_t)B * (SC + K) * H * 4);
     l.total = o;
     return l;
 }
@@ -512,6 +777,8 @@ int hs_batch_decode(const hs_moe_layer* L, const uint16_t* x, const float* logit
     io.pair_tok = reinterpret_cast<int*>(w + l.pair_tok);
     io.pair_w = reinterpret_cast<float*>(w + l.pair_w);
     io.pair_slot = reinterpret_cast<int*>(w + l.pair_slot);
+    io.xt = reinterpret_cast<uint8_t*>(w + l.xt);
+    io.xsc = reinterpret_cast<float*>(w + l.xsc);
     io.h_pair = reinterpret_cast<float*>(w + l.h_pair);
     io.h_sh = reinterpret_cast<float*>(w + l.h_sh);
     io.mask_r = reinterpret_cast<uint32_t*>(w + l.mask_r);
@@ -531,8 +798,12 @@ int hs_batch_decode(const hs_moe_layer* L, const uint16_t* x, const float* logit
     const int dn_smem = hs::BatchDownSmem::total();
     if (set_smem_attr((const void*)hs::batch_up_kernel, up_smem) != HS_OK) return HS_ERR_CUDA;
     if (set_smem_attr((const void*)hs::batch_down_kernel, dn_smem) != HS_OK) return HS_ERR_CUDA;
-    if (launch_pdl(hs::batch_route_kernel, dim3(1), dim3(256), 0, s, P, io) != cudaSuccess) return HS_ERR_CUDA;
-    if (launch_pdl(hs::batch_up_kernel, dim3(2 * sms), dim3(256), up_smem, s, P, io) != cudaSuccess) return HS_ERR_CUDA;
+    if (cudaMemsetAsync(io.meta, 0, sizeof(hs::BatchMeta), s) != cudaSuccess) return HS_ERR_CUDA;
+    // the first kernel follows the memset with ordinary stream ordering
+    hs::batch_route_kernel<<<dim3(batch), dim3(256), 0, s>>>(P, io);
+    if (cudaGetLastError() != cudaSuccess) return HS_ERR_CUDA;
+    if (launch_pdl(hs::batch_plan_kernel, dim3(1), dim3(512), 0, s, P, io) != cudaSuccess) return HS_ERR_CUDA;
+    if (launch_pdl(hs::batch_up_kernel, dim3(sms), dim3(256), up_smem, s, P, io) != cudaSuccess) return HS_ERR_CUDA;
     if (launch_pdl(hs::batch_down_kernel, dim3(2 * sms), dim3(256), dn_smem, s, P, io) != cudaSuccess)
         return HS_ERR_CUDA;
     const int nred = (batch * (L->hidden / 4) + 255) / 256;
