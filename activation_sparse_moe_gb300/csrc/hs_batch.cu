@@ -177,14 +177,15 @@ __global__ void __launch_bounds__(512) batch_plan_kernel(const __grid_constant__
 }
 
 // ------------------------------------------------------------------ up
-// Double-buffered unit stage: 32 rows of codes and (scale, bias) pairs, the
-// x tables of up to kTC tokens, and the offsets of the rows.
+// Unit stage of the weight ring: 32 rows of codes and their (scale, bias)
+// pairs.  Three stages: two units' copies are in flight while one is computed.
+// The x tables (L2-resident, a few KB per token) are read straight into
+// registers one unit ahead.
+constexpr int kUpStages = 3;
 struct BatchUpSmem {
     __host__ __device__ static int codes(int H) { return 32 * (H / 2); }
     __host__ __device__ static int sb(int H) { return 32 * (H / 64) * 4; }
-    __host__ __device__ static int xf(int H) { return kTC * (H / 64) * kXfStride; }
-    __host__ __device__ static int xs(int H) { return kTC * (H / 64) * 8; }
-    __host__ __device__ static int stage(int H) { return codes(H) + sb(H) + xf(H) + xs(H) + 128; }
+    __host__ __device__ static int stage(int H) { return codes(H) + sb(H); }
     // parts row stride: 1 mod 32 words, so row-sum loads (lane = row) are conflict-free
     __host__ __device__ static int pstride(int H) { return ((H / 64 + 31) / 32) * 32 + 1; }
     __host__ __device__ static int parts(int H) { return kTC * 32 * pstride(H) * 4; }
@@ -204,7 +205,9 @@ struct MetaTables {
     int e_off[kMaxRouted + 1];
 };
 
-__host__ __device__ inline int BatchUpSmem::total(int H) { return 2 * stage(H) + parts(H) + 64 + (int)sizeof(MetaTables); }
+__host__ __device__ inline int BatchUpSmem::total(int H) {
+    return kUpStages * stage(H) + parts(H) + 64 + (int)sizeof(MetaTables) + 32 * 4;
+}
 
 __device__ __forceinline__ void load_tables(const BatchMeta* m, int nt, int E, MetaTables* s) {
     for (int i = threadIdx.x; i < nt + 2; i += blockDim.x) s->up_off[i] = __ldcg(&m->up_off[i]);
@@ -246,18 +249,42 @@ __device__ __forceinline__ UpUnitDesc up_unit_desc(const LayerParams& P, const B
     return d;
 }
 
+// This thread's role in a unit of T tokens: (group gc, token tk, row slice rs of RS).
+struct UpRole {
+    int gc, tk, rs, RS;
+    bool active;
+};
+__device__ __forceinline__ UpRole up_role(int T, int G) {
+    UpRole r;
+    const int t = threadIdx.x;
+    r.RS = 6 / T;  // 6, 3, 2, 1 row slices for 1..4 tokens: up to 252 threads busy
+    r.gc = t % G;
+    const int rest = t / G;
+    r.tk = rest % T;
+    r.rs = rest / T;
+    r.active = rest < T * r.RS;
+    return r;
+}
+
+// The x table of this thread's (token, group) of a unit, from global memory.
+__device__ __forceinline__ void load_unit_x(const BatchIO& io, const UpUnitDesc& d, const UpRole& r, int G, XFixed& xf) {
+    if (!r.active) return;
+    const int tok = d.shared ? d.pbase + r.tk : __ldcg(io.pair_tok + d.pbase + r.tk);
+    load_x_fixed(io.xt + (size_t)tok * G * kXfStride, io.xsc + (size_t)tok * G * 2, r.gc, xf);
+}
+
 __global__ void __launch_bounds__(256, 1) batch_up_kernel(const __grid_constant__ LayerParams P, const BatchIO io) {
     extern __shared__ __align__(128) uint8_t smem[];
     const int H = P.hidden, G = H / 64, rowb = H / 2;
     const int stage_bytes = BatchUpSmem::stage(H);
-    float* parts = reinterpret_cast<float*>(smem + 2 * stage_bytes);     // [kTC][32][pstride]
-    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + 2 * stage_bytes + BatchUpSmem::parts(H));  // [2]
+    float* parts = reinterpret_cast<float*>(smem + kUpStages * stage_bytes);  // [kTC][32][pstride]
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kUpStages * stage_bytes + BatchUpSmem::parts(H));
     MetaTables* tb = reinterpret_cast<MetaTables*>(bars + 8);
+    float* offs_s = reinterpret_cast<float*>(tb + 1);   // [32] offsets of the current unit's rows
     const int t = threadIdx.x;
     const bool dense = (io.flags & HS_FORCE_DENSE) != 0;
     if (t == 0) {
-        mbar_init(&bars[0], 1);
-        mbar_init(&bars[1], 1);
+        for (int i = 0; i < kUpStages; ++i) mbar_init(&bars[i], 1);
         fence_mbar_init();
     }
     __syncthreads();
@@ -269,82 +296,85 @@ __global__ void __launch_bounds__(256, 1) batch_up_kernel(const __grid_constant_
     load_tables(m, nt, P.n_routed, tb);
     __syncthreads();
 
-    // stage buffer layout
     auto codes_of = [&](int b) { return smem + b * stage_bytes; };
     auto sb_of = [&](int b) { return reinterpret_cast<uint32_t*>(smem + b * stage_bytes + BatchUpSmem::codes(H)); };
-    auto xf_of = [&](int b) { return smem + b * stage_bytes + BatchUpSmem::codes(H) + BatchUpSmem::sb(H); };
-    auto xs_of = [&](int b) {
-        return reinterpret_cast<float*>(smem + b * stage_bytes + BatchUpSmem::codes(H) + BatchUpSmem::sb(H) +
-                                        BatchUpSmem::xf(H));
-    };
-    auto off_of = [&](int b) {
-        return reinterpret_cast<float*>(smem + b * stage_bytes + BatchUpSmem::codes(H) + BatchUpSmem::sb(H) +
-                                        BatchUpSmem::xf(H) + BatchUpSmem::xs(H));
-    };
-    // thread 0 issues one unit's copies into stage b
+    // thread 0 issues one unit's weight copies into stage b
     auto issue = [&](const UpUnitDesc& d, int b) {
-        const uint64_t pol = policy_evict_first(), polx = policy_evict_last();
-        const uint32_t bytes = 32 * rowb + 32 * G * 4 + d.T * (G * kXfStride + G * 8);
-        mbar_arrive_expect_tx(&bars[b], bytes);
+        const uint64_t pol = policy_evict_first();
+        mbar_arrive_expect_tx(&bars[b], 32 * rowb + 32 * G * 4);
         bulk_g2s(codes_of(b), d.ep.up_codes + (size_t)(32 * d.hg) * rowb, 32 * rowb, &bars[b], pol);
         bulk_g2s(sb_of(b), d.ep.up_sb + (size_t)(32 * d.hg) * G, 32 * G * 4, &bars[b], pol);
-        for (int k = 0; k < d.T; ++k) {
-            const int tok = d.shared ? d.pbase + k : __ldcg(io.pair_tok + d.pbase + k);
-            bulk_g2s(xf_of(b) + (size_t)k * G * kXfStride, io.xt + (size_t)tok * G * kXfStride, G * kXfStride,
-                     &bars[b], polx);
-            bulk_g2s(xs_of(b) + (size_t)k * G * 2, io.xsc + (size_t)tok * G * 2, G * 8, &bars[b], polx);
-        }
     };
-    int u = blockIdx.x;
-    UpUnitDesc cur;
-    if (u < U) {
-        cur = up_unit_desc(P, io, tb, nt, u);
-        if (t == 0) issue(cur, 0);
+    const int u0 = blockIdx.x;
+    if (u0 >= U) return;
+    UpUnitDesc cur = up_unit_desc(P, io, tb, nt, u0);
+    if (t == 0) {
+        issue(cur, 0);
+        if (u0 + (int)gridDim.x < U) issue(up_unit_desc(P, io, tb, nt, u0 + gridDim.x), 1);
     }
+    UpRole role = up_role(cur.T, G);
+    XFixed xcur;
+    load_unit_x(io, cur, role, G, xcur);
+    float off_cur = 0.f;
+    if (t < 32) off_cur = cur.ep.up_off ? __ldg(cur.ep.up_off + 32 * cur.hg + t) : 0.f;
     uint32_t phases = 0u;  // bit b: parity of stage b's next phase
-    for (int it = 0; u < U; ++it, u += gridDim.x) {
-        const int b = it & 1;
-        // offsets of the rows (plain loads; read after the barrier below)
-        if (t < 32) off_of(b)[t] = cur.ep.up_off ? __ldg(cur.ep.up_off + 32 * cur.hg + t) : 0.f;
-        // the next unit's copies go into the other stage (its previous unit finished last iteration)
-        const int un = u + gridDim.x;
-        UpUnitDesc nxt;
-        if (un < U) {
-            nxt = up_unit_desc(P, io, tb, nt, un);
-            if (t == 0) issue(nxt, b ^ 1);
+    int it = 0;
+    for (int u = u0; u < U; u += gridDim.x, ++it) {
+        const int b = it % kUpStages;
+        // copies two units ahead go into the stage the previous unit used
+        const int u2 = u + 2 * (int)gridDim.x;
+        if (t == 0 && u2 < U) issue(up_unit_desc(P, io, tb, nt, u2), (it + 2) % kUpStages);
+        // the next unit's x tables and offsets, into registers (used next iteration)
+        const int u1 = u + gridDim.x;
+        UpUnitDesc nxt = cur;
+        UpRole role_n = role;
+        XFixed xnext = xcur;
+        float off_next = 0.f;
+        if (u1 < U) {
+            nxt = up_unit_desc(P, io, tb, nt, u1);
+            role_n = up_role(nxt.T, G);
+            load_unit_x(io, nxt, role_n, G, xnext);
+            if (t < 32) off_next = nxt.ep.up_off ? __ldg(nxt.ep.up_off + 32 * nxt.hg + t) : 0.f;
         }
+        // offsets of this unit's rows (prefetched by warp 0), read after the barrier below
+        if (t < 32) offs_s[t] = off_cur;
         const bool ok = mbar_wait(&bars[b], (phases >> b) & 1u);
         phases ^= 1u << b;
         if (!__syncthreads_and(ok)) return;
         // ---- dot products: thread (gc, tk, rs) over rows rs, rs + RS, ...
-        const int T = cur.T;
-        const int RS = 6 / T;  // 6, 3, 2, 1 row slices for 1..4 tokens: up to 252 threads busy
-        const int gc = t % G, rest = t / G, tk = rest % T, rs = rest / T;
-        if (rest < T * RS) {
-            XFixed xf;
-            load_x_fixed(xf_of(b) + (size_t)tk * G * kXfStride, xs_of(b) + (size_t)tk * G * 2, gc, xf);
-            float* pp = parts + (size_t)tk * 32 * pstride;
+        if (role.active) {
+            float* pp = parts + (size_t)role.tk * 32 * pstride;
             const uint8_t* cb = codes_of(b);
             const uint32_t* sbb = sb_of(b);
-            for (int r = rs; r < 32; r += RS) {
-                uint4 a0, a1;
-                load_group_codes(cb + r * rowb, gc, a0, a1);
-                const float2 sbv = half2_to_float2(sbb[r * G + gc]);
-                const int dd = group_dot_fixed16(a0, a1, xf);
-                pp[r * pstride + gc] = fmaf(sbv.x * xf.inv, (float)dd, sbv.y * xf.xsum);
+            // two rows at a time: independent DP4A chains hide the pipe latency
+            for (int r = role.rs; r < 32; r += 2 * role.RS) {
+                const int r2 = r + role.RS;
+                const bool two = r2 < 32;
+                uint4 a0, a1, b0 = make_uint4(0, 0, 0, 0), b1 = make_uint4(0, 0, 0, 0);
+                load_group_codes(cb + r * rowb, role.gc, a0, a1);
+                if (two) load_group_codes(cb + r2 * rowb, role.gc, b0, b1);
+                const int da = group_dot_fixed16(a0, a1, xcur);
+                const int db = group_dot_fixed16(b0, b1, xcur);
+                const float2 sa = half2_to_float2(sbb[r * G + role.gc]);
+                pp[r * pstride + role.gc] = fmaf(sa.x * xcur.inv, (float)da, sa.y * xcur.xsum);
+                if (two) {
+                    const float2 sbv = half2_to_float2(sbb[r2 * G + role.gc]);
+                    pp[r2 * pstride + role.gc] = fmaf(sbv.x * xcur.inv, (float)db, sbv.y * xcur.xsum);
+                }
             }
         }
         __syncthreads();
-        // ---- row sums, ReLU^2, h out, union live bits (warp w: token w)
+        // ---- row sums, ReLU^2, h out, union live bits (warp w: token w; lane = row)
         {
             const int lane = t & 31, w = t >> 5;
-            if (w < T) {
+            if (w < cur.T) {
                 const float* pp = parts + (size_t)w * 32 * pstride + lane * pstride;
-                float s0 = 0.f, s1 = 0.f;
+                // four independent chains over the groups (G is even), then a fixed combination
+                float s0 = 0.f, s1 = 0.f, s2 = 0.f, s3 = 0.f;
                 int g = 0;
-                for (; g + 1 < G; g += 2) { s0 += pp[g]; s1 += pp[g + 1]; }
-                if (g < G) s0 += pp[g];
-                const float z = (s0 + s1) + off_of(b)[lane];
+                for (; g + 3 < G; g += 4) { s0 += pp[g]; s1 += pp[g + 1]; s2 += pp[g + 2]; s3 += pp[g + 3]; }
+                if (g < G) { s0 += pp[g]; s1 += pp[g + 1]; }
+                const float z = ((s0 + s1) + (s2 + s3)) + offs_s[lane];
                 const float h = z > 0.f ? z * z : 0.f;
                 const int n = 32 * cur.hg + lane;
                 if (cur.shared) io.h_sh[(size_t)(cur.pbase + w) * cur.N + n] = h;
@@ -356,8 +386,11 @@ __global__ void __launch_bounds__(256, 1) batch_up_kernel(const __grid_constant_
                 }
             }
         }
-        __syncthreads();  // parts and this stage are reused
+        __syncthreads();  // parts, the offsets and this stage are reused
         cur = nxt;
+        role = role_n;
+        xcur = xnext;
+        off_cur = off_next;
     }
 }
 
