@@ -47,69 +47,72 @@ __device__ __forceinline__ ExpertPtrs routed_ptrs(const LayerParams& P, int e) {
 
 // ------------------------------------------------------------------ router
 // Top-k of n <= 128 logits (ties -> lower index) and a softmax over the chosen
-// k <= 8, by one warp in registers.  Lane l sorts logits l, l+32, l+64, l+96
-// (value descending, index ascending) into a list of 8 padded with losers.
-// Five butterfly levels merge each lane's list with its xor partner's: the
-// elementwise best of L[j] and R[7-j] is the top 8 of the union as a bitonic
-// sequence, which a 3-stage bitonic merger sorts.  After the last level every
-// lane holds the overall top 8.  Lane 0 writes idx[k], w[k] (shared memory).
+// k <= 8, by one warp in registers.  Each logit becomes an order-preserving
+// 32-bit key (-0 taken as +0).  Lane l sorts its keys l, l+32, l+64, l+96
+// (key descending, index ascending); then k rounds of a warp-wide maximum of
+// the lanes' heads (redux.sync), the lowest index among the lanes that hold
+// it (a second redux), and a pop by the winning lane.  Lane 0 writes idx[k]
+// and w[k].
 
-__device__ __forceinline__ bool topk_better(float a, int ia, float b, int ib) {
-    return a > b || (a == b && ia < ib);
+__device__ __forceinline__ uint32_t topk_key(float f) {
+    const uint32_t b = __float_as_uint(f + 0.f);   // -0 -> +0
+    return (b & 0x80000000u) ? ~b : (b | 0x80000000u);
 }
 
-__device__ __forceinline__ void topk_cx(float (&v)[8], int (&id)[8], int a, int b) {
-    // order positions a < b best-first
-    const bool sw = topk_better(v[b], id[b], v[a], id[a]);
-    const float va = v[a], vb = v[b];
+__device__ __forceinline__ float topk_value(uint32_t key) {
+    return __uint_as_float((key & 0x80000000u) ? (key & 0x7fffffffu) : ~key);
+}
+
+__device__ __forceinline__ void topk_cx(uint32_t (&k)[4], int (&id)[4], int a, int b) {
+    // order positions a < b best-first (larger key; equal keys: lower index)
+    const bool sw = k[b] > k[a] || (k[b] == k[a] && id[b] < id[a]);
+    const uint32_t ka = k[a], kb = k[b];
     const int ia = id[a], ib = id[b];
-    v[a] = sw ? vb : va; v[b] = sw ? va : vb;
+    k[a] = sw ? kb : ka; k[b] = sw ? ka : kb;
     id[a] = sw ? ib : ia; id[b] = sw ? ia : ib;
 }
 
 __device__ inline void warp_topk_softmax(const float* __restrict__ logits, int n, int k, int* idx, float* w) {
     const int lane = threadIdx.x & 31;
-    float v[8];
-    int id[8];
+    uint32_t key[4];
+    int id[4];
 #pragma unroll
-    for (int i = 0; i < 8; ++i) {
+    for (int i = 0; i < 4; ++i) {
         const int e = lane + 32 * i;
-        const bool real = i < 4 && e < n;
-        id[i] = real ? e : 1024 + 32 * i + lane;  // padding loses every comparison
-        v[i] = real ? logits[e] : -INFINITY;
+        const bool real = e < n;
+        key[i] = real ? topk_key(logits[e]) : 0u;   // no finite logit has key 0
+        id[i] = real ? e : 1024 + e;
     }
-    topk_cx(v, id, 0, 1); topk_cx(v, id, 2, 3); topk_cx(v, id, 0, 2); topk_cx(v, id, 1, 3); topk_cx(v, id, 1, 2);
+    topk_cx(key, id, 0, 1); topk_cx(key, id, 2, 3); topk_cx(key, id, 0, 2); topk_cx(key, id, 1, 3); topk_cx(key, id, 1, 2);
+    uint32_t sk[kMaxTopK];
+    int si[kMaxTopK];
 #pragma unroll
-    for (int off = 16; off; off >>= 1) {
-        float rv[8];
-        int ri[8];
-#pragma unroll
-        for (int j = 0; j < 8; ++j) {
-            rv[j] = __shfl_xor_sync(0xffffffffu, v[j], off);
-            ri[j] = __shfl_xor_sync(0xffffffffu, id[j], off);
-        }
-#pragma unroll
-        for (int j = 0; j < 8; ++j) {
-            if (topk_better(rv[7 - j], ri[7 - j], v[j], id[j])) { v[j] = rv[7 - j]; id[j] = ri[7 - j]; }
-        }
-#pragma unroll
-        for (int d = 4; d; d >>= 1) {
-#pragma unroll
-            for (int j = 0; j < 8; ++j)
-                if (!(j & d)) topk_cx(v, id, j, j + d);
+    for (int r = 0; r < kMaxTopK; ++r) {
+        sk[r] = 0u;
+        si[r] = 0;
+        if (r < k) {
+            const uint32_t mx = __reduce_max_sync(0xffffffffu, key[0]);
+            const uint32_t win = __reduce_min_sync(0xffffffffu, key[0] == mx ? (uint32_t)id[0] : 0xffffffffu);
+            sk[r] = mx;
+            si[r] = (int)win;
+            if ((uint32_t)id[0] == win) {   // pop this lane's head
+                key[0] = key[1]; key[1] = key[2]; key[2] = key[3]; key[3] = 0u;
+                id[0] = id[1]; id[1] = id[2]; id[2] = id[3]; id[3] = 4096;
+            }
         }
     }
     if (lane == 0) {
+        const float v0 = topk_value(sk[0]);
         float ex[kMaxTopK];
         float den = 0.f;
 #pragma unroll
-        for (int j = 0; j < kMaxTopK; ++j) ex[j] = (j < k) ? expf(v[j] - v[0]) : 0.f;
+        for (int j = 0; j < kMaxTopK; ++j) ex[j] = (j < k) ? expf(topk_value(sk[j]) - v0) : 0.f;
 #pragma unroll
         for (int j = 0; j < kMaxTopK; ++j) den += ex[j];
         const float inv = 1.f / den;
 #pragma unroll
         for (int j = 0; j < kMaxTopK; ++j)
-            if (j < k) { idx[j] = id[j]; w[j] = ex[j] * inv; }
+            if (j < k) { idx[j] = si[j]; w[j] = ex[j] * inv; }
     }
 }
 
