@@ -43,6 +43,13 @@ class DeviceExperts:
             hs.hs_repack_down_nm(dc[e], ds[e], db[e], H, N, self.dn_codes[e], self.dn_sb[e], stream)
         self.offsets = None if offsets is None else offsets.to(dev, torch.float32).contiguous()
 
+    def with_offsets(self, offsets) -> "DeviceExperts":
+        """The same device weights with other pre-activation offsets [E][N] (fp32)."""
+        other = object.__new__(DeviceExperts)
+        other.__dict__.update(self.__dict__)
+        other.offsets = None if offsets is None else offsets.to(self.up_codes.device, torch.float32).contiguous()
+        return other
+
     def desc(self, e: int) -> hs.hs_expert:
         return hs.make_expert(self.up_codes[e], self.up_sb[e], self.dn_codes[e], self.dn_sb[e],
                               None if self.offsets is None else self.offsets[e], self.N)

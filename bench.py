@@ -50,6 +50,7 @@ def _args():
     ap.add_argument("--batch-sizes", type=str, default="2,8,32,64",
                     help="batch decode leg (one MoE layer, 30%% dead neurons); empty to skip")
     ap.add_argument("--no-prefill", action="store_true", help="skip the 2048-token prefill leg")
+    ap.add_argument("--no-sweep", action="store_true", help="skip the live-fraction sweep")
     ap.add_argument("--profile", action="store_true",
                     help="minimal run for profilers: no clock soak, dense, end-to-end or CPU legs")
     return ap.parse_args()
@@ -130,19 +131,27 @@ class ClockSampler:
 
 
 # ----------------------------------------------------------- ncu traffic
-def _recorded_traffic(kernel: str, src: str):
+def _sources_sha256(srcs) -> str:
+    """One hash over the kernel's source files (the .cu and the headers it includes)."""
+    h = hashlib.sha256()
+    for src in srcs:
+        h.update(open(src, "rb").read())
+    return h.hexdigest()
+
+
+def _recorded_traffic(kernel: str, srcs):
     """DRAM bytes per launch recorded under profiles/ for `kernel`, if the
-    recorded source hash still matches the kernel's source file."""
+    recorded source hash still matches the kernel's sources (None otherwise:
+    the counters describe an older kernel)."""
     path = os.path.join(ROOT, "profiles", f"{kernel}.txt")
     if not os.path.exists(path):
         return None
-    sha = hashlib.sha256(open(src, "rb").read()).hexdigest()
     rec = {}
     for ln in open(path):
-        if ":" in ln:
+        if ":" in ln and not ln.startswith("#"):
             k, v = ln.split(":", 1)
             rec[k.strip()] = v.strip()
-    if rec.get("source_sha256") != sha:
+    if rec.get("source_sha256") != _sources_sha256(srcs):
         return None
     try:
         return float(rec["dram_bytes_per_launch"])
@@ -252,6 +261,49 @@ def bench_batch(args, dev, stream, timed, bytemodel, hs):
         del g, WS
     del layers
     torch.cuda.empty_cache()
+    return out
+
+
+def bench_p_sweep(args, layers, X, LG, dev, stream, timed, bytemodel, hs, peak):
+    """Configuration 3's live-fraction sweep on the same 23 resident layers: the
+    routed experts' offsets for live fraction p are the p = 0.1 offsets scaled by
+    Phi^-1(p) / Phi^-1(0.1) (the calibration off = Phi^-1(p) * ||w|| is linear
+    in Phi^-1(p)); the shared expert keeps its own per-layer fraction; p = 1.0 is
+    the dense path on the p = 0.1 inputs (reported as dense_path)."""
+    import numpy as np
+    import torch
+    from scipy.special import ndtri
+    from activation_sparse_moe_gb300.layer import DeviceLayer
+    n = len(layers)
+    Y = torch.empty((n, 2688), dtype=torch.bfloat16, device=dev)
+    WS = torch.zeros(max(d.workspace_size(1) for d in layers), dtype=torch.uint8, device=dev)
+    out = {}
+    for p in (0.02, 0.05, 0.2, 0.5):
+        ratio = float(ndtri(p) / ndtri(0.1))
+        lp = [DeviceLayer(dl.routed.with_offsets((dl.routed.offsets.double() * ratio).float()), dl.shared, 6)
+              for dl in layers]
+        rows, groups = [], []
+        with torch.cuda.stream(stream):
+            for l, dl in enumerate(lp):
+                dbg = {"live_rows": torch.empty(1, dtype=torch.int32, device=dev),
+                       "live_groups": torch.empty(1, dtype=torch.int32, device=dev)}
+                hs.hs_moe_layer_decode(dl.c, X[l], LG[l], 1, Y[l], None, 0, dbg, WS, stream=stream)
+                stream.synchronize()
+                rows.append(int(dbg["live_rows"].item()))
+                groups.append(int(dbg["live_groups"].item()))
+        step_bytes = sum(bytemodel.decode_layer_bytes(2688, [3712] + [1856] * 6, r, g, 128) for r, g in zip(rows, groups))
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            for l, dl in enumerate(lp):
+                hs.hs_moe_layer_decode(dl.c, X[l], LG[l], 1, Y[l], None, 0, None, WS, stream=stream)
+        K = max(20, args.steps // 4)
+        ms, _ = timed(g, K, 3, repeats=3)
+        us = ms * 1e3 / (K * n)
+        gbs = step_bytes / (ms * 1e-3 / K) / 1e9
+        out[str(p)] = {"us_per_layer": round(us, 3), "required_MB_per_layer": round(step_bytes / n / 1e6, 2),
+                       "achieved_GBs": round(gbs, 1), "frac": round(gbs / peak, 4),
+                       "live_rows_per_layer": round(float(np.mean(rows)), 1)}
+        del g, lp
     return out
 
 
@@ -460,6 +512,14 @@ def main():
     h2d = X.numel() * X.element_size() + LG.numel() * LG.element_size()
     d2h = Y.numel() * Y.element_size()
 
+    sweep = None
+    if not args.profile and not args.no_sweep:
+        sweep = bench_p_sweep(args, layers, X, LG, dev, stream, timed, bytemodel, hs, peak)
+        sweep["0.1"] = {"us_per_layer": round(us_layer, 3), "required_MB_per_layer": round(step_bytes / n / 1e6, 2),
+                        "achieved_GBs": round(achieved, 1), "frac": round(achieved / peak, 4)}
+        sweep["1.0"] = {"us_per_layer": round(us_layer_dense, 3), "note": "HS_FORCE_DENSE on the p = 0.1 inputs",
+                        "required_MB_per_layer": round(dense_bytes / 1e6, 2),
+                        "achieved_GBs": round(dense_bytes / (us_layer_dense * 1e-6) / 1e9, 1)}
     batch = None
     if not args.profile and args.batch_sizes:
         batch = bench_batch(args, dev, stream, timed, bytemodel, hs)
@@ -476,7 +536,8 @@ def main():
                          "single-threaded BLAS), median per layer"}
 
     if rank == 0:
-        src = os.path.join(ROOT, "activation_sparse_moe_gb300", "csrc", "hs_decode.cu")
+        csrc = os.path.join(ROOT, "activation_sparse_moe_gb300", "csrc")
+        src = [os.path.join(csrc, f) for f in ("hs_decode.cu", "hs_kernels.cuh", "hs_common.cuh", "hs_host.h")]
         out = {
             "metric": METRIC, "value": round(us_layer, 4), "unit": UNIT, "n_gpus": ws, "steps": K, "warmup": W,
             "ms_per_step": round(ms / K, 6), "repeats_us_per_layer": [round(r * 1e3 / (K * n), 3) for r in ms_runs],
@@ -498,6 +559,7 @@ def main():
             "live": {"rows_per_layer": round(float(np.mean(live_rows)), 1),
                      "groups_per_layer": round(float(np.mean(live_groups)), 1),
                      "required_MB_per_step": round(step_bytes / 1e6, 2)},
+            "p_sweep": sweep,
             "batch_decode": batch,
             "prefill": prefill,
             "cpu_baseline": cpu,
