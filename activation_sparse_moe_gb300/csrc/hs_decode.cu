@@ -189,6 +189,72 @@ __device__ __forceinline__ void warp0_mask_and_issue(const float* h_s, bool dens
     if (lane == 0) { *mask_out = live; *hsum_out = s; }
 }
 
+// Down phase of the fused kernel: thread j < hidden/OPT owns outputs
+// OPT*j .. OPT*j+OPT-1 (OPT = 12 when hidden is a multiple of 48, so that 224
+// threads share the work at hidden 2688; else 16) and adds the live rows in
+// ascending neuron order in one fp32 chain per output (a dead row would add
+// h * q = +0 exactly, so the dense flag, which adds every row, gives
+// identical bits), then
+//   partial_o = wgt * (s_o * sum_n h_n q_{n,o} + b_o * sum_n h_n).
+// Nibble i of a code word becomes a float by masking it in place under the
+// exponent of 2^23 and subtracting 2^23 (exact: q * 16^i < 2^23); the row's h
+// is pre-scaled by 16^-i to undo the position.
+template <int OPT>
+__device__ __forceinline__ void down_acc_and_store(const uint8_t* codes_buf, const uint32_t* sb_buf,
+                                                   const float* h_s, uint64_t live, float Hsum, float wgt,
+                                                   int rowb, int j, const PartialOut out) {
+    static_assert(OPT == 12 || OPT == 16, "12 or 16 outputs per thread");
+    float acc[OPT];
+#pragma unroll
+    for (int e = 0; e < OPT; ++e) acc[e] = 0.f;
+    while (live) {
+        const int n = __ffsll((long long)live) - 1;
+        live &= live - 1;
+        const float hn = h_s[n];
+        const float hs[5] = {hn, hn * 0.0625f, hn * 0.00390625f, hn * 0.000244140625f, hn * 1.52587890625e-05f};
+        const uint8_t* row = codes_buf + (size_t)n * rowb;
+        uint32_t w[2];
+        if (OPT == 16) {
+            const uint2 cw = *reinterpret_cast<const uint2*>(row + 8 * j);
+            w[0] = cw.x;
+            w[1] = cw.y;
+        } else if (j & 1) {  // bytes 6j .. 6j+5 start 2 bytes into a word
+            const uint32_t lo = *reinterpret_cast<const uint16_t*>(row + 6 * j);
+            const uint32_t hi = *reinterpret_cast<const uint32_t*>(row + 6 * j + 2);
+            w[0] = lo | (hi << 16);
+            w[1] = hi >> 16;
+        } else {
+            w[0] = *reinterpret_cast<const uint32_t*>(row + 6 * j);
+            w[1] = *reinterpret_cast<const uint16_t*>(row + 6 * j + 4);
+        }
+#pragma unroll
+        for (int jj = 0; jj < OPT / 8 + (OPT % 8 != 0); ++jj) {
+            const uint32_t hi = w[jj] >> 12;  // nibbles 5, 6, 7 at positions 2, 3, 4
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                if (8 * jj + i >= OPT) break;
+                const uint32_t src = i < 5 ? w[jj] : hi;
+                const int pos = i < 5 ? i : i - 3;
+                const float q = __uint_as_float((src & (15u << (4 * pos))) | 0x4B000000u) - 8388608.f;
+                acc[8 * jj + i] = fmaf(hs[pos], q, acc[8 * jj + i]);
+            }
+        }
+    }
+    const uint4* sbq = reinterpret_cast<const uint4*>(sb_buf) + (OPT / 4) * j;
+#pragma unroll
+    for (int i = 0; i < OPT / 4; ++i) {
+        const uint4 v = sbq[i];
+        const uint32_t sbw[4] = {v.x, v.y, v.z, v.w};
+        float r[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            const float2 sb = half2_to_float2(sbw[e]);
+            r[e] = wgt * fmaf(sb.x, acc[4 * i + e], sb.y * Hsum);
+        }
+        *out.quad((OPT / 4) * j + i) = make_float4(r[0], r[1], r[2], r[3]);
+    }
+}
+
 // --------------------------------------------------- fused layer kernel (B=1)
 __global__ void __launch_bounds__(256, 2)
 moe_decode_b1_kernel(const __grid_constant__ LayerParams P, const DecodeIO io) {
@@ -360,8 +426,11 @@ moe_decode_b1_kernel(const __grid_constant__ LayerParams P, const DecodeIO io) {
         return;
     }
     if (!__syncthreads_and(mbar_wait(&bars[4], 0))) return;
-    down_accumulate_and_store(codes_buf, sb_buf, reinterpret_cast<float*>(codes_buf), h_s, live, *hsum_s, wgt,
-                              hidden, out_row);
+    if (hidden % 48 == 0) {
+        if (t < hidden / 12) down_acc_and_store<12>(codes_buf, sb_buf, h_s, live, *hsum_s, wgt, rowb, t, out_row);
+    } else if (t < hidden / 16) {
+        down_acc_and_store<16>(codes_buf, sb_buf, h_s, live, *hsum_s, wgt, rowb, t, out_row);
+    }
 }
 
 // ------------------------------------------ single-expert sparse down (K1)

@@ -153,39 +153,6 @@ __device__ __forceinline__ void tma_load_2d_hint(void* dst, const CUtensorMap* m
         : "memory");
 }
 
-// Non-blocking test of an mbarrier phase.
-__device__ __forceinline__ bool mbar_test(uint64_t* bar, uint32_t parity) {
-    uint32_t ok;
-    asm volatile(
-        "{\n .reg .pred p;\n"
-        " mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n"
-        " selp.u32 %0, 1, 0, p;\n}"
-        : "=r"(ok)
-        : "r"(smem_u32(bar)), "r"(parity)
-        : "memory");
-    return ok != 0;
-}
-
-// Bounded wait that sleeps `ns` between polls, for roles whose reaction time
-// is not on the critical path (they then take few issue slots).
-__device__ __forceinline__ bool mbar_wait_sleep(uint64_t* bar, uint32_t parity, unsigned ns) {
-    if (mbar_test(bar, parity)) return true;
-    const unsigned long long t0 = clock64();
-    while (!mbar_test(bar, parity)) {
-        if (clock64() - t0 > kWaitLimitCycles) {
-            atomicOr(&g_status, 1u);
-            return false;
-        }
-        __nanosleep(ns);
-    }
-    return true;
-}
-
-// Plain arrival (count 1) on an mbarrier.
-__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
-    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
-}
-
 // Byte offset of 16-byte chunk c (0..7) of row r inside a 128-byte-swizzled tile.
 __device__ __forceinline__ uint32_t sw128_offset(int r, int c) { return (uint32_t)(r * 128 + ((c ^ (r & 7)) << 4)); }
 
