@@ -46,6 +46,11 @@ __device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t by
                  : "memory");
 }
 
+// Adds expected transaction bytes to the current phase without arriving.
+__device__ __forceinline__ void mbar_expect_tx(uint64_t* bar, uint32_t bytes) {
+    asm volatile("mbarrier.expect_tx.relaxed.cta.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(bytes) : "memory");
+}
+
 // One try: the thread may sleep in the instruction until the phase completes
 // or the suspend-time hint (10 ms) passes, so waiting warps do not spin.
 __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {

@@ -384,9 +384,14 @@ moe_decode_b1_kernel(const __grid_constant__ LayerParams P, const DecodeIO io) {
         for (int k = 0; k < 4; ++k) ok &= mbar_wait(&bars[k], 0);
     }
     if (t < 64) off_s[t] = off_r;
+    fence_proxy_async_smem();  // the partial stores come before the down copies into the same rows
     if (!__syncthreads_and(ok)) return;
 
-    // ---- row sums: thread (r, q) adds groups q, q+4, ... then a fixed 4-way tree
+    // ---- row sums: thread (r, q) adds groups q, q+4, ... then a fixed 4-way
+    // tree; the row's first thread then copies the row's down codes into the
+    // row's slot if the neuron fired (the slot's partials are consumed)
+    uint8_t* live8 = misc + SmemLayout::kLive;  // live bits of rows 8w .. 8w+7 per warp w
+    bool lv = false;
     {
         const int r = t >> 2, q = t & 3;
         float s0 = 0.f, s1 = 0.f;
@@ -408,29 +413,45 @@ moe_decode_b1_kernel(const __grid_constant__ LayerParams P, const DecodeIO io) {
                 const int base = is_shared ? 0 : P.shared_neurons + (slot - 1) * P.routed_neurons;
                 io.dbg_h[base + n] = h;
             }
+            lv = dense || h > 0.f;
+            if (lv) {
+                mbar_expect_tx(&bars[4], (uint32_t)rowb);
+                bulk_g2s(codes_buf + (size_t)r * rowb, ep.dn_codes + ((size_t)g * 64 + r) * rowb, rowb, &bars[4], pol);
+            }
+        }
+        const unsigned b = __ballot_sync(0xffffffffu, lv);  // bits at lanes 4i
+        if ((t & 31) == 0) {
+            unsigned m8 = 0;
+#pragma unroll
+            for (int i = 0; i < 8; ++i) m8 |= ((b >> (4 * i)) & 1u) << i;
+            live8[t >> 5] = (uint8_t)m8;
         }
     }
-    fence_proxy_async_smem();
-    __syncthreads();
-
-    // ---- live mask, fixed-order sum of h, down copies
-    if (t < 32)
-        warp0_mask_and_issue(h_s, dense, ep.dn_codes + (size_t)g * 64 * rowb, ep.dn_sb + (size_t)g * hidden, hidden,
-                             codes_buf, sb_buf, &bars[4], live_s, hsum_s, pol);
-    __syncthreads();
-    const uint64_t live = *live_s;
+    // the group's slab is fetched if any neuron fired; the single arrival on
+    // the down barrier comes after every row's expected bytes were added
+    const bool any = __syncthreads_or(lv) != 0;
+    if (t == 0 && any) {
+        mbar_arrive_expect_tx(&bars[4], (uint32_t)hidden * 4);
+        bulk_g2s(sb_buf, ep.dn_sb + (size_t)g * hidden, hidden * 4, &bars[4], pol);
+    }
+    const uint64_t live = *reinterpret_cast<const uint64_t*>(live8);
     const PartialOut out_row{io.partial, io.units, u};
     if (t == 0) io.live_counts[u] = __popcll(live);
-    if (!live) {
+    if (!any) {
         store_zero_row(out_row, hidden);
         return;
     }
-    if (!__syncthreads_and(mbar_wait(&bars[4], 0))) return;
-    if (hidden % 48 == 0) {
-        if (t < hidden / 12) down_acc_and_store<12>(codes_buf, sb_buf, h_s, live, *hsum_s, wgt, rowb, t, out_row);
-    } else if (t < hidden / 16) {
-        down_acc_and_store<16>(codes_buf, sb_buf, h_s, live, *hsum_s, wgt, rowb, t, out_row);
-    }
+    // fixed-order sum of the 64 h values (every warp computes the same value)
+    float Hsum = h_s[t & 31] + h_s[(t & 31) + 32];
+#pragma unroll
+    for (int off = 16; off; off >>= 1) Hsum += __shfl_xor_sync(0xffffffffu, Hsum, off);
+    const int nthr = hidden % 48 == 0 ? hidden / 12 : hidden / 16;
+    if (t >= nthr) return;
+    if (!mbar_wait(&bars[4], 0)) return;
+    if (hidden % 48 == 0)
+        down_acc_and_store<12>(codes_buf, sb_buf, h_s, live, Hsum, wgt, rowb, t, out_row);
+    else
+        down_acc_and_store<16>(codes_buf, sb_buf, h_s, live, Hsum, wgt, rowb, t, out_row);
 }
 
 // ------------------------------------------ single-expert sparse down (K1)
