@@ -16,10 +16,11 @@
 //             for the integer-pipe GEMV (all threads).
 //  2. plan:   one CTA: pair offsets, (token, slot) pairs grouped by expert in
 //             token order, work-unit tables, zeroed union masks.
-//  3. up:     persistent CTAs over units (expert, 32 neuron rows, <= 4 tokens),
-//             the next unit's bulk copies in flight while the current one is
-//             computed: DP4A fixed-point GEMV per token, ReLU^2, h to global,
-//             union live bits OR-ed into a per-(expert, 32 rows) mask word.
+//  3. up:     four persistent CTAs per SM over units (expert, 32 neuron rows,
+//             <= 2 tokens) handed out by an atomic ticket, shared expert first:
+//             two chunked bulk copies per unit, DP4A fixed-point
+//             GEMV per token, ReLU^2, h to global, union live bits OR-ed into
+//             per-(expert, 32 rows) mask words.
 //  4. down:   persistent CTAs over units (expert or shared-expert row chunk,
 //             128-output band): the union live rows' band slices (and the
 //             scale slabs of their groups) staged by asynchronous copies, two
@@ -30,18 +31,24 @@
 
 namespace hs {
 
-constexpr int kTC = 4;          // tokens per up unit
+constexpr int kTC = 2;          // tokens per up unit
+constexpr int kUpRows = 32;     // neuron rows per up unit (two 16-row chunks)
+constexpr int kUpThreads = 128; // threads of an up CTA
+constexpr int kUpCtasPerSm = 4;
 constexpr int kMaxBatch = 64;
 constexpr int kBand = 128;      // outputs per down unit
 constexpr int kMaxShChunks = 8; // shared-expert row chunks in the down pass
 
 // Row chunks of the shared expert's down product: the shared expert has every
-// token of the batch, so its work is split into ranges of rows.
-__host__ __device__ inline int shared_chunks(int B) { return min(kMaxShChunks, (B + 7) / 8); }
+// token of the batch and the widest union of live rows, so its work is split
+// into ranges of rows (each a separate work item with its own partial rows).
+__host__ __device__ inline int shared_chunks(int B) { return B > 0 ? kMaxShChunks : 0; }
 
 struct BatchMeta {
     int cnt[kMaxRouted];            // pairs per expert (route kernel, atomics)
     int n_pairs, n_touched, up_units, dn_units, n_items;
+    int up_shared;                  // shared-expert up units (numbered first)
+    int up_next;                    // next up unit to hand out (atomic ticket)
     int touched[kMaxRouted];        // routed experts with tokens, ascending
     int e_off[kMaxRouted + 1];      // grouped pair offsets per expert id
     int up_off[kMaxRouted + 2];     // up unit offsets per touched index (+ shared)
@@ -128,7 +135,7 @@ __global__ void __launch_bounds__(512) batch_plan_kernel(const __grid_constant__
     BatchMeta* m = io.meta;
     for (int p = t; p < npair; p += blockDim.x) s_idx[p] = io.topk_idx[p];
     // offsets, touched experts and unit offsets: block scans over the experts (thread e)
-    const int HGr = P.routed_neurons / 32;
+    const int HGr = P.routed_neurons / kUpRows;
     const int c = t < E ? __ldcg(&m->cnt[t]) : 0;
     const int touched = c > 0 ? 1 : 0;
     const int units = ((c + kTC - 1) / kTC) * HGr;
@@ -151,11 +158,12 @@ __global__ void __launch_bounds__(512) batch_plan_kernel(const __grid_constant__
         s_off[E] = tot[0];
         m->e_off[E] = tot[0];
         m->up_off[nt] = un;
-        if (P.shared_neurons) un += ((B + kTC - 1) / kTC) * (P.shared_neurons / 32);
-        m->up_off[nt + 1] = un;
+        const int su = P.shared_neurons ? ((B + kTC - 1) / kTC) * (P.shared_neurons / kUpRows) : 0;
+        m->up_off[nt + 1] = un + su;
         m->n_pairs = npair;
         m->n_touched = nt;
-        m->up_units = un;
+        m->up_units = un + su;
+        m->up_shared = su;
         m->n_items = nt + (P.shared_neurons ? shared_chunks(B) : 0);
         m->dn_units = m->n_items * (P.hidden / kBand);
     }
@@ -177,24 +185,20 @@ __global__ void __launch_bounds__(512) batch_plan_kernel(const __grid_constant__
 }
 
 // ------------------------------------------------------------------ up
-// Unit stage of the weight ring: 32 rows of codes and their (scale, bias)
-// pairs.  Three stages: two units' copies are in flight while one is computed.
-// The x tables (L2-resident, a few KB per token) are read straight into
-// registers one unit ahead.
-constexpr int kUpStages = 3;
+// Unit = (expert, kUpRows neurons, up to kTC of the expert's tokens).  Four
+// small CTAs per SM, each working through units in turn: the unit's up rows
+// are bulk-copied in 16-row chunks (scales with the first) so the dot
+// products start on the first chunk while the rest is in flight, and the
+// other CTAs of the SM compute while this one waits.
 struct BatchUpSmem {
-    __host__ __device__ static int codes(int H) { return 32 * (H / 2); }
-    __host__ __device__ static int sb(int H) { return 32 * (H / 64) * 4; }
-    __host__ __device__ static int stage(int H) { return codes(H) + sb(H); }
-    // parts row stride: 1 mod 32 words, so row-sum loads (lane = row) are conflict-free
-    __host__ __device__ static int pstride(int H) { return ((H / 64 + 31) / 32) * 32 + 1; }
-    __host__ __device__ static int parts(int H) { return kTC * 32 * pstride(H) * 4; }
+    __host__ __device__ static int codes(int H) { return kUpRows * (H / 2); }
+    __host__ __device__ static int sb(int H) { return kUpRows * (H / 64) * 4; }
     __host__ __device__ static int total(int H);
 };
 
 struct UpUnitDesc {
     bool shared;
-    int e, c, hg, T, pbase, N, HG;
+    int e, c, g, T, pbase, N, NG;
     ExpertPtrs ep;
 };
 
@@ -206,7 +210,7 @@ struct MetaTables {
 };
 
 __host__ __device__ inline int BatchUpSmem::total(int H) {
-    return kUpStages * stage(H) + parts(H) + 64 + (int)sizeof(MetaTables) + 32 * 4;
+    return codes(H) + sb(H) + 64 + (int)sizeof(MetaTables) + kUpRows * 4;
 }
 
 __device__ __forceinline__ void load_tables(const BatchMeta* m, int nt, int E, MetaTables* s) {
@@ -225,16 +229,18 @@ __device__ __forceinline__ int unit_owner(const int* off, int n, int u) {
     return lo;
 }
 
+// Units 0 .. su-1 are the shared expert's (the heaviest, handed out first),
+// then the routed experts' in the order of the unit table.
 __device__ __forceinline__ UpUnitDesc up_unit_desc(const LayerParams& P, const BatchIO& io, const MetaTables* tb, int nt,
-                                                   int u) {
+                                                   int su, int u) {
     UpUnitDesc d;
-    const int i = unit_owner(tb->up_off, nt + 1, u);
-    d.shared = (i == nt);
+    d.shared = u < su;
+    const int i = d.shared ? nt : unit_owner(tb->up_off, nt, u - su);
     d.N = d.shared ? P.shared_neurons : P.routed_neurons;
-    d.HG = d.N / 32;
-    const int local = u - tb->up_off[i];
-    d.c = local / d.HG;
-    d.hg = local % d.HG;
+    d.NG = d.N / kUpRows;
+    const int local = d.shared ? u : u - su - tb->up_off[i];
+    d.c = local / d.NG;
+    d.g = local % d.NG;
     if (d.shared) {
         d.e = -1;
         d.ep = P.shared;
@@ -249,148 +255,156 @@ __device__ __forceinline__ UpUnitDesc up_unit_desc(const LayerParams& P, const B
     return d;
 }
 
-// This thread's role in a unit of T tokens: (group gc, token tk, row slice rs of RS).
+// This thread's role in a unit of T <= 2 tokens: token lane tk (the TL lanes
+// of one scale group are adjacent in a warp), group gc, row lane rs of RS.
 struct UpRole {
-    int gc, tk, rs, RS;
-    bool active;
+    int tk, gc, rs, RS, TL;
+    bool active;  // owns (token, group) work
 };
 __device__ __forceinline__ UpRole up_role(int T, int G) {
     UpRole r;
     const int t = threadIdx.x;
-    r.RS = 6 / T;  // 6, 3, 2, 1 row slices for 1..4 tokens: up to 252 threads busy
-    r.gc = t % G;
-    const int rest = t / G;
-    r.tk = rest % T;
-    r.rs = rest / T;
-    r.active = rest < T * r.RS;
+    r.TL = T == 1 ? 1 : 2;
+    r.RS = kUpThreads / (r.TL * G);
+    r.tk = t % r.TL;
+    r.gc = (t / r.TL) % G;
+    r.rs = t / (r.TL * G);
+    r.active = r.rs < r.RS && r.tk < T;
     return r;
 }
 
-// The x table of this thread's (token, group) of a unit, from global memory.
-__device__ __forceinline__ void load_unit_x(const BatchIO& io, const UpUnitDesc& d, const UpRole& r, int G, XFixed& xf) {
-    if (!r.active) return;
-    const int tok = d.shared ? d.pbase + r.tk : __ldcg(io.pair_tok + d.pbase + r.tk);
-    load_x_fixed(io.xt + (size_t)tok * G * kXfStride, io.xsc + (size_t)tok * G * 2, r.gc, xf);
+// Where the dot product of (row r, group gc, token lane tk) is left: word
+// (tk + gc/4 + r) % 8 of the group's own 32-byte code block, once every lane
+// of the group has read the codes.
+__device__ __forceinline__ float* up_part(uint8_t* codes, int rowb, int r, int gc, int tk) {
+    return reinterpret_cast<float*>(codes + r * rowb + 32 * gc + 4 * ((tk + (gc >> 2) + r) & 7));
 }
 
-__global__ void __launch_bounds__(256, 1) batch_up_kernel(const __grid_constant__ LayerParams P, const BatchIO io) {
+__global__ void __launch_bounds__(kUpThreads, kUpCtasPerSm) batch_up_kernel(const __grid_constant__ LayerParams P, const BatchIO io) {
     extern __shared__ __align__(128) uint8_t smem[];
     const int H = P.hidden, G = H / 64, rowb = H / 2;
-    const int stage_bytes = BatchUpSmem::stage(H);
-    float* parts = reinterpret_cast<float*>(smem + kUpStages * stage_bytes);  // [kTC][32][pstride]
-    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kUpStages * stage_bytes + BatchUpSmem::parts(H));
+    uint8_t* codes = smem;
+    uint32_t* sbs = reinterpret_cast<uint32_t*>(smem + BatchUpSmem::codes(H));
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + BatchUpSmem::codes(H) + BatchUpSmem::sb(H));
     MetaTables* tb = reinterpret_cast<MetaTables*>(bars + 8);
-    float* offs_s = reinterpret_cast<float*>(tb + 1);   // [32] offsets of the current unit's rows
-    const int t = threadIdx.x;
+    float* offs_s = reinterpret_cast<float*>(tb + 1);  // [kUpRows] offsets of the unit's rows
+    int* ticket_s = reinterpret_cast<int*>(bars + 4);   // the next unit of this CTA
+    const int t = threadIdx.x, lane = t & 31;
     const bool dense = (io.flags & HS_FORCE_DENSE) != 0;
     if (t == 0) {
-        for (int i = 0; i < kUpStages; ++i) mbar_init(&bars[i], 1);
+        for (int i = 0; i < kUpRows / 16; ++i) mbar_init(&bars[i], 1);
         fence_mbar_init();
     }
     __syncthreads();
     pdl_wait();
     pdl_trigger();
-    const BatchMeta* m = io.meta;
-    const int U = __ldcg(&m->up_units), nt = __ldcg(&m->n_touched);
-    const int pstride = BatchUpSmem::pstride(H);
+    BatchMeta* m = io.meta;
+    const int U = __ldcg(&m->up_units), nt = __ldcg(&m->n_touched), su = __ldcg(&m->up_shared);
     load_tables(m, nt, P.n_routed, tb);
+    // units are handed out one at a time (heaviest first), so CTAs that drew
+    // compute-heavy units take fewer of them
+    if (t == 0) *ticket_s = atomicAdd(&m->up_next, 1);
     __syncthreads();
-
-    auto codes_of = [&](int b) { return smem + b * stage_bytes; };
-    auto sb_of = [&](int b) { return reinterpret_cast<uint32_t*>(smem + b * stage_bytes + BatchUpSmem::codes(H)); };
-    // thread 0 issues one unit's weight copies into stage b
-    auto issue = [&](const UpUnitDesc& d, int b) {
-        const uint64_t pol = policy_evict_first();
-        mbar_arrive_expect_tx(&bars[b], 32 * rowb + 32 * G * 4);
-        bulk_g2s(codes_of(b), d.ep.up_codes + (size_t)(32 * d.hg) * rowb, 32 * rowb, &bars[b], pol);
-        bulk_g2s(sb_of(b), d.ep.up_sb + (size_t)(32 * d.hg) * G, 32 * G * 4, &bars[b], pol);
-    };
-    const int u0 = blockIdx.x;
-    if (u0 >= U) return;
-    UpUnitDesc cur = up_unit_desc(P, io, tb, nt, u0);
-    if (t == 0) {
-        issue(cur, 0);
-        if (u0 + (int)gridDim.x < U) issue(up_unit_desc(P, io, tb, nt, u0 + gridDim.x), 1);
-    }
-    UpRole role = up_role(cur.T, G);
-    XFixed xcur;
-    load_unit_x(io, cur, role, G, xcur);
-    float off_cur = 0.f;
-    if (t < 32) off_cur = cur.ep.up_off ? __ldg(cur.ep.up_off + 32 * cur.hg + t) : 0.f;
-    uint32_t phases = 0u;  // bit b: parity of stage b's next phase
-    int it = 0;
-    for (int u = u0; u < U; u += gridDim.x, ++it) {
-        const int b = it % kUpStages;
-        // copies two units ahead go into the stage the previous unit used
-        const int u2 = u + 2 * (int)gridDim.x;
-        if (t == 0 && u2 < U) issue(up_unit_desc(P, io, tb, nt, u2), (it + 2) % kUpStages);
-        // the next unit's x tables and offsets, into registers (used next iteration)
-        const int u1 = u + gridDim.x;
-        UpUnitDesc nxt = cur;
-        UpRole role_n = role;
-        XFixed xnext = xcur;
-        float off_next = 0.f;
-        if (u1 < U) {
-            nxt = up_unit_desc(P, io, tb, nt, u1);
-            role_n = up_role(nxt.T, G);
-            load_unit_x(io, nxt, role_n, G, xnext);
-            if (t < 32) off_next = nxt.ep.up_off ? __ldg(nxt.ep.up_off + 32 * nxt.hg + t) : 0.f;
+    const uint64_t pol = policy_evict_first();
+    for (int it = 0;; ++it) {
+        const int u = *ticket_s;
+        if (u >= U) break;
+        const UpUnitDesc d = up_unit_desc(P, io, tb, nt, su, u);
+        const uint32_t par = it & 1;
+        __syncthreads();  // every thread has read the ticket before the next one lands
+        // the next ticket, fetched while this unit streams (read after the unit's last barrier)
+        if (t == blockDim.x - 1) *ticket_s = atomicAdd(&m->up_next, 1);
+        if (t == 0) {
+            const uint8_t* src = d.ep.up_codes + (size_t)d.g * kUpRows * rowb;
+            const uint32_t chunk = 16 * rowb;
+            mbar_arrive_expect_tx(&bars[0], chunk + kUpRows * G * 4);
+            bulk_g2s(sbs, d.ep.up_sb + (size_t)d.g * kUpRows * G, kUpRows * G * 4, &bars[0], pol);
+            bulk_g2s(codes, src, chunk, &bars[0], pol);
+            for (int k = 1; k < kUpRows / 16; ++k) {
+                mbar_arrive_expect_tx(&bars[k], chunk);
+                bulk_g2s(codes + k * chunk, src + (size_t)k * chunk, chunk, &bars[k], pol);
+            }
         }
-        // offsets of this unit's rows (prefetched by warp 0), read after the barrier below
-        if (t < 32) offs_s[t] = off_cur;
-        const bool ok = mbar_wait(&bars[b], (phases >> b) & 1u);
-        phases ^= 1u << b;
-        if (!__syncthreads_and(ok)) return;
-        // ---- dot products: thread (gc, tk, rs) over rows rs, rs + RS, ...
+        const UpRole role = up_role(d.T, G);
+        XFixed xf = {};
         if (role.active) {
-            float* pp = parts + (size_t)role.tk * 32 * pstride;
-            const uint8_t* cb = codes_of(b);
-            const uint32_t* sbb = sb_of(b);
-            // two rows at a time: independent DP4A chains hide the pipe latency
-            for (int r = role.rs; r < 32; r += 2 * role.RS) {
-                const int r2 = r + role.RS;
-                const bool two = r2 < 32;
-                uint4 a0, a1, b0 = make_uint4(0, 0, 0, 0), b1 = make_uint4(0, 0, 0, 0);
-                load_group_codes(cb + r * rowb, role.gc, a0, a1);
-                if (two) load_group_codes(cb + r2 * rowb, role.gc, b0, b1);
-                const int da = group_dot_fixed16(a0, a1, xcur);
-                const int db = group_dot_fixed16(b0, b1, xcur);
-                const float2 sa = half2_to_float2(sbb[r * G + role.gc]);
-                pp[r * pstride + role.gc] = fmaf(sa.x * xcur.inv, (float)da, sa.y * xcur.xsum);
+            const int tok = d.shared ? d.pbase + role.tk : __ldcg(io.pair_tok + d.pbase + role.tk);
+            load_x_fixed(io.xt + (size_t)tok * G * kXfStride, io.xsc + (size_t)tok * G * 2, role.gc, xf);
+        }
+        if (t < kUpRows) offs_s[t] = d.ep.up_off ? __ldg(d.ep.up_off + kUpRows * d.g + t) : 0.f;
+        // ---- dot products: rows rs, rs + RS, ... two at a time, chunk by chunk.
+        // Every thread runs the same number of steps (the warp synchronises
+        // inside); threads without a row in a step only keep step.
+        bool ok = true;
+        int waited = -1;
+        const int n_steps = (kUpRows + 2 * role.RS - 1) / (2 * role.RS);
+        for (int i = 0; i < n_steps; ++i) {
+            const int r = role.rs + 2 * role.RS * i, r2 = r + role.RS;
+            const bool act = role.rs < role.RS && r < kUpRows;
+            const bool two = act && r2 < kUpRows;
+            if (act) {
+                const int k = (two ? r2 : r) >> 4;
+                while (ok && waited < k) { ++waited; ok = mbar_wait(&bars[waited], par); }
+            }
+            uint4 a0 = make_uint4(0, 0, 0, 0), a1 = a0, b0 = a0, b1 = a0;
+            uint32_t sw0 = 0, sw1 = 0;
+            if (act && ok) {
+                load_group_codes(codes + r * rowb, role.gc, a0, a1);
+                sw0 = sbs[r * G + role.gc];
                 if (two) {
-                    const float2 sbv = half2_to_float2(sbb[r2 * G + role.gc]);
-                    pp[r2 * pstride + role.gc] = fmaf(sbv.x * xcur.inv, (float)db, sbv.y * xcur.xsum);
+                    load_group_codes(codes + r2 * rowb, role.gc, b0, b1);
+                    sw1 = sbs[r2 * G + role.gc];
+                }
+            }
+            const int da = group_dot_fixed16(a0, a1, xf);
+            const int db = group_dot_fixed16(b0, b1, xf);
+            // the token lanes of a group have all read its codes before any part lands there
+            __syncwarp();
+            if (act && ok && role.active) {
+                const float2 sa = half2_to_float2(sw0);
+                *up_part(codes, rowb, r, role.gc, role.tk) = fmaf(sa.x * xf.inv, (float)da, sa.y * xf.xsum);
+                if (two) {
+                    const float2 sbv = half2_to_float2(sw1);
+                    *up_part(codes, rowb, r2, role.gc, role.tk) = fmaf(sbv.x * xf.inv, (float)db, sbv.y * xf.xsum);
                 }
             }
         }
-        __syncthreads();
-        // ---- row sums, ReLU^2, h out, union live bits (warp w: token w; lane = row)
-        {
-            const int lane = t & 31, w = t >> 5;
-            if (w < cur.T) {
-                const float* pp = parts + (size_t)w * 32 * pstride + lane * pstride;
-                // four independent chains over the groups (G is even), then a fixed combination
-                float s0 = 0.f, s1 = 0.f, s2 = 0.f, s3 = 0.f;
-                int g = 0;
-                for (; g + 3 < G; g += 4) { s0 += pp[g]; s1 += pp[g + 1]; s2 += pp[g + 2]; s3 += pp[g + 3]; }
-                if (g < G) { s0 += pp[g]; s1 += pp[g + 1]; }
-                const float z = ((s0 + s1) + (s2 + s3)) + offs_s[lane];
-                const float h = z > 0.f ? z * z : 0.f;
-                const int n = 32 * cur.hg + lane;
-                if (cur.shared) io.h_sh[(size_t)(cur.pbase + w) * cur.N + n] = h;
-                else io.h_pair[(size_t)(cur.pbase + w) * cur.N + n] = h;
-                const uint32_t anyl = __ballot_sync(0xffffffffu, h > 0.f);
-                if (lane == 0 && (anyl || dense)) {
-                    uint32_t* mw = cur.shared ? io.mask_s + cur.hg : io.mask_r + (size_t)cur.e * cur.HG + cur.hg;
-                    atomicOr(mw, dense ? 0xffffffffu : anyl);
-                }
+        while (ok && waited < kUpRows / 16 - 1) { ++waited; ok = mbar_wait(&bars[waited], par); }
+        if (!__syncthreads_and(ok)) return;
+        // ---- row sums, ReLU^2, h out, union live bits: pass pt covers (row, token) pairs
+        // (row t/4, token pt); four threads per pair add groups q, q+4, ... in two chains
+        for (int pt = 0; pt < d.T; ++pt) {
+            const int r = (t >> 2), q = t & 3, tk = pt;
+            float s0 = 0.f, s1 = 0.f;
+            int cc = q;
+            for (; cc + 4 < G; cc += 8) {
+                s0 += *up_part(codes, rowb, r, cc, tk);
+                s1 += *up_part(codes, rowb, r, cc + 4, tk);
+            }
+            if (cc < G) s0 += *up_part(codes, rowb, r, cc, tk);
+            float sum = s0 + s1;
+            sum += __shfl_xor_sync(0xffffffffu, sum, 1);
+            sum += __shfl_xor_sync(0xffffffffu, sum, 2);
+            const float z = sum + offs_s[r];
+            const float h = z > 0.f ? z * z : 0.f;
+            const int n = kUpRows * d.g + r;
+            if (q == 0) {
+                if (d.shared) io.h_sh[(size_t)(d.pbase + tk) * d.N + n] = h;
+                else io.h_pair[(size_t)(d.pbase + tk) * d.N + n] = h;
+            }
+            const unsigned bl = __ballot_sync(0xffffffffu, q == 0 && (dense || h > 0.f));
+            if (lane == 0 && bl) {
+                unsigned m8 = 0;
+#pragma unroll
+                for (int i = 0; i < 8; ++i) m8 |= ((bl >> (4 * i)) & 1u) << i;
+                // this warp's 8 rows: r = 8 (t / 32) .. + 7 of the unit
+                const int r8 = kUpRows * d.g + 8 * (t >> 5);
+                uint32_t* mw = d.shared ? io.mask_s + (r8 >> 5) : io.mask_r + (size_t)d.e * (d.N / 32) + (r8 >> 5);
+                atomicOr(mw, m8 << (r8 & 31));
             }
         }
-        __syncthreads();  // parts, the offsets and this stage are reused
-        cur = nxt;
-        role = role_n;
-        xcur = xnext;
-        off_cur = off_next;
+        fence_proxy_async_smem();  // the parts in the code buffer come before the next unit's copies
+        __syncthreads();           // the code buffer, the parts and the offsets are reused by the next unit
     }
 }
 
@@ -836,7 +850,8 @@ int hs_batch_decode(const hs_moe_layer* L, const uint16_t* x, const float* logit
     hs::batch_route_kernel<<<dim3(batch), dim3(256), 0, s>>>(P, io);
     if (cudaGetLastError() != cudaSuccess) return HS_ERR_CUDA;
     if (launch_pdl(hs::batch_plan_kernel, dim3(1), dim3(512), 0, s, P, io) != cudaSuccess) return HS_ERR_CUDA;
-    if (launch_pdl(hs::batch_up_kernel, dim3(sms), dim3(256), up_smem, s, P, io) != cudaSuccess) return HS_ERR_CUDA;
+    if (launch_pdl(hs::batch_up_kernel, dim3(hs::kUpCtasPerSm * sms), dim3(hs::kUpThreads), up_smem, s, P, io) != cudaSuccess)
+        return HS_ERR_CUDA;
     if (launch_pdl(hs::batch_down_kernel, dim3(2 * sms), dim3(256), dn_smem, s, P, io) != cudaSuccess)
         return HS_ERR_CUDA;
     const int nred = (batch * (L->hidden / 4) + 255) / 256;
