@@ -35,6 +35,8 @@ constexpr int kTC = 2;          // tokens per up unit
 constexpr int kUpRows = 32;     // neuron rows per up unit (two 16-row chunks)
 constexpr int kUpThreads = 128; // threads of an up CTA
 constexpr int kUpCtasPerSm = 4;
+constexpr int kFusedMaxBatch = 8;  // batches up to this size take the fused path
+constexpr int kFTok = 4;            // tokens per fused unit
 constexpr int kMaxBatch = 64;
 constexpr int kBand = 128;      // outputs per down unit
 constexpr int kMaxShChunks = 8; // shared-expert row chunks in the down pass
@@ -49,6 +51,8 @@ struct BatchMeta {
     int n_pairs, n_touched, up_units, dn_units, n_items;
     int up_shared;                  // shared-expert up units (numbered first)
     int up_next;                    // next up unit to hand out (atomic ticket)
+    int fu_off[kMaxRouted + 1];     // fused-path unit offsets per touched index
+    int fu_units, fu_shared, fu_next;
     int touched[kMaxRouted];        // routed experts with tokens, ascending
     int e_off[kMaxRouted + 1];      // grouped pair offsets per expert id
     int up_off[kMaxRouted + 2];     // up unit offsets per touched index (+ shared)
@@ -126,7 +130,7 @@ __global__ void __launch_bounds__(512) batch_plan_kernel(const __grid_constant__
     __shared__ int s_idx[kMaxBatch * kMaxTopK];
     __shared__ int s_off[kMaxRouted + 1];
     __shared__ int tmp[32];
-    __shared__ int tot[3];
+    __shared__ int tot[4];
     pdl_wait();
     pdl_trigger();
     const int t = threadIdx.x;
@@ -142,15 +146,18 @@ __global__ void __launch_bounds__(512) batch_plan_kernel(const __grid_constant__
     const int c_in = block_incl_sum(c, tmp);
     const int t_in = block_incl_sum(touched, tmp);
     const int u_in = block_incl_sum(units, tmp);
+    const int funits = ((c + kFTok - 1) / kFTok) * (P.routed_neurons / 64);
+    const int f_in = block_incl_sum(funits, tmp);
     if (t < E) {
         s_off[t] = c_in - c;
         m->e_off[t] = c_in - c;
         if (touched) {
             m->touched[t_in - 1] = t;
             m->up_off[t_in - 1] = u_in - units;
+            m->fu_off[t_in - 1] = f_in - funits;
         }
     }
-    if (t == E - 1) { tot[0] = c_in; tot[1] = t_in; tot[2] = u_in; }
+    if (t == E - 1) { tot[0] = c_in; tot[1] = t_in; tot[2] = u_in; tot[3] = f_in; }
     __syncthreads();
     if (t == 0) {
         const int nt = tot[1];
@@ -166,6 +173,10 @@ __global__ void __launch_bounds__(512) batch_plan_kernel(const __grid_constant__
         m->up_shared = su;
         m->n_items = nt + (P.shared_neurons ? shared_chunks(B) : 0);
         m->dn_units = m->n_items * (P.hidden / kBand);
+        const int fsu = P.shared_neurons ? ((B + kFTok - 1) / kFTok) * (P.shared_neurons / 64) : 0;
+        m->fu_off[nt] = tot[3];
+        m->fu_shared = fsu;
+        m->fu_units = tot[3] + fsu;
     }
     __syncthreads();
     // place pairs: tokens ascending within an expert (pair order is token-major)
@@ -716,6 +727,393 @@ __global__ void __launch_bounds__(256) batch_down_kernel(const __grid_constant__
     }
 }
 
+// ------------------------------------------------------------------ fused (B <= 8)
+// For a few tokens the whole expert product runs per unit (expert, 64-neuron
+// group, up to kFTok of the expert's tokens), as in the batch-1 kernel: the
+// group's 64 up rows stream in four chunked bulk copies, the DP4A GEMV runs
+// per token, four threads per row add the row's partial sums for every
+// token, and the first of them copies the row's down codes once if the row
+// fired for ANY token (the union of the tokens' live rows, each read once);
+// the group's slab follows if any row fired.  Thread j then owns OPT outputs
+// of every token and adds the union rows in ascending order (one fp32 chain
+// per (token, output); a row dead for one token adds h * q = +0 for it), and
+// writes one partial row per (token, slot, group).  A second kernel adds each
+// token's partial rows in a fixed order.
+struct FusedTables {
+    int fu_off[kMaxRouted + 1];
+    int touched[kMaxRouted];
+    int e_off[kMaxRouted + 1];
+};
+struct FusedSmem {
+    // misc: h[kFTok][64] f32, off[64] f32, bars[8] u64, ticket, live bits u64, tables
+    static constexpr int kHs = 0, kOffs = kFTok * 64 * 4, kBarsOff = kOffs + 256, kTicket = kBarsOff + 64,
+                         kLive = kTicket + 8, kTables = kLive + 8;
+    __host__ __device__ static int codes(int H) { return 64 * (H / 2); }
+    __host__ __device__ static int sb(int H) { return H * 4; }  // up scales of 64 rows, then the down slab
+    __host__ __device__ static int misc(int H) { return codes(H) + sb(H); }
+    __host__ __device__ static int total(int H) { return misc(H) + kTables + (int)sizeof(FusedTables); }
+};
+
+// Partial row of (token b, row ri) in the fused layout [B][H/32][Ut][32].
+struct FusedOut {
+    float* base;
+    int Ut, H;
+    __device__ __forceinline__ float4* quad(int b, int ri, int o4) const {
+        return reinterpret_cast<float4*>(base + (size_t)b * H * Ut + ((size_t)(o4 >> 3) * Ut + ri) * 32) + (o4 & 7);
+    }
+};
+
+template <int OPT>
+__device__ __forceinline__ void fused_down(const uint8_t* codes, const uint32_t* sb, const float* h_s, uint64_t live,
+                                           const float (&Hsum)[kFTok], const float (&wgt)[kFTok],
+                                           const int (&tok)[kFTok], const int (&ri)[kFTok], int T, int rowb, int j,
+                                           const FusedOut& out) {
+    float acc[kFTok][OPT];
+#pragma unroll
+    for (int k = 0; k < kFTok; ++k)
+#pragma unroll
+        for (int e = 0; e < OPT; ++e) acc[k][e] = 0.f;
+    while (live) {
+        const int n = __ffsll((long long)live) - 1;
+        live &= live - 1;
+        const uint8_t* row = codes + (size_t)n * rowb;
+        uint32_t w[2];
+        if (OPT == 16) {
+            const uint2 cw = *reinterpret_cast<const uint2*>(row + 8 * j);
+            w[0] = cw.x;
+            w[1] = cw.y;
+        } else if (j & 1) {
+            const uint32_t lo = *reinterpret_cast<const uint16_t*>(row + 6 * j);
+            const uint32_t hi = *reinterpret_cast<const uint32_t*>(row + 6 * j + 2);
+            w[0] = lo | (hi << 16);
+            w[1] = hi >> 16;
+        } else {
+            w[0] = *reinterpret_cast<const uint32_t*>(row + 6 * j);
+            w[1] = *reinterpret_cast<const uint16_t*>(row + 6 * j + 4);
+        }
+        float hs[kFTok][5];
+#pragma unroll
+        for (int k = 0; k < kFTok; ++k) {
+            const float hn = k < T ? h_s[k * 64 + n] : 0.f;
+            hs[k][0] = hn; hs[k][1] = hn * 0.0625f; hs[k][2] = hn * 0.00390625f;
+            hs[k][3] = hn * 0.000244140625f; hs[k][4] = hn * 1.52587890625e-05f;
+        }
+#pragma unroll
+        for (int jj = 0; jj < OPT / 8 + (OPT % 8 != 0); ++jj) {
+            const uint32_t hi = w[jj] >> 12;  // nibbles 5, 6, 7 at positions 2, 3, 4
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                if (8 * jj + i >= OPT) break;
+                const uint32_t src = i < 5 ? w[jj] : hi;
+                const int pos = i < 5 ? i : i - 3;
+                const float q = __uint_as_float((src & (15u << (4 * pos))) | 0x4B000000u) - 8388608.f;
+#pragma unroll
+                for (int k = 0; k < kFTok; ++k)
+                    if (k < T) acc[k][8 * jj + i] = fmaf(hs[k][pos], q, acc[k][8 * jj + i]);
+            }
+        }
+    }
+    const uint4* sbq = reinterpret_cast<const uint4*>(sb) + (OPT / 4) * j;
+#pragma unroll
+    for (int i = 0; i < OPT / 4; ++i) {
+        const uint4 v = sbq[i];
+        const uint32_t sbw[4] = {v.x, v.y, v.z, v.w};
+        float2 sbf[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) sbf[e] = half2_to_float2(sbw[e]);
+#pragma unroll
+        for (int k = 0; k < kFTok; ++k) {
+            if (k < T) {
+                float r[4];
+#pragma unroll
+                for (int e = 0; e < 4; ++e) r[e] = wgt[k] * fmaf(sbf[e].x, acc[k][4 * i + e], sbf[e].y * Hsum[k]);
+                *out.quad(tok[k], ri[k], (OPT / 4) * j + i) = make_float4(r[0], r[1], r[2], r[3]);
+            }
+        }
+    }
+}
+
+__global__ void __launch_bounds__(256, 2) batch_fused_kernel(const __grid_constant__ LayerParams P, const BatchIO io) {
+    extern __shared__ __align__(128) uint8_t smem[];
+    using S = FusedSmem;
+    const int H = P.hidden, G = H / 64, rowb = H / 2;
+    uint8_t* codes = smem;
+    uint32_t* sbs = reinterpret_cast<uint32_t*>(smem + S::codes(H));
+    uint8_t* misc = smem + S::misc(H);
+    float* h_s = reinterpret_cast<float*>(misc + S::kHs);  // [kFTok][64]
+    float* offs_s = reinterpret_cast<float*>(misc + S::kOffs);
+    uint64_t* bars = reinterpret_cast<uint64_t*>(misc + S::kBarsOff);  // 4 up chunks, down
+    int* ticket_s = reinterpret_cast<int*>(misc + S::kTicket);
+    uint8_t* live8 = misc + S::kLive;
+    FusedTables* tb = reinterpret_cast<FusedTables*>(misc + S::kTables);
+    const int t = threadIdx.x, lane = t & 31;
+    const bool dense = (io.flags & HS_FORCE_DENSE) != 0;
+    if (t == 0) {
+        for (int i = 0; i < 5; ++i) mbar_init(&bars[i], 1);
+        fence_mbar_init();
+    }
+    __syncthreads();
+    pdl_wait();
+    pdl_trigger();
+    BatchMeta* m = io.meta;
+    const int U = __ldcg(&m->fu_units), nt = __ldcg(&m->n_touched), su = __ldcg(&m->fu_shared);
+    for (int i = t; i <= nt; i += blockDim.x) tb->fu_off[i] = __ldcg(&m->fu_off[i]);
+    for (int i = t; i < nt; i += blockDim.x) tb->touched[i] = __ldcg(&m->touched[i]);
+    for (int i = t; i <= P.n_routed; i += blockDim.x) tb->e_off[i] = __ldcg(&m->e_off[i]);
+    if (t == 0) *ticket_s = atomicAdd(&m->fu_next, 1);
+    __syncthreads();
+    const int NGs = P.shared_neurons / 64, NGr = P.routed_neurons / 64;
+    const int Ut = NGs + P.top_k * NGr;  // partial rows per token
+    const FusedOut out{io.partial, Ut, H};
+    const int nthr = H % 48 == 0 ? H / 12 : H / 16;
+    const uint64_t pol = policy_evict_first();
+    uint32_t dn_par = 0;
+    for (int it = 0;; ++it) {
+        const int u = *ticket_s;
+        if (u >= U) break;
+        // ---- the unit: expert, group g, tokens pbase .. pbase + T - 1 of the expert's list
+        const bool shared = u < su;
+        int g, T, pbase, e = -1;
+        ExpertPtrs ep;
+        if (shared) {
+            const int c = u / NGs;
+            g = u % NGs;
+            pbase = c * kFTok;
+            T = min(kFTok, io.batch - pbase);
+            ep = P.shared;
+        } else {
+            const int i = unit_owner(tb->fu_off, nt, u - su);
+            const int local = u - su - tb->fu_off[i];
+            g = local % NGr;
+            e = tb->touched[i];
+            pbase = tb->e_off[e] + (local / NGr) * kFTok;
+            T = min(kFTok, tb->e_off[e + 1] - pbase);
+            ep = routed_ptrs(P, e);
+        }
+        const uint32_t par = it & 1;
+        __syncthreads();  // every thread has read the ticket
+        if (t == blockDim.x - 1) *ticket_s = atomicAdd(&m->fu_next, 1);
+        if (t == 0) {
+            const uint8_t* src = ep.up_codes + (size_t)g * 64 * rowb;
+            const uint32_t chunk = 16 * rowb;
+            mbar_arrive_expect_tx(&bars[0], chunk + 64 * G * 4);
+            bulk_g2s(sbs, ep.up_sb + (size_t)g * 64 * G, 64 * G * 4, &bars[0], pol);
+            bulk_g2s(codes, src, chunk, &bars[0], pol);
+            for (int k = 1; k < 4; ++k) {
+                mbar_arrive_expect_tx(&bars[k], chunk);
+                bulk_g2s(codes + k * chunk, src + (size_t)k * chunk, chunk, &bars[k], pol);
+            }
+        }
+        // token lanes: TL adjacent lanes per scale group
+        const int TL = T == 1 ? 1 : (T == 2 ? 2 : 4);
+        const int RS = 256 / (TL * G);
+        const int tk = t % TL, gc = (t / TL) % G, rs = t / (TL * G);
+        const bool active = rs < RS && tk < T;
+        XFixed xf = {};
+        if (active) {
+            const int tok = shared ? pbase + tk : __ldcg(io.pair_tok + pbase + tk);
+            load_x_fixed(io.xt + (size_t)tok * G * kXfStride, io.xsc + (size_t)tok * G * 2, gc, xf);
+        }
+        float off_r = 0.f;
+        if (t < 64 && ep.up_off) off_r = __ldg(ep.up_off + 64 * g + t);
+        // ---- dot products (every thread keeps the warp's step count)
+        bool ok = true;
+        int waited = -1;
+        const int n_steps = (64 + 2 * RS - 1) / (2 * RS);
+        for (int i = 0; i < n_steps; ++i) {
+            const int r = rs + 2 * RS * i, r2 = r + RS;
+            const bool act = rs < RS && r < 64;
+            const bool two = act && r2 < 64;
+            if (act) {
+                const int k = (two ? r2 : r) >> 4;
+                while (ok && waited < k) { ++waited; ok = mbar_wait(&bars[waited], par); }
+            }
+            uint4 a0 = make_uint4(0, 0, 0, 0), a1 = a0, b0 = a0, b1 = a0;
+            uint32_t sw0 = 0, sw1 = 0;
+            if (act && ok) {
+                load_group_codes(codes + r * rowb, gc, a0, a1);
+                sw0 = sbs[r * G + gc];
+                if (two) {
+                    load_group_codes(codes + r2 * rowb, gc, b0, b1);
+                    sw1 = sbs[r2 * G + gc];
+                }
+            }
+            const int da = group_dot_fixed16(a0, a1, xf);
+            const int db = group_dot_fixed16(b0, b1, xf);
+            __syncwarp();  // the token lanes of a group have read its codes before parts land there
+            if (act && ok && active) {
+                const float2 sa = half2_to_float2(sw0);
+                *up_part(codes, rowb, r, gc, tk) = fmaf(sa.x * xf.inv, (float)da, sa.y * xf.xsum);
+                if (two) {
+                    const float2 sbv = half2_to_float2(sw1);
+                    *up_part(codes, rowb, r2, gc, tk) = fmaf(sbv.x * xf.inv, (float)db, sbv.y * xf.xsum);
+                }
+            }
+        }
+        while (ok && waited < 3) { ++waited; ok = mbar_wait(&bars[waited], par); }
+        if (t < 64) offs_s[t] = off_r;
+        fence_proxy_async_smem();  // the parts come before the down copies into the same rows
+        if (!__syncthreads_and(ok)) return;
+        // ---- row sums for every token; the row's down codes are copied once if it fired for any
+        bool lv = false;
+        {
+            const int r = t >> 2, q = t & 3;
+            bool anyh = false;
+            for (int k = 0; k < T; ++k) {
+                float s0 = 0.f, s1 = 0.f;
+                int cc = q;
+                for (; cc + 4 < G; cc += 8) {
+                    s0 += *up_part(codes, rowb, r, cc, k);
+                    s1 += *up_part(codes, rowb, r, cc + 4, k);
+                }
+                if (cc < G) s0 += *up_part(codes, rowb, r, cc, k);
+                float sum = s0 + s1;
+                sum += __shfl_xor_sync(0xffffffffu, sum, 1);
+                sum += __shfl_xor_sync(0xffffffffu, sum, 2);
+                const float z = sum + offs_s[r];
+                const float h = z > 0.f ? z * z : 0.f;
+                if (q == 0) h_s[k * 64 + r] = h;
+                anyh |= h > 0.f;
+            }
+            if (q == 0) {
+                lv = dense || anyh;
+                if (lv) {
+                    mbar_expect_tx(&bars[4], (uint32_t)rowb);
+                    bulk_g2s(codes + (size_t)r * rowb, ep.dn_codes + ((size_t)g * 64 + r) * rowb, rowb, &bars[4], pol);
+                }
+            }
+            const unsigned bl = __ballot_sync(0xffffffffu, lv);
+            if (lane == 0) {
+                unsigned m8 = 0;
+#pragma unroll
+                for (int i = 0; i < 8; ++i) m8 |= ((bl >> (4 * i)) & 1u) << i;
+                live8[t >> 5] = (uint8_t)m8;
+            }
+        }
+        const bool any = __syncthreads_or(lv) != 0;
+        if (t == 0 && any) {
+            mbar_arrive_expect_tx(&bars[4], (uint32_t)H * 4);
+            bulk_g2s(sbs, ep.dn_sb + (size_t)g * H, H * 4, &bars[4], pol);
+        }
+        const uint64_t live = *reinterpret_cast<const uint64_t*>(live8);
+        if (t < 2 && live) {  // the expert's union over all its tokens (for the live-row counts)
+            const uint32_t bits = (uint32_t)(live >> (32 * t));
+            uint32_t* mw = shared ? io.mask_s + 2 * g + t : io.mask_r + (size_t)e * (P.routed_neurons / 32) + 2 * g + t;
+            if (bits) atomicOr(mw, bits);
+        }
+        // ---- per token: partial row index, router weight, fixed-order sum of h
+        int tokv[kFTok], riv[kFTok];
+        float wv[kFTok], hsum[kFTok];
+#pragma unroll
+        for (int k = 0; k < kFTok; ++k) {
+            tokv[k] = 0; riv[k] = 0; wv[k] = 0.f; hsum[k] = 0.f;
+            if (k < T) {
+                if (shared) {
+                    tokv[k] = pbase + k;
+                    riv[k] = g;
+                    wv[k] = 1.f;
+                } else {
+                    tokv[k] = __ldcg(io.pair_tok + pbase + k);
+                    riv[k] = NGs + (__ldcg(io.pair_slot + pbase + k) - 1) * NGr + g;
+                    wv[k] = __ldcg(io.pair_w + pbase + k);
+                }
+                float hs = h_s[k * 64 + lane] + h_s[k * 64 + lane + 32];
+#pragma unroll
+                for (int off = 16; off; off >>= 1) hs += __shfl_xor_sync(0xffffffffu, hs, off);
+                hsum[k] = hs;
+            }
+        }
+        if (t < nthr) {
+            if (!any) {
+                for (int k = 0; k < T; ++k)
+                    for (int i = 0; i < (nthr == H / 12 ? 3 : 4); ++i)
+                        *out.quad(tokv[k], riv[k], (H % 48 == 0 ? 3 : 4) * t + i) = make_float4(0.f, 0.f, 0.f, 0.f);
+            } else {
+                ok = mbar_wait(&bars[4], dn_par);
+                if (ok) {
+                    if (H % 48 == 0)
+                        fused_down<12>(codes, sbs, h_s, live, hsum, wv, tokv, riv, T, rowb, t, out);
+                    else
+                        fused_down<16>(codes, sbs, h_s, live, hsum, wv, tokv, riv, T, rowb, t, out);
+                }
+            }
+        } else if (any) {
+            ok = mbar_wait(&bars[4], dn_par);  // every thread sees the phase before the buffers are reused
+        }
+        if (any) dn_par ^= 1u;
+        fence_proxy_async_smem();
+        if (!__syncthreads_and(ok)) return;
+    }
+}
+
+// y[b][o] = the token's partial rows added in a fixed order (32 outputs per
+// CTA, token b = blockIdx.y): one bulk copy of the [Ut][32] slice, thread
+// (lane, p) adds rows p, p+8, ..., then the 8 sums in order; bf16 RNE.
+__global__ void __launch_bounds__(256) batch_fused_reduce_kernel(const __grid_constant__ LayerParams P, const BatchIO io) {
+    extern __shared__ __align__(128) float slice[];  // [Ut][32]
+    __shared__ float part[8][33];
+    __shared__ __align__(8) uint64_t bar;
+    const int t = threadIdx.x, cb = blockIdx.x, b = blockIdx.y, H = P.hidden;
+    const int Ut = P.shared_neurons / 64 + P.top_k * (P.routed_neurons / 64);
+    if (t == 0) { mbar_init(&bar, 1); fence_mbar_init(); }
+    __syncthreads();
+    pdl_wait();
+    pdl_trigger();
+    if (t == 0) {
+        mbar_arrive_expect_tx(&bar, (uint32_t)Ut * 128u);
+        const float* src = io.partial + (size_t)b * H * Ut + (size_t)cb * Ut * 32;
+        for (int r0 = 0; r0 < Ut; r0 += 256) {
+            const int rows = min(256, Ut - r0);
+            bulk_g2s(slice + (size_t)r0 * 32, src + (size_t)r0 * 32, (uint32_t)rows * 128u, &bar, policy_evict_first());
+        }
+    }
+    const bool ok = mbar_wait(&bar, 0);
+    if (!__syncthreads_and(ok)) return;
+    const int lane = t & 31, p = t >> 5;
+    float a0 = 0.f, a1 = 0.f;
+    int r = p;
+    for (; r + 8 < Ut; r += 16) {
+        a0 += slice[r * 32 + lane];
+        a1 += slice[(r + 8) * 32 + lane];
+    }
+    if (r < Ut) a0 += slice[r * 32 + lane];
+    part[p][lane] = a0 + a1;
+    __syncthreads();
+    if (t < 32) {
+        float y = part[0][t];
+#pragma unroll
+        for (int i = 1; i < 8; ++i) y += part[i][t];
+        const size_t o = (size_t)b * H + cb * 32 + t;
+        if (io.y_f32) io.y_f32[o] = y;
+        io.y_bf16[o] = f32_to_bf16_bits(y);
+    }
+    if ((io.live_total || io.live_groups) && cb == 0 && b == 0) {
+        __syncthreads();  // part[] is reused below
+        // union live rows and groups per expert, from the union masks
+        const BatchMeta* m = io.meta;
+        const int nt = __ldcg(&m->n_touched), WR = P.routed_neurons / 32, WS = P.shared_neurons / 32;
+        int n = 0, ng = 0;
+        for (int q = t; q < nt * (WR / 2) + WS / 2; q += blockDim.x) {
+            const uint32_t* mw = q < nt * (WR / 2)
+                                     ? io.mask_r + (size_t)__ldcg(&m->touched[q / (WR / 2)]) * WR + 2 * (q % (WR / 2))
+                                     : io.mask_s + 2 * (q - nt * (WR / 2));
+            const uint32_t a = __ldcg(mw), c = __ldcg(mw + 1);
+            n += __popc(a) + __popc(c);
+            ng += (a | c) != 0u;
+        }
+        n = __reduce_add_sync(0xffffffffu, (unsigned)n);
+        ng = __reduce_add_sync(0xffffffffu, (unsigned)ng);
+        if (lane == 0) { part[p][0] = __int_as_float(n); part[p][1] = __int_as_float(ng); }
+        __syncthreads();
+        if (t == 0) {
+            int tn = 0, tg = 0;
+            for (int i = 0; i < 8; ++i) { tn += __float_as_int(part[i][0]); tg += __float_as_int(part[i][1]); }
+            if (io.live_total) *io.live_total = tn;
+            if (io.live_groups) *io.live_groups = tg;
+        }
+    }
+}
+
 // ------------------------------------------------------------------ reduce
 // y[t][o] = sum over the token's partial rows in slot order (shared-expert
 // chunks first, then the routed slots 1..K); bf16 RNE.
@@ -776,7 +1174,8 @@ BatchLayout batch_layout(const hs_moe_layer* L, int B) {
     l.h_sh = take((size_t)B * (NS ? NS : 1) * 4);
     l.mask_r = take((size_t)E * (NR / 32) * 4);
     l.mask_s = take((size_t)(NS ? NS / 32 : 1) * 4);
-    l.partial = take((size_t)B * (SC + K) * H * 4);
+    const int Ut = (NS / 64) + K * (NR / 64);
+    l.partial = take(B <= hs::kFusedMaxBatch ? (size_t)B * Ut * H * 4 : (size_t)B * (SC + K) * H * 4);
     l.total = o;
     return l;
 }
@@ -843,13 +1242,25 @@ int hs_batch_decode(const hs_moe_layer* L, const uint16_t* x, const float* logit
     if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return HS_ERR_CUDA;
     const int up_smem = hs::BatchUpSmem::total(L->hidden);
     const int dn_smem = hs::BatchDownSmem::total();
-    if (set_smem_attr((const void*)hs::batch_up_kernel, up_smem) != HS_OK) return HS_ERR_CUDA;
-    if (set_smem_attr((const void*)hs::batch_down_kernel, dn_smem) != HS_OK) return HS_ERR_CUDA;
     if (cudaMemsetAsync(io.meta, 0, sizeof(hs::BatchMeta), s) != cudaSuccess) return HS_ERR_CUDA;
     // the first kernel follows the memset with ordinary stream ordering
     hs::batch_route_kernel<<<dim3(batch), dim3(256), 0, s>>>(P, io);
     if (cudaGetLastError() != cudaSuccess) return HS_ERR_CUDA;
     if (launch_pdl(hs::batch_plan_kernel, dim3(1), dim3(512), 0, s, P, io) != cudaSuccess) return HS_ERR_CUDA;
+    if (batch <= hs::kFusedMaxBatch) {
+        const int f_smem = hs::FusedSmem::total(L->hidden);
+        const int Ut = (L->shared ? L->shared->neurons / 64 : 0) + L->top_k * (L->routed[0].neurons / 64);
+        if (set_smem_attr((const void*)hs::batch_fused_kernel, f_smem) != HS_OK) return HS_ERR_CUDA;
+        if (set_smem_attr((const void*)hs::batch_fused_reduce_kernel, Ut * 128) != HS_OK) return HS_ERR_CUDA;
+        if (launch_pdl(hs::batch_fused_kernel, dim3(2 * sms), dim3(256), f_smem, s, P, io) != cudaSuccess)
+            return HS_ERR_CUDA;
+        if (launch_pdl(hs::batch_fused_reduce_kernel, dim3(L->hidden / 32, batch), dim3(256), (size_t)Ut * 128, s, P,
+                       io) != cudaSuccess)
+            return HS_ERR_CUDA;
+        return launch_err();
+    }
+    if (set_smem_attr((const void*)hs::batch_up_kernel, up_smem) != HS_OK) return HS_ERR_CUDA;
+    if (set_smem_attr((const void*)hs::batch_down_kernel, dn_smem) != HS_OK) return HS_ERR_CUDA;
     if (launch_pdl(hs::batch_up_kernel, dim3(hs::kUpCtasPerSm * sms), dim3(hs::kUpThreads), up_smem, s, P, io) != cudaSuccess)
         return HS_ERR_CUDA;
     if (launch_pdl(hs::batch_down_kernel, dim3(2 * sms), dim3(256), dn_smem, s, P, io) != cudaSuccess)
