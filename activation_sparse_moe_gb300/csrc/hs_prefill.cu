@@ -32,6 +32,7 @@ namespace hs {
 
 constexpr int kNt = 128;          // max tokens per tile (MMA N)
 constexpr int kMaxTokens = 4096;
+constexpr int kTokBlk = 16;      // tokens per CTA of the list/gather kernel
 constexpr int kMaxKTiles = 64;    // 64-neuron tiles per expert (neurons <= 4096): one 64-bit mask
 
 // Output band width of the down product: 192 when it divides the hidden size, else 128.
@@ -60,6 +61,7 @@ struct PrefillIO {
     int T;
     unsigned flags;
     PrefillMeta* meta;
+    int* blk_cnt;             // [ceil(T / kTokBlk)][E] pairs per (token block, expert), zeroed with meta
     TileInfo* tiles;          // [max tiles]
     int* idx;                 // [T][K]
     float* w;                 // [T][K]
@@ -101,6 +103,7 @@ __global__ void __launch_bounds__(256) prefill_route_kernel(const __grid_constan
         if (lane < K) {
             const int e = io.idx[(size_t)tok * K + lane];
             atomicAdd(&io.meta->cnt[e], 1);
+            atomicAdd(&io.blk_cnt[(tok / kTokBlk) * P.n_routed + e], 1);
             if (io.dbg_idx) {
                 io.dbg_idx[(size_t)tok * K + lane] = e;
                 io.dbg_w[(size_t)tok * K + lane] = io.w[(size_t)tok * K + lane];
@@ -164,71 +167,82 @@ __global__ void __launch_bounds__(256) prefill_tiles_kernel(const __grid_constan
     for (int i = threadIdx.x; i < words; i += blockDim.x) io.flag_r[i] = 0u;
 }
 
-// CTA e < E: lists the pairs routed to expert e in token order (a block-wide
-// scan over contiguous chunks of the token-major pair list), records their
-// grouped positions and router weights, and gathers their tokens' x rows.
-// CTAs >= E gather the rows of the shared expert (every token).  Gathered
-// rows are fp16; inside each group of 8 inputs (one word of codes) the order
-// is e0 e4 e1 e5 e2 e6 e3 e7, the order in which the dequantiser emits nibble
-// pairs (both operands of the up product use it).
+// CTA b handles tokens [16b, 16b + 16): each of its pairs (token, slot) gets
+// its position in its expert's list, which keeps token order: the expert's
+// offset, plus its pairs in earlier token blocks (counted by the route
+// kernel), plus its pairs earlier in this block.  The CTA records positions
+// and router weights, then gathers each of its tokens' x rows once and writes
+// the row to the token's K routed positions and to its shared-expert row.
+// Gathered rows are fp16; inside each group of 8 inputs (one word of codes)
+// the order is e0 e4 e1 e5 e2 e6 e3 e7, the order in which the dequantiser
+// emits nibble pairs (both operands of the up product use it).
 constexpr int kListThreads = 256;
 
-__device__ __forceinline__ void gather_row(const uint16_t* __restrict__ xrow, uint16_t* __restrict__ dst, int H,
-                                           int first, int stride) {
-    for (int c8 = first; c8 < H / 8; c8 += stride) {
-        const uint4 v = __ldg(reinterpret_cast<const uint4*>(xrow) + c8);
-        const uint32_t wv[4] = {v.x, v.y, v.z, v.w};
-        __half hv[8];
+__device__ __forceinline__ uint4 bf16x8_to_fp16_perm(const uint4 v) {
+    const uint32_t wv[4] = {v.x, v.y, v.z, v.w};
+    __half hv[8];
 #pragma unroll
-        for (int i = 0; i < 4; ++i) {
-            hv[2 * i] = __float2half_rn(__uint_as_float(wv[i] << 16));
-            hv[2 * i + 1] = __float2half_rn(__uint_as_float(wv[i] & 0xffff0000u));
-        }
-        const __half2 p0 = __halves2half2(hv[0], hv[4]), p1 = __halves2half2(hv[1], hv[5]);
-        const __half2 p2 = __halves2half2(hv[2], hv[6]), p3 = __halves2half2(hv[3], hv[7]);
-        reinterpret_cast<uint4*>(dst)[c8] =
-            make_uint4(*reinterpret_cast<const uint32_t*>(&p0), *reinterpret_cast<const uint32_t*>(&p1),
-                       *reinterpret_cast<const uint32_t*>(&p2), *reinterpret_cast<const uint32_t*>(&p3));
+    for (int i = 0; i < 4; ++i) {
+        hv[2 * i] = __float2half_rn(__uint_as_float(wv[i] << 16));
+        hv[2 * i + 1] = __float2half_rn(__uint_as_float(wv[i] & 0xffff0000u));
     }
+    const __half2 p0 = __halves2half2(hv[0], hv[4]), p1 = __halves2half2(hv[1], hv[5]);
+    const __half2 p2 = __halves2half2(hv[2], hv[6]), p3 = __halves2half2(hv[3], hv[7]);
+    return make_uint4(*reinterpret_cast<const uint32_t*>(&p0), *reinterpret_cast<const uint32_t*>(&p1),
+                      *reinterpret_cast<const uint32_t*>(&p2), *reinterpret_cast<const uint32_t*>(&p3));
 }
 
 __global__ void __launch_bounds__(kListThreads) prefill_list_kernel(const __grid_constant__ LayerParams P,
                                                                     const PrefillIO io) {
-    __shared__ int tmp[8];
-    __shared__ int toks[kMaxTokens];
+    __shared__ int base_e[kMaxRouted];
+    __shared__ int e_of[kTokBlk * kMaxTopK];
+    __shared__ int dst[kTokBlk][kMaxTopK + 1];  // destination rows of each token
     pdl_wait();
     pdl_trigger();
     const int E = P.n_routed, K = P.top_k, H = P.hidden, n = io.T * K;
-    if ((int)blockIdx.x >= E) {
-        // shared expert rows: token t -> row T*K + t
-        const int nb = gridDim.x - E, b = blockIdx.x - E;
-        if (!P.shared_neurons) return;
-        for (int t = b; t < io.T; t += nb) gather_row(io.x + (size_t)t * H, io.xg + ((size_t)n + t) * H, H, threadIdx.x, kListThreads);
-        return;
+    const int b = blockIdx.x, t0 = b * kTokBlk, nt = min(kTokBlk, io.T - t0), t = threadIdx.x;
+    // expert offsets of this token block
+    for (int e = t; e < E; e += blockDim.x) {
+        int c = __ldcg(&io.meta->off[e]);
+        for (int bb = 0; bb < b; ++bb) c += __ldcg(&io.blk_cnt[bb * E + e]);
+        base_e[e] = c;
     }
-    const int e = blockIdx.x;
-    const int chunk = (n + kListThreads - 1) / kListThreads;
-    const int p0 = threadIdx.x * chunk, p1 = min(n, p0 + chunk);
-    int hits = 0;
-    for (int p = p0; p < p1; ++p) hits += (io.idx[p] == e);
-    const int incl = block_inclusive_sum(hits, tmp);
-    const int base = __ldcg(&io.meta->off[e]);
-    int pos = incl - hits;
-    for (int p = p0; p < p1; ++p) {
-        if (io.idx[p] == e) {
-            io.pair_tok[base + pos] = p / K;
-            io.pair_w[base + pos] = io.w[p];
-            io.pos_of[p] = base + pos;
-            toks[pos] = p / K;
-            ++pos;
+    for (int i = t; i < nt * K; i += blockDim.x) e_of[i] = __ldcg(io.idx + (size_t)t0 * K + i);
+    __syncthreads();
+    // positions: pairs of the block in token-major order, ranked within their expert
+    for (int i = t; i < nt * K; i += blockDim.x) {
+        const int e = e_of[i];
+        int rank = 0;
+        for (int j = 0; j < i; ++j) rank += (e_of[j] == e);
+        const int p = t0 * K + i, pos = base_e[e] + rank;
+        io.pair_tok[pos] = p / K;
+        io.pair_w[pos] = __ldcg(io.w + p);
+        io.pos_of[p] = pos;
+        dst[i / K][i % K] = pos;
+    }
+    if (t < nt) dst[t][K] = P.shared_neurons ? n + t0 + t : -1;
+    __syncthreads();
+    // gather: each 16-byte piece of a token's row is loaded once and stored to every destination
+    const int c8n = H / 8, nd = K + (P.shared_neurons ? 1 : 0);
+    constexpr int kU = 4;
+    for (int q0 = t; q0 < nt * c8n; q0 += kU * blockDim.x) {
+        uint4 v[kU];
+#pragma unroll
+        for (int u = 0; u < kU; ++u) {
+            const int q = q0 + u * blockDim.x;
+            v[u] = q < nt * c8n ? __ldg(reinterpret_cast<const uint4*>(io.x + (size_t)(t0 + q / c8n) * H) + q % c8n)
+                                : make_uint4(0, 0, 0, 0);
+        }
+#pragma unroll
+        for (int u = 0; u < kU; ++u) {
+            const int q = q0 + u * blockDim.x;
+            if (q >= nt * c8n) break;
+            const uint4 h = bf16x8_to_fp16_perm(v[u]);
+            const int tk = q / c8n, c8 = q % c8n;
+            for (int d = 0; d < nd; ++d)
+                reinterpret_cast<uint4*>(io.xg + (size_t)dst[tk][d] * H)[c8] = h;
         }
     }
-    __syncthreads();
-    const int cnt = __ldcg(&io.meta->cnt[e]);
-    // gather: one warp per row
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    for (int i = warp; i < cnt; i += kListThreads / 32)
-        gather_row(io.x + (size_t)toks[i] * H, io.xg + (size_t)(base + i) * H, H, lane, 32);
 }
 
 struct TMaps {
@@ -259,7 +273,6 @@ constexpr int kWarpW = kEpiWarps + kDqWarps;   // 20
 constexpr int kWarpX = kWarpW + 1;             // 21
 constexpr int kWarpMma = kWarpX + 2;           // 23: sub-partition 3, which hosts the fewest other warps
 constexpr int kGemmThreads = 32 * (kWarpMma + 1);
-constexpr int kTileA = 128 * 128;       // 128 rows x 64 fp16
 constexpr int kTileX = kNt * 128;       // up to 128 rows x 64 fp16
 constexpr unsigned kProducerSleepNs = 64;
 constexpr unsigned kEpilogueSleepNs = 256;
@@ -861,11 +874,18 @@ __global__ void __launch_bounds__(256) prefill_combine_kernel(const __grid_const
     for (size_t q = (size_t)blockIdx.x * blockDim.x + threadIdx.x; q < n4; q += (size_t)gridDim.x * blockDim.x) {
         const int tok = (int)(q / (H / 4)), c4 = (int)(q % (H / 4));
         float4 a = make_float4(0.f, 0.f, 0.f, 0.f);
-        if (P.shared_neurons) a = __ldcg(reinterpret_cast<const float4*>(io.partial + ((size_t)io.T * K + tok) * H) + c4);
-        for (int j = 0; j < K; ++j) {
-            const int row = io.pos_of[tok * K + j];
-            const float4 v = __ldcg(reinterpret_cast<const float4*>(io.partial + (size_t)row * H) + c4);
-            a.x += v.x; a.y += v.y; a.z += v.z; a.w += v.w;
+        int row[kMaxTopK];
+#pragma unroll
+        for (int j = 0; j < kMaxTopK; ++j) row[j] = j < K ? __ldg(io.pos_of + tok * K + j) : 0;
+        float4 v[kMaxTopK];
+#pragma unroll
+        for (int j = 0; j < kMaxTopK; ++j)
+            v[j] = j < K ? __ldcs(reinterpret_cast<const float4*>(io.partial + (size_t)row[j] * H) + c4)
+                         : make_float4(0.f, 0.f, 0.f, 0.f);
+        if (P.shared_neurons) a = __ldcs(reinterpret_cast<const float4*>(io.partial + ((size_t)io.T * K + tok) * H) + c4);
+#pragma unroll
+        for (int j = 0; j < kMaxTopK; ++j) {
+            if (j < K) { a.x += v[j].x; a.y += v[j].y; a.z += v[j].z; a.w += v[j].w; }
         }
         if (io.y_f32) reinterpret_cast<float4*>(io.y_f32)[q] = a;
         const uint32_t lo = (uint32_t)f32_to_bf16_bits(a.x) | ((uint32_t)f32_to_bf16_bits(a.y) << 16);
@@ -927,7 +947,7 @@ bool make_map(EncodeTiledFn enc, CUtensorMap* m, CUtensorMapDataType dt, const v
 }
 
 struct PrefillLayout {
-    size_t meta, tiles, idx, w, pair_tok, pos_of, pair_w, xg, h_r, h_s, flags, partial, total;
+    size_t meta, blk_cnt, tiles, idx, w, pair_tok, pos_of, pair_w, xg, h_r, h_s, flags, partial, total;
     int max_tiles;
 };
 
@@ -940,6 +960,7 @@ PrefillLayout prefill_layout(const hs_moe_layer* L, int T) {
     auto take = [&](size_t bytes) { const size_t at = o; o += round_up(bytes, 1024); return at; };
     const size_t rows = (size_t)T * K + (NS ? T : 0);
     l.meta = take(sizeof(hs::PrefillMeta));
+    l.blk_cnt = take((size_t)((T + hs::kTokBlk - 1) / hs::kTokBlk) * E * 4);
     l.tiles = take((size_t)l.max_tiles * sizeof(hs::TileInfo));
     l.idx = take((size_t)T * K * 4);
     l.w = take((size_t)T * K * 4);
@@ -1003,6 +1024,7 @@ extern "C" int hs_moe_prefill(const hs_moe_layer* L, const uint16_t* x, const fl
     io.T = T;
     io.flags = flags;
     io.meta = reinterpret_cast<hs::PrefillMeta*>(w + l.meta);
+    io.blk_cnt = reinterpret_cast<int*>(w + l.blk_cnt);
     io.tiles = reinterpret_cast<hs::TileInfo*>(w + l.tiles);
     io.idx = reinterpret_cast<int*>(w + l.idx);
     io.w = reinterpret_cast<float*>(w + l.w);
@@ -1059,13 +1081,14 @@ extern "C" int hs_moe_prefill(const hs_moe_layer* L, const uint16_t* x, const fl
     if (set_smem_attr((const void*)hs::prefill_up_kernel, up_smem) != HS_OK) return HS_ERR_CUDA;
     if (set_smem_attr((const void*)hs::prefill_down_kernel, dn_smem) != HS_OK) return HS_ERR_CUDA;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-    if (cudaMemsetAsync(io.meta, 0, sizeof(hs::PrefillMeta), s) != cudaSuccess) return HS_ERR_CUDA;
+    // the meta block and the block counts are contiguous: one memset clears both
+    if (cudaMemsetAsync(io.meta, 0, l.tiles - l.meta, s) != cudaSuccess) return HS_ERR_CUDA;
     // the first kernel follows the memset with ordinary stream ordering
     hs::prefill_route_kernel<<<dim3((T + 7) / 8), dim3(256), 0, s>>>(P, io);
     if (cudaGetLastError() != cudaSuccess) return HS_ERR_CUDA;
     if (launch_pdl(hs::prefill_tiles_kernel, dim3(1), dim3(256), 0, s, P, io) != cudaSuccess) return HS_ERR_CUDA;
-    if (launch_pdl(hs::prefill_list_kernel, dim3(E + (NS ? 2 * sms - E % sms : 0)), dim3(hs::kListThreads), 0, s, P, io) !=
-        cudaSuccess)
+    if (launch_pdl(hs::prefill_list_kernel, dim3((T + hs::kTokBlk - 1) / hs::kTokBlk), dim3(hs::kListThreads), 0, s, P,
+                   io) != cudaSuccess)
         return HS_ERR_CUDA;
     if (launch_pdl(hs::prefill_up_kernel, dim3(sms), dim3(hs::kGemmThreads), up_smem, s, P, io, tm) != cudaSuccess)
         return HS_ERR_CUDA;
