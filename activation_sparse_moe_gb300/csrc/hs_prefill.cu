@@ -27,6 +27,7 @@
 
 #include "hs_host.h"
 #include "hs_tc.cuh"
+#include "hs_transpose.cuh"
 
 namespace hs {
 
@@ -36,7 +37,6 @@ constexpr int kTokBlk = 16;      // tokens per CTA of the list/gather kernel
 constexpr int kMaxKTiles = 64;    // 64-neuron tiles per expert (neurons <= 4096): one 64-bit mask
 
 // Output band width of the down product: 192 when it divides the hidden size, else 128.
-__host__ __device__ inline int down_band(int H) { return H % 192 == 0 ? 192 : 128; }
 
 struct PrefillMeta {
     int n_tiles;                  // token tiles (routed experts first, then shared)
@@ -160,7 +160,7 @@ __global__ void __launch_bounds__(256) prefill_tiles_kernel(const __grid_constan
         m->n_tiles = nrt + nst;
         const int mr = (P.routed_neurons + 127) / 128, ms = (P.shared_neurons + 127) / 128;
         m->up_units = nrt * mr + nst * ms;
-        m->dn_units = (nrt + nst) * (P.hidden / down_band(P.hidden));
+        m->dn_units = (nrt + nst) * (P.hidden / 128);  // 128-output bands of the down product
     }
     // live flags: one word per (tile, 32 k-tiles)
     const int words = io.max_tiles * ((max(P.routed_neurons, P.shared_neurons) / 64 + 31) / 32);
@@ -247,9 +247,9 @@ __global__ void __launch_bounds__(kListThreads) prefill_list_kernel(const __grid
 
 struct TMaps {
     CUtensorMap up_codes_r, up_codes_s;      // [rows][H/2] bytes, box 64 x 128, 64-byte swizzle
-    CUtensorMap dn_codes_r, dn_codes_s;      // [rows][H/2] bytes, box (band / 2) x 64
+    CUtensorMap dn_codes_r, dn_codes_s;      // [rows][H/2] bytes, box 64 x 64, 64-byte swizzle
     CUtensorMap xg[8];                       // fp16 [rows][H], box 64 x 16(i+1), 128-byte swizzle
-    CUtensorMap hr[2], hsh[2];               // fp16 h, box 64 x {64, 128}
+    CUtensorMap hr[8], hsh[8];               // fp16 h, box 64 x 16(i+1), 128-byte swizzle
 };
 
 // ------------------------------------------------------------ GEMM kernels
@@ -549,7 +549,10 @@ prefill_up_kernel(const __grid_constant__ LayerParams P, const PrefillIO io, con
             const int r = 32 * warp + lane, n = d.row0 + r;
             const bool rowok = r < d.rows;
             const float off = (rowok && d.ep.up_off) ? __ldg(d.ep.up_off + n) : 0.f;
-            uint16_t* hcol = (d.shared ? io.h_s : io.h_r) + (size_t)d.row_out * d.N + n;
+            // h is stored with each group of 8 neurons in the order n0 n4 n1 n5 n2 n6 n3 n7 (the order
+            // in which the down product's dequantiser yields nibble pairs)
+            const int n8 = n & 7, nst = (n & ~7) | (n8 < 4 ? 2 * n8 : 2 * (n8 - 4) + 1);
+            uint16_t* hcol = (d.shared ? io.h_s : io.h_r) + (size_t)d.row_out * d.N + nst;
             ok = __all_sync(0xffffffffu, wait_full_sleep(br.tfull, 2, nu, kEpilogueSleepNs));
             if (!ok) break;
             tc_fence_after();
@@ -587,32 +590,29 @@ prefill_up_kernel(const __grid_constant__ LayerParams P, const PrefillIO io, con
     if (warp == 0) tmem_dealloc(tmem, 512);
 }
 
-// ---- down GEMM: unit = (token tile, band of BN outputs); D[token][output] over the live
-// 64-neuron tiles of the expert.  A = h of the tile's tokens (K-major, by TMA); B = the
-// neuron-major codes of one 64-neuron tile dequantised in place into an MN-major fp16 tile
-// (64 neurons x BN outputs: 128-byte rows of 64 outputs, 8-neuron x 64-output swizzle atoms),
-// so no transpose is needed.  Within each group of 8 outputs (one word of codes) the tile
-// holds the order o0 o4 o1 o5 o2 o6 o3 o7; the epilogue undoes it when it writes a row.
+// ---- down GEMM (operands swapped): unit = (token tile, band of 128 outputs); D^T[output][token]
+// over the live 64-neuron tiles of the expert.  A = the band's weights, transposed and dequantised
+// straight into TMEM: each warp loads 32 neuron rows x 32 outputs of codes (one 16-byte chunk per
+// lane), transposes the 32 x 32 nibbles in registers (lane = output) and writes the fp16 weights
+// (column c = the neurons at stored h positions 2c, 2c+1).  B = h of the tile's tokens (K-major,
+// by TMA).  The up epilogue stores h with the neurons of each group of 8 in the order
+// n0 n4 n1 n5 n2 n6 n3 n7, the order in which a code word yields nibble pairs, so no further
+// shuffling is needed.  The epilogue lane owns one output and writes it for every token.
+constexpr int kDnBand = 128;
 constexpr int kDnWD = 6, kDnSD = 4;
 using DnBars = GemmBars<kDnWD, kDnSD>;
 
 struct DownLayout {
-    int bn, sbo, tile_b, wslot, codes, x, w, bars, total;
-    __host__ __device__ explicit DownLayout(int BN) {
-        bn = BN;
-        sbo = (BN / 64) * 1024;                 // bytes between 8-neuron groups of the B tile
-        tile_b = 8 * sbo;                       // 64 neurons x BN outputs
-        codes = 64 * (BN / 2);                  // 64 neurons x BN/2 bytes
-        wslot = (codes + BN * 4 + 127) / 128 * 128;
-        x = kDnSD * tile_b;
-        w = x + kDnSD * kTileX;
-        bars = w + kDnWD * wslot;
-        total = 1024 + bars + 8 * DnBars::kCount + 64;
-    }
+    static constexpr int kCodes = 64 * kDnBand / 2;     // 64 neurons x 64 bytes, 64-byte swizzle
+    static constexpr int kWSlot = kCodes + kDnBand * 4;  // + the slab slice (scale, bias) of the band
+    static constexpr int kX = 0;                         // h tiles: up to 128 rows x 128 B
+    static constexpr int kW = kX + kDnSD * kTileX;
+    static constexpr int kBarsOff = kW + kDnWD * kWSlot;
+    static constexpr int kTotal = 1024 + kBarsOff + 8 * DnBars::kCount + 64;
 };
 
 struct DownUnit {
-    int tile, ob, ntok, cy0, NK, row0;
+    int tile, ob, ntok, nt16, cy0, NK, row0;
     bool shared;
     ExpertPtrs ep;
     uint64_t live;   // bit j: 64-neuron tile j is multiplied
@@ -628,6 +628,7 @@ __device__ __forceinline__ DownUnit down_unit(const LayerParams& P, const Prefil
     d.NK = (d.shared ? P.shared_neurons : P.routed_neurons) / 64;
     d.ep = d.shared ? P.shared : routed_ptrs(P, ti.e);
     d.ntok = ti.ntok;
+    d.nt16 = (ti.ntok + 15) & ~15;
     d.cy0 = d.shared ? 0 : ti.e * P.routed_neurons;
     d.row0 = ti.row0;
     const uint32_t* f = io.flag_r + (size_t)d.tile * words;
@@ -643,29 +644,14 @@ __device__ __forceinline__ int pop_live(uint64_t& m) {
     return j;
 }
 
-// Shared-memory descriptor of an MN-major operand in the 128-byte swizzle layout: leading
-// byte offset = 1024 (next 64-wide block along MN), stride byte offset = between 8-row groups
-// along K.
-__device__ __forceinline__ uint64_t umma_desc_sw128_mn(uint32_t smem_addr, uint32_t sbo) {
-    uint64_t d = 0;
-    d |= (uint64_t)((smem_addr & 0x3FFFFu) >> 4);
-    d |= (uint64_t)(1024u >> 4) << 16;
-    d |= (uint64_t)((sbo >> 4) & 0x3FFFu) << 32;
-    d |= (uint64_t)1u << 46;
-    d |= (uint64_t)2u << 61;
-    return d;
-}
-
 __global__ void __launch_bounds__(kGemmThreads, 1)
 prefill_down_kernel(const __grid_constant__ LayerParams P, const PrefillIO io, const __grid_constant__ TMaps tm) {
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    const int H = P.hidden, BN = down_band(H);
-    const DownLayout lay(BN);
-    uint8_t* sB = smem;
-    uint8_t* sX = smem + lay.x;
-    uint8_t* sW = smem + lay.w;
-    DnBars br(smem + lay.bars);
+    const int H = P.hidden;
+    uint8_t* sX = smem + DownLayout::kX;
+    uint8_t* sW = smem + DownLayout::kW;
+    DnBars br(smem + DownLayout::kBarsOff);
     const int t = threadIdx.x, warp = t >> 5, lane = t & 31;
     if (t == 0) br.init();
     if (warp == 0) tmem_alloc(br.tmem_slot, 512);
@@ -673,11 +659,12 @@ prefill_down_kernel(const __grid_constant__ LayerParams P, const PrefillIO io, c
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *br.tmem_slot;
+    const uint32_t tmem_a = tmem + 256;   // kDnSD dequantised A tiles of 32 columns
     pdl_wait();
     pdl_trigger();
     PrefillMeta* m = io.meta;
     const int NR = P.routed_neurons, NS = P.shared_neurons, K = P.top_k;
-    const int nb = H / BN;
+    const int nb = H / kDnBand;
     const int U = m->dn_units;
     const int words = (max(NR, NS) / 64 + 31) / 32;
     const bool dense = (io.flags & HS_FORCE_DENSE) != 0;
@@ -697,10 +684,11 @@ prefill_down_kernel(const __grid_constant__ LayerParams P, const PrefillIO io, c
                     const int j = pop_live(lm);
                     if (!(ok = wait_free_sleep(br.wempty, kDnWD, wq, kProducerSleepNs))) break;
                     const int s = wq % kDnWD;
-                    uint8_t* slot = sW + s * lay.wslot;
-                    mbar_arrive_expect_tx(&br.wfull[s], (uint32_t)(lay.codes + BN * 4));
-                    tma_load_2d_hint(slot, cmap, (BN / 2) * d.ob, d.cy0 + 64 * j, &br.wfull[s], pol);
-                    bulk_g2s(slot + lay.codes, d.ep.dn_sb + (size_t)j * H + BN * d.ob, BN * 4, &br.wfull[s], pol);
+                    uint8_t* slot = sW + s * DownLayout::kWSlot;
+                    mbar_arrive_expect_tx(&br.wfull[s], (uint32_t)DownLayout::kWSlot);
+                    tma_load_2d_hint(slot, cmap, (kDnBand / 2) * d.ob, d.cy0 + 64 * j, &br.wfull[s], pol);
+                    bulk_g2s(slot + DownLayout::kCodes, d.ep.dn_sb + (size_t)j * H + kDnBand * d.ob, kDnBand * 4,
+                             &br.wfull[s], pol);
                     ++wq;
                 }
                 if (ok && d.ob == 0) {
@@ -714,18 +702,18 @@ prefill_down_kernel(const __grid_constant__ LayerParams P, const PrefillIO io, c
         }
         __syncwarp();
     } else if (warp == kWarpX) {
-        // ---- h of the tile's tokens (A operand: 128 rows, the rows past the tile are ignored)
+        // ---- h of the tile's tokens (B operand): a box of the tile's rows rounded up to 16
         if (lane == 0) {
             const uint64_t pol = policy_evict_last();
             uint32_t xq = 0;
             for (int u = blockIdx.x; u < U && ok; u += gridDim.x) {
                 const DownUnit d = down_unit(P, io, nb, words, dense, u);
-                const CUtensorMap* hmap = d.shared ? &tm.hsh[1] : &tm.hr[1];
+                const CUtensorMap* hmap = d.shared ? &tm.hsh[d.nt16 / 16 - 1] : &tm.hr[d.nt16 / 16 - 1];
                 for (uint64_t lm = d.live; lm && ok;) {
                     const int j = pop_live(lm);
                     if (!(ok = wait_free_sleep(br.sempty, kDnSD, xq, kProducerSleepNs))) break;
                     const int x = xq % kDnSD;
-                    mbar_arrive_expect_tx(&br.sfull[x], (uint32_t)kTileX);
+                    mbar_arrive_expect_tx(&br.sfull[x], (uint32_t)d.nt16 * 128u);
                     tma_load_2d_hint(sX + x * kTileX, hmap, 64 * j, d.row0, &br.sfull[x], pol);
                     ++xq;
                 }
@@ -734,26 +722,25 @@ prefill_down_kernel(const __grid_constant__ LayerParams P, const PrefillIO io, c
         }
         __syncwarp();
     } else if (warp == kWarpMma) {
+        // ---- MMA issue: A (weights) from TMEM, B (h) from shared memory
         if (lane == 0) {
             uint32_t sq = 0, nu = 0;
-            const uint32_t idesc = umma_idesc_f16_f32(128, BN) | (1u << 16);   // B is MN-major
             for (int u = blockIdx.x; u < U && ok; u += gridDim.x, ++nu) {
                 const DownUnit d = down_unit(P, io, nb, words, dense, u);
                 const int acc = nu & 1;
                 if (!(ok = wait_free(br.tempty, 2, nu))) break;
                 tc_fence_after();
-                const uint32_t dt = tmem + (uint32_t)(acc * 256);
+                const uint32_t idesc = umma_idesc_f16_f32(128, d.nt16);
+                const uint32_t dt = tmem + (uint32_t)(acc * 128);
                 const int nk = __popcll(d.live);
                 for (int kk = 0; kk < nk; ++kk) {
                     if (!(ok = wait_full(br.sfull, kDnSD, sq))) break;
                     tc_fence_after();
                     const int a = sq % kDnSD;
-                    const uint64_t ad = umma_desc_sw128(smem_u32(sX + a * kTileX));
-                    const uint32_t b0 = smem_u32(sB + a * lay.tile_b);
+                    const uint64_t bd = umma_desc_sw128(smem_u32(sX + a * kTileX));
 #pragma unroll
-                    for (int q = 0; q < 4; ++q)
-                        umma_f16(dt, ad + 2 * q, umma_desc_sw128_mn(b0 + q * 2 * lay.sbo, lay.sbo), idesc,
-                                 (kk | q) != 0);
+                    for (int j = 0; j < 4; ++j)
+                        umma_f16_tmem_a(dt, tmem_a + 32 * a + 8 * j, bd + 2 * j, idesc, (kk | j) != 0);
                     umma_commit(&br.sempty[a]);
                     ++sq;
                 }
@@ -763,14 +750,13 @@ prefill_down_kernel(const __grid_constant__ LayerParams P, const PrefillIO io, c
         }
         __syncwarp();
     } else if (warp >= kEpiWarps && warp < kWarpW) {
-        // ---- dequantise: group g takes the k-steps q with q % 2 == g.  Item (word w, neuron
-        // octet v): outputs 8w..8w+7 of neurons 8v..8v+7, one 16-byte chunk per neuron.
-        const int dw = warp - kEpiWarps, g = dw / kDqGroup;
-        const int it = t - 32 * (kEpiWarps + g * kDqGroup);
-        const int nw = BN / 8, w = it % nw, v = it / nw;
-        const bool active = v < 8;
+        // ---- dequantise into TMEM: group g takes the k-steps q with q % 2 == g.  Warp (quadrant
+        // qd = warp % 4, half hh): outputs 32qd .. 32qd+31 of the band (TMEM lanes), neurons
+        // 32hh .. 32hh+31 of the tile (columns 16hh .. 16hh+15 of the A tile)
+        const int dw = warp - kEpiWarps, g = dw / kDqGroup, hh = (dw % kDqGroup) >> 2, qd = warp & 3;
+        const uint32_t trow = tmem_a + ((uint32_t)(32 * qd) << 16) + 16 * hh;
+        const int rbase = 32 * hh + (lane & 7), wsel = 4 * (lane >> 3);
         const __half2 k1024 = __floats2half2_rn(1024.f, 1024.f);
-        const __half2 sixteenth = __floats2half2_rn(0.0625f, 0.0625f);
         uint32_t q = 0;
         for (int u = blockIdx.x; u < U && ok; u += gridDim.x) {
             const DownUnit d = down_unit(P, io, nb, words, dense, u);
@@ -779,40 +765,41 @@ prefill_down_kernel(const __grid_constant__ LayerParams P, const PrefillIO io, c
                 const uint32_t qk = q + kk;
                 ok = __all_sync(0xffffffffu, wait_full(br.wfull, kDnWD, qk) && wait_free(br.sempty, kDnSD, qk));
                 if (!ok) break;
+                tc_fence_after();
                 const int s = qk % kDnWD;
-                if (active) {
-                    const uint8_t* cs = sW + s * lay.wslot;
-                    const uint4* sbq = reinterpret_cast<const uint4*>(cs + lay.codes) + 2 * w;
-                    const uint4 sa = sbq[0], sb = sbq[1];                 // (s, b) of outputs 8w..8w+3, 8w+4..8w+7
-                    const uint32_t lo[4] = {sa.x, sa.y, sa.z, sa.w}, hi[4] = {sb.x, sb.y, sb.z, sb.w};
-                    __half2 sc[4], bi[4];
+                const uint8_t* cs = sW + s * DownLayout::kWSlot;
+                // lane l takes word l/8 of the quadrant's 16-byte chunk in rows 8k + l%8 (the word-level
+                // steps of the transpose done by the loads); 64-byte swizzle: chunk c of row r sits at
+                // chunk c ^ ((r >> 1) & 3)
+                uint32_t a[4];
 #pragma unroll
-                    for (int p = 0; p < 4; ++p) {
-                        // pair p holds outputs (p, p+4); odd p arrive as 16 * code
-                        const uint32_t s2 = __byte_perm(lo[p], hi[p], 0x5410), b2 = __byte_perm(lo[p], hi[p], 0x7632);
-                        sc[p] = *reinterpret_cast<const __half2*>(&s2);
-                        if (p & 1) sc[p] = __hmul2(sc[p], sixteenth);
-                        bi[p] = *reinterpret_cast<const __half2*>(&b2);
-                    }
-                    uint8_t* B = sB + (qk % kDnSD) * lay.tile_b + (w >> 3) * 1024;
+                for (int k = 0; k < 4; ++k) {
+                    const int r = rbase + 8 * k;
+                    a[k] = *reinterpret_cast<const uint32_t*>(cs + r * (kDnBand / 2) + ((qd ^ ((r >> 1) & 3)) << 4) + wsel);
+                }
+                nib_transpose32_in_words(a);   // now: lane = output 32qd + lane, nibble j of word k = neuron 32hh + 8k + j
+                const float2 sbv = half2_to_float2(reinterpret_cast<const uint32_t*>(cs + DownLayout::kCodes)[32 * qd + lane]);
+                const __half2 s1 = __floats2half2_rn(sbv.x, sbv.x);
+                const __half2 s16 = __floats2half2_rn(sbv.x * 0.0625f, sbv.x * 0.0625f);
+                const __half2 b2 = __floats2half2_rn(sbv.y, sbv.y);
+                uint32_t o[16];
 #pragma unroll
-                    for (int i = 0; i < 8; ++i) {
-                        const int k = 8 * v + i;
-                        const uint32_t W = *reinterpret_cast<const uint32_t*>(cs + k * (BN / 2) + 4 * w);
-                        const uint32_t lw = W, hw = W >> 8;
-                        const uint32_t pr[4] = {(lw & 0x000F000Fu) | 0x64006400u, (lw & 0x00F000F0u) | 0x64006400u,
-                                                (hw & 0x000F000Fu) | 0x64006400u, (hw & 0x00F000F0u) | 0x64006400u};
-                        uint32_t o[4];
+                for (int k = 0; k < 4; ++k) {
+                    const uint32_t lo = a[k], hi = a[k] >> 8;
+                    // fp16 1024 + c (or 1024 + 16c): nibble pairs (0,4) (1,5) (2,6) (3,7)
+                    const uint32_t pr[4] = {(lo & 0x000F000Fu) | 0x64006400u, (lo & 0x00F000F0u) | 0x64006400u,
+                                            (hi & 0x000F000Fu) | 0x64006400u, (hi & 0x00F000F0u) | 0x64006400u};
 #pragma unroll
-                        for (int p = 0; p < 4; ++p) {
-                            const __half2 r = __hfma2(__hsub2(*reinterpret_cast<const __half2*>(&pr[p]), k1024), sc[p], bi[p]);
-                            o[p] = *reinterpret_cast<const uint32_t*>(&r);
-                        }
-                        *reinterpret_cast<uint4*>(B + (k >> 3) * lay.sbo + (k & 7) * 128 + (((w & 7) ^ (k & 7)) << 4)) =
-                            make_uint4(o[0], o[1], o[2], o[3]);
+                    for (int pp = 0; pp < 4; ++pp) {
+                        const __half2 qv = __hsub2(*reinterpret_cast<const __half2*>(&pr[pp]), k1024);
+                        const __half2 v = __hfma2(qv, (pp & 1) ? s16 : s1, b2);
+                        o[4 * k + pp] = *reinterpret_cast<const uint32_t*>(&v);
                     }
                 }
-                fence_proxy_async_smem();
+                __syncwarp();
+                tmem_st16(trow + 32 * (qk % kDnSD), o);
+                tmem_st_wait();
+                tc_fence_before();
                 __syncwarp();
                 if (lane == 0) {
                     mbar_arrive(&br.wempty[s]);
@@ -823,34 +810,31 @@ prefill_down_kernel(const __grid_constant__ LayerParams P, const PrefillIO io, c
             q += nk;
         }
     } else if (warp < kEpiWarps) {
-        // ---- epilogue: thread = token row of the tile; router-weighted partial row for this band
+        // ---- epilogue: lane = output of the band; router-weighted partial rows of the tile's tokens
         uint32_t nu = 0;
         for (int u = blockIdx.x; u < U && ok; u += gridDim.x, ++nu) {
             const DownUnit d = down_unit(P, io, nb, words, dense, u);
             const int acc = nu & 1;
-            const int c = 32 * warp + lane;               // row of the tile
-            const bool rowok = c < d.ntok;
-            const int row = d.row0 + c;
-            const float wgt = (rowok && !d.shared) ? __ldg(io.pair_w + row) : 1.f;
-            float* prow = io.partial + (d.shared ? (size_t)io.T * K + row : (size_t)row) * H + BN * d.ob;
+            const int col = kDnBand * d.ob + 32 * warp + lane;
+            float* pbase = io.partial + (d.shared ? (size_t)io.T * K + d.row0 : (size_t)d.row0) * H + col;
+            const float* wrow = io.pair_w + d.row0;
             ok = __all_sync(0xffffffffu, wait_full_sleep(br.tfull, 2, nu, kEpilogueSleepNs));
             if (!ok) break;
             tc_fence_after();
-            for (int c0 = 0; c0 < BN; c0 += 32) {
+            for (int c0 = 0; c0 < d.nt16; c0 += 32) {
                 float v[32];
                 if (d.live) {
-                    tmem_ld32(tmem + ((uint32_t)(32 * warp) << 16) + (uint32_t)(acc * 256 + c0), v);
+                    tmem_ld32(tmem + ((uint32_t)(32 * warp) << 16) + (uint32_t)(acc * 128 + c0), v);
                 } else {
 #pragma unroll
                     for (int i = 0; i < 32; ++i) v[i] = 0.f;
                 }
-                if (rowok) {
 #pragma unroll
-                    for (int g8 = 0; g8 < 4; ++g8) {
-                        const float* e = v + 8 * g8;   // o0 o4 o1 o5 o2 o6 o3 o7
-                        float4* dst = reinterpret_cast<float4*>(prow + c0 + 8 * g8);
-                        dst[0] = make_float4(wgt * e[0], wgt * e[2], wgt * e[4], wgt * e[6]);
-                        dst[1] = make_float4(wgt * e[1], wgt * e[3], wgt * e[5], wgt * e[7]);
+                for (int i = 0; i < 32; ++i) {
+                    const int c = c0 + i;
+                    if (c < d.ntok) {
+                        const float wgt = d.shared ? 1.f : __ldg(wrow + c);
+                        pbase[(size_t)c * H] = wgt * v[i];
                     }
                 }
             }
@@ -1051,20 +1035,19 @@ extern "C" int hs_moe_prefill(const hs_moe_layer* L, const uint16_t* x, const fl
     bool okm = true;
     okm &= make_map(enc, &tm.up_codes_r, CU_TENSOR_MAP_DATA_TYPE_UINT8, L->routed[0].up.codes, H / 2, (uint64_t)E * NR,
                     H / 2, hs::kUpK / 2, 128, CU_TENSOR_MAP_SWIZZLE_64B);
-    const int BN = hs::down_band(H);
     okm &= make_map(enc, &tm.dn_codes_r, CU_TENSOR_MAP_DATA_TYPE_UINT8, L->routed[0].down_nm.codes, H / 2,
-                    (uint64_t)E * NR, H / 2, BN / 2, 64, CU_TENSOR_MAP_SWIZZLE_NONE);
+                    (uint64_t)E * NR, H / 2, hs::kDnBand / 2, 64, CU_TENSOR_MAP_SWIZZLE_64B);
     if (NS) {
         okm &= make_map(enc, &tm.up_codes_s, CU_TENSOR_MAP_DATA_TYPE_UINT8, L->shared->up.codes, H / 2, NS, H / 2,
                         hs::kUpK / 2, 128, CU_TENSOR_MAP_SWIZZLE_64B);
         okm &= make_map(enc, &tm.dn_codes_s, CU_TENSOR_MAP_DATA_TYPE_UINT8, L->shared->down_nm.codes, H / 2, NS, H / 2,
-                        BN / 2, 64, CU_TENSOR_MAP_SWIZZLE_NONE);
+                        hs::kDnBand / 2, 64, CU_TENSOR_MAP_SWIZZLE_64B);
     }
     for (int b = 0; b < 8; ++b)
         okm &= make_map(enc, &tm.xg[b], CU_TENSOR_MAP_DATA_TYPE_FLOAT16, io.xg, H, rows_x, (uint64_t)H * 2, 64,
                         16u * (b + 1), CU_TENSOR_MAP_SWIZZLE_128B);
-    for (int b = 0; b < 2; ++b) {
-        const uint32_t br = 64u << b;
+    for (int b = 0; b < 8; ++b) {
+        const uint32_t br = 16u * (b + 1);
         okm &= make_map(enc, &tm.hr[b], CU_TENSOR_MAP_DATA_TYPE_FLOAT16, io.h_r, NR, (uint64_t)T * K, (uint64_t)NR * 2,
                         64, br, CU_TENSOR_MAP_SWIZZLE_128B);
         if (NS)
@@ -1077,7 +1060,7 @@ extern "C" int hs_moe_prefill(const hs_moe_layer* L, const uint16_t* x, const fl
     if (cudaGetDevice(&dev) != cudaSuccess) return HS_ERR_CUDA;
     if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return HS_ERR_CUDA;
     const int up_smem = hs::UpLayout::total(H);
-    const int dn_smem = hs::DownLayout(hs::down_band(H)).total;
+    const int dn_smem = hs::DownLayout::kTotal;
     if (set_smem_attr((const void*)hs::prefill_up_kernel, up_smem) != HS_OK) return HS_ERR_CUDA;
     if (set_smem_attr((const void*)hs::prefill_down_kernel, dn_smem) != HS_OK) return HS_ERR_CUDA;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
