@@ -755,7 +755,16 @@ prefill_down_kernel(const __grid_constant__ LayerParams P, const PrefillIO io, c
         // 32hh .. 32hh+31 of the tile (columns 16hh .. 16hh+15 of the A tile)
         const int dw = warp - kEpiWarps, g = dw / kDqGroup, hh = (dw % kDqGroup) >> 2, qd = warp & 3;
         const uint32_t trow = tmem_a + ((uint32_t)(32 * qd) << 16) + 16 * hh;
-        const int rbase = 32 * hh + (lane & 7), wsel = 4 * (lane >> 3);
+        // lane l takes word l/8 of the quadrant's 16-byte chunk in rows 32hh + 8k + l%8 (the
+        // word-level steps of the transpose done by the loads); 64-byte swizzle: chunk c of row r
+        // sits at chunk c ^ ((r >> 1) & 3)
+        int ldoff[4];
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            const int r = 32 * hh + (lane & 7) + 8 * k;
+            ldoff[k] = r * (kDnBand / 2) + ((qd ^ ((r >> 1) & 3)) << 4) + 4 * (lane >> 3);
+        }
+        const NibTrLane trc = nib_tr_lane();
         const __half2 k1024 = __floats2half2_rn(1024.f, 1024.f);
         uint32_t q = 0;
         for (int u = blockIdx.x; u < U && ok; u += gridDim.x) {
@@ -768,16 +777,10 @@ prefill_down_kernel(const __grid_constant__ LayerParams P, const PrefillIO io, c
                 tc_fence_after();
                 const int s = qk % kDnWD;
                 const uint8_t* cs = sW + s * DownLayout::kWSlot;
-                // lane l takes word l/8 of the quadrant's 16-byte chunk in rows 8k + l%8 (the word-level
-                // steps of the transpose done by the loads); 64-byte swizzle: chunk c of row r sits at
-                // chunk c ^ ((r >> 1) & 3)
                 uint32_t a[4];
 #pragma unroll
-                for (int k = 0; k < 4; ++k) {
-                    const int r = rbase + 8 * k;
-                    a[k] = *reinterpret_cast<const uint32_t*>(cs + r * (kDnBand / 2) + ((qd ^ ((r >> 1) & 3)) << 4) + wsel);
-                }
-                nib_transpose32_in_words(a);   // now: lane = output 32qd + lane, nibble j of word k = neuron 32hh + 8k + j
+                for (int k = 0; k < 4; ++k) a[k] = *reinterpret_cast<const uint32_t*>(cs + ldoff[k]);
+                nib_transpose32_in_words(a, trc);   // lane = output 32qd + lane, nibble j of word k = neuron 32hh + 8k + j
                 const float2 sbv = half2_to_float2(reinterpret_cast<const uint32_t*>(cs + DownLayout::kCodes)[32 * qd + lane]);
                 const __half2 s1 = __floats2half2_rn(sbv.x, sbv.x);
                 const __half2 s16 = __floats2half2_rn(sbv.x * 0.0625f, sbv.x * 0.0625f);
