@@ -281,7 +281,7 @@ constexpr unsigned kEpilogueSleepNs = 256;
 // 16-bit operand (loaded by TMA) together with its dequantised tile: its
 // "full" barrier completes when the TMA bytes have landed and the 8 warps of
 // the dequantising group have arrived; one MMA commit releases both.
-template <int WD, int SD>
+template <int WD, int SD, int DQ = kDqGroup>
 struct GemmBars {
     uint64_t *wfull, *wempty, *sfull, *sempty, *sbfull, *sbempty, *tfull, *tempty;
     uint32_t* tmem_slot;
@@ -293,8 +293,8 @@ struct GemmBars {
         tmem_slot = reinterpret_cast<uint32_t*>(tempty + 2);
     }
     __device__ void init() {
-        for (int i = 0; i < WD; ++i) { mbar_init(&wfull[i], 1); mbar_init(&wempty[i], kDqGroup); }
-        for (int i = 0; i < SD; ++i) { mbar_init(&sfull[i], kDqGroup + 1); mbar_init(&sempty[i], 1); }
+        for (int i = 0; i < WD; ++i) { mbar_init(&wfull[i], 1); mbar_init(&wempty[i], DQ); }
+        for (int i = 0; i < SD; ++i) { mbar_init(&sfull[i], DQ + 1); mbar_init(&sempty[i], 1); }
         for (int i = 0; i < 2; ++i) {
             mbar_init(&sbfull[i], 1); mbar_init(&sbempty[i], kDqWarps);
             mbar_init(&tfull[i], 1); mbar_init(&tempty[i], kEpiWarps);
@@ -599,8 +599,9 @@ prefill_up_kernel(const __grid_constant__ LayerParams P, const PrefillIO io, con
 // n0 n4 n1 n5 n2 n6 n3 n7, the order in which a code word yields nibble pairs, so no further
 // shuffling is needed.  The epilogue lane owns one output and writes it for every token.
 constexpr int kDnBand = 128;
-constexpr int kDnWD = 6, kDnSD = 4;
-using DnBars = GemmBars<kDnWD, kDnSD>;
+constexpr int kDnWD = 6, kDnSD = 6;
+constexpr int kDnDqGroup = 4;   // warps per dequantising group (one per TMEM lane quadrant); 4 groups
+using DnBars = GemmBars<kDnWD, kDnSD, kDnDqGroup>;
 
 struct DownLayout {
     static constexpr int kCodes = 64 * kDnBand / 2;     // 64 neurons x 64 bytes, 64-byte swizzle
@@ -750,57 +751,62 @@ prefill_down_kernel(const __grid_constant__ LayerParams P, const PrefillIO io, c
         }
         __syncwarp();
     } else if (warp >= kEpiWarps && warp < kWarpW) {
-        // ---- dequantise into TMEM: group g takes the k-steps q with q % 2 == g.  Warp (quadrant
-        // qd = warp % 4, half hh): outputs 32qd .. 32qd+31 of the band (TMEM lanes), neurons
-        // 32hh .. 32hh+31 of the tile (columns 16hh .. 16hh+15 of the A tile)
-        const int dw = warp - kEpiWarps, g = dw / kDqGroup, hh = (dw % kDqGroup) >> 2, qd = warp & 3;
-        const uint32_t trow = tmem_a + ((uint32_t)(32 * qd) << 16) + 16 * hh;
+        // ---- dequantise into TMEM: group g = (warp - 4) / 4 takes the k-steps q with q % 4 == g.
+        // Warp quadrant qd = warp % 4: outputs 32qd .. 32qd+31 of the band (TMEM lanes), all 64
+        // neurons of the tile (32 columns of the A tile), in two halves of 32 neurons
+        const int g = (warp - kEpiWarps) / kDnDqGroup, qd = warp & 3;
+        const uint32_t trow = tmem_a + ((uint32_t)(32 * qd) << 16);
         // lane l takes word l/8 of the quadrant's 16-byte chunk in rows 32hh + 8k + l%8 (the
         // word-level steps of the transpose done by the loads); 64-byte swizzle: chunk c of row r
         // sits at chunk c ^ ((r >> 1) & 3)
-        int ldoff[4];
+        int ldoff[2][4];
 #pragma unroll
-        for (int k = 0; k < 4; ++k) {
-            const int r = 32 * hh + (lane & 7) + 8 * k;
-            ldoff[k] = r * (kDnBand / 2) + ((qd ^ ((r >> 1) & 3)) << 4) + 4 * (lane >> 3);
-        }
+        for (int hh = 0; hh < 2; ++hh)
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+                const int r = 32 * hh + (lane & 7) + 8 * k;
+                ldoff[hh][k] = r * (kDnBand / 2) + ((qd ^ ((r >> 1) & 3)) << 4) + 4 * (lane >> 3);
+            }
         const NibTrLane trc = nib_tr_lane();
         const __half2 k1024 = __floats2half2_rn(1024.f, 1024.f);
         uint32_t q = 0;
         for (int u = blockIdx.x; u < U && ok; u += gridDim.x) {
             const DownUnit d = down_unit(P, io, nb, words, dense, u);
             const int nk = __popcll(d.live);
-            for (int kk = (int)((q & 1u) != (uint32_t)g); kk < nk; kk += 2) {
+            for (int kk = (g - (int)(q & 3u) + 4) & 3; kk < nk; kk += 4) {
                 const uint32_t qk = q + kk;
                 ok = __all_sync(0xffffffffu, wait_full(br.wfull, kDnWD, qk) && wait_free(br.sempty, kDnSD, qk));
                 if (!ok) break;
                 tc_fence_after();
                 const int s = qk % kDnWD;
                 const uint8_t* cs = sW + s * DownLayout::kWSlot;
-                uint32_t a[4];
-#pragma unroll
-                for (int k = 0; k < 4; ++k) a[k] = *reinterpret_cast<const uint32_t*>(cs + ldoff[k]);
-                nib_transpose32_in_words(a, trc);   // lane = output 32qd + lane, nibble j of word k = neuron 32hh + 8k + j
                 const float2 sbv = half2_to_float2(reinterpret_cast<const uint32_t*>(cs + DownLayout::kCodes)[32 * qd + lane]);
                 const __half2 s1 = __floats2half2_rn(sbv.x, sbv.x);
                 const __half2 s16 = __floats2half2_rn(sbv.x * 0.0625f, sbv.x * 0.0625f);
                 const __half2 b2 = __floats2half2_rn(sbv.y, sbv.y);
-                uint32_t o[16];
+                uint32_t o[32];
 #pragma unroll
-                for (int k = 0; k < 4; ++k) {
-                    const uint32_t lo = a[k], hi = a[k] >> 8;
-                    // fp16 1024 + c (or 1024 + 16c): nibble pairs (0,4) (1,5) (2,6) (3,7)
-                    const uint32_t pr[4] = {(lo & 0x000F000Fu) | 0x64006400u, (lo & 0x00F000F0u) | 0x64006400u,
-                                            (hi & 0x000F000Fu) | 0x64006400u, (hi & 0x00F000F0u) | 0x64006400u};
+                for (int hh = 0; hh < 2; ++hh) {
+                    uint32_t a[4];
 #pragma unroll
-                    for (int pp = 0; pp < 4; ++pp) {
-                        const __half2 qv = __hsub2(*reinterpret_cast<const __half2*>(&pr[pp]), k1024);
-                        const __half2 v = __hfma2(qv, (pp & 1) ? s16 : s1, b2);
-                        o[4 * k + pp] = *reinterpret_cast<const uint32_t*>(&v);
+                    for (int k = 0; k < 4; ++k) a[k] = *reinterpret_cast<const uint32_t*>(cs + ldoff[hh][k]);
+                    nib_transpose32_in_words(a, trc);   // lane = output 32qd + lane, nibble j of word k = neuron 32hh + 8k + j
+#pragma unroll
+                    for (int k = 0; k < 4; ++k) {
+                        const uint32_t lo = a[k], hi = a[k] >> 8;
+                        // fp16 1024 + c (or 1024 + 16c): nibble pairs (0,4) (1,5) (2,6) (3,7)
+                        const uint32_t pr[4] = {(lo & 0x000F000Fu) | 0x64006400u, (lo & 0x00F000F0u) | 0x64006400u,
+                                                (hi & 0x000F000Fu) | 0x64006400u, (hi & 0x00F000F0u) | 0x64006400u};
+#pragma unroll
+                        for (int pp = 0; pp < 4; ++pp) {
+                            const __half2 qv = __hsub2(*reinterpret_cast<const __half2*>(&pr[pp]), k1024);
+                            const __half2 v = __hfma2(qv, (pp & 1) ? s16 : s1, b2);
+                            o[16 * hh + 4 * k + pp] = *reinterpret_cast<const uint32_t*>(&v);
+                        }
                     }
                 }
                 __syncwarp();
-                tmem_st16(trow + 32 * (qk % kDnSD), o);
+                tmem_st32(trow + 32 * (qk % kDnSD), o);
                 tmem_st_wait();
                 tc_fence_before();
                 __syncwarp();
