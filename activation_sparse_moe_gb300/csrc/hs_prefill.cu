@@ -398,8 +398,12 @@ prefill_up_kernel(const __grid_constant__ LayerParams P, const PrefillIO io, con
         if (lane == 0) {
             const uint64_t pol_stream = policy_evict_first(), pol_keep = policy_evict_last();
             uint32_t wq = 0, nsb = 0;
+            // the next unit's descriptor is loaded one unit ahead (its loads overlap this unit's work)
+            UpUnit dnext;
+            if ((int)blockIdx.x < U) dnext = up_unit(P, io, ntr, mr, ms, blockIdx.x);
             for (int u = blockIdx.x; u < U && ok; u += gridDim.x) {
-                const UpUnit d = up_unit(P, io, ntr, mr, ms, u);
+                const UpUnit d = dnext;
+                if (u + (int)gridDim.x < U) dnext = up_unit(P, io, ntr, mr, ms, u + gridDim.x);
                 const int b = nsb & 1;
                 if (!(ok = wait_free_sleep(br.sbempty, 2, nsb, kProducerSleepNs))) break;
                 mbar_arrive_expect_tx(&br.sbfull[b], (uint32_t)d.rows * G * 4);
@@ -425,8 +429,12 @@ prefill_up_kernel(const __grid_constant__ LayerParams P, const PrefillIO io, con
         if (lane == 0) {
             const uint64_t pol = policy_evict_last();
             uint32_t xq = 0;
+            // the next unit's descriptor is loaded one unit ahead (its loads overlap this unit's work)
+            UpUnit dnext;
+            if ((int)blockIdx.x < U) dnext = up_unit(P, io, ntr, mr, ms, blockIdx.x);
             for (int u = blockIdx.x; u < U && ok; u += gridDim.x) {
-                const UpUnit d = up_unit(P, io, ntr, mr, ms, u);
+                const UpUnit d = dnext;
+                if (u + (int)gridDim.x < U) dnext = up_unit(P, io, ntr, mr, ms, u + gridDim.x);
                 // a box of exactly the tile's rows rounded up to 16 (the MMA's N)
                 const CUtensorMap* xmap = &tm.xg[d.nt16 / 16 - 1];
                 const uint32_t bytes = (uint32_t)d.nt16 * 128;
@@ -447,8 +455,12 @@ prefill_up_kernel(const __grid_constant__ LayerParams P, const PrefillIO io, con
         // ---- MMA issue: A (weights) from TMEM, B (tokens) from shared memory
         if (lane == 0) {
             uint32_t sq = 0, nu = 0;
+            // the next unit's descriptor is loaded one unit ahead (its loads overlap this unit's work)
+            UpUnit dnext;
+            if ((int)blockIdx.x < U) dnext = up_unit(P, io, ntr, mr, ms, blockIdx.x);
             for (int u = blockIdx.x; u < U && ok; u += gridDim.x, ++nu) {
-                const UpUnit d = up_unit(P, io, ntr, mr, ms, u);
+                const UpUnit d = dnext;
+                if (u + (int)gridDim.x < U) dnext = up_unit(P, io, ntr, mr, ms, u + gridDim.x);
                 const int acc = nu & 1;
                 if (!(ok = wait_free(br.tempty, 2, nu))) break;
                 tc_fence_after();
@@ -482,8 +494,12 @@ prefill_up_kernel(const __grid_constant__ LayerParams P, const PrefillIO io, con
         const uint32_t trow = tmem_a + ((uint32_t)(32 * (warp & 3)) << 16) + 32 * h;
         uint32_t q = 0, nsb = 0;
         const __half2 k1024 = __floats2half2_rn(1024.f, 1024.f);
+        // the next unit's descriptor is loaded one unit ahead (its loads overlap this unit's work)
+        UpUnit dnext;
+        if ((int)blockIdx.x < U) dnext = up_unit(P, io, ntr, mr, ms, blockIdx.x);
         for (int u = blockIdx.x; u < U && ok; u += gridDim.x) {
-            const UpUnit d = up_unit(P, io, ntr, mr, ms, u);
+            const UpUnit d = dnext;
+            if (u + (int)gridDim.x < U) dnext = up_unit(P, io, ntr, mr, ms, u + gridDim.x);
             const int b = nsb & 1;
             ok = __all_sync(0xffffffffu, wait_full(br.sbfull, 2, nsb));
             if (!ok) break;
@@ -543,8 +559,12 @@ prefill_up_kernel(const __grid_constant__ LayerParams P, const PrefillIO io, con
     } else if (warp < kEpiWarps) {
         // ---- epilogue: + offset, ReLU^2, H (fp16) and the live flags of the block's 64-neuron tiles
         uint32_t nu = 0;
+        // the next unit's descriptor is loaded one unit ahead (its loads overlap this unit's work)
+        UpUnit dnext;
+        if ((int)blockIdx.x < U) dnext = up_unit(P, io, ntr, mr, ms, blockIdx.x);
         for (int u = blockIdx.x; u < U && ok; u += gridDim.x, ++nu) {
-            const UpUnit d = up_unit(P, io, ntr, mr, ms, u);
+            const UpUnit d = dnext;
+            if (u + (int)gridDim.x < U) dnext = up_unit(P, io, ntr, mr, ms, u + gridDim.x);
             const int acc = nu & 1;
             const int r = 32 * warp + lane, n = d.row0 + r;
             const bool rowok = r < d.rows;
@@ -676,8 +696,12 @@ prefill_down_kernel(const __grid_constant__ LayerParams P, const PrefillIO io, c
         if (lane == 0) {
             const uint64_t pol_stream = policy_evict_first(), pol_keep = policy_evict_last();
             uint32_t wq = 0;
+            // the next unit's descriptor is loaded one unit ahead (its loads overlap this unit's work)
+            DownUnit dnext;
+            if ((int)blockIdx.x < U) dnext = down_unit(P, io, nb, words, dense, blockIdx.x);
             for (int u = blockIdx.x; u < U && ok; u += gridDim.x) {
-                const DownUnit d = down_unit(P, io, nb, words, dense, u);
+                const DownUnit d = dnext;
+                if (u + (int)gridDim.x < U) dnext = down_unit(P, io, nb, words, dense, u + gridDim.x);
                 const CUtensorMap* cmap = d.shared ? &tm.dn_codes_s : &tm.dn_codes_r;
                 const uint64_t pol = d.shared ? pol_keep : pol_stream;
                 const int nk = __popcll(d.live);
@@ -707,8 +731,12 @@ prefill_down_kernel(const __grid_constant__ LayerParams P, const PrefillIO io, c
         if (lane == 0) {
             const uint64_t pol = policy_evict_last();
             uint32_t xq = 0;
+            // the next unit's descriptor is loaded one unit ahead (its loads overlap this unit's work)
+            DownUnit dnext;
+            if ((int)blockIdx.x < U) dnext = down_unit(P, io, nb, words, dense, blockIdx.x);
             for (int u = blockIdx.x; u < U && ok; u += gridDim.x) {
-                const DownUnit d = down_unit(P, io, nb, words, dense, u);
+                const DownUnit d = dnext;
+                if (u + (int)gridDim.x < U) dnext = down_unit(P, io, nb, words, dense, u + gridDim.x);
                 const CUtensorMap* hmap = d.shared ? &tm.hsh[d.nt16 / 16 - 1] : &tm.hr[d.nt16 / 16 - 1];
                 for (uint64_t lm = d.live; lm && ok;) {
                     const int j = pop_live(lm);
@@ -726,8 +754,12 @@ prefill_down_kernel(const __grid_constant__ LayerParams P, const PrefillIO io, c
         // ---- MMA issue: A (weights) from TMEM, B (h) from shared memory
         if (lane == 0) {
             uint32_t sq = 0, nu = 0;
+            // the next unit's descriptor is loaded one unit ahead (its loads overlap this unit's work)
+            DownUnit dnext;
+            if ((int)blockIdx.x < U) dnext = down_unit(P, io, nb, words, dense, blockIdx.x);
             for (int u = blockIdx.x; u < U && ok; u += gridDim.x, ++nu) {
-                const DownUnit d = down_unit(P, io, nb, words, dense, u);
+                const DownUnit d = dnext;
+                if (u + (int)gridDim.x < U) dnext = down_unit(P, io, nb, words, dense, u + gridDim.x);
                 const int acc = nu & 1;
                 if (!(ok = wait_free(br.tempty, 2, nu))) break;
                 tc_fence_after();
@@ -770,8 +802,12 @@ prefill_down_kernel(const __grid_constant__ LayerParams P, const PrefillIO io, c
         const NibTrLane trc = nib_tr_lane();
         const __half2 k1024 = __floats2half2_rn(1024.f, 1024.f);
         uint32_t q = 0;
+        // the next unit's descriptor is loaded one unit ahead (its loads overlap this unit's work)
+        DownUnit dnext;
+        if ((int)blockIdx.x < U) dnext = down_unit(P, io, nb, words, dense, blockIdx.x);
         for (int u = blockIdx.x; u < U && ok; u += gridDim.x) {
-            const DownUnit d = down_unit(P, io, nb, words, dense, u);
+            const DownUnit d = dnext;
+            if (u + (int)gridDim.x < U) dnext = down_unit(P, io, nb, words, dense, u + gridDim.x);
             const int nk = __popcll(d.live);
             for (int kk = (g - (int)(q & 3u) + 4) & 3; kk < nk; kk += 4) {
                 const uint32_t qk = q + kk;
@@ -821,8 +857,12 @@ prefill_down_kernel(const __grid_constant__ LayerParams P, const PrefillIO io, c
     } else if (warp < kEpiWarps) {
         // ---- epilogue: lane = output of the band; router-weighted partial rows of the tile's tokens
         uint32_t nu = 0;
+        // the next unit's descriptor is loaded one unit ahead (its loads overlap this unit's work)
+        DownUnit dnext;
+        if ((int)blockIdx.x < U) dnext = down_unit(P, io, nb, words, dense, blockIdx.x);
         for (int u = blockIdx.x; u < U && ok; u += gridDim.x, ++nu) {
-            const DownUnit d = down_unit(P, io, nb, words, dense, u);
+            const DownUnit d = dnext;
+            if (u + (int)gridDim.x < U) dnext = down_unit(P, io, nb, words, dense, u + gridDim.x);
             const int acc = nu & 1;
             const int col = kDnBand * d.ob + 32 * warp + lane;
             float* pbase = io.partial + (d.shared ? (size_t)io.T * K + d.row0 : (size_t)d.row0) * H + col;
