@@ -326,7 +326,8 @@ __device__ __forceinline__ void drain_loads(uint64_t* full, int d, uint32_t issu
 // 128 inputs (two scale groups).  TMEM: columns 0-255 the two accumulators, 256-511 four
 // dequantised A tiles (128 lanes x 64 columns = 128 rows x 128 fp16 each).
 constexpr int kUpWD = 5, kUpSD = 4;
-using UpBars = GemmBars<kUpWD, kUpSD>;
+constexpr int kUpDqGroup = 4;   // warps per dequantising group (one per TMEM lane quadrant); 4 groups
+using UpBars = GemmBars<kUpWD, kUpSD, kUpDqGroup>;
 constexpr int kUpK = 128;                  // inputs per k-step
 
 struct UpLayout {
@@ -486,12 +487,13 @@ prefill_up_kernel(const __grid_constant__ LayerParams P, const PrefillIO io, con
         }
         __syncwarp();
     } else if (warp >= kEpiWarps && warp < kWarpW) {
-        // ---- dequantise into TMEM: group g takes the k-steps q with q % 2 == g.  Thread (row r,
-        // half h) converts the 64 codes of scale group 2k+h and writes columns 32h..32h+31 of row r;
-        // each column holds two codes of one word in the order (c0 c4) (c1 c5) (c2 c6) (c3 c7)
-        const int dw = warp - kEpiWarps, g = dw / kDqGroup, h = (dw % kDqGroup) >> 2;
+        // ---- dequantise into TMEM: group g = (warp - 4) / 4 takes the k-steps q with q % 4 == g.
+        // Thread (row r) converts the 128 codes of scale groups 2k and 2k+1 (halves h = 0, 1) and
+        // writes columns 32h..32h+31 of row r; each column holds two codes of one word in the
+        // order (c0 c4) (c1 c5) (c2 c6) (c3 c7)
+        const int g = (warp - kEpiWarps) / kUpDqGroup;
         const int r = 32 * (warp & 3) + lane;
-        const uint32_t trow = tmem_a + ((uint32_t)(32 * (warp & 3)) << 16) + 32 * h;
+        const uint32_t trow = tmem_a + ((uint32_t)(32 * (warp & 3)) << 16);
         uint32_t q = 0, nsb = 0;
         const __half2 k1024 = __floats2half2_rn(1024.f, 1024.f);
         // the next unit's descriptor is loaded one unit ahead (its loads overlap this unit's work)
@@ -503,13 +505,15 @@ prefill_up_kernel(const __grid_constant__ LayerParams P, const PrefillIO io, con
             const int b = nsb & 1;
             ok = __all_sync(0xffffffffu, wait_full(br.sbfull, 2, nsb));
             if (!ok) break;
-            const uint32_t* sbr = sSB + b * sbw + r * G + h;
-            for (int k = (int)((q & 1u) != (uint32_t)g); k < KS; k += 2) {
+            const uint32_t* sbr = sSB + b * sbw + r * G;
+            for (int k = (g - (int)(q & 3u) + 4) & 3; k < KS; k += 4) {
                 const uint32_t qk = q + k;
                 ok = __all_sync(0xffffffffu, wait_full(br.wfull, kUpWD, qk) && wait_free(br.sempty, kUpSD, qk));
                 if (!ok) break;
                 tc_fence_after();
                 const int s = qk % kUpWD;
+#pragma unroll
+                for (int h = 0; h < 2; ++h) {
                 uint32_t o[32];
                 if (r < d.rows) {
                     // the codes tile arrives with the 64-byte swizzle: 16-byte chunk c of row r sits at
@@ -518,7 +522,7 @@ prefill_up_kernel(const __grid_constant__ LayerParams P, const PrefillIO io, con
                     const int sw = (r >> 1) & 3;
                     const uint4 c0 = *reinterpret_cast<const uint4*>(crow + (((2 * h) ^ sw) << 4));
                     const uint4 c1 = *reinterpret_cast<const uint4*>(crow + (((2 * h + 1) ^ sw) << 4));
-                    const float2 sbv = half2_to_float2(sbr[2 * k]);
+                    const float2 sbv = half2_to_float2(sbr[2 * k + h]);
                     const __half2 s1 = __floats2half2_rn(sbv.x, sbv.x);
                     const __half2 s16 = __floats2half2_rn(sbv.x * 0.0625f, sbv.x * 0.0625f);
                     const __half2 b2 = __floats2half2_rn(sbv.y, sbv.y);
@@ -541,7 +545,8 @@ prefill_up_kernel(const __grid_constant__ LayerParams P, const PrefillIO io, con
                     for (int i = 0; i < 32; ++i) o[i] = 0u;
                 }
                 __syncwarp();
-                tmem_st32(trow + 64 * (qk % kUpSD), o);
+                tmem_st32(trow + 64 * (qk % kUpSD) + 32 * h, o);
+                }
                 tmem_st_wait();
                 tc_fence_before();
                 __syncwarp();
