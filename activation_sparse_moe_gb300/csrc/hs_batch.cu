@@ -29,13 +29,15 @@
 //  5. reduce: y[t] = sum of the token's partial rows in slot order; bf16.
 #include "hs_host.h"
 
+#include <algorithm>
+
 namespace hs {
 
 constexpr int kTC = 2;          // tokens per up unit
 constexpr int kUpRows = 32;     // neuron rows per up unit (two 16-row chunks)
 constexpr int kUpThreads = 128; // threads of an up CTA
 constexpr int kUpCtasPerSm = 4;
-constexpr int kFusedMaxBatch = 8;  // batches up to this size take the fused path
+constexpr int kFusedMaxBatch = 64;  // batches up to this size take the fused path (unless HS_BATCH_EXPERT_UNION)
 constexpr int kFTok = 4;            // tokens per fused unit
 constexpr int kMaxBatch = 64;
 constexpr int kBand = 128;      // outputs per down unit
@@ -1175,7 +1177,8 @@ BatchLayout batch_layout(const hs_moe_layer* L, int B) {
     l.mask_r = take((size_t)E * (NR / 32) * 4);
     l.mask_s = take((size_t)(NS ? NS / 32 : 1) * 4);
     const int Ut = (NS / 64) + K * (NR / 64);
-    l.partial = take(B <= hs::kFusedMaxBatch ? (size_t)B * Ut * H * 4 : (size_t)B * (SC + K) * H * 4);
+    // the fused path's partial rows (per token, slot and group) or the banded path's (per token and slot)
+    l.partial = take((size_t)B * std::max(Ut, SC + K) * H * 4);
     l.total = o;
     return l;
 }
@@ -1247,7 +1250,7 @@ int hs_batch_decode(const hs_moe_layer* L, const uint16_t* x, const float* logit
     hs::batch_route_kernel<<<dim3(batch), dim3(256), 0, s>>>(P, io);
     if (cudaGetLastError() != cudaSuccess) return HS_ERR_CUDA;
     if (launch_pdl(hs::batch_plan_kernel, dim3(1), dim3(512), 0, s, P, io) != cudaSuccess) return HS_ERR_CUDA;
-    if (batch <= hs::kFusedMaxBatch) {
+    if (batch <= hs::kFusedMaxBatch && !(flags & HS_BATCH_EXPERT_UNION)) {
         const int f_smem = hs::FusedSmem::total(L->hidden);
         const int Ut = (L->shared ? L->shared->neurons / 64 : 0) + L->top_k * (L->routed[0].neurons / 64);
         if (set_smem_attr((const void*)hs::batch_fused_kernel, f_smem) != HS_OK) return HS_ERR_CUDA;

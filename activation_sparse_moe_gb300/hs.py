@@ -23,6 +23,7 @@ HS_ERR_WORKSPACE = -4
 HS_ERR_CUDA = -5
 HS_ERR_TIMEOUT = -6
 HS_FORCE_DENSE = 0x1
+HS_BATCH_EXPERT_UNION = 0x2
 
 
 class HsError(RuntimeError):

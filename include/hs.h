@@ -70,6 +70,12 @@ typedef struct CUstream_st* hs_stream_t;
                                  the dense comparison path through the same
                                  kernels (section "The standard way reads
                                  everything"); results equal the sparse path */
+#define HS_BATCH_EXPERT_UNION 0x2u  /* batch decode only: read each expert's
+                                 weights and the union of ALL its tokens' live
+                                 rows exactly once (banded up / down kernels)
+                                 instead of once per group of up to 4 of its
+                                 tokens (fused kernel, the default); results
+                                 agree within the stated tolerance */
 
 /* One 4-bit projection in one of the layouts above. */
 typedef struct {
@@ -181,9 +187,12 @@ int hs_expert_down_sparse_noalloc(const float* h_dev, const hs_w4* down_nm, int 
  *   y_bf16_dev       [batch][hidden] bf16, required;  y_f32_dev fp32 or NULL
  *   debug            host pointer to device debug outputs, or NULL
  * batch 1..64.  For batch > 1 the tokens are grouped by expert (section
- * "Sorted by expert") and each expert reads the union of its tokens' live
- * rows once; hidden must then be a multiple of 128, neurons <= 3712, and the
- * debug h dump is not available (HS_ERR_INVALID_ARG).  Deterministic.
+ * "Sorted by expert") and each unit of work (expert, 64-neuron group, up to
+ * 4 of the expert's tokens) reads its weights and the union of its tokens'
+ * live rows once; with HS_BATCH_EXPERT_UNION each expert reads the union of
+ * all its tokens' live rows once.  hidden must then be a multiple of 128,
+ * neurons <= 3712, and the debug h dump is not available
+ * (HS_ERR_INVALID_ARG).  Deterministic.
  * Calls sharing one workspace must not overlap on the GPU. */
 size_t hs_moe_layer_decode_workspace_size(const hs_moe_layer* layer, int batch);
 int hs_moe_layer_decode(const hs_moe_layer* layer, const uint16_t* x_bf16_dev,

@@ -61,8 +61,8 @@ def union_rows(ref, L):
     return n, ng
 
 
-def check_batch(L, dl, X, LG, K, what, flips_allowed=4):
-    y, yf, dbg = run_batch(dl, X, LG)
+def check_batch(L, dl, X, LG, K, what, flips_allowed=4, flags=0):
+    y, yf, dbg = run_batch(dl, X, LG, flags=flags)
     ref = oracle.moe_tokens(X, LG, L.routed_expert, L.shared, k=K)
     assert np.array_equal(dbg["topk_idx"].numpy(), ref["idx"]), what
     np.testing.assert_allclose(dbg["topk_w"].double().numpy(), ref["w"], rtol=2e-6, atol=1e-7)
@@ -106,6 +106,20 @@ def test_config4_parity(cfg4_layer, B):
     check_batch(L, dl, X, LG, 6, f"config 4 B={B}", flips_allowed=8)
 
 
+@pytest.mark.parametrize("B", [8, 64])
+def test_config4_parity_expert_union_path(cfg4_layer, B):
+    """HS_BATCH_EXPERT_UNION: every expert reads the union of all its tokens'
+    live rows once (banded kernels); same oracle bar, and the union count is
+    the same as the default path's."""
+    L, dl = cfg4_layer
+    X, LG = synth.tokens(0, "cfg4", B, B)
+    y1, yf1, d1 = check_batch(L, dl, X, LG, 6, f"config 4 B={B} expert union", flips_allowed=8,
+                              flags=hs.HS_BATCH_EXPERT_UNION)
+    y2, yf2, d2 = run_batch(dl, X, LG)
+    assert int(d1["live_rows"].item()) == int(d2["live_rows"].item())
+    assert int(d1["live_groups"].item()) == int(d2["live_groups"].item())
+
+
 def test_config4_dense_flag_and_determinism(cfg4_layer):
     L, dl = cfg4_layer
     X, LG = synth.tokens(0, "cfg4", 8, 8)
@@ -117,3 +131,9 @@ def test_config4_dense_flag_and_determinism(cfg4_layer):
     ntouched = len(np.unique(d1["topk_idx"].numpy()))
     assert int(dd["live_rows"].item()) == ntouched * synth.N_ROUTED + synth.N_SHARED
     assert int(d1["live_rows"].item()) < int(dd["live_rows"].item())
+    # the same on the banded path
+    f = hs.HS_BATCH_EXPERT_UNION
+    yu, yfu, du = run_batch(dl, X, LG, flags=f)
+    yud, yfud, dud = run_batch(dl, X, LG, flags=f | hs.HS_FORCE_DENSE)
+    assert np.array_equal(yfu, yfud) and torch.equal(yu, yud)
+    assert int(dud["live_rows"].item()) == ntouched * synth.N_ROUTED + synth.N_SHARED
