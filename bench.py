@@ -255,10 +255,19 @@ def bench_batch(args, dev, stream, timed, bytemodel, hs):
         K = max(10, args.steps // 4)
         ms, _ = timed(g, K, 3, repeats=3)
         us = ms * 1e3 / (K * n_layers)
+        # the same calls with every expert reading the union of all its tokens' live rows once
+        gu = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(gu, stream=stream):
+            for l, dl in enumerate(layers):
+                hs.hs_moe_layer_decode(dl.c, X[l], LG[l], B, Y[l], None, hs.HS_BATCH_EXPERT_UNION, None, WS,
+                                       stream=stream)
+        ms_u, _ = timed(gu, K, 3, repeats=3)
+        us_u = ms_u * 1e3 / (K * n_layers)
         out[f"B{B}"] = {"us_per_layer": round(us, 3), "us_per_token_layer": round(us / B, 4),
                         "required_MB_per_layer": round(req / n_layers / 1e6, 2),
-                        "achieved_GBs": round(req / n_layers / (us * 1e-6) / 1e9, 1)}
-        del g, WS
+                        "achieved_GBs": round(req / n_layers / (us * 1e-6) / 1e9, 1),
+                        "expert_union_path_us_per_layer": round(us_u, 3)}
+        del g, gu, WS
     del layers
     torch.cuda.empty_cache()
     return out
