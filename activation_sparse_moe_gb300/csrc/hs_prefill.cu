@@ -201,10 +201,17 @@ __global__ void __launch_bounds__(kListThreads) prefill_list_kernel(const __grid
     pdl_trigger();
     const int E = P.n_routed, K = P.top_k, H = P.hidden, n = io.T * K;
     const int b = blockIdx.x, t0 = b * kTokBlk, nt = min(kTokBlk, io.T - t0), t = threadIdx.x;
-    // expert offsets of this token block
+    // expert offsets of this token block: the expert's offset plus its pairs in earlier blocks,
+    // loaded 16 blocks at a time so that the loads are in flight together
     for (int e = t; e < E; e += blockDim.x) {
         int c = __ldcg(&io.meta->off[e]);
-        for (int bb = 0; bb < b; ++bb) c += __ldcg(&io.blk_cnt[bb * E + e]);
+        for (int b0 = 0; b0 < b; b0 += 16) {
+            int v[16];
+#pragma unroll
+            for (int i = 0; i < 16; ++i) v[i] = b0 + i < b ? __ldcg(&io.blk_cnt[(b0 + i) * E + e]) : 0;
+#pragma unroll
+            for (int i = 0; i < 16; ++i) c += v[i];
+        }
         base_e[e] = c;
     }
     for (int i = t; i < nt * K; i += blockDim.x) e_of[i] = __ldcg(io.idx + (size_t)t0 * K + i);
