@@ -321,6 +321,7 @@ def bench_prefill(args, dev, stream, timed, hs, peaks):
     expert's neurons permanently dead, p = 0.1 on the rest).  Roofline: the
     tensor cores (fp16 operands, fp32 accumulation) against the measured dense
     bf16 GEMM peak (same rate for fp16); the weights (0.73 GB) exceed L2."""
+    import numpy as np
     import torch
     import synth
     from activation_sparse_moe_gb300.layer import DeviceLayer, from_synth_expert, from_synth_stack
@@ -372,7 +373,37 @@ def bench_prefill(args, dev, stream, timed, hs, peaks):
                         "flops": "up dense + down over union-live rows per (expert, token tile)",
                         "executed_TFLOPs": round((up_flops + down_exec) / (us * 1e-6) / 1e12, 1)},
            "operands": "fp16 x fp16 -> fp32 (tcgen05.mma kind::f16, accumulators in TMEM)"}
-    del g_sparse, g_dense, WS, dl
+    del g_sparse, g_dense, dl
+    # our sub-configuration: the same 30% dead, but as whole 64-neuron groups (seeded choice per
+    # expert, shared included), so that the tile skip has whole tiles to skip
+    L = synth.layer_inputs(0, "cfg5", 0, p=0.1, p_shared=0.1, dead_frac=0.0, device=dev)
+    rng = np.random.default_rng(5)
+    for offs in [L.offsets[e] for e in range(L.offsets.shape[0])] + [L.shared.offset]:
+        ng = offs.shape[0] // 64
+        for gi in rng.choice(ng, size=int(round(0.3 * ng)), replace=False):
+            offs[64 * int(gi):64 * (int(gi) + 1)] = float("-inf")
+    dl = DeviceLayer(from_synth_stack(L.up, L.down, L.offsets, dev), from_synth_expert(L.shared, dev), 6)
+    del L
+    with torch.cuda.stream(stream):
+        hs.hs_moe_prefill(dl.c, X, LG, T, Y, None, 0, dbg, WS, stream=stream)
+    stream.synchronize()
+    assert hs.hs_device_status() == hs.HS_OK
+    tiles_c = [int(v) for v in dbg["tiles"].cpu()]
+    work_c = [int(v) for v in dbg["work"].cpu()]
+    g_c, g_cd = graph(0), graph(hs.HS_FORCE_DENSE)
+    ms_c = timed(g_c, K, 3, repeats=3)[0]
+    ms_cd = timed(g_cd, K, 3, repeats=3)[0]
+    us_c = ms_c * 1e3 / K
+    alg_c = up_flops + 2 * H * work_c[0]
+    out["clustered_dead"] = {
+        "note": "ours: the 30% dead neurons as whole 64-neuron groups (the tile skip's best case)",
+        "us_per_chunk": round(us_c, 2), "us_per_chunk_dense_flag": round(ms_cd * 1e3 / K, 2),
+        "skipped_tiles": tiles_c[0], "considered_tiles": tiles_c[1],
+        "gflop_down_union_live": round(2 * H * work_c[0] / 1e9, 2),
+        "gflop_down_executed": round(2 * H * work_c[1] / 1e9, 2),
+        "achieved_TFLOPs": round(alg_c / (us_c * 1e-6) / 1e12, 1),
+        "frac": round(alg_c / (us_c * 1e-6) / 1e12 / peak, 4)}
+    del g_c, g_cd, WS, dl
     torch.cuda.empty_cache()
     return out
 
