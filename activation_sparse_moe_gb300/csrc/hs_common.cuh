@@ -112,25 +112,6 @@ __device__ __forceinline__ bool mbar_wait_sleep(uint64_t* bar, uint32_t parity, 
     return true;
 }
 
-// Barrier `id` (1..15) among `threads` threads (whole warps) of the CTA.
-__device__ __forceinline__ void named_bar_sync(int id, int threads) {
-    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(threads) : "memory");
-}
-
-// Barrier `id` among `threads` threads that also ANDs a predicate over them.
-__device__ __forceinline__ bool named_bar_and(int id, int threads, bool pred) {
-    uint32_t r;
-    asm volatile(
-        "{\n .reg .pred p, q;\n"
-        " setp.ne.u32 p, %1, 0;\n"
-        " bar.red.and.pred q, %2, %3, p;\n"
-        " selp.u32 %0, 1, 0, q;\n}"
-        : "=r"(r)
-        : "r"((uint32_t)pred), "r"(id), "r"(threads)
-        : "memory");
-    return r != 0;
-}
-
 // L2 policy for weights that are streamed once per call.
 __device__ __forceinline__ uint64_t policy_evict_first() {
     uint64_t p;
