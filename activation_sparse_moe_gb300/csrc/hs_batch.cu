@@ -13,9 +13,9 @@
 // dependent launch between the kernels):
 //  1. route:  one CTA per token: top-k + softmax (warp 0), per-expert pair
 //             counts (integer atomics), and the token's fixed-point x table
-//             for the integer-pipe GEMV (all threads).
-//  2. plan:   one CTA: pair offsets, (token, slot) pairs grouped by expert in
-//             token order, work-unit tables, zeroed union masks.
+//             for the integer-pipe GEMV (all threads).  The last CTA to finish
+//  2. plans:  pair offsets, (token, slot) pairs grouped by expert in token
+//             order, work-unit tables, zeroed union masks.
 //  3. up:     four persistent CTAs per SM over units (expert, 32 neuron rows,
 //             <= 2 tokens) handed out by an atomic ticket, shared expert first:
 //             two chunked bulk copies per unit, DP4A fixed-point
@@ -55,6 +55,7 @@ struct BatchMeta {
     int up_next;                    // next up unit to hand out (atomic ticket)
     int fu_off[kMaxRouted + 1];     // fused-path unit offsets per touched index
     int fu_units, fu_shared, fu_next;
+    int route_done;                 // route CTAs finished (the last one plans the batch)
     int touched[kMaxRouted];        // routed experts with tokens, ascending
     int e_off[kMaxRouted + 1];      // grouped pair offsets per expert id
     int up_off[kMaxRouted + 2];     // up unit offsets per touched index (+ shared)
@@ -88,29 +89,6 @@ struct BatchIO {
     int* live_groups;
 };
 
-// ------------------------------------------------------------------ route
-__global__ void __launch_bounds__(256) batch_route_kernel(const __grid_constant__ LayerParams P, const BatchIO io) {
-    __shared__ __align__(16) int s_idx[kMaxTopK];
-    __shared__ __align__(16) float s_w[kMaxTopK];
-    pdl_wait();
-    pdl_trigger();
-    const int b = blockIdx.x, t = threadIdx.x;
-    const int K = P.top_k, E = P.n_routed, H = P.hidden, G = H / 64;
-    if (t < 32) {
-        warp_topk_softmax(io.logits + (size_t)b * E, E, K, s_idx, s_w);
-        __syncwarp();
-        if (t < K) {
-            const int p = b * K + t;
-            io.topk_idx[p] = s_idx[t];
-            io.topk_w[p] = s_w[t];
-            atomicAdd(&io.meta->cnt[s_idx[t]], 1);
-            if (io.dbg_topk_idx) { io.dbg_topk_idx[p] = s_idx[t]; io.dbg_topk_w[p] = s_w[t]; }
-        }
-    }
-    // the token's fixed-point x table (read by every up unit that has this token)
-    convert_x_fixed(io.x + (size_t)b * H, G, io.xt + (size_t)b * G * kXfStride, io.xsc + (size_t)b * G * 2, 0);
-}
-
 // ------------------------------------------------------------------ plan
 // Inclusive sum over the threads of a CTA of at most 32 warps; `tmp` holds 32 ints.
 __device__ __forceinline__ int block_incl_sum(int v, int* tmp) {
@@ -128,18 +106,19 @@ __device__ __forceinline__ int block_incl_sum(int v, int* tmp) {
     return v + before;
 }
 
-__global__ void __launch_bounds__(512) batch_plan_kernel(const __grid_constant__ LayerParams P, const BatchIO io) {
+// Run by the last route CTA to finish: pair offsets per expert, the touched
+// experts, the unit tables of both paths, the pairs grouped by expert in
+// token order, and cleared union masks.
+__device__ __noinline__ void batch_plan(const LayerParams& P, const BatchIO& io) {
     __shared__ int s_idx[kMaxBatch * kMaxTopK];
     __shared__ int s_off[kMaxRouted + 1];
     __shared__ int tmp[32];
     __shared__ int tot[4];
-    pdl_wait();
-    pdl_trigger();
     const int t = threadIdx.x;
     const int B = io.batch, K = P.top_k, E = P.n_routed;
     const int npair = B * K;
     BatchMeta* m = io.meta;
-    for (int p = t; p < npair; p += blockDim.x) s_idx[p] = io.topk_idx[p];
+    for (int p = t; p < npair; p += blockDim.x) s_idx[p] = __ldcg(io.topk_idx + p);
     // offsets, touched experts and unit offsets: block scans over the experts (thread e)
     const int HGr = P.routed_neurons / kUpRows;
     const int c = t < E ? __ldcg(&m->cnt[t]) : 0;
@@ -188,13 +167,45 @@ __global__ void __launch_bounds__(512) batch_plan_kernel(const __grid_constant__
         for (int q = 0; q < p; ++q) rank += (s_idx[q] == e);
         const int pos = s_off[e] + rank;
         io.pair_tok[pos] = p / K;
-        io.pair_w[pos] = io.topk_w[p];
+        io.pair_w[pos] = __ldcg(io.topk_w + p);
         io.pair_slot[pos] = p % K + 1;
     }
     // clear the union masks
     const int wr = P.routed_neurons / 32;
     for (int i = t; i < E * wr; i += blockDim.x) io.mask_r[i] = 0u;
     for (int i = t; i < P.shared_neurons / 32; i += blockDim.x) io.mask_s[i] = 0u;
+}
+
+// ------------------------------------------------------------------ route
+__global__ void __launch_bounds__(256) batch_route_kernel(const __grid_constant__ LayerParams P, const BatchIO io) {
+    __shared__ __align__(16) int s_idx[kMaxTopK];
+    __shared__ __align__(16) float s_w[kMaxTopK];
+    pdl_wait();
+    pdl_trigger();
+    const int b = blockIdx.x, t = threadIdx.x;
+    const int K = P.top_k, E = P.n_routed, H = P.hidden, G = H / 64;
+    if (t < 32) {
+        warp_topk_softmax(io.logits + (size_t)b * E, E, K, s_idx, s_w);
+        __syncwarp();
+        if (t < K) {
+            const int p = b * K + t;
+            io.topk_idx[p] = s_idx[t];
+            io.topk_w[p] = s_w[t];
+            atomicAdd(&io.meta->cnt[s_idx[t]], 1);
+            if (io.dbg_topk_idx) { io.dbg_topk_idx[p] = s_idx[t]; io.dbg_topk_w[p] = s_w[t]; }
+        }
+    }
+    // the token's fixed-point x table (read by every up unit that has this token)
+    convert_x_fixed(io.x + (size_t)b * H, G, io.xt + (size_t)b * G * kXfStride, io.xsc + (size_t)b * G * 2, 0);
+    // the last CTA to finish plans the batch (no CTA waits for another)
+    __shared__ int last;
+    __threadfence();   // this CTA's top-k, counts and x table before its increment
+    __syncthreads();
+    if (t == 0) last = atomicAdd(&io.meta->route_done, 1) == io.batch - 1;
+    __syncthreads();
+    if (!last) return;
+    __threadfence();
+    batch_plan(P, io);
 }
 
 // ------------------------------------------------------------------ up
@@ -1249,7 +1260,6 @@ int hs_batch_decode(const hs_moe_layer* L, const uint16_t* x, const float* logit
     // the first kernel follows the memset with ordinary stream ordering
     hs::batch_route_kernel<<<dim3(batch), dim3(256), 0, s>>>(P, io);
     if (cudaGetLastError() != cudaSuccess) return HS_ERR_CUDA;
-    if (launch_pdl(hs::batch_plan_kernel, dim3(1), dim3(512), 0, s, P, io) != cudaSuccess) return HS_ERR_CUDA;
     if (batch <= hs::kFusedMaxBatch && !(flags & HS_BATCH_EXPERT_UNION)) {
         const int f_smem = hs::FusedSmem::total(L->hidden);
         const int Ut = (L->shared ? L->shared->neurons / 64 : 0) + L->top_k * (L->routed[0].neurons / 64);
