@@ -53,12 +53,11 @@ struct SmemLayout {
     __host__ __device__ static int codes_bytes(int hidden) { return 64 * hidden / 2; }
     __host__ __device__ static int sb_bytes(int hidden) { return hidden * 4; }
     __host__ __device__ static int misc_off(int hidden) { return codes_bytes(hidden) + sb_bytes(hidden); }
-    // misc: h[64] f32, off[64] f32, logits[kMaxRouted] f32, rank parts[256] i32, sel_v[8] f32,
-    //       sel_i[8] i32, topk_i[8], topk_w[8], bars[8] u64, live u64, hsum f32,
+    // misc: h[64] f32, off[64] f32, topk_i[8] i32, topk_w[8] f32, bars[8] u64, live mask (u64, or
+    //       8 bytes of per-warp row bits), hsum f32,
     // then x[hidden] bf16 (staging), the fixed-point x table [G][144 B] and its
     // per-group (2^(E-15), sum x) pairs [G][2] f32.
-    static constexpr int kH = 0, kOff = 256, kLg = 512, kRank = kLg + 4 * kMaxRouted, kSelV = kRank + 1024,
-                         kSelI = kSelV + 32, kTopI = kSelI + 32, kTopW = kTopI + 32, kBarsOff = kTopW + 32,
+    static constexpr int kH = 0, kOff = 256, kTopI = 512, kTopW = kTopI + 32, kBarsOff = kTopW + 32,
                          kLive = kBarsOff + 64, kHsum = kLive + 8, kX = kHsum + 24;
     __host__ __device__ static int x_off(int hidden) { return misc_off(hidden) + kX; }
     __host__ __device__ static int xf_off(int hidden) { return x_off(hidden) + 2 * hidden; }
@@ -544,6 +543,24 @@ reduce_partials_kernel(const float* __restrict__ partial, int U, int hidden, uin
     }
 }
 
+// Failure-path self-test: the same bounded wait as every kernel's (try_wait
+// with a suspend hint, clock64 limit, error word), on a barrier that nothing
+// completes, with a caller-chosen limit.
+__global__ void selftest_wait_kernel(long long limit) {
+    __shared__ __align__(8) uint64_t bar;
+    if (threadIdx.x != 0) return;
+    mbar_init(&bar, 1);
+    fence_mbar_init();
+    const unsigned long long t0 = clock64();
+    while (!mbar_test(&bar, 0)) {
+        if ((long long)(clock64() - t0) > limit) {
+            atomicOr(&g_status, 1u);
+            return;
+        }
+        __nanosleep(1000);
+    }
+}
+
 }  // namespace hs
 
 // ===================================================================== host
@@ -573,6 +590,12 @@ extern "C" int hs_device_status(int* status) {
     v |= hs_prefill_take_status();
     *status = v ? HS_ERR_TIMEOUT : HS_OK;
     return HS_OK;
+}
+
+extern "C" int hs_selftest_bounded_wait(long long limit_cycles, hs_stream_t stream) {
+    if (limit_cycles < 1 || limit_cycles > (1ll << 31)) return HS_ERR_INVALID_ARG;
+    hs::selftest_wait_kernel<<<1, 32, 0, reinterpret_cast<cudaStream_t>(stream)>>>(limit_cycles);
+    return launch_err();
 }
 
 // ----------------------------------------------------------- sparse down

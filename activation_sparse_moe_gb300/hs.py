@@ -59,6 +59,7 @@ _lib = None
 _SIGS = {
     "hs_status_string": (C.c_char_p, [C.c_int]),
     "hs_device_status": (C.c_int, [C.POINTER(C.c_int)]),
+    "hs_selftest_bounded_wait": (C.c_int, [C.c_longlong, C.c_void_p]),
     "hs_repack_down_nm": (C.c_int, [C.c_void_p, C.c_void_p, C.c_void_p, C.c_int, C.c_int, C.c_void_p, C.c_void_p,
                                     C.c_void_p]),
     "hs_pack_sb": (C.c_int, [C.c_void_p, C.c_void_p, C.c_int, C.c_int, C.c_void_p, C.c_void_p]),
@@ -132,6 +133,10 @@ def hs_device_status() -> int:
     v = C.c_int(0)
     _check("hs_device_status", lib().hs_device_status(C.byref(v)))
     return v.value
+
+
+def hs_selftest_bounded_wait(limit_cycles, stream=None):
+    _check("hs_selftest_bounded_wait", lib().hs_selftest_bounded_wait(int(limit_cycles), _stream(stream)))
 
 
 def hs_repack_down_nm(codes_om, scale_om, bias_om, out_dim, neurons, codes_nm, sb_nm, stream=None):

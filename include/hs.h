@@ -123,6 +123,15 @@ const char* hs_status_string(int status);
  * *status receives HS_OK or HS_ERR_TIMEOUT. */
 int hs_device_status(int* status);
 
+/* Self-test of the failure path: one thread waits on an mbarrier that nothing
+ * completes, with the library's bounded wait but a limit of `limit_cycles`
+ * clock cycles (1 .. 2^31), then gives up and sets the device error word, as
+ * every kernel's bounded waits do.  The next hs_device_status reports
+ * HS_ERR_TIMEOUT (and clears the word); the context stays usable.  No fault,
+ * trap or unbounded wait is involved.  HS_ERR_INVALID_ARG for a limit out of
+ * range. */
+int hs_selftest_bounded_wait(long long limit_cycles, hs_stream_t stream);
+
 /* ------------------------------------------------------------------ repack
  * Output-major (checkpoint) down projection -> neuron-major layout.
  * Section "Transposing to skip the zeros" and "Two layouts, one problem":

@@ -133,3 +133,24 @@ def test_generator_device_independent(full_layer):
     cpu = synth.gen_expert((0, "cfg2", 0, "routed"), synth.N_ROUTED, index=e)
     assert torch.equal(cpu.up.codes, L.up.codes[e].cpu()) and torch.equal(cpu.down.scale, L.down.scale[e].cpu())
     assert torch.equal(cpu.offset, L.offsets[e])
+
+
+def test_bounded_wait_gives_up_and_reports():
+    """Failure detection without a fault: a wait that nothing completes gives
+    up after its limit, the error word reads HS_ERR_TIMEOUT once, and the
+    context still runs a layer decode correctly afterwards."""
+    import time
+    t0 = time.time()
+    hs.hs_selftest_bounded_wait(20_000_000)   # ~10 ms of clock cycles
+    torch.cuda.synchronize()
+    assert hs.hs_device_status() == hs.HS_ERR_TIMEOUT
+    assert hs.hs_device_status() == hs.HS_OK   # read and cleared
+    assert time.time() - t0 < 30
+    with pytest.raises(hs.HsError) as e:
+        hs.hs_selftest_bounded_wait(0)
+    assert e.value.status == hs.HS_ERR_INVALID_ARG
+    # the context is still usable
+    H, E, NR, NS, K = 256, 4, 128, 128, 2
+    L = synth.layer_inputs(9, "t-after-timeout", 0, E, NR, NS, H, p=0.3, p_shared=0.3)
+    X, LG = synth.tokens(9, "t-after-timeout", 0, 1, H, E)
+    check_layer(L, make_layer(L, K), X[0], LG[0], K, "after timeout")
