@@ -9,8 +9,18 @@
 // live rows once (the verify step of section "Speculative decoding." reads
 // three rows' activations through the same weights this way).
 //
-// Kernels (one stream; the meta block is zeroed first, then programmatic
-// dependent launch between the kernels):
+// B <= 4 (batch_small_kernel + batch_fused_reduce_kernel): one CTA per
+// (expert, 64-neuron group) unit with all of that expert's tokens, numbered
+// before routing; every CTA routes the batch itself.  Two kernels, no meta
+// block, programmatic dependent launch in between.
+//
+// B <= 64 (batch_route_kernel, batch_fused_kernel, batch_fused_reduce_kernel):
+// routing and planning first, then persistent CTAs take (expert, group, up to
+// 4 tokens) units by an atomic ticket.
+//
+// HS_BATCH_EXPERT_UNION, every expert reading the union of all its tokens'
+// live rows once (one stream; the meta block is zeroed first, then
+// programmatic dependent launch between the kernels):
 //  1. route:  one CTA per token: top-k + softmax (warp 0), per-expert pair
 //             counts (integer atomics), and the token's fixed-point x table
 //             for the integer-pipe GEMV (all threads).  The last CTA to finish
@@ -87,6 +97,8 @@ struct BatchIO {
     float* dbg_topk_w;
     int* live_total;
     int* live_groups;
+    int* unit_live;         // small-batch path: union live rows per unit (else null)
+    int n_units;
 };
 
 // ------------------------------------------------------------------ plan
@@ -846,23 +858,222 @@ __device__ __forceinline__ void fused_down(const uint8_t* codes, const uint32_t*
     }
 }
 
-__global__ void __launch_bounds__(256, 2) batch_fused_kernel(const __grid_constant__ LayerParams P, const BatchIO io) {
-    extern __shared__ __align__(128) uint8_t smem[];
+// Shared-memory buffers of a fused-unit CTA.
+struct FusedBufs {
+    uint8_t* codes;    // 64 up rows, then the parts, then the live rows' down codes
+    uint32_t* sbs;     // the up scales of 64 rows, then the down slab
+    float* h_s;        // [kFTok][64]
+    float* offs_s;     // [64]
+    uint64_t* bars;    // 4 up chunks, down
+    uint8_t* live8;    // live bits of rows 8w .. 8w+7 per warp w
+    uint8_t* tables;   // the kernel's own tables
+};
+__device__ __forceinline__ FusedBufs fused_bufs(uint8_t* smem, int H) {
     using S = FusedSmem;
-    const int H = P.hidden, G = H / 64, rowb = H / 2;
-    uint8_t* codes = smem;
-    uint32_t* sbs = reinterpret_cast<uint32_t*>(smem + S::codes(H));
     uint8_t* misc = smem + S::misc(H);
-    float* h_s = reinterpret_cast<float*>(misc + S::kHs);  // [kFTok][64]
-    float* offs_s = reinterpret_cast<float*>(misc + S::kOffs);
-    uint64_t* bars = reinterpret_cast<uint64_t*>(misc + S::kBarsOff);  // 4 up chunks, down
-    int* ticket_s = reinterpret_cast<int*>(misc + S::kTicket);
-    uint8_t* live8 = misc + S::kLive;
-    FusedTables* tb = reinterpret_cast<FusedTables*>(misc + S::kTables);
+    return FusedBufs{smem, reinterpret_cast<uint32_t*>(smem + S::codes(H)), reinterpret_cast<float*>(misc + S::kHs),
+                     reinterpret_cast<float*>(misc + S::kOffs), reinterpret_cast<uint64_t*>(misc + S::kBarsOff),
+                     misc + S::kLive, misc + S::kTables};
+}
+
+// Per-token facts of a unit: the token, its partial row and its router weight.
+struct UnitTokens {
+    int tok[kFTok], ri[kFTok];
+    float w[kFTok];
+};
+
+__device__ __forceinline__ int pick(const int (&a)[kFTok], int i) {
+    int v = a[0];
+#pragma unroll
+    for (int k = 1; k < kFTok; ++k) v = i == k ? a[k] : v;
+    return v;
+}
+
+// Thread 0: the bulk copies of chunks c0 .. c1-1 of group g's 64 up rows
+// (16 rows each, chunk k on bars[k]; the group's up scales ride on chunk 0).
+__device__ __forceinline__ void fused_issue_up(const FusedBufs& sm, const ExpertPtrs& ep, int g, int H, uint64_t pol,
+                                               int c0 = 0, int c1 = 4) {
+    const int rowb = H / 2, G = H / 64;
+    const uint8_t* src = ep.up_codes + (size_t)g * 64 * rowb;
+    const uint32_t chunk = 16 * rowb;
+    if (c0 == 0) {
+        mbar_arrive_expect_tx(&sm.bars[0], chunk + 64 * G * 4);
+        bulk_g2s(sm.sbs, ep.up_sb + (size_t)g * 64 * G, 64 * G * 4, &sm.bars[0], pol);
+        bulk_g2s(sm.codes, src, chunk, &sm.bars[0], pol);
+        c0 = 1;
+    }
+    for (int k = c0; k < c1; ++k) {
+        mbar_arrive_expect_tx(&sm.bars[k], chunk);
+        bulk_g2s(sm.codes + k * chunk, src + (size_t)k * chunk, chunk, &sm.bars[k], pol);
+    }
+}
+
+// A thread's part of a unit's up GEMV for T <= kFTok tokens: token lane tk
+// (the TL lanes of one scale group are adjacent in a warp), group gc, row
+// lane rs of RS.
+struct FusedRole {
+    int tk, gc, rs, RS;
+    bool active;  // owns (token, group) work
+};
+__device__ __forceinline__ FusedRole fused_role(int T, int G) {
+    const int t = threadIdx.x;
+    const int TL = T == 1 ? 1 : (T == 2 ? 2 : 4);
+    FusedRole r;
+    r.RS = 256 / (TL * G);
+    r.tk = t % TL;
+    r.gc = (t / TL) % G;
+    r.rs = t / (TL * G);
+    r.active = r.rs < r.RS && r.tk < T;
+    return r;
+}
+
+// One unit after its up copies were issued (phase `par` of bars[0..3]), with
+// each active thread's x fixed-point copy in xf: the DP4A GEMV per token,
+// ReLU^2, the union-live rows' down codes and the slab, the down products
+// into the tokens' partial rows.  Returns false (on every thread) if a
+// bounded wait gave up; `live` gets the unit's union live rows.
+__device__ __forceinline__ bool fused_unit(const LayerParams& P, const BatchIO& io, const FusedBufs& sm,
+                                           const ExpertPtrs& ep, int g, int T, const UnitTokens& ut, const XFixed& xf,
+                                           uint32_t par, uint32_t& dn_par, uint64_t& live) {
+    const int H = P.hidden, G = H / 64, rowb = H / 2;
     const int t = threadIdx.x, lane = t & 31;
     const bool dense = (io.flags & HS_FORCE_DENSE) != 0;
+    const uint64_t pol = policy_evict_first();
+    uint8_t* codes = sm.codes;
+    const FusedRole role = fused_role(T, G);
+    const int tk = role.tk, gc = role.gc, rs = role.rs, RS = role.RS;
+    const bool active = role.active;
+    float off_r = 0.f;
+    if (t < 64 && ep.up_off) off_r = __ldg(ep.up_off + 64 * g + t);
+    // ---- dot products (every thread keeps the warp's step count)
+    bool ok = true;
+    int waited = -1;
+    const int n_steps = (64 + 2 * RS - 1) / (2 * RS);
+    for (int i = 0; i < n_steps; ++i) {
+        const int r = rs + 2 * RS * i, r2 = r + RS;
+        const bool act = rs < RS && r < 64;
+        const bool two = act && r2 < 64;
+        if (act) {
+            const int k = (two ? r2 : r) >> 4;
+            while (ok && waited < k) { ++waited; ok = mbar_wait(&sm.bars[waited], par); }
+        }
+        uint4 a0 = make_uint4(0, 0, 0, 0), a1 = a0, b0 = a0, b1 = a0;
+        uint32_t sw0 = 0, sw1 = 0;
+        if (act && ok) {
+            load_group_codes(codes + r * rowb, gc, a0, a1);
+            sw0 = sm.sbs[r * G + gc];
+            if (two) {
+                load_group_codes(codes + r2 * rowb, gc, b0, b1);
+                sw1 = sm.sbs[r2 * G + gc];
+            }
+        }
+        const int da = group_dot_fixed16(a0, a1, xf);
+        const int db = group_dot_fixed16(b0, b1, xf);
+        __syncwarp();  // the token lanes of a group have read its codes before parts land there
+        if (act && ok && active) {
+            const float2 sa = half2_to_float2(sw0);
+            *up_part(codes, rowb, r, gc, tk) = fmaf(sa.x * xf.inv, (float)da, sa.y * xf.xsum);
+            if (two) {
+                const float2 sbv = half2_to_float2(sw1);
+                *up_part(codes, rowb, r2, gc, tk) = fmaf(sbv.x * xf.inv, (float)db, sbv.y * xf.xsum);
+            }
+        }
+    }
+    while (ok && waited < 3) { ++waited; ok = mbar_wait(&sm.bars[waited], par); }
+    if (t < 64) sm.offs_s[t] = off_r;
+    fence_proxy_async_smem();  // the parts come before the down copies into the same rows
+    if (!__syncthreads_and(ok)) return false;
+    // ---- row sums for every token; the row's down codes are copied once if it fired for any
+    bool lv = false;
+    {
+        const int r = t >> 2, q = t & 3;
+        bool anyh = false;
+        for (int k = 0; k < T; ++k) {
+            float s0 = 0.f, s1 = 0.f;
+            int cc = q;
+            for (; cc + 4 < G; cc += 8) {
+                s0 += *up_part(codes, rowb, r, cc, k);
+                s1 += *up_part(codes, rowb, r, cc + 4, k);
+            }
+            if (cc < G) s0 += *up_part(codes, rowb, r, cc, k);
+            float sum = s0 + s1;
+            sum += __shfl_xor_sync(0xffffffffu, sum, 1);
+            sum += __shfl_xor_sync(0xffffffffu, sum, 2);
+            const float z = sum + sm.offs_s[r];
+            const float h = z > 0.f ? z * z : 0.f;
+            if (q == 0) sm.h_s[k * 64 + r] = h;
+            anyh |= h > 0.f;
+        }
+        if (q == 0) {
+            lv = dense || anyh;
+            if (lv) {
+                mbar_expect_tx(&sm.bars[4], (uint32_t)rowb);
+                bulk_g2s(codes + (size_t)r * rowb, ep.dn_codes + ((size_t)g * 64 + r) * rowb, rowb, &sm.bars[4], pol);
+            }
+        }
+        const unsigned bl = __ballot_sync(0xffffffffu, lv);
+        if (lane == 0) {
+            unsigned m8 = 0;
+#pragma unroll
+            for (int i = 0; i < 8; ++i) m8 |= ((bl >> (4 * i)) & 1u) << i;
+            sm.live8[t >> 5] = (uint8_t)m8;
+        }
+    }
+    const bool any = __syncthreads_or(lv) != 0;
+    if (t == 0 && any) {
+        mbar_arrive_expect_tx(&sm.bars[4], (uint32_t)H * 4);
+        bulk_g2s(sm.sbs, ep.dn_sb + (size_t)g * H, H * 4, &sm.bars[4], pol);
+    }
+    live = *reinterpret_cast<const uint64_t*>(sm.live8);
+    // ---- per token: fixed-order sum of h
+    float hsum[kFTok];
+#pragma unroll
+    for (int k = 0; k < kFTok; ++k) {
+        hsum[k] = 0.f;
+        if (k < T) {
+            float hs = sm.h_s[k * 64 + lane] + sm.h_s[k * 64 + lane + 32];
+#pragma unroll
+            for (int off = 16; off; off >>= 1) hs += __shfl_xor_sync(0xffffffffu, hs, off);
+            hsum[k] = hs;
+        }
+    }
+    const int Ut = P.shared_neurons / 64 + P.top_k * (P.routed_neurons / 64);  // partial rows per token
+    const FusedOut out{io.partial, Ut, H};
+    const int nthr = H % 48 == 0 ? H / 12 : H / 16;
+    if (t < nthr) {
+        if (!any) {
+            const int nq = H % 48 == 0 ? 3 : 4;
+#pragma unroll
+            for (int k = 0; k < kFTok; ++k)
+                if (k < T)
+                    for (int i = 0; i < nq; ++i)
+                        *out.quad(ut.tok[k], ut.ri[k], nq * t + i) = make_float4(0.f, 0.f, 0.f, 0.f);
+        } else {
+            ok = mbar_wait(&sm.bars[4], dn_par);
+            if (ok) {
+                if (H % 48 == 0)
+                    fused_down<12>(codes, sm.sbs, sm.h_s, live, hsum, ut.w, ut.tok, ut.ri, T, rowb, t, out);
+                else
+                    fused_down<16>(codes, sm.sbs, sm.h_s, live, hsum, ut.w, ut.tok, ut.ri, T, rowb, t, out);
+            }
+        }
+    } else if (any) {
+        ok = mbar_wait(&sm.bars[4], dn_par);  // every thread sees the phase before the buffers are reused
+    }
+    if (any) dn_par ^= 1u;
+    fence_proxy_async_smem();
+    return __syncthreads_and(ok) != 0;
+}
+
+__global__ void __launch_bounds__(256, 2) batch_fused_kernel(const __grid_constant__ LayerParams P, const BatchIO io) {
+    extern __shared__ __align__(128) uint8_t smem[];
+    const int H = P.hidden;
+    const FusedBufs sm = fused_bufs(smem, H);
+    int* ticket_s = reinterpret_cast<int*>(smem + FusedSmem::misc(H) + FusedSmem::kTicket);
+    FusedTables* tb = reinterpret_cast<FusedTables*>(sm.tables);
+    const int t = threadIdx.x;
     if (t == 0) {
-        for (int i = 0; i < 5; ++i) mbar_init(&bars[i], 1);
+        for (int i = 0; i < 5; ++i) mbar_init(&sm.bars[i], 1);
         fence_mbar_init();
     }
     __syncthreads();
@@ -875,10 +1086,7 @@ __global__ void __launch_bounds__(256, 2) batch_fused_kernel(const __grid_consta
     for (int i = t; i <= P.n_routed; i += blockDim.x) tb->e_off[i] = __ldcg(&m->e_off[i]);
     if (t == 0) *ticket_s = atomicAdd(&m->fu_next, 1);
     __syncthreads();
-    const int NGs = P.shared_neurons / 64, NGr = P.routed_neurons / 64;
-    const int Ut = NGs + P.top_k * NGr;  // partial rows per token
-    const FusedOut out{io.partial, Ut, H};
-    const int nthr = H % 48 == 0 ? H / 12 : H / 16;
+    const int NGs = P.shared_neurons / 64, NGr = P.routed_neurons / 64, G = H / 64;
     const uint64_t pol = policy_evict_first();
     uint32_t dn_par = 0;
     for (int it = 0;; ++it) {
@@ -903,160 +1111,175 @@ __global__ void __launch_bounds__(256, 2) batch_fused_kernel(const __grid_consta
             T = min(kFTok, tb->e_off[e + 1] - pbase);
             ep = routed_ptrs(P, e);
         }
-        const uint32_t par = it & 1;
         __syncthreads();  // every thread has read the ticket
         if (t == blockDim.x - 1) *ticket_s = atomicAdd(&m->fu_next, 1);
-        if (t == 0) {
-            const uint8_t* src = ep.up_codes + (size_t)g * 64 * rowb;
-            const uint32_t chunk = 16 * rowb;
-            mbar_arrive_expect_tx(&bars[0], chunk + 64 * G * 4);
-            bulk_g2s(sbs, ep.up_sb + (size_t)g * 64 * G, 64 * G * 4, &bars[0], pol);
-            bulk_g2s(codes, src, chunk, &bars[0], pol);
-            for (int k = 1; k < 4; ++k) {
-                mbar_arrive_expect_tx(&bars[k], chunk);
-                bulk_g2s(codes + k * chunk, src + (size_t)k * chunk, chunk, &bars[k], pol);
-            }
-        }
-        // token lanes: TL adjacent lanes per scale group
-        const int TL = T == 1 ? 1 : (T == 2 ? 2 : 4);
-        const int RS = 256 / (TL * G);
-        const int tk = t % TL, gc = (t / TL) % G, rs = t / (TL * G);
-        const bool active = rs < RS && tk < T;
-        XFixed xf = {};
-        if (active) {
-            const int tok = shared ? pbase + tk : __ldcg(io.pair_tok + pbase + tk);
-            load_x_fixed(io.xt + (size_t)tok * G * kXfStride, io.xsc + (size_t)tok * G * 2, gc, xf);
-        }
-        float off_r = 0.f;
-        if (t < 64 && ep.up_off) off_r = __ldg(ep.up_off + 64 * g + t);
-        // ---- dot products (every thread keeps the warp's step count)
-        bool ok = true;
-        int waited = -1;
-        const int n_steps = (64 + 2 * RS - 1) / (2 * RS);
-        for (int i = 0; i < n_steps; ++i) {
-            const int r = rs + 2 * RS * i, r2 = r + RS;
-            const bool act = rs < RS && r < 64;
-            const bool two = act && r2 < 64;
-            if (act) {
-                const int k = (two ? r2 : r) >> 4;
-                while (ok && waited < k) { ++waited; ok = mbar_wait(&bars[waited], par); }
-            }
-            uint4 a0 = make_uint4(0, 0, 0, 0), a1 = a0, b0 = a0, b1 = a0;
-            uint32_t sw0 = 0, sw1 = 0;
-            if (act && ok) {
-                load_group_codes(codes + r * rowb, gc, a0, a1);
-                sw0 = sbs[r * G + gc];
-                if (two) {
-                    load_group_codes(codes + r2 * rowb, gc, b0, b1);
-                    sw1 = sbs[r2 * G + gc];
-                }
-            }
-            const int da = group_dot_fixed16(a0, a1, xf);
-            const int db = group_dot_fixed16(b0, b1, xf);
-            __syncwarp();  // the token lanes of a group have read its codes before parts land there
-            if (act && ok && active) {
-                const float2 sa = half2_to_float2(sw0);
-                *up_part(codes, rowb, r, gc, tk) = fmaf(sa.x * xf.inv, (float)da, sa.y * xf.xsum);
-                if (two) {
-                    const float2 sbv = half2_to_float2(sw1);
-                    *up_part(codes, rowb, r2, gc, tk) = fmaf(sbv.x * xf.inv, (float)db, sbv.y * xf.xsum);
-                }
-            }
-        }
-        while (ok && waited < 3) { ++waited; ok = mbar_wait(&bars[waited], par); }
-        if (t < 64) offs_s[t] = off_r;
-        fence_proxy_async_smem();  // the parts come before the down copies into the same rows
-        if (!__syncthreads_and(ok)) return;
-        // ---- row sums for every token; the row's down codes are copied once if it fired for any
-        bool lv = false;
-        {
-            const int r = t >> 2, q = t & 3;
-            bool anyh = false;
-            for (int k = 0; k < T; ++k) {
-                float s0 = 0.f, s1 = 0.f;
-                int cc = q;
-                for (; cc + 4 < G; cc += 8) {
-                    s0 += *up_part(codes, rowb, r, cc, k);
-                    s1 += *up_part(codes, rowb, r, cc + 4, k);
-                }
-                if (cc < G) s0 += *up_part(codes, rowb, r, cc, k);
-                float sum = s0 + s1;
-                sum += __shfl_xor_sync(0xffffffffu, sum, 1);
-                sum += __shfl_xor_sync(0xffffffffu, sum, 2);
-                const float z = sum + offs_s[r];
-                const float h = z > 0.f ? z * z : 0.f;
-                if (q == 0) h_s[k * 64 + r] = h;
-                anyh |= h > 0.f;
-            }
-            if (q == 0) {
-                lv = dense || anyh;
-                if (lv) {
-                    mbar_expect_tx(&bars[4], (uint32_t)rowb);
-                    bulk_g2s(codes + (size_t)r * rowb, ep.dn_codes + ((size_t)g * 64 + r) * rowb, rowb, &bars[4], pol);
-                }
-            }
-            const unsigned bl = __ballot_sync(0xffffffffu, lv);
-            if (lane == 0) {
-                unsigned m8 = 0;
+        if (t == 0) fused_issue_up(sm, ep, g, H, pol);
+        UnitTokens ut;
 #pragma unroll
-                for (int i = 0; i < 8; ++i) m8 |= ((bl >> (4 * i)) & 1u) << i;
-                live8[t >> 5] = (uint8_t)m8;
+        for (int k = 0; k < kFTok; ++k) {
+            ut.tok[k] = 0; ut.ri[k] = 0; ut.w[k] = 0.f;
+            if (k < T) {
+                if (shared) {
+                    ut.tok[k] = pbase + k;
+                    ut.ri[k] = g;
+                    ut.w[k] = 1.f;
+                } else {
+                    ut.tok[k] = __ldcg(io.pair_tok + pbase + k);
+                    ut.ri[k] = NGs + (__ldcg(io.pair_slot + pbase + k) - 1) * NGr + g;
+                    ut.w[k] = __ldcg(io.pair_w + pbase + k);
+                }
             }
         }
-        const bool any = __syncthreads_or(lv) != 0;
-        if (t == 0 && any) {
-            mbar_arrive_expect_tx(&bars[4], (uint32_t)H * 4);
-            bulk_g2s(sbs, ep.dn_sb + (size_t)g * H, H * 4, &bars[4], pol);
+        // x from the route kernel's fixed-point tables (here, unlike the
+        // small-batch kernel, staging x ahead of the weights measured slower:
+        // it serialises each unit's copies behind an extra wait)
+        const FusedRole role = fused_role(T, G);
+        XFixed xf = {};
+        if (role.active) {
+            const int tok = pick(ut.tok, role.tk);
+            load_x_fixed(io.xt + (size_t)tok * G * kXfStride, io.xsc + (size_t)tok * G * 2, role.gc, xf);
         }
-        const uint64_t live = *reinterpret_cast<const uint64_t*>(live8);
+        uint64_t live = 0;
+        if (!fused_unit(P, io, sm, ep, g, T, ut, xf, it & 1, dn_par, live)) return;
         if (t < 2 && live) {  // the expert's union over all its tokens (for the live-row counts)
             const uint32_t bits = (uint32_t)(live >> (32 * t));
             uint32_t* mw = shared ? io.mask_s + 2 * g + t : io.mask_r + (size_t)e * (P.routed_neurons / 32) + 2 * g + t;
             if (bits) atomicOr(mw, bits);
         }
-        // ---- per token: partial row index, router weight, fixed-order sum of h
-        int tokv[kFTok], riv[kFTok];
-        float wv[kFTok], hsum[kFTok];
+    }
+}
+
+// ------------------------------------------------------------------ small batch (B <= kFTok)
+// Every expert of the batch has all its tokens in one unit, so the units can
+// be numbered before routing: CTA u < NGs is the shared expert's group u with
+// every token; CTA NGs + j * NGr + g is group g of the j-th distinct routed
+// expert of the batch (ascending id) with its tokens, and exits if the batch
+// has fewer distinct experts.  Each routed CTA routes the B tokens itself (one
+// warp per token), so there is no route kernel, plan, ticket or zeroed meta
+// block.  x of the B tokens (2BH <= 8H bytes) is bulk-copied once into the
+// space of the last 16-row weight chunk, right after the wait for the
+// previous kernel and before any routed weights are requested (x read by
+// every thread from L2 instead waited behind the weight stream); each thread
+// converts its group from there, and the last chunk is fetched after.  The
+// shared expert's CTAs issue their other weight copies before waiting for the
+// previous kernel, as in the batch-1 kernel.
+struct SmallTables {
+    int topi[kFTok][kMaxTopK];
+    float topw[kFTok][kMaxTopK];
+    int tok[kFTok], slot[kFTok];
+    float w[kFTok];
+    int T, e;
+};
+static_assert(sizeof(SmallTables) <= sizeof(FusedTables), "small-batch tables exceed the tables region");
+
+__global__ void __launch_bounds__(256, 2) batch_small_kernel(const __grid_constant__ LayerParams P, const BatchIO io) {
+    extern __shared__ __align__(128) uint8_t smem[];
+    const int H = P.hidden;
+    const FusedBufs sm = fused_bufs(smem, H);
+    SmallTables* st = reinterpret_cast<SmallTables*>(sm.tables);
+    const int t = threadIdx.x, lane = t & 31, warp = t >> 5, u = blockIdx.x;
+    const int B = io.batch, K = P.top_k, E = P.n_routed;
+    const int NGs = P.shared_neurons / 64, NGr = P.routed_neurons / 64;
+    const bool shared = u < NGs;
+    uint64_t* xbar = &sm.bars[5];
+    const uint16_t* x_s = reinterpret_cast<const uint16_t*>(sm.codes + 3 * 8 * H);  // chunk 3's space
+    if (t == 0) {
+        for (int i = 0; i < 6; ++i) mbar_init(&sm.bars[i], 1);
+        fence_mbar_init();
+        if (shared) fused_issue_up(sm, P.shared, u, H, policy_evict_first(), 0, 3);  // weights only
+    }
+    __syncthreads();
+    pdl_wait();
+    pdl_trigger();
+    if (t == 0) {
+        mbar_arrive_expect_tx(xbar, (uint32_t)(2 * B * H));
+        bulk_g2s(sm.codes + 3 * 8 * H, io.x, (uint32_t)(2 * B * H), xbar, policy_evict_last());
+    }
+    if (!shared || (u == 0 && io.dbg_topk_idx)) {
+        if (warp < B) warp_topk_softmax(io.logits + (size_t)warp * E, E, K, st->topi[warp], st->topw[warp]);
+        __syncthreads();
+        if (u == 0 && io.dbg_topk_idx && t < B * K) {
+            io.dbg_topk_idx[t] = st->topi[t / K][t % K];
+            io.dbg_topk_w[t] = st->topw[t / K][t % K];
+        }
+    }
+    UnitTokens ut;
+    ExpertPtrs ep;
+    int g, T;
+    if (shared) {
+        g = u;
+        T = B;
+        ep = P.shared;
+#pragma unroll
+        for (int k = 0; k < kFTok; ++k) { ut.tok[k] = k < B ? k : 0; ut.ri[k] = g; ut.w[k] = 1.f; }
+    } else {
+        const int j = (u - NGs) / NGr;
+        g = (u - NGs) % NGr;
+        if (warp == 0) {
+            // the batch's distinct experts as a 128-bit set; this CTA's is its j-th member
+            const int ei = lane < B * K ? st->topi[lane / K][lane % K] : -1;
+            int e = -1, before = 0;
+#pragma unroll
+            for (int w = 0; w < kMaxRouted / 32; ++w) {
+                uint32_t m = __reduce_or_sync(0xffffffffu, (ei >= 0 && (ei >> 5) == w) ? 1u << (ei & 31) : 0u);
+                const int c = __popc(m);
+                if (e < 0 && j < before + c) {
+                    for (int i = 0; i < j - before; ++i) m &= m - 1;
+                    e = 32 * w + __ffs(m) - 1;
+                }
+                before += c;
+            }
+            // its tokens in ascending order, with their slots and weights
+            int slot = -1;
+            if (e >= 0 && lane < B)
+                for (int s = 0; s < K; ++s)
+                    if (st->topi[lane][s] == e) slot = s;
+            const unsigned has = __ballot_sync(0xffffffffu, slot >= 0);
+            if (slot >= 0) {
+                const int k = __popc(has & ((1u << lane) - 1u));
+                st->tok[k] = lane;
+                st->slot[k] = slot;
+                st->w[k] = st->topw[lane][slot];
+            }
+            if (lane == 0) {
+                st->T = e >= 0 ? __popc(has) : 0;
+                st->e = e;
+            }
+        }
+        __syncthreads();
+        T = st->T;
+        if (T == 0) {
+            if (t == 0) {
+                io.unit_live[u] = 0;
+                mbar_wait(xbar, 0);  // no copy may be in flight into an exiting CTA
+            }
+            return;
+        }
+        ep = routed_ptrs(P, st->e);
 #pragma unroll
         for (int k = 0; k < kFTok; ++k) {
-            tokv[k] = 0; riv[k] = 0; wv[k] = 0.f; hsum[k] = 0.f;
-            if (k < T) {
-                if (shared) {
-                    tokv[k] = pbase + k;
-                    riv[k] = g;
-                    wv[k] = 1.f;
-                } else {
-                    tokv[k] = __ldcg(io.pair_tok + pbase + k);
-                    riv[k] = NGs + (__ldcg(io.pair_slot + pbase + k) - 1) * NGr + g;
-                    wv[k] = __ldcg(io.pair_w + pbase + k);
-                }
-                float hs = h_s[k * 64 + lane] + h_s[k * 64 + lane + 32];
-#pragma unroll
-                for (int off = 16; off; off >>= 1) hs += __shfl_xor_sync(0xffffffffu, hs, off);
-                hsum[k] = hs;
-            }
+            ut.tok[k] = k < T ? st->tok[k] : 0;
+            ut.ri[k] = k < T ? NGs + st->slot[k] * NGr + g : 0;
+            ut.w[k] = k < T ? st->w[k] : 0.f;
         }
-        if (t < nthr) {
-            if (!any) {
-                for (int k = 0; k < T; ++k)
-                    for (int i = 0; i < (nthr == H / 12 ? 3 : 4); ++i)
-                        *out.quad(tokv[k], riv[k], (H % 48 == 0 ? 3 : 4) * t + i) = make_float4(0.f, 0.f, 0.f, 0.f);
-            } else {
-                ok = mbar_wait(&bars[4], dn_par);
-                if (ok) {
-                    if (H % 48 == 0)
-                        fused_down<12>(codes, sbs, h_s, live, hsum, wv, tokv, riv, T, rowb, t, out);
-                    else
-                        fused_down<16>(codes, sbs, h_s, live, hsum, wv, tokv, riv, T, rowb, t, out);
-                }
-            }
-        } else if (any) {
-            ok = mbar_wait(&bars[4], dn_par);  // every thread sees the phase before the buffers are reused
-        }
-        if (any) dn_par ^= 1u;
-        fence_proxy_async_smem();
-        if (!__syncthreads_and(ok)) return;
     }
+    if (!shared && t == 0) fused_issue_up(sm, ep, g, H, policy_evict_first(), 0, 3);
+    // each active thread's x group from shared memory, then the last chunk into that space
+    const FusedRole role = fused_role(T, H / 64);
+    const bool xok = mbar_wait(xbar, 0);
+    XFixed xf = {};
+    if (role.active && xok) {
+        uint32_t xw[4][8];
+        x_group_load(x_s + (size_t)pick(ut.tok, role.tk) * H, role.gc, xw);
+        x_group_fixed(xw, xf);
+    }
+    fence_proxy_async_smem();  // the reads of x come before the copy that overwrites them
+    if (!__syncthreads_and(xok)) return;
+    if (t == 0) fused_issue_up(sm, ep, g, H, policy_evict_first(), 3, 4);
+    uint32_t dn_par = 0;
+    uint64_t live = 0;
+    if (!fused_unit(P, io, sm, ep, g, T, ut, xf, 0, dn_par, live)) return;
+    if (t == 0) io.unit_live[u] = __popcll(live);
 }
 
 // y[b][o] = the token's partial rows added in a fixed order (32 outputs per
@@ -1102,17 +1325,26 @@ __global__ void __launch_bounds__(256) batch_fused_reduce_kernel(const __grid_co
     }
     if ((io.live_total || io.live_groups) && cb == 0 && b == 0) {
         __syncthreads();  // part[] is reused below
-        // union live rows and groups per expert, from the union masks
-        const BatchMeta* m = io.meta;
-        const int nt = __ldcg(&m->n_touched), WR = P.routed_neurons / 32, WS = P.shared_neurons / 32;
         int n = 0, ng = 0;
-        for (int q = t; q < nt * (WR / 2) + WS / 2; q += blockDim.x) {
-            const uint32_t* mw = q < nt * (WR / 2)
-                                     ? io.mask_r + (size_t)__ldcg(&m->touched[q / (WR / 2)]) * WR + 2 * (q % (WR / 2))
-                                     : io.mask_s + 2 * (q - nt * (WR / 2));
-            const uint32_t a = __ldcg(mw), c = __ldcg(mw + 1);
-            n += __popc(a) + __popc(c);
-            ng += (a | c) != 0u;
+        if (io.unit_live) {
+            // small-batch path: every unit holds all the tokens of its expert
+            for (int q = t; q < io.n_units; q += blockDim.x) {
+                const int c = __ldcg(io.unit_live + q);
+                n += c;
+                ng += c > 0;
+            }
+        } else {
+            // union live rows and groups per expert, from the union masks
+            const BatchMeta* m = io.meta;
+            const int nt = __ldcg(&m->n_touched), WR = P.routed_neurons / 32, WS = P.shared_neurons / 32;
+            for (int q = t; q < nt * (WR / 2) + WS / 2; q += blockDim.x) {
+                const uint32_t* mw = q < nt * (WR / 2)
+                                         ? io.mask_r + (size_t)__ldcg(&m->touched[q / (WR / 2)]) * WR + 2 * (q % (WR / 2))
+                                         : io.mask_s + 2 * (q - nt * (WR / 2));
+                const uint32_t a = __ldcg(mw), c = __ldcg(mw + 1);
+                n += __popc(a) + __popc(c);
+                ng += (a | c) != 0u;
+            }
         }
         n = __reduce_add_sync(0xffffffffu, (unsigned)n);
         ng = __reduce_add_sync(0xffffffffu, (unsigned)ng);
@@ -1165,8 +1397,15 @@ using namespace hs_host;
 
 namespace {
 struct BatchLayout {
-    size_t meta, topk_idx, topk_w, pair_tok, pair_w, pair_slot, xt, xsc, h_pair, h_sh, mask_r, mask_s, partial, total;
+    size_t meta, topk_idx, topk_w, pair_tok, pair_w, pair_slot, xt, xsc, h_pair, h_sh, mask_r, mask_s, unit_live, partial,
+        total;
 };
+
+// Grid of the small-batch kernel: the shared expert's groups, then room for
+// B * K distinct routed experts.
+int small_units(const hs_moe_layer* L, int B) {
+    return (L->shared ? L->shared->neurons / 64 : 0) + B * L->top_k * (L->routed[0].neurons / 64);
+}
 
 BatchLayout batch_layout(const hs_moe_layer* L, int B) {
     const int K = L->top_k, E = L->n_routed, NR = L->routed[0].neurons;
@@ -1188,6 +1427,7 @@ BatchLayout batch_layout(const hs_moe_layer* L, int B) {
     l.mask_r = take((size_t)E * (NR / 32) * 4);
     l.mask_s = take((size_t)(NS ? NS / 32 : 1) * 4);
     const int Ut = (NS / 64) + K * (NR / 64);
+    l.unit_live = take((size_t)small_units(L, B) * 4);
     // the fused path's partial rows (per token, slot and group) or the banded path's (per token and slot)
     l.partial = take((size_t)B * std::max(Ut, SC + K) * H * 4);
     l.total = o;
@@ -1256,6 +1496,21 @@ int hs_batch_decode(const hs_moe_layer* L, const uint16_t* x, const float* logit
     if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return HS_ERR_CUDA;
     const int up_smem = hs::BatchUpSmem::total(L->hidden);
     const int dn_smem = hs::BatchDownSmem::total();
+    if (batch <= hs::kFTok && !(flags & HS_BATCH_EXPERT_UNION)) {
+        // every expert's tokens fit one unit: no route kernel, plan or meta block
+        const int f_smem = hs::FusedSmem::total(L->hidden);
+        const int Ut = (L->shared ? L->shared->neurons / 64 : 0) + L->top_k * (L->routed[0].neurons / 64);
+        io.unit_live = reinterpret_cast<int*>(w + l.unit_live);
+        io.n_units = small_units(L, batch);
+        if (set_smem_attr((const void*)hs::batch_small_kernel, f_smem) != HS_OK) return HS_ERR_CUDA;
+        if (set_smem_attr((const void*)hs::batch_fused_reduce_kernel, Ut * 128) != HS_OK) return HS_ERR_CUDA;
+        if (launch_pdl(hs::batch_small_kernel, dim3(io.n_units), dim3(256), f_smem, s, P, io) != cudaSuccess)
+            return HS_ERR_CUDA;
+        if (launch_pdl(hs::batch_fused_reduce_kernel, dim3(L->hidden / 32, batch), dim3(256), (size_t)Ut * 128, s, P,
+                       io) != cudaSuccess)
+            return HS_ERR_CUDA;
+        return launch_err();
+    }
     if (cudaMemsetAsync(io.meta, 0, sizeof(hs::BatchMeta), s) != cudaSuccess) return HS_ERR_CUDA;
     // the first kernel follows the memset with ordinary stream ordering
     hs::batch_route_kernel<<<dim3(batch), dim3(256), 0, s>>>(P, io);

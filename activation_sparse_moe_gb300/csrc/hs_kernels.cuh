@@ -134,12 +134,58 @@ struct XFixed {
     float xsum;                // sum of the 64 x values (fp32)
 };
 
+// The fixed-point copy is built from quarters of a group: 16 bf16 values
+// x[16q..16q+15] in 8 words (code words 2q, 2q+1).
+// Maximum magnitude and sum of one quarter (even and odd elements in two
+// ordered chains, then added).
+__device__ __forceinline__ void x_quarter_stats(const uint32_t (&w)[8], float& mx, float& sm) {
+    float sa = 0.f, sb = 0.f;
+    mx = 0.f;
+#pragma unroll
+    for (int m = 0; m < 8; ++m) {
+        const float x0 = __uint_as_float(w[m] << 16), x1 = __uint_as_float(w[m] & 0xffff0000u);
+        mx = fmaxf(mx, fmaxf(fabsf(x0), fabsf(x1)));
+        sa += x0;
+        sb += x1;
+    }
+    sm = sa + sb;
+}
+
+// E from the exponent field of the group maximum (max < 2^E).
+__device__ __forceinline__ int x_group_exp(float mx) {
+    const int e = (int)((__float_as_uint(mx) >> 23) & 0xff) - 126;  // mx normal
+    return max(e, -100);                                            // zero / subnormal maxima
+}
+
+// Words 2q, 2q+1 of the fixed-point copy: byte b of word j <-> x[8j + 2b]
+// (even) and x[8j + 2b + 1] (odd).  Rounding to the integer grid uses the
+// 1.5 * 2^23 magic constant (exact: |x * 2^(15-E)| < 2^15).
+__device__ __forceinline__ void x_quarter_fixed(const uint32_t (&w)[8], int e, uint32_t (&hE)[2], uint32_t (&hO)[2],
+                                                uint32_t (&lE)[2], uint32_t (&lO)[2]) {
+    const float scale = __int_as_float((127 + 15 - e) << 23);  // 2^(15-e)
+#pragma unroll
+    for (int jj = 0; jj < 2; ++jj) {
+        hE[jj] = hO[jj] = lE[jj] = lO[jj] = 0;
+#pragma unroll
+        for (int b = 0; b < 4; ++b) {
+            const uint32_t v = w[4 * jj + b];
+            const int X0 = __float_as_int(fmaf(__uint_as_float(v << 16), scale, 12582912.f)) - 0x4B400000;
+            const int X1 = __float_as_int(fmaf(__uint_as_float(v & 0xffff0000u), scale, 12582912.f)) - 0x4B400000;
+            hE[jj] |= (uint32_t)((X0 >> 8) & 0xff) << (8 * b);
+            lE[jj] |= (uint32_t)(X0 & 0xff) << (8 * b);
+            hO[jj] |= (uint32_t)((X1 >> 8) & 0xff) << (8 * b);
+            lO[jj] |= (uint32_t)(X1 & 0xff) << (8 * b);
+        }
+    }
+}
+
+// 2^(E-15) / 16: the factor that turns a group dot product into x units.
+__device__ __forceinline__ float x_group_inv(int e) { return __int_as_float((127 + e - 19) << 23); }
+
 // Cooperative conversion of x into the fixed-point table: 4 threads per
-// group of 64, thread q covering x[16q..16q+15] (code words 2q, 2q+1).  The
-// group maximum and sum combine the 4 partials by a fixed 2-level tree.
+// group of 64, thread q covering quarter q.  The group maximum and sum
+// combine the 4 partials by a fixed 2-level tree (lanes q^1, then q^2).
 // Threads first..blockDim-1 (whole warps) take the work items round-robin.
-// E comes from the exponent field of the maximum (max < 2^E); rounding to the
-// integer grid uses the 1.5 * 2^23 magic constant (exact: |x * 2^(15-E)| < 2^15).
 __device__ __forceinline__ void convert_x_fixed(const uint16_t* x_s, int G, uint8_t* xf_s, float* xs_s, int first) {
     const int nthr = blockDim.x - first;
     for (int i0 = threadIdx.x - first; i0 - (int)(threadIdx.x & 31) < 4 * G; i0 += nthr) {
@@ -150,43 +196,16 @@ __device__ __forceinline__ void convert_x_fixed(const uint16_t* x_s, int G, uint
         const uint4 r0 = reinterpret_cast<const uint4*>(x_s + 64 * grp + 16 * q)[0];
         const uint4 r1 = reinterpret_cast<const uint4*>(x_s + 64 * grp + 16 * q)[1];
         const uint32_t w[8] = {r0.x, r0.y, r0.z, r0.w, r1.x, r1.y, r1.z, r1.w};
-        float xv[16];
-#pragma unroll
-        for (int m = 0; m < 8; ++m) {
-            xv[2 * m] = __uint_as_float(w[m] << 16);
-            xv[2 * m + 1] = __uint_as_float(w[m] & 0xffff0000u);
-        }
-        float mx = 0.f, sa = 0.f, sb = 0.f;
-#pragma unroll
-        for (int m = 0; m < 16; m += 2) {
-            mx = fmaxf(mx, fmaxf(fabsf(xv[m]), fabsf(xv[m + 1])));
-            sa += xv[m];
-            sb += xv[m + 1];
-        }
-        float sm = sa + sb;
+        float mx, sm;
+        x_quarter_stats(w, mx, sm);
         // the 4 threads of a group are adjacent lanes: fixed xor tree
         mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
         sm += __shfl_xor_sync(0xffffffffu, sm, 1);
         mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
         sm += __shfl_xor_sync(0xffffffffu, sm, 2);
-        int e = (int)((__float_as_uint(mx) >> 23) & 0xff) - 126;  // mx < 2^e (mx normal)
-        e = max(e, -100);                                          // zero / subnormal maxima
-        const float scale = __int_as_float((127 + 15 - e) << 23);  // 2^(15-e)
-        // words 2q, 2q+1: byte b of word j <-> x[8j + 2b] (even) and x[8j + 2b + 1] (odd)
+        const int e = x_group_exp(mx);
         uint32_t hE[2], hO[2], lE[2], lO[2];
-#pragma unroll
-        for (int jj = 0; jj < 2; ++jj) {
-            hE[jj] = hO[jj] = lE[jj] = lO[jj] = 0;
-#pragma unroll
-            for (int b = 0; b < 4; ++b) {
-                const int X0 = __float_as_int(fmaf(xv[8 * jj + 2 * b], scale, 12582912.f)) - 0x4B400000;
-                const int X1 = __float_as_int(fmaf(xv[8 * jj + 2 * b + 1], scale, 12582912.f)) - 0x4B400000;
-                hE[jj] |= (uint32_t)((X0 >> 8) & 0xff) << (8 * b);
-                lE[jj] |= (uint32_t)(X0 & 0xff) << (8 * b);
-                hO[jj] |= (uint32_t)((X1 >> 8) & 0xff) << (8 * b);
-                lO[jj] |= (uint32_t)(X1 & 0xff) << (8 * b);
-            }
-        }
+        x_quarter_fixed(w, e, hE, hO, lE, lO);
         if (act) {
             uint8_t* tb = xf_s + grp * kXfStride + 8 * q;
             *reinterpret_cast<uint2*>(tb) = make_uint2(hE[0], hE[1]);
@@ -194,11 +213,46 @@ __device__ __forceinline__ void convert_x_fixed(const uint16_t* x_s, int G, uint
             *reinterpret_cast<uint2*>(tb + 64) = make_uint2(lE[0], lE[1]);
             *reinterpret_cast<uint2*>(tb + 96) = make_uint2(lO[0], lO[1]);
             if (q == 0) {
-                xs_s[2 * grp] = __int_as_float((127 + e - 19) << 23);   // 2^(E-15) / 16
+                xs_s[2 * grp] = x_group_inv(e);
                 xs_s[2 * grp + 1] = sm;
             }
         }
     }
+}
+
+// The same fixed-point copy of group gc built by one thread from x in shared
+// memory, in two steps (x_group_load reads the group's 64 values, then
+// x_group_fixed converts them), combining the four quarter sums in the same
+// tree order as convert_x_fixed: identical values, no table.
+__device__ __forceinline__ void x_group_load(const uint16_t* x_s, int gc, uint32_t (&w)[4][8]) {
+    const uint4* src = reinterpret_cast<const uint4*>(x_s + 64 * gc);
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+        const uint4 r0 = src[2 * q], r1 = src[2 * q + 1];
+        w[q][0] = r0.x; w[q][1] = r0.y; w[q][2] = r0.z; w[q][3] = r0.w;
+        w[q][4] = r1.x; w[q][5] = r1.y; w[q][6] = r1.z; w[q][7] = r1.w;
+    }
+}
+
+__device__ __forceinline__ void x_group_fixed(const uint32_t (&w)[4][8], XFixed& xf) {
+    float mq[4], sq[4];
+#pragma unroll
+    for (int q = 0; q < 4; ++q) x_quarter_stats(w[q], mq[q], sq[q]);
+    const int e = x_group_exp(fmaxf(fmaxf(mq[0], mq[1]), fmaxf(mq[2], mq[3])));
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+        uint32_t hE[2], hO[2], lE[2], lO[2];
+        x_quarter_fixed(w[q], e, hE, hO, lE, lO);
+#pragma unroll
+        for (int jj = 0; jj < 2; ++jj) {
+            xf.hE[2 * q + jj] = (int)hE[jj];
+            xf.hO[2 * q + jj] = (int)hO[jj];
+            xf.lE[2 * q + jj] = lE[jj];
+            xf.lO[2 * q + jj] = lO[jj];
+        }
+    }
+    xf.inv = x_group_inv(e);
+    xf.xsum = (sq[0] + sq[1]) + (sq[2] + sq[3]);
 }
 
 __device__ __forceinline__ void load_x_fixed(const uint8_t* xf_s, const float* xs_s, int gc, XFixed& xf) {

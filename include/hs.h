@@ -201,7 +201,8 @@ int hs_expert_down_sparse_noalloc(const float* h_dev, const hs_w4* down_nm, int 
  * live rows once; with HS_BATCH_EXPERT_UNION each expert reads the union of
  * all its tokens' live rows once.  hidden must then be a multiple of 128,
  * neurons <= 3712, and the debug h dump is not available
- * (HS_ERR_INVALID_ARG).  Deterministic.
+ * (HS_ERR_INVALID_ARG).  Deterministic; without HS_BATCH_EXPERT_UNION each
+ * token's y equals, bit for bit, a batch-1 call on that token alone.
  * Calls sharing one workspace must not overlap on the GPU. */
 size_t hs_moe_layer_decode_workspace_size(const hs_moe_layer* layer, int batch);
 int hs_moe_layer_decode(const hs_moe_layer* layer, const uint16_t* x_bf16_dev,

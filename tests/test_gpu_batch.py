@@ -92,6 +92,47 @@ def test_small_batch_no_shared_with_ties():
     check_batch(L, make_layer(L, K), X, LG, K, "no shared, ties")
 
 
+def single_token_decodes(dl, X, LG):
+    """Each token of the batch decoded alone (batch 1)."""
+    H = X.shape[1]
+    ws = torch.zeros(dl.workspace_size(1), dtype=torch.uint8, device="cuda")
+    out = []
+    for b in range(X.shape[0]):
+        y = torch.empty(H, dtype=torch.bfloat16, device="cuda")
+        yf = torch.empty(H, dtype=torch.float32, device="cuda")
+        hs.hs_moe_layer_decode(dl.c, X[b].cuda(), LG[b].cuda(), 1, y, yf, 0, None, ws)
+        torch.cuda.synchronize()
+        out.append((y.cpu(), yf.cpu().double().numpy()))
+    return out
+
+
+@pytest.mark.parametrize("B,H,E,NR,NS,K", [(2, 512, 8, 128, 256, 3), (3, 3072, 6, 192, 0, 2),
+                                           (4, 512, 8, 128, 256, 3), (5, 512, 8, 128, 256, 3),
+                                           (8, 512, 8, 128, 256, 3)])
+def test_batch_rows_equal_single_token_decode(B, H, E, NR, NS, K):
+    """Batching changes no token's result: every unit adds each token's terms
+    in the same order as the batch-1 kernel (rows live only for another token
+    add +0), so each row of a batch decode equals that token decoded alone,
+    bit for bit (B <= 4: one unit per expert; B > 4: the ticketed units)."""
+    L = synth.layer_inputs(2, "t-batch-eq", H, E, NR, NS, H, p=0.2, p_shared=0.3)
+    X, LG = synth.tokens(2, "t-batch-eq", B, B, H, E)
+    dl = make_layer(L, K)
+    y, yf, _ = check_batch(L, dl, X, LG, K, f"B={B} H={H}")
+    for b, (y1, yf1) in enumerate(single_token_decodes(dl, X, LG)):
+        assert np.array_equal(yf[b], yf1), f"token {b}: batch row differs from its batch-1 decode"
+        assert torch.equal(y[b], y1)
+
+
+def test_small_path_every_token_on_the_same_experts():
+    """All tokens route alike: each routed unit holds all B = 4 tokens."""
+    H, E, NR, NS, K = 512, 8, 128, 256, 3
+    L = synth.layer_inputs(3, "t-batch-same", 0, E, NR, NS, H, p=0.2, p_shared=0.3)
+    X, LG = synth.tokens(3, "t-batch-same", 0, 4, H, E)
+    LG[:] = LG[0].clone()
+    y, yf, dbg = check_batch(L, make_layer(L, K), X, LG, K, "same experts")
+    assert len(np.unique(dbg["topk_idx"].numpy())) == K
+
+
 @pytest.fixture(scope="module")
 def cfg4_layer():
     """Configuration 4: full-size layer, 30% permanently dead, p = 0.1 on the rest."""
@@ -99,7 +140,7 @@ def cfg4_layer():
     return L, make_layer(L, 6)
 
 
-@pytest.mark.parametrize("B", [2, 8, 32, 64])
+@pytest.mark.parametrize("B", [2, 3, 4, 8, 32, 64])
 def test_config4_parity(cfg4_layer, B):
     L, dl = cfg4_layer
     X, LG = synth.tokens(0, "cfg4", B, B)
@@ -137,3 +178,19 @@ def test_config4_dense_flag_and_determinism(cfg4_layer):
     yud, yfud, dud = run_batch(dl, X, LG, flags=f | hs.HS_FORCE_DENSE)
     assert np.array_equal(yfu, yfud) and torch.equal(yu, yud)
     assert int(dud["live_rows"].item()) == ntouched * synth.N_ROUTED + synth.N_SHARED
+
+
+def test_config4_small_path_dense_flag_and_determinism(cfg4_layer):
+    """B = 3 (one unit per expert, no route kernel): repeatable, dense flag
+    gives the same bits, and each row equals the token decoded alone."""
+    L, dl = cfg4_layer
+    X, LG = synth.tokens(0, "cfg4", 3, 3)
+    y1, yf1, d1 = run_batch(dl, X, LG)
+    y2, yf2, d2 = run_batch(dl, X, LG)
+    yd, yfd, dd = run_batch(dl, X, LG, flags=hs.HS_FORCE_DENSE)
+    assert np.array_equal(yf1, yf2) and torch.equal(y1, y2)
+    assert np.array_equal(yf1, yfd) and torch.equal(y1, yd)
+    ntouched = len(np.unique(d1["topk_idx"].numpy()))
+    assert int(dd["live_rows"].item()) == ntouched * synth.N_ROUTED + synth.N_SHARED
+    for b, (ys, yfs) in enumerate(single_token_decodes(dl, X, LG)):
+        assert np.array_equal(yf1[b], yfs) and torch.equal(y1[b], ys)
