@@ -267,8 +267,6 @@ moe_decode_b1_kernel(const __grid_constant__ LayerParams P, const DecodeIO io) {
     int* topk_i = reinterpret_cast<int*>(misc + SmemLayout::kTopI);
     float* topk_w = reinterpret_cast<float*>(misc + SmemLayout::kTopW);
     uint64_t* bars = reinterpret_cast<uint64_t*>(misc + SmemLayout::kBarsOff);
-    uint64_t* live_s = reinterpret_cast<uint64_t*>(misc + SmemLayout::kLive);
-    float* hsum_s = reinterpret_cast<float*>(misc + SmemLayout::kHsum);
     uint16_t* x_s = reinterpret_cast<uint16_t*>(smem + SmemLayout::x_off(hidden));
 
     const int t = threadIdx.x;
