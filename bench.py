@@ -51,6 +51,8 @@ def _args():
                     help="batch decode leg (one MoE layer, 30%% dead neurons); empty to skip")
     ap.add_argument("--no-prefill", action="store_true", help="skip the 2048-token prefill leg")
     ap.add_argument("--no-sweep", action="store_true", help="skip the live-fraction sweep")
+    ap.add_argument("--no-expert-down", action="store_true",
+                    help="skip the single-expert sparse down leg (512 distinct experts)")
     ap.add_argument("--profile", action="store_true",
                     help="minimal run for profilers: no clock soak, dense, end-to-end or CPU legs")
     return ap.parse_args()
@@ -271,6 +273,62 @@ def bench_batch(args, dev, stream, timed, bytemodel, hs):
     del layers
     torch.cuda.empty_cache()
     return out
+
+
+def bench_expert_down(args, dev, stream, timed, bytemodel, hs, peak):
+    """Configuration 1: hs_expert_down_sparse of one token's h (relu(z)^2 with
+    z ~ N(Phi^-1(0.1), 1), its own draw per copy) through 512 distinct routed
+    experts' 2688 x 1856 down projections (1.44 GB of weights, far above L2),
+    called back to back in one CUDA graph; per-call time and the bandwidth on
+    the bytes each call must move (live rows, live groups' scale slabs, h, y)."""
+    import numpy as np
+    import torch
+    import synth
+    n_copies, N, H = 512, 1856, 2688
+    codes = torch.empty((n_copies, N, H // 2), dtype=torch.uint8, device=dev)
+    sb = torch.empty((n_copies, N // 64, H), dtype=torch.int32, device=dev)
+    for l in range(n_copies // 128):
+        _, down = synth.gen_routed_stack((0, "cfg1", l), 128, N, H, device=dev)
+        ds, db = down.scale.view(torch.int16), down.bias.view(torch.int16)
+        for e in range(128):
+            i = 128 * l + e
+            hs.hs_repack_down_nm(down.codes[e], ds[e], db[e], H, N, codes[i], sb[i])
+        del down
+    Hs = torch.stack([synth.config1_h(i, N, 0.1) for i in range(n_copies)]).to(dev)
+    Y = torch.empty((n_copies, H), dtype=torch.bfloat16, device=dev)
+    cnt = torch.zeros(n_copies, dtype=torch.int32, device=dev)
+    WS = torch.empty(hs.hs_expert_down_sparse_workspace_size(N, H), dtype=torch.uint8, device=dev)
+    with torch.cuda.stream(stream):
+        for i in range(n_copies):
+            hs.hs_expert_down_sparse(Hs[i], codes[i], sb[i], N, H, Y[i], None, cnt[i:i + 1], 0, WS, stream=stream)
+    stream.synchronize()
+    assert hs.hs_device_status() == hs.HS_OK
+    h_cpu = Hs.cpu().numpy()
+    live_rows = cnt.cpu().numpy()
+    assert np.array_equal(live_rows, (h_cpu > 0).sum(axis=1))
+    live_groups = (h_cpu.reshape(n_copies, -1, 64) > 0).any(axis=2).sum(axis=1)
+    req = sum(bytemodel.down_sparse_bytes(int(r), int(g), H) + N * 4 + H * 2 for r, g in zip(live_rows, live_groups))
+    dense = n_copies * (bytemodel.down_sparse_bytes(N, N // 64, H) + N * 4 + H * 2)
+
+    def capture(flags):
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            for i in range(n_copies):
+                hs.hs_expert_down_sparse(Hs[i], codes[i], sb[i], N, H, Y[i], None, None, flags, WS, stream=stream)
+        return g
+    K = max(5, args.steps // 20)
+    ms, _ = timed(capture(0), K, 3, repeats=3)
+    ms_d, _ = timed(capture(hs.HS_FORCE_DENSE), K, 3, repeats=3)
+    us, us_d = ms * 1e3 / (K * n_copies), ms_d * 1e3 / (K * n_copies)
+    gbs = req / n_copies / (us * 1e-6) / 1e9
+    return {"workload": "expert_down_sparse_1tok_512copies_p0.1 (configuration 1: 2688x1856 W4 neuron-major)",
+            "unit": "us/call", "us_per_call": round(us, 3), "required_KB_per_call": round(req / n_copies / 1e3, 1),
+            "live_rows_per_call": round(float(live_rows.mean()), 1),
+            "live_groups_per_call": round(float(live_groups.mean()), 2),
+            "achieved_GBs": round(gbs, 1), "frac": round(gbs / peak, 4),
+            "dense_flag_us_per_call": round(us_d, 3),
+            "dense_flag_GBs": round(dense / n_copies / (us_d * 1e-6) / 1e9, 1),
+            "kernels_per_call": 2}
 
 
 def bench_p_sweep(args, layers, X, LG, dev, stream, timed, bytemodel, hs, peak):
@@ -560,6 +618,9 @@ def main():
         sweep["1.0"] = {"us_per_layer": round(us_layer_dense, 3), "note": "HS_FORCE_DENSE on the p = 0.1 inputs",
                         "required_MB_per_layer": round(dense_bytes / 1e6, 2),
                         "achieved_GBs": round(dense_bytes / (us_layer_dense * 1e-6) / 1e9, 1)}
+    expert_down = None
+    if not args.profile and not args.no_expert_down:
+        expert_down = bench_expert_down(args, dev, stream, timed, bytemodel, hs, peak)
     batch = None
     if not args.profile and args.batch_sizes:
         batch = bench_batch(args, dev, stream, timed, bytemodel, hs)
@@ -600,6 +661,7 @@ def main():
                      "groups_per_layer": round(float(np.mean(live_groups)), 1),
                      "required_MB_per_step": round(step_bytes / 1e6, 2)},
             "p_sweep": sweep,
+            "expert_down": expert_down,
             "batch_decode": batch,
             "prefill": prefill,
             "cpu_baseline": cpu,
