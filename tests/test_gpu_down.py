@@ -130,8 +130,10 @@ def test_edge_cases(case):
         check_bf16_within_one_ulp(y, ref, case, yf)
 
 
-@pytest.mark.parametrize("H,N", [(64, 64), (64, 128), (128, 192), (512, 64), (3072, 320)])
+@pytest.mark.parametrize("H,N", [(64, 64), (64, 128), (128, 192), (512, 64), (3072, 320), (128, 4096), (128, 4160),
+                                 (192, 8192)])
 def test_small_shapes_vs_oracle(H, N):
+    """Small and wide experts (up to 128 groups of 64 neurons)."""
     down = synth.gen_proj(H, N, (1, "small", H, N))
     codes, sb = repack(down)
     rng = np.random.default_rng(H + N)
@@ -142,3 +144,20 @@ def test_small_shapes_vs_oracle(H, N):
     check_close(yf, ref, f"{H}x{N}")
     check_bf16_within_one_ulp(y, ref, f"{H}x{N}", yf)
     assert cnt == int((h > 0).sum())
+
+
+@pytest.mark.parametrize("N", [4096, 4160])
+def test_dense_flag_equals_sparse_wide_experts(N):
+    """HS_FORCE_DENSE gives the sparse result bit for bit for wide experts
+    too, and repeats are identical."""
+    H = 256
+    down = synth.gen_proj(H, N, (2, "both", N))
+    codes, sb = repack(down)
+    z = np.random.default_rng(N).normal(-1.2815516, 1.0, N)
+    h = torch.from_numpy(oracle.relu2(z).astype(np.float32))
+    y1, yf1, c1 = run_down(h, codes, sb, N, H)
+    y2, yf2, c2 = run_down(h, codes, sb, N, H)
+    yd, yfd, cd = run_down(h, codes, sb, N, H, flags=hs.HS_FORCE_DENSE)
+    assert np.array_equal(yf1, yf2) and torch.equal(y1, y2) and c1 == c2
+    assert np.array_equal(yf1, yfd) and torch.equal(y1, yd)
+    assert cd == N
