@@ -47,7 +47,7 @@ def _args():
     ap.add_argument("--p", type=float, default=0.1)
     ap.add_argument("--layers", type=int, default=LAYERS)
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--batch-sizes", type=str, default="2,8,32,64",
+    ap.add_argument("--batch-sizes", type=str, default="2,3,8,32,64",
                     help="batch decode leg (one MoE layer, 30%% dead neurons); empty to skip")
     ap.add_argument("--no-prefill", action="store_true", help="skip the 2048-token prefill leg")
     ap.add_argument("--no-sweep", action="store_true", help="skip the live-fraction sweep")
@@ -221,7 +221,9 @@ def time_oracle(n_layers_max, p, budget_s, steps=None):
 def bench_batch(args, dev, stream, timed, bytemodel, hs):
     """Batch decode through one MoE layer: 8 distinct layers with 30% of every
     expert's neurons permanently dead and p = 0.1 on the rest, cycled so that
-    the weights a call reads are not left in L2 by the previous call."""
+    the weights a call reads are not left in L2 by the previous call.  B = 3
+    stands for the verify step of speculative decoding (three rows through the
+    same weights, sharing the permanently dead neurons)."""
     import torch
     import synth
     from activation_sparse_moe_gb300.layer import DeviceLayer, from_synth_expert, from_synth_stack
