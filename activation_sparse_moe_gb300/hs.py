@@ -72,6 +72,7 @@ _SIGS = {
     "hs_moe_layer_decode": (C.c_int, [C.POINTER(hs_moe_layer), C.c_void_p, C.c_void_p, C.c_int, C.c_void_p,
                                       C.c_void_p, C.c_uint, C.POINTER(hs_decode_debug), C.c_void_p, C.c_size_t,
                                       C.c_void_p]),
+    "hs_router_logits": (C.c_int, [C.c_void_p, C.c_void_p, C.c_int, C.c_int, C.c_int, C.c_void_p, C.c_void_p]),
     "hs_moe_prefill_workspace_size": (C.c_size_t, [C.POINTER(hs_moe_layer), C.c_int]),
     "hs_moe_prefill": (C.c_int, [C.POINTER(hs_moe_layer), C.c_void_p, C.c_void_p, C.c_int, C.c_void_p, C.c_void_p,
                                  C.c_uint, C.POINTER(hs_prefill_debug), C.c_void_p, C.c_size_t, C.c_void_p]),
@@ -206,6 +207,11 @@ def hs_moe_layer_decode(layer: Layer, x_bf16, logits, batch, y_bf16, y_f32=None,
     _check("hs_moe_layer_decode", lib().hs_moe_layer_decode(
         layer.ref, _p(x_bf16), _p(logits), batch, _p(y_bf16), _p(y_f32), flags, dbg, _p(workspace), nb,
         _stream(stream)))
+
+
+def hs_router_logits(x_bf16, w_router, batch, hidden, n_experts, logits, stream=None):
+    _check("hs_router_logits", lib().hs_router_logits(_p(x_bf16), _p(w_router), batch, hidden, n_experts,
+                                                      _p(logits), _stream(stream)))
 
 
 def hs_moe_prefill_workspace_size(layer: Layer, tokens: int) -> int:

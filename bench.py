@@ -51,6 +51,7 @@ def _args():
                     help="batch decode leg (one MoE layer, 30%% dead neurons); empty to skip")
     ap.add_argument("--no-prefill", action="store_true", help="skip the 2048-token prefill leg")
     ap.add_argument("--no-sweep", action="store_true", help="skip the live-fraction sweep")
+    ap.add_argument("--no-router", action="store_true", help="skip the router projection leg")
     ap.add_argument("--no-expert-down", action="store_true",
                     help="skip the single-expert sparse down leg (512 distinct experts)")
     ap.add_argument("--profile", action="store_true",
@@ -331,6 +332,43 @@ def bench_expert_down(args, dev, stream, timed, bytemodel, hs, peak):
             "dense_flag_us_per_call": round(us_d, 3),
             "dense_flag_GBs": round(dense / n_copies / (us_d * 1e-6) / 1e9, 1),
             "kernels_per_call": 2}
+
+
+def bench_router(args, layers, X, dev, stream, timed, hs, peak):
+    """The router projection ahead of each of the 23 resident layers: logits =
+    W_router x (bf16 [128][2688] per layer, 688 KB), alone and chained into
+    the layer decode on one stream (the decode then routes on these logits)."""
+    import torch
+    import synth
+    n, H, E = len(layers), 2688, 128
+    W = torch.stack([synth.router_weights(0, "cfg3-router", l) for l in range(n)]).to(dev)
+    LGr = torch.empty((n, E), dtype=torch.float32, device=dev)
+    Y = torch.empty((n, H), dtype=torch.bfloat16, device=dev)
+    WS = torch.zeros(max(dl.workspace_size(1) for dl in layers), dtype=torch.uint8, device=dev)
+    with torch.cuda.stream(stream):
+        for l, dl in enumerate(layers):
+            hs.hs_router_logits(X[l], W[l], 1, H, E, LGr[l], stream=stream)
+            hs.hs_moe_layer_decode(dl.c, X[l], LGr[l], 1, Y[l], None, 0, None, WS, stream=stream)
+    stream.synchronize()
+    assert hs.hs_device_status() == hs.HS_OK
+
+    def capture(with_layer):
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            for l, dl in enumerate(layers):
+                hs.hs_router_logits(X[l], W[l], 1, H, E, LGr[l], stream=stream)
+                if with_layer:
+                    hs.hs_moe_layer_decode(dl.c, X[l], LGr[l], 1, Y[l], None, 0, None, WS, stream=stream)
+        return g
+    K = max(10, args.steps // 4)
+    ms_r, _ = timed(capture(False), K, 3, repeats=3)
+    ms_rl, _ = timed(capture(True), K, 3, repeats=3)
+    us_r, us_rl = ms_r * 1e3 / (K * n), ms_rl * 1e3 / (K * n)
+    wbytes = E * H * 2 + H * 2 + E * 4
+    return {"workload": "router projection bf16 128x2688 per layer, 23 layers, batch 1", "unit": "us/layer",
+            "router_us_per_call": round(us_r, 3), "router_GBs": round(wbytes / (us_r * 1e-6) / 1e9, 1),
+            "router_frac": round(wbytes / (us_r * 1e-6) / 1e9 / peak, 4),
+            "router_and_layer_us_per_layer": round(us_rl, 3)}
 
 
 def bench_p_sweep(args, layers, X, LG, dev, stream, timed, bytemodel, hs, peak):
@@ -620,6 +658,9 @@ def main():
         sweep["1.0"] = {"us_per_layer": round(us_layer_dense, 3), "note": "HS_FORCE_DENSE on the p = 0.1 inputs",
                         "required_MB_per_layer": round(dense_bytes / 1e6, 2),
                         "achieved_GBs": round(dense_bytes / (us_layer_dense * 1e-6) / 1e9, 1)}
+    router = None
+    if not args.profile and not args.no_router:
+        router = bench_router(args, layers, X, dev, stream, timed, hs, peak)
     expert_down = None
     if not args.profile and not args.no_expert_down:
         expert_down = bench_expert_down(args, dev, stream, timed, bytemodel, hs, peak)
@@ -663,6 +704,7 @@ def main():
                      "groups_per_layer": round(float(np.mean(live_groups)), 1),
                      "required_MB_per_step": round(step_bytes / 1e6, 2)},
             "p_sweep": sweep,
+            "router": router,
             "expert_down": expert_down,
             "batch_decode": batch,
             "prefill": prefill,

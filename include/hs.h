@@ -184,6 +184,19 @@ int hs_expert_down_sparse_noalloc(const float* h_dev, const hs_w4* down_nm, int 
                                   uint16_t* y_bf16_dev, float* y_f32_dev, int* live_count_dev,
                                   unsigned flags, hs_stream_t stream);
 
+/* ------------------------------------------------------------------ router
+ * The router projection ahead of the layer (section "Inside a MoE layer": a
+ * router picks 6 of 128 experts for each token; the projection itself is not
+ * printed and is read as a linear map): logits[b][e] = sum_k W[e][k] x[b][k].
+ *   x_bf16_dev         [batch][hidden] bf16
+ *   w_router_bf16_dev  [n_experts][hidden] bf16, row-major, 16-byte aligned
+ *   logits_dev         [batch][n_experts] fp32 (the logits hs_moe_layer_decode
+ *                      and hs_moe_prefill take)
+ * hidden a multiple of 64, at most 3072.  fp32 accumulation, one fixed order
+ * per logit: deterministic.  No workspace. */
+int hs_router_logits(const uint16_t* x_bf16_dev, const uint16_t* w_router_bf16_dev, int batch, int hidden,
+                     int n_experts, float* logits_dev, hs_stream_t stream);
+
 /* ---------------------------------------------------------- layer decode
  * One MoE layer at decode for `batch` tokens (sections "Inside a MoE layer",
  * "Two projections and a switch", "Our way reads only the rows that fired"):

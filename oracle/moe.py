@@ -35,7 +35,7 @@ import numpy as np
 __all__ = [
     "as_f64", "unpack_codes", "dequant", "up_preact", "relu2", "live_set",
     "down_dense", "down_dense_sequential", "down_sparse_sequential",
-    "router_topk", "expert_forward", "moe_layer", "moe_tokens", "bf16_rne",
+    "router_logits", "router_topk", "expert_forward", "moe_layer", "moe_tokens", "bf16_rne",
     "group_live", "down_required_bytes",
 ]
 
@@ -132,6 +132,15 @@ def down_sparse_sequential(h, down) -> np.ndarray:
     for n in live_set(h):
         y = y + w[:, n] * h[n]
     return y
+
+
+def router_logits(x, w_router) -> np.ndarray:
+    """The router projection ("Inside a MoE layer": a router picks 6 of 128
+    experts; the projection is not printed, reading: a linear map from the
+    token to one logit per expert), logits[..., e] = sum_k W[e][k] x[..., k].
+
+    x: [H] or [T][H]; w_router: [E][H].  fp64 (inputs widened exactly)."""
+    return as_f64(x) @ as_f64(w_router).T
 
 
 def router_topk(logits, k: int = 6):

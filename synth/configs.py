@@ -23,7 +23,7 @@ import torch
 from .gen import (HIDDEN, N_EXPERTS, N_ROUTED, N_SHARED, Expert, W4Proj, config1_h, dead_mask, gen_expert,
                   gen_proj, gen_routed_stack, normal_bf16, normal_f32, stack_offsets)
 
-__all__ = ["LayerInputs", "layer_inputs", "tokens", "single_expert_down"]
+__all__ = ["LayerInputs", "layer_inputs", "tokens", "router_weights", "single_expert_down"]
 
 
 @dataclass
@@ -66,6 +66,12 @@ def tokens(seed: int, tag: str, layer: int, batch: int, hidden: int = HIDDEN, n_
     x = normal_bf16((batch, hidden), seed, tag, layer, "x")
     lg = normal_f32((batch, n_experts), seed, tag, layer, "logits")
     return x, lg
+
+
+def router_weights(seed: int, tag: str, layer: int, n_experts: int = N_EXPERTS, hidden: int = HIDDEN):
+    """Router projection W [n_experts][hidden] bf16 with entries N(0, 1/hidden),
+    so that the logits of x ~ N(0, 1) are about N(0, 1) like the given ones."""
+    return (normal_f32((n_experts, hidden), seed, tag, layer, "router") / float(np.sqrt(hidden))).to(torch.bfloat16)
 
 
 def single_expert_down(seed: int = 0, neurons: int = N_ROUTED, hidden: int = HIDDEN, p: float = 0.1,

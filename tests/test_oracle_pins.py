@@ -257,6 +257,29 @@ def test_router_softmax_closed_forms():
     assert (np.diff(w, axis=1) <= 0).all()
 
 
+def test_router_projection_hand_values_and_selectors():
+    """The router projection (reading of "Inside a MoE layer": one logit per
+    expert, a linear map of x): a hand-worked 3 x 4 case, selector rows that
+    must return single entries of x (a transposed W or a wrong axis fails),
+    an all-ones row that must return the exact sum, and linearity."""
+    x = np.array([1.0, 2.0, -3.0, 0.5])
+    W = np.array([[1.0, 0.0, 0.0, 0.0], [0.5, 0.5, 0.5, 0.5], [-1.0, 2.0, 0.0, 4.0]])
+    assert oracle.router_logits(x, W).tolist() == [1.0, 0.25, 5.0]
+    rng = np.random.default_rng(21)
+    H, E = 64, 8
+    xs = rng.integers(-64, 64, size=(3, H)) / 8.0           # dyadic: every sum below is exact in fp64
+    sel = np.zeros((E, H))
+    cols = [5, 0, 63, 17, 17, 2, 40, 9]
+    sel[np.arange(E), cols] = 1.0
+    L = oracle.router_logits(xs, sel)
+    assert L.shape == (3, E) and np.array_equal(L, xs[:, cols])
+    ones = np.ones((1, H))
+    assert oracle.router_logits(xs[0], ones)[0] == math.fsum(xs[0])
+    Wr = rng.integers(-8, 8, size=(E, H)) / 4.0
+    np.testing.assert_array_equal(oracle.router_logits(xs[0] + xs[1], Wr),
+                                  oracle.router_logits(xs[0], Wr) + oracle.router_logits(xs[1], Wr))
+
+
 # ------------------------------------------------------------ layer --------
 
 def _tiny_expert(rng, N, H, zero=False):
