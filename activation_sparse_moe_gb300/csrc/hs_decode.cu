@@ -51,18 +51,28 @@ struct DecodeIO {
 struct SmemLayout {
     static constexpr int kBars = 6;  // 4 up chunks, 1 down, 1 activations
     __host__ __device__ static int codes_bytes(int hidden) { return 64 * hidden / 2; }
-    __host__ __device__ static int sb_bytes(int hidden) { return hidden * 4; }
-    __host__ __device__ static int misc_off(int hidden) { return codes_bytes(hidden) + sb_bytes(hidden); }
+    // the up scales of 64 rows or the down slab (hidden pairs); with row scales
+    // (row = true) at least the 64 rows' (scale, bias) rows of hidden/64 pairs
+    // padded to 16 bytes
+    __host__ __device__ static int row_sb_words(int hidden) { return ((hidden / 64) + 3) & ~3; }
+    __host__ __device__ static int sb_bytes(int hidden, bool row = false) {
+        return row && 64 * 4 * row_sb_words(hidden) > hidden * 4 ? 64 * 4 * row_sb_words(hidden) : hidden * 4;
+    }
+    __host__ __device__ static int misc_off(int hidden, bool row = false) {
+        return codes_bytes(hidden) + sb_bytes(hidden, row);
+    }
     // misc: h[64] f32, off[64] f32, topk_i[8] i32, topk_w[8] f32, bars[8] u64, live mask (u64, or
     //       8 bytes of per-warp row bits), hsum f32,
     // then x[hidden] bf16 (staging), the fixed-point x table [G][144 B] and its
     // per-group (2^(E-15), sum x) pairs [G][2] f32.
     static constexpr int kH = 0, kOff = 256, kTopI = 512, kTopW = kTopI + 32, kBarsOff = kTopW + 32,
                          kLive = kBarsOff + 64, kHsum = kLive + 8, kX = kHsum + 24;
-    __host__ __device__ static int x_off(int hidden) { return misc_off(hidden) + kX; }
-    __host__ __device__ static int xf_off(int hidden) { return x_off(hidden) + 2 * hidden; }
-    __host__ __device__ static int xs_off(int hidden) { return xf_off(hidden) + (hidden / 64) * hs::kXfStride; }
-    __host__ __device__ static int total(int hidden) { return xs_off(hidden) + (hidden / 64) * 8; }
+    __host__ __device__ static int x_off(int hidden, bool row = false) { return misc_off(hidden, row) + kX; }
+    __host__ __device__ static int xf_off(int hidden, bool row = false) { return x_off(hidden, row) + 2 * hidden; }
+    __host__ __device__ static int xs_off(int hidden, bool row = false) {
+        return xf_off(hidden, row) + (hidden / 64) * hs::kXfStride;
+    }
+    __host__ __device__ static int total(int hidden, bool row = false) { return xs_off(hidden, row) + (hidden / 64) * 8; }
 };
 
 // Partial rows are stored column-block-major: the 32 outputs of block cb of
@@ -198,19 +208,39 @@ __device__ __forceinline__ void warp0_mask_and_issue(const float* h_s, bool dens
 // Nibble i of a code word becomes a float by masking it in place under the
 // exponent of 2^23 and subtracting 2^23 (exact: q * 16^i < 2^23); the row's h
 // is pre-scaled by 16^-i to undo the position.
-template <int OPT>
+//
+// kRow (HS_DOWN_ROW_SCALES): sb_buf holds each live row's own (scale, bias)
+// per 64 outputs (row n at n * rsw words) instead of the group's slab, and
+// each term is h_n * (s_{n,g(o)} q_{n,o} + b_{n,g(o)}), added to the chain as
+// fma(h s 16^-i, q 16^i, acc + h b); partial_o = wgt * sum.
+template <int OPT, bool kRow>
 __device__ __forceinline__ void down_acc_and_store(const uint8_t* codes_buf, const uint32_t* sb_buf,
                                                    const float* h_s, uint64_t live, float Hsum, float wgt,
-                                                   int rowb, int j, const PartialOut out) {
+                                                   int rowb, int j, const PartialOut out, int rsw) {
     static_assert(OPT == 12 || OPT == 16, "12 or 16 outputs per thread");
     float acc[OPT];
 #pragma unroll
     for (int e = 0; e < OPT; ++e) acc[e] = 0.f;
+    // with row scales, this thread's outputs OPT*j .. OPT*j+OPT-1 lie in groups g0 and g0 + 1
+    const int g0 = (OPT * j) >> 6;
     while (live) {
         const int n = __ffsll((long long)live) - 1;
         live &= live - 1;
         const float hn = h_s[n];
-        const float hs[5] = {hn, hn * 0.0625f, hn * 0.00390625f, hn * 0.000244140625f, hn * 1.52587890625e-05f};
+        float hs[5] = {hn, hn * 0.0625f, hn * 0.00390625f, hn * 0.000244140625f, hn * 1.52587890625e-05f};
+        float hs1[5], hb0 = 0.f, hb1 = 0.f;
+        if (kRow) {
+            const uint32_t* sr = sb_buf + (size_t)n * rsw;
+            const float2 p0 = half2_to_float2(sr[g0]);
+            const float2 p1 = half2_to_float2(sr[min(g0 + 1, rsw - 1)]);
+#pragma unroll
+            for (int i = 0; i < 5; ++i) {
+                hs1[i] = hs[i] * p1.x;
+                hs[i] *= p0.x;
+            }
+            hb0 = hn * p0.y;
+            hb1 = hn * p1.y;
+        }
         const uint8_t* row = codes_buf + (size_t)n * rowb;
         uint32_t w[2];
         if (OPT == 16) {
@@ -235,9 +265,21 @@ __device__ __forceinline__ void down_acc_and_store(const uint8_t* codes_buf, con
                 const uint32_t src = i < 5 ? w[jj] : hi;
                 const int pos = i < 5 ? i : i - 3;
                 const float q = __uint_as_float((src & (15u << (4 * pos))) | 0x4B000000u) - 8388608.f;
-                acc[8 * jj + i] = fmaf(hs[pos], q, acc[8 * jj + i]);
+                if (kRow) {
+                    const bool second = OPT * j + 8 * jj + i >= 64 * (g0 + 1);
+                    acc[8 * jj + i] = fmaf(second ? hs1[pos] : hs[pos], q, acc[8 * jj + i] + (second ? hb1 : hb0));
+                } else {
+                    acc[8 * jj + i] = fmaf(hs[pos], q, acc[8 * jj + i]);
+                }
             }
         }
+    }
+    if (kRow) {
+#pragma unroll
+        for (int i = 0; i < OPT / 4; ++i)
+            *out.quad((OPT / 4) * j + i) =
+                make_float4(wgt * acc[4 * i], wgt * acc[4 * i + 1], wgt * acc[4 * i + 2], wgt * acc[4 * i + 3]);
+        return;
     }
     const uint4* sbq = reinterpret_cast<const uint4*>(sb_buf) + (OPT / 4) * j;
 #pragma unroll
@@ -255,19 +297,21 @@ __device__ __forceinline__ void down_acc_and_store(const uint8_t* codes_buf, con
 }
 
 // --------------------------------------------------- fused layer kernel (B=1)
+// kRow: the experts' down projections carry per-row scales (HS_DOWN_ROW_SCALES).
+template <bool kRow>
 __global__ void __launch_bounds__(256, 2)
 moe_decode_b1_kernel(const __grid_constant__ LayerParams P, const DecodeIO io) {
     extern __shared__ __align__(128) uint8_t smem[];
     const int hidden = P.hidden;
     uint8_t* codes_buf = smem;
     uint32_t* sb_buf = reinterpret_cast<uint32_t*>(smem + SmemLayout::codes_bytes(hidden));
-    uint8_t* misc = smem + SmemLayout::misc_off(hidden);
+    uint8_t* misc = smem + SmemLayout::misc_off(hidden, kRow);
     float* h_s = reinterpret_cast<float*>(misc + SmemLayout::kH);
     float* off_s = reinterpret_cast<float*>(misc + SmemLayout::kOff);
     int* topk_i = reinterpret_cast<int*>(misc + SmemLayout::kTopI);
     float* topk_w = reinterpret_cast<float*>(misc + SmemLayout::kTopW);
     uint64_t* bars = reinterpret_cast<uint64_t*>(misc + SmemLayout::kBarsOff);
-    uint16_t* x_s = reinterpret_cast<uint16_t*>(smem + SmemLayout::x_off(hidden));
+    uint16_t* x_s = reinterpret_cast<uint16_t*>(smem + SmemLayout::x_off(hidden, kRow));
 
     const int t = threadIdx.x;
     const int u = blockIdx.x;
@@ -317,8 +361,8 @@ moe_decode_b1_kernel(const __grid_constant__ LayerParams P, const DecodeIO io) {
     const int S = 256 / G;
     const int gc = t % G, r0 = t / G;
     const bool up_active = r0 < S;
-    uint8_t* xf_s = smem + SmemLayout::xf_off(hidden);
-    float* xs_s = reinterpret_cast<float*>(smem + SmemLayout::xs_off(hidden));
+    uint8_t* xf_s = smem + SmemLayout::xf_off(hidden, kRow);
+    float* xs_s = reinterpret_cast<float*>(smem + SmemLayout::xs_off(hidden, kRow));
     // routing first, with the rest of the CTA idle (a latency-bound chain);
     // the routed weight copies go out before x is converted, so the
     // conversion overlaps their latency
@@ -412,8 +456,12 @@ moe_decode_b1_kernel(const __grid_constant__ LayerParams P, const DecodeIO io) {
             }
             lv = dense || h > 0.f;
             if (lv) {
-                mbar_expect_tx(&bars[4], (uint32_t)rowb);
+                const uint32_t rsb = kRow ? 4u * SmemLayout::row_sb_words(hidden) : 0u;
+                mbar_expect_tx(&bars[4], (uint32_t)rowb + rsb);
                 bulk_g2s(codes_buf + (size_t)r * rowb, ep.dn_codes + ((size_t)g * 64 + r) * rowb, rowb, &bars[4], pol);
+                if (kRow)
+                    bulk_g2s(reinterpret_cast<uint8_t*>(sb_buf) + (size_t)r * rsb,
+                             reinterpret_cast<const uint8_t*>(ep.dn_sb) + ((size_t)g * 64 + r) * rsb, rsb, &bars[4], pol);
             }
         }
         const unsigned b = __ballot_sync(0xffffffffu, lv);  // bits at lanes 4i
@@ -428,8 +476,12 @@ moe_decode_b1_kernel(const __grid_constant__ LayerParams P, const DecodeIO io) {
     // the down barrier comes after every row's expected bytes were added
     const bool any = __syncthreads_or(lv) != 0;
     if (t == 0 && any) {
-        mbar_arrive_expect_tx(&bars[4], (uint32_t)hidden * 4);
-        bulk_g2s(sb_buf, ep.dn_sb + (size_t)g * hidden, hidden * 4, &bars[4], pol);
+        if (kRow) {
+            mbar_arrive(&bars[4]);  // the rows' scales came with the rows
+        } else {
+            mbar_arrive_expect_tx(&bars[4], (uint32_t)hidden * 4);
+            bulk_g2s(sb_buf, ep.dn_sb + (size_t)g * hidden, hidden * 4, &bars[4], pol);
+        }
     }
     const uint64_t live = *reinterpret_cast<const uint64_t*>(live8);
     const PartialOut out_row{io.partial, io.units, u};
@@ -445,10 +497,11 @@ moe_decode_b1_kernel(const __grid_constant__ LayerParams P, const DecodeIO io) {
     const int nthr = hidden % 48 == 0 ? hidden / 12 : hidden / 16;
     if (t >= nthr) return;
     if (!mbar_wait(&bars[4], 0)) return;
+    const int rsw = SmemLayout::row_sb_words(hidden);
     if (hidden % 48 == 0)
-        down_acc_and_store<12>(codes_buf, sb_buf, h_s, live, Hsum, wgt, rowb, t, out_row);
+        down_acc_and_store<12, kRow>(codes_buf, sb_buf, h_s, live, Hsum, wgt, rowb, t, out_row, rsw);
     else
-        down_acc_and_store<16>(codes_buf, sb_buf, h_s, live, Hsum, wgt, rowb, t, out_row);
+        down_acc_and_store<16, kRow>(codes_buf, sb_buf, h_s, live, Hsum, wgt, rowb, t, out_row, rsw);
 }
 
 // ------------------------------------------ single-expert sparse down (K1)
@@ -607,6 +660,7 @@ extern "C" int hs_expert_down_sparse(const float* h, const hs_w4* down_nm, int n
                                      float* y_f32, int* live_count, unsigned flags, void* ws, size_t ws_bytes,
                                      hs_stream_t stream) {
     if (!h || !down_nm || !down_nm->codes || !down_nm->sb || !y_bf16) return HS_ERR_INVALID_ARG;
+    if (flags & HS_DOWN_ROW_SCALES) return HS_ERR_INVALID_ARG;  // group slabs only
     if (neurons <= 0 || out_dim <= 0) return HS_ERR_INVALID_ARG;
     if (neurons % 64 || out_dim % 64 || out_dim > hs::kMaxHidden) return HS_ERR_UNSUPPORTED_SHAPE;
     if (!al16(h) || !al16(down_nm->codes) || !al16(down_nm->sb) || !al16(y_bf16) || (y_f32 && !al16(y_f32)) ||
@@ -648,9 +702,11 @@ extern "C" int hs_moe_layer_decode(const hs_moe_layer* L, const uint16_t* x, con
     if (batch < 1) return HS_ERR_INVALID_ARG;
     if (!al16(x) || !al4(logits) || !al16(y_bf16) || (y_f32 && !al16(y_f32)) || !al16(ws)) return HS_ERR_MISALIGNED;
     if (dbg && ((dbg->topk_idx == nullptr) != (dbg->topk_w == nullptr))) return HS_ERR_INVALID_ARG;
-    if (batch > 1)
+    if (batch > 1) {
+        if (flags & HS_DOWN_ROW_SCALES) return HS_ERR_INVALID_ARG;  // batch 1 only
         return hs_batch_decode(L, x, logits, batch, y_bf16, y_f32, flags, dbg, ws, ws_bytes,
                                reinterpret_cast<cudaStream_t>(stream));
+    }
     const size_t need = hs_moe_layer_decode_workspace_size(L, batch);
     if (!ws || ws_bytes < need) return HS_ERR_WORKSPACE;
     if (dbg && ((dbg->topk_idx == nullptr) != (dbg->topk_w == nullptr))) return HS_ERR_INVALID_ARG;
@@ -671,10 +727,12 @@ extern "C" int hs_moe_layer_decode(const hs_moe_layer* L, const uint16_t* x, con
     io.dbg_h = dbg ? dbg->h : nullptr;
     int* live_out = dbg ? dbg->live_rows : nullptr;
 
-    const int smem = hs::SmemLayout::total(L->hidden);
-    if (set_smem_attr((const void*)hs::moe_decode_b1_kernel, smem) != HS_OK) return HS_ERR_CUDA;
+    const int smem = hs::SmemLayout::total(L->hidden, (flags & HS_DOWN_ROW_SCALES) != 0);
+    void (*kern)(const hs::LayerParams, const hs::DecodeIO) =
+        (flags & HS_DOWN_ROW_SCALES) ? hs::moe_decode_b1_kernel<true> : hs::moe_decode_b1_kernel<false>;
+    if (set_smem_attr((const void*)kern, smem) != HS_OK) return HS_ERR_CUDA;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-    if (launch_pdl(hs::moe_decode_b1_kernel, dim3(U), dim3(256), smem, s, P, io) != cudaSuccess) return HS_ERR_CUDA;
+    if (launch_pdl(kern, dim3(U), dim3(256), smem, s, P, io) != cudaSuccess) return HS_ERR_CUDA;
     if (set_smem_attr((const void*)hs::reduce_partials_kernel, U * 128) != HS_OK) return HS_ERR_CUDA;
     if (launch_pdl(hs::reduce_partials_kernel, dim3(L->hidden / 32), dim3(256), (size_t)U * 128, s,
                    (const float*)io.partial, U, L->hidden, y_bf16, y_f32, (const int*)io.live_counts,
@@ -730,6 +788,7 @@ extern "C" int hs_expert_down_sparse_noalloc(const float* h, const hs_w4* down_n
                                              uint16_t* y_bf16, float* y_f32, int* live_count, unsigned flags,
                                              hs_stream_t stream) {
     if (!h || !down_nm || !down_nm->codes || !down_nm->sb || !y_bf16) return HS_ERR_INVALID_ARG;
+    if (flags & HS_DOWN_ROW_SCALES) return HS_ERR_INVALID_ARG;  // group slabs only
     if (neurons <= 0 || out_dim <= 0) return HS_ERR_INVALID_ARG;
     if (neurons % 64 || out_dim % 64) return HS_ERR_UNSUPPORTED_SHAPE;
     // beyond the compiled-in scratch capacity

@@ -1050,6 +1050,7 @@ extern "C" int hs_moe_prefill(const hs_moe_layer* L, const uint16_t* x, const fl
     if (st != HS_OK) return st;
     if (!x || !logits || !y_bf16) return HS_ERR_INVALID_ARG;
     if (tokens < 1) return HS_ERR_INVALID_ARG;
+    if (flags & HS_DOWN_ROW_SCALES) return HS_ERR_INVALID_ARG;  // group slabs only
     st = prefill_shape_ok(L, tokens);
     if (st != HS_OK) return st;
     if (!al16(x) || !al4(logits) || !al16(y_bf16) || (y_f32 && !al16(y_f32)) || !al16(ws)) return HS_ERR_MISALIGNED;

@@ -49,9 +49,76 @@ __global__ void pack_sb_kernel(const uint16_t* __restrict__ s, const uint16_t* _
     if (i < n) sb[i] = (uint32_t)s[i] | ((uint32_t)b[i] << 16);
 }
 
+// Re-quantisation of a checkpoint down projection with its scales along the
+// neuron axis (section "The whole decode step": the checkpoint's scales per
+// group of 64 neurons make one live neuron cost its group's scales).  Thread
+// (n, j) takes neuron n's outputs 64j .. 64j+63: w = fma(s, q, b) in fp32
+// (the exact value rounded once), scale = fp16((max - min) / 15), bias =
+// fp16(min), q = clamp(rint((w - bias) / scale), 0, 15) (0 where scale is 0),
+// every step rounded to fp32 as written.  Writes the neuron-major codes and
+// the row's (scale, bias) pair for group j; thread (n, 0) zeroes the row's
+// padding words.
+__global__ void __launch_bounds__(256) requant_rowscale_kernel(const uint8_t* __restrict__ om,
+                                                               const uint16_t* __restrict__ s_om,
+                                                               const uint16_t* __restrict__ b_om, int out_dim,
+                                                               int neurons, uint8_t* __restrict__ nm,
+                                                               uint32_t* __restrict__ sb_row, int sbw) {
+    const int n = blockIdx.x * blockDim.x + threadIdx.x, j = blockIdx.y;
+    if (n >= neurons) return;
+    const int Gn = neurons / 64;
+    float w[64];
+    float mx = -INFINITY, mn = INFINITY;
+#pragma unroll
+    for (int k = 0; k < 64; ++k) {
+        const int o = 64 * j + k;
+        const uint8_t byte = om[(size_t)o * (neurons / 2) + n / 2];
+        const float q = (float)((n & 1) ? byte >> 4 : byte & 15);
+        const size_t gi = (size_t)o * Gn + n / 64;
+        w[k] = fmaf(__half2float(__ushort_as_half(s_om[gi])), q, __half2float(__ushort_as_half(b_om[gi])));
+        mx = fmaxf(mx, w[k]);
+        mn = fminf(mn, w[k]);
+    }
+    const __half sh = __float2half_rn((mx - mn) / 15.0f);
+    const __half bh = __float2half_rn(mn);
+    const float sf = __half2float(sh), bf = __half2float(bh);
+    uint32_t packed[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        uint32_t v = 0;
+#pragma unroll
+        for (int m = 0; m < 8; ++m) {
+            const float qf = sf == 0.f ? 0.f : fminf(fmaxf(rintf((w[8 * i + m] - bf) / sf), 0.f), 15.f);
+            v |= (uint32_t)qf << (4 * m);
+        }
+        packed[i] = v;
+    }
+    uint4* dst = reinterpret_cast<uint4*>(nm + (size_t)n * (out_dim / 2) + 32 * j);
+    dst[0] = make_uint4(packed[0], packed[1], packed[2], packed[3]);
+    dst[1] = make_uint4(packed[4], packed[5], packed[6], packed[7]);
+    uint32_t* row = sb_row + (size_t)n * sbw;
+    row[j] = (uint32_t)__half_as_ushort(sh) | ((uint32_t)__half_as_ushort(bh) << 16);
+    if (j == 0)
+        for (int p = out_dim / 64; p < sbw; ++p) row[p] = 0u;
+}
+
 }  // namespace hs
 
 static bool aligned16(const void* p) { return ((uintptr_t)p & 15u) == 0; }
+
+extern "C" int hs_requant_down_rowscale(const uint8_t* codes_om, const uint16_t* scale_om, const uint16_t* bias_om,
+                                        int out_dim, int neurons, uint8_t* codes_nm, void* sb_row,
+                                        hs_stream_t stream) {
+    if (!codes_om || !scale_om || !bias_om || !codes_nm || !sb_row) return HS_ERR_INVALID_ARG;
+    if (out_dim <= 0 || neurons <= 0) return HS_ERR_INVALID_ARG;
+    if (out_dim % 64 || neurons % 64) return HS_ERR_UNSUPPORTED_SHAPE;
+    if (!aligned16(codes_nm) || !aligned16(sb_row) || ((uintptr_t)scale_om & 1) || ((uintptr_t)bias_om & 1))
+        return HS_ERR_MISALIGNED;
+    dim3 grid((neurons + 255) / 256, out_dim / 64);
+    hs::requant_rowscale_kernel<<<grid, 256, 0, reinterpret_cast<cudaStream_t>(stream)>>>(
+        codes_om, scale_om, bias_om, out_dim, neurons, codes_nm, reinterpret_cast<uint32_t*>(sb_row),
+        hs_row_sb_words(out_dim));
+    return cudaGetLastError() == cudaSuccess ? HS_OK : HS_ERR_CUDA;
+}
 
 extern "C" int hs_repack_down_nm(const uint8_t* codes_om, const uint16_t* scale_om, const uint16_t* bias_om,
                                  int out_dim, int neurons, uint8_t* codes_nm, void* sb_nm, hs_stream_t stream) {

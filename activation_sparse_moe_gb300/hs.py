@@ -24,6 +24,7 @@ HS_ERR_CUDA = -5
 HS_ERR_TIMEOUT = -6
 HS_FORCE_DENSE = 0x1
 HS_BATCH_EXPERT_UNION = 0x2
+HS_DOWN_ROW_SCALES = 0x4
 
 
 class HsError(RuntimeError):
@@ -72,6 +73,8 @@ _SIGS = {
     "hs_moe_layer_decode": (C.c_int, [C.POINTER(hs_moe_layer), C.c_void_p, C.c_void_p, C.c_int, C.c_void_p,
                                       C.c_void_p, C.c_uint, C.POINTER(hs_decode_debug), C.c_void_p, C.c_size_t,
                                       C.c_void_p]),
+    "hs_requant_down_rowscale": (C.c_int, [C.c_void_p, C.c_void_p, C.c_void_p, C.c_int, C.c_int, C.c_void_p,
+                                           C.c_void_p, C.c_void_p]),
     "hs_router_logits": (C.c_int, [C.c_void_p, C.c_void_p, C.c_int, C.c_int, C.c_int, C.c_void_p, C.c_void_p]),
     "hs_moe_prefill_workspace_size": (C.c_size_t, [C.POINTER(hs_moe_layer), C.c_int]),
     "hs_moe_prefill": (C.c_int, [C.POINTER(hs_moe_layer), C.c_void_p, C.c_void_p, C.c_int, C.c_void_p, C.c_void_p,
@@ -97,10 +100,18 @@ def lib() -> C.CDLL:
 
 
 def declared_functions() -> list[str]:
-    """Names of the functions include/hs.h declares."""
+    """Names of the functions include/hs.h declares for export (its static
+    inline helpers are compiled into the caller and are not exported)."""
     txt = open(HEADER).read()
     txt = re.sub(r"/\*.*?\*/", "", txt, flags=re.S)
+    txt = re.sub(r"^\s*static\s+inline\b.*$", "", txt, flags=re.M)
     return sorted(set(re.findall(r"^\s*(?:const\s+)?[A-Za-z_][\w\s\*]*?\b(hs_\w+)\s*\(", txt, flags=re.M)))
+
+
+def hs_row_sb_words(out_dim: int) -> int:
+    """Words per neuron row of a row-scale (scale, bias) array (the header's
+    inline helper of the same name): one per 64 outputs, padded to 16 bytes."""
+    return ((out_dim // 64) + 3) & ~3
 
 
 def _p(t) -> int | None:
@@ -207,6 +218,11 @@ def hs_moe_layer_decode(layer: Layer, x_bf16, logits, batch, y_bf16, y_f32=None,
     _check("hs_moe_layer_decode", lib().hs_moe_layer_decode(
         layer.ref, _p(x_bf16), _p(logits), batch, _p(y_bf16), _p(y_f32), flags, dbg, _p(workspace), nb,
         _stream(stream)))
+
+
+def hs_requant_down_rowscale(codes_om, scale_om, bias_om, out_dim, neurons, codes_nm, sb_row, stream=None):
+    _check("hs_requant_down_rowscale", lib().hs_requant_down_rowscale(
+        _p(codes_om), _p(scale_om), _p(bias_om), out_dim, neurons, _p(codes_nm), _p(sb_row), _stream(stream)))
 
 
 def hs_router_logits(x_bf16, w_router, batch, hidden, n_experts, logits, stream=None):

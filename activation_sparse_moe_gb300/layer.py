@@ -26,7 +26,7 @@ class DeviceExperts:
     [E][H][N/64] fp16, offsets [E][N] fp32 or None."""
 
     def __init__(self, up_codes, up_scale, up_bias, down_codes, down_scale, down_bias, offsets=None,
-                 device="cuda", stream=None):
+                 device="cuda", stream=None, down_row_scales: bool = False):
         E, N, Hh = up_codes.shape
         H = Hh * 2
         self.E, self.N, self.H = E, N, H
@@ -36,11 +36,18 @@ class DeviceExperts:
         us, ub = _u16(up_scale.to(dev)), _u16(up_bias.to(dev))
         hs.hs_pack_sb(us, ub, E * N, H // 64, self.up_sb, stream)
         self.dn_codes = torch.empty((E, N, H // 2), dtype=torch.uint8, device=dev)
-        self.dn_sb = torch.empty((E, N // 64, H), dtype=torch.int32, device=dev)
         dc = down_codes.to(dev).contiguous()
         ds, db = _u16(down_scale.to(dev)), _u16(down_bias.to(dev))
-        for e in range(E):
-            hs.hs_repack_down_nm(dc[e], ds[e], db[e], H, N, self.dn_codes[e], self.dn_sb[e], stream)
+        self.down_row_scales = down_row_scales
+        if down_row_scales:
+            # re-quantised with one (scale, bias) per neuron row and 64 outputs (HS_DOWN_ROW_SCALES)
+            self.dn_sb = torch.empty((E, N, hs.hs_row_sb_words(H)), dtype=torch.int32, device=dev)
+            for e in range(E):
+                hs.hs_requant_down_rowscale(dc[e], ds[e], db[e], H, N, self.dn_codes[e], self.dn_sb[e], stream)
+        else:
+            self.dn_sb = torch.empty((E, N // 64, H), dtype=torch.int32, device=dev)
+            for e in range(E):
+                hs.hs_repack_down_nm(dc[e], ds[e], db[e], H, N, self.dn_codes[e], self.dn_sb[e], stream)
         self.offsets = None if offsets is None else offsets.to(dev, torch.float32).contiguous()
 
     def with_offsets(self, offsets) -> "DeviceExperts":
@@ -58,17 +65,18 @@ class DeviceExperts:
         return sum(t.numel() * t.element_size() for t in (self.up_codes, self.up_sb, self.dn_codes, self.dn_sb))
 
 
-def from_synth_stack(up, down, offsets, device="cuda", stream=None) -> DeviceExperts:
+def from_synth_stack(up, down, offsets, device="cuda", stream=None, down_row_scales=False) -> DeviceExperts:
     """DeviceExperts from stacked checkpoint-layout projections (objects with
     .codes/.scale/.bias tensors carrying a leading expert axis)."""
-    return DeviceExperts(up.codes, up.scale, up.bias, down.codes, down.scale, down.bias, offsets, device, stream)
+    return DeviceExperts(up.codes, up.scale, up.bias, down.codes, down.scale, down.bias, offsets, device, stream,
+                         down_row_scales)
 
 
-def from_synth_expert(ex, device="cuda", stream=None) -> DeviceExperts:
+def from_synth_expert(ex, device="cuda", stream=None, down_row_scales=False) -> DeviceExperts:
     """A one-expert DeviceExperts from a single checkpoint-layout expert."""
     u, d = ex.up, ex.down
     return DeviceExperts(u.codes[None], u.scale[None], u.bias[None], d.codes[None], d.scale[None], d.bias[None],
-                         None if ex.offset is None else ex.offset[None], device, stream)
+                         None if ex.offset is None else ex.offset[None], device, stream, down_row_scales)
 
 
 class DeviceLayer:

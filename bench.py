@@ -52,6 +52,8 @@ def _args():
     ap.add_argument("--no-prefill", action="store_true", help="skip the 2048-token prefill leg")
     ap.add_argument("--no-sweep", action="store_true", help="skip the live-fraction sweep")
     ap.add_argument("--no-router", action="store_true", help="skip the router projection leg")
+    ap.add_argument("--no-row-scales", action="store_true",
+                    help="skip the leg with the down projections re-quantised with row scales")
     ap.add_argument("--no-expert-down", action="store_true",
                     help="skip the single-expert sparse down leg (512 distinct experts)")
     ap.add_argument("--profile", action="store_true",
@@ -163,14 +165,14 @@ def _recorded_traffic(kernel: str, srcs):
 
 
 # ------------------------------------------------------------- workload
-def build_layers(n_layers, p, device):
+def build_layers(n_layers, p, device, down_row_scales=False):
     import synth
     from activation_sparse_moe_gb300.layer import DeviceLayer, from_synth_expert, from_synth_stack
     layers = []
     for l in range(n_layers):
         L = synth.layer_inputs(0, "cfg3", l, p=p, p_shared=synth.shared_live_fraction(0, l), device=device)
-        dl = DeviceLayer(from_synth_stack(L.up, L.down, L.offsets, device),
-                         from_synth_expert(L.shared, device), top_k=6)
+        dl = DeviceLayer(from_synth_stack(L.up, L.down, L.offsets, device, down_row_scales=down_row_scales),
+                         from_synth_expert(L.shared, device, down_row_scales=down_row_scales), top_k=6)
         layers.append(dl)
         del L
     return layers
@@ -369,6 +371,44 @@ def bench_router(args, layers, X, dev, stream, timed, hs, peak):
             "router_us_per_call": round(us_r, 3), "router_GBs": round(wbytes / (us_r * 1e-6) / 1e9, 1),
             "router_frac": round(wbytes / (us_r * 1e-6) / 1e9 / peak, 4),
             "router_and_layer_us_per_layer": round(us_rl, 3)}
+
+
+def bench_row_scales(args, X, LG, dev, stream, timed, bytemodel, hs, peak):
+    """The same 23 layers with every down projection re-quantised along the
+    neuron axis (one (scale, bias) per neuron row and 64 outputs, section "The
+    whole decode step"), decoded with HS_DOWN_ROW_SCALES: a live row brings
+    its own 176 bytes of scales and no group slab is read."""
+    import torch
+    n, H = X.shape[0], 2688
+    layers = build_layers(n, args.p, dev, down_row_scales=True)
+    Y = torch.empty((n, H), dtype=torch.bfloat16, device=dev)
+    WS = torch.zeros(max(dl.workspace_size(1) for dl in layers), dtype=torch.uint8, device=dev)
+    flags = hs.HS_DOWN_ROW_SCALES
+    rows = []
+    with torch.cuda.stream(stream):
+        for l, dl in enumerate(layers):
+            dbg = {"live_rows": torch.empty(1, dtype=torch.int32, device=dev),
+                   "live_groups": torch.empty(1, dtype=torch.int32, device=dev)}
+            hs.hs_moe_layer_decode(dl.c, X[l], LG[l], 1, Y[l], None, flags, dbg, WS, stream=stream)
+            stream.synchronize()
+            rows.append(int(dbg["live_rows"].item()))
+    assert hs.hs_device_status() == hs.HS_OK
+    row_bytes = H // 2 + 4 * hs.hs_row_sb_words(H)
+    req = sum(bytemodel.decode_layer_bytes(H, [3712] + [1856] * 6, 0, 0, 128) + r * row_bytes for r in rows)
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=stream):
+        for l, dl in enumerate(layers):
+            hs.hs_moe_layer_decode(dl.c, X[l], LG[l], 1, Y[l], None, flags, None, WS, stream=stream)
+    K = max(20, args.steps // 2)
+    ms, _ = timed(g, K, 3, repeats=3)
+    us = ms * 1e3 / (K * n)
+    gbs = req / n / (us * 1e-6) / 1e9
+    del layers, g
+    torch.cuda.empty_cache()
+    return {"workload": "moe_decode_b1_23layers_p0.1, down projections re-quantised with row scales",
+            "unit": "us/layer", "us_per_layer": round(us, 3), "required_MB_per_layer": round(req / n / 1e6, 2),
+            "live_rows_per_layer": round(sum(rows) / n, 1), "bytes_per_live_row": row_bytes,
+            "achieved_GBs": round(gbs, 1), "frac": round(gbs / peak, 4), "flag": "HS_DOWN_ROW_SCALES"}
 
 
 def bench_p_sweep(args, layers, X, LG, dev, stream, timed, bytemodel, hs, peak):
@@ -658,6 +698,9 @@ def main():
         sweep["1.0"] = {"us_per_layer": round(us_layer_dense, 3), "note": "HS_FORCE_DENSE on the p = 0.1 inputs",
                         "required_MB_per_layer": round(dense_bytes / 1e6, 2),
                         "achieved_GBs": round(dense_bytes / (us_layer_dense * 1e-6) / 1e9, 1)}
+    row_scales = None
+    if not args.profile and not args.no_row_scales:
+        row_scales = bench_row_scales(args, X, LG, dev, stream, timed, bytemodel, hs, peak)
     router = None
     if not args.profile and not args.no_router:
         router = bench_router(args, layers, X, dev, stream, timed, hs, peak)
@@ -704,6 +747,7 @@ def main():
                      "groups_per_layer": round(float(np.mean(live_groups)), 1),
                      "required_MB_per_step": round(step_bytes / 1e6, 2)},
             "p_sweep": sweep,
+            "row_scales": row_scales,
             "router": router,
             "expert_down": expert_down,
             "batch_decode": batch,

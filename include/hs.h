@@ -70,6 +70,12 @@ typedef struct CUstream_st* hs_stream_t;
                                  the dense comparison path through the same
                                  kernels (section "The standard way reads
                                  everything"); results equal the sparse path */
+#define HS_DOWN_ROW_SCALES 0x4u  /* batch-1 layer decode only: every expert's
+                                 down_nm.sb holds per-row scales (the layout
+                                 of hs_requant_down_rowscale) instead of the
+                                 per-group slabs; no slab is read.  Other
+                                 entry points and batch > 1 return
+                                 HS_ERR_INVALID_ARG */
 #define HS_BATCH_EXPERT_UNION 0x2u  /* batch decode only: read each expert's
                                  weights and the union of ALL its tokens' live
                                  rows exactly once (banded up / down kernels)
@@ -183,6 +189,27 @@ int hs_expert_down_sparse(const float* h_dev, const hs_w4* down_nm, int neurons,
 int hs_expert_down_sparse_noalloc(const float* h_dev, const hs_w4* down_nm, int neurons, int out_dim,
                                   uint16_t* y_bf16_dev, float* y_f32_dev, int* live_count_dev,
                                   unsigned flags, hs_stream_t stream);
+
+/* ------------------------------------------------- row-scale re-quantising
+ * Section "The whole decode step": the checkpoint keeps one (scale, bias) per
+ * group of 64 neurons along the output axis, so one live neuron costs its
+ * group's whole slab; re-quantising with the scales along the neuron axis
+ * removes that toll (the page measured a small perplexity cost and did not
+ * ship it; this library offers it as an option, bytes and time only).
+ * For each neuron n and group j of 64 consecutive outputs, min-max affine
+ * 4-bit quantisation of the checkpoint's dequantised weights:
+ *   scale = fp16((max - min) / 15), bias = fp16(min),
+ *   q = clamp(rint((w - bias) / scale), 0, 15)   (q = 0 where scale = 0),
+ * each step in fp32 (w = fma(scale_om, q_om, bias_om)), round to nearest even.
+ *   inputs   as hs_repack_down_nm (checkpoint layout [out_dim][neurons])
+ *   codes_nm [neurons][out_dim/2] neuron-major codes (output 2j low nibble)
+ *   sb_row   [neurons][hs_row_sb_words(out_dim)] u32 (scale, bias) fp16 pairs,
+ *            one per 64 outputs, each row padded with zero words to 16 bytes
+ * A layer whose experts carry these arrays as down_nm is decoded with
+ * HS_DOWN_ROW_SCALES. */
+static inline int hs_row_sb_words(int out_dim) { return ((out_dim / 64) + 3) & ~3; }
+int hs_requant_down_rowscale(const uint8_t* codes_om, const uint16_t* scale_om, const uint16_t* bias_om,
+                             int out_dim, int neurons, uint8_t* codes_nm, void* sb_row, hs_stream_t stream);
 
 /* ------------------------------------------------------------------ router
  * The router projection ahead of the layer (section "Inside a MoE layer": a

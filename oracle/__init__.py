@@ -14,3 +14,4 @@ quoted in the section "The whole decode step" (the byte model here is pinned
 to the page's 5.6 MB and 8.4 GB figures instead).
 """
 from .moe import *  # noqa: F401,F403
+from .requant import *  # noqa: F401,F403

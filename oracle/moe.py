@@ -75,7 +75,11 @@ def unpack_codes(codes) -> np.ndarray:
 def dequant(proj) -> np.ndarray:
     """Dequantised fp64 matrix [rows][cols] of a checkpoint-layout projection.
 
-    w[r, c] = scale[r, c // 64] * q[r, c] + bias[r, c // 64]."""
+    w[r, c] = scale[r, c // 64] * q[r, c] + bias[r, c // 64].  A matrix that
+    is already dense (a numpy array, e.g. a re-quantised down projection
+    dequantised elsewhere) is taken as it is."""
+    if isinstance(proj, np.ndarray):
+        return proj.astype(np.float64)
     q = unpack_codes(proj.codes).astype(np.float64)
     s = np.repeat(as_f64(proj.scale), 64, axis=-1)
     b = np.repeat(as_f64(proj.bias), 64, axis=-1)

@@ -280,6 +280,63 @@ def test_router_projection_hand_values_and_selectors():
                                   oracle.router_logits(xs[0], Wr) + oracle.router_logits(xs[1], Wr))
 
 
+# ------------------------------------------------- row-scale requant ------
+
+def _ckpt(H, N, codes_fn, scale=1.0, bias=-8.0):
+    """A checkpoint-layout projection [H][N] with constant scale and bias."""
+    q = np.fromfunction(codes_fn, (H, N), dtype=np.int64).astype(np.uint8) & 15
+    packed = (q[:, 0::2] | (q[:, 1::2] << 4)).astype(np.uint8)
+    s = np.full((H, N // 64), scale, dtype=np.float16)
+    b = np.full((H, N // 64), bias, dtype=np.float16)
+    return type("P", (), {"codes": packed, "scale": s, "bias": b})()
+
+
+def test_requant_rowscale_hand_group_and_round_trip():
+    """Re-quantisation along the neuron axis ("The whole decode step"):
+    (a) a hand-worked group: neuron 1's 64 outputs take the values
+    1 + 0.5 k (k = 0..15, each four times) -> scale 0.5, bias 1, codes k;
+    (b) integer weights whose every (neuron, 64-output) group spans -8..7
+    come back exactly (scale 1, bias -8, the checkpoint's own codes);
+    (c) a constant group gets scale 0 and codes 0."""
+    H, N = 64, 64
+    # checkpoint scale 0.5, bias 1 on neuron group 0: w = 0.5 q + 1
+    k_of_o = np.arange(64) % 16
+    P = _ckpt(H, N, lambda o, n: np.where(n == 1, k_of_o[o], 3), scale=0.5, bias=1.0)
+    codes, s, b = oracle.requant_down_rowscale(P)
+    assert s.shape == (N, 1) and codes.shape == (N, 32)
+    assert float(s[1, 0]) == 0.5 and float(b[1, 0]) == 1.0
+    q1 = oracle.unpack_codes(codes)[1]
+    assert q1.tolist() == k_of_o.tolist()
+    assert float(s[0, 0]) == 0.0 and float(b[0, 0]) == 2.5 and not oracle.unpack_codes(codes)[0].any()  # w = 2.5
+    # (b) round trip on groups spanning the full 16-value grid
+    H, N = 256, 192
+    rng = np.random.default_rng(31)
+    Q = rng.integers(0, 16, size=(H, N))
+    Q[0::64, :] = 0
+    Q[1::64, :] = 15
+    P = _ckpt(H, N, lambda o, n: Q[o, n])
+    codes, s, b = oracle.requant_down_rowscale(P)
+    assert (s == 1.0).all() and (b == -8.0).all()
+    np.testing.assert_array_equal(oracle.dequant_rowscale(codes, s, b), oracle.dequant(P))
+    np.testing.assert_array_equal(oracle.unpack_codes(codes), Q.T)
+
+
+def test_requant_rowscale_error_within_one_step():
+    """Random checkpoint weights: every re-quantised weight lies within one
+    step (its own group's scale) of the original; scales are positive and
+    follow the range of their own (neuron, 64-output) group."""
+    import synth
+    H, N = 256, 128
+    down = synth.gen_proj(H, N, (3, "requant-pin"))
+    W = oracle.dequant(down)
+    codes, s, b = oracle.requant_down_rowscale(down)
+    Wr = oracle.dequant_rowscale(codes, s, b)
+    step = np.repeat(s.astype(np.float64), 64, axis=-1).T     # [H][N]
+    assert (np.abs(Wr - W) <= step * 0.51 + 1e-3 * step + 2.0 ** -20).all()
+    rng_ = W.T.reshape(N, H // 64, 64)
+    np.testing.assert_allclose(s.astype(np.float64), (rng_.max(2) - rng_.min(2)) / 15, rtol=2e-3)
+
+
 # ------------------------------------------------------------ layer --------
 
 def _tiny_expert(rng, N, H, zero=False):
