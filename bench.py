@@ -68,6 +68,16 @@ def _dist():
     return ws, rank, local
 
 
+def max_over_ranks(value: float, device) -> float:
+    """The largest of every rank's value (all ranks call it; any backend whose
+    tensors live on `device`)."""
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
 def _config(args, extra=None):
     c = {"workload": WORKLOAD if args.p == 0.1 and args.layers == LAYERS else
          f"moe_decode_b1_{args.layers}layers_p{args.p}",
@@ -644,9 +654,7 @@ def main():
             barrier()
             ms = e0.elapsed_time(e1)
             if ws > 1:
-                t = torch.tensor([ms], device=dev)
-                torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-                ms = float(t.item())
+                ms = max_over_ranks(ms, dev)
             runs.append(ms)
         return statistics.median(runs), runs
 

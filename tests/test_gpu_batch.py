@@ -194,3 +194,35 @@ def test_config4_small_path_dense_flag_and_determinism(cfg4_layer):
     assert int(dd["live_rows"].item()) == ntouched * synth.N_ROUTED + synth.N_SHARED
     for b, (ys, yfs) in enumerate(single_token_decodes(dl, X, LG)):
         assert np.array_equal(yf1[b], yfs) and torch.equal(y1[b], ys)
+
+
+@pytest.mark.parametrize("B,flags", [(1, 0), (3, 0), (8, 0), (8, hs.HS_BATCH_EXPERT_UNION)])
+def test_graph_capture_equals_eager(B, flags):
+    """The layer decode captured in a CUDA graph (as a serving loop replays
+    it) gives the eager call's bits, replay after replay, on every path:
+    batch 1, 2..4 tokens, the ticketed units and the expert-union kernels."""
+    H, E, NR, NS, K = 512, 8, 128, 256, 3
+    L = synth.layer_inputs(8, "t-graph", 0, E, NR, NS, H, p=0.2, p_shared=0.3, dead_frac=0.3)
+    dl = make_layer(L, K)
+    X, LG = synth.tokens(8, "t-graph", B, B, H, E)
+    Xc, LGc = X.cuda(), LG.cuda()
+    ws = torch.zeros(dl.workspace_size(B), dtype=torch.uint8, device="cuda")
+    y_e = torch.empty((B, H), dtype=torch.bfloat16, device="cuda")
+    yf_e = torch.empty((B, H), dtype=torch.float32, device="cuda")
+    y_g = torch.empty_like(y_e)
+    yf_g = torch.empty_like(yf_e)
+    s = torch.cuda.Stream()
+    torch.cuda.synchronize()
+    with torch.cuda.stream(s):
+        hs.hs_moe_layer_decode(dl.c, Xc, LGc, B, y_e, yf_e, flags, None, ws, stream=s)
+    s.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        hs.hs_moe_layer_decode(dl.c, Xc, LGc, B, y_g, yf_g, flags, None, ws, stream=s)
+    for _ in range(3):
+        y_g.zero_()
+        yf_g.zero_()
+        g.replay()
+        torch.cuda.synchronize()
+        assert torch.equal(yf_g, yf_e) and torch.equal(y_g, y_e)
+    assert hs.hs_device_status() == hs.HS_OK
