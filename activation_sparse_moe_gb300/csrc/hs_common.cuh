@@ -19,6 +19,7 @@ constexpr int kGroup = 64;           // neurons (or hidden inputs) per scale gro
 constexpr int kMaxHidden = 3072;     // hidden sizes the decode kernels support
 constexpr int kMaxTopK = 8;
 constexpr int kMaxRouted = 128;
+constexpr int kMaxBatchDecode = 64;  // tokens the batch decode kernels take (more: prefill kernels)
 constexpr unsigned long long kWaitLimitCycles = 2000000000ull;  // ~1 s at 2 GHz
 
 // Device error word of this translation unit: set when a bounded wait gives

@@ -687,7 +687,13 @@ extern "C" int hs_expert_down_sparse(const float* h, const hs_w4* down_nm, int n
 
 // ---------------------------------------------------------- layer decode
 extern "C" size_t hs_moe_layer_decode_workspace_size(const hs_moe_layer* L, int batch) {
-    if (batch > 1) return hs_batch_decode_workspace_size(L, batch);
+    if (batch > 1) {
+        // the larger of the two batch paths' needs (the flags choose between them per call)
+        const size_t a = batch <= hs::kMaxBatchDecode ? hs_batch_decode_workspace_size(L, batch) : 0;
+        const size_t b = batch >= kPrefillMinBatch && hs_prefill_layer_ok(L, batch) == HS_OK
+                             ? hs_moe_prefill_workspace_size(L, batch) : 0;
+        return std::max(a, b);
+    }
     if (check_layer(L) != HS_OK || batch != 1) return 0;
     const size_t U = decode_units(L);
     return round_up(U * L->hidden * sizeof(float), 256) + round_up(U * sizeof(int), 256);
@@ -704,8 +710,18 @@ extern "C" int hs_moe_layer_decode(const hs_moe_layer* L, const uint16_t* x, con
     if (dbg && ((dbg->topk_idx == nullptr) != (dbg->topk_w == nullptr))) return HS_ERR_INVALID_ARG;
     if (batch > 1) {
         if (flags & HS_DOWN_ROW_SCALES) return HS_ERR_INVALID_ARG;  // batch 1 only
-        return hs_batch_decode(L, x, logits, batch, y_bf16, y_f32, flags, dbg, ws, ws_bytes,
-                               reinterpret_cast<cudaStream_t>(stream));
+        cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+        if (batch >= kPrefillMinBatch && !(flags & HS_BATCH_EXPERT_UNION) && hs_prefill_layer_ok(L, batch) == HS_OK) {
+            // many tokens per expert: the prefill's tensor-core products
+            if (dbg && dbg->h) return HS_ERR_INVALID_ARG;  // the h dump covers batch 1 only
+            const hs_prefill_debug pd{dbg ? dbg->topk_idx : nullptr, dbg ? dbg->topk_w : nullptr, nullptr, nullptr};
+            const int st = hs_moe_prefill(L, x, logits, batch, y_bf16, y_f32, flags & HS_FORCE_DENSE,
+                                          dbg ? &pd : nullptr, ws, ws_bytes, stream);
+            if (st != HS_OK || !dbg) return st;
+            return hs_prefill_union_live(L, batch, ws, dbg->live_rows, dbg->live_groups, s);
+        }
+        if (batch > hs::kMaxBatchDecode) return HS_ERR_UNSUPPORTED_SHAPE;
+        return hs_batch_decode(L, x, logits, batch, y_bf16, y_f32, flags, dbg, ws, ws_bytes, s);
     }
     const size_t need = hs_moe_layer_decode_workspace_size(L, batch);
     if (!ws || ws_bytes < need) return HS_ERR_WORKSPACE;

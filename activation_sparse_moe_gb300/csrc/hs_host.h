@@ -133,3 +133,14 @@ int hs_batch_decode(const hs_moe_layer* L, const uint16_t* x, const float* logit
 unsigned hs_batch_take_status();
 // Reads and clears the prefill translation unit's device error word.
 unsigned hs_prefill_take_status();
+// Batch decode of this many tokens or more runs on the prefill kernels (tensor
+// cores: each weight tile is dequantised once for all of an expert's tokens),
+// where the layer allows it; below, the batch decode kernels are faster.
+constexpr int kPrefillMinBatch = 41;
+// HS_OK if hs_moe_prefill takes this layer and token count.
+int hs_prefill_layer_ok(const hs_moe_layer* L, int tokens);
+// After an hs_moe_prefill call on workspace ws (stream-ordered): the union
+// over each expert's tokens of its live neurons (h > 0), summed over the
+// experts, and the 64-neuron groups holding one.  Either output may be null.
+int hs_prefill_union_live(const hs_moe_layer* L, int tokens, void* ws, int* live_rows, int* live_groups,
+                          cudaStream_t stream);

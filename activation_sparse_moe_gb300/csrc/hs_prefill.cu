@@ -950,6 +950,44 @@ __global__ void __launch_bounds__(256) prefill_combine_kernel(const __grid_const
     }
 }
 
+// Debug counts after a prefill: CTA e < E walks expert e's pair rows of h_r
+// (rows off[e] .. off[e+1]), CTA E the shared expert's T rows of h_s; thread
+// n ORs neuron n's h > 0 over the rows (fp16 bits; h >= 0).  h is stored
+// permuted within blocks of 8 neurons only, so 64-neuron groups keep their
+// members.  The totals are added into *live_rows and *live_groups.
+__global__ void __launch_bounds__(256) prefill_union_live_kernel(const PrefillMeta* __restrict__ meta,
+                                                                 const uint16_t* __restrict__ h_r,
+                                                                 const uint16_t* __restrict__ h_s, int T, int E,
+                                                                 int NR, int NS, int* live_rows, int* live_groups) {
+    __shared__ int grp[kMaxKTiles];
+    __shared__ int rows_cnt;
+    const int e = blockIdx.x, t = threadIdx.x;
+    const bool shared = e == E;
+    const int N = shared ? NS : NR;
+    const int r0 = shared ? 0 : meta->off[e], r1 = shared ? T : meta->off[e + 1];
+    const uint16_t* h = shared ? h_s : h_r;
+    for (int g = t; g < N / 64; g += blockDim.x) grp[g] = 0;
+    if (t == 0) rows_cnt = 0;
+    __syncthreads();
+    int cnt = 0;
+    for (int n = t; n < N; n += blockDim.x) {
+        bool live = false;
+        for (int r = r0; r < r1 && !live; ++r) live = (h[(size_t)r * N + n] & 0x7fffu) != 0u;
+        if (live) {
+            ++cnt;
+            grp[n >> 6] = 1;
+        }
+    }
+    atomicAdd(&rows_cnt, cnt);
+    __syncthreads();
+    if (t == 0) {
+        int ng = 0;
+        for (int g = 0; g < N / 64; ++g) ng += grp[g];
+        if (live_rows) atomicAdd(live_rows, rows_cnt);
+        if (live_groups) atomicAdd(live_groups, ng);
+    }
+}
+
 }  // namespace hs
 
 // ===================================================================== host
@@ -1037,6 +1075,25 @@ int prefill_shape_ok(const hs_moe_layer* L, int T) {
     return HS_OK;
 }
 }  // namespace
+
+int hs_prefill_layer_ok(const hs_moe_layer* L, int tokens) {
+    const int st = check_layer(L);
+    return st != HS_OK ? st : prefill_shape_ok(L, tokens);
+}
+
+int hs_prefill_union_live(const hs_moe_layer* L, int tokens, void* ws, int* live_rows, int* live_groups,
+                          cudaStream_t s) {
+    if (!live_rows && !live_groups) return HS_OK;
+    const PrefillLayout l = prefill_layout(L, tokens);
+    char* w = static_cast<char*>(ws);
+    if (live_rows && cudaMemsetAsync(live_rows, 0, sizeof(int), s) != cudaSuccess) return HS_ERR_CUDA;
+    if (live_groups && cudaMemsetAsync(live_groups, 0, sizeof(int), s) != cudaSuccess) return HS_ERR_CUDA;
+    const int E = L->n_routed, NS = L->shared ? L->shared->neurons : 0;
+    hs::prefill_union_live_kernel<<<E + (NS ? 1 : 0), 256, 0, s>>>(
+        reinterpret_cast<const hs::PrefillMeta*>(w + l.meta), reinterpret_cast<const uint16_t*>(w + l.h_r),
+        reinterpret_cast<const uint16_t*>(w + l.h_s), tokens, E, L->routed[0].neurons, NS, live_rows, live_groups);
+    return launch_err();
+}
 
 extern "C" size_t hs_moe_prefill_workspace_size(const hs_moe_layer* L, int tokens) {
     if (check_layer(L) != HS_OK || prefill_shape_ok(L, tokens) != HS_OK) return 0;

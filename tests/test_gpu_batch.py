@@ -11,7 +11,7 @@ import torch
 
 import oracle
 import synth
-from _util import check_bf16_within_one_ulp, check_close
+from _util import check_bf16_rounding, check_bf16_within_one_ulp, check_close
 from activation_sparse_moe_gb300 import hs
 from activation_sparse_moe_gb300.layer import DeviceLayer, from_synth_expert, from_synth_stack
 
@@ -61,22 +61,36 @@ def union_rows(ref, L):
     return n, ng
 
 
+PREFILL_MIN_BATCH = 41  # from here on the decode runs on the prefill's tensor-core kernels
+
+
+def on_prefill_kernels(B, flags=0):
+    return B >= PREFILL_MIN_BATCH and not (flags & hs.HS_BATCH_EXPERT_UNION)
+
+
 def check_batch(L, dl, X, LG, K, what, flips_allowed=4, flags=0):
     y, yf, dbg = run_batch(dl, X, LG, flags=flags)
     ref = oracle.moe_tokens(X, LG, L.routed_expert, L.shared, k=K)
     assert np.array_equal(dbg["topk_idx"].numpy(), ref["idx"]), what
     np.testing.assert_allclose(dbg["topk_w"].double().numpy(), ref["w"], rtol=2e-6, atol=1e-7)
     check_close(yf, ref["out"], f"{what} y_f32")
-    for b in range(X.shape[0]):
-        check_bf16_within_one_ulp(y[b], ref["out"][b], f"{what} token {b}", yf[b])
-    # rows read = union live rows (neurons within fp32 error of 0 may flip)
     n, ng = union_rows(ref, L)
-    assert abs(int(dbg["live_rows"].item()) - n) <= flips_allowed
-    assert abs(int(dbg["live_groups"].item()) - ng) <= flips_allowed
+    if on_prefill_kernels(X.shape[0], flags):
+        # fp16 operands: the prefill's output contract, and neurons within
+        # fp16 rounding of 0 (or whose fp16 h underflows) may flip
+        check_bf16_rounding(y, yf, ref["out"], what)
+        slack = flips_allowed + n // 100
+    else:
+        for b in range(X.shape[0]):
+            check_bf16_within_one_ulp(y[b], ref["out"][b], f"{what} token {b}", yf[b])
+        slack = flips_allowed  # neurons within fp32 error of 0 may flip
+    # rows read = union live rows
+    assert abs(int(dbg["live_rows"].item()) - n) <= slack, (what, int(dbg["live_rows"].item()), n)
+    assert abs(int(dbg["live_groups"].item()) - ng) <= slack, (what, int(dbg["live_groups"].item()), ng)
     return y, yf, dbg
 
 
-@pytest.mark.parametrize("B", [2, 5, 8])
+@pytest.mark.parametrize("B", [2, 5, 8, 41, 96, 200])
 def test_small_batch(B):
     H, E, NR, NS, K = 512, 8, 128, 256, 3
     L = synth.layer_inputs(0, "t-batch", 0, E, NR, NS, H, p=0.2, p_shared=0.3)
@@ -157,8 +171,12 @@ def test_config4_parity_expert_union_path(cfg4_layer, B):
     y1, yf1, d1 = check_batch(L, dl, X, LG, 6, f"config 4 B={B} expert union", flips_allowed=8,
                               flags=hs.HS_BATCH_EXPERT_UNION)
     y2, yf2, d2 = run_batch(dl, X, LG)
-    assert int(d1["live_rows"].item()) == int(d2["live_rows"].item())
-    assert int(d1["live_groups"].item()) == int(d2["live_groups"].item())
+    r1, r2 = int(d1["live_rows"].item()), int(d2["live_rows"].item())
+    g1, g2 = int(d1["live_groups"].item()), int(d2["live_groups"].item())
+    if on_prefill_kernels(B):  # the default path's fp16 products: near-zero neurons may flip
+        assert abs(r1 - r2) <= 8 + r1 // 100 and abs(g1 - g2) <= 8
+    else:                      # the same integer up products: the same live sets
+        assert r1 == r2 and g1 == g2
 
 
 def test_config4_dense_flag_and_determinism(cfg4_layer):
@@ -226,3 +244,15 @@ def test_graph_capture_equals_eager(B, flags):
         torch.cuda.synchronize()
         assert torch.equal(yf_g, yf_e) and torch.equal(y_g, y_e)
     assert hs.hs_device_status() == hs.HS_OK
+
+
+def test_config4_batch64_on_prefill_kernels_dense_flag_and_determinism(cfg4_layer):
+    """B = 64 runs on the prefill's tensor-core kernels: repeatable, and the
+    dense flag (no 64-neuron tile skipped) gives the same bits."""
+    L, dl = cfg4_layer
+    X, LG = synth.tokens(0, "cfg4", 64, 64)
+    y1, yf1, d1 = run_batch(dl, X, LG)
+    y2, yf2, _ = run_batch(dl, X, LG)
+    yd, yfd, _ = run_batch(dl, X, LG, flags=hs.HS_FORCE_DENSE)
+    assert np.array_equal(yf1, yf2) and torch.equal(y1, y2)
+    assert np.array_equal(yf1, yfd) and torch.equal(y1, yd)
