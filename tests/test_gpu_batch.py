@@ -214,11 +214,12 @@ def test_config4_small_path_dense_flag_and_determinism(cfg4_layer):
         assert np.array_equal(yf1[b], yfs) and torch.equal(y1[b], ys)
 
 
-@pytest.mark.parametrize("B,flags", [(1, 0), (3, 0), (8, 0), (8, hs.HS_BATCH_EXPERT_UNION)])
+@pytest.mark.parametrize("B,flags", [(1, 0), (3, 0), (8, 0), (8, hs.HS_BATCH_EXPERT_UNION), (48, 0)])
 def test_graph_capture_equals_eager(B, flags):
     """The layer decode captured in a CUDA graph (as a serving loop replays
     it) gives the eager call's bits, replay after replay, on every path:
-    batch 1, 2..4 tokens, the ticketed units and the expert-union kernels."""
+    batch 1, 2..4 tokens, the ticketed units, the expert-union kernels and
+    (48 tokens) the prefill's tensor-core kernels."""
     H, E, NR, NS, K = 512, 8, 128, 256, 3
     L = synth.layer_inputs(8, "t-graph", 0, E, NR, NS, H, p=0.2, p_shared=0.3, dead_frac=0.3)
     dl = make_layer(L, K)
