@@ -911,16 +911,21 @@ __device__ __forceinline__ void fused_issue_up(const FusedBufs& sm, const Expert
 // A thread's part of a unit's up GEMV for T <= kFTok tokens: token lane tk
 // (the TL lanes of one scale group are adjacent in a warp), group gc, row
 // lane rs of RS.
+// With pair (3 or 4 tokens) each lane takes two tokens, tk and tk + 2, at the
+// same rows: the code masks are shared and every thread has rows to walk.
+// Worth it where x comes ready-made (the ticketed kernel: 8.7% at 32 tokens);
+// the small-batch kernel, which converts x per thread, keeps one token per lane.
 struct FusedRole {
-    int tk, gc, rs, RS;
-    bool active;  // owns (token, group) work
+    int tk, tk2, gc, rs, RS;  // tk2: the lane's second token, or -1
+    bool active;              // owns (token, group) work
 };
-__device__ __forceinline__ FusedRole fused_role(int T, int G) {
+__device__ __forceinline__ FusedRole fused_role(int T, int G, bool pair) {
     const int t = threadIdx.x;
-    const int TL = T == 1 ? 1 : (T == 2 ? 2 : 4);
+    const int TL = T == 1 ? 1 : (T == 2 || pair ? 2 : 4);
     FusedRole r;
     r.RS = 256 / (TL * G);
     r.tk = t % TL;
+    r.tk2 = pair && T >= 3 && r.tk + 2 < T ? r.tk + 2 : -1;
     r.gc = (t / TL) % G;
     r.rs = t / (TL * G);
     r.active = r.rs < r.RS && r.tk < T;
@@ -928,20 +933,22 @@ __device__ __forceinline__ FusedRole fused_role(int T, int G) {
 }
 
 // One unit after its up copies were issued (phase `par` of bars[0..3]), with
-// each active thread's x fixed-point copy in xf: the DP4A GEMV per token,
-// ReLU^2, the union-live rows' down codes and the slab, the down products
-// into the tokens' partial rows.  Returns false (on every thread) if a
-// bounded wait gave up; `live` gets the unit's union live rows.
+// each active thread's x fixed-point copies in xf (token tk) and, with kPair,
+// xf2 (token tk2): the DP4A GEMV per token, ReLU^2, the union-live rows' down
+// codes and the slab, the down products into the tokens' partial rows.
+// Returns false (on every thread) if a bounded wait gave up; `live` gets the
+// unit's union live rows.
+template <bool kPair>
 __device__ __forceinline__ bool fused_unit(const LayerParams& P, const BatchIO& io, const FusedBufs& sm,
                                            const ExpertPtrs& ep, int g, int T, const UnitTokens& ut, const XFixed& xf,
-                                           uint32_t par, uint32_t& dn_par, uint64_t& live) {
+                                           const XFixed& xf2, uint32_t par, uint32_t& dn_par, uint64_t& live) {
     const int H = P.hidden, G = H / 64, rowb = H / 2;
     const int t = threadIdx.x, lane = t & 31;
     const bool dense = (io.flags & HS_FORCE_DENSE) != 0;
     const uint64_t pol = policy_evict_first();
     uint8_t* codes = sm.codes;
-    const FusedRole role = fused_role(T, G);
-    const int tk = role.tk, gc = role.gc, rs = role.rs, RS = role.RS;
+    const FusedRole role = fused_role(T, G, kPair);
+    const int tk = role.tk, tk2 = role.tk2, gc = role.gc, rs = role.rs, RS = role.RS;
     const bool active = role.active;
     float off_r = 0.f;
     if (t < 64 && ep.up_off) off_r = __ldg(ep.up_off + 64 * g + t);
@@ -969,13 +976,21 @@ __device__ __forceinline__ bool fused_unit(const LayerParams& P, const BatchIO& 
         }
         const int da = group_dot_fixed16(a0, a1, xf);
         const int db = group_dot_fixed16(b0, b1, xf);
+        int da2 = 0, db2 = 0;
+        if (kPair && tk2 >= 0) {
+            da2 = group_dot_fixed16(a0, a1, xf2);
+            db2 = group_dot_fixed16(b0, b1, xf2);
+        }
         __syncwarp();  // the token lanes of a group have read its codes before parts land there
         if (act && ok && active) {
             const float2 sa = half2_to_float2(sw0);
             *up_part(codes, rowb, r, gc, tk) = fmaf(sa.x * xf.inv, (float)da, sa.y * xf.xsum);
+            if (kPair && tk2 >= 0) *up_part(codes, rowb, r, gc, tk2) = fmaf(sa.x * xf2.inv, (float)da2, sa.y * xf2.xsum);
             if (two) {
                 const float2 sbv = half2_to_float2(sw1);
                 *up_part(codes, rowb, r2, gc, tk) = fmaf(sbv.x * xf.inv, (float)db, sbv.y * xf.xsum);
+                if (kPair && tk2 >= 0)
+                    *up_part(codes, rowb, r2, gc, tk2) = fmaf(sbv.x * xf2.inv, (float)db2, sbv.y * xf2.xsum);
             }
         }
     }
@@ -1133,14 +1148,18 @@ __global__ void __launch_bounds__(256, 2) batch_fused_kernel(const __grid_consta
         // x from the route kernel's fixed-point tables (here, unlike the
         // small-batch kernel, staging x ahead of the weights measured slower:
         // it serialises each unit's copies behind an extra wait)
-        const FusedRole role = fused_role(T, G);
-        XFixed xf = {};
+        const FusedRole role = fused_role(T, G, true);
+        XFixed xf = {}, xf2 = {};
         if (role.active) {
             const int tok = pick(ut.tok, role.tk);
             load_x_fixed(io.xt + (size_t)tok * G * kXfStride, io.xsc + (size_t)tok * G * 2, role.gc, xf);
+            if (role.tk2 >= 0) {
+                const int tok2 = pick(ut.tok, role.tk2);
+                load_x_fixed(io.xt + (size_t)tok2 * G * kXfStride, io.xsc + (size_t)tok2 * G * 2, role.gc, xf2);
+            }
         }
         uint64_t live = 0;
-        if (!fused_unit(P, io, sm, ep, g, T, ut, xf, it & 1, dn_par, live)) return;
+        if (!fused_unit<true>(P, io, sm, ep, g, T, ut, xf, xf2, it & 1, dn_par, live)) return;
         if (t < 2 && live) {  // the expert's union over all its tokens (for the live-row counts)
             const uint32_t bits = (uint32_t)(live >> (32 * t));
             uint32_t* mw = shared ? io.mask_s + 2 * g + t : io.mask_r + (size_t)e * (P.routed_neurons / 32) + 2 * g + t;
@@ -1265,7 +1284,7 @@ __global__ void __launch_bounds__(256, 2) batch_small_kernel(const __grid_consta
     }
     if (!shared && t == 0) fused_issue_up(sm, ep, g, H, policy_evict_first(), 0, 3);
     // each active thread's x group from shared memory, then the last chunk into that space
-    const FusedRole role = fused_role(T, H / 64);
+    const FusedRole role = fused_role(T, H / 64, false);
     const bool xok = mbar_wait(xbar, 0);
     XFixed xf = {};
     if (role.active && xok) {
@@ -1278,7 +1297,7 @@ __global__ void __launch_bounds__(256, 2) batch_small_kernel(const __grid_consta
     if (t == 0) fused_issue_up(sm, ep, g, H, policy_evict_first(), 3, 4);
     uint32_t dn_par = 0;
     uint64_t live = 0;
-    if (!fused_unit(P, io, sm, ep, g, T, ut, xf, 0, dn_par, live)) return;
+    if (!fused_unit<false>(P, io, sm, ep, g, T, ut, xf, xf, 0, dn_par, live)) return;
     if (t == 0) io.unit_live[u] = __popcll(live);
 }
 

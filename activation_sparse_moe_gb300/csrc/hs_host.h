@@ -136,7 +136,7 @@ unsigned hs_prefill_take_status();
 // Batch decode of this many tokens or more runs on the prefill kernels (tensor
 // cores: each weight tile is dequantised once for all of an expert's tokens),
 // where the layer allows it; below, the batch decode kernels are faster.
-constexpr int kPrefillMinBatch = 41;
+constexpr int kPrefillMinBatch = 51;
 // HS_OK if hs_moe_prefill takes this layer and token count.
 int hs_prefill_layer_ok(const hs_moe_layer* L, int tokens);
 // After an hs_moe_prefill call on workspace ws (stream-ordered): the union

@@ -236,11 +236,11 @@ int hs_router_logits(const uint16_t* x_bf16_dev, const uint16_t* w_router_bf16_d
  *   y_bf16_dev       [batch][hidden] bf16, required;  y_f32_dev fp32 or NULL
  *   debug            host pointer to device debug outputs, or NULL
  * batch 1..4096.  For batch > 1 the tokens are grouped by expert (section
- * "Sorted by expert").  2..40 tokens (or up to 64 where the next case does
+ * "Sorted by expert").  2..50 tokens (or up to 64 where the next case does
  * not apply): each unit of work (expert, 64-neuron group, up to 4 of the
  * expert's tokens) reads its weights and the union of its tokens' live rows
  * once, on CUDA cores; with HS_BATCH_EXPERT_UNION each expert reads the union
- * of all its tokens' live rows once.  41 tokens or more, without that flag,
+ * of all its tokens' live rows once.  51 tokens or more, without that flag,
  * when the routed experts are stacked as hs_moe_prefill requires: the
  * prefill's tensor-core products (fp16 operands; its output contract), which
  * dequantise each weight tile once for all of an expert's tokens.  hidden

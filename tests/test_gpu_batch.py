@@ -61,7 +61,7 @@ def union_rows(ref, L):
     return n, ng
 
 
-PREFILL_MIN_BATCH = 41  # from here on the decode runs on the prefill's tensor-core kernels
+PREFILL_MIN_BATCH = 51  # from here on the decode runs on the prefill's tensor-core kernels
 
 
 def on_prefill_kernels(B, flags=0):
@@ -90,7 +90,7 @@ def check_batch(L, dl, X, LG, K, what, flips_allowed=4, flags=0):
     return y, yf, dbg
 
 
-@pytest.mark.parametrize("B", [2, 5, 8, 41, 96, 200])
+@pytest.mark.parametrize("B", [2, 5, 8, 50, 51, 96, 200])
 def test_small_batch(B):
     H, E, NR, NS, K = 512, 8, 128, 256, 3
     L = synth.layer_inputs(0, "t-batch", 0, E, NR, NS, H, p=0.2, p_shared=0.3)
@@ -214,12 +214,12 @@ def test_config4_small_path_dense_flag_and_determinism(cfg4_layer):
         assert np.array_equal(yf1[b], yfs) and torch.equal(y1[b], ys)
 
 
-@pytest.mark.parametrize("B,flags", [(1, 0), (3, 0), (8, 0), (8, hs.HS_BATCH_EXPERT_UNION), (48, 0)])
+@pytest.mark.parametrize("B,flags", [(1, 0), (3, 0), (8, 0), (8, hs.HS_BATCH_EXPERT_UNION), (56, 0)])
 def test_graph_capture_equals_eager(B, flags):
     """The layer decode captured in a CUDA graph (as a serving loop replays
     it) gives the eager call's bits, replay after replay, on every path:
     batch 1, 2..4 tokens, the ticketed units, the expert-union kernels and
-    (48 tokens) the prefill's tensor-core kernels."""
+    (56 tokens) the prefill's tensor-core kernels."""
     H, E, NR, NS, K = 512, 8, 128, 256, 3
     L = synth.layer_inputs(8, "t-graph", 0, E, NR, NS, H, p=0.2, p_shared=0.3, dead_frac=0.3)
     dl = make_layer(L, K)
