@@ -97,7 +97,8 @@ struct BatchIO {
     float* dbg_topk_w;
     int* live_total;
     int* live_groups;
-    int* unit_live;         // small-batch path: union live rows per unit (else null)
+    uint64_t* unit_live;    // small-batch path: live mask per unit (else null)
+    int* unit_key;          // small-batch path: the unit's expert (n_routed = shared, -1 = none)
     int n_units;
 };
 
@@ -776,8 +777,10 @@ struct FusedSmem {
     __host__ __device__ static int codes(int H) { return 64 * (H / 2); }
     __host__ __device__ static int sb(int H) { return H * 4; }  // up scales of 64 rows, then the down slab
     __host__ __device__ static int misc(int H) { return codes(H) + sb(H); }
-    __host__ __device__ static int total(int H) { return misc(H) + kTables + (int)sizeof(FusedTables); }
+    static constexpr int kTablesBytes = 1664;  // the ticketed kernel's FusedTables or the small kernel's tables
+    __host__ __device__ static int total(int H) { return misc(H) + kTables + kTablesBytes; }
 };
+static_assert(sizeof(FusedTables) <= FusedSmem::kTablesBytes, "fused tables exceed their region");
 
 // Partial row of (token b, row ri) in the fused layout [B][H/32][Ut][32].
 struct FusedOut {
@@ -1168,28 +1171,38 @@ __global__ void __launch_bounds__(256, 2) batch_fused_kernel(const __grid_consta
     }
 }
 
-// ------------------------------------------------------------------ small batch (B <= kFTok)
-// Every expert of the batch has all its tokens in one unit, so the units can
-// be numbered before routing: CTA u < NGs is the shared expert's group u with
-// every token; CTA NGs + j * NGr + g is group g of the j-th distinct routed
-// expert of the batch (ascending id) with its tokens, and exits if the batch
-// has fewer distinct experts.  Each routed CTA routes the B tokens itself (one
-// warp per token), so there is no route kernel, plan, ticket or zeroed meta
-// block.  x of the B tokens (2BH <= 8H bytes) is bulk-copied once into the
-// space of the last 16-row weight chunk, right after the wait for the
-// previous kernel and before any routed weights are requested (x read by
-// every thread from L2 instead waited behind the weight stream); each thread
-// converts its group from there, and the last chunk is fetched after.  The
-// shared expert's CTAs issue their other weight copies before waiting for the
-// previous kernel, as in the batch-1 kernel.
+// ------------------------------------------------------------------ small batch (B <= kSmallMaxBatch)
+// With at most 8 tokens the units can be numbered before routing.  A unit
+// holds at most kFTok of an expert's tokens: CTA u < NSu = NGs * ceil(B / 4)
+// is the shared expert's group u % NGs with token group u / NGs; CTA
+// NSu + j * NGr + g is group g of the j-th (routed expert, token group) entry
+// of the batch, experts ascending, each expert's tokens in order (an expert
+// with c tokens has ceil(c / 4) entries), and exits if the batch has fewer
+// entries.  Each routed CTA routes the B tokens itself (one warp per token)
+// and finds its entry from per-expert pair counts, so there is no route
+// kernel, plan, ticket or zeroed meta block.  x of the B tokens (2BH bytes,
+// at most 16H) is bulk-copied once into the space of the last one or two
+// 16-row weight chunks right after the wait for the previous kernel and
+// before any routed weights are requested (x read by every thread from L2
+// instead waited behind the weight stream); each thread converts its group
+// from there, and those chunks are fetched after.  The shared expert's CTAs
+// issue their other weight copies before waiting for the previous kernel, as
+// in the batch-1 kernel.  Each unit leaves its live mask and expert for the
+// live-row counts (the union over an expert's units).
+constexpr int kSmallMaxBatch = 8;
+
 struct SmallTables {
-    int topi[kFTok][kMaxTopK];
-    float topw[kFTok][kMaxTopK];
+    int topi[kSmallMaxBatch][kMaxTopK];
+    float topw[kSmallMaxBatch][kMaxTopK];
+    int cnt[kMaxRouted];       // pairs per routed expert
+    int off[kMaxRouted + 1];   // first entry of each expert
     int tok[kFTok], slot[kFTok];
     float w[kFTok];
     int T, e;
 };
-static_assert(sizeof(SmallTables) <= sizeof(FusedTables), "small-batch tables exceed the tables region");
+static_assert(sizeof(SmallTables) <= FusedSmem::kTablesBytes, "small-batch tables exceed their region");
+
+__host__ __device__ inline int small_shared_units(int NGs, int B) { return NGs * ((B + kFTok - 1) / kFTok); }
 
 __global__ void __launch_bounds__(256, 2) batch_small_kernel(const __grid_constant__ LayerParams P, const BatchIO io) {
     extern __shared__ __align__(128) uint8_t smem[];
@@ -1199,20 +1212,23 @@ __global__ void __launch_bounds__(256, 2) batch_small_kernel(const __grid_consta
     const int t = threadIdx.x, lane = t & 31, warp = t >> 5, u = blockIdx.x;
     const int B = io.batch, K = P.top_k, E = P.n_routed;
     const int NGs = P.shared_neurons / 64, NGr = P.routed_neurons / 64;
-    const bool shared = u < NGs;
+    const int NSu = small_shared_units(NGs, B);
+    const bool shared = u < NSu;
     uint64_t* xbar = &sm.bars[5];
-    const uint16_t* x_s = reinterpret_cast<const uint16_t*>(sm.codes + 3 * 8 * H);  // chunk 3's space
+    const int nx = (B + kFTok - 1) / kFTok;  // chunks whose space holds x (1 or 2)
+    uint8_t* x_dst = sm.codes + (4 - nx) * 8 * H;
+    const uint16_t* x_s = reinterpret_cast<const uint16_t*>(x_dst);
     if (t == 0) {
         for (int i = 0; i < 6; ++i) mbar_init(&sm.bars[i], 1);
         fence_mbar_init();
-        if (shared) fused_issue_up(sm, P.shared, u, H, policy_evict_first(), 0, 3);  // weights only
+        if (shared) fused_issue_up(sm, P.shared, u % NGs, H, policy_evict_first(), 0, 4 - nx);  // weights only
     }
     __syncthreads();
     pdl_wait();
     pdl_trigger();
     if (t == 0) {
         mbar_arrive_expect_tx(xbar, (uint32_t)(2 * B * H));
-        bulk_g2s(sm.codes + 3 * 8 * H, io.x, (uint32_t)(2 * B * H), xbar, policy_evict_last());
+        bulk_g2s(x_dst, io.x, (uint32_t)(2 * B * H), xbar, policy_evict_last());
     }
     if (!shared || (u == 0 && io.dbg_topk_idx)) {
         if (warp < B) warp_topk_softmax(io.logits + (size_t)warp * E, E, K, st->topi[warp], st->topw[warp]);
@@ -1226,50 +1242,103 @@ __global__ void __launch_bounds__(256, 2) batch_small_kernel(const __grid_consta
     ExpertPtrs ep;
     int g, T;
     if (shared) {
-        g = u;
-        T = B;
+        const int c = u / NGs;
+        g = u % NGs;
+        T = min(kFTok, B - kFTok * c);
         ep = P.shared;
 #pragma unroll
-        for (int k = 0; k < kFTok; ++k) { ut.tok[k] = k < B ? k : 0; ut.ri[k] = g; ut.w[k] = 1.f; }
+        for (int k = 0; k < kFTok; ++k) { ut.tok[k] = kFTok * c + (k < T ? k : 0); ut.ri[k] = g; ut.w[k] = 1.f; }
     } else {
-        const int j = (u - NGs) / NGr;
-        g = (u - NGs) % NGr;
-        if (warp == 0) {
-            // the batch's distinct experts as a 128-bit set; this CTA's is its j-th member
-            const int ei = lane < B * K ? st->topi[lane / K][lane % K] : -1;
-            int e = -1, before = 0;
+        const int j = (u - NSu) / NGr;
+        g = (u - NSu) % NGr;
+        if (B <= kFTok) {
+            // one entry per distinct expert: the j-th member of the batch's 128-bit expert set
+            if (warp == 0) {
+                const int ei = lane < B * K ? st->topi[lane / K][lane % K] : -1;
+                int e = -1, before = 0;
 #pragma unroll
-            for (int w = 0; w < kMaxRouted / 32; ++w) {
-                uint32_t m = __reduce_or_sync(0xffffffffu, (ei >= 0 && (ei >> 5) == w) ? 1u << (ei & 31) : 0u);
-                const int c = __popc(m);
-                if (e < 0 && j < before + c) {
-                    for (int i = 0; i < j - before; ++i) m &= m - 1;
-                    e = 32 * w + __ffs(m) - 1;
+                for (int w = 0; w < kMaxRouted / 32; ++w) {
+                    uint32_t m = __reduce_or_sync(0xffffffffu, (ei >= 0 && (ei >> 5) == w) ? 1u << (ei & 31) : 0u);
+                    const int c = __popc(m);
+                    if (e < 0 && j < before + c) {
+                        for (int i = 0; i < j - before; ++i) m &= m - 1;
+                        e = 32 * w + __ffs(m) - 1;
+                    }
+                    before += c;
                 }
-                before += c;
+                if (lane == 0) {
+                    st->off[0] = 0;  // the entry is the expert's first (token group 0)
+                    st->e = e;
+                }
             }
-            // its tokens in ascending order, with their slots and weights
+        } else {
+        // pairs per expert, then each expert's first entry (ceil(pairs / kFTok) entries each)
+        for (int e = t; e < E; e += blockDim.x) st->cnt[e] = 0;
+        __syncthreads();
+        if (t < B * K) atomicAdd(&st->cnt[st->topi[t / K][t % K]], 1);
+        __syncthreads();
+        if (warp == 0) {
+            int n[kMaxRouted / 32], sum = 0;
+#pragma unroll
+            for (int i = 0; i < kMaxRouted / 32; ++i) {
+                const int e = (kMaxRouted / 32) * lane + i;
+                n[i] = e < E ? (st->cnt[e] + kFTok - 1) / kFTok : 0;
+                sum += n[i];
+            }
+            int incl = sum;
+#pragma unroll
+            for (int off = 1; off < 32; off <<= 1) {
+                const int o = __shfl_up_sync(0xffffffffu, incl, off);
+                if (lane >= off) incl += o;
+            }
+            int run = incl - sum;
+#pragma unroll
+            for (int i = 0; i < kMaxRouted / 32; ++i) {
+                const int e = (kMaxRouted / 32) * lane + i;
+                if (e < E) st->off[e] = run;
+                run += n[i];
+            }
+            if (lane == 31) st->off[E] = incl;
+        }
+        __syncthreads();
+        if (warp == 0) {
+            // this CTA's entry: the expert whose entries cover j, and its token group
+            int e = -1;
+#pragma unroll
+            for (int i = 0; i < kMaxRouted / 32; ++i) {
+                const int ee = (kMaxRouted / 32) * lane + i;
+                if (ee < E && st->off[ee] <= j && j < st->off[ee + 1]) e = ee;
+            }
+            e = __reduce_max_sync(0xffffffffu, e);
+            if (lane == 0) {
+                st->e = e;
+                st->off[0] = e >= 0 ? j - st->off[e] : 0;  // the token group within the expert
+            }
+        }
+        }
+        __syncwarp();
+        if (warp == 0) {
+            // the expert's tokens in ascending order; the entry's group of up to kFTok of them
+            const int e = st->e, h = st->off[0];
             int slot = -1;
             if (e >= 0 && lane < B)
-                for (int s = 0; s < K; ++s)
-                    if (st->topi[lane][s] == e) slot = s;
-            const unsigned has = __ballot_sync(0xffffffffu, slot >= 0);
-            if (slot >= 0) {
-                const int k = __popc(has & ((1u << lane) - 1u));
+                for (int s2 = 0; s2 < K; ++s2)
+                    if (st->topi[lane][s2] == e) slot = s2;
+            const unsigned has = __ballot_sync(0xffffffffu, slot >= 0);  // the expert's tokens, ascending
+            const int k = __popc(has & ((1u << lane) - 1u)) - kFTok * h;
+            if (slot >= 0 && k >= 0 && k < kFTok) {
                 st->tok[k] = lane;
                 st->slot[k] = slot;
                 st->w[k] = st->topw[lane][slot];
             }
-            if (lane == 0) {
-                st->T = e >= 0 ? __popc(has) : 0;
-                st->e = e;
-            }
+            if (lane == 0) st->T = e >= 0 ? min(kFTok, max(0, __popc(has) - kFTok * h)) : 0;
         }
         __syncthreads();
         T = st->T;
         if (T == 0) {
             if (t == 0) {
                 io.unit_live[u] = 0;
+                io.unit_key[u] = -1;
                 mbar_wait(xbar, 0);  // no copy may be in flight into an exiting CTA
             }
             return;
@@ -1282,8 +1351,8 @@ __global__ void __launch_bounds__(256, 2) batch_small_kernel(const __grid_consta
             ut.w[k] = k < T ? st->w[k] : 0.f;
         }
     }
-    if (!shared && t == 0) fused_issue_up(sm, ep, g, H, policy_evict_first(), 0, 3);
-    // each active thread's x group from shared memory, then the last chunk into that space
+    if (!shared && t == 0) fused_issue_up(sm, ep, g, H, policy_evict_first(), 0, 4 - nx);
+    // each active thread's x group from shared memory, then the chunks whose space x took
     const FusedRole role = fused_role(T, H / 64, false);
     const bool xok = mbar_wait(xbar, 0);
     XFixed xf = {};
@@ -1292,13 +1361,16 @@ __global__ void __launch_bounds__(256, 2) batch_small_kernel(const __grid_consta
         x_group_load(x_s + (size_t)pick(ut.tok, role.tk) * H, role.gc, xw);
         x_group_fixed(xw, xf);
     }
-    fence_proxy_async_smem();  // the reads of x come before the copy that overwrites them
+    fence_proxy_async_smem();  // the reads of x come before the copies that overwrite them
     if (!__syncthreads_and(xok)) return;
-    if (t == 0) fused_issue_up(sm, ep, g, H, policy_evict_first(), 3, 4);
+    if (t == 0) fused_issue_up(sm, ep, g, H, policy_evict_first(), 4 - nx, 4);
     uint32_t dn_par = 0;
     uint64_t live = 0;
     if (!fused_unit<false>(P, io, sm, ep, g, T, ut, xf, xf, 0, dn_par, live)) return;
-    if (t == 0) io.unit_live[u] = __popcll(live);
+    if (t == 0) {
+        io.unit_live[u] = live;
+        io.unit_key[u] = shared ? E : st->e;
+    }
 }
 
 // y[b][o] = the token's partial rows added in a fixed order (32 outputs per
@@ -1346,11 +1418,28 @@ __global__ void __launch_bounds__(256) batch_fused_reduce_kernel(const __grid_co
         __syncthreads();  // part[] is reused below
         int n = 0, ng = 0;
         if (io.unit_live) {
-            // small-batch path: every unit holds all the tokens of its expert
-            for (int q = t; q < io.n_units; q += blockDim.x) {
-                const int c = __ldcg(io.unit_live + q);
-                n += c;
-                ng += c > 0;
+            // small-batch path: thread q walks group q's units in order (an
+            // expert's units are adjacent) and ORs the masks of each expert
+            const int NGs = P.shared_neurons / 64, NGr = P.routed_neurons / 64;
+            const int NSu = small_shared_units(NGs, io.batch);
+            for (int q = t; q < NGs + NGr; q += blockDim.x) {
+                const bool sh = q < NGs;
+                const int first = sh ? q : NSu + (q - NGs), step = sh ? NGs : NGr;
+                const int last = sh ? NSu : io.n_units;
+                int key = -2;
+                unsigned long long acc = 0;
+                for (int v = first; v < last; v += step) {
+                    const int kv = __ldcg(io.unit_key + v);
+                    if (kv != key) {
+                        n += __popcll(acc);
+                        ng += acc != 0ull;
+                        acc = 0;
+                        key = kv;
+                    }
+                    if (kv >= 0) acc |= __ldcg(reinterpret_cast<const unsigned long long*>(io.unit_live) + v);
+                }
+                n += __popcll(acc);
+                ng += acc != 0ull;
             }
         } else {
             // union live rows and groups per expert, from the union masks
@@ -1416,14 +1505,15 @@ using namespace hs_host;
 
 namespace {
 struct BatchLayout {
-    size_t meta, topk_idx, topk_w, pair_tok, pair_w, pair_slot, xt, xsc, h_pair, h_sh, mask_r, mask_s, unit_live, partial,
-        total;
+    size_t meta, topk_idx, topk_w, pair_tok, pair_w, pair_slot, xt, xsc, h_pair, h_sh, mask_r, mask_s, unit_live, unit_key,
+        partial, total;
 };
 
-// Grid of the small-batch kernel: the shared expert's groups, then room for
-// B * K distinct routed experts.
+// Grid of the small-batch kernel: the shared expert's units, then room for
+// B * K (routed expert, token group) entries.
 int small_units(const hs_moe_layer* L, int B) {
-    return (L->shared ? L->shared->neurons / 64 : 0) + B * L->top_k * (L->routed[0].neurons / 64);
+    return hs::small_shared_units(L->shared ? L->shared->neurons / 64 : 0, B) +
+           B * L->top_k * (L->routed[0].neurons / 64);
 }
 
 BatchLayout batch_layout(const hs_moe_layer* L, int B) {
@@ -1446,7 +1536,8 @@ BatchLayout batch_layout(const hs_moe_layer* L, int B) {
     l.mask_r = take((size_t)E * (NR / 32) * 4);
     l.mask_s = take((size_t)(NS ? NS / 32 : 1) * 4);
     const int Ut = (NS / 64) + K * (NR / 64);
-    l.unit_live = take((size_t)small_units(L, B) * 4);
+    l.unit_live = take((size_t)small_units(L, B) * 8);
+    l.unit_key = take((size_t)small_units(L, B) * 4);
     // the fused path's partial rows (per token, slot and group) or the banded path's (per token and slot)
     l.partial = take((size_t)B * std::max(Ut, SC + K) * H * 4);
     l.total = o;
@@ -1515,11 +1606,12 @@ int hs_batch_decode(const hs_moe_layer* L, const uint16_t* x, const float* logit
     if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return HS_ERR_CUDA;
     const int up_smem = hs::BatchUpSmem::total(L->hidden);
     const int dn_smem = hs::BatchDownSmem::total();
-    if (batch <= hs::kFTok && !(flags & HS_BATCH_EXPERT_UNION)) {
+    if (batch <= hs::kSmallMaxBatch && !(flags & HS_BATCH_EXPERT_UNION)) {
         // every expert's tokens fit one unit: no route kernel, plan or meta block
         const int f_smem = hs::FusedSmem::total(L->hidden);
         const int Ut = (L->shared ? L->shared->neurons / 64 : 0) + L->top_k * (L->routed[0].neurons / 64);
-        io.unit_live = reinterpret_cast<int*>(w + l.unit_live);
+        io.unit_live = reinterpret_cast<uint64_t*>(w + l.unit_live);
+        io.unit_key = reinterpret_cast<int*>(w + l.unit_key);
         io.n_units = small_units(L, batch);
         if (set_smem_attr((const void*)hs::batch_small_kernel, f_smem) != HS_OK) return HS_ERR_CUDA;
         if (set_smem_attr((const void*)hs::batch_fused_reduce_kernel, Ut * 128) != HS_OK) return HS_ERR_CUDA;

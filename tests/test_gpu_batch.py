@@ -122,12 +122,14 @@ def single_token_decodes(dl, X, LG):
 
 @pytest.mark.parametrize("B,H,E,NR,NS,K", [(2, 512, 8, 128, 256, 3), (3, 3072, 6, 192, 0, 2),
                                            (4, 512, 8, 128, 256, 3), (5, 512, 8, 128, 256, 3),
-                                           (8, 512, 8, 128, 256, 3)])
+                                           (8, 512, 8, 128, 256, 3), (9, 512, 8, 128, 256, 3),
+                                           (16, 3072, 6, 192, 0, 2)])
 def test_batch_rows_equal_single_token_decode(B, H, E, NR, NS, K):
     """Batching changes no token's result: every unit adds each token's terms
     in the same order as the batch-1 kernel (rows live only for another token
     add +0), so each row of a batch decode equals that token decoded alone,
-    bit for bit (B <= 4: one unit per expert; B > 4: the ticketed units)."""
+    bit for bit (B <= 8: units numbered before routing; B > 8: the ticketed
+    units)."""
     L = synth.layer_inputs(2, "t-batch-eq", H, E, NR, NS, H, p=0.2, p_shared=0.3)
     X, LG = synth.tokens(2, "t-batch-eq", B, B, H, E)
     dl = make_layer(L, K)
@@ -137,14 +139,21 @@ def test_batch_rows_equal_single_token_decode(B, H, E, NR, NS, K):
         assert torch.equal(y[b], y1)
 
 
-def test_small_path_every_token_on_the_same_experts():
-    """All tokens route alike: each routed unit holds all B = 4 tokens."""
+@pytest.mark.parametrize("B", [4, 8])
+def test_small_path_every_token_on_the_same_experts(B):
+    """All tokens route alike: with B = 4 each routed unit holds all 4 tokens;
+    with B = 8 each expert's tokens fill two units (token groups of 4), whose
+    live masks the counts must unite, and each row still equals its batch-1
+    decode."""
     H, E, NR, NS, K = 512, 8, 128, 256, 3
     L = synth.layer_inputs(3, "t-batch-same", 0, E, NR, NS, H, p=0.2, p_shared=0.3)
-    X, LG = synth.tokens(3, "t-batch-same", 0, 4, H, E)
+    X, LG = synth.tokens(3, "t-batch-same", 0, B, H, E)
     LG[:] = LG[0].clone()
-    y, yf, dbg = check_batch(L, make_layer(L, K), X, LG, K, "same experts")
+    dl = make_layer(L, K)
+    y, yf, dbg = check_batch(L, dl, X, LG, K, f"same experts B={B}")
     assert len(np.unique(dbg["topk_idx"].numpy())) == K
+    for b, (y1, yf1) in enumerate(single_token_decodes(dl, X, LG)):
+        assert np.array_equal(yf[b], yf1) and torch.equal(y[b], y1)
 
 
 @pytest.fixture(scope="module")
@@ -154,7 +163,7 @@ def cfg4_layer():
     return L, make_layer(L, 6)
 
 
-@pytest.mark.parametrize("B", [2, 3, 4, 8, 32, 64])
+@pytest.mark.parametrize("B", [2, 3, 4, 6, 8, 16, 32, 64])
 def test_config4_parity(cfg4_layer, B):
     L, dl = cfg4_layer
     X, LG = synth.tokens(0, "cfg4", B, B)
