@@ -1179,8 +1179,10 @@ __global__ void __launch_bounds__(256, 2) batch_fused_kernel(const __grid_consta
 // of the batch, experts ascending, each expert's tokens in order (an expert
 // with c tokens has ceil(c / 4) entries), and exits if the batch has fewer
 // entries.  Each routed CTA routes the B tokens itself (one warp per token)
-// and finds its entry from per-expert pair counts, so there is no route
-// kernel, plan, ticket or zeroed meta block.  x of the B tokens (2BH bytes,
+// and finds its entry (up to 4 tokens: the j-th distinct expert, from a
+// 128-bit set; 5 to 8: from per-expert pair counts and a scan, a step that
+// costs the smaller batches ~0.5 us), so there is no route kernel, plan,
+// ticket or zeroed meta block.  x of the B tokens (2BH bytes,
 // at most 16H) is bulk-copied once into the space of the last one or two
 // 16-row weight chunks right after the wait for the previous kernel and
 // before any routed weights are requested (x read by every thread from L2
