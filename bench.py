@@ -47,6 +47,7 @@ def _args():
     ap.add_argument("--p", type=float, default=0.1)
     ap.add_argument("--layers", type=int, default=LAYERS)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-cpu-all-cores", action="store_true", help="skip the all-cores oracle timing")
     ap.add_argument("--batch-sizes", type=str, default="2,3,8,32,64",
                     help="batch decode leg (one MoE layer, 30%% dead neurons); empty to skip")
     ap.add_argument("--no-prefill", action="store_true", help="skip the 2048-token prefill leg")
@@ -203,7 +204,8 @@ def oracle_layer_expert_source(l, p):
 
 
 def time_oracle(n_layers_max, p, budget_s, steps=None):
-    """Times the oracle per layer on the host; returns (us per layer, layers done, threads)."""
+    """Times the oracle on the host, one layer decode at a time over the first
+    n_layers_max layers; returns the seconds of each decode."""
     import oracle
     import synth
     prepared = []
@@ -229,6 +231,64 @@ def time_oracle(n_layers_max, p, budget_s, steps=None):
         elif time.perf_counter() - t_all > budget_s:
             break
     return times
+
+
+def _oracle_all_cores_worker(i, p, n_layers, reps, barrier, queue):
+    """One process of the all-cores oracle timing: prepares layers
+    0..n_layers-1, waits for every process, then runs `reps` layer decodes
+    (single-threaded BLAS) and reports its start and end (system-wide
+    monotonic clock)."""
+    for v in ("OPENBLAS_NUM_THREADS", "OMP_NUM_THREADS", "MKL_NUM_THREADS"):
+        os.environ[v] = "1"
+    try:
+        import oracle
+        import synth
+        prepared = []
+        for l in range(n_layers):
+            x, lg = synth.tokens(0, "cfg3", l, 1)
+            routed, shared = oracle_layer_expert_source(l, p)
+            idx, _ = oracle.router_topk(lg[0], 6)
+            for e in idx:
+                routed(int(e))
+            prepared.append((x[0], lg[0], routed, shared))
+        barrier.wait(timeout=300)
+        t0 = time.monotonic()
+        for r in range(reps):
+            x, lg, routed, shared = prepared[(i + r) % n_layers]
+            oracle.moe_layer(x, lg, routed, shared, k=6)
+        queue.put((i, t0, time.monotonic(), None))
+    except Exception as e:  # reported to the parent, which gives up on the leg
+        queue.put((i, None, None, repr(e)))
+
+
+def time_oracle_all_cores(p, reps=6, n_layers=2, timeout_s=600):
+    """Oracle throughput on every host core the process may use: one process
+    per core (spawned: the parent has a CUDA context), each decoding layers of
+    the same workload independently (the 23 layers of a step are independent).
+    Returns (seconds per layer decode, processes, layer decodes timed)."""
+    import multiprocessing as mp
+    n = len(os.sched_getaffinity(0))
+    ctx = mp.get_context("spawn")
+    barrier, queue = ctx.Barrier(n), ctx.Queue()
+    procs = [ctx.Process(target=_oracle_all_cores_worker, args=(i, p, n_layers, reps, barrier, queue), daemon=True)
+             for i in range(n)]
+    for pr in procs:
+        pr.start()
+    res = []
+    try:
+        for _ in range(n):
+            res.append(queue.get(timeout=timeout_s))
+    finally:
+        for pr in procs:
+            pr.join(timeout=10)
+            if pr.is_alive():
+                pr.kill()
+                pr.join()
+    errs = [r[3] for r in res if r[3]]
+    if errs:
+        raise RuntimeError(errs[0])
+    wall = max(r[2] for r in res) - min(r[1] for r in res)
+    return wall / (n * reps), n, n * reps
 
 
 def bench_batch(args, dev, stream, timed, bytemodel, hs):
@@ -729,6 +789,14 @@ def main():
         cpu = {"value": statistics.median(times) * 1e6, "unit": UNIT, "cores": 1, "kind": "oracle",
                "sample": f"{len(times)} layer decodes of layers 0-2 of the same workload (fp64 numpy, "
                          "single-threaded BLAS), median per layer"}
+        if not args.no_cpu_all_cores:
+            try:
+                s_all, n_proc, n_dec = time_oracle_all_cores(args.p)
+                cpu["all_cores"] = {"value": round(s_all * 1e6, 1), "unit": UNIT, "cores": n_proc,
+                                    "sample": f"{n_proc} processes (one per host core), each {n_dec // n_proc} "
+                                              "layer decodes of layers 0-1; wall time of all of them / decodes"}
+            except Exception as e:  # the single-core figure above stands on its own
+                cpu["all_cores"] = {"error": repr(e)[:200]}
 
     if rank == 0:
         csrc = os.path.join(ROOT, "activation_sparse_moe_gb300", "csrc")
