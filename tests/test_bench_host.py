@@ -1,0 +1,46 @@
+"""Host-side pieces of bench.py that need no GPU: the clock record taken
+during the timed region, and the ncu traffic record lookup (a record whose
+source hash no longer matches its kernel's sources is not used)."""
+import hashlib
+import os
+import sys
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+sys.path.insert(0, ROOT)
+
+import bench  # noqa: E402
+
+
+def test_clock_summary_median_max_and_reasons():
+    c = bench.ClockSampler("0")
+    c.lines = [
+        "0, 2070, 2070, 812.5, 0x0000000000000000, Not Active, Not Active, Not Active, Not Active",
+        "0, 1980, 2070, 1390.1, 0x0000000000000004, Not Active, Not Active, Not Active, Active",
+        "0, 2070, 2070, 905.0, 0x0000000000000000, Not Active, Not Active, Not Active, Not Active",
+        "0, [N/A], 2070, 905.0, 0x0, Not Active, Not Active, Not Active, Not Active",  # unreadable: skipped
+        "garbage",
+    ]
+    s = c.summary()
+    assert s == {"sm_mhz": 2070.0, "sm_max_mhz": 2070.0, "reasons": ["sw_power_cap"], "samples": 3}
+
+
+def test_clock_summary_flags_thermal_and_empty_record():
+    c = bench.ClockSampler("0")
+    c.lines = ["0, 1500, 2070, 1400.0, 0x48, Active, Not Active, Active, Not Active"]
+    assert c.summary()["reasons"] == ["hw_slowdown", "sw_thermal_slowdown"]
+    c.lines = []
+    assert c.summary() == {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+
+
+def test_recorded_traffic_requires_matching_source_hash(tmp_path, monkeypatch):
+    src = tmp_path / "k.cu"
+    src.write_bytes(b"__global__ void k() {}\n")
+    h = hashlib.sha256(src.read_bytes()).hexdigest()
+    prof = tmp_path / "profiles"
+    prof.mkdir()
+    (prof / "k.txt").write_text(f"# k\nsource_sha256: {h}\nkernel: k\ndram_bytes_per_launch: 12345\n")
+    monkeypatch.setattr(bench, "ROOT", str(tmp_path))
+    assert bench._recorded_traffic("k", [str(src)]) == 12345.0
+    src.write_bytes(b"__global__ void k() { }\n")  # the kernel changed since the counters were taken
+    assert bench._recorded_traffic("k", [str(src)]) is None
+    assert bench._recorded_traffic("missing", [str(src)]) is None
