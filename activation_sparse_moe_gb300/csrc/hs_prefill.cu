@@ -36,8 +36,6 @@ constexpr int kMaxTokens = 4096;
 constexpr int kTokBlk = 8;       // tokens per CTA of the list/gather kernel
 constexpr int kMaxKTiles = 64;    // 64-neuron tiles per expert (neurons <= 4096): one 64-bit mask
 
-// Output band width of the down product: 192 when it divides the hidden size, else 128.
-
 struct PrefillMeta {
     int n_tiles;                  // token tiles (routed experts first, then shared)
     int up_units, dn_units;
