@@ -68,14 +68,17 @@ def on_prefill_kernels(B, flags=0):
     return B >= PREFILL_MIN_BATCH and not (flags & hs.HS_BATCH_EXPERT_UNION)
 
 
-def check_batch(L, dl, X, LG, K, what, flips_allowed=4, flags=0):
+def check_batch(L, dl, X, LG, K, what, flips_allowed=4, flags=0, prefill=None, routed_expert=None):
+    """prefill: whether the call runs on the prefill's kernels (by default the
+    library's rule for stacked layers); routed_expert: the oracle's expert of
+    each descriptor index (by default the stack's)."""
     y, yf, dbg = run_batch(dl, X, LG, flags=flags)
-    ref = oracle.moe_tokens(X, LG, L.routed_expert, L.shared, k=K)
+    ref = oracle.moe_tokens(X, LG, routed_expert or L.routed_expert, L.shared, k=K)
     assert np.array_equal(dbg["topk_idx"].numpy(), ref["idx"]), what
     np.testing.assert_allclose(dbg["topk_w"].double().numpy(), ref["w"], rtol=2e-6, atol=1e-7)
     check_close(yf, ref["out"], f"{what} y_f32")
     n, ng = union_rows(ref, L)
-    if on_prefill_kernels(X.shape[0], flags):
+    if on_prefill_kernels(X.shape[0], flags) if prefill is None else prefill:
         # fp16 operands: the prefill's output contract, and neurons within
         # fp16 rounding of 0 (or whose fp16 h underflows) may flip
         check_bf16_rounding(y, yf, ref["out"], what)
@@ -223,12 +226,13 @@ def test_config4_small_path_dense_flag_and_determinism(cfg4_layer):
         assert np.array_equal(yf1[b], yfs) and torch.equal(y1[b], ys)
 
 
-@pytest.mark.parametrize("B,flags", [(1, 0), (3, 0), (8, 0), (8, hs.HS_BATCH_EXPERT_UNION), (56, 0)])
+@pytest.mark.parametrize("B,flags", [(1, 0), (3, 0), (8, 0), (16, 0), (8, hs.HS_BATCH_EXPERT_UNION), (56, 0)])
 def test_graph_capture_equals_eager(B, flags):
     """The layer decode captured in a CUDA graph (as a serving loop replays
     it) gives the eager call's bits, replay after replay, on every path:
-    batch 1, 2..4 tokens, the ticketed units, the expert-union kernels and
-    (56 tokens) the prefill's tensor-core kernels."""
+    batch 1, 2..8 tokens (units numbered before routing), the ticketed units
+    (16 tokens), the expert-union kernels and (56 tokens) the prefill's
+    tensor-core kernels."""
     H, E, NR, NS, K = 512, 8, 128, 256, 3
     L = synth.layer_inputs(8, "t-graph", 0, E, NR, NS, H, p=0.2, p_shared=0.3, dead_frac=0.3)
     dl = make_layer(L, K)
@@ -266,3 +270,44 @@ def test_config4_batch64_on_prefill_kernels_dense_flag_and_determinism(cfg4_laye
     yd, yfd, _ = run_batch(dl, X, LG, flags=hs.HS_FORCE_DENSE)
     assert np.array_equal(yf1, yf2) and torch.equal(y1, y2)
     assert np.array_equal(yf1, yfd) and torch.equal(y1, yd)
+
+
+def permuted_layer(L, K, pi):
+    """The stacked experts handed to the library in the order pi (descriptor e
+    is stack expert pi[e]): the experts no longer sit at uniform strides, so
+    the kernels take each expert's pointers from the descriptor table (as for
+    experts allocated one by one), and the prefill's kernels, which need one
+    tensor map over a uniform stack, do not take the layer."""
+    dl = make_layer(L, K)
+    dl.c = hs.Layer([dl.routed.desc(int(pi[e])) for e in range(dl.routed.E)], dl.shared.desc(0), dl.hidden, K)
+    return dl, (lambda e: L.routed_expert(int(pi[e])))
+
+
+@pytest.mark.parametrize("B", [1, 3, 8, 16, 64])
+def test_experts_not_stacked_uniformly(B):
+    """Batch 1, the small-batch kernel, the ticketed kernel and, at 64 tokens
+    (the CUDA-core kernels' largest batch, the prefill refusing the layer),
+    the ticketed kernel again, against the oracle with the same permutation;
+    the prefill entry point refuses the layer and batches above 64 are
+    refused."""
+    H, E, NR, NS, K = 512, 8, 128, 256, 3
+    L = synth.layer_inputs(9, "t-nonuniform", 0, E, NR, NS, H, p=0.2, p_shared=0.3, dead_frac=0.3)
+    pi = np.random.default_rng(9).permutation(E)
+    assert not np.array_equal(pi, np.arange(E))
+    dl, routed_expert = permuted_layer(L, K, pi)
+    X, LG = synth.tokens(9, "t-nonuniform", B, B, H, E)
+    check_batch(L, dl, X, LG, K, f"non-uniform B={B}", prefill=False, routed_expert=routed_expert)
+    if B == 64:
+        assert dl.prefill_workspace_size(64) == 0
+        assert dl.workspace_size(65) == 0
+        y = torch.empty((65, H), dtype=torch.bfloat16, device="cuda")
+        X65, LG65 = synth.tokens(9, "t-nonuniform", 65, 65, H, E)
+        ws = torch.zeros(dl.workspace_size(64), dtype=torch.uint8, device="cuda")
+        with pytest.raises(hs.HsError) as e:
+            hs.hs_moe_layer_decode(dl.c, X65.cuda(), LG65.cuda(), 65, y, None, 0, None, ws)
+        assert e.value.status == hs.HS_ERR_UNSUPPORTED_SHAPE
+        with pytest.raises(hs.HsError) as e:
+            hs.hs_moe_prefill(dl.c, X65.cuda(), LG65.cuda(), 65, y, workspace=ws)
+        assert e.value.status == hs.HS_ERR_UNSUPPORTED_SHAPE
+        torch.cuda.synchronize()
+        assert hs.hs_device_status() == hs.HS_OK

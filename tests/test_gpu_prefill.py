@@ -208,3 +208,26 @@ def test_config5_dense_flag_equal(cfg5):
     yd, yfd, dd = run_prefill(dl, X, LG, flags=hs.HS_FORCE_DENSE)
     assert np.array_equal(yf1, yfd) and torch.equal(y1, yd)
     assert int(dd["tiles"][0]) == 0
+
+
+def test_config5_layer_at_max_tokens(cfg5):
+    """The largest prompt chunk the library takes (4096 tokens: 24,576 routed
+    pairs, 32 shared-expert tiles) on the full-size layer: sampled tokens
+    (the first, the last and random ones; each routed expert's last tile is
+    ragged) against the oracle, every (expert, token tile) pair counted once."""
+    L, dl, _, _ = cfg5
+    T = 4096
+    assert dl.prefill_workspace_size(T) > 0 and dl.prefill_workspace_size(T + 1) == 0
+    X, LG = synth.tokens(0, "cfg5-max", 0, T)
+    y, yf, dbg = run_prefill(dl, X, LG)
+    rng = np.random.default_rng(6)
+    sample = np.unique(np.concatenate([[0, T - 1], rng.choice(T, size=10, replace=False)]))
+    ref = oracle.moe_tokens(X[sample], LG[sample], L.routed_expert, L.shared, k=6)
+    assert np.array_equal(dbg["topk_idx"].numpy()[sample], ref["idx"])
+    rel, mx = check_close(yf[sample], ref["out"], "4096 tokens sampled y_f32")
+    check_bf16_rounding(y[sample], yf[sample], ref["out"], "4096 tokens sampled")
+    counts = np.bincount(dbg["topk_idx"].numpy().ravel(), minlength=128)
+    tiles = int(sum((c + TILE - 1) // TILE for c in counts)) * (synth.N_ROUTED // 64)
+    tiles += (T // TILE) * (synth.N_SHARED // 64)
+    assert int(dbg["tiles"][1]) == tiles
+    assert np.isfinite(yf).all()
