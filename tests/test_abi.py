@@ -116,3 +116,13 @@ def test_prefill_argument_errors(lib):
     assert hs.hs_moe_prefill_workspace_size(_stacked_layer(hidden=192), 100) == 0
     # the workspace grows with the token count
     assert hs.hs_moe_prefill_workspace_size(L, 200) > need
+
+
+def test_missing_library_fails_loudly(monkeypatch, tmp_path):
+    """Without the built library every call raises: there is no fallback."""
+    monkeypatch.setattr(hs, "LIB_PATH", str(tmp_path / "libhs.so"))
+    monkeypatch.setattr(hs, "_lib", None)
+    with pytest.raises(RuntimeError, match="not built"):
+        hs.lib()
+    with pytest.raises(RuntimeError, match="not built"):
+        hs.hs_status_string(0)
