@@ -9,8 +9,8 @@
 // live rows once (the verify step of section "Speculative decoding." reads
 // three rows' activations through the same weights this way).
 //
-// B <= 4 (batch_small_kernel + batch_fused_reduce_kernel): one CTA per
-// (expert, 64-neuron group) unit with all of that expert's tokens, numbered
+// B <= 8 (batch_small_kernel + batch_fused_reduce_kernel): one CTA per
+// (expert, 64-neuron group, up to 4 of the expert's tokens) unit, numbered
 // before routing; every CTA routes the batch itself.  Two kernels, no meta
 // block, programmatic dependent launch in between.
 //
@@ -1609,7 +1609,7 @@ int hs_batch_decode(const hs_moe_layer* L, const uint16_t* x, const float* logit
     const int up_smem = hs::BatchUpSmem::total(L->hidden);
     const int dn_smem = hs::BatchDownSmem::total();
     if (batch <= hs::kSmallMaxBatch && !(flags & HS_BATCH_EXPERT_UNION)) {
-        // every expert's tokens fit one unit: no route kernel, plan or meta block
+        // units numbered before routing: no route kernel, plan or meta block
         const int f_smem = hs::FusedSmem::total(L->hidden);
         const int Ut = (L->shared ? L->shared->neurons / 64 : 0) + L->top_k * (L->routed[0].neurons / 64);
         io.unit_live = reinterpret_cast<uint64_t*>(w + l.unit_live);
