@@ -44,3 +44,12 @@ def test_recorded_traffic_requires_matching_source_hash(tmp_path, monkeypatch):
     src.write_bytes(b"__global__ void k() { }\n")  # the kernel changed since the counters were taken
     assert bench._recorded_traffic("k", [str(src)]) is None
     assert bench._recorded_traffic("missing", [str(src)]) is None
+
+
+def test_all_cores_oracle_timing_spawns_one_process_per_core():
+    """The all-cores CPU baseline: one spawned process per usable core, each
+    timing whole layer decodes of the oracle; the per-decode time is the wall
+    time of all of them divided by the decodes."""
+    s, n_proc, n_dec = bench.time_oracle_all_cores(0.1, reps=1, n_layers=1)
+    assert n_proc == len(os.sched_getaffinity(0)) and n_dec == n_proc
+    assert 0 < s < 60
