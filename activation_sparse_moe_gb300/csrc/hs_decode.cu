@@ -23,10 +23,13 @@
 //    and rounds to bf16.  Both kernels use programmatic dependent launch, so
 //    a kernel's launch overlaps the previous one; CTAs of the shared expert
 //    start streaming their weights before waiting on the previous kernel.
-//  * The up GEMV is CUDA-core work (HBM bound, no tensor cores): codes are
-//    turned into bf16 (128 + q) with one LOP3 per two codes and multiplied
-//    with the bf16 activations by mixed-precision FMA into fp32 (exact
-//    products); the 128 * sum(x) term is removed per 32-code chunk.
+//  * The up GEMV is integer-pipe work (HBM bound, no tensor cores): x is
+//    converted once per CTA into a 16-bit fixed-point copy with one exponent
+//    per 64-input scale group, split into a signed high and an unsigned low
+//    byte; each 32-byte group of codes is split into even and odd nibbles by
+//    two masks and dotted with the bytes by DP4A (exact int32 sums); the
+//    group's scale and bias are applied to the integer sum in fp32
+//    (group_dot_fixed16 in hs_kernels.cuh).
 #include "hs_kernels.cuh"
 #include "hs_host.h"
 
@@ -44,6 +47,7 @@ struct DecodeIO {
     float* dbg_topk_w;
     float* dbg_h;
     int* live_counts;        // [units] live rows per unit (workspace)
+    uint64_t* dbg_live;      // [units] live mask (h > 0) per unit, or null
     int units;
 };
 
@@ -88,114 +92,8 @@ struct PartialOut {
 };
 
 // ------------------------------------------------------------ down phase
-// Given h[64] and the live mask in shared memory, accumulate
-//   partial_o = wgt * (sum_{n live} h_n * (s_o q_{n,o} + b_o))
-// for the CTA's group, with the live rows at their row slot in codes_buf and
-// the slab (s_o, b_o) in sb_buf.  Thread (c, r3) owns outputs 32c..32c+31 and
-// sums the live rows n with n % S == r3 in ascending order; the S sums are
-// added in order r3 = 0..S-1 by all threads, one output each (the result does
-// not depend on which rows are live beyond the +0 terms, so the dense flag
-// gives identical bits).
-// A nibble at bit 4i of a code word becomes a float by masking it in place
-// under the exponent of 2^23 and subtracting 2^23 (exact: q * 16^i < 2^23);
-// the row's h is pre-scaled by 16^-i to undo the position.
-__device__ void down_accumulate_and_store(const uint8_t* codes_buf, const uint32_t* sb_buf, float* red_buf,
-                                          const float* h_s, uint64_t live, float Hsum, float wgt, int hidden,
-                                          const PartialOut out) {
-    const int C = hidden / 32;
-    const int S = min(256 / C, 7);  // S * C * 33 floats fit in the 64-row code buffer
-    const int t = threadIdx.x;
-    const int c = t % C, r3 = t / C;
-    const int rowb = hidden / 2;
-    float acc[32];
-#pragma unroll
-    for (int k = 0; k < 32; ++k) acc[k] = 0.f;
-    if (r3 < S) {
-        uint64_t m = 0;
-        for (int n = r3; n < 64; n += S) m |= 1ull << n;
-        m &= live;
-        while (m) {
-            const int n = __ffsll((long long)m) - 1;
-            m &= m - 1;
-            const float hn = h_s[n];
-            const float hs[5] = {hn, hn * 0.0625f, hn * 0.00390625f, hn * 0.000244140625f, hn * 1.52587890625e-05f};
-            const uint4 cw = *reinterpret_cast<const uint4*>(codes_buf + n * rowb + 16 * c);
-            const uint32_t w[4] = {cw.x, cw.y, cw.z, cw.w};
-#pragma unroll
-            for (int j = 0; j < 4; ++j) {
-                const uint32_t hi = w[j] >> 12;  // nibbles 5, 6, 7 at positions 2, 3, 4
-#pragma unroll
-                for (int i = 0; i < 8; ++i) {
-                    const uint32_t src = i < 5 ? w[j] : hi;
-                    const int pos = i < 5 ? i : i - 3;
-                    const float q = __uint_as_float((src & (15u << (4 * pos))) | 0x4B000000u) - 8388608.f;
-                    acc[8 * j + i] = fmaf(hs[pos], q, acc[8 * j + i]);
-                }
-            }
-        }
-    }
-    __syncthreads();  // all reads of codes_buf done: reuse it for the cross-subset sum
-    // red[s][c][k] with rows of 33 floats: the 32-float stores of a warp
-    // (consecutive c) and the combine's loads (consecutive outputs) are
-    // both free of bank conflicts
-    if (r3 < S) {
-        float* dst = red_buf + ((size_t)r3 * C + c) * 33;
-#pragma unroll
-        for (int k = 0; k < 32; ++k) dst[k] = acc[k];
-    }
-    __syncthreads();
-    // every thread finishes a strided set of 4-output quads: subsets added in order 0..S-1
-    for (int o4 = t; o4 < hidden / 4; o4 += blockDim.x) {
-        const int o = 4 * o4, oc = o >> 5, ok = o & 31;
-        float a[4];
-#pragma unroll
-        for (int e = 0; e < 4; ++e) a[e] = red_buf[(size_t)oc * 33 + ok + e];
-        for (int s = 1; s < S; ++s) {
-#pragma unroll
-            for (int e = 0; e < 4; ++e) a[e] += red_buf[((size_t)s * C + oc) * 33 + ok + e];
-        }
-        const uint4 sb4 = reinterpret_cast<const uint4*>(sb_buf)[o4];
-        const uint32_t sbw[4] = {sb4.x, sb4.y, sb4.z, sb4.w};
-        float r[4];
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-            const float2 sb = half2_to_float2(sbw[e]);
-            r[e] = wgt * fmaf(sb.x, a[e], sb.y * Hsum);
-        }
-        *out.quad(o4) = make_float4(r[0], r[1], r[2], r[3]);
-    }
-}
-
 __device__ __forceinline__ void store_zero_row(const PartialOut out, int hidden) {
     for (int i = threadIdx.x; i < hidden / 4; i += blockDim.x) *out.quad(i) = make_float4(0.f, 0.f, 0.f, 0.f);
-}
-
-// Live mask of h_s[0..63] (warp 0), the fixed-order sum of h, and the issue
-// of the down copies: live rows to their row slots and, if any, the slab.
-// Returns (through smem) the mask and sum.  Executed by warp 0.
-__device__ __forceinline__ void warp0_mask_and_issue(const float* h_s, bool dense, const uint8_t* dn_codes_g,
-                                                     const uint32_t* dn_slab, int hidden, uint8_t* codes_buf,
-                                                     uint32_t* sb_buf, uint64_t* bar, uint64_t* mask_out,
-                                                     float* hsum_out, uint64_t policy) {
-    const int lane = threadIdx.x & 31;
-    const float h0 = h_s[lane], h1 = h_s[lane + 32];
-    const unsigned b0 = __ballot_sync(0xffffffffu, h0 > 0.f);
-    const unsigned b1 = __ballot_sync(0xffffffffu, h1 > 0.f);
-    uint64_t live = dense ? ~0ull : ((uint64_t)b1 << 32 | b0);
-    const int rowb = hidden / 2;
-    if (live) {
-        if (lane == 0) mbar_arrive_expect_tx(bar, (uint32_t)(__popcll(live) * rowb + hidden * 4));
-        __syncwarp();
-        if (lane == 0) bulk_g2s(sb_buf, dn_slab, hidden * 4, bar, policy);
-        if ((live >> lane) & 1) bulk_g2s(codes_buf + lane * rowb, dn_codes_g + (size_t)lane * rowb, rowb, bar, policy);
-        if ((live >> (lane + 32)) & 1)
-            bulk_g2s(codes_buf + (lane + 32) * rowb, dn_codes_g + (size_t)(lane + 32) * rowb, rowb, bar, policy);
-    }
-    // the fixed-order sum of h is needed only at the end: after the copies
-    float s = h0 + h1;
-#pragma unroll
-    for (int off = 16; off; off >>= 1) s += __shfl_xor_sync(0xffffffffu, s, off);
-    if (lane == 0) { *mask_out = live; *hsum_out = s; }
 }
 
 // Down phase of the fused kernel: thread j < hidden/OPT owns outputs
@@ -486,6 +384,10 @@ moe_decode_b1_kernel(const __grid_constant__ LayerParams P, const DecodeIO io) {
     const uint64_t live = *reinterpret_cast<const uint64_t*>(live8);
     const PartialOut out_row{io.partial, io.units, u};
     if (t == 0) io.live_counts[u] = __popcll(live);
+    if (io.dbg_live && t < 32) {  // the live set itself (h > 0), whatever the dense flag reads
+        const unsigned m0 = __ballot_sync(0xffffffffu, h_s[t] > 0.f), m1 = __ballot_sync(0xffffffffu, h_s[t + 32] > 0.f);
+        if (t == 0) io.dbg_live[u] = (uint64_t)m1 << 32 | m0;
+    }
     if (!any) {
         store_zero_row(out_row, hidden);
         return;
@@ -502,40 +404,6 @@ moe_decode_b1_kernel(const __grid_constant__ LayerParams P, const DecodeIO io) {
         down_acc_and_store<12, kRow>(codes_buf, sb_buf, h_s, live, Hsum, wgt, rowb, t, out_row, rsw);
     else
         down_acc_and_store<16, kRow>(codes_buf, sb_buf, h_s, live, Hsum, wgt, rowb, t, out_row, rsw);
-}
-
-// ------------------------------------------ single-expert sparse down (K1)
-__global__ void __launch_bounds__(256, 2)
-down_sparse_kernel(const float* __restrict__ h, const uint8_t* __restrict__ dn_codes,
-                   const uint32_t* __restrict__ dn_sb, int hidden, unsigned flags, float* __restrict__ partial,
-                   int* __restrict__ live_counts) {
-    extern __shared__ __align__(128) uint8_t smem[];
-    uint8_t* codes_buf = smem;
-    uint32_t* sb_buf = reinterpret_cast<uint32_t*>(smem + SmemLayout::codes_bytes(hidden));
-    uint8_t* misc = smem + SmemLayout::misc_off(hidden);
-    float* h_s = reinterpret_cast<float*>(misc + SmemLayout::kH);
-    uint64_t* bars = reinterpret_cast<uint64_t*>(misc + SmemLayout::kBarsOff);
-    uint64_t* live_s = reinterpret_cast<uint64_t*>(misc + SmemLayout::kLive);
-    float* hsum_s = reinterpret_cast<float*>(misc + SmemLayout::kHsum);
-    const int t = threadIdx.x, g = blockIdx.x;
-    const int rowb = hidden / 2;
-    if (t == 0) { mbar_init(&bars[0], 1); fence_mbar_init(); }
-    pdl_wait();
-    pdl_trigger();
-    if (t < 64) h_s[t] = h[g * 64 + t];
-    __syncthreads();
-    if (t < 32)
-        warp0_mask_and_issue(h_s, (flags & HS_FORCE_DENSE) != 0, dn_codes + (size_t)g * 64 * rowb,
-                             dn_sb + (size_t)g * hidden, hidden, codes_buf, sb_buf, &bars[0], live_s, hsum_s,
-                             policy_evict_first());
-    __syncthreads();
-    const uint64_t live = *live_s;
-    const PartialOut out_row{partial, (int)gridDim.x, g};
-    if (t == 0) live_counts[g] = __popcll(live);
-    if (!live) { store_zero_row(out_row, hidden); return; }
-    if (!__syncthreads_and(mbar_wait(&bars[0], 0))) return;
-    down_accumulate_and_store(codes_buf, sb_buf, reinterpret_cast<float*>(codes_buf), h_s, live, *hsum_s, 1.f,
-                              hidden, out_row);
 }
 
 // ------------------------------------------------ fixed-order partial sum
@@ -649,42 +517,6 @@ extern "C" int hs_selftest_bounded_wait(long long limit_cycles, hs_stream_t stre
     return launch_err();
 }
 
-// ----------------------------------------------------------- sparse down
-extern "C" size_t hs_expert_down_sparse_workspace_size(int neurons, int out_dim) {
-    if (neurons <= 0 || out_dim <= 0 || neurons % 64 || out_dim % 64) return 0;
-    const size_t G = neurons / 64;
-    return round_up(G * out_dim * sizeof(float), 256) + round_up(G * sizeof(int), 256);
-}
-
-extern "C" int hs_expert_down_sparse(const float* h, const hs_w4* down_nm, int neurons, int out_dim, uint16_t* y_bf16,
-                                     float* y_f32, int* live_count, unsigned flags, void* ws, size_t ws_bytes,
-                                     hs_stream_t stream) {
-    if (!h || !down_nm || !down_nm->codes || !down_nm->sb || !y_bf16) return HS_ERR_INVALID_ARG;
-    if (flags & HS_DOWN_ROW_SCALES) return HS_ERR_INVALID_ARG;  // group slabs only
-    if (neurons <= 0 || out_dim <= 0) return HS_ERR_INVALID_ARG;
-    if (neurons % 64 || out_dim % 64 || out_dim > hs::kMaxHidden) return HS_ERR_UNSUPPORTED_SHAPE;
-    if (!al16(h) || !al16(down_nm->codes) || !al16(down_nm->sb) || !al16(y_bf16) || (y_f32 && !al16(y_f32)) ||
-        (live_count && !al4(live_count)) || !al16(ws))
-        return HS_ERR_MISALIGNED;
-    const size_t need = hs_expert_down_sparse_workspace_size(neurons, out_dim);
-    if (!ws || ws_bytes < need) return HS_ERR_WORKSPACE;
-    const int G = neurons / 64;
-    float* partial = static_cast<float*>(ws);
-    int* counts = reinterpret_cast<int*>(static_cast<char*>(ws) + round_up((size_t)G * out_dim * sizeof(float), 256));
-    const int smem = hs::SmemLayout::total(out_dim);
-    if (set_smem_attr((const void*)hs::down_sparse_kernel, smem) != HS_OK) return HS_ERR_CUDA;
-    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-    if (launch_pdl(hs::down_sparse_kernel, dim3(G), dim3(256), smem, s, h, down_nm->codes,
-                   static_cast<const uint32_t*>(down_nm->sb), out_dim, flags, partial, counts) != cudaSuccess)
-        return HS_ERR_CUDA;
-    if (set_smem_attr((const void*)hs::reduce_partials_kernel, G * 128) != HS_OK) return HS_ERR_CUDA;
-    if (launch_pdl(hs::reduce_partials_kernel, dim3(out_dim / 32), dim3(256), (size_t)G * 128, s,
-                   (const float*)partial, G, out_dim, y_bf16, y_f32, (const int*)counts, live_count,
-                   (int*)nullptr) != cudaSuccess)
-        return HS_ERR_CUDA;
-    return launch_err();
-}
-
 // ---------------------------------------------------------- layer decode
 extern "C" size_t hs_moe_layer_decode_workspace_size(const hs_moe_layer* L, int batch) {
     if (batch > 1) {
@@ -714,7 +546,8 @@ extern "C" int hs_moe_layer_decode(const hs_moe_layer* L, const uint16_t* x, con
         if (batch >= kPrefillMinBatch && !(flags & HS_BATCH_EXPERT_UNION) && hs_prefill_layer_ok(L, batch) == HS_OK) {
             // many tokens per expert: the prefill's tensor-core products
             if (dbg && dbg->h) return HS_ERR_INVALID_ARG;  // the h dump covers batch 1 only
-            const hs_prefill_debug pd{dbg ? dbg->topk_idx : nullptr, dbg ? dbg->topk_w : nullptr, nullptr, nullptr};
+            const hs_prefill_debug pd{dbg ? dbg->topk_idx : nullptr, dbg ? dbg->topk_w : nullptr, nullptr, nullptr,
+                                      dbg ? dbg->live_mask : nullptr, nullptr};
             const int st = hs_moe_prefill(L, x, logits, batch, y_bf16, y_f32, flags & HS_FORCE_DENSE,
                                           dbg ? &pd : nullptr, ws, ws_bytes, stream);
             if (st != HS_OK || !dbg) return st;
@@ -741,6 +574,8 @@ extern "C" int hs_moe_layer_decode(const hs_moe_layer* L, const uint16_t* x, con
     io.dbg_topk_idx = dbg ? dbg->topk_idx : nullptr;
     io.dbg_topk_w = dbg ? dbg->topk_w : nullptr;
     io.dbg_h = dbg ? dbg->h : nullptr;
+    io.dbg_live = dbg ? dbg->live_mask : nullptr;
+    if (io.dbg_live && ((uintptr_t)io.dbg_live & 7u)) return HS_ERR_MISALIGNED;
     int* live_out = dbg ? dbg->live_rows : nullptr;
 
     const int smem = hs::SmemLayout::total(L->hidden, (flags & HS_DOWN_ROW_SCALES) != 0);
@@ -753,82 +588,6 @@ extern "C" int hs_moe_layer_decode(const hs_moe_layer* L, const uint16_t* x, con
     if (launch_pdl(hs::reduce_partials_kernel, dim3(L->hidden / 32), dim3(256), (size_t)U * 128, s,
                    (const float*)io.partial, U, L->hidden, y_bf16, y_f32, (const int*)io.live_counts,
                    live_out, dbg ? dbg->live_groups : (int*)nullptr) != cudaSuccess)
-        return HS_ERR_CUDA;
-    return launch_err();
-}
-
-// ============================================================================
-// Allocation-free variant of hs_expert_down_sparse.
-//
-// Some callers cannot hand the library a workspace: code that runs where
-// device allocation is not allowed or not available at call time (a plugin
-// that only receives the tensors it must read and write from a host framework
-// which owns every allocation, or a real-time path that must never enter the
-// CUDA allocator).  For them the scratch of the two kernels below lives in a
-// fixed array compiled into the library; each GPU that loads the library
-// keeps that array (about 0.75 MB) until the process exits.
-//
-// The host never dereferences or passes the array's name to a kernel: in host
-// code that name is only a stand-in.  Its device address is looked up once per
-// device with cudaGetSymbolAddress and cached.
-// ============================================================================
-namespace {
-constexpr int kNoAllocMaxNeurons = 4096;   // at most 64 groups of 64 neurons
-constexpr int kNoAllocMaxOut = 3072;
-constexpr size_t kNoAllocPartialBytes = (size_t)(kNoAllocMaxNeurons / 64) * kNoAllocMaxOut * sizeof(float);
-constexpr size_t kNoAllocBytes = kNoAllocPartialBytes + (kNoAllocMaxNeurons / 64) * sizeof(int);
-}  // namespace
-
-static __device__ __align__(256) unsigned char hs_noalloc_scratch[kNoAllocBytes];
-
-namespace {
-// Device address of hs_noalloc_scratch on the current device (looked up on the
-// first call per device).  Returns nullptr if the lookup fails.
-void* noalloc_scratch_address() {
-    constexpr int kMaxDevices = 64;
-    static void* addr[kMaxDevices] = {};
-    static std::mutex mu;
-    int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
-    std::lock_guard<std::mutex> lock(mu);
-    if (!addr[dev]) {
-        void* p = nullptr;
-        if (cudaGetSymbolAddress(&p, hs_noalloc_scratch) != cudaSuccess) return nullptr;
-        addr[dev] = p;
-    }
-    return addr[dev];
-}
-}  // namespace
-
-extern "C" int hs_expert_down_sparse_noalloc(const float* h, const hs_w4* down_nm, int neurons, int out_dim,
-                                             uint16_t* y_bf16, float* y_f32, int* live_count, unsigned flags,
-                                             hs_stream_t stream) {
-    if (!h || !down_nm || !down_nm->codes || !down_nm->sb || !y_bf16) return HS_ERR_INVALID_ARG;
-    if (flags & HS_DOWN_ROW_SCALES) return HS_ERR_INVALID_ARG;  // group slabs only
-    if (neurons <= 0 || out_dim <= 0) return HS_ERR_INVALID_ARG;
-    if (neurons % 64 || out_dim % 64) return HS_ERR_UNSUPPORTED_SHAPE;
-    // beyond the compiled-in scratch capacity
-    if (neurons > kNoAllocMaxNeurons || out_dim > kNoAllocMaxOut) return HS_ERR_UNSUPPORTED_SHAPE;
-    if (!al16(h) || !al16(down_nm->codes) || !al16(down_nm->sb) || !al16(y_bf16) || (y_f32 && !al16(y_f32)) ||
-        (live_count && !al4(live_count)))
-        return HS_ERR_MISALIGNED;
-    char* scratch = static_cast<char*>(noalloc_scratch_address());
-    if (!scratch) return HS_ERR_CUDA;
-    const int G = neurons / 64;
-    float* partial = reinterpret_cast<float*>(scratch);
-    int* counts = reinterpret_cast<int*>(scratch + kNoAllocPartialBytes);
-    // every partial row and count is written before it is read: nothing in the
-    // scratch has to start at zero
-    const int smem = hs::SmemLayout::total(out_dim);
-    if (set_smem_attr((const void*)hs::down_sparse_kernel, smem) != HS_OK) return HS_ERR_CUDA;
-    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-    if (launch_pdl(hs::down_sparse_kernel, dim3(G), dim3(256), smem, s, h, down_nm->codes,
-                   static_cast<const uint32_t*>(down_nm->sb), out_dim, flags, partial, counts) != cudaSuccess)
-        return HS_ERR_CUDA;
-    if (set_smem_attr((const void*)hs::reduce_partials_kernel, G * 128) != HS_OK) return HS_ERR_CUDA;
-    if (launch_pdl(hs::reduce_partials_kernel, dim3(out_dim / 32), dim3(256), (size_t)G * 128, s,
-                   (const float*)partial, G, out_dim, y_bf16, y_f32, (const int*)counts, live_count,
-                   (int*)nullptr) != cudaSuccess)
         return HS_ERR_CUDA;
     return launch_err();
 }

@@ -35,18 +35,26 @@ def test_down_sparse_argument_errors(lib):
     w = hs.hs_w4(0x10000, 0x20000)
     W = C.byref(w)
     A = 0x100000  # fake, 16-byte aligned; validation fails before it is touched
-    assert f(None, W, 1856, 2688, A, None, None, 0, A, 1 << 30, None) == hs.HS_ERR_INVALID_ARG
-    assert f(A, W, 1856, 2688, None, None, None, 0, A, 1 << 30, None) == hs.HS_ERR_INVALID_ARG
-    assert f(A, W, 1800, 2688, A, None, None, 0, A, 1 << 30, None) == hs.HS_ERR_UNSUPPORTED_SHAPE
-    assert f(A, W, 1856, 2690, A, None, None, 0, A, 1 << 30, None) == hs.HS_ERR_UNSUPPORTED_SHAPE
-    assert f(A, W, -64, 2688, A, None, None, 0, A, 1 << 30, None) == hs.HS_ERR_INVALID_ARG
-    assert f(A + 4, W, 1856, 2688, A, None, None, 0, A, 1 << 30, None) == hs.HS_ERR_MISALIGNED
-    assert f(A, W, 1856, 2688, A + 2, None, None, 0, A, 1 << 30, None) == hs.HS_ERR_MISALIGNED
+    assert f(None, W, 1856, 2688, A, None, None, None, 0, A, 1 << 30, None) == hs.HS_ERR_INVALID_ARG
+    assert f(A, W, 1856, 2688, None, None, None, None, 0, A, 1 << 30, None) == hs.HS_ERR_INVALID_ARG
+    assert f(A, W, 1800, 2688, A, None, None, None, 0, A, 1 << 30, None) == hs.HS_ERR_UNSUPPORTED_SHAPE
+    assert f(A, W, 1856, 2690, A, None, None, None, 0, A, 1 << 30, None) == hs.HS_ERR_UNSUPPORTED_SHAPE
+    assert f(A, W, 1856, 3136, A, None, None, None, 0, A, 1 << 30, None) == hs.HS_ERR_UNSUPPORTED_SHAPE
+    assert f(A, W, 65600, 2688, A, None, None, None, 0, A, 1 << 30, None) == hs.HS_ERR_UNSUPPORTED_SHAPE
+    assert f(A, W, -64, 2688, A, None, None, None, 0, A, 1 << 30, None) == hs.HS_ERR_INVALID_ARG
+    assert f(A + 4, W, 1856, 2688, A, None, None, None, 0, A, 1 << 30, None) == hs.HS_ERR_MISALIGNED
+    assert f(A, W, 1856, 2688, A + 2, None, None, None, 0, A, 1 << 30, None) == hs.HS_ERR_MISALIGNED
+    assert f(A, W, 1856, 2688, A, None, A + 2, None, 0, A, 1 << 30, None) == hs.HS_ERR_MISALIGNED
+    assert f(A, W, 1856, 2688, A, None, None, A + 1, 0, A, 1 << 30, None) == hs.HS_ERR_MISALIGNED
+    # flags other than HS_FORCE_DENSE belong to the layer entry points
+    for fl in (hs.HS_BATCH_EXPERT_UNION, hs.HS_DOWN_ROW_SCALES):
+        assert f(A, W, 1856, 2688, A, None, None, None, fl, A, 1 << 30, None) == hs.HS_ERR_INVALID_ARG
     need = hs.hs_expert_down_sparse_workspace_size(1856, 2688)
-    assert need >= 29 * 2688 * 4
-    assert f(A, W, 1856, 2688, A, None, None, 0, A, need - 1, None) == hs.HS_ERR_WORKSPACE
-    assert f(A, W, 1856, 2688, A, None, None, 0, None, need, None) == hs.HS_ERR_WORKSPACE
+    assert need >= 2688 * 4 + 29 * 8  # one chunk's partial band per output, the group masks
+    assert f(A, W, 1856, 2688, A, None, None, None, 0, A, need - 1, None) == hs.HS_ERR_WORKSPACE
+    assert f(A, W, 1856, 2688, A, None, None, None, 0, None, need, None) == hs.HS_ERR_WORKSPACE
     assert hs.hs_expert_down_sparse_workspace_size(100, 2688) == 0
+    assert hs.hs_expert_down_sparse_workspace_size(1856, 3136) == 0
 
 
 def _layer(n_routed=4, top_k=2, hidden=256, neurons=128, shared=True, base=0x1000000):

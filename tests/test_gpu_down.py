@@ -38,15 +38,30 @@ def repack(down: synth.W4Proj):
     return codes, sb
 
 
-def run_down(h, codes, sb, N, H, flags=0):
-    ws = torch.empty(hs.hs_expert_down_sparse_workspace_size(N, H), dtype=torch.uint8, device="cuda")
+def run_down(h, codes, sb, N, H, flags=0, ws=None):
+    """One call through the C ABI; returns y (bf16, cpu), y_f32 (float64),
+    the live count and the live index list (ascending, count entries)."""
+    if ws is None:
+        ws = torch.zeros(hs.hs_expert_down_sparse_workspace_size(N, H), dtype=torch.uint8, device="cuda")
     y = torch.empty(H, dtype=torch.bfloat16, device="cuda")
     yf = torch.empty(H, dtype=torch.float32, device="cuda")
     cnt = torch.full((1,), -1, dtype=torch.int32, device="cuda")
-    hs.hs_expert_down_sparse(h.cuda().float().contiguous(), codes, sb, N, H, y, yf, cnt, flags, ws)
+    idx = torch.full((N + 1,), -7, dtype=torch.int32, device="cuda")
+    hs.hs_expert_down_sparse(h.cuda().float().contiguous(), codes, sb, N, H, y, yf, cnt, flags, ws, live_idx=idx)
     torch.cuda.synchronize()
     assert hs.hs_device_status() == hs.HS_OK
-    return y.cpu(), yf.cpu().double().numpy(), int(cnt.item())
+    c = int(cnt.item())
+    li = idx.cpu().numpy()
+    assert (li[c:] == -7).all(), "live_idx written past the live count"
+    return y.cpu(), yf.cpu().double().numpy(), c, li[:c]
+
+
+def check_live_idx(li, h, dense=False):
+    """The kernel's rows read equal the oracle's live set {n : h_n > 0}
+    (h is given, so the set is exact), ascending; every row when dense."""
+    h = np.asarray(h, dtype=np.float64)
+    want = np.arange(len(h)) if dense else np.asarray(oracle.live_set(h))
+    assert np.array_equal(li, want), (len(li), len(want))
 
 
 @pytest.mark.parametrize("H,N", [(64, 64), (128, 192), (256, 320), (2688, 1856), (2688, 3712), (3072, 128)])
@@ -61,11 +76,11 @@ def test_config1_single_expert_parity():
     """Routed expert 2688x1856, h = relu(z)^2 with about 10% live."""
     h, down = synth.single_expert_down(0)
     codes, sb = repack(down)
-    y, yf, cnt = run_down(h, codes, sb, 1856, 2688)
+    y, yf, cnt, li = run_down(h, codes, sb, 1856, 2688)
     ref = oracle.down_dense(h, down)
     check_close(yf, ref, "config 1 y_f32")
     check_bf16_within_one_ulp(y, ref, "config 1 y_bf16", yf)
-    assert cnt == len(oracle.live_set(h.double().numpy()))  # live set exact: h is given
+    check_live_idx(li, h.double().numpy())  # live set exact: h is given
 
 
 def test_twelve_neuron_golden_bit_exact():
@@ -84,20 +99,22 @@ def test_twelve_neuron_golden_bit_exact():
     codes_om = torch.from_numpy((q[:, 0::2] | (q[:, 1::2] << 4)).astype(np.uint8))
     down = synth.W4Proj(codes_om, torch.ones((H, 1), dtype=torch.float16), torch.full((H, 1), -8.0, dtype=torch.float16))
     codes, sb = repack(down)
-    y, yf, cnt = run_down(torch.from_numpy(h).float(), codes, sb, 64, H)
+    y, yf, cnt, li = run_down(torch.from_numpy(h).float(), codes, sb, 64, H)
     assert yf[:4].tolist() == rows["y"]
-    assert cnt == len(rows["live"])
+    assert li.tolist() == [int(v) for v in rows["live"]]
     assert np.array_equal(yf, oracle.down_dense(h, down))
 
 
 def test_dense_flag_equals_sparse_and_is_deterministic():
     h, down = synth.single_expert_down(0)
     codes, sb = repack(down)
-    y1, yf1, c1 = run_down(h, codes, sb, 1856, 2688)
-    y2, yf2, c2 = run_down(h, codes, sb, 1856, 2688)
-    yd, yfd, cd = run_down(h, codes, sb, 1856, 2688, flags=hs.HS_FORCE_DENSE)
-    assert np.array_equal(yf1, yf2) and torch.equal(y1, y2) and c1 == c2
+    ws = torch.zeros(hs.hs_expert_down_sparse_workspace_size(1856, 2688), dtype=torch.uint8, device="cuda")
+    y1, yf1, c1, l1 = run_down(h, codes, sb, 1856, 2688, ws=ws)
+    y2, yf2, c2, l2 = run_down(h, codes, sb, 1856, 2688, ws=ws)   # same workspace: counters back at zero
+    yd, yfd, cd, ld = run_down(h, codes, sb, 1856, 2688, flags=hs.HS_FORCE_DENSE, ws=ws)
+    assert np.array_equal(yf1, yf2) and torch.equal(y1, y2) and np.array_equal(l1, l2)
     assert np.array_equal(yf1, yfd) and torch.equal(y1, yd)
+    check_live_idx(ld, h.double().numpy(), dense=True)
     assert cd == 1856
 
 
@@ -120,9 +137,9 @@ def test_edge_cases(case):
     elif case == "group_dead":
         h[:] = rng.uniform(0.01, 2.0, N)
         h[64:128] = 0.0
-    y, yf, cnt = run_down(torch.from_numpy(h), codes, sb, N, H)
+    y, yf, cnt, li = run_down(torch.from_numpy(h), codes, sb, N, H)
     ref = oracle.down_dense(h.astype(np.float64), down)
-    assert cnt == int((h > 0).sum())
+    check_live_idx(li, h)
     if case == "all_dead":
         assert np.all(yf == 0) and torch.all(y.float() == 0)
     else:
@@ -139,11 +156,11 @@ def test_small_shapes_vs_oracle(H, N):
     rng = np.random.default_rng(H + N)
     z = rng.normal(-0.8, 1.0, N)
     h = oracle.relu2(z).astype(np.float32)
-    y, yf, cnt = run_down(torch.from_numpy(h), codes, sb, N, H)
+    y, yf, cnt, li = run_down(torch.from_numpy(h), codes, sb, N, H)
     ref = oracle.down_dense(h.astype(np.float64), down)
     check_close(yf, ref, f"{H}x{N}")
     check_bf16_within_one_ulp(y, ref, f"{H}x{N}", yf)
-    assert cnt == int((h > 0).sum())
+    check_live_idx(li, h)
 
 
 @pytest.mark.parametrize("N", [4096, 4160])
@@ -155,9 +172,30 @@ def test_dense_flag_equals_sparse_wide_experts(N):
     codes, sb = repack(down)
     z = np.random.default_rng(N).normal(-1.2815516, 1.0, N)
     h = torch.from_numpy(oracle.relu2(z).astype(np.float32))
-    y1, yf1, c1 = run_down(h, codes, sb, N, H)
-    y2, yf2, c2 = run_down(h, codes, sb, N, H)
-    yd, yfd, cd = run_down(h, codes, sb, N, H, flags=hs.HS_FORCE_DENSE)
-    assert np.array_equal(yf1, yf2) and torch.equal(y1, y2) and c1 == c2
+    y1, yf1, c1, l1 = run_down(h, codes, sb, N, H)
+    y2, yf2, c2, l2 = run_down(h, codes, sb, N, H)
+    yd, yfd, cd, ld = run_down(h, codes, sb, N, H, flags=hs.HS_FORCE_DENSE)
+    assert np.array_equal(yf1, yf2) and torch.equal(y1, y2) and np.array_equal(l1, l2)
     assert np.array_equal(yf1, yfd) and torch.equal(y1, yd)
+    check_live_idx(l1, h.numpy())
     assert cd == N
+
+
+def test_one_workspace_across_shapes_and_repeats():
+    """Every call leaves the workspace's completion counters at zero, so one
+    zero-filled workspace (sized for the largest shape) serves a sequence of
+    calls of different shapes and band counts, each equal to a call on a
+    fresh workspace."""
+    shapes = [(2688, 1856), (64, 64), (3072, 4096), (256, 320), (2688, 1856)]
+    big = max(hs.hs_expert_down_sparse_workspace_size(N, H) for H, N in shapes)
+    ws = torch.zeros(big, dtype=torch.uint8, device="cuda")
+    for i, (H, N) in enumerate(shapes):
+        down = synth.gen_proj(H, N, (3, "reuse", H, N))
+        codes, sb = repack(down)
+        z = np.random.default_rng(i).normal(-1.2815516, 1.0, N)
+        h = torch.from_numpy(oracle.relu2(z).astype(np.float32))
+        y, yf, c, li = run_down(h, codes, sb, N, H, ws=ws)
+        y0, yf0, c0, l0 = run_down(h, codes, sb, N, H)
+        assert np.array_equal(yf, yf0) and torch.equal(y, y0) and np.array_equal(li, l0)
+        check_live_idx(li, h.numpy())
+        check_close(yf, oracle.down_dense(h.double().numpy(), down), f"reuse {H}x{N}")
