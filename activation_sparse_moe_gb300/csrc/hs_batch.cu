@@ -97,6 +97,7 @@ struct BatchIO {
     float* dbg_topk_w;
     int* live_total;
     int* live_groups;
+    uint64_t* dbg_live;     // [B][Ut] live mask (h > 0) per (token, slot group), or null
     uint64_t* unit_live;    // small-batch path: live mask per unit (else null)
     int* unit_key;          // small-batch path: the unit's expert (n_routed = shared, -1 = none)
     int n_units;
@@ -428,6 +429,26 @@ __global__ void __launch_bounds__(kUpThreads, kUpCtasPerSm) batch_up_kernel(cons
             if (q == 0) {
                 if (d.shared) io.h_sh[(size_t)(d.pbase + tk) * d.N + n] = h;
                 else io.h_pair[(size_t)(d.pbase + tk) * d.N + n] = h;
+            }
+            if (io.dbg_live) {  // this token's own live bits (h > 0) for the warp's 8 rows
+                const unsigned bt = __ballot_sync(0xffffffffu, q == 0 && h > 0.f);
+                if (lane == 0 && bt) {
+                    unsigned m8 = 0;
+#pragma unroll
+                    for (int i = 0; i < 8; ++i) m8 |= ((bt >> (4 * i)) & 1u) << i;
+                    const int r8 = kUpRows * d.g + 8 * (t >> 5);  // neuron of the warp's first row
+                    const int Ut = P.shared_neurons / 64 + P.top_k * (P.routed_neurons / 64);
+                    int tok, uidx;
+                    if (d.shared) {
+                        tok = d.pbase + tk;
+                        uidx = r8 >> 6;
+                    } else {
+                        tok = __ldcg(io.pair_tok + d.pbase + tk);
+                        uidx = P.shared_neurons / 64 + (__ldcg(io.pair_slot + d.pbase + tk) - 1) * (d.N / 64) + (r8 >> 6);
+                    }
+                    uint32_t* mw = reinterpret_cast<uint32_t*>(io.dbg_live + (size_t)tok * Ut + uidx) + ((r8 & 63) >> 5);
+                    atomicOr(mw, m8 << (r8 & 31));
+                }
             }
             const unsigned bl = __ballot_sync(0xffffffffu, q == 0 && (dense || h > 0.f));
             if (lane == 0 && bl) {
@@ -1043,6 +1064,14 @@ __device__ __forceinline__ bool fused_unit(const LayerParams& P, const BatchIO& 
         bulk_g2s(sm.sbs, ep.dn_sb + (size_t)g * H, H * 4, &sm.bars[4], pol);
     }
     live = *reinterpret_cast<const uint64_t*>(sm.live8);
+    if (io.dbg_live && t < 32) {  // each token's own live set (h > 0) for this group
+        const int Ut = P.shared_neurons / 64 + P.top_k * (P.routed_neurons / 64);
+        for (int k = 0; k < T; ++k) {
+            const unsigned m0 = __ballot_sync(0xffffffffu, sm.h_s[k * 64 + t] > 0.f);
+            const unsigned m1 = __ballot_sync(0xffffffffu, sm.h_s[k * 64 + t + 32] > 0.f);
+            if (t == 0) io.dbg_live[(size_t)pick(ut.tok, k) * Ut + pick(ut.ri, k)] = (uint64_t)m1 << 32 | m0;
+        }
+    }
     // ---- per token: fixed-order sum of h
     float hsum[kFTok];
 #pragma unroll
@@ -1602,6 +1631,8 @@ int hs_batch_decode(const hs_moe_layer* L, const uint16_t* x, const float* logit
     io.dbg_topk_w = dbg ? dbg->topk_w : nullptr;
     io.live_total = dbg ? dbg->live_rows : nullptr;
     io.live_groups = dbg ? dbg->live_groups : nullptr;
+    io.dbg_live = dbg ? dbg->live_mask : nullptr;
+    if (io.dbg_live && ((uintptr_t)io.dbg_live & 7u)) return HS_ERR_MISALIGNED;
 
     int dev = 0, sms = 148;
     if (cudaGetDevice(&dev) != cudaSuccess) return HS_ERR_CUDA;
@@ -1642,6 +1673,10 @@ int hs_batch_decode(const hs_moe_layer* L, const uint16_t* x, const float* logit
     }
     if (set_smem_attr((const void*)hs::batch_up_kernel, up_smem) != HS_OK) return HS_ERR_CUDA;
     if (set_smem_attr((const void*)hs::batch_down_kernel, dn_smem) != HS_OK) return HS_ERR_CUDA;
+    if (io.dbg_live) {  // debug only: the up kernel ORs each token's bits into zeroed words
+        const int Ut = (L->shared ? L->shared->neurons / 64 : 0) + L->top_k * (L->routed[0].neurons / 64);
+        if (cudaMemsetAsync(io.dbg_live, 0, (size_t)batch * Ut * sizeof(uint64_t), s) != cudaSuccess) return HS_ERR_CUDA;
+    }
     if (launch_pdl(hs::batch_up_kernel, dim3(hs::kUpCtasPerSm * sms), dim3(hs::kUpThreads), up_smem, s, P, io) != cudaSuccess)
         return HS_ERR_CUDA;
     if (launch_pdl(hs::batch_down_kernel, dim3(2 * sms), dim3(256), dn_smem, s, P, io) != cudaSuccess)

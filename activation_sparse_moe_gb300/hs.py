@@ -48,11 +48,12 @@ class hs_moe_layer(C.Structure):
 
 class hs_decode_debug(C.Structure):
     _fields_ = [("topk_idx", C.c_void_p), ("topk_w", C.c_void_p), ("h", C.c_void_p), ("live_rows", C.c_void_p),
-                ("live_groups", C.c_void_p)]
+                ("live_groups", C.c_void_p), ("live_mask", C.c_void_p)]
 
 
 class hs_prefill_debug(C.Structure):
-    _fields_ = [("topk_idx", C.c_void_p), ("topk_w", C.c_void_p), ("tiles", C.c_void_p), ("work", C.c_void_p)]
+    _fields_ = [("topk_idx", C.c_void_p), ("topk_w", C.c_void_p), ("tiles", C.c_void_p), ("work", C.c_void_p),
+                ("live_mask", C.c_void_p), ("tile_live", C.c_void_p)]
 
 
 _lib = None
@@ -66,9 +67,9 @@ _SIGS = {
     "hs_pack_sb": (C.c_int, [C.c_void_p, C.c_void_p, C.c_int, C.c_int, C.c_void_p, C.c_void_p]),
     "hs_expert_down_sparse_workspace_size": (C.c_size_t, [C.c_int, C.c_int]),
     "hs_expert_down_sparse": (C.c_int, [C.c_void_p, C.POINTER(hs_w4), C.c_int, C.c_int, C.c_void_p, C.c_void_p,
-                                        C.c_void_p, C.c_uint, C.c_void_p, C.c_size_t, C.c_void_p]),
+                                        C.c_void_p, C.c_void_p, C.c_uint, C.c_void_p, C.c_size_t, C.c_void_p]),
     "hs_expert_down_sparse_noalloc": (C.c_int, [C.c_void_p, C.POINTER(hs_w4), C.c_int, C.c_int, C.c_void_p,
-                                                C.c_void_p, C.c_void_p, C.c_uint, C.c_void_p]),
+                                                C.c_void_p, C.c_void_p, C.c_void_p, C.c_uint, C.c_void_p]),
     "hs_moe_layer_decode_workspace_size": (C.c_size_t, [C.POINTER(hs_moe_layer), C.c_int]),
     "hs_moe_layer_decode": (C.c_int, [C.POINTER(hs_moe_layer), C.c_void_p, C.c_void_p, C.c_int, C.c_void_p,
                                       C.c_void_p, C.c_uint, C.POINTER(hs_decode_debug), C.c_void_p, C.c_size_t,
@@ -165,21 +166,24 @@ def hs_expert_down_sparse_workspace_size(neurons, out_dim) -> int:
 
 
 def hs_expert_down_sparse(h, down_codes, down_sb, neurons, out_dim, y_bf16, y_f32=None, live_count=None, flags=0,
-                          workspace=None, workspace_bytes=None, stream=None):
+                          workspace=None, workspace_bytes=None, stream=None, live_idx=None):
+    """One expert's sparse down projection.  The workspace must be zero-filled
+    before its first use (the call leaves it so)."""
     w = hs_w4(_p(down_codes), _p(down_sb))
     nb = workspace_bytes if workspace_bytes is not None else (workspace.numel() * workspace.element_size()
                                                               if workspace is not None else 0)
     _check("hs_expert_down_sparse", lib().hs_expert_down_sparse(
-        _p(h), C.byref(w), neurons, out_dim, _p(y_bf16), _p(y_f32), _p(live_count), flags, _p(workspace), nb,
-        _stream(stream)))
+        _p(h), C.byref(w), neurons, out_dim, _p(y_bf16), _p(y_f32), _p(live_idx), _p(live_count), flags,
+        _p(workspace), nb, _stream(stream)))
 
 
 def hs_expert_down_sparse_noalloc(h, down_codes, down_sb, neurons, out_dim, y_bf16, y_f32=None, live_count=None,
-                                  flags=0, stream=None):
+                                  flags=0, stream=None, live_idx=None):
     """hs_expert_down_sparse with the library's built-in scratch (no workspace)."""
     w = hs_w4(_p(down_codes), _p(down_sb))
     _check("hs_expert_down_sparse_noalloc", lib().hs_expert_down_sparse_noalloc(
-        _p(h), C.byref(w), neurons, out_dim, _p(y_bf16), _p(y_f32), _p(live_count), flags, _stream(stream)))
+        _p(h), C.byref(w), neurons, out_dim, _p(y_bf16), _p(y_f32), _p(live_idx), _p(live_count), flags,
+        _stream(stream)))
 
 
 def make_expert(up_codes, up_sb, down_codes, down_sb, offset, neurons) -> hs_expert:
@@ -214,7 +218,8 @@ def hs_moe_layer_decode(layer: Layer, x_bf16, logits, batch, y_bf16, y_f32=None,
     dbg = None
     if debug is not None:
         dbg = C.byref(hs_decode_debug(_p(debug.get("topk_idx")), _p(debug.get("topk_w")), _p(debug.get("h")),
-                                      _p(debug.get("live_rows")), _p(debug.get("live_groups"))))
+                                      _p(debug.get("live_rows")), _p(debug.get("live_groups")),
+                                      _p(debug.get("live_mask"))))
     _check("hs_moe_layer_decode", lib().hs_moe_layer_decode(
         layer.ref, _p(x_bf16), _p(logits), batch, _p(y_bf16), _p(y_f32), flags, dbg, _p(workspace), nb,
         _stream(stream)))
@@ -241,7 +246,8 @@ def hs_moe_prefill(layer: Layer, x_bf16, logits, tokens, y_bf16, y_f32=None, fla
     dbg = None
     if debug is not None:
         dbg = C.byref(hs_prefill_debug(_p(debug.get("topk_idx")), _p(debug.get("topk_w")), _p(debug.get("tiles")),
-                                       _p(debug.get("work"))))
+                                       _p(debug.get("work")), _p(debug.get("live_mask")),
+                                       _p(debug.get("tile_live"))))
     _check("hs_moe_prefill", lib().hs_moe_prefill(
         layer.ref, _p(x_bf16), _p(logits), tokens, _p(y_bf16), _p(y_f32), flags, dbg, _p(workspace), nb,
         _stream(stream)))

@@ -119,6 +119,15 @@ typedef struct {
                           all (token group, expert) pairs                    */
     int*   live_groups;/* int: 64-neuron groups whose (scale, bias) slab the
                           call read, summed the same way                     */
+    uint64_t* live_mask;/* [batch][units] the live sets (section "Our way reads
+                          only the rows that fired": neuron n of an expert is
+                          live for a token when h_n > 0), one 64-bit word per
+                          (token, slot, group of 64 neurons); units = shared
+                          neurons/64 + top_k * routed neurons/64, shared
+                          groups first, then the chosen experts' groups in
+                          topk order; bit r of a group's word = its neuron r.
+                          The live set does not depend on HS_FORCE_DENSE
+                          (which only makes every row be read).            */
 } hs_decode_debug;
 
 /* Human-readable text of a status code (static storage). */
@@ -163,11 +172,23 @@ int hs_pack_sb(const uint16_t* scale_dev, const uint16_t* bias_dev, int rows, in
  *   h_dev        [neurons] fp32, h >= 0 (ReLU^2 outputs); h_n > 0 means live
  *   y_bf16_dev   [out_dim] bf16 (round to nearest even), required
  *   y_f32_dev    [out_dim] fp32 pre-rounding sums, or NULL
- *   live_count_dev  int: number of live rows read, or NULL
+ *   live_idx_dev [neurons] int: the indices of the rows read, ascending
+ *                (the live set {n : h_n > 0}; every row with HS_FORCE_DENSE);
+ *                entries past *live_count are left untouched; or NULL
+ *   live_count_dev  int: number of rows read, or NULL
+ * neurons a multiple of 64 up to 65536; out_dim a multiple of 64 up to 3072.
+ * Flags: HS_FORCE_DENSE only (else HS_ERR_INVALID_ARG).
+ * Workspace: hs_expert_down_sparse_workspace_size bytes, ZERO-FILLED before
+ * its first use.  Experts of more than 2048 neurons use it: the partial sums
+ * of their 32-group chunks and one completion counter per 64-output band,
+ * kept at the start of the workspace for every shape; each call leaves the
+ * counters at zero again, so consecutive calls of any shapes the workspace is
+ * large enough for (and CUDA graph replays) need no clearing in between.  A
+ * workspace another entry point has written must be zero-filled again first.
  * Deterministic: the same inputs give bit-identical outputs. */
 size_t hs_expert_down_sparse_workspace_size(int neurons, int out_dim);
 int hs_expert_down_sparse(const float* h_dev, const hs_w4* down_nm, int neurons, int out_dim,
-                          uint16_t* y_bf16_dev, float* y_f32_dev, int* live_count_dev,
+                          uint16_t* y_bf16_dev, float* y_f32_dev, int* live_idx_dev, int* live_count_dev,
                           unsigned flags, void* workspace_dev, size_t workspace_bytes,
                           hs_stream_t stream);
 
@@ -177,17 +198,24 @@ int hs_expert_down_sparse(const float* h_dev, const hs_w4* down_nm, int neurons,
  * or a path that must never enter the CUDA allocator.  The page has no
  * counterpart; this is an interface convenience of this library.
  *   Same arguments and results as hs_expert_down_sparse, minus the workspace.
- *   Scratch: a fixed array inside the library (about 0.75 MB on every GPU
- *   that loads it, held until the process exits), sized for at most 4096
- *   neurons and out_dim 3072; larger shapes return HS_ERR_UNSUPPORTED_SHAPE.
+ *   Scratch: a fixed array inside the library (about 0.4 MB on every GPU
+ *   that loads it, held until the process exits), sized for the largest
+ *   shape the workspace entry point takes (65536 neurons, out_dim 3072);
+ *   larger shapes return HS_ERR_UNSUPPORTED_SHAPE.  An expert of at most
+ *   2048 neurons runs in one pass and does not touch it; wider experts keep
+ *   their partial sums and completion counters there.
  *   Allocates nothing (no cudaMalloc, no allocating library routine).
- *   The first call on each device looks up the array's device address once
- *   (cudaGetSymbolAddress); make that first call before any stream capture.
- *   Every call shares the one array and overwrites it (nothing in it needs to
- *   start at zero): calls that can overlap on the GPU, on different streams,
- *   race with each other; order them on one stream or with events. */
+ *   The first call in each CUDA context looks up the array's device address
+ *   (cudaGetSymbolAddress) and caches it under the context's unique id; make
+ *   that first call before any stream capture.  A context created later (for
+ *   instance after a device reset) gets its own lookup on its first call.
+ *   Every call shares the one array: its counters start at zero when the
+ *   library loads and every call leaves them at zero; the partial sums are
+ *   overwritten before they are read.  Calls that can overlap on the GPU, on
+ *   different streams, race with each other; order them on one stream or
+ *   with events. */
 int hs_expert_down_sparse_noalloc(const float* h_dev, const hs_w4* down_nm, int neurons, int out_dim,
-                                  uint16_t* y_bf16_dev, float* y_f32_dev, int* live_count_dev,
+                                  uint16_t* y_bf16_dev, float* y_f32_dev, int* live_idx_dev, int* live_count_dev,
                                   unsigned flags, hs_stream_t stream);
 
 /* ------------------------------------------------- row-scale re-quantising
@@ -284,6 +312,17 @@ typedef struct {
                          neurons the down product multiplied (64 per tile
                          not skipped), [2] all of the expert's neurons.
                          Down-product flops = 2 * hidden * each entry.     */
+    uint64_t* live_mask; /* [tokens][units] the kernel's live sets (h > 0 in
+                         its fp16 h), laid out as hs_decode_debug.live_mask */
+    uint64_t* tile_live; /* [tiles] per (expert, token tile): bit j set when
+                         the down product multiplies 64-neuron tile j (some
+                         token of the tile has a live neuron in it, or
+                         HS_FORCE_DENSE).  Tiles: the routed experts that
+                         have tokens, ascending, each expert's (token, slot)
+                         pairs in token order cut into tiles of 128, then
+                         the shared expert's tokens in tiles of 128; at most
+                         n_routed + ceil(tokens * top_k / 128) +
+                         ceil(tokens / 128) entries are written.           */
 } hs_prefill_debug;
 
 size_t hs_moe_prefill_workspace_size(const hs_moe_layer* layer, int tokens);

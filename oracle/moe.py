@@ -194,25 +194,29 @@ def moe_tokens(X, logits, routed, shared, k: int = 6) -> dict:
     X: [T][H]; logits: [T][E].  The per-token definition of moe_layer, with
     every expert's products evaluated for all of its tokens at once.
     Returns dict(out fp64 [T][H], idx [T][k], w [T][k],
-    h={e: (token ids, h [t][N])}, h_shared [T][N] or None)."""
+    h={e: (token ids, h [t][N])}, h_shared [T][N] or None, and the
+    pre-activations z={e: z [t][N]}, z_shared [T][N] or None)."""
     X = as_f64(X)
     T = X.shape[0]
     idx, w = router_topk(logits, k)
     out = np.zeros_like(X)
-    hs = None
+    hs = zs = None
     if shared is not None:
-        hs = relu2(up_preact(X, shared.up, shared.offset))
+        zs = up_preact(X, shared.up, shared.offset)
+        hs = relu2(zs)
         out += hs @ dequant(shared.down).T
-    hmap = {}
+    hmap, zmap = {}, {}
     for e in np.unique(idx):
         e = int(e)
         toks, slot = np.nonzero(idx == e)
         ex = routed(e)
-        h = relu2(up_preact(X[toks], ex.up, ex.offset))
+        z = up_preact(X[toks], ex.up, ex.offset)
+        h = relu2(z)
         y = h @ dequant(ex.down).T
         out[toks] += w[toks, slot][:, None] * y
         hmap[e] = (toks, h)
-    return {"out": out, "idx": idx, "w": w, "h": hmap, "h_shared": hs}
+        zmap[e] = z
+    return {"out": out, "idx": idx, "w": w, "h": hmap, "h_shared": hs, "z": zmap, "z_shared": zs}
 
 
 _BF16_MAX = (2.0 - 2.0 ** -7) * 2.0 ** 127

@@ -96,3 +96,117 @@ def check_bf16_rounding(y_bf16: torch.Tensor, y_f32, ref: np.ndarray, what=""):
     err = np.abs(yb - ref)
     assert (err <= bound).all(), f"{what}: bf16 error {err.max():.3e} above the bar"
     return float((np.abs(yb - oracle.bf16_rne(ref)) / (2 * half_ulp)).max())
+
+
+# ------------------------------------------------------------------ live sets
+def mask_bits(words) -> np.ndarray:
+    """64-bit live-mask words [..., units] -> bool [..., units * 64] (bit r of
+    word u = neuron 64u + r of that slot)."""
+    w = np.asarray(words).astype(np.uint64)
+    bits = (w[..., None] >> np.arange(64, dtype=np.uint64)) & np.uint64(1)
+    return bits.reshape(w.shape[:-1] + (w.shape[-1] * 64,)).astype(bool)
+
+
+def _abs_terms(up, x):
+    """Per neuron: sum_k (|s| q + |b|) |x_k| and sum_k |w_nk|, and per-group
+    sums of |w| (the magnitudes every rounding of the up product scales)."""
+    q = oracle.unpack_codes(up.codes).astype(np.float64)
+    s = np.repeat(np.abs(oracle.as_f64(up.scale)), 64, axis=-1)
+    b = np.repeat(np.abs(oracle.as_f64(up.bias)), 64, axis=-1)
+    xa = np.abs(oracle.as_f64(x))
+    w = np.abs(oracle.dequant(up))
+    return (s * q + b) @ xa, w @ xa, w
+
+
+def z_bound_cuda_core(x, up, offset=None) -> np.ndarray:
+    """Per neuron, an upper bound of |z_kernel - z_oracle| for the CUDA-core
+    up product: x as a 16-bit fixed-point copy per 64-input group (an element
+    is off by at most 2^(E-16), max|x_g| < 2^E), integer dot products (exact),
+    the group's scale and bias applied and the groups summed in fp32
+    ((H + 64) 2^-24 of the magnitudes involved), the offset added in fp32."""
+    xf = oracle.as_f64(x)
+    H = xf.shape[-1]
+    split, _, w = _abs_terms(up, xf)
+    mx = np.abs(xf).reshape(-1, 64).max(axis=1)
+    E = np.where(mx > 0, np.floor(np.log2(np.where(mx > 0, mx, 1.0))) + 1, -100)
+    fixed = w.reshape(w.shape[0], -1, 64).sum(axis=2) @ np.ldexp(1.0, (E - 16).astype(int))
+    off = 0.0 if offset is None else np.abs(oracle.as_f64(offset))
+    return 2.0 * ((H + 64) * 2.0 ** -24 * split + fixed + 2.0 ** -24 * off)
+
+
+def z_bound_fp16_operands(x, up, offset=None) -> np.ndarray:
+    """The same for the tensor-core products: the weight dequantised to fp16
+    by one rounding (2^-11 relative, 2^-25 absolute below fp16's normal
+    range), x converted bf16 -> fp16 (exact in the normal range, 2^-25
+    below), fp32 accumulation in the tensor core ((H + 64) 2^-23 of
+    sum |w||x|), the offset added in fp32."""
+    xf = oracle.as_f64(x)
+    H = xf.shape[-1]
+    _, wx, w = _abs_terms(up, xf)
+    off = 0.0 if offset is None else np.abs(oracle.as_f64(offset))
+    rnd = 2.0 ** -11 * wx + 2.0 ** -25 * (w.sum(axis=1) + np.abs(xf).sum())
+    return 2.0 * (rnd + (H + 64) * 2.0 ** -23 * wx + 2.0 ** -24 * off)
+
+
+def live_in_precision(z, kind) -> np.ndarray:
+    """The oracle's live decision taken in the kernel's precision: h = z^2
+    (z > 0) rounded to fp32 ("fp32", CUDA-core kernels) or to fp16 ("fp16",
+    the tensor-core kernels store h as fp16; a positive z below about
+    2^-12.5 gives h = 0, a dead neuron).  h > 0 decides."""
+    zz = np.where(z > 0, z * z, 0.0)
+    return (zz.astype(np.float16 if kind == "fp16" else np.float32) > 0)
+
+
+def check_token_live_masks(words, X, ref, shared, routed_expert, NR, K, kind, what):
+    """Element-wise live-set parity of a batch call: the kernel's live mask of
+    every (token, slot, neuron) equals the oracle's {h > 0}, except neurons
+    whose oracle |z| lies within the kind's rounding bound ("fp32": CUDA-core
+    kernels, "fp16": tensor-core kernels), which may flip.  words: [B][Ut]
+    uint64 from the call's live_mask output (shared groups first, then the
+    slots in topk order); shared: the shared Expert or None; routed_expert:
+    descriptor index -> Expert.  The oracle's side of the decision is
+    live_in_precision (h rounded as the kernel stores it).  Returns the
+    number of flipped neurons."""
+    bound_fn = z_bound_cuda_core if kind == "fp32" else z_bound_fp16_operands
+    got = mask_bits(np.asarray(words))
+    X = oracle.as_f64(X)
+    B = X.shape[0]
+    NS = shared.neurons if shared is not None else 0
+    flips = 0
+    for b in range(B):
+        slots = []
+        if NS:
+            slots.append((shared, ref["z_shared"][b], ref["h_shared"][b], 0))
+        for j in range(K):
+            e = int(ref["idx"][b][j])
+            toks, h = ref["h"][e]
+            r = int(np.flatnonzero(toks == b)[0])
+            slots.append((routed_expert(e), ref["z"][e][r], h[r], NS + j * NR))
+        for ex, z, h, base in slots:
+            n = ex.neurons
+            mism = got[b, base:base + n] != live_in_precision(z, kind)
+            if mism.any():
+                bound = bound_fn(X[b], ex.up, ex.offset)
+                bad = np.abs(z[mism]) > bound[mism]
+                assert not bad.any(), (f"{what}: token {b}: live-set mismatch beyond the {kind} bound at "
+                                       f"neurons {np.flatnonzero(mism)[bad][:8]}, |z| {np.abs(z[mism])[bad][:4]}")
+                flips += int(mism.sum())
+    return flips
+
+
+def union_counts_from_masks(words, idx, NS, NR, K):
+    """Rows and 64-neuron groups of the per-expert union of the kernel's own
+    live masks (each expert once, the shared expert over every token)."""
+    got = np.asarray(words).astype(np.uint64)
+    B = got.shape[0]
+    NGs, NGr = NS // 64, NR // 64
+    per = {}
+    for b in range(B):
+        if NS:
+            per["s"] = per.get("s", np.zeros(NGs, np.uint64)) | got[b, :NGs]
+        for j in range(K):
+            e = int(idx[b][j])
+            per[e] = per.get(e, np.zeros(NGr, np.uint64)) | got[b, NGs + j * NGr:NGs + (j + 1) * NGr]
+    rows = sum(int(mask_bits(v).sum()) for v in per.values())
+    groups = sum(int((v != 0).sum()) for v in per.values())
+    return rows, groups

@@ -10,7 +10,7 @@ import torch
 
 import oracle
 import synth
-from _util import check_bf16_within_one_ulp, check_close, live_flip_bound
+from _util import check_bf16_within_one_ulp, check_close, mask_bits, z_bound_cuda_core
 from activation_sparse_moe_gb300 import hs
 from activation_sparse_moe_gb300.layer import DeviceLayer, from_synth_expert, from_synth_stack
 
@@ -40,7 +40,8 @@ def run_layer(dl: DeviceLayer, x, lg, flags=0):
            "topk_w": torch.zeros(dl.top_k, dtype=torch.float32, device="cuda"),
            "h": torch.full((NS + dl.top_k * dl.routed.N,), -1.0, dtype=torch.float32, device="cuda"),
            "live_rows": torch.full((1,), -1, dtype=torch.int32, device="cuda"),
-           "live_groups": torch.full((1,), -1, dtype=torch.int32, device="cuda")}
+           "live_groups": torch.full((1,), -1, dtype=torch.int32, device="cuda"),
+           "live_mask": torch.full(((NS + dl.top_k * dl.routed.N) // 64,), -1, dtype=torch.int64, device="cuda")}
     hs.hs_moe_layer_decode(dl.c, x.reshape(-1).cuda(), lg.reshape(-1).cuda(), 1, y, yf, flags, dbg, ws)
     torch.cuda.synchronize()
     assert hs.hs_device_status() == hs.HS_OK
@@ -54,8 +55,10 @@ def check_layer(L: synth.LayerInputs, dl, x, lg, top_k, what):
     assert dbg["topk_idx"].tolist() == ref["idx"].tolist(), what
     np.testing.assert_allclose(dbg["topk_w"].double().numpy(), ref["w"], rtol=2e-6, atol=1e-7)
     # live sets: the kernel's own h > 0 equals the oracle's, except where the
-    # oracle's |z| is within fp32 accumulation error of 0
+    # oracle's |z| is within the CUDA-core up product's rounding bound of 0
     hk = dbg["h"].double().numpy()
+    # the live-set output is exactly the kernel's own h > 0, neuron by neuron
+    assert np.array_equal(mask_bits(dbg["live_mask"].numpy().view(np.uint64)), hk > 0), what
     NS = L.shared.neurons if L.shared is not None else 0
     slots = ([(L.shared, ref["shared"], 0)] if L.shared is not None else []) + [
         (L.routed_expert(int(e)), ref["experts"][int(e)], NS + j * L.up.codes.shape[1])
@@ -71,9 +74,9 @@ def check_layer(L: synth.LayerInputs, dl, x, lg, top_k, what):
         live_groups += int((hg.reshape(-1, 64) > 0).any(axis=1).sum())
         mism = (hg > 0) != (r["h"] > 0)
         if mism.any():
-            bound = live_flip_bound(x.reshape(-1), ex.up)
+            bound = z_bound_cuda_core(x.reshape(-1), ex.up, ex.offset)
             zmag = np.abs(r["z"])
-            assert (zmag[mism] <= bound[mism]).all(), f"{what}: live-set mismatch beyond fp32 bound"
+            assert (zmag[mism] <= bound[mism]).all(), f"{what}: live-set mismatch beyond the rounding bound"
             flips += int(mism.sum())
         check_close(hg, r["h"], f"{what} h")
     assert int(dbg["live_rows"].item()) == live_total
@@ -122,6 +125,7 @@ def test_full_layer_dense_flag_and_determinism(full_layer):
     assert np.array_equal(yf1, yf2) and torch.equal(y1, y2)
     assert np.array_equal(yf1, yfd) and torch.equal(y1, yd)
     assert int(dd["live_rows"].item()) == 3712 + 6 * 1856
+    assert torch.equal(dd["live_mask"], d1["live_mask"])  # the live set, not the rows the dense flag reads
     frac = int(d1["live_rows"].item()) / (3712 + 6 * 1856)
     assert 0.07 < frac < 0.13
 
@@ -154,3 +158,46 @@ def test_bounded_wait_gives_up_and_reports():
     L = synth.layer_inputs(9, "t-after-timeout", 0, E, NR, NS, H, p=0.3, p_shared=0.3)
     X, LG = synth.tokens(9, "t-after-timeout", 0, 1, H, E)
     check_layer(L, make_layer(L, K), X[0], LG[0], K, "after timeout")
+
+
+def test_up_gemv_mixed_magnitude_x_within_fixed_point_bound():
+    """The up GEMV takes x as a 16-bit fixed-point copy with one exponent per
+    64-input group, so inputs far below their group's maximum lose bits.
+    Every group here holds one large input (64) and small ones (~2^-6), and
+    every neuron is made live (offset 10 times the spread of z), so the
+    kernel's z = sqrt(h) can be compared with the oracle's neuron by neuron:
+    the difference stays within the bound that adds the fixed-point rounding
+    (2^(E-16) per input, max |x_g| < 2^E) to the fp32 rounding."""
+    from _util import z_bound_cuda_core
+    H, E, NR, NS, K = 512, 4, 128, 128, 2
+    L = synth.layer_inputs(11, "t-mixed", 0, E, NR, NS, H, p=0.5, p_shared=0.5)
+    rng = np.random.default_rng(11)
+    xs = rng.normal(0.0, 2.0 ** -6, H)
+    xs[rng.integers(0, 64, H // 64) + 64 * np.arange(H // 64)] = 64.0 * rng.choice([-1.0, 1.0], H // 64)
+    x = torch.from_numpy(xs.astype(np.float32)).to(torch.bfloat16)
+    lg = synth.normal_f32((1, E), 11, "t-mixed", "logits")
+    xv = oracle.as_f64(x)
+
+    def live_offsets(up):
+        w = oracle.dequant(up)
+        return torch.from_numpy((10.0 * np.sqrt((w * w) @ (xv * xv))).astype(np.float32))
+
+    for e in range(E):
+        L.offsets[e] = live_offsets(L.routed_expert(e).up)
+    L.shared = synth.Expert(L.shared.up, L.shared.down, live_offsets(L.shared.up))
+    dl = make_layer(L, K)
+    y, yf, dbg = run_layer(dl, x, lg)
+    ref = oracle.moe_layer(x, lg.reshape(-1), L.routed_expert, L.shared, k=K)
+    hk = dbg["h"].double().numpy()
+    assert (hk > 0).all()
+    slots = [(L.shared, ref["shared"], 0)] + [(L.routed_expert(int(e)), ref["experts"][int(e)], NS + j * NR)
+                                              for j, e in enumerate(ref["idx"])]
+    worst = 0.0
+    for ex, r, base in slots:
+        zk = np.sqrt(hk[base:base + ex.neurons])
+        bound = z_bound_cuda_core(x, ex.up, ex.offset) + 2.0 ** -22 * np.abs(r["z"])
+        err = np.abs(zk - r["z"])
+        assert (err <= bound).all(), f"z error {err.max():.3e} beyond the fixed-point + fp32 bound"
+        worst = max(worst, float((err / bound).max()))
+    check_close(yf, ref["out"], "mixed-magnitude x y_f32")
+    print(f"mixed-magnitude x: largest z error {worst:.3f} of its bound")

@@ -9,9 +9,12 @@ tokens, top-6 of 128 plus the shared expert, 30% of every expert's neurons
 permanently dead, p = 0.1 on the rest.
 
 The tile skip must not change the result: the sparse call equals the
-HS_FORCE_DENSE call bit for bit, and the number of skipped 64-neuron tiles
-matches the oracle's count of tiles whose h is zero for every token of the
-tile (up to neurons within rounding of zero).
+HS_FORCE_DENSE call bit for bit.  Live sets are checked element by element:
+each (token, slot, neuron) of the kernel's live mask equals the oracle's
+h > 0 except neurons whose oracle |z| lies within the rounding bound of the
+fp16-operand products; every token tile's multiplied 64-neuron tiles equal
+the union of its tokens' masks, and the skip and work counts follow from
+those masks exactly.
 """
 import numpy as np
 import pytest
@@ -19,7 +22,7 @@ import torch
 
 import oracle
 import synth
-from _util import check_bf16_rounding, check_close
+from _util import check_bf16_rounding, check_close, check_token_live_masks, mask_bits
 from activation_sparse_moe_gb300 import hs
 from activation_sparse_moe_gb300.layer import DeviceLayer, from_synth_expert, from_synth_stack
 
@@ -41,7 +44,16 @@ def make_layer(L, top_k):
     return DeviceLayer(routed, shared, top_k)
 
 
-def run_prefill(dl, X, LG, flags=0):
+def units_of(dl):
+    NS = dl.shared.N if dl.shared is not None else 0
+    return NS // 64 + dl.top_k * (dl.routed.N // 64)
+
+
+def max_tiles(dl, T):
+    return dl.routed.E + (T * dl.top_k + TILE - 1) // TILE + (T + TILE - 1) // TILE
+
+
+def run_prefill(dl, X, LG, flags=0, masks=True):
     T, H = X.shape
     ws = torch.zeros(dl.prefill_workspace_size(T), dtype=torch.uint8, device="cuda")
     assert ws.numel() > 0
@@ -51,51 +63,75 @@ def run_prefill(dl, X, LG, flags=0):
            "topk_w": torch.zeros((T, dl.top_k), dtype=torch.float32, device="cuda"),
            "tiles": torch.full((2,), -1, dtype=torch.int32, device="cuda"),
            "work": torch.full((3,), -1, dtype=torch.int64, device="cuda")}
+    if masks:
+        dbg["live_mask"] = torch.full((T, units_of(dl)), -1, dtype=torch.int64, device="cuda")
+        dbg["tile_live"] = torch.full((max_tiles(dl, T),), -1, dtype=torch.int64, device="cuda")
     hs.hs_moe_prefill(dl.c, X.cuda(), LG.cuda(), T, y, yf, flags, dbg, ws)
     torch.cuda.synchronize()
     assert hs.hs_device_status() == hs.HS_OK
     return y.cpu(), yf.cpu().double().numpy(), {k: v.cpu() for k, v in dbg.items()}
 
 
-def oracle_tiles(ref, n_routed_neurons, n_shared_neurons, T):
-    """Over (expert, token tile) pairs (an expert's tokens in ascending order,
-    cut into tiles of TILE tokens): 64-neuron down tiles skipped and
-    considered, and the tokens x (union-live, multiplied, all) neurons sums."""
-    skipped = total = union = execd = dense = 0
-    mats = [h for (_toks, h) in ref["h"].values()]
-    if ref["h_shared"] is not None:
-        mats.append(ref["h_shared"])
-    for h in mats:
-        for r in range(0, h.shape[0], TILE):
-            ht = h[r:r + TILE]
-            rows = (ht > 0).any(axis=0)
-            live = rows.reshape(-1, 64).any(axis=1)
-            total += live.size
-            skipped += int((~live).sum())
-            union += ht.shape[0] * int(rows.sum())
-            execd += ht.shape[0] * 64 * int(live.sum())
-            dense += ht.shape[0] * ht.shape[1]
-    return skipped, total, union, execd, dense
+def kernel_tiles(dl, idx, words):
+    """The library's token tiles rebuilt from the routing (the routed experts
+    with tokens ascending, each expert's tokens in order cut into tiles of
+    TILE, then the shared expert's tokens), with, per tile, the union over its
+    tokens of the kernel's own live masks: (n_tokens, group words [NK],
+    union-live neurons, NK)."""
+    T, K = idx.shape
+    NS = dl.shared.N if dl.shared is not None else 0
+    NGs, NGr = NS // 64, dl.routed.N // 64
+    out = []
+    for e in range(dl.routed.E):
+        toks, slots = np.nonzero(idx == e)
+        for r in range(0, len(toks), TILE):
+            w = np.zeros(NGr, np.uint64)
+            for b, j in zip(toks[r:r + TILE], slots[r:r + TILE]):
+                w |= words[b, NGs + j * NGr:NGs + (j + 1) * NGr]
+            out.append((len(toks[r:r + TILE]), w, NGr))
+    if NS:
+        for r in range(0, T, TILE):
+            w = np.bitwise_or.reduce(words[r:r + TILE, :NGs], axis=0)
+            out.append((min(TILE, T - r), w, NGs))
+    return out
 
 
-def check_prefill(L, dl, X, LG, K, what, tile_slack=2):
+def check_tiles_from_masks(dl, dbg, what, dense=False):
+    """Each tile's multiplied 64-neuron tiles are exactly the groups where the
+    union of its tokens' masks has a live neuron (all of them with the dense
+    flag); the skip and work counts follow."""
+    words = dbg["live_mask"].numpy().view(np.uint64)
+    tl = dbg["tile_live"].numpy().view(np.uint64)
+    tiles = kernel_tiles(dl, dbg["topk_idx"].numpy(), words)
+    skipped = total = union = execd = dense_w = 0
+    for i, (nt, w, NK) in enumerate(tiles):
+        gl = (w != 0)
+        want = sum(1 << int(j) for j in np.flatnonzero(gl)) if not dense else (1 << NK) - 1
+        assert int(tl[i]) == want, (what, i, hex(int(tl[i])), hex(want))
+        total += NK
+        skipped += NK - int(bin(want).count("1"))
+        union += nt * int(mask_bits(w[None])[0].sum())
+        execd += nt * 64 * int(bin(want).count("1"))
+        dense_w += nt * 64 * NK
+    assert [int(v) for v in dbg["tiles"]] == [skipped, total], what
+    assert [int(v) for v in dbg["work"]] == [union, execd, dense_w], what
+    return skipped
+
+
+def check_prefill(L, dl, X, LG, K, what, flips_allowed=4):
     y, yf, dbg = run_prefill(dl, X, LG)
     ref = oracle.moe_tokens(X, LG, L.routed_expert, L.shared, k=K)
     assert np.array_equal(dbg["topk_idx"].numpy(), ref["idx"]), what
     np.testing.assert_allclose(dbg["topk_w"].double().numpy(), ref["w"], rtol=2e-6, atol=1e-7)
     rel, mx = check_close(yf, ref["out"], f"{what} y_f32")
     ulps = check_bf16_rounding(y, yf, ref["out"], what)
-    print(f"{what}: rel-L2 {rel:.2e} max-abs/max {mx:.2e} bf16 max ulps from RNE(oracle) {ulps:.0f}")
-    NS = L.shared.neurons if L.shared is not None else 0
-    sk, tot, union, execd, dense = oracle_tiles(ref, L.up.codes.shape[1], NS, X.shape[0])
-    assert int(dbg["tiles"][1]) == tot, what
-    assert abs(int(dbg["tiles"][0]) - sk) <= tile_slack, (what, int(dbg["tiles"][0]), sk)
-    w = [int(v) for v in dbg["work"]]
-    assert w[2] == dense, what
-    # a neuron whose h rounds differently near 0 moves the union by at most one tile's tokens
-    assert abs(w[0] - union) <= tile_slack * TILE, (what, w[0], union)
-    assert abs(w[1] - execd) <= tile_slack * TILE * 64, (what, w[1], execd)
-    assert w[0] <= w[1] <= w[2]
+    words = dbg["live_mask"].numpy().view(np.uint64)
+    flips = check_token_live_masks(words, X, ref, L.shared, L.routed_expert, dl.routed.N, K, "fp16", what)
+    print(f"{what}: rel-L2 {rel:.2e} max-abs/max {mx:.2e} bf16 max ulps from RNE(oracle) {ulps:.0f}, "
+          f"live-set flips within the fp16 bound {flips}")
+    n_neurons = X.shape[0] * ((L.shared.neurons if L.shared is not None else 0) + K * dl.routed.N)
+    assert flips <= flips_allowed + n_neurons // 2000, (what, flips)
+    check_tiles_from_masks(dl, dbg, what)
     return y, yf, dbg
 
 
@@ -152,6 +188,10 @@ def test_dense_flag_bit_identical_and_deterministic():
     assert np.array_equal(yf1, yfd) and torch.equal(y1, yd)
     assert int(dd["tiles"][0]) == 0 and int(d1["tiles"][0]) > 0
     assert int(dd["tiles"][1]) == int(d1["tiles"][1])
+    # the live sets do not depend on the flag; the dense call multiplies every tile
+    assert torch.equal(d1["live_mask"], dd["live_mask"]) and torch.equal(d1["live_mask"], d2["live_mask"])
+    check_tiles_from_masks(dl, d1, "sparse")
+    check_tiles_from_masks(dl, dd, "dense flag", dense=True)
 
 
 def test_prefill_argument_errors():
@@ -193,7 +233,13 @@ def test_config5_sampled_parity(cfg5):
     assert np.array_equal(dbg["topk_idx"].numpy()[sample], ref["idx"])
     rel, mx = check_close(yf[sample], ref["out"], "config 5 sampled y_f32")
     ulps = check_bf16_rounding(y[sample], yf[sample], ref["out"], "config 5 sampled")
-    print(f"config 5 sampled: rel-L2 {rel:.2e} max-abs/max {mx:.2e} bf16 max ulps {ulps:.0f}")
+    words = dbg["live_mask"].numpy().view(np.uint64)
+    flips = check_token_live_masks(words[sample], X[sample], ref, L.shared, L.routed_expert, synth.N_ROUTED, 6,
+                                   "fp16", "config 5 sampled")
+    print(f"config 5 sampled: rel-L2 {rel:.2e} max-abs/max {mx:.2e} bf16 max ulps {ulps:.0f} flips {flips}")
+    assert flips <= 4 + len(sample) * (synth.N_SHARED + 6 * synth.N_ROUTED) // 2000
+    skipped = check_tiles_from_masks(dl, dbg, "config 5")
+    print(f"config 5: skipped 64-neuron tiles {skipped}")
     # every (expert, token tile) pair is counted once: 58-tile shared expert + 29 tiles per routed tile
     counts = np.bincount(dbg["topk_idx"].numpy().ravel(), minlength=128)
     tiles = int(sum((c + TILE - 1) // TILE for c in counts)) * (synth.N_ROUTED // 64)
@@ -204,8 +250,8 @@ def test_config5_sampled_parity(cfg5):
 
 def test_config5_dense_flag_equal(cfg5):
     L, dl, X, LG = cfg5
-    y1, yf1, d1 = run_prefill(dl, X, LG)
-    yd, yfd, dd = run_prefill(dl, X, LG, flags=hs.HS_FORCE_DENSE)
+    y1, yf1, d1 = run_prefill(dl, X, LG, masks=False)
+    yd, yfd, dd = run_prefill(dl, X, LG, flags=hs.HS_FORCE_DENSE, masks=False)
     assert np.array_equal(yf1, yfd) and torch.equal(y1, yd)
     assert int(dd["tiles"][0]) == 0
 
@@ -226,8 +272,35 @@ def test_config5_layer_at_max_tokens(cfg5):
     assert np.array_equal(dbg["topk_idx"].numpy()[sample], ref["idx"])
     rel, mx = check_close(yf[sample], ref["out"], "4096 tokens sampled y_f32")
     check_bf16_rounding(y[sample], yf[sample], ref["out"], "4096 tokens sampled")
+    words = dbg["live_mask"].numpy().view(np.uint64)
+    check_token_live_masks(words[sample], X[sample], ref, L.shared, L.routed_expert, synth.N_ROUTED, 6, "fp16",
+                           "4096 tokens sampled")
+    check_tiles_from_masks(dl, dbg, "4096 tokens")
     counts = np.bincount(dbg["topk_idx"].numpy().ravel(), minlength=128)
     tiles = int(sum((c + TILE - 1) // TILE for c in counts)) * (synth.N_ROUTED // 64)
     tiles += (T // TILE) * (synth.N_SHARED // 64)
     assert int(dbg["tiles"][1]) == tiles
     assert np.isfinite(yf).all()
+
+
+def test_config5_repeated_calls_bit_identical(cfg5):
+    """Determinism under repetition: the full-size prefill called 16 times on
+    the same inputs (fresh and reused workspaces alternating) gives the same
+    bits every time."""
+    L, dl, X, LG = cfg5
+    T, H = X.shape
+    Xc, LGc = X.cuda(), LG.cuda()
+    ws_keep = torch.zeros(dl.prefill_workspace_size(T), dtype=torch.uint8, device="cuda")
+    ref = None
+    for i in range(16):
+        ws = ws_keep if i % 2 else torch.zeros_like(ws_keep)
+        yf = torch.empty((T, H), dtype=torch.float32, device="cuda")
+        y = torch.empty((T, H), dtype=torch.bfloat16, device="cuda")
+        hs.hs_moe_prefill(dl.c, Xc, LGc, T, y, yf, 0, None, ws)
+        torch.cuda.synchronize()
+        if ref is None:
+            ref = yf.clone()
+        else:
+            bad = (yf != ref).any(dim=1).nonzero().flatten().tolist()
+            assert not bad, f"call {i}: {len(bad)} tokens differ from the first call"
+    assert hs.hs_device_status() == hs.HS_OK
