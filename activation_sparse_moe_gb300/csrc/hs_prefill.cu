@@ -77,6 +77,8 @@ struct PrefillIO {
     float* dbg_w;
     int* dbg_tiles;           // [2] skipped, total
     long long* dbg_work;      // [3] union_rt, exec_rt, dense_rt
+    uint64_t* dbg_live;       // [T][Ut] live mask (fp16 h > 0) per (token, slot group), or null
+    uint64_t* dbg_tile_live;  // [tiles] 64-neuron tiles the down product multiplies, or null
     int max_tiles;
 };
 
@@ -284,8 +286,8 @@ constexpr unsigned kEpilogueSleepNs = 256;
 
 // Ring depths: weight codes (WD) and stages (SD).  A stage is one k-step's
 // 16-bit operand (loaded by TMA) together with its dequantised tile: its
-// "full" barrier completes when the TMA bytes have landed and the 8 warps of
-// the dequantising group have arrived; one MMA commit releases both.
+// "full" barrier completes when the TMA bytes have landed and every lane of
+// the dequantising group's warps has arrived; one MMA commit releases both.
 template <int WD, int SD, int DQ = kDqGroup>
 struct GemmBars {
     uint64_t *wfull, *wempty, *sfull, *sempty, *sbfull, *sbempty, *tfull, *tempty;
@@ -299,10 +301,14 @@ struct GemmBars {
     }
     __device__ void init() {
         for (int i = 0; i < WD; ++i) { mbar_init(&wfull[i], 1); mbar_init(&wempty[i], DQ); }
-        for (int i = 0; i < SD; ++i) { mbar_init(&sfull[i], DQ + 1); mbar_init(&sempty[i], 1); }
+        // every thread that wrote or read tensor memory arrives itself, after its
+        // own wait and tcgen05 fence: the dequantising warps' 32 lanes on the
+        // stage's full barrier (plus the TMA's arrival), the epilogue's on the
+        // accumulator's empty barrier
+        for (int i = 0; i < SD; ++i) { mbar_init(&sfull[i], 32 * DQ + 1); mbar_init(&sempty[i], 1); }
         for (int i = 0; i < 2; ++i) {
             mbar_init(&sbfull[i], 1); mbar_init(&sbempty[i], kDqWarps);
-            mbar_init(&tfull[i], 1); mbar_init(&tempty[i], kEpiWarps);
+            mbar_init(&tfull[i], 1); mbar_init(&tempty[i], 32 * kEpiWarps);
         }
         fence_mbar_init();
     }
@@ -551,14 +557,14 @@ prefill_up_kernel(const __grid_constant__ LayerParams P, const PrefillIO io, con
                 }
                 __syncwarp();
                 tmem_st32(trow + 64 * (qk % kUpSD) + 32 * h, o);
-                }
+                // tcgen05.st reads its source registers asynchronously: they hold
+                // this half until the wait, before the next half is computed into them
                 tmem_st_wait();
-                tc_fence_before();
-                __syncwarp();
-                if (lane == 0) {
-                    mbar_arrive(&br.wempty[s]);
-                    mbar_arrive(&br.sfull[qk % kUpSD]);
                 }
+                tc_fence_before();
+                mbar_arrive(&br.sfull[qk % kUpSD]);   // each lane, after its own stores' wait and fence
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&br.wempty[s]);
             }
             if (!ok) break;
             q += KS;
@@ -602,8 +608,7 @@ prefill_up_kernel(const __grid_constant__ LayerParams P, const PrefillIO io, con
                 }
             }
             tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&br.tempty[acc]);
+            mbar_arrive(&br.tempty[acc]);   // each lane, after its own loads and fence
             const unsigned anylive = __ballot_sync(0xffffffffu, live != 0);
             const bool force = (io.flags & HS_FORCE_DENSE) != 0;
             if (lane == 0 && 32 * warp < d.rows && (anylive || force)) {
@@ -855,11 +860,9 @@ prefill_down_kernel(const __grid_constant__ LayerParams P, const PrefillIO io, c
                 tmem_st32(trow + 32 * (qk % kDnSD), o);
                 tmem_st_wait();
                 tc_fence_before();
+                mbar_arrive(&br.sfull[qk % kDnSD]);   // each lane, after its own stores' wait and fence
                 __syncwarp();
-                if (lane == 0) {
-                    mbar_arrive(&br.wempty[s]);
-                    mbar_arrive(&br.sfull[qk % kDnSD]);
-                }
+                if (lane == 0) mbar_arrive(&br.wempty[s]);
             }
             if (!ok) break;
             q += nk;
@@ -898,8 +901,7 @@ prefill_down_kernel(const __grid_constant__ LayerParams P, const PrefillIO io, c
                 }
             }
             tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&br.tempty[acc]);
+            mbar_arrive(&br.tempty[acc]);   // each lane, after its own loads and fence
         }
     }
     tc_fence_before();
@@ -983,6 +985,62 @@ __global__ void __launch_bounds__(256) prefill_union_live_kernel(const PrefillMe
         for (int g = 0; g < N / 64; ++g) ng += grp[g];
         if (live_rows) atomicAdd(live_rows, rows_cnt);
         if (live_groups) atomicAdd(live_groups, ng);
+    }
+}
+
+// Debug outputs after a prefill (launched only when asked for).  CTA t: token
+// t's live masks, one 64-bit word per (slot, 64-neuron group) in the decode
+// layout (shared groups first, then slot j's groups), from the kernel's fp16
+// h, which keeps each group of 8 neurons in the order n0 n4 n1 n5 n2 n6 n3 n7
+// (stored position p holds neuron kPos8[p]).  CTA 0 also copies each token
+// tile's multiplied 64-neuron tiles (the down product's own rule: the live
+// flags of the up epilogue, or every tile with the dense flag).
+__global__ void __launch_bounds__(256) prefill_live_debug_kernel(const __grid_constant__ LayerParams P,
+                                                                 const PrefillIO io) {
+    pdl_wait();
+    pdl_trigger();
+    const int tok = blockIdx.x, K = P.top_k;
+    const int NGs = P.shared_neurons / 64, NGr = P.routed_neurons / 64, Ut = NGs + K * NGr;
+    if (io.dbg_live) {
+        for (int u = threadIdx.x; u < Ut; u += blockDim.x) {
+            const uint16_t* row;
+            int gi;
+            if (u < NGs) {
+                row = io.h_s + (size_t)tok * P.shared_neurons;
+                gi = u;
+            } else {
+                const int j = (u - NGs) / NGr;
+                gi = (u - NGs) % NGr;
+                row = io.h_r + (size_t)__ldcg(io.pos_of + (size_t)tok * K + j) * P.routed_neurons;
+            }
+            const uint4* p = reinterpret_cast<const uint4*>(row + 64 * gi);
+            uint64_t m = 0;
+#pragma unroll
+            for (int b = 0; b < 8; ++b) {
+                const uint4 v = __ldcg(p + b);
+                const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+                for (int q = 0; q < 4; ++q) {
+                    constexpr int kPos8[8] = {0, 4, 1, 5, 2, 6, 3, 7};
+                    if (w[q] & 0x7fffu) m |= 1ull << (8 * b + kPos8[2 * q]);
+                    if ((w[q] >> 16) & 0x7fffu) m |= 1ull << (8 * b + kPos8[2 * q + 1]);
+                }
+            }
+            io.dbg_live[(size_t)tok * Ut + u] = m;
+        }
+    }
+    if (io.dbg_tile_live && tok == 0) {
+        const int n_tiles = __ldcg(&io.meta->n_tiles);
+        const int words = (max(P.routed_neurons, P.shared_neurons) / 64 + 31) / 32;
+        const bool dense = (io.flags & HS_FORCE_DENSE) != 0;
+        for (int i = threadIdx.x; i < n_tiles; i += blockDim.x) {
+            const TileInfo ti = io.tiles[i];
+            const int NK = (ti.e == P.n_routed ? P.shared_neurons : P.routed_neurons) / 64;
+            const uint64_t all = NK == 64 ? ~0ull : ((1ull << NK) - 1ull);
+            const uint32_t* f = io.flag_r + (size_t)i * words;
+            io.dbg_tile_live[i] =
+                dense ? all : ((uint64_t)__ldcg(f) | (words > 1 ? (uint64_t)__ldcg(f + 1) << 32 : 0ull)) & all;
+        }
     }
 }
 
@@ -1143,6 +1201,9 @@ extern "C" int hs_moe_prefill(const hs_moe_layer* L, const uint16_t* x, const fl
     io.dbg_w = dbg ? dbg->topk_w : nullptr;
     io.dbg_tiles = dbg ? dbg->tiles : nullptr;
     io.dbg_work = dbg ? dbg->work : nullptr;
+    io.dbg_live = dbg ? dbg->live_mask : nullptr;
+    io.dbg_tile_live = dbg ? dbg->tile_live : nullptr;
+    if (((uintptr_t)io.dbg_live & 7u) || ((uintptr_t)io.dbg_tile_live & 7u)) return HS_ERR_MISALIGNED;
     io.max_tiles = l.max_tiles;
 
     // tensor maps
@@ -1195,6 +1256,9 @@ extern "C" int hs_moe_prefill(const hs_moe_layer* L, const uint16_t* x, const fl
     if (launch_pdl(hs::prefill_down_kernel, dim3(sms), dim3(hs::kGemmThreads), dn_smem, s, P, io, tm) != cudaSuccess)
         return HS_ERR_CUDA;
     if (launch_pdl(hs::prefill_combine_kernel, dim3(4 * sms), dim3(256), 0, s, P, io) != cudaSuccess)
+        return HS_ERR_CUDA;
+    if ((io.dbg_live || io.dbg_tile_live) &&
+        launch_pdl(hs::prefill_live_debug_kernel, dim3(T), dim3(256), 0, s, P, io) != cudaSuccess)
         return HS_ERR_CUDA;
     (void)NR;
     return launch_err();
