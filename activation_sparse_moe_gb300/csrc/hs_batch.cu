@@ -408,7 +408,12 @@ __global__ void __launch_bounds__(kUpThreads, kUpCtasPerSm) batch_up_kernel(cons
             }
         }
         while (ok && waited < kUpRows / 16 - 1) { ++waited; ok = mbar_wait(&bars[waited], par); }
-        if (!__syncthreads_and(ok)) return;
+        if (!__syncthreads_and(ok)) {
+            // a wait gave up (the error word is set): the unit's copies land before the CTA leaves
+            if (t == 0)
+                for (int i = 0; i < kUpRows / 16; ++i) mbar_wait(&bars[i], par);
+            return;
+        }
         // ---- row sums, ReLU^2, h out, union live bits: pass pt covers (row, token) pairs
         // (row t/4, token pt); four threads per pair add groups q, q+4, ... in two chains
         for (int pt = 0; pt < d.T; ++pt) {
@@ -1021,7 +1026,12 @@ __device__ __forceinline__ bool fused_unit(const LayerParams& P, const BatchIO& 
     while (ok && waited < 3) { ++waited; ok = mbar_wait(&sm.bars[waited], par); }
     if (t < 64) sm.offs_s[t] = off_r;
     fence_proxy_async_smem();  // the parts come before the down copies into the same rows
-    if (!__syncthreads_and(ok)) return false;
+    if (!__syncthreads_and(ok)) {
+        // a wait gave up (the error word is set): the unit's copies land before the CTA leaves
+        if (t == 0)
+            for (int i = 0; i < 4; ++i) mbar_wait(&sm.bars[i], par);
+        return false;
+    }
     // ---- row sums for every token; the row's down codes are copied once if it fired for any
     bool lv = false;
     {
@@ -1109,7 +1119,11 @@ __device__ __forceinline__ bool fused_unit(const LayerParams& P, const BatchIO& 
     }
     if (any) dn_par ^= 1u;
     fence_proxy_async_smem();
-    return __syncthreads_and(ok) != 0;
+    if (!__syncthreads_and(ok)) {
+        if (t == 0 && any) mbar_wait(&sm.bars[4], dn_par ^ 1u);  // the down copies land before the CTA leaves
+        return false;
+    }
+    return true;
 }
 
 __global__ void __launch_bounds__(256, 2) batch_fused_kernel(const __grid_constant__ LayerParams P, const BatchIO io) {
@@ -1393,7 +1407,12 @@ __global__ void __launch_bounds__(256, 2) batch_small_kernel(const __grid_consta
         x_group_fixed(xw, xf);
     }
     fence_proxy_async_smem();  // the reads of x come before the copies that overwrite them
-    if (!__syncthreads_and(xok)) return;
+    if (!__syncthreads_and(xok)) {
+        // a wait gave up (the error word is set): the chunks already requested land before the CTA leaves
+        if (t == 0)
+            for (int i = 0; i < 4 - nx; ++i) mbar_wait(&sm.bars[i], 0);
+        return;
+    }
     if (t == 0) fused_issue_up(sm, ep, g, H, policy_evict_first(), 4 - nx, 4);
     uint32_t dn_par = 0;
     uint64_t live = 0;
@@ -1426,7 +1445,10 @@ __global__ void __launch_bounds__(256) batch_fused_reduce_kernel(const __grid_co
         }
     }
     const bool ok = mbar_wait(&bar, 0);
-    if (!__syncthreads_and(ok)) return;
+    if (!__syncthreads_and(ok)) {
+        if (t == 0) mbar_wait(&bar, 0);  // the slice's copies land before the CTA leaves
+        return;
+    }
     const int lane = t & 31, p = t >> 5;
     float a0 = 0.f, a1 = 0.f;
     int r = p;

@@ -281,9 +281,17 @@ moe_decode_b1_kernel(const __grid_constant__ LayerParams P, const DecodeIO io) {
     }
     float off_r = 0.f;
     if (t < 64 && ep.up_off) off_r = ep.up_off[g * 64 + t];
+    // after a wait gave up (the error word is set): one thread waits, bounded
+    // again, for every copy this CTA still has in flight before the CTA leaves
+    auto drain_up = [&]() {
+        if (t == 0) {
+            for (int i = 0; i < 4; ++i) mbar_wait(&bars[i], 0);
+            mbar_wait(&bars[5], 0);
+        }
+    };
     bool ok = mbar_wait(&bars[5], 0);
     if (ok) convert_x_fixed(x_s, G, xf_s, xs_s, 0);
-    if (!__syncthreads_and(ok)) return;
+    if (!__syncthreads_and(ok)) { drain_up(); return; }
 
     // ---- up projection for 64 rows
     XFixed xf;
@@ -324,7 +332,7 @@ moe_decode_b1_kernel(const __grid_constant__ LayerParams P, const DecodeIO io) {
     }
     if (t < 64) off_s[t] = off_r;
     fence_proxy_async_smem();  // the partial stores come before the down copies into the same rows
-    if (!__syncthreads_and(ok)) return;
+    if (!__syncthreads_and(ok)) { drain_up(); return; }
 
     // ---- row sums: thread (r, q) adds groups q, q+4, ... then a fixed 4-way
     // tree; the row's first thread then copies the row's down codes into the
@@ -398,7 +406,10 @@ moe_decode_b1_kernel(const __grid_constant__ LayerParams P, const DecodeIO io) {
     for (int off = 16; off; off >>= 1) Hsum += __shfl_xor_sync(0xffffffffu, Hsum, off);
     const int nthr = hidden % 48 == 0 ? hidden / 12 : hidden / 16;
     if (t >= nthr) return;
-    if (!mbar_wait(&bars[4], 0)) return;
+    if (!mbar_wait(&bars[4], 0)) {
+        if (t == 0) mbar_wait(&bars[4], 0);  // the rows' copies land before the CTA leaves
+        return;
+    }
     const int rsw = SmemLayout::row_sb_words(hidden);
     if (hidden % 48 == 0)
         down_acc_and_store<12, kRow>(codes_buf, sb_buf, h_s, live, Hsum, wgt, rowb, t, out_row, rsw);
@@ -435,7 +446,10 @@ reduce_partials_kernel(const float* __restrict__ partial, int U, int hidden, uin
         }
     }
     const bool ok = mbar_wait(&bar, 0);
-    if (!__syncthreads_and(ok)) return;
+    if (!__syncthreads_and(ok)) {
+        if (t == 0) mbar_wait(&bar, 0);  // the slice's copies land before the CTA leaves
+        return;
+    }
     const int lane = t & 31, p = t >> 5;
     float a0 = 0.f, a1 = 0.f;
     int r = p;
