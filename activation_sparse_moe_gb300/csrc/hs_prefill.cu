@@ -314,6 +314,15 @@ struct GemmBars {
     }
 };
 
+// A parity wait is only sound when the barrier is at most one phase behind
+// the phase waited for: two phases behind, the current (incomplete) phase has
+// the parity of the one wanted and the test passes at once.  A role that
+// takes every use of a slot has seen the slot's previous phase itself.  The
+// dequantising groups take the k-steps round robin, so every ring they wait on
+// either has a depth that is a multiple of the group count (each slot belongs
+// to one group), or is waited on only after a wait that proves its previous
+// phase complete (see the up kernel's weight ring).
+
 // Producer-side wait for slot q of a ring of depth d to be free.
 __device__ __forceinline__ bool wait_free(uint64_t* empty, int d, uint32_t q) {
     return mbar_wait(&empty[q % d], ((q / d) & 1u) ^ 1u);
@@ -339,6 +348,12 @@ __device__ __forceinline__ void drain_loads(uint64_t* full, int d, uint32_t issu
 constexpr int kUpWD = 5, kUpSD = 4;
 constexpr int kUpDqGroup = 4;   // warps per dequantising group (one per TMEM lane quadrant); 4 groups
 using UpBars = GemmBars<kUpWD, kUpSD, kUpDqGroup>;
+// Stage slot q % 4 belongs to group q % 4.  The weight slot q % 5 was last
+// filled for k-step q - 5, which another group dequantised; a group therefore
+// waits for its stage slot's release first: the MMA has then consumed k-step
+// q - 4, hence q - 5, whose codes had landed, and the weight slot's barrier is
+// at most one phase behind when the group waits on it.
+static_assert(kUpSD == kDqWarps / kUpDqGroup && kUpWD >= kUpSD, "up rings: see the parity-wait invariant");
 constexpr int kUpK = 128;                  // inputs per k-step
 
 struct UpLayout {
@@ -519,7 +534,8 @@ prefill_up_kernel(const __grid_constant__ LayerParams P, const PrefillIO io, con
             const uint32_t* sbr = sSB + b * sbw + r * G;
             for (int k = (g - (int)(q & 3u) + 4) & 3; k < KS; k += 4) {
                 const uint32_t qk = q + k;
-                ok = __all_sync(0xffffffffu, wait_full(br.wfull, kUpWD, qk) && wait_free(br.sempty, kUpSD, qk));
+                // stage release first: it proves the weight slot's previous load complete
+                ok = __all_sync(0xffffffffu, wait_free(br.sempty, kUpSD, qk) && wait_full(br.wfull, kUpWD, qk));
                 if (!ok) break;
                 tc_fence_after();
                 const int s = qk % kUpWD;
@@ -634,9 +650,15 @@ prefill_up_kernel(const __grid_constant__ LayerParams P, const PrefillIO io, con
 // n0 n4 n1 n5 n2 n6 n3 n7, the order in which a code word yields nibble pairs, so no further
 // shuffling is needed.  The epilogue lane owns one output and writes it for every token.
 constexpr int kDnBand = 128;
-constexpr int kDnWD = 6, kDnSD = 6;
+constexpr int kDnWD = 8, kDnSD = 8;
 constexpr int kDnDqGroup = 4;   // warps per dequantising group (one per TMEM lane quadrant); 4 groups
 using DnBars = GemmBars<kDnWD, kDnSD, kDnDqGroup>;
+// Both rings a multiple of the group count: slot q % 8 of either ring belongs
+// to group q % 4, which has seen the slot's previous phase itself.  TMEM holds
+// the two accumulators (256 columns) and the 8 A tiles of 32 columns.
+static_assert(kDnWD % (kDqWarps / kDnDqGroup) == 0 && kDnSD % (kDqWarps / kDnDqGroup) == 0,
+              "down rings: see the parity-wait invariant");
+static_assert(256 + 32 * kDnSD <= 512, "down A tiles exceed the TMEM allocation");
 
 struct DownLayout {
     static constexpr int kCodes = 64 * kDnBand / 2;     // 64 neurons x 64 bytes, 64-byte swizzle
@@ -826,7 +848,7 @@ prefill_down_kernel(const __grid_constant__ LayerParams P, const PrefillIO io, c
             const int nk = __popcll(d.live);
             for (int kk = (g - (int)(q & 3u) + 4) & 3; kk < nk; kk += 4) {
                 const uint32_t qk = q + kk;
-                ok = __all_sync(0xffffffffu, wait_full(br.wfull, kDnWD, qk) && wait_free(br.sempty, kDnSD, qk));
+                ok = __all_sync(0xffffffffu, wait_free(br.sempty, kDnSD, qk) && wait_full(br.wfull, kDnWD, qk));
                 if (!ok) break;
                 tc_fence_after();
                 const int s = qk % kDnWD;
