@@ -206,7 +206,8 @@ __global__ void __launch_bounds__(256) batch_route_kernel(const __grid_constant_
             io.topk_idx[p] = s_idx[t];
             io.topk_w[p] = s_w[t];
             atomicAdd(&io.meta->cnt[s_idx[t]], 1);
-            if (io.dbg_topk_idx) { io.dbg_topk_idx[p] = s_idx[t]; io.dbg_topk_w[p] = s_w[t]; }
+            if (io.dbg_topk_idx) io.dbg_topk_idx[p] = s_idx[t];
+            if (io.dbg_topk_w) io.dbg_topk_w[p] = s_w[t];
         }
     }
     // the token's fixed-point x table (read by every up unit that has this token)
@@ -1275,12 +1276,13 @@ __global__ void __launch_bounds__(256, 2) batch_small_kernel(const __grid_consta
         mbar_arrive_expect_tx(xbar, (uint32_t)(2 * B * H));
         bulk_g2s(x_dst, io.x, (uint32_t)(2 * B * H), xbar, policy_evict_last());
     }
-    if (!shared || (u == 0 && io.dbg_topk_idx)) {
+    const bool dbg_topk = io.dbg_topk_idx || io.dbg_topk_w;
+    if (!shared || (u == 0 && dbg_topk)) {
         if (warp < B) warp_topk_softmax(io.logits + (size_t)warp * E, E, K, st->topi[warp], st->topw[warp]);
         __syncthreads();
-        if (u == 0 && io.dbg_topk_idx && t < B * K) {
-            io.dbg_topk_idx[t] = st->topi[t / K][t % K];
-            io.dbg_topk_w[t] = st->topw[t / K][t % K];
+        if (u == 0 && dbg_topk && t < B * K) {
+            if (io.dbg_topk_idx) io.dbg_topk_idx[t] = st->topi[t / K][t % K];
+            if (io.dbg_topk_w) io.dbg_topk_w[t] = st->topw[t / K][t % K];
         }
     }
     UnitTokens ut;

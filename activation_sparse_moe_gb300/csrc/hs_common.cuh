@@ -140,6 +140,20 @@ __device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t by
 
 // Programmatic dependent launch: wait for the preceding grid's memory, and let
 // the next grid start launching.  Both are no-ops without the launch attribute.
+// 16-byte global -> shared copy through L2 (cp.async), with an L2 cache policy;
+// both addresses 16-byte aligned.
+__device__ __forceinline__ void cp_async16_hint(void* dst, const void* src, uint64_t policy) {
+    asm volatile("cp.async.cg.shared.global.L2::cache_hint [%0], [%1], 16, %2;" ::"r"(smem_u32(dst)), "l"(src),
+                 "l"(policy)
+                 : "memory");
+}
+// One arrival on bar once every earlier cp.async of this thread has landed; the
+// arrival is not added to the phase's count (the barrier's count includes it).
+__device__ __forceinline__ void cp_async_arrive_noinc(uint64_t* bar) {
+    asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
+
 __device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 __device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
 

@@ -254,7 +254,8 @@ moe_decode_b1_kernel(const __grid_constant__ LayerParams P, const DecodeIO io) {
         mbar_arrive_expect_tx(&bars[5], hidden * 2);
         bulk_g2s(x_s, io.x, hidden * 2, &bars[5], policy_evict_last());
     }
-    const bool need_topk = !is_shared || (u == 0 && io.dbg_topk_idx);
+    const bool dbg_topk = io.dbg_topk_idx || io.dbg_topk_w;
+    const bool need_topk = !is_shared || (u == 0 && dbg_topk);
     // warp 0 routes (if this CTA needs it); the other warps convert x meanwhile
     const int S = 256 / G;
     const int gc = t % G, r0 = t / G;
@@ -267,9 +268,9 @@ moe_decode_b1_kernel(const __grid_constant__ LayerParams P, const DecodeIO io) {
     if (need_topk) {
         if (t < 32) warp_topk_softmax(io.logits, P.n_routed, P.top_k, topk_i, topk_w);
         __syncthreads();
-        if (u == 0 && io.dbg_topk_idx && t < P.top_k) {
-            io.dbg_topk_idx[t] = topk_i[t];
-            io.dbg_topk_w[t] = topk_w[t];
+        if (u == 0 && dbg_topk && t < P.top_k) {
+            if (io.dbg_topk_idx) io.dbg_topk_idx[t] = topk_i[t];
+            if (io.dbg_topk_w) io.dbg_topk_w[t] = topk_w[t];
         }
     }
     float wgt = 1.f;
@@ -553,7 +554,6 @@ extern "C" int hs_moe_layer_decode(const hs_moe_layer* L, const uint16_t* x, con
     if (!x || !logits || !y_bf16) return HS_ERR_INVALID_ARG;
     if (batch < 1) return HS_ERR_INVALID_ARG;
     if (!al16(x) || !al4(logits) || !al16(y_bf16) || (y_f32 && !al16(y_f32)) || !al16(ws)) return HS_ERR_MISALIGNED;
-    if (dbg && ((dbg->topk_idx == nullptr) != (dbg->topk_w == nullptr))) return HS_ERR_INVALID_ARG;
     if (batch > 1) {
         if (flags & HS_DOWN_ROW_SCALES) return HS_ERR_INVALID_ARG;  // batch 1 only
         cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
@@ -572,7 +572,6 @@ extern "C" int hs_moe_layer_decode(const hs_moe_layer* L, const uint16_t* x, con
     }
     const size_t need = hs_moe_layer_decode_workspace_size(L, batch);
     if (!ws || ws_bytes < need) return HS_ERR_WORKSPACE;
-    if (dbg && ((dbg->topk_idx == nullptr) != (dbg->topk_w == nullptr))) return HS_ERR_INVALID_ARG;
 
     hs::LayerParams P;
     fill_layer_params(L, P);

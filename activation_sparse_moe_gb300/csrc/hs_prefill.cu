@@ -25,9 +25,12 @@
 //  * One fp32 partial row per (token, slot), combined per token in slot order.
 #include <cuda.h>
 
+#include <type_traits>
+
 #include "hs_host.h"
 #include "hs_tc.cuh"
 #include "hs_transpose.cuh"
+#include "hs_rowgather.cuh"
 
 namespace hs {
 
@@ -80,7 +83,15 @@ struct PrefillIO {
     uint64_t* dbg_live;       // [T][Ut] live mask (fp16 h > 0) per (token, slot group), or null
     uint64_t* dbg_tile_live;  // [tiles] 64-neuron tiles the down product multiplies, or null
     int max_tiles;
+    // row gather (HS_PREFILL_ROW_GATHER)
+    uint32_t* umask;          // [max tiles][kUWords]: bit i of word w = neuron 32w + i live for a token of the tile
+    int* nks;                 // [max tiles] k-steps of the tile's plan
+    uint32_t* ksd;            // [max tiles][kMaxKTiles] k-step descriptors (gA, gB, split8)
+    uint16_t* glist;          // [max tiles][64 * kMaxKTiles] entries: neuron, or rowgather::kPad
+    uint16_t* hc_r;           // [T*K][NR] fp16: h of each tile's entries, in k-step order
+    uint16_t* hc_s;           // [T][NS] fp16
 };
+constexpr int kUWords = 2 * kMaxKTiles;
 
 // Inside each 64-block the gathered x holds, for every group of 8 elements
 // e0..e7 (one 32-bit word of codes), the order e0 e4 e1 e5 e2 e6 e3 e7: the
@@ -104,10 +115,8 @@ __global__ void __launch_bounds__(256) prefill_route_kernel(const __grid_constan
             const int e = io.idx[(size_t)tok * K + lane];
             atomicAdd(&io.meta->cnt[e], 1);
             atomicAdd(&io.blk_cnt[(tok / kTokBlk) * P.n_routed + e], 1);
-            if (io.dbg_idx) {
-                io.dbg_idx[(size_t)tok * K + lane] = e;
-                io.dbg_w[(size_t)tok * K + lane] = io.w[(size_t)tok * K + lane];
-            }
+            if (io.dbg_idx) io.dbg_idx[(size_t)tok * K + lane] = e;
+            if (io.dbg_w) io.dbg_w[(size_t)tok * K + lane] = io.w[(size_t)tok * K + lane];
         }
     }
 }
@@ -257,6 +266,7 @@ struct TMaps {
     CUtensorMap dn_codes_r, dn_codes_s;      // [rows][H/2] bytes, box 64 x 64, 64-byte swizzle
     CUtensorMap xg[8];                       // fp16 [rows][H], box 64 x 16(i+1), 128-byte swizzle
     CUtensorMap hr[8], hsh[8];               // fp16 h, box 64 x 16(i+1), 128-byte swizzle
+    CUtensorMap hcr[8], hcs[8];              // fp16 h in entry order (row gather), same boxes
 };
 
 // ------------------------------------------------------------ GEMM kernels
@@ -299,8 +309,10 @@ struct GemmBars {
         sbfull = sempty + SD; sbempty = sbfull + 2; tfull = sbempty + 2; tempty = tfull + 2;
         tmem_slot = reinterpret_cast<uint32_t*>(tempty + 2);
     }
-    __device__ void init() {
-        for (int i = 0; i < WD; ++i) { mbar_init(&wfull[i], 1); mbar_init(&wempty[i], DQ); }
+    // wfull_count: arrivals that fill a weight slot (1: one TMA issuer; 32: a warp
+    // whose lanes each count their own cp.async copies)
+    __device__ void init(uint32_t wfull_count = 1) {
+        for (int i = 0; i < WD; ++i) { mbar_init(&wfull[i], wfull_count); mbar_init(&wempty[i], DQ); }
         // every thread that wrote or read tensor memory arrives itself, after its
         // own wait and tcgen05 fence: the dequantising warps' 32 lanes on the
         // stage's full barrier (plus the TMA's arrival), the epilogue's on the
@@ -633,6 +645,8 @@ prefill_up_kernel(const __grid_constant__ LayerParams P, const PrefillIO io, con
             }
             if (lane == 0 && anylive)
                 atomicAdd(&io.meta->union_rt, (unsigned long long)__popc(anylive) * (unsigned long long)d.ntok);
+            if (io.umask && lane == 0 && 32 * warp < d.rows)
+                io.umask[(size_t)d.tile * kUWords + (d.row0 + 32 * warp) / 32] = anylive;
         }
     }
     tc_fence_before();
@@ -669,13 +683,31 @@ struct DownLayout {
     static constexpr int kTotal = 1024 + kBarsOff + 8 * DnBars::kCount + 64;
 };
 
-struct DownUnit {
-    int tile, ob, ntok, nt16, cy0, NK, row0;
-    bool shared;
-    ExpertPtrs ep;
-    uint64_t live;   // bit j: 64-neuron tile j is multiplied
+// Row-gather weight slot: the k-step's 64 entry rows (64 bytes of codes each,
+// at a stride of 80 bytes: the dequantiser's lane pattern then touches every
+// bank once), the (scale, bias) slab slices of groups gA and gB, and the
+// aligned 16 bytes of the tile's descriptor row that hold the k-step's
+// descriptor (word kk % 4).
+struct DownLayoutG {
+    static constexpr int kRowStride = 80;
+    static constexpr int kCodes = 64 * kRowStride;
+    static constexpr int kSlab = kCodes;                       // two slices of kDnBand (scale, bias) pairs
+    static constexpr int kDesc = kSlab + 2 * kDnBand * 4;
+    static constexpr int kWSlot = (kDesc + 16 + 127) & ~127;
+    static constexpr int kX = 0;
+    static constexpr int kW = kX + kDnSD * kTileX;
+    static constexpr int kBarsOff = kW + kDnWD * kWSlot;
+    static constexpr int kTotal = 1024 + kBarsOff + 8 * DnBars::kCount + 64;
 };
 
+struct DownUnit {
+    int tile, ob, ntok, nt16, cy0, NK, row0, nk;
+    bool shared;
+    ExpertPtrs ep;
+    uint64_t live;   // tile mode: bit j = 64-neuron tile j is multiplied
+};
+
+template <bool kGather>
 __device__ __forceinline__ DownUnit down_unit(const LayerParams& P, const PrefillIO& io, int nb, int words, bool dense,
                                               int u) {
     DownUnit d;
@@ -689,9 +721,15 @@ __device__ __forceinline__ DownUnit down_unit(const LayerParams& P, const Prefil
     d.nt16 = (ti.ntok + 15) & ~15;
     d.cy0 = d.shared ? 0 : ti.e * P.routed_neurons;
     d.row0 = ti.row0;
-    const uint32_t* f = io.flag_r + (size_t)d.tile * words;
-    const uint64_t all = d.NK == 64 ? ~0ull : ((1ull << d.NK) - 1ull);
-    d.live = dense ? all : ((uint64_t)__ldcg(f) | (words > 1 ? (uint64_t)__ldcg(f + 1) << 32 : 0ull)) & all;
+    if (kGather) {
+        d.live = 0;
+        d.nk = __ldcg(io.nks + d.tile);
+    } else {
+        const uint32_t* f = io.flag_r + (size_t)d.tile * words;
+        const uint64_t all = d.NK == 64 ? ~0ull : ((1ull << d.NK) - 1ull);
+        d.live = dense ? all : ((uint64_t)__ldcg(f) | (words > 1 ? (uint64_t)__ldcg(f + 1) << 32 : 0ull)) & all;
+        d.nk = __popcll(d.live);
+    }
     return d;
 }
 
@@ -702,16 +740,20 @@ __device__ __forceinline__ int pop_live(uint64_t& m) {
     return j;
 }
 
+// kGather: k-step kk of a unit multiplies the tile's entries 64 kk .. 64 kk + 63
+// (rowgather plan) instead of its kk-th live 64-neuron tile.
+template <bool kGather>
 __global__ void __launch_bounds__(kGemmThreads, 1)
 prefill_down_kernel(const __grid_constant__ LayerParams P, const PrefillIO io, const __grid_constant__ TMaps tm) {
+    using Lay = typename std::conditional<kGather, DownLayoutG, DownLayout>::type;
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const int H = P.hidden;
-    uint8_t* sX = smem + DownLayout::kX;
-    uint8_t* sW = smem + DownLayout::kW;
-    DnBars br(smem + DownLayout::kBarsOff);
+    uint8_t* sX = smem + Lay::kX;
+    uint8_t* sW = smem + Lay::kW;
+    DnBars br(smem + Lay::kBarsOff);
     const int t = threadIdx.x, warp = t >> 5, lane = t & 31;
-    if (t == 0) br.init();
+    if (t == 0) br.init(kGather ? 32u : 1u);
     if (warp == 0) tmem_alloc(br.tmem_slot, 512);
     tc_fence_before();
     __syncthreads();
@@ -728,25 +770,89 @@ prefill_down_kernel(const __grid_constant__ LayerParams P, const PrefillIO io, c
     const bool dense = (io.flags & HS_FORCE_DENSE) != 0;
     bool ok = true;
 
-    if (warp == kWarpW) {
+    if (warp == kWarpW && kGather) {
+        // ---- each k-step's 64 entry rows and the slab slices of its groups gA and gB, by
+        // 16-byte cp.async from every lane (row copies of 64 bytes are too small for the bulk
+        // copy engine to keep up): 256 row chunks and 64 slab chunks, 10 per lane, plus the
+        // k-step's descriptor (lane 0); each lane's copies arrive on the slot's barrier once
+        // they have landed (32 arrivals)
+        const uint64_t pol_stream = policy_evict_first(), pol_keep = policy_evict_last();
+        uint32_t wq = 0;
+        DownUnit dnext;
+        if ((int)blockIdx.x < U) dnext = down_unit<kGather>(P, io, nb, words, dense, blockIdx.x);
+        for (int u = blockIdx.x; u < U && ok; u += gridDim.x) {
+            const DownUnit d = dnext;
+            if (u + (int)gridDim.x < U) dnext = down_unit<kGather>(P, io, nb, words, dense, u + gridDim.x);
+            const uint64_t pol = d.shared ? pol_keep : pol_stream;
+            const uint16_t* L = io.glist + (size_t)d.tile * 64 * kMaxKTiles;
+            const uint32_t* D = io.ksd + (size_t)d.tile * kMaxKTiles;
+            const uint8_t* codes = d.ep.dn_codes + (kDnBand / 2) * d.ob;
+            const uint8_t* slab = reinterpret_cast<const uint8_t*>(d.ep.dn_sb + kDnBand * d.ob);
+            // the entries (two per lane) and descriptor of k-step kk + 1 are loaded while kk is issued
+            uint32_t e2 = d.nk > 0 ? __ldcg(reinterpret_cast<const uint32_t*>(L) + lane) : 0u;
+            uint32_t desc = d.nk > 0 ? __ldcg(D) : 0u;
+            for (int kk = 0; kk < d.nk; ++kk) {
+                const uint32_t e2c = e2, descc = desc;
+                if (kk + 1 < d.nk) {
+                    e2 = __ldcg(reinterpret_cast<const uint32_t*>(L + 64 * (kk + 1)) + lane);
+                    desc = __ldcg(D + kk + 1);
+                }
+                if (lane == 0) ok = wait_free_sleep(br.wempty, kDnWD, wq, kProducerSleepNs);
+                ok = __shfl_sync(0xffffffffu, ok, 0);
+                if (!ok) break;
+                const int s = wq % kDnWD;
+                uint8_t* slot = sW + s * Lay::kWSlot;
+                // chunk c = lane + 32 i: row c / 4 (entry lane / 4 + 8 i), 16-byte part c % 4
+#pragma unroll
+                for (int i = 0; i < 8; ++i) {
+                    const int row = (lane >> 2) + 8 * i;
+                    const uint32_t pair = __shfl_sync(0xffffffffu, e2c, row >> 1);
+                    const uint32_t v = (pair >> (16 * (row & 1))) & 0xFFFFu;
+                    const int n = v == rowgather::kPad ? 0 : (int)v;   // a padding entry reads row 0 against h = 0
+                    cp_async16_hint(slot + row * DownLayoutG::kRowStride + 16 * (lane & 3),
+                                    codes + (size_t)n * (H / 2) + 16 * (lane & 3), pol);
+                }
+                cp_async16_hint(slot + DownLayoutG::kSlab + 16 * lane,
+                                slab + (size_t)rowgather::ksd_gA(descc) * H * 4 + 16 * lane, pol);
+                cp_async16_hint(slot + DownLayoutG::kSlab + kDnBand * 4 + 16 * lane,
+                                slab + (size_t)rowgather::ksd_gB(descc) * H * 4 + 16 * lane, pol);
+                // the dequantisers read the descriptor from the slot, not from global memory
+                if (lane == 0)
+                    cp_async16_hint(slot + DownLayoutG::kDesc, D + (kk & ~3), pol_keep);
+                cp_async_arrive_noinc(&br.wfull[s]);
+                ++wq;
+            }
+            if (ok && d.ob == 0 && lane == 0) {
+                atomicAdd(&m->total, d.NK);
+                atomicAdd(&m->skipped, d.NK - d.nk);
+                atomicAdd(&m->exec_rt, (unsigned long long)d.ntok * 64ull * (unsigned long long)d.nk);
+                atomicAdd(&m->dense_rt, (unsigned long long)d.ntok * 64ull * (unsigned long long)d.NK);
+            }
+        }
+        // every lane's copies have landed, and their arrivals are on the barriers, before the
+        // CTA can leave
+        cp_async_wait_all();
+        __syncwarp();
+        if (lane == 0) drain_loads(br.wfull, kDnWD, wq);
+        __syncwarp();
+    } else if (warp == kWarpW) {
         // ---- codes + (scale, bias) slab slice of each live 64-neuron tile, this band
         if (lane == 0) {
             const uint64_t pol_stream = policy_evict_first(), pol_keep = policy_evict_last();
             uint32_t wq = 0;
             // the next unit's descriptor is loaded one unit ahead (its loads overlap this unit's work)
             DownUnit dnext;
-            if ((int)blockIdx.x < U) dnext = down_unit(P, io, nb, words, dense, blockIdx.x);
+            if ((int)blockIdx.x < U) dnext = down_unit<kGather>(P, io, nb, words, dense, blockIdx.x);
             for (int u = blockIdx.x; u < U && ok; u += gridDim.x) {
                 const DownUnit d = dnext;
-                if (u + (int)gridDim.x < U) dnext = down_unit(P, io, nb, words, dense, u + gridDim.x);
+                if (u + (int)gridDim.x < U) dnext = down_unit<kGather>(P, io, nb, words, dense, u + gridDim.x);
                 const CUtensorMap* cmap = d.shared ? &tm.dn_codes_s : &tm.dn_codes_r;
                 const uint64_t pol = d.shared ? pol_keep : pol_stream;
-                const int nk = __popcll(d.live);
                 for (uint64_t lm = d.live; lm && ok;) {
                     const int j = pop_live(lm);
                     if (!(ok = wait_free_sleep(br.wempty, kDnWD, wq, kProducerSleepNs))) break;
                     const int s = wq % kDnWD;
-                    uint8_t* slot = sW + s * DownLayout::kWSlot;
+                    uint8_t* slot = sW + s * Lay::kWSlot;
                     mbar_arrive_expect_tx(&br.wfull[s], (uint32_t)DownLayout::kWSlot);
                     tma_load_2d_hint(slot, cmap, (kDnBand / 2) * d.ob, d.cy0 + 64 * j, &br.wfull[s], pol);
                     bulk_g2s(slot + DownLayout::kCodes, d.ep.dn_sb + (size_t)j * H + kDnBand * d.ob, kDnBand * 4,
@@ -755,8 +861,8 @@ prefill_down_kernel(const __grid_constant__ LayerParams P, const PrefillIO io, c
                 }
                 if (ok && d.ob == 0) {
                     atomicAdd(&m->total, d.NK);
-                    atomicAdd(&m->skipped, d.NK - nk);
-                    atomicAdd(&m->exec_rt, (unsigned long long)d.ntok * 64ull * (unsigned long long)nk);
+                    atomicAdd(&m->skipped, d.NK - d.nk);
+                    atomicAdd(&m->exec_rt, (unsigned long long)d.ntok * 64ull * (unsigned long long)d.nk);
                     atomicAdd(&m->dense_rt, (unsigned long long)d.ntok * 64ull * (unsigned long long)d.NK);
                 }
             }
@@ -770,17 +876,19 @@ prefill_down_kernel(const __grid_constant__ LayerParams P, const PrefillIO io, c
             uint32_t xq = 0;
             // the next unit's descriptor is loaded one unit ahead (its loads overlap this unit's work)
             DownUnit dnext;
-            if ((int)blockIdx.x < U) dnext = down_unit(P, io, nb, words, dense, blockIdx.x);
+            if ((int)blockIdx.x < U) dnext = down_unit<kGather>(P, io, nb, words, dense, blockIdx.x);
             for (int u = blockIdx.x; u < U && ok; u += gridDim.x) {
                 const DownUnit d = dnext;
-                if (u + (int)gridDim.x < U) dnext = down_unit(P, io, nb, words, dense, u + gridDim.x);
-                const CUtensorMap* hmap = d.shared ? &tm.hsh[d.nt16 / 16 - 1] : &tm.hr[d.nt16 / 16 - 1];
-                for (uint64_t lm = d.live; lm && ok;) {
-                    const int j = pop_live(lm);
+                if (u + (int)gridDim.x < U) dnext = down_unit<kGather>(P, io, nb, words, dense, u + gridDim.x);
+                const CUtensorMap* hmap = kGather ? (d.shared ? &tm.hcs[d.nt16 / 16 - 1] : &tm.hcr[d.nt16 / 16 - 1])
+                                                  : (d.shared ? &tm.hsh[d.nt16 / 16 - 1] : &tm.hr[d.nt16 / 16 - 1]);
+                uint64_t lm = d.live;
+                for (int kk = 0; kk < d.nk && ok; ++kk) {
+                    const int col = kGather ? 64 * kk : 64 * pop_live(lm);
                     if (!(ok = wait_free_sleep(br.sempty, kDnSD, xq, kProducerSleepNs))) break;
                     const int x = xq % kDnSD;
                     mbar_arrive_expect_tx(&br.sfull[x], (uint32_t)d.nt16 * 128u);
-                    tma_load_2d_hint(sX + x * kTileX, hmap, 64 * j, d.row0, &br.sfull[x], pol);
+                    tma_load_2d_hint(sX + x * kTileX, hmap, col, d.row0, &br.sfull[x], pol);
                     ++xq;
                 }
             }
@@ -793,17 +901,16 @@ prefill_down_kernel(const __grid_constant__ LayerParams P, const PrefillIO io, c
             uint32_t sq = 0, nu = 0;
             // the next unit's descriptor is loaded one unit ahead (its loads overlap this unit's work)
             DownUnit dnext;
-            if ((int)blockIdx.x < U) dnext = down_unit(P, io, nb, words, dense, blockIdx.x);
+            if ((int)blockIdx.x < U) dnext = down_unit<kGather>(P, io, nb, words, dense, blockIdx.x);
             for (int u = blockIdx.x; u < U && ok; u += gridDim.x, ++nu) {
                 const DownUnit d = dnext;
-                if (u + (int)gridDim.x < U) dnext = down_unit(P, io, nb, words, dense, u + gridDim.x);
+                if (u + (int)gridDim.x < U) dnext = down_unit<kGather>(P, io, nb, words, dense, u + gridDim.x);
                 const int acc = nu & 1;
                 if (!(ok = wait_free(br.tempty, 2, nu))) break;
                 tc_fence_after();
                 const uint32_t idesc = umma_idesc_f16_f32(128, d.nt16);
                 const uint32_t dt = tmem + (uint32_t)(acc * 128);
-                const int nk = __popcll(d.live);
-                for (int kk = 0; kk < nk; ++kk) {
+                for (int kk = 0; kk < d.nk; ++kk) {
                     if (!(ok = wait_full(br.sfull, kDnSD, sq))) break;
                     tc_fence_after();
                     const int a = sq % kDnSD;
@@ -822,50 +929,60 @@ prefill_down_kernel(const __grid_constant__ LayerParams P, const PrefillIO io, c
     } else if (warp >= kEpiWarps && warp < kWarpW) {
         // ---- dequantise into TMEM: group g = (warp - 4) / 4 takes the k-steps q with q % 4 == g.
         // Warp quadrant qd = warp % 4: outputs 32qd .. 32qd+31 of the band (TMEM lanes), all 64
-        // neurons of the tile (32 columns of the A tile), in two halves of 32 neurons
+        // neurons (entries) of the k-step (32 columns of the A tile), in two halves of 32
         const int g = (warp - kEpiWarps) / kDnDqGroup, qd = warp & 3;
         const uint32_t trow = tmem_a + ((uint32_t)(32 * qd) << 16);
         // lane l takes word l/8 of the quadrant's 16-byte chunk in rows 32hh + 8k + l%8 (the
-        // word-level steps of the transpose done by the loads); 64-byte swizzle: chunk c of row r
-        // sits at chunk c ^ ((r >> 1) & 3)
+        // word-level steps of the transpose done by the loads).  Tile mode: 64-byte swizzle, chunk c
+        // of row r at chunk c ^ ((r >> 1) & 3).  Gather mode: rows 80 bytes apart, unswizzled.
         int ldoff[2][4];
 #pragma unroll
         for (int hh = 0; hh < 2; ++hh)
 #pragma unroll
             for (int k = 0; k < 4; ++k) {
                 const int r = 32 * hh + (lane & 7) + 8 * k;
-                ldoff[hh][k] = r * (kDnBand / 2) + ((qd ^ ((r >> 1) & 3)) << 4) + 4 * (lane >> 3);
+                ldoff[hh][k] = kGather ? r * DownLayoutG::kRowStride + (qd << 4) + 4 * (lane >> 3)
+                                       : r * (kDnBand / 2) + ((qd ^ ((r >> 1) & 3)) << 4) + 4 * (lane >> 3);
             }
         const NibTrLane trc = nib_tr_lane();
         const __half2 k1024 = __floats2half2_rn(1024.f, 1024.f);
         uint32_t q = 0;
         // the next unit's descriptor is loaded one unit ahead (its loads overlap this unit's work)
         DownUnit dnext;
-        if ((int)blockIdx.x < U) dnext = down_unit(P, io, nb, words, dense, blockIdx.x);
+        if ((int)blockIdx.x < U) dnext = down_unit<kGather>(P, io, nb, words, dense, blockIdx.x);
         for (int u = blockIdx.x; u < U && ok; u += gridDim.x) {
             const DownUnit d = dnext;
-            if (u + (int)gridDim.x < U) dnext = down_unit(P, io, nb, words, dense, u + gridDim.x);
-            const int nk = __popcll(d.live);
+            if (u + (int)gridDim.x < U) dnext = down_unit<kGather>(P, io, nb, words, dense, u + gridDim.x);
+            const int nk = d.nk;
             for (int kk = (g - (int)(q & 3u) + 4) & 3; kk < nk; kk += 4) {
                 const uint32_t qk = q + kk;
                 ok = __all_sync(0xffffffffu, wait_free(br.sempty, kDnSD, qk) && wait_full(br.wfull, kDnWD, qk));
                 if (!ok) break;
                 tc_fence_after();
                 const int s = qk % kDnWD;
-                const uint8_t* cs = sW + s * DownLayout::kWSlot;
-                const float2 sbv = half2_to_float2(reinterpret_cast<const uint32_t*>(cs + DownLayout::kCodes)[32 * qd + lane]);
-                const __half2 s1 = __floats2half2_rn(sbv.x, sbv.x);
-                const __half2 s16 = __floats2half2_rn(sbv.x * 0.0625f, sbv.x * 0.0625f);
-                const __half2 b2 = __floats2half2_rn(sbv.y, sbv.y);
+                const uint8_t* cs = sW + s * Lay::kWSlot;
+                // (scale, bias) of groups A and B; 8-entry block kb takes A if kb < split8
+                const uint32_t* sbw = reinterpret_cast<const uint32_t*>(cs + (kGather ? DownLayoutG::kSlab : DownLayout::kCodes));
+                const float2 sa = half2_to_float2(sbw[32 * qd + lane]);
+                const float2 sbb = kGather ? half2_to_float2(sbw[kDnBand + 32 * qd + lane]) : sa;
+                const int split8 =
+                    kGather ? rowgather::ksd_split8(reinterpret_cast<const uint32_t*>(cs + DownLayoutG::kDesc)[kk & 3])
+                            : 8;
+                const __half2 s1a = __floats2half2_rn(sa.x, sa.x), s1b = __floats2half2_rn(sbb.x, sbb.x);
+                const __half2 s16a = __floats2half2_rn(sa.x * 0.0625f, sa.x * 0.0625f);
+                const __half2 s16b = __floats2half2_rn(sbb.x * 0.0625f, sbb.x * 0.0625f);
+                const __half2 b2a = __floats2half2_rn(sa.y, sa.y), b2b = __floats2half2_rn(sbb.y, sbb.y);
                 uint32_t o[32];
 #pragma unroll
                 for (int hh = 0; hh < 2; ++hh) {
                     uint32_t a[4];
 #pragma unroll
                     for (int k = 0; k < 4; ++k) a[k] = *reinterpret_cast<const uint32_t*>(cs + ldoff[hh][k]);
-                    nib_transpose32_in_words(a, trc);   // lane = output 32qd + lane, nibble j of word k = neuron 32hh + 8k + j
+                    nib_transpose32_in_words(a, trc);   // lane = output 32qd + lane, nibble j of word k = entry 32hh + 8k + j
 #pragma unroll
                     for (int k = 0; k < 4; ++k) {
+                        const bool useA = 4 * hh + k < split8;
+                        const __half2 s1 = useA ? s1a : s1b, s16 = useA ? s16a : s16b, b2 = useA ? b2a : b2b;
                         const uint32_t lo = a[k], hi = a[k] >> 8;
                         // fp16 1024 + c (or 1024 + 16c): nibble pairs (0,4) (1,5) (2,6) (3,7)
                         const uint32_t pr[4] = {(lo & 0x000F000Fu) | 0x64006400u, (lo & 0x00F000F0u) | 0x64006400u,
@@ -894,10 +1011,10 @@ prefill_down_kernel(const __grid_constant__ LayerParams P, const PrefillIO io, c
         uint32_t nu = 0;
         // the next unit's descriptor is loaded one unit ahead (its loads overlap this unit's work)
         DownUnit dnext;
-        if ((int)blockIdx.x < U) dnext = down_unit(P, io, nb, words, dense, blockIdx.x);
+        if ((int)blockIdx.x < U) dnext = down_unit<kGather>(P, io, nb, words, dense, blockIdx.x);
         for (int u = blockIdx.x; u < U && ok; u += gridDim.x, ++nu) {
             const DownUnit d = dnext;
-            if (u + (int)gridDim.x < U) dnext = down_unit(P, io, nb, words, dense, u + gridDim.x);
+            if (u + (int)gridDim.x < U) dnext = down_unit<kGather>(P, io, nb, words, dense, u + gridDim.x);
             const int acc = nu & 1;
             const int col = kDnBand * d.ob + 32 * warp + lane;
             float* pbase = io.partial + (d.shared ? (size_t)io.T * K + d.row0 : (size_t)d.row0) * H + col;
@@ -907,7 +1024,7 @@ prefill_down_kernel(const __grid_constant__ LayerParams P, const PrefillIO io, c
             tc_fence_after();
             for (int c0 = 0; c0 < d.nt16; c0 += 32) {
                 float v[32];
-                if (d.live) {
+                if (d.nk > 0) {
                     tmem_ld32(tmem + ((uint32_t)(32 * warp) << 16) + (uint32_t)(acc * 128 + c0), v);
                 } else {
 #pragma unroll
@@ -1066,6 +1183,117 @@ __global__ void __launch_bounds__(256) prefill_live_debug_kernel(const __grid_co
     }
 }
 
+// ------------------------------------------------------------ row gather
+// The page's prefill gathers, per token tile, the rows live for any of its
+// tokens into a dense product ("What we do instead").  Here the up epilogue
+// leaves each tile's union-live mask (one bit per neuron); this kernel plans
+// the tile's down product and copies the tile's h into entry order, and the
+// down product then copies the entries' weight rows.
+//
+// CTA (tile, part): every CTA of a tile plans it in shared memory
+// (rowgather::plan_tile: each group's live neurons padded to 8 entries, at
+// most two scale groups per 64-entry k-step; the identity plan if packing
+// would take more k-steps than groups) and lists the entries; part 0 also
+// publishes the plan (k-step count, descriptors, entry list) for the down
+// product.  Then each CTA copies rows part * kGatherRows + ... of the tile's
+// h into H_c: a pass reads kGatherRows rows whole (16-byte loads) into shared
+// memory, and thread task (row, 8-entry block b) gathers the block's 8 values
+// (zero at padding entries) into one 16-byte word at columns 8b .. 8b + 7, in
+// the stored order of h.  H_c columns beyond the plan are never read.
+constexpr int kGatherRows = 4;   // rows of h staged per pass
+constexpr int kGatherParts = 8;  // CTAs per tile
+__global__ void __launch_bounds__(256) prefill_gather_kernel(const __grid_constant__ LayerParams P, const PrefillIO io) {
+    __shared__ __align__(16) uint16_t list_s[64 * kMaxKTiles];
+    __shared__ __align__(16) uint16_t row_s[kGatherRows][64 * kMaxKTiles];
+    __shared__ uint64_t msk[kMaxKTiles];
+    __shared__ uint32_t ksd_s[kMaxKTiles];
+    __shared__ int ofs[kMaxKTiles];
+    __shared__ int nks_s, ident_s;
+    pdl_wait();
+    pdl_trigger();
+    const int tile = blockIdx.x, t = threadIdx.x, lane = t & 31, warp = t >> 5;
+    if (tile >= __ldcg(&io.meta->n_tiles)) return;
+    const TileInfo ti = io.tiles[tile];
+    const bool shared = ti.e == P.n_routed;
+    const int N = shared ? P.shared_neurons : P.routed_neurons, NG = N / 64;
+    // ---- plan (thread 0), while warps 1-7 stage the first pass of rows of h
+    const uint32_t* um = io.umask + (size_t)tile * kUWords;
+    const uint16_t* H = shared ? io.h_s : io.h_r;
+    uint16_t* Hc = shared ? io.hc_s : io.hc_r;
+    const int c16 = N / 8;   // 16-byte chunks per row of h
+    auto load_rows = [&](int r0, int nr, int first, int step) {
+        for (int q = first; q < nr * c16; q += step) {
+            const int rr = q / c16, c = q % c16;
+            reinterpret_cast<uint4*>(row_s[rr])[c] =
+                __ldcg(reinterpret_cast<const uint4*>(H + (size_t)(ti.row0 + r0 + rr) * N) + c);
+        }
+    };
+    const int r_first = blockIdx.y * kGatherRows;
+    if (warp == 0) {
+        for (int g = lane; g < NG; g += 32)
+            msk[g] = (uint64_t)__ldcg(um + 2 * g) | ((uint64_t)__ldcg(um + 2 * g + 1) << 32);
+        __syncwarp();
+        if (lane == 0) {
+            int n = rowgather::plan_tile(msk, NG, ksd_s, ofs);
+            ident_s = n < 0;
+            if (n < 0) n = rowgather::plan_identity(NG, ksd_s, ofs);
+            nks_s = n;
+        }
+    } else if (r_first < ti.ntok) {
+        load_rows(r_first, min(kGatherRows, ti.ntok - r_first), t - 32, blockDim.x - 32);
+    }
+    __syncthreads();
+    const int nks = nks_s, nb = 8 * nks;
+    const bool ident = ident_s != 0;
+    for (int e = t; e < 64 * nks; e += blockDim.x) list_s[e] = rowgather::kPad;
+    __syncthreads();
+    // warp per group: its live neurons, ascending, from the group's first entry
+    for (int g = warp; g < NG; g += blockDim.x / 32) {
+        if (ofs[g] < 0) continue;
+        const uint64_t m = ident ? ~0ull : msk[g];
+#pragma unroll
+        for (int half = 0; half < 2; ++half) {
+            const bool live = (m >> (32 * half + lane)) & 1ull;
+            const unsigned below = (unsigned)(m >> (32 * half)) & ((1u << lane) - 1u);
+            const int rank = (half ? __popc((unsigned)m) : 0) + __popc(below);
+            if (live) list_s[ofs[g] + rank] = (uint16_t)(64 * g + 32 * half + lane);
+        }
+    }
+    __syncthreads();
+    if (blockIdx.y == 0) {
+        uint4* L = reinterpret_cast<uint4*>(io.glist + (size_t)tile * 64 * kMaxKTiles);
+        for (int b = t; b < nb; b += blockDim.x) L[b] = reinterpret_cast<const uint4*>(list_s)[b];
+        for (int k = t; k < nks; k += blockDim.x) io.ksd[(size_t)tile * kMaxKTiles + k] = ksd_s[k];
+        if (t == 0) io.nks[tile] = nks;
+    }
+    // ---- H_c rows of this part (the first pass's rows are staged)
+    for (int r0 = r_first; r0 < ti.ntok; r0 += gridDim.y * kGatherRows) {
+        const int nr = min(kGatherRows, ti.ntok - r0);
+        if (r0 != r_first) {
+            __syncthreads();   // the previous pass has read its rows
+            load_rows(r0, nr, t, blockDim.x);
+            __syncthreads();
+        }
+        for (int q = t; q < nr * nb; q += blockDim.x) {
+            const int rr = q / nb, b = q % nb;
+            const uint4 ids = reinterpret_cast<const uint4*>(list_s)[b];
+            const uint32_t w[4] = {ids.x, ids.y, ids.z, ids.w};
+            uint16_t v[8];
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                const uint32_t n = (w[i >> 1] >> (16 * (i & 1))) & 0xFFFFu;
+                v[rowgather::stored_pos(i)] = n == rowgather::kPad ? (uint16_t)0 : row_s[rr][rowgather::stored_pos((int)n)];
+            }
+            uint4 o;
+            o.x = (uint32_t)v[0] | ((uint32_t)v[1] << 16);
+            o.y = (uint32_t)v[2] | ((uint32_t)v[3] << 16);
+            o.z = (uint32_t)v[4] | ((uint32_t)v[5] << 16);
+            o.w = (uint32_t)v[6] | ((uint32_t)v[7] << 16);
+            *reinterpret_cast<uint4*>(Hc + (size_t)(ti.row0 + r0 + rr) * N + 8 * b) = o;
+        }
+    }
+}
+
 }  // namespace hs
 
 // ===================================================================== host
@@ -1108,7 +1336,8 @@ bool make_map(EncodeTiledFn enc, CUtensorMap* m, CUtensorMapDataType dt, const v
 }
 
 struct PrefillLayout {
-    size_t meta, blk_cnt, tiles, idx, w, pair_tok, pos_of, pair_w, xg, h_r, h_s, flags, partial, total;
+    size_t meta, blk_cnt, tiles, idx, w, pair_tok, pos_of, pair_w, xg, h_r, h_s, flags, partial, umask, nks, ksd, glist,
+        hc_r, hc_s, total;
     int max_tiles;
 };
 
@@ -1133,6 +1362,13 @@ PrefillLayout prefill_layout(const hs_moe_layer* L, int T) {
     l.h_s = take((size_t)(NS ? T : 1) * (NS ? NS : 64) * 2);
     l.flags = take((size_t)l.max_tiles * ((std::max(NR, NS) / 64 + 31) / 32) * 4);
     l.partial = take(rows * H * 4);
+    // row gather
+    l.umask = take((size_t)l.max_tiles * hs::kUWords * 4);
+    l.nks = take((size_t)l.max_tiles * 4);
+    l.ksd = take((size_t)l.max_tiles * hs::kMaxKTiles * 4);
+    l.glist = take((size_t)l.max_tiles * 64 * hs::kMaxKTiles * 2);
+    l.hc_r = take((size_t)T * K * NR * 2);
+    l.hc_s = take((size_t)(NS ? T : 1) * (NS ? NS : 64) * 2);
     l.total = o;
     return l;
 }
@@ -1227,6 +1463,15 @@ extern "C" int hs_moe_prefill(const hs_moe_layer* L, const uint16_t* x, const fl
     io.dbg_tile_live = dbg ? dbg->tile_live : nullptr;
     if (((uintptr_t)io.dbg_live & 7u) || ((uintptr_t)io.dbg_tile_live & 7u)) return HS_ERR_MISALIGNED;
     io.max_tiles = l.max_tiles;
+    const bool gather = (flags & HS_PREFILL_ROW_GATHER) && !(flags & HS_FORCE_DENSE);
+    if (gather) {
+        io.umask = reinterpret_cast<uint32_t*>(w + l.umask);
+        io.nks = reinterpret_cast<int*>(w + l.nks);
+        io.ksd = reinterpret_cast<uint32_t*>(w + l.ksd);
+        io.glist = reinterpret_cast<uint16_t*>(w + l.glist);
+        io.hc_r = reinterpret_cast<uint16_t*>(w + l.hc_r);
+        io.hc_s = reinterpret_cast<uint16_t*>(w + l.hc_s);
+    }
 
     // tensor maps
     hs::TMaps tm;
@@ -1253,6 +1498,13 @@ extern "C" int hs_moe_prefill(const hs_moe_layer* L, const uint16_t* x, const fl
         if (NS)
             okm &= make_map(enc, &tm.hsh[b], CU_TENSOR_MAP_DATA_TYPE_FLOAT16, io.h_s, NS, T, (uint64_t)NS * 2, 64, br,
                             CU_TENSOR_MAP_SWIZZLE_128B);
+        if (gather) {
+            okm &= make_map(enc, &tm.hcr[b], CU_TENSOR_MAP_DATA_TYPE_FLOAT16, io.hc_r, NR, (uint64_t)T * K,
+                            (uint64_t)NR * 2, 64, br, CU_TENSOR_MAP_SWIZZLE_128B);
+            if (NS)
+                okm &= make_map(enc, &tm.hcs[b], CU_TENSOR_MAP_DATA_TYPE_FLOAT16, io.hc_s, NS, T, (uint64_t)NS * 2, 64,
+                                br, CU_TENSOR_MAP_SWIZZLE_128B);
+        }
     }
     if (!okm) return HS_ERR_CUDA;
 
@@ -1260,9 +1512,10 @@ extern "C" int hs_moe_prefill(const hs_moe_layer* L, const uint16_t* x, const fl
     if (cudaGetDevice(&dev) != cudaSuccess) return HS_ERR_CUDA;
     if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return HS_ERR_CUDA;
     const int up_smem = hs::UpLayout::total(H);
-    const int dn_smem = hs::DownLayout::kTotal;
+    const int dn_smem = gather ? hs::DownLayoutG::kTotal : hs::DownLayout::kTotal;
+    const void* dn_kernel = gather ? (const void*)hs::prefill_down_kernel<true> : (const void*)hs::prefill_down_kernel<false>;
     if (set_smem_attr((const void*)hs::prefill_up_kernel, up_smem) != HS_OK) return HS_ERR_CUDA;
-    if (set_smem_attr((const void*)hs::prefill_down_kernel, dn_smem) != HS_OK) return HS_ERR_CUDA;
+    if (set_smem_attr(dn_kernel, dn_smem) != HS_OK) return HS_ERR_CUDA;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     // the meta block and the block counts are contiguous: one memset clears both
     if (cudaMemsetAsync(io.meta, 0, l.tiles - l.meta, s) != cudaSuccess) return HS_ERR_CUDA;
@@ -1275,8 +1528,17 @@ extern "C" int hs_moe_prefill(const hs_moe_layer* L, const uint16_t* x, const fl
         return HS_ERR_CUDA;
     if (launch_pdl(hs::prefill_up_kernel, dim3(sms), dim3(hs::kGemmThreads), up_smem, s, P, io, tm) != cudaSuccess)
         return HS_ERR_CUDA;
-    if (launch_pdl(hs::prefill_down_kernel, dim3(sms), dim3(hs::kGemmThreads), dn_smem, s, P, io, tm) != cudaSuccess)
+    if (gather) {
+        if (launch_pdl(hs::prefill_gather_kernel, dim3(l.max_tiles, hs::kGatherParts), dim3(256), 0, s, P, io) !=
+            cudaSuccess)
+            return HS_ERR_CUDA;
+        if (launch_pdl(hs::prefill_down_kernel<true>, dim3(sms), dim3(hs::kGemmThreads), dn_smem, s, P, io, tm) !=
+            cudaSuccess)
+            return HS_ERR_CUDA;
+    } else if (launch_pdl(hs::prefill_down_kernel<false>, dim3(sms), dim3(hs::kGemmThreads), dn_smem, s, P, io, tm) !=
+               cudaSuccess) {
         return HS_ERR_CUDA;
+    }
     if (launch_pdl(hs::prefill_combine_kernel, dim3(4 * sms), dim3(256), 0, s, P, io) != cudaSuccess)
         return HS_ERR_CUDA;
     if ((io.dbg_live || io.dbg_tile_live) &&

@@ -25,6 +25,7 @@ HS_ERR_TIMEOUT = -6
 HS_FORCE_DENSE = 0x1
 HS_BATCH_EXPERT_UNION = 0x2
 HS_DOWN_ROW_SCALES = 0x4
+HS_PREFILL_ROW_GATHER = 0x8
 
 
 class HsError(RuntimeError):

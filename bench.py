@@ -524,6 +524,31 @@ def bench_p_sweep(args, layers, X, LG, dev, stream, timed, bytemodel, hs, peak):
     return out
 
 
+def union_fractions(idx, words, NS, NR, tiles=(32, 128)):
+    """Mean over token tiles of the fraction of an expert's neurons that are
+    live for some token of the tile (the union), from the kernel's own
+    (token, slot) live masks: each routed expert's tokens in token order cut
+    into tiles of 32 and 128, the shared expert's likewise."""
+    import numpy as np
+    T, K = idx.shape
+    w = words.view(np.uint64)
+    gs, gr = NS // 64, NR // 64
+    bits = lambda a: np.unpackbits(a.view(np.uint8), axis=-1).sum(axis=-1)
+    out = {}
+    for tt in tiles:
+        fr = []
+        for e in range(int(idx.max()) + 1):
+            toks, slots = np.nonzero(idx == e)
+            rows = np.stack([w[b, gs + j * gr:gs + (j + 1) * gr] for b, j in zip(toks, slots)]) if len(toks) else None
+            for r in range(0, len(toks), tt):
+                fr.append(bits(np.bitwise_or.reduce(rows[r:r + tt], axis=0)).sum() / NR)
+        fs = [bits(np.bitwise_or.reduce(w[r:r + tt, :gs], axis=0)).sum() / NS for r in range(0, T, tt)]
+        out[f"tile{tt}"] = {"routed": round(float(np.mean(fr)), 4), "shared": round(float(np.mean(fs)), 4)}
+    out["note"] = ("synthetic activations are independent per token (p = 0.1 on the 70% of neurons not dead), "
+                   "so a tile's union approaches the live 70%; real prompts' activations are correlated")
+    return out
+
+
 def bench_prefill(args, dev, stream, timed, hs, peaks):
     """Prefill of a 2048-token chunk through one MoE layer (30% of every
     expert's neurons permanently dead, p = 0.1 on the rest).  Roofline: the
@@ -543,12 +568,17 @@ def bench_prefill(args, dev, stream, timed, hs, peaks):
     WS = torch.zeros(dl.prefill_workspace_size(T), dtype=torch.uint8, device=dev)
     dbg = {"tiles": torch.zeros(2, dtype=torch.int32, device=dev),
            "work": torch.zeros(3, dtype=torch.int64, device=dev)}
+    # the first call also returns the routing and every (token, slot) live mask, for the union statistic
+    dbg0 = dict(dbg, topk_idx=torch.zeros((T, 6), dtype=torch.int32, device=dev),
+                topk_w=torch.zeros((T, 6), dtype=torch.float32, device=dev),
+                live_mask=torch.zeros((T, NS // 64 + 6 * NR // 64), dtype=torch.int64, device=dev))
     with torch.cuda.stream(stream):
-        hs.hs_moe_prefill(dl.c, X, LG, T, Y, None, 0, dbg, WS, stream=stream)
+        hs.hs_moe_prefill(dl.c, X, LG, T, Y, None, 0, dbg0, WS, stream=stream)
     stream.synchronize()
     assert hs.hs_device_status() == hs.HS_OK
     tiles = [int(v) for v in dbg["tiles"].cpu()]
     work = [int(v) for v in dbg["work"].cpu()]
+    union = union_fractions(dbg0["topk_idx"].cpu().numpy(), dbg0["live_mask"].cpu().numpy(), NS, NR)
     up_flops = 2 * H * (T * 6 * NR + T * NS)
     down_alg = 2 * H * work[0]      # union-live rows per (expert, token tile)
     down_exec = 2 * H * work[1]     # rows of the 64-neuron tiles not skipped
@@ -565,6 +595,16 @@ def bench_prefill(args, dev, stream, timed, hs, peaks):
     ms, runs = timed(g_sparse, K, 3, repeats=3)
     ms_dense = timed(g_dense, K, 3, repeats=3)[0]
     us = ms * 1e3 / K
+    # the row gather (HS_PREFILL_ROW_GATHER): k-steps over each tile's union-live rows
+    with torch.cuda.stream(stream):
+        hs.hs_moe_prefill(dl.c, X, LG, T, Y, None, hs.HS_PREFILL_ROW_GATHER, dbg, WS, stream=stream)
+    stream.synchronize()
+    assert hs.hs_device_status() == hs.HS_OK
+    tiles_g = [int(v) for v in dbg["tiles"].cpu()]
+    work_g = [int(v) for v in dbg["work"].cpu()]
+    g_gather = graph(hs.HS_PREFILL_ROW_GATHER)
+    us_g = timed(g_gather, K, 3, repeats=3)[0] * 1e3 / K
+    del g_gather
     alg = up_flops + down_alg
     achieved = alg / (us * 1e-6) / 1e12
     peak = float(peaks.get("bf16_tflops", 1900.0)) if peaks else 1900.0
@@ -580,7 +620,12 @@ def bench_prefill(args, dev, stream, timed, hs, peaks):
                         "peak_source": "measured" if peaks else "fallback",
                         "flops": "up dense + down over union-live rows per (expert, token tile)",
                         "executed_TFLOPs": round((up_flops + down_exec) / (us * 1e-6) / 1e12, 1)},
-           "operands": "fp16 x fp16 -> fp32 (tcgen05.mma kind::f16, accumulators in TMEM)"}
+           "operands": "fp16 x fp16 -> fp32 (tcgen05.mma kind::f16, accumulators in TMEM)",
+           "row_gather": {"flag": "HS_PREFILL_ROW_GATHER", "us_per_chunk": round(us_g, 2),
+                          "skipped_ksteps": tiles_g[0], "ksteps_without_skip": tiles_g[1],
+                          "gflop_down_executed": round(2 * H * work_g[1] / 1e9, 2),
+                          "achieved_TFLOPs": round(alg / (us_g * 1e-6) / 1e12, 1)},
+           "union_live_fraction": union}
     del g_sparse, g_dense, dl
     # our sub-configuration: the same 30% dead, but as whole 64-neuron groups (seeded choice per
     # expert, shared included), so that the tile skip has whole tiles to skip

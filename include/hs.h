@@ -82,6 +82,14 @@ typedef struct CUstream_st* hs_stream_t;
                                  instead of once per group of up to 4 of its
                                  tokens (fused kernel, the default); results
                                  agree within the stated tolerance */
+#define HS_PREFILL_ROW_GATHER 0x8u  /* prefill (and batch decode on the prefill
+                                 kernels): the down product multiplies, per
+                                 token tile, only the neurons live for some
+                                 token of the tile, packed into dense k-steps
+                                 (section "What we do instead"); results
+                                 agree with the tile path within the fp16-
+                                 operand tolerance (the summation grouping
+                                 differs).  Ignored with HS_FORCE_DENSE */
 
 /* One 4-bit projection in one of the layouts above. */
 typedef struct {
@@ -305,12 +313,16 @@ typedef struct {
     int*   topk_idx;  /* [tokens][top_k] chosen experts, descending logit  */
     float* topk_w;    /* [tokens][top_k] router weights                    */
     int*   tiles;     /* int[2]: 64-neuron down tiles skipped, considered,
-                         summed over (expert, token tile) pairs            */
+                         summed over (expert, token tile) pairs; with
+                         HS_PREFILL_ROW_GATHER: [0] the down k-steps the
+                         gather saves against one per 64-neuron group      */
     long long* work;  /* int64[3], each summed over (expert, token tile)
                          pairs of the tile's tokens times: [0] the neurons
                          live for at least one of them (the union), [1] the
                          neurons the down product multiplied (64 per tile
-                         not skipped), [2] all of the expert's neurons.
+                         not skipped, or per k-step with the row gather,
+                         padding entries included), [2] all of the
+                         expert's neurons.
                          Down-product flops = 2 * hidden * each entry.     */
     uint64_t* live_mask; /* [tokens][units] the kernel's live sets (h > 0 in
                          its fp16 h), laid out as hs_decode_debug.live_mask */

@@ -210,3 +210,37 @@ def union_counts_from_masks(words, idx, NS, NR, K):
     rows = sum(int(mask_bits(v).sum()) for v in per.values())
     groups = sum(int((v != 0).sum()) for v in per.values())
     return rows, groups
+
+
+def plan_ksteps(union_words) -> int:
+    """Down-product k-steps of one token tile under the prefill's row gather,
+    from the tile's union-live words (uint64 [NG], bit i of word g = neuron
+    64 g + i live for some token of the tile).  The rule, restated from its
+    description: each group's live neurons padded to a multiple of 8 entries;
+    k-steps of 64 entries holding at most two groups (a third group closes
+    the k-step, whose tail stays padding); a plan of more k-steps than
+    groups gives way to one k-step per group."""
+    NG = len(union_words)
+    ks, fill, groups = 0, 0, 0
+    for w in union_words:
+        c = bin(int(w)).count("1")
+        if c == 0:
+            continue
+        left = -(-c // 8) * 8
+        if fill > 0 and groups == 2:
+            ks, fill, groups = ks + 1, 0, 0
+        first = True
+        while left:
+            if fill == 0:
+                groups = 1
+            elif first:
+                groups = 2
+            first = False
+            take = min(64 - fill, left)
+            fill += take
+            left -= take
+            if fill == 64:
+                ks, fill, groups = ks + 1, 0, 0
+    if fill:
+        ks += 1
+    return ks if ks <= NG else NG

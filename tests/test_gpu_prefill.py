@@ -22,7 +22,7 @@ import torch
 
 import oracle
 import synth
-from _util import check_bf16_rounding, check_close, check_token_live_masks, mask_bits
+from _util import check_bf16_rounding, check_close, check_token_live_masks, mask_bits, plan_ksteps
 from activation_sparse_moe_gb300 import hs
 from activation_sparse_moe_gb300.layer import DeviceLayer, from_synth_expert, from_synth_stack
 
@@ -96,10 +96,12 @@ def kernel_tiles(dl, idx, words):
     return out
 
 
-def check_tiles_from_masks(dl, dbg, what, dense=False):
+def check_tiles_from_masks(dl, dbg, what, dense=False, gather=False):
     """Each tile's multiplied 64-neuron tiles are exactly the groups where the
     union of its tokens' masks has a live neuron (all of them with the dense
-    flag); the skip and work counts follow."""
+    flag); the skip and work counts follow.  With the row gather the down
+    product runs the k-steps of each tile's plan instead (plan_ksteps of the
+    union words): 'skipped' counts the k-steps saved against one per group."""
     words = dbg["live_mask"].numpy().view(np.uint64)
     tl = dbg["tile_live"].numpy().view(np.uint64)
     tiles = kernel_tiles(dl, dbg["topk_idx"].numpy(), words)
@@ -109,17 +111,18 @@ def check_tiles_from_masks(dl, dbg, what, dense=False):
         want = sum(1 << int(j) for j in np.flatnonzero(gl)) if not dense else (1 << NK) - 1
         assert int(tl[i]) == want, (what, i, hex(int(tl[i])), hex(want))
         total += NK
-        skipped += NK - int(bin(want).count("1"))
+        nks = plan_ksteps([int(v) for v in w]) if gather and not dense else int(bin(want).count("1"))
+        skipped += NK - nks
         union += nt * int(mask_bits(w[None])[0].sum())
-        execd += nt * 64 * int(bin(want).count("1"))
+        execd += nt * 64 * nks
         dense_w += nt * 64 * NK
     assert [int(v) for v in dbg["tiles"]] == [skipped, total], what
     assert [int(v) for v in dbg["work"]] == [union, execd, dense_w], what
     return skipped
 
 
-def check_prefill(L, dl, X, LG, K, what, flips_allowed=4):
-    y, yf, dbg = run_prefill(dl, X, LG)
+def check_prefill(L, dl, X, LG, K, what, flips_allowed=4, flags=0):
+    y, yf, dbg = run_prefill(dl, X, LG, flags=flags)
     ref = oracle.moe_tokens(X, LG, L.routed_expert, L.shared, k=K)
     assert np.array_equal(dbg["topk_idx"].numpy(), ref["idx"]), what
     np.testing.assert_allclose(dbg["topk_w"].double().numpy(), ref["w"], rtol=2e-6, atol=1e-7)
@@ -131,7 +134,7 @@ def check_prefill(L, dl, X, LG, K, what, flips_allowed=4):
           f"live-set flips within the fp16 bound {flips}")
     n_neurons = X.shape[0] * ((L.shared.neurons if L.shared is not None else 0) + K * dl.routed.N)
     assert flips <= flips_allowed + n_neurons // 2000, (what, flips)
-    check_tiles_from_masks(dl, dbg, what)
+    check_tiles_from_masks(dl, dbg, what, gather=bool(flags & hs.HS_PREFILL_ROW_GATHER))
     return y, yf, dbg
 
 
@@ -145,15 +148,20 @@ def cluster_dead(L, n_groups, seed=0):
             L.offsets[e, 64 * g:64 * (g + 1)] = -np.inf
 
 
+GATHER = [0, hs.HS_PREFILL_ROW_GATHER]
+
+
+@pytest.mark.parametrize("flags", GATHER, ids=["tiles", "gather"])
 @pytest.mark.parametrize("T", [1, 37, 300])
-def test_small_prefill(T):
+def test_small_prefill(T, flags):
     H, E, NR, NS, K = 512, 8, 128, 256, 3
     L = synth.layer_inputs(0, "t-prefill", 0, E, NR, NS, H, p=0.2, p_shared=0.3)
     X, LG = synth.tokens(0, "t-prefill", T, T, H, E)
-    check_prefill(L, make_layer(L, K), X, LG, K, f"small T={T}")
+    check_prefill(L, make_layer(L, K), X, LG, K, f"small T={T} flags={flags}", flags=flags)
 
 
-def test_multi_tile_experts_and_clustered_dead():
+@pytest.mark.parametrize("flags", GATHER, ids=["tiles", "gather"])
+def test_multi_tile_experts_and_clustered_dead(flags):
     """More than 256 tokens per expert (several token tiles), the shared expert
     over 4 tiles, and whole dead 64-neuron groups that the skip must find."""
     H, E, NR, NS, K = 256, 4, 256, 192, 2
@@ -161,18 +169,44 @@ def test_multi_tile_experts_and_clustered_dead():
     cluster_dead(L, 2, seed=2)
     T = 900
     X, LG = synth.tokens(2, "t-prefill-mt", 0, T, H, E)
-    y, yf, dbg = check_prefill(L, make_layer(L, K), X, LG, K, "multi-tile")
+    y, yf, dbg = check_prefill(L, make_layer(L, K), X, LG, K, f"multi-tile flags={flags}", flags=flags)
     assert int(dbg["tiles"][0]) >= 2 * E * 2   # every routed tile skips at least the dead groups
 
 
-def test_no_shared_with_ties_and_ragged_neurons():
+@pytest.mark.parametrize("flags", GATHER, ids=["tiles", "gather"])
+def test_no_shared_with_ties_and_ragged_neurons(flags):
     """No shared expert, tied logits, a neuron count that is not a multiple of
     128 (the last 128-neuron block is half empty)."""
     H, E, NR, K = 128, 6, 192, 2
     L = synth.layer_inputs(1, "t-prefill-ns", 0, E, NR, 0, H, p=0.3, dead_frac=0.3)
     X, LG = synth.tokens(1, "t-prefill-ns", 0, 50, H, E)
     LG[3, :] = 0.5
-    check_prefill(L, make_layer(L, K), X, LG, K, "no shared, ties")
+    check_prefill(L, make_layer(L, K), X, LG, K, f"no shared, ties flags={flags}", flags=flags)
+
+
+def test_row_gather_deterministic_dense_flag_and_scattered_dead():
+    """The row gather on scattered dead neurons (no 64-neuron group is dead
+    for a whole tile, so the tile skip saves nothing and the gather saves the
+    k-steps of the dead rows): repeat calls give the same bits; its result
+    agrees with the tile path within the oracle's bar (the k-steps group the
+    fp32 sums differently); with HS_FORCE_DENSE the flag is ignored and the
+    call equals the plain dense call bit for bit."""
+    H, E, NR, NS, K = 256, 4, 512, 256, 2
+    L = synth.layer_inputs(5, "t-prefill-g", 0, E, NR, NS, H, p=0.1, p_shared=0.1, dead_frac=0.4)
+    dl = make_layer(L, K)
+    X, LG = synth.tokens(5, "t-prefill-g", 0, 700, H, E)
+    G = hs.HS_PREFILL_ROW_GATHER
+    y1, yf1, d1 = check_prefill(L, dl, X, LG, K, "gather, scattered dead", flags=G)
+    y2, yf2, d2 = run_prefill(dl, X, LG, flags=G)
+    assert np.array_equal(yf1, yf2) and torch.equal(y1, y2)
+    yt, yft, dt = run_prefill(dl, X, LG)
+    assert int(dt["tiles"][0]) == 0 and int(d1["tiles"][0]) > 0
+    assert torch.equal(d1["live_mask"], dt["live_mask"])
+    np.testing.assert_allclose(yf1, yft, rtol=0, atol=1e-4 * np.abs(yft).max())
+    yd, yfd, dd = run_prefill(dl, X, LG, flags=hs.HS_FORCE_DENSE)
+    ydg, yfdg, ddg = run_prefill(dl, X, LG, flags=hs.HS_FORCE_DENSE | G)
+    assert np.array_equal(yfd, yfdg) and torch.equal(yd, ydg)
+    assert [int(v) for v in ddg["tiles"]] == [int(v) for v in dd["tiles"]]
 
 
 def test_dense_flag_bit_identical_and_deterministic():
@@ -221,12 +255,13 @@ def cfg5():
     return L, make_layer(L, 6), X, LG
 
 
-def test_config5_sampled_parity(cfg5):
+@pytest.mark.parametrize("flags", GATHER, ids=["tiles", "gather"])
+def test_config5_sampled_parity(cfg5, flags):
     """Full size, in the launch configuration the bench times; the oracle
     evaluates a sample of tokens one by one (each token's output depends on
     that token alone)."""
     L, dl, X, LG = cfg5
-    y, yf, dbg = run_prefill(dl, X, LG)
+    y, yf, dbg = run_prefill(dl, X, LG, flags=flags)
     rng = np.random.default_rng(5)
     sample = np.sort(rng.choice(X.shape[0], size=16, replace=False))
     ref = oracle.moe_tokens(X[sample], LG[sample], L.routed_expert, L.shared, k=6)
@@ -238,8 +273,11 @@ def test_config5_sampled_parity(cfg5):
                                    "fp16", "config 5 sampled")
     print(f"config 5 sampled: rel-L2 {rel:.2e} max-abs/max {mx:.2e} bf16 max ulps {ulps:.0f} flips {flips}")
     assert flips <= 4 + len(sample) * (synth.N_SHARED + 6 * synth.N_ROUTED) // 2000
-    skipped = check_tiles_from_masks(dl, dbg, "config 5")
-    print(f"config 5: skipped 64-neuron tiles {skipped}")
+    gather = bool(flags & hs.HS_PREFILL_ROW_GATHER)
+    skipped = check_tiles_from_masks(dl, dbg, "config 5", gather=gather)
+    print(f"config 5 flags={flags}: skipped k-steps {skipped}")
+    if gather:   # the scattered 30% dead rows leave about a quarter of the k-steps out
+        assert skipped > int(dbg["tiles"][1]) // 5
     # every (expert, token tile) pair is counted once: 58-tile shared expert + 29 tiles per routed tile
     counts = np.bincount(dbg["topk_idx"].numpy().ravel(), minlength=128)
     tiles = int(sum((c + TILE - 1) // TILE for c in counts)) * (synth.N_ROUTED // 64)
@@ -256,7 +294,8 @@ def test_config5_dense_flag_equal(cfg5):
     assert int(dd["tiles"][0]) == 0
 
 
-def test_config5_layer_at_max_tokens(cfg5):
+@pytest.mark.parametrize("flags", GATHER, ids=["tiles", "gather"])
+def test_config5_layer_at_max_tokens(cfg5, flags):
     """The largest prompt chunk the library takes (4096 tokens: 24,576 routed
     pairs, 32 shared-expert tiles) on the full-size layer: sampled tokens
     (the first, the last and random ones; each routed expert's last tile is
@@ -265,7 +304,7 @@ def test_config5_layer_at_max_tokens(cfg5):
     T = 4096
     assert dl.prefill_workspace_size(T) > 0 and dl.prefill_workspace_size(T + 1) == 0
     X, LG = synth.tokens(0, "cfg5-max", 0, T)
-    y, yf, dbg = run_prefill(dl, X, LG)
+    y, yf, dbg = run_prefill(dl, X, LG, flags=flags)
     rng = np.random.default_rng(6)
     sample = np.unique(np.concatenate([[0, T - 1], rng.choice(T, size=10, replace=False)]))
     ref = oracle.moe_tokens(X[sample], LG[sample], L.routed_expert, L.shared, k=6)
@@ -275,7 +314,7 @@ def test_config5_layer_at_max_tokens(cfg5):
     words = dbg["live_mask"].numpy().view(np.uint64)
     check_token_live_masks(words[sample], X[sample], ref, L.shared, L.routed_expert, synth.N_ROUTED, 6, "fp16",
                            "4096 tokens sampled")
-    check_tiles_from_masks(dl, dbg, "4096 tokens")
+    check_tiles_from_masks(dl, dbg, "4096 tokens", gather=bool(flags & hs.HS_PREFILL_ROW_GATHER))
     counts = np.bincount(dbg["topk_idx"].numpy().ravel(), minlength=128)
     tiles = int(sum((c + TILE - 1) // TILE for c in counts)) * (synth.N_ROUTED // 64)
     tiles += (T // TILE) * (synth.N_SHARED // 64)
@@ -283,7 +322,8 @@ def test_config5_layer_at_max_tokens(cfg5):
     assert np.isfinite(yf).all()
 
 
-def test_config5_repeated_calls_bit_identical(cfg5):
+@pytest.mark.parametrize("flags", GATHER, ids=["tiles", "gather"])
+def test_config5_repeated_calls_bit_identical(cfg5, flags):
     """Determinism under repetition: the full-size prefill called 16 times on
     the same inputs (fresh and reused workspaces alternating) gives the same
     bits every time."""
@@ -296,7 +336,7 @@ def test_config5_repeated_calls_bit_identical(cfg5):
         ws = ws_keep if i % 2 else torch.zeros_like(ws_keep)
         yf = torch.empty((T, H), dtype=torch.float32, device="cuda")
         y = torch.empty((T, H), dtype=torch.bfloat16, device="cuda")
-        hs.hs_moe_prefill(dl.c, Xc, LGc, T, y, yf, 0, None, ws)
+        hs.hs_moe_prefill(dl.c, Xc, LGc, T, y, yf, flags, None, ws)
         torch.cuda.synchronize()
         if ref is None:
             ref = yf.clone()
