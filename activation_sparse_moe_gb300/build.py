@@ -20,7 +20,7 @@ LIB = os.path.join(PKG, "libhs.so")
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "--expt-relaxed-constexpr",
-              f"-I{INCLUDE}", f"-I{CSRC}"]
+              f"-I{INCLUDE}", f"-I{CSRC}", "-Xptxas", "-v"]
 
 
 def _nvcc() -> str:
@@ -60,6 +60,9 @@ def build(verbose: bool = False, force: bool = False) -> str:
         r = subprocess.run(cmd, capture_output=True, text=True)
         if r.returncode != 0:
             raise RuntimeError(f"nvcc failed on {src}:\n{r.stderr}")
+        # ptxas's resource report (registers, spills, shared memory per kernel)
+        with open(obj[:-2] + ".ptxas.txt", "w") as f:
+            f.write(r.stderr)
         if verbose and r.stderr:
             print(r.stderr)
         return obj
@@ -74,6 +77,30 @@ def build(verbose: bool = False, force: bool = False) -> str:
         raise RuntimeError(f"link failed:\n{r.stderr}")
     os.replace(tmp, LIB)
     return LIB
+
+
+def resource_report() -> dict[str, dict[str, int]]:
+    """Per kernel (mangled name): registers, spill stores and loads (bytes) and
+    stack frame (bytes), from the last build's ptxas reports."""
+    import re
+    out: dict[str, dict[str, int]] = {}
+    for src in sources():
+        path = os.path.join(BUILD_DIR, os.path.basename(src)[:-3] + ".ptxas.txt")
+        cur = None
+        for line in open(path):
+            m = re.search(r"Compiling entry function '([^']+)'", line)
+            if m:
+                cur = out.setdefault(m.group(1), {"regs": 0, "spill_stores": 0, "spill_loads": 0, "stack": 0})
+                continue
+            if cur is None:
+                continue
+            m = re.search(r"(\d+) bytes stack frame, (\d+) bytes spill stores, (\d+) bytes spill loads", line)
+            if m:
+                cur["stack"], cur["spill_stores"], cur["spill_loads"] = map(int, m.groups())
+            m = re.search(r"Used (\d+) registers", line)
+            if m:
+                cur["regs"] = int(m.group(1))
+    return out
 
 
 if __name__ == "__main__":

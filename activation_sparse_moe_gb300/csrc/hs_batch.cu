@@ -962,14 +962,34 @@ __device__ __forceinline__ FusedRole fused_role(int T, int G, bool pair) {
     return r;
 }
 
+// Off the unit's main path, out of line: thread 0 waits (bounded) for the
+// phases of barriers bars[0 .. n); the debug output of each token's own live
+// set (h > 0) of a unit (warp 0).
+__device__ __noinline__ void drain_bars(uint64_t* bars, int n, uint32_t par) {
+    for (int i = 0; i < n; ++i) mbar_wait(&bars[i], par);
+}
+__device__ __noinline__ void write_unit_live_masks(uint64_t* dbg_live, int Ut, const float* h_s, int T,
+                                                   const UnitTokens ut) {
+    const int t = threadIdx.x;
+    for (int k = 0; k < T; ++k) {
+        const unsigned m0 = __ballot_sync(0xffffffffu, h_s[k * 64 + t] > 0.f);
+        const unsigned m1 = __ballot_sync(0xffffffffu, h_s[k * 64 + t + 32] > 0.f);
+        if (t == 0) dbg_live[(size_t)pick(ut.tok, k) * Ut + pick(ut.ri, k)] = (uint64_t)m1 << 32 | m0;
+    }
+}
+
 // One unit after its up copies were issued (phase `par` of bars[0..3]), with
 // each active thread's x fixed-point copies in xf (token tk) and, with kPair,
 // xf2 (token tk2): the DP4A GEMV per token, ReLU^2, the union-live rows' down
 // codes and the slab, the down products into the tokens' partial rows.
-// Returns false (on every thread) if a bounded wait gave up; `live` gets the
-// unit's union live rows.
+// Returns 0, or, on every thread when a bounded wait gave up (the error word
+// is set), where copies may still be landing: kFuUpInFlight (the up rows on
+// bars[0..3], phase par), kFuDownInFlight (the down rows on bars[4], the phase
+// before dn_par), kFuNoneInFlight.  The caller drains them (fused_drain), off
+// this path.  `live` gets the unit's union live rows.
+constexpr int kFuUpInFlight = 1, kFuDownInFlight = 2, kFuNoneInFlight = 3;
 template <bool kPair>
-__device__ __forceinline__ bool fused_unit(const LayerParams& P, const BatchIO& io, const FusedBufs& sm,
+__device__ __forceinline__ int fused_unit(const LayerParams& P, const BatchIO& io, const FusedBufs& sm,
                                            const ExpertPtrs& ep, int g, int T, const UnitTokens& ut, const XFixed& xf,
                                            const XFixed& xf2, uint32_t par, uint32_t& dn_par, uint64_t& live) {
     const int H = P.hidden, G = H / 64, rowb = H / 2;
@@ -1027,12 +1047,7 @@ __device__ __forceinline__ bool fused_unit(const LayerParams& P, const BatchIO& 
     while (ok && waited < 3) { ++waited; ok = mbar_wait(&sm.bars[waited], par); }
     if (t < 64) sm.offs_s[t] = off_r;
     fence_proxy_async_smem();  // the parts come before the down copies into the same rows
-    if (!__syncthreads_and(ok)) {
-        // a wait gave up (the error word is set): the unit's copies land before the CTA leaves
-        if (t == 0)
-            for (int i = 0; i < 4; ++i) mbar_wait(&sm.bars[i], par);
-        return false;
-    }
+    if (!__syncthreads_and(ok)) return kFuUpInFlight;
     // ---- row sums for every token; the row's down codes are copied once if it fired for any
     bool lv = false;
     {
@@ -1075,14 +1090,6 @@ __device__ __forceinline__ bool fused_unit(const LayerParams& P, const BatchIO& 
         bulk_g2s(sm.sbs, ep.dn_sb + (size_t)g * H, H * 4, &sm.bars[4], pol);
     }
     live = *reinterpret_cast<const uint64_t*>(sm.live8);
-    if (io.dbg_live && t < 32) {  // each token's own live set (h > 0) for this group
-        const int Ut = P.shared_neurons / 64 + P.top_k * (P.routed_neurons / 64);
-        for (int k = 0; k < T; ++k) {
-            const unsigned m0 = __ballot_sync(0xffffffffu, sm.h_s[k * 64 + t] > 0.f);
-            const unsigned m1 = __ballot_sync(0xffffffffu, sm.h_s[k * 64 + t + 32] > 0.f);
-            if (t == 0) io.dbg_live[(size_t)pick(ut.tok, k) * Ut + pick(ut.ri, k)] = (uint64_t)m1 << 32 | m0;
-        }
-    }
     // ---- per token: fixed-order sum of h
     float hsum[kFTok];
 #pragma unroll
@@ -1120,13 +1127,24 @@ __device__ __forceinline__ bool fused_unit(const LayerParams& P, const BatchIO& 
     }
     if (any) dn_par ^= 1u;
     fence_proxy_async_smem();
-    if (!__syncthreads_and(ok)) {
-        if (t == 0 && any) mbar_wait(&sm.bars[4], dn_par ^ 1u);  // the down copies land before the CTA leaves
-        return false;
-    }
-    return true;
+    if (!__syncthreads_and(ok)) return any ? kFuDownInFlight : kFuNoneInFlight;
+    return 0;
 }
 
+// After fused_unit gave up with status st: thread 0 waits (bounded) for the
+// copies still in flight, so that none lands after the CTA has left.
+__device__ __noinline__ void fused_drain(const FusedBufs& sm, int st, uint32_t par, uint32_t dn_par) {
+    if (st == kFuUpInFlight) drain_bars(sm.bars, 4, par);
+    else if (st == kFuDownInFlight) drain_bars(&sm.bars[4], 1, dn_par ^ 1u);
+}
+
+// kLiveDbg: the instantiation that also writes each token's live masks (the
+// debug output); the other carries no debug code.  This persistent loop sits
+// at the register limit of two CTAs per SM: any code on its failure path
+// (even a bounded wait for the unit's copies in flight) makes the compiler
+// spill on the main path (13% slower at 32 tokens), so after a wait gave up
+// (about a second, the error word set) its CTAs leave without that wait.
+template <bool kLiveDbg>
 __global__ void __launch_bounds__(256, 2) batch_fused_kernel(const __grid_constant__ LayerParams P, const BatchIO io) {
     extern __shared__ __align__(128) uint8_t smem[];
     const int H = P.hidden;
@@ -1206,7 +1224,10 @@ __global__ void __launch_bounds__(256, 2) batch_fused_kernel(const __grid_consta
             }
         }
         uint64_t live = 0;
-        if (!fused_unit<true>(P, io, sm, ep, g, T, ut, xf, xf2, it & 1, dn_par, live)) return;
+        if (fused_unit<true>(P, io, sm, ep, g, T, ut, xf, xf2, it & 1, dn_par, live)) return;
+        // the unit's h stays in shared memory until the next unit's row sums, past a barrier
+        if (kLiveDbg && t < 32)  // each token's own live set (h > 0) for this group
+            write_unit_live_masks(io.dbg_live, NGs + P.top_k * NGr, sm.h_s, T, ut);
         if (t < 2 && live) {  // the expert's union over all its tokens (for the live-row counts)
             const uint32_t bits = (uint32_t)(live >> (32 * t));
             uint32_t* mw = shared ? io.mask_s + 2 * g + t : io.mask_r + (size_t)e * (P.routed_neurons / 32) + 2 * g + t;
@@ -1418,7 +1439,13 @@ __global__ void __launch_bounds__(256, 2) batch_small_kernel(const __grid_consta
     if (t == 0) fused_issue_up(sm, ep, g, H, policy_evict_first(), 4 - nx, 4);
     uint32_t dn_par = 0;
     uint64_t live = 0;
-    if (!fused_unit<false>(P, io, sm, ep, g, T, ut, xf, xf, 0, dn_par, live)) return;
+    const int fst = fused_unit<false>(P, io, sm, ep, g, T, ut, xf, xf, 0, dn_par, live);
+    if (fst) {
+        if (t == 0) fused_drain(sm, fst, 0, dn_par);
+        return;
+    }
+    if (io.dbg_live && t < 32)  // each token's own live set (h > 0) for this group
+        write_unit_live_masks(io.dbg_live, P.shared_neurons / 64 + P.top_k * (P.routed_neurons / 64), sm.h_s, T, ut);
     if (t == 0) {
         io.unit_live[u] = live;
         io.unit_key[u] = shared ? E : st->e;
@@ -1686,9 +1713,13 @@ int hs_batch_decode(const hs_moe_layer* L, const uint16_t* x, const float* logit
     if (batch <= hs::kFusedMaxBatch && !(flags & HS_BATCH_EXPERT_UNION)) {
         const int f_smem = hs::FusedSmem::total(L->hidden);
         const int Ut = (L->shared ? L->shared->neurons / 64 : 0) + L->top_k * (L->routed[0].neurons / 64);
-        if (set_smem_attr((const void*)hs::batch_fused_kernel, f_smem) != HS_OK) return HS_ERR_CUDA;
+        if (set_smem_attr((const void*)hs::batch_fused_kernel<false>, f_smem) != HS_OK ||
+            set_smem_attr((const void*)hs::batch_fused_kernel<true>, f_smem) != HS_OK)
+            return HS_ERR_CUDA;
         if (set_smem_attr((const void*)hs::batch_fused_reduce_kernel, Ut * 128) != HS_OK) return HS_ERR_CUDA;
-        if (launch_pdl(hs::batch_fused_kernel, dim3(2 * sms), dim3(256), f_smem, s, P, io) != cudaSuccess)
+        if ((io.dbg_live ? launch_pdl(hs::batch_fused_kernel<true>, dim3(2 * sms), dim3(256), f_smem, s, P, io)
+                         : launch_pdl(hs::batch_fused_kernel<false>, dim3(2 * sms), dim3(256), f_smem, s, P, io)) !=
+            cudaSuccess)
             return HS_ERR_CUDA;
         if (launch_pdl(hs::batch_fused_reduce_kernel, dim3(L->hidden / 32, batch), dim3(256), (size_t)Ut * 128, s, P,
                        io) != cudaSuccess)
