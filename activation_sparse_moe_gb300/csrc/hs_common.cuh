@@ -154,6 +154,16 @@ __device__ __forceinline__ void cp_async_arrive_noinc(uint64_t* bar) {
 }
 __device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
 
+// Brings the 128-byte line of p into L2 (no value is returned).
+__device__ __forceinline__ void prefetch_l2(const void* p) {
+    asm volatile("prefetch.global.L2 [%0];" ::"l"(p));
+}
+// Lines [p, p + bytes) into L2, one line per lane of the calling warp.
+__device__ __forceinline__ void prefetch_l2_span(const void* p, int bytes, int lane) {
+    const char* c = static_cast<const char*>(p);
+    for (int off = 128 * lane; off < bytes; off += 32 * 128) prefetch_l2(c + off);
+}
+
 __device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 __device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
 

@@ -246,6 +246,12 @@ moe_decode_b1_kernel(const __grid_constant__ LayerParams P, const DecodeIO io) {
         ep = P.shared;
         if (t == 0) issue_up(ep);  // weights do not depend on the previous kernel
     }
+    // x and the logits into L2 ahead of the wait: nothing is read from them before it, and L2 holds
+    // whatever the previous kernel writes there (when it produced them, they are in L2 already)
+    if (t >= 32 && t < 64) {
+        prefetch_l2_span(io.x, hidden * 2, t - 32);
+        if (!is_shared) prefetch_l2_span(io.logits, P.n_routed * 4, t - 32);
+    }
     pdl_wait();
     pdl_trigger();
 

@@ -129,6 +129,8 @@ down_sparse_kernel(const float* __restrict__ h, const uint8_t* __restrict__ dn_c
     const int gbase = c * kDsChunk, ng = min(kDsChunk, G - gbase);
     const int rowb = hidden / 2;
     const bool dense = (flags & HS_FORCE_DENSE) != 0;
+    // h of the chunk's groups into L2 ahead of the wait (nothing is read from it before it)
+    if (warp == 1) prefetch_l2_span(h + (size_t)gbase * 64, ng * 64 * 4, lane);
     pdl_wait();
     pdl_trigger();
     // h of the chunk's groups: every load issued before any is used
