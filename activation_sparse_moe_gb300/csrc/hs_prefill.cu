@@ -37,6 +37,7 @@ namespace hs {
 constexpr int kNt = 128;          // max tokens per tile (MMA N)
 constexpr int kMaxTokens = 4096;
 constexpr int kTokBlk = 8;       // tokens per CTA of the list/gather kernel
+constexpr int kSuperBlk = 16;    // token blocks per superblock (pair counts are kept per superblock too)
 constexpr int kMaxKTiles = 64;    // 64-neuron tiles per expert (neurons <= 4096): one 64-bit mask
 
 struct PrefillMeta {
@@ -63,6 +64,7 @@ struct PrefillIO {
     unsigned flags;
     PrefillMeta* meta;
     int* blk_cnt;             // [ceil(T / kTokBlk)][E] pairs per (token block, expert), zeroed with meta
+    int* sb_cnt;              // [ceil(T / (kTokBlk * kSuperBlk))][E] the same per superblock, zeroed with meta
     TileInfo* tiles;          // [max tiles]
     int* idx;                 // [T][K]
     float* w;                 // [T][K]
@@ -115,6 +117,7 @@ __global__ void __launch_bounds__(256) prefill_route_kernel(const __grid_constan
             const int e = io.idx[(size_t)tok * K + lane];
             atomicAdd(&io.meta->cnt[e], 1);
             atomicAdd(&io.blk_cnt[(tok / kTokBlk) * P.n_routed + e], 1);
+            atomicAdd(&io.sb_cnt[(tok / (kTokBlk * kSuperBlk)) * P.n_routed + e], 1);
             if (io.dbg_idx) io.dbg_idx[(size_t)tok * K + lane] = e;
             if (io.dbg_w) io.dbg_w[(size_t)tok * K + lane] = io.w[(size_t)tok * K + lane];
         }
@@ -210,17 +213,25 @@ __global__ void __launch_bounds__(kListThreads) prefill_list_kernel(const __grid
     pdl_trigger();
     const int E = P.n_routed, K = P.top_k, H = P.hidden, n = io.T * K;
     const int b = blockIdx.x, t0 = b * kTokBlk, nt = min(kTokBlk, io.T - t0), t = threadIdx.x;
-    // expert offsets of this token block: the expert's offset plus its pairs in earlier blocks,
-    // loaded 16 blocks at a time so that the loads are in flight together
+    // expert offsets of this token block: the expert's offset, plus its pairs in the superblocks
+    // before this block's (at most 31), plus those in the earlier blocks of this block's superblock
+    // (at most kSuperBlk - 1); every load of a pass in flight together
+    const int sb = b / kSuperBlk;
     for (int e = t; e < E; e += blockDim.x) {
         int c = __ldcg(&io.meta->off[e]);
-        for (int b0 = 0; b0 < b; b0 += 16) {
+        for (int s0 = 0; s0 < sb; s0 += 16) {
             int v[16];
 #pragma unroll
-            for (int i = 0; i < 16; ++i) v[i] = b0 + i < b ? __ldcg(&io.blk_cnt[(b0 + i) * E + e]) : 0;
+            for (int i = 0; i < 16; ++i) v[i] = s0 + i < sb ? __ldcg(&io.sb_cnt[(s0 + i) * E + e]) : 0;
 #pragma unroll
             for (int i = 0; i < 16; ++i) c += v[i];
         }
+        int w[kSuperBlk - 1];
+#pragma unroll
+        for (int i = 0; i < kSuperBlk - 1; ++i)
+            w[i] = kSuperBlk * sb + i < b ? __ldcg(&io.blk_cnt[(kSuperBlk * sb + i) * E + e]) : 0;
+#pragma unroll
+        for (int i = 0; i < kSuperBlk - 1; ++i) c += w[i];
         base_e[e] = c;
     }
     for (int i = t; i < nt * K; i += blockDim.x) e_of[i] = __ldcg(io.idx + (size_t)t0 * K + i);
@@ -1336,7 +1347,7 @@ bool make_map(EncodeTiledFn enc, CUtensorMap* m, CUtensorMapDataType dt, const v
 }
 
 struct PrefillLayout {
-    size_t meta, blk_cnt, tiles, idx, w, pair_tok, pos_of, pair_w, xg, h_r, h_s, flags, partial, umask, nks, ksd, glist,
+    size_t meta, blk_cnt, sb_cnt, tiles, idx, w, pair_tok, pos_of, pair_w, xg, h_r, h_s, flags, partial, umask, nks, ksd, glist,
         hc_r, hc_s, total;
     int max_tiles;
 };
@@ -1351,6 +1362,7 @@ PrefillLayout prefill_layout(const hs_moe_layer* L, int T) {
     const size_t rows = (size_t)T * K + (NS ? T : 0);
     l.meta = take(sizeof(hs::PrefillMeta));
     l.blk_cnt = take((size_t)((T + hs::kTokBlk - 1) / hs::kTokBlk) * E * 4);
+    l.sb_cnt = take((size_t)((T + hs::kTokBlk * hs::kSuperBlk - 1) / (hs::kTokBlk * hs::kSuperBlk)) * E * 4);
     l.tiles = take((size_t)l.max_tiles * sizeof(hs::TileInfo));
     l.idx = take((size_t)T * K * 4);
     l.w = take((size_t)T * K * 4);
@@ -1442,6 +1454,7 @@ extern "C" int hs_moe_prefill(const hs_moe_layer* L, const uint16_t* x, const fl
     io.flags = flags;
     io.meta = reinterpret_cast<hs::PrefillMeta*>(w + l.meta);
     io.blk_cnt = reinterpret_cast<int*>(w + l.blk_cnt);
+    io.sb_cnt = reinterpret_cast<int*>(w + l.sb_cnt);
     io.tiles = reinterpret_cast<hs::TileInfo*>(w + l.tiles);
     io.idx = reinterpret_cast<int*>(w + l.idx);
     io.w = reinterpret_cast<float*>(w + l.w);
@@ -1517,7 +1530,7 @@ extern "C" int hs_moe_prefill(const hs_moe_layer* L, const uint16_t* x, const fl
     if (set_smem_attr((const void*)hs::prefill_up_kernel, up_smem) != HS_OK) return HS_ERR_CUDA;
     if (set_smem_attr(dn_kernel, dn_smem) != HS_OK) return HS_ERR_CUDA;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-    // the meta block and the block counts are contiguous: one memset clears both
+    // the meta block and the block and superblock counts are contiguous: one memset clears them
     if (cudaMemsetAsync(io.meta, 0, l.tiles - l.meta, s) != cudaSuccess) return HS_ERR_CUDA;
     // the first kernel follows the memset with ordinary stream ordering
     hs::prefill_route_kernel<<<dim3((T + 7) / 8), dim3(256), 0, s>>>(P, io);

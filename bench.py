@@ -857,7 +857,9 @@ def main():
                          "kernel": "hs_moe_layer_decode (moe_decode_b1_kernel + reduce_partials_kernel)",
                          "bytes_per_launch": round(step_bytes / n),
                          "traffic": _recorded_traffic("moe_decode_b1_kernel", src),
-                         "frac_of_8TBs": round(achieved / 8000.0, 4)},
+                         "frac_of_8TBs": round(achieved / 8000.0, 4),
+                         # the time the required bytes take at the peak, beside the measured us_per_layer
+                         "byte_floor_us_per_layer": round(step_bytes / n / (peak * 1e3), 3)},
             "e2e": {"value": round(us_e2e, 4), "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
             "gpu_launches": 2 * n * K,  # the timed region of the headline metric
             "clocks": clocks,
