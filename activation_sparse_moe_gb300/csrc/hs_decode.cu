@@ -568,7 +568,8 @@ extern "C" int hs_moe_layer_decode(const hs_moe_layer* L, const uint16_t* x, con
             if (dbg && dbg->h) return HS_ERR_INVALID_ARG;  // the h dump covers batch 1 only
             const hs_prefill_debug pd{dbg ? dbg->topk_idx : nullptr, dbg ? dbg->topk_w : nullptr, nullptr, nullptr,
                                       dbg ? dbg->live_mask : nullptr, nullptr};
-            const int st = hs_moe_prefill(L, x, logits, batch, y_bf16, y_f32, flags & HS_FORCE_DENSE,
+            const int st = hs_moe_prefill(L, x, logits, batch, y_bf16, y_f32,
+                                          flags & (HS_FORCE_DENSE | HS_PREFILL_ROW_GATHER),
                                           dbg ? &pd : nullptr, ws, ws_bytes, stream);
             if (st != HS_OK || !dbg) return st;
             return hs_prefill_union_live(L, batch, ws, dbg->live_rows, dbg->live_groups, s);

@@ -30,6 +30,8 @@ import threading
 import time
 
 ROOT = os.path.dirname(os.path.abspath(__file__))
+# fp32 FMA peak of the GPU: 152 SMs x 128 lanes x 2 flops per FMA x 2.07 GHz (maximum SM clock)
+FP32_PEAK_TFLOPS = 152 * 128 * 2 * 2.07e9 / 1e12
 sys.path.insert(0, ROOT)
 
 METRIC = "MoE-layer decode us/token (batch 1, per layer) and achieved HBM GB/s at live frac 0.1"
@@ -291,12 +293,13 @@ def time_oracle_all_cores(p, reps=6, n_layers=2, timeout_s=600):
     return wall / (n * reps), n, n * reps
 
 
-def bench_batch(args, dev, stream, timed, bytemodel, hs):
+def bench_batch(args, dev, stream, timed, bytemodel, hs, hbm_peak_gbs):
     """Batch decode through one MoE layer: 8 distinct layers with 30% of every
     expert's neurons permanently dead and p = 0.1 on the rest, cycled so that
     the weights a call reads are not left in L2 by the previous call.  B = 3
     stands for the verify step of speculative decoding (three rows through the
     same weights, sharing the permanently dead neurons)."""
+    import numpy as np
     import torch
     import synth
     from activation_sparse_moe_gb300.layer import DeviceLayer, from_synth_expert, from_synth_stack
@@ -314,17 +317,20 @@ def bench_batch(args, dev, stream, timed, bytemodel, hs):
         Y = torch.empty((n_layers, B, 2688), dtype=torch.bfloat16, device=dev)
         WS = torch.zeros(max(d.workspace_size(B) for d in layers), dtype=torch.uint8, device=dev)
         req = 0
+        token_live = 0   # sum over (token, slot) of the token's own live neurons
         with torch.cuda.stream(stream):
             for l, dl in enumerate(layers):
                 dbg = {"topk_idx": torch.empty((B, 6), dtype=torch.int32, device=dev),
                        "topk_w": torch.empty((B, 6), dtype=torch.float32, device=dev),
                        "live_rows": torch.empty(1, dtype=torch.int32, device=dev),
-                       "live_groups": torch.empty(1, dtype=torch.int32, device=dev)}
+                       "live_groups": torch.empty(1, dtype=torch.int32, device=dev),
+                       "live_mask": torch.empty((B, 3712 // 64 + 6 * 1856 // 64), dtype=torch.int64, device=dev)}
                 hs.hs_moe_layer_decode(dl.c, X[l], LG[l], B, Y[l], None, 0, dbg, WS, stream=stream)
                 stream.synchronize()
                 touched = len(set(dbg["topk_idx"].cpu().numpy().ravel().tolist()))
                 req += bytemodel.decode_layer_bytes(2688, [3712] + [1856] * touched, int(dbg["live_rows"].item()),
                                                     int(dbg["live_groups"].item()), 128, batch=B)
+                token_live += int(np.unpackbits(dbg["live_mask"].cpu().numpy().view(np.uint8)).sum())
         g = torch.cuda.CUDAGraph()
         with torch.cuda.graph(g, stream=stream):
             for l, dl in enumerate(layers):
@@ -340,9 +346,18 @@ def bench_batch(args, dev, stream, timed, bytemodel, hs):
                                        stream=stream)
         ms_u, _ = timed(gu, K, 3, repeats=3)
         us_u = ms_u * 1e3 / (K * n_layers)
+        # algorithmic work: the dense up product of every (token, expert) pair and the down product over
+        # each token's own live rows; floors at the measured HBM peak and at the fp32 FMA peak
+        # (152 SMs x 128 lanes x 2 flops x 2.07 GHz = 80.5 TFLOP/s), and which one binds
+        flop = 2 * 2688 * (B * (3712 + 6 * 1856) + token_live / n_layers)
+        hbm_floor = req / n_layers / (hbm_peak_gbs * 1e3)
+        alu_floor = flop / (FP32_PEAK_TFLOPS * 1e6)
         out[f"B{B}"] = {"us_per_layer": round(us, 3), "us_per_token_layer": round(us / B, 4),
                         "required_MB_per_layer": round(req / n_layers / 1e6, 2),
                         "achieved_GBs": round(req / n_layers / (us * 1e-6) / 1e9, 1),
+                        "gflop_per_layer": round(flop / 1e9, 3),
+                        "hbm_floor_us": round(hbm_floor, 2), "fp32_alu_floor_us": round(alu_floor, 2),
+                        "binds": "hbm" if hbm_floor >= alu_floor else "fp32 alu",
                         "expert_union_path_us_per_layer": round(us_u, 3)}
         del g, gu, WS
     del layers
@@ -822,7 +837,7 @@ def main():
         expert_down = bench_expert_down(args, dev, stream, timed, bytemodel, hs, peak)
     batch = None
     if not args.profile and args.batch_sizes:
-        batch = bench_batch(args, dev, stream, timed, bytemodel, hs)
+        batch = bench_batch(args, dev, stream, timed, bytemodel, hs, peak)
     prefill = None
     if not args.profile and not args.no_prefill:
         prefill = bench_prefill(args, dev, stream, timed, hs,

@@ -82,8 +82,9 @@ typedef struct CUstream_st* hs_stream_t;
                                  instead of once per group of up to 4 of its
                                  tokens (fused kernel, the default); results
                                  agree within the stated tolerance */
-#define HS_PREFILL_ROW_GATHER 0x8u  /* prefill (and batch decode on the prefill
-                                 kernels): the down product multiplies, per
+#define HS_PREFILL_ROW_GATHER 0x8u  /* prefill (and batch decode when it runs on
+                                 the prefill kernels, from 51 tokens; ignored
+                                 below): the down product multiplies, per
                                  token tile, only the neurons live for some
                                  token of the tile, packed into dense k-steps
                                  (section "What we do instead"); results

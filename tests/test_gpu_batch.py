@@ -321,3 +321,27 @@ def test_experts_not_stacked_uniformly(B):
         assert e.value.status == hs.HS_ERR_UNSUPPORTED_SHAPE
         torch.cuda.synchronize()
         assert hs.hs_device_status() == hs.HS_OK
+
+
+@pytest.mark.parametrize("B", [8, 64])
+def test_config4_row_gather_flag(cfg4_layer, B):
+    """HS_PREFILL_ROW_GATHER reaches the prefill kernels that a batch of 51 or
+    more tokens runs on (same oracle bar, the same live sets, the same bits as
+    the prefill entry point called with the flag); below 51 tokens it is
+    ignored (the same bits as without it)."""
+    L, dl = cfg4_layer
+    X, LG = synth.tokens(0, "cfg4", B, B)
+    G = hs.HS_PREFILL_ROW_GATHER
+    y, yf, d = check_batch(L, dl, X, LG, 6, f"config 4 B={B} row gather flag", flips_allowed=8, flags=G)
+    y0, yf0, d0 = run_batch(dl, X, LG)
+    assert torch.equal(d["live_mask"], d0["live_mask"])
+    if on_prefill_kernels(B):
+        T, H = X.shape
+        ws = torch.zeros(dl.prefill_workspace_size(T), dtype=torch.uint8, device="cuda")
+        yp = torch.empty((T, H), dtype=torch.bfloat16, device="cuda")
+        yfp = torch.empty((T, H), dtype=torch.float32, device="cuda")
+        hs.hs_moe_prefill(dl.c, X.cuda(), LG.cuda(), T, yp, yfp, G, None, ws)
+        torch.cuda.synchronize()
+        assert np.array_equal(yf, yfp.cpu().double().numpy()) and torch.equal(y, yp.cpu())
+    else:
+        assert np.array_equal(yf, yf0) and torch.equal(y, y0)
