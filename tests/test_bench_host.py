@@ -53,3 +53,24 @@ def test_all_cores_oracle_timing_spawns_one_process_per_core():
     s, n_proc, n_dec = bench.time_oracle_all_cores(0.1, reps=1, n_layers=1)
     assert n_proc == len(os.sched_getaffinity(0)) and n_dec == n_proc
     assert 0 < s < 60
+
+
+def test_union_fractions_by_hand():
+    """Two routed experts (one 64-neuron group each, top-1), one shared
+    group: expert 0 has tokens 0, 1, 2 (live neurons {0,1}, {1,2}, {40}),
+    expert 1 has token 3 (live {63}); the shared group's tokens have live
+    sets {0}, {0}, {5}, {6}.  Tiles of 2 tokens: expert 0's tiles have
+    unions {0,1,2} and {40}, expert 1's {63}: (3 + 1 + 1) / 3 / 64; the
+    shared tiles {0} and {5,6}: (1 + 2) / 2 / 64.  Tiles of 128: one tile
+    per expert: (4 + 1) / 2 / 64 routed, 3 / 64 shared."""
+    import numpy as np
+    idx = np.array([[0], [0], [0], [1]], dtype=np.int32)
+    bit = lambda *ns: sum(1 << n for n in ns)
+    shared = [bit(0), bit(0), bit(5), bit(6)]
+    routed = [bit(0, 1), bit(1, 2), bit(40), bit(63)]
+    words = np.array([[s, r] for s, r in zip(shared, routed)], dtype=np.uint64).view(np.int64)
+    out = bench.union_fractions(idx, words, 64, 64, tiles=(2, 128))
+    assert out["tile2"]["routed"] == round((3 + 1 + 1) / 3 / 64, 4)
+    assert out["tile2"]["shared"] == round((1 + 2) / 2 / 64, 4)
+    assert out["tile128"]["routed"] == round((4 + 1) / 2 / 64, 4)
+    assert out["tile128"]["shared"] == round(3 / 64, 4)
