@@ -1258,6 +1258,32 @@ __global__ void __launch_bounds__(256, 2) batch_fused_kernel(const __grid_consta
 // live-row counts (the union over an expert's units).
 constexpr int kSmallMaxBatch = 8;
 
+// x_group_load with the group's eight 16-byte chunks read in an order rotated by the group
+// index: the threads of a warp read different groups 128 bytes apart, so in the natural order
+// every load of the warp falls on the same four banks.  The chunks are then rotated back into
+// their natural registers (three select stages), so the values are exactly x_group_load's.
+__device__ __forceinline__ void x_group_load_staggered(const uint16_t* x_s, int gc, uint32_t (&w)[4][8]) {
+    const uint4* src = reinterpret_cast<const uint4*>(x_s + 64 * gc);
+    const int r = gc & 7;
+    uint4 v[8];
+#pragma unroll
+    for (int c = 0; c < 8; ++c) v[c] = src[(c + r) & 7];   // slot c holds chunk (c + r) % 8
+#pragma unroll
+    for (int st = 0; st < 3; ++st) {                       // rotate right by r: chunk k = slot (k - r) % 8
+        const bool b = (r >> st) & 1;
+        uint4 nv[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) nv[i] = b ? v[(i - (1 << st) + 8) & 7] : v[i];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) v[i] = nv[i];
+    }
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+        w[q][0] = v[2 * q].x; w[q][1] = v[2 * q].y; w[q][2] = v[2 * q].z; w[q][3] = v[2 * q].w;
+        w[q][4] = v[2 * q + 1].x; w[q][5] = v[2 * q + 1].y; w[q][6] = v[2 * q + 1].z; w[q][7] = v[2 * q + 1].w;
+    }
+}
+
 struct SmallTables {
     int topi[kSmallMaxBatch][kMaxTopK];
     float topw[kSmallMaxBatch][kMaxTopK];
@@ -1426,7 +1452,7 @@ __global__ void __launch_bounds__(256, 2) batch_small_kernel(const __grid_consta
     XFixed xf = {};
     if (role.active && xok) {
         uint32_t xw[4][8];
-        x_group_load(x_s + (size_t)pick(ut.tok, role.tk) * H, role.gc, xw);
+        x_group_load_staggered(x_s + (size_t)pick(ut.tok, role.tk) * H, role.gc, xw);
         x_group_fixed(xw, xf);
     }
     fence_proxy_async_smem();  // the reads of x come before the copies that overwrite them
