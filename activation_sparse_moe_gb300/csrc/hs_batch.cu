@@ -192,22 +192,18 @@ __device__ __noinline__ void batch_plan(const LayerParams& P, const BatchIO& io)
 
 // ------------------------------------------------------------------ route
 __global__ void __launch_bounds__(256) batch_route_kernel(const __grid_constant__ LayerParams P, const BatchIO io) {
-    __shared__ __align__(16) int s_idx[kMaxTopK];
-    __shared__ __align__(16) float s_w[kMaxTopK];
     pdl_wait();
     pdl_trigger();
     const int b = blockIdx.x, t = threadIdx.x;
     const int K = P.top_k, E = P.n_routed, H = P.hidden, G = H / 64;
     if (t < 32) {
-        warp_topk_softmax(io.logits + (size_t)b * E, E, K, s_idx, s_w);
-        __syncwarp();
-        if (t < K) {
+        const TopkPick pk = warp_topk_softmax(io.logits + (size_t)b * E, E, K, io.topk_idx + (size_t)b * K,
+                                              io.topk_w + (size_t)b * K);
+        if (t < K) {   // lane j holds choice j
             const int p = b * K + t;
-            io.topk_idx[p] = s_idx[t];
-            io.topk_w[p] = s_w[t];
-            atomicAdd(&io.meta->cnt[s_idx[t]], 1);
-            if (io.dbg_topk_idx) io.dbg_topk_idx[p] = s_idx[t];
-            if (io.dbg_topk_w) io.dbg_topk_w[p] = s_w[t];
+            atomicAdd(&io.meta->cnt[pk.idx], 1);
+            if (io.dbg_topk_idx) io.dbg_topk_idx[p] = pk.idx;
+            if (io.dbg_topk_w) io.dbg_topk_w[p] = pk.w;
         }
     }
     // the token's fixed-point x table (read by every up unit that has this token)
@@ -1352,7 +1348,7 @@ __global__ void __launch_bounds__(256, 2) batch_small_kernel(const __grid_consta
                 int e = -1, before = 0;
 #pragma unroll
                 for (int w = 0; w < kMaxRouted / 32; ++w) {
-                    uint32_t m = __reduce_or_sync(0xffffffffu, (ei >= 0 && (ei >> 5) == w) ? 1u << (ei & 31) : 0u);
+                    uint32_t m = warp_or_b32((ei >= 0 && (ei >> 5) == w) ? 1u << (ei & 31) : 0u);
                     const int c = __popc(m);
                     if (e < 0 && j < before + c) {
                         for (int i = 0; i < j - before; ++i) m &= m - 1;
@@ -1403,7 +1399,7 @@ __global__ void __launch_bounds__(256, 2) batch_small_kernel(const __grid_consta
                 const int ee = (kMaxRouted / 32) * lane + i;
                 if (ee < E && st->off[ee] <= j && j < st->off[ee + 1]) e = ee;
             }
-            e = __reduce_max_sync(0xffffffffu, e);
+            e = warp_max_s32(e);
             if (lane == 0) {
                 st->e = e;
                 st->off[0] = e >= 0 ? j - st->off[e] : 0;  // the token group within the expert
@@ -1562,8 +1558,8 @@ __global__ void __launch_bounds__(256) batch_fused_reduce_kernel(const __grid_co
                 ng += (a | c) != 0u;
             }
         }
-        n = __reduce_add_sync(0xffffffffu, (unsigned)n);
-        ng = __reduce_add_sync(0xffffffffu, (unsigned)ng);
+        n = (int)warp_add_u32((unsigned)n);
+        ng = (int)warp_add_u32((unsigned)ng);
         if (lane == 0) { part[p][0] = __int_as_float(n); part[p][1] = __int_as_float(ng); }
         __syncthreads();
         if (t == 0) {

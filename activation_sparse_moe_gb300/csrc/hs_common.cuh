@@ -26,6 +26,34 @@ constexpr unsigned long long kWaitLimitCycles = 2000000000ull;  // ~1 s at 2 GHz
 // up.  Each .cu file has its own copy and a host function that reads it.
 static __device__ unsigned int g_status = 0;
 
+// Warp-wide reductions over all 32 lanes (redux.sync), as volatile asm: each
+// executes exactly where it stands in the program, with the full warp.
+__device__ __forceinline__ uint32_t warp_max_u32(uint32_t v) {
+    uint32_t r;
+    asm volatile("redux.sync.max.u32 %0, %1, 0xffffffff;" : "=r"(r) : "r"(v));
+    return r;
+}
+__device__ __forceinline__ uint32_t warp_min_u32(uint32_t v) {
+    uint32_t r;
+    asm volatile("redux.sync.min.u32 %0, %1, 0xffffffff;" : "=r"(r) : "r"(v));
+    return r;
+}
+__device__ __forceinline__ int warp_max_s32(int v) {
+    int r;
+    asm volatile("redux.sync.max.s32 %0, %1, 0xffffffff;" : "=r"(r) : "r"(v));
+    return r;
+}
+__device__ __forceinline__ uint32_t warp_or_b32(uint32_t v) {
+    uint32_t r;
+    asm volatile("redux.sync.or.b32 %0, %1, 0xffffffff;" : "=r"(r) : "r"(v));
+    return r;
+}
+__device__ __forceinline__ uint32_t warp_add_u32(uint32_t v) {
+    uint32_t r;
+    asm volatile("redux.sync.add.u32 %0, %1, 0xffffffff;" : "=r"(r) : "r"(v));
+    return r;
+}
+
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
     return static_cast<uint32_t>(__cvta_generic_to_shared(p));
 }
@@ -138,8 +166,6 @@ __device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t by
         : "memory");
 }
 
-// Programmatic dependent launch: wait for the preceding grid's memory, and let
-// the next grid start launching.  Both are no-ops without the launch attribute.
 // 16-byte global -> shared copy through L2 (cp.async), with an L2 cache policy;
 // both addresses 16-byte aligned.
 __device__ __forceinline__ void cp_async16_hint(void* dst, const void* src, uint64_t policy) {
@@ -164,6 +190,8 @@ __device__ __forceinline__ void prefetch_l2_span(const void* p, int bytes, int l
     for (int off = 128 * lane; off < bytes; off += 32 * 128) prefetch_l2(c + off);
 }
 
+// Programmatic dependent launch: wait for the preceding grid's memory, and let
+// the next grid start launching.  Both are no-ops without the launch attribute.
 __device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 __device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
 

@@ -51,8 +51,17 @@ __device__ __forceinline__ ExpertPtrs routed_ptrs(const LayerParams& P, int e) {
 // 32-bit key (-0 taken as +0).  Lane l sorts its keys l, l+32, l+64, l+96
 // (key descending, index ascending); then k rounds of a warp-wide maximum of
 // the lanes' heads (redux.sync), the lowest index among the lanes that hold
-// it (a second redux), and a pop by the winning lane.  Lane 0 writes idx[k]
-// and w[k].
+// it (a second redux), and a pop by the winning lane.  Every lane then forms
+// the softmax, and lane j < k stores choice j (idx[j], w[j]) and returns it.
+// The whole routine is straight-line code for every lane (the pop is a
+// select; no block runs on one lane only): an earlier form in which lane 0
+// alone stored all k choices gave -1 for the 8th index at k = 8 in kernels
+// whose other lanes then read the choices back, though not elsewhere.
+
+struct TopkPick {
+    int idx;    // expert of this lane's choice (lanes >= k: -1)
+    float w;    // its softmax weight (lanes >= k: 0)
+};
 
 __device__ __forceinline__ uint32_t topk_key(float f) {
     const uint32_t b = __float_as_uint(f + 0.f);   // -0 -> +0
@@ -72,7 +81,7 @@ __device__ __forceinline__ void topk_cx(uint32_t (&k)[4], int (&id)[4], int a, i
     id[a] = sw ? ib : ia; id[b] = sw ? ia : ib;
 }
 
-__device__ inline void warp_topk_softmax(const float* __restrict__ logits, int n, int k, int* idx, float* w) {
+__device__ inline TopkPick warp_topk_softmax(const float* __restrict__ logits, int n, int k, int* idx, float* w) {
     const int lane = threadIdx.x & 31;
     uint32_t key[4];
     int id[4];
@@ -90,30 +99,35 @@ __device__ inline void warp_topk_softmax(const float* __restrict__ logits, int n
     for (int r = 0; r < kMaxTopK; ++r) {
         sk[r] = 0u;
         si[r] = 0;
-        if (r < k) {
-            const uint32_t mx = __reduce_max_sync(0xffffffffu, key[0]);
-            const uint32_t win = __reduce_min_sync(0xffffffffu, key[0] == mx ? (uint32_t)id[0] : 0xffffffffu);
+        if (r < k) {   // k is the same for the whole warp
+            const uint32_t mx = warp_max_u32(key[0]);
+            const uint32_t win = warp_min_u32(key[0] == mx ? (uint32_t)id[0] : 0xffffffffu);
             sk[r] = mx;
             si[r] = (int)win;
-            if ((uint32_t)id[0] == win) {   // pop this lane's head
-                key[0] = key[1]; key[1] = key[2]; key[2] = key[3]; key[3] = 0u;
-                id[0] = id[1]; id[1] = id[2]; id[2] = id[3]; id[3] = 4096;
-            }
+            const bool pop = (uint32_t)id[0] == win;   // the winner drops its head
+            key[0] = pop ? key[1] : key[0]; key[1] = pop ? key[2] : key[1]; key[2] = pop ? key[3] : key[2];
+            key[3] = pop ? 0u : key[3];
+            id[0] = pop ? id[1] : id[0]; id[1] = pop ? id[2] : id[1]; id[2] = pop ? id[3] : id[2];
+            id[3] = pop ? 4096 : id[3];
         }
     }
-    if (lane == 0) {
-        const float v0 = topk_value(sk[0]);
-        float ex[kMaxTopK];
-        float den = 0.f;
+    const float v0 = topk_value(sk[0]);
+    float den = 0.f, mine = 0.f;
+    int mine_i = -1;
 #pragma unroll
-        for (int j = 0; j < kMaxTopK; ++j) ex[j] = (j < k) ? expf(topk_value(sk[j]) - v0) : 0.f;
-#pragma unroll
-        for (int j = 0; j < kMaxTopK; ++j) den += ex[j];
-        const float inv = 1.f / den;
-#pragma unroll
-        for (int j = 0; j < kMaxTopK; ++j)
-            if (j < k) { idx[j] = si[j]; w[j] = ex[j] * inv; }
+    for (int j = 0; j < kMaxTopK; ++j) {
+        const float ex = j < k ? expf(topk_value(sk[j]) - v0) : 0.f;
+        den += ex;
+        if (j == lane) { mine = ex; mine_i = si[j]; }
     }
+    TopkPick p{-1, 0.f};
+    if (lane < k) {
+        p.idx = mine_i;
+        p.w = mine * (1.f / den);
+        idx[lane] = p.idx;
+        w[lane] = p.w;
+    }
+    return p;
 }
 
 // ------------------------------------------------------------- up phase

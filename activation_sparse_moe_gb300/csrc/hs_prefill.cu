@@ -110,16 +110,15 @@ __global__ void __launch_bounds__(256) prefill_route_kernel(const __grid_constan
     const int tok = blockIdx.x * 8 + (threadIdx.x >> 5), lane = threadIdx.x & 31;
     if (tok < io.T) {
         const int K = P.top_k;
-        warp_topk_softmax(io.logits + (size_t)tok * P.n_routed, P.n_routed, K, io.idx + (size_t)tok * K,
-                          io.w + (size_t)tok * K);
-        __syncwarp();
-        if (lane < K) {
-            const int e = io.idx[(size_t)tok * K + lane];
+        const TopkPick pk = warp_topk_softmax(io.logits + (size_t)tok * P.n_routed, P.n_routed, K,
+                                              io.idx + (size_t)tok * K, io.w + (size_t)tok * K);
+        if (lane < K) {   // lane j holds choice j
+            const int e = pk.idx;
             atomicAdd(&io.meta->cnt[e], 1);
             atomicAdd(&io.blk_cnt[(tok / kTokBlk) * P.n_routed + e], 1);
             atomicAdd(&io.sb_cnt[(tok / (kTokBlk * kSuperBlk)) * P.n_routed + e], 1);
             if (io.dbg_idx) io.dbg_idx[(size_t)tok * K + lane] = e;
-            if (io.dbg_w) io.dbg_w[(size_t)tok * K + lane] = io.w[(size_t)tok * K + lane];
+            if (io.dbg_w) io.dbg_w[(size_t)tok * K + lane] = pk.w;
         }
     }
 }

@@ -183,7 +183,7 @@ def build_layers(n_layers, p, device, down_row_scales=False):
     from activation_sparse_moe_gb300.layer import DeviceLayer, from_synth_expert, from_synth_stack
     layers = []
     for l in range(n_layers):
-        L = synth.layer_inputs(0, "cfg3", l, p=p, p_shared=synth.shared_live_fraction(0, l), device=device)
+        L = synth.layer_inputs(0, "decode-23layers", l, p=p, p_shared=synth.shared_live_fraction(0, l), device=device)
         dl = DeviceLayer(from_synth_stack(L.up, L.down, L.offsets, device, down_row_scales=down_row_scales),
                          from_synth_expert(L.shared, device, down_row_scales=down_row_scales), top_k=6)
         layers.append(dl)
@@ -198,10 +198,10 @@ def oracle_layer_expert_source(l, p):
 
     def routed(e):
         if e not in cache:
-            cache[e] = synth.gen_expert((0, "cfg3", l, "routed"), synth.N_ROUTED, p=p, index=e)
+            cache[e] = synth.gen_expert((0, "decode-23layers", l, "routed"), synth.N_ROUTED, p=p, index=e)
         return cache[e]
 
-    shared = synth.gen_expert((0, "cfg3", l, "shared"), synth.N_SHARED, p=synth.shared_live_fraction(0, l))
+    shared = synth.gen_expert((0, "decode-23layers", l, "shared"), synth.N_SHARED, p=synth.shared_live_fraction(0, l))
     return routed, shared
 
 
@@ -212,7 +212,7 @@ def time_oracle(n_layers_max, p, budget_s, steps=None):
     import synth
     prepared = []
     for l in range(n_layers_max):
-        x, lg = synth.tokens(0, "cfg3", l, 1)
+        x, lg = synth.tokens(0, "decode-23layers", l, 1)
         routed, shared = oracle_layer_expert_source(l, p)
         idx, _ = oracle.router_topk(lg[0], 6)
         for e in idx:
@@ -247,7 +247,7 @@ def _oracle_all_cores_worker(i, p, n_layers, reps, barrier, queue):
         import synth
         prepared = []
         for l in range(n_layers):
-            x, lg = synth.tokens(0, "cfg3", l, 1)
+            x, lg = synth.tokens(0, "decode-23layers", l, 1)
             routed, shared = oracle_layer_expert_source(l, p)
             idx, _ = oracle.router_topk(lg[0], 6)
             for e in idx:
@@ -306,12 +306,12 @@ def bench_batch(args, dev, stream, timed, bytemodel, hs, hbm_peak_gbs):
     n_layers = 8
     layers = []
     for l in range(n_layers):
-        L = synth.layer_inputs(0, "cfg4", l, p=0.1, p_shared=0.1, dead_frac=0.3, device=dev)
+        L = synth.layer_inputs(0, "batch-dead0.3", l, p=0.1, p_shared=0.1, dead_frac=0.3, device=dev)
         layers.append(DeviceLayer(from_synth_stack(L.up, L.down, L.offsets, dev), from_synth_expert(L.shared, dev), 6))
         del L
     out = {"workload": "moe_decode_batch_1layer_dead0.3_p0.1 (8 distinct layers cycled)", "unit": "us/layer"}
     for B in [int(b) for b in args.batch_sizes.split(",") if b]:
-        xs, lgs = zip(*[synth.tokens(0, "cfg4", 100 * B + l, B) for l in range(n_layers)])
+        xs, lgs = zip(*[synth.tokens(0, "batch-dead0.3", 100 * B + l, B) for l in range(n_layers)])
         X = torch.stack(xs).to(dev)
         LG = torch.stack(lgs).to(dev)
         Y = torch.empty((n_layers, B, 2688), dtype=torch.bfloat16, device=dev)
@@ -366,7 +366,7 @@ def bench_batch(args, dev, stream, timed, bytemodel, hs, hbm_peak_gbs):
 
 
 def bench_expert_down(args, dev, stream, timed, bytemodel, hs, peak):
-    """Configuration 1: hs_expert_down_sparse of one token's h (relu(z)^2 with
+    """Single-expert sparse down: hs_expert_down_sparse of one token's h (relu(z)^2 with
     z ~ N(Phi^-1(0.1), 1), its own draw per copy) through 512 distinct routed
     experts' 2688 x 1856 down projections (1.44 GB of weights, far above L2),
     called back to back in one CUDA graph; per-call time and the bandwidth on
@@ -378,13 +378,13 @@ def bench_expert_down(args, dev, stream, timed, bytemodel, hs, peak):
     codes = torch.empty((n_copies, N, H // 2), dtype=torch.uint8, device=dev)
     sb = torch.empty((n_copies, N // 64, H), dtype=torch.int32, device=dev)
     for l in range(n_copies // 128):
-        _, down = synth.gen_routed_stack((0, "cfg1", l), 128, N, H, device=dev)
+        _, down = synth.gen_routed_stack((0, "expert-down", l), 128, N, H, device=dev)
         ds, db = down.scale.view(torch.int16), down.bias.view(torch.int16)
         for e in range(128):
             i = 128 * l + e
             hs.hs_repack_down_nm(down.codes[e], ds[e], db[e], H, N, codes[i], sb[i])
         del down
-    Hs = torch.stack([synth.config1_h(i, N, 0.1) for i in range(n_copies)]).to(dev)
+    Hs = torch.stack([synth.expert_down_h(i, N, 0.1) for i in range(n_copies)]).to(dev)
     Y = torch.empty((n_copies, H), dtype=torch.bfloat16, device=dev)
     cnt = torch.zeros(n_copies, dtype=torch.int32, device=dev)
     WS = torch.zeros(hs.hs_expert_down_sparse_workspace_size(N, H), dtype=torch.uint8, device=dev)  # counters start at 0
@@ -411,7 +411,7 @@ def bench_expert_down(args, dev, stream, timed, bytemodel, hs, peak):
     ms_d, _ = timed(capture(hs.HS_FORCE_DENSE), K, 3, repeats=3)
     us, us_d = ms * 1e3 / (K * n_copies), ms_d * 1e3 / (K * n_copies)
     gbs = req / n_copies / (us * 1e-6) / 1e9
-    return {"workload": "expert_down_sparse_1tok_512copies_p0.1 (configuration 1: 2688x1856 W4 neuron-major)",
+    return {"workload": "expert_down_sparse_1tok_512copies_p0.1 (2688x1856 W4 neuron-major)",
             "unit": "us/call", "us_per_call": round(us, 3), "required_KB_per_call": round(req / n_copies / 1e3, 1),
             "live_rows_per_call": round(float(live_rows.mean()), 1),
             "live_groups_per_call": round(float(live_groups.mean()), 2),
@@ -428,7 +428,7 @@ def bench_router(args, layers, X, dev, stream, timed, hs, peak):
     import torch
     import synth
     n, H, E = len(layers), 2688, 128
-    W = torch.stack([synth.router_weights(0, "cfg3-router", l) for l in range(n)]).to(dev)
+    W = torch.stack([synth.router_weights(0, "decode-23layers-router", l) for l in range(n)]).to(dev)
     LGr = torch.empty((n, E), dtype=torch.float32, device=dev)
     Y = torch.empty((n, H), dtype=torch.bfloat16, device=dev)
     WS = torch.zeros(max(dl.workspace_size(1) for dl in layers), dtype=torch.uint8, device=dev)
@@ -497,7 +497,7 @@ def bench_row_scales(args, X, LG, dev, stream, timed, bytemodel, hs, peak):
 
 
 def bench_p_sweep(args, layers, X, LG, dev, stream, timed, bytemodel, hs, peak):
-    """Configuration 3's live-fraction sweep on the same 23 resident layers: the
+    """The live-fraction sweep on the same 23 resident layers: the
     routed experts' offsets for live fraction p are the p = 0.1 offsets scaled by
     Phi^-1(p) / Phi^-1(0.1) (the calibration off = Phi^-1(p) * ||w|| is linear
     in Phi^-1(p)); the shared expert keeps its own per-layer fraction; p = 1.0 is
@@ -574,10 +574,10 @@ def bench_prefill(args, dev, stream, timed, hs, peaks):
     import synth
     from activation_sparse_moe_gb300.layer import DeviceLayer, from_synth_expert, from_synth_stack
     T, H, NR, NS = 2048, 2688, 1856, 3712
-    L = synth.layer_inputs(0, "cfg5", 0, p=0.1, p_shared=0.1, dead_frac=0.3, device=dev)
+    L = synth.layer_inputs(0, "prefill-2048", 0, p=0.1, p_shared=0.1, dead_frac=0.3, device=dev)
     dl = DeviceLayer(from_synth_stack(L.up, L.down, L.offsets, dev), from_synth_expert(L.shared, dev), 6)
     del L
-    x, lg = synth.tokens(0, "cfg5", 0, T)
+    x, lg = synth.tokens(0, "prefill-2048", 0, T)
     X, LG = x.to(dev), lg.to(dev)
     Y = torch.empty((T, H), dtype=torch.bfloat16, device=dev)
     WS = torch.zeros(dl.prefill_workspace_size(T), dtype=torch.uint8, device=dev)
@@ -644,7 +644,7 @@ def bench_prefill(args, dev, stream, timed, hs, peaks):
     del g_sparse, g_dense, dl
     # our sub-configuration: the same 30% dead, but as whole 64-neuron groups (seeded choice per
     # expert, shared included), so that the tile skip has whole tiles to skip
-    L = synth.layer_inputs(0, "cfg5", 0, p=0.1, p_shared=0.1, dead_frac=0.0, device=dev)
+    L = synth.layer_inputs(0, "prefill-2048", 0, p=0.1, p_shared=0.1, dead_frac=0.0, device=dev)
     rng = np.random.default_rng(5)
     for offs in [L.offsets[e] for e in range(L.offsets.shape[0])] + [L.shared.offset]:
         ng = offs.shape[0] // 64
@@ -702,7 +702,7 @@ def main():
     layers = build_layers(n, args.p, dev)
     xs, lgs = [], []
     for l in range(n):
-        x, lg = synth.tokens(0, "cfg3", l, 1)
+        x, lg = synth.tokens(0, "decode-23layers", l, 1)
         xs.append(x[0])
         lgs.append(lg[0])
     X = torch.stack(xs).to(dev)

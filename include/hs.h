@@ -280,8 +280,11 @@ int hs_router_logits(const uint16_t* x_bf16_dev, const uint16_t* w_router_bf16_d
  * of all its tokens' live rows once.  51 tokens or more, without that flag,
  * when the routed experts are stacked as hs_moe_prefill requires: the
  * prefill's tensor-core products (fp16 operands; its output contract), which
- * dequantise each weight tile once for all of an expert's tokens.  hidden
- * must be a multiple of 128, neurons <= 3712, and the debug h dump is not
+ * dequantise each weight tile once for all of an expert's tokens.  For
+ * batch > 1: hidden must be a multiple of 128; the CUDA-core kernels (2..50
+ * tokens, or up to 64 as above) take experts of at most 3712 neurons (more:
+ * HS_ERR_UNSUPPORTED_SHAPE, and the workspace size is 0 unless the prefill
+ * kernels apply), the prefill kernels up to 4096; the debug h dump is not
  * available (HS_ERR_INVALID_ARG).  Deterministic; on the CUDA-core kernels
  * without HS_BATCH_EXPERT_UNION each token's y equals, bit for bit, a batch-1
  * call on that token alone.

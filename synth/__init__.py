@@ -7,4 +7,4 @@ contains none of the method's arithmetic (no up-projection, no ReLU^2 of a
 model activation, no down-projection, no routing).
 """
 from .gen import *  # noqa: F401,F403
-from .configs import *  # noqa: F401,F403,E402
+from .workloads import *  # noqa: F401,F403,E402

@@ -21,7 +21,7 @@ integer hash evaluated with torch integer ops, so that the same tensor is
 produced bit for bit on the CPU and on a GPU, and so that any single expert
 can be regenerated without generating the others (its values depend only on
 the stream key and the element index).  Normal draws (activations, logits,
-configuration-1 pre-activations) come from numpy's PCG64 seeded per stream.
+single-expert pre-activations) come from numpy's PCG64 seeded per stream.
 
 Calibration of the live fraction.  Each neuron gets a pre-activation offset
 off_n = Phi^-1(p) * ||w_n||_2 so that, for x ~ N(0, I), P(w_n . x + off_n > 0)
@@ -45,7 +45,7 @@ __all__ = [
     "stream_key", "hash_u32", "random_code_bytes", "random_scales",
     "W4Proj", "Expert", "gen_proj", "gen_expert", "gen_routed_stack", "stack_offsets",
     "code_group_sq_sums", "calibrated_offsets", "dead_mask",
-    "normal_f32", "normal_bf16", "config1_h", "shared_live_fraction",
+    "normal_f32", "normal_bf16", "expert_down_h", "shared_live_fraction",
     "uniform_f64",
 ]
 
@@ -250,9 +250,9 @@ def shared_live_fraction(seed: int, layer: int) -> float:
     return float(uniform_f64((), 0.05, 0.15, seed, "p_shared", layer))
 
 
-def config1_h(seed: int = 0, neurons: int = N_ROUTED, p: float = 0.1) -> torch.Tensor:
+def expert_down_h(seed: int = 0, neurons: int = N_ROUTED, p: float = 0.1) -> torch.Tensor:
     """Input of the single-expert down projection: the squared positive part of
     z ~ N(Phi^-1(p), 1), so that a fraction p of the entries is non-zero (fp32)."""
-    z = _rng(seed, "cfg1", "z").normal(float(ndtri(p)), 1.0, size=neurons)
+    z = _rng(seed, "expert-down", "z").normal(float(ndtri(p)), 1.0, size=neurons)
     h = np.where(z > 0.0, z * z, 0.0)
     return torch.from_numpy(h.astype(np.float32))

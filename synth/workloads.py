@@ -20,7 +20,7 @@ from dataclasses import dataclass
 import numpy as np
 import torch
 
-from .gen import (HIDDEN, N_EXPERTS, N_ROUTED, N_SHARED, Expert, W4Proj, config1_h, dead_mask, gen_expert,
+from .gen import (HIDDEN, N_EXPERTS, N_ROUTED, N_SHARED, Expert, W4Proj, expert_down_h, dead_mask, gen_expert,
                   gen_proj, gen_routed_stack, normal_bf16, normal_f32, stack_offsets)
 
 __all__ = ["LayerInputs", "layer_inputs", "tokens", "router_weights", "single_expert_down"]
@@ -77,5 +77,5 @@ def router_weights(seed: int, tag: str, layer: int, n_experts: int = N_EXPERTS, 
 def single_expert_down(seed: int = 0, neurons: int = N_ROUTED, hidden: int = HIDDEN, p: float = 0.1,
                        device="cpu"):
     """(h fp32 [neurons], down W4Proj in checkpoint layout [hidden][neurons])."""
-    down = gen_proj(hidden, neurons, (seed, "cfg1", "down"), device)
-    return config1_h(seed, neurons, p), down
+    down = gen_proj(hidden, neurons, (seed, "expert-down", "down"), device)
+    return expert_down_h(seed, neurons, p), down

@@ -126,6 +126,28 @@ def test_prefill_argument_errors(lib):
     assert hs.hs_moe_prefill_workspace_size(L, 200) > need
 
 
+def test_batch_decode_shape_limits(lib):
+    """The CUDA-core batch kernels (2..50 tokens) take experts of at most 3712
+    neurons and a hidden size that is a multiple of 128; from 51 tokens the
+    prefill kernels (stacked experts) take up to 4096 neurons."""
+    f = lib.hs_moe_layer_decode
+    A = 0x500000
+    ok = _stacked_layer(neurons=3712)
+    big = _stacked_layer(neurons=4096)
+    for B in (2, 9, 50):
+        assert hs.hs_moe_layer_decode_workspace_size(ok, B) > 0
+        assert hs.hs_moe_layer_decode_workspace_size(big, B) == 0
+        assert f(big.ref, A, A, B, A, None, 0, None, A, 1 << 40, None) == hs.HS_ERR_UNSUPPORTED_SHAPE
+    assert hs.hs_moe_layer_decode_workspace_size(big, 51) == hs.hs_moe_prefill_workspace_size(big, 51) > 0
+    # the same limit on the shared expert
+    ex = [hs.make_expert(0x1000000 + e * 128 * 128, 0x1000000, 0x1000000, 0x1000000, None, 128) for e in range(4)]
+    wide_shared = hs.Layer(ex, hs.make_expert(A, A, A, A, None, 3776), 256, 2)
+    assert hs.hs_moe_layer_decode_workspace_size(wide_shared, 9) == 0
+    assert hs.hs_moe_layer_decode_workspace_size(_stacked_layer(hidden=192), 9) == 0
+    # batch 1 takes the 4096-neuron experts
+    assert hs.hs_moe_layer_decode_workspace_size(big, 1) > 0
+
+
 def test_missing_library_fails_loudly(monkeypatch, tmp_path):
     """Without the built library every call raises: there is no fallback."""
     monkeypatch.setattr(hs, "LIB_PATH", str(tmp_path / "libhs.so"))

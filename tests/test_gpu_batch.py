@@ -2,8 +2,8 @@
 
 "Skipping dead neurons..." sections "Inside a MoE layer" and "Sorted by
 expert": each token routes on its own; the tokens are grouped by expert and
-each expert reads the union of its tokens' live rows.  Configuration 4: batch
-2..64, 30% of every expert's neurons permanently dead, p = 0.1 on the rest.
+each expert reads the union of its tokens' live rows.  The full-size layer at
+batch 2..64, with 30% of every expert's neurons permanently dead, p = 0.1 on the rest.
 """
 import numpy as np
 import pytest
@@ -170,27 +170,27 @@ def test_small_path_every_token_on_the_same_experts(B):
 
 
 @pytest.fixture(scope="module")
-def cfg4_layer():
-    """Configuration 4: full-size layer, 30% permanently dead, p = 0.1 on the rest."""
-    L = synth.layer_inputs(0, "cfg4", 0, p=0.1, p_shared=0.1, dead_frac=0.3, device="cuda")
+def batch_layer():
+    """The full-size layer, 30% permanently dead, p = 0.1 on the rest."""
+    L = synth.layer_inputs(0, "batch-dead0.3", 0, p=0.1, p_shared=0.1, dead_frac=0.3, device="cuda")
     return L, make_layer(L, 6)
 
 
 @pytest.mark.parametrize("B", [2, 3, 4, 6, 8, 16, 32, 64])
-def test_config4_parity(cfg4_layer, B):
-    L, dl = cfg4_layer
-    X, LG = synth.tokens(0, "cfg4", B, B)
-    check_batch(L, dl, X, LG, 6, f"config 4 B={B}", flips_allowed=8)
+def test_batch_layer_parity(batch_layer, B):
+    L, dl = batch_layer
+    X, LG = synth.tokens(0, "batch-dead0.3", B, B)
+    check_batch(L, dl, X, LG, 6, f"batch layer B={B}", flips_allowed=8)
 
 
 @pytest.mark.parametrize("B", [8, 64])
-def test_config4_parity_expert_union_path(cfg4_layer, B):
+def test_batch_layer_parity_expert_union_path(batch_layer, B):
     """HS_BATCH_EXPERT_UNION: every expert reads the union of all its tokens'
     live rows once (banded kernels); same oracle bar, and the union count is
     the same as the default path's."""
-    L, dl = cfg4_layer
-    X, LG = synth.tokens(0, "cfg4", B, B)
-    y1, yf1, d1 = check_batch(L, dl, X, LG, 6, f"config 4 B={B} expert union", flips_allowed=8,
+    L, dl = batch_layer
+    X, LG = synth.tokens(0, "batch-dead0.3", B, B)
+    y1, yf1, d1 = check_batch(L, dl, X, LG, 6, f"batch layer B={B} expert union", flips_allowed=8,
                               flags=hs.HS_BATCH_EXPERT_UNION)
     y2, yf2, d2 = run_batch(dl, X, LG)
     r1, r2 = int(d1["live_rows"].item()), int(d2["live_rows"].item())
@@ -201,9 +201,9 @@ def test_config4_parity_expert_union_path(cfg4_layer, B):
         assert r1 == r2 and g1 == g2
 
 
-def test_config4_dense_flag_and_determinism(cfg4_layer):
-    L, dl = cfg4_layer
-    X, LG = synth.tokens(0, "cfg4", 8, 8)
+def test_batch_layer_dense_flag_and_determinism(batch_layer):
+    L, dl = batch_layer
+    X, LG = synth.tokens(0, "batch-dead0.3", 8, 8)
     y1, yf1, d1 = run_batch(dl, X, LG)
     y2, yf2, d2 = run_batch(dl, X, LG)
     yd, yfd, dd = run_batch(dl, X, LG, flags=hs.HS_FORCE_DENSE)
@@ -220,11 +220,11 @@ def test_config4_dense_flag_and_determinism(cfg4_layer):
     assert int(dud["live_rows"].item()) == ntouched * synth.N_ROUTED + synth.N_SHARED
 
 
-def test_config4_small_path_dense_flag_and_determinism(cfg4_layer):
+def test_batch_layer_small_path_dense_flag_and_determinism(batch_layer):
     """B = 3 (one unit per expert, no route kernel): repeatable, dense flag
     gives the same bits, and each row equals the token decoded alone."""
-    L, dl = cfg4_layer
-    X, LG = synth.tokens(0, "cfg4", 3, 3)
+    L, dl = batch_layer
+    X, LG = synth.tokens(0, "batch-dead0.3", 3, 3)
     y1, yf1, d1 = run_batch(dl, X, LG)
     y2, yf2, d2 = run_batch(dl, X, LG)
     yd, yfd, dd = run_batch(dl, X, LG, flags=hs.HS_FORCE_DENSE)
@@ -270,11 +270,11 @@ def test_graph_capture_equals_eager(B, flags):
     assert hs.hs_device_status() == hs.HS_OK
 
 
-def test_config4_batch64_on_prefill_kernels_dense_flag_and_determinism(cfg4_layer):
+def test_batch64_on_prefill_kernels_dense_flag_and_determinism(batch_layer):
     """B = 64 runs on the prefill's tensor-core kernels: repeatable, and the
     dense flag (no 64-neuron tile skipped) gives the same bits."""
-    L, dl = cfg4_layer
-    X, LG = synth.tokens(0, "cfg4", 64, 64)
+    L, dl = batch_layer
+    X, LG = synth.tokens(0, "batch-dead0.3", 64, 64)
     y1, yf1, d1 = run_batch(dl, X, LG)
     y2, yf2, _ = run_batch(dl, X, LG)
     yd, yfd, _ = run_batch(dl, X, LG, flags=hs.HS_FORCE_DENSE)
@@ -324,15 +324,15 @@ def test_experts_not_stacked_uniformly(B):
 
 
 @pytest.mark.parametrize("B", [8, 64])
-def test_config4_row_gather_flag(cfg4_layer, B):
+def test_batch_layer_row_gather_flag(batch_layer, B):
     """HS_PREFILL_ROW_GATHER reaches the prefill kernels that a batch of 51 or
     more tokens runs on (same oracle bar, the same live sets, the same bits as
     the prefill entry point called with the flag); below 51 tokens it is
     ignored (the same bits as without it)."""
-    L, dl = cfg4_layer
-    X, LG = synth.tokens(0, "cfg4", B, B)
+    L, dl = batch_layer
+    X, LG = synth.tokens(0, "batch-dead0.3", B, B)
     G = hs.HS_PREFILL_ROW_GATHER
-    y, yf, d = check_batch(L, dl, X, LG, 6, f"config 4 B={B} row gather flag", flips_allowed=8, flags=G)
+    y, yf, d = check_batch(L, dl, X, LG, 6, f"batch layer B={B} row gather flag", flips_allowed=8, flags=G)
     y0, yf0, d0 = run_batch(dl, X, LG)
     assert torch.equal(d["live_mask"], d0["live_mask"])
     if on_prefill_kernels(B):

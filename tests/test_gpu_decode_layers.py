@@ -1,11 +1,11 @@
-"""GPU parity of configuration 3 (23 stacked layers, the benchmark's workload).
+"""GPU parity of the 23-layer batch-1 decode stack (the benchmark's workload).
 
 "Skipping dead neurons..." section "Most neurons are dead in every layer": the
-live fraction differs from layer to layer; configuration 3 sweeps the routed
+live fraction differs from layer to layer; the benchmark sweeps the routed
 live fraction p over {0.02, 0.05, 0.1, 0.2, 0.5, 1.0} (1.0 = the dense path)
 with the shared expert's fraction drawn per layer from U(0.05, 0.15).  The
 layers here are built exactly as the benchmark builds them: layer l of seed
-0, tag "cfg3", p_shared from synth.shared_live_fraction, and a sweep point's
+0, tag "decode-23layers", p_shared from synth.shared_live_fraction, and a sweep point's
 routed offsets are the p = 0.1 offsets scaled by Phi^-1(p) / Phi^-1(0.1) (the
 calibration off = Phi^-1(p) * ||w|| is linear in Phi^-1(p)).  Layers 0, 11
 and 22 of the stack are checked against the oracle element by element at the
@@ -35,12 +35,12 @@ def _lib():
 
 
 @pytest.fixture(scope="module", params=LAYERS)
-def cfg3_layer(request):
+def decode_layer(request):
     """Layer l of the benchmark's stack (weights generated on the GPU)."""
     l = request.param
-    L = synth.layer_inputs(0, "cfg3", l, p=0.1, p_shared=synth.shared_live_fraction(0, l), device="cuda")
+    L = synth.layer_inputs(0, "decode-23layers", l, p=0.1, p_shared=synth.shared_live_fraction(0, l), device="cuda")
     dl = make_layer(L, 6)
-    x, lg = synth.tokens(0, "cfg3", l, 1)
+    x, lg = synth.tokens(0, "decode-23layers", l, 1)
     yield l, L, dl, x, lg
     del dl, L
     torch.cuda.empty_cache()
@@ -55,10 +55,10 @@ def at_live_fraction(L, dl, p):
 
 
 @pytest.mark.parametrize("p", [0.02, 0.5])
-def test_config3_sweep_point_parity(cfg3_layer, p):
-    l, L, dl, x, lg = cfg3_layer
+def test_decode_layers_sweep_point_parity(decode_layer, p):
+    l, L, dl, x, lg = decode_layer
     Lp, dlp = at_live_fraction(L, dl, p)
-    y, yf, flips = check_layer(Lp, dlp, x, lg, 6, f"config 3 layer {l} p={p}")
+    y, yf, flips = check_layer(Lp, dlp, x, lg, 6, f"decode layer {l} p={p}")
     assert flips <= 2
     # the routed live fraction follows p (one token: the chosen experts' neurons
     # share the same x, so a layer's fraction scatters around p)
@@ -68,11 +68,11 @@ def test_config3_sweep_point_parity(cfg3_layer, p):
     assert abs(frac - p) < 0.1, (l, p, frac)
 
 
-def test_config3_dense_flag_bit_identical(cfg3_layer):
+def test_decode_layers_dense_flag_bit_identical(decode_layer):
     """p = 1.0 of the sweep is the dense path on the p = 0.1 inputs: the same
     bits as the sparse call, every row read."""
     from activation_sparse_moe_gb300 import hs
-    l, L, dl, x, lg = cfg3_layer
+    l, L, dl, x, lg = decode_layer
     y1, yf1, d1 = run_layer(dl, x, lg)
     yd, yfd, dd = run_layer(dl, x, lg, flags=hs.HS_FORCE_DENSE)
     assert np.array_equal(yf1, yfd) and torch.equal(y1, yd), l

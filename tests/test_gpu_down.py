@@ -72,14 +72,14 @@ def test_repack_matches_oracle_dequant(H, N):
     assert np.array_equal(w_nm, oracle.dequant(down))
 
 
-def test_config1_single_expert_parity():
+def test_single_expert_down_parity():
     """Routed expert 2688x1856, h = relu(z)^2 with about 10% live."""
     h, down = synth.single_expert_down(0)
     codes, sb = repack(down)
     y, yf, cnt, li = run_down(h, codes, sb, 1856, 2688)
     ref = oracle.down_dense(h, down)
-    check_close(yf, ref, "config 1 y_f32")
-    check_bf16_within_one_ulp(y, ref, "config 1 y_bf16", yf)
+    check_close(yf, ref, "single expert y_f32")
+    check_bf16_within_one_ulp(y, ref, "single expert y_bf16", yf)
     check_live_idx(li, h.double().numpy())  # live set exact: h is given
 
 

@@ -105,9 +105,9 @@ def test_no_shared_top1_and_extreme_hidden():
 @pytest.fixture(scope="module")
 def full_layer():
     """One full-size MoE layer at live fraction 0.1 (weights generated on the GPU)."""
-    L = synth.layer_inputs(0, "cfg2", 0, device="cuda")
+    L = synth.layer_inputs(0, "layer-p0.1", 0, device="cuda")
     dl = make_layer(L, 6)
-    x, lg = synth.tokens(0, "cfg2", 0, 1)
+    x, lg = synth.tokens(0, "layer-p0.1", 0, 1)
     return L, dl, x, lg
 
 
@@ -134,7 +134,7 @@ def test_generator_device_independent(full_layer):
     """The GPU-generated stack equals the CPU generator for a sampled expert."""
     L, dl, x, lg = full_layer
     e = 77
-    cpu = synth.gen_expert((0, "cfg2", 0, "routed"), synth.N_ROUTED, index=e)
+    cpu = synth.gen_expert((0, "layer-p0.1", 0, "routed"), synth.N_ROUTED, index=e)
     assert torch.equal(cpu.up.codes, L.up.codes[e].cpu()) and torch.equal(cpu.down.scale, L.down.scale[e].cpu())
     assert torch.equal(cpu.offset, L.offsets[e])
 

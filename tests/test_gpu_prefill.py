@@ -4,7 +4,7 @@
 expert", "Per token sparse, per prompt dense" and "What we do instead": the
 prompt's tokens are routed one by one, grouped by expert, and each expert's
 up projection, ReLU^2 and down projection run as matrix products; the result
-is the per-token MoE layer (oracle.moe_tokens).  Configuration 5: 2048
+is the per-token MoE layer (oracle.moe_tokens).  The full-size prompt: 2048
 tokens, top-6 of 128 plus the shared expert, 30% of every expert's neurons
 permanently dead, p = 0.1 on the rest.
 
@@ -248,34 +248,34 @@ def test_prefill_argument_errors():
 
 
 @pytest.fixture(scope="module")
-def cfg5():
-    """Configuration 5: full-size layer, 30% permanently dead, p = 0.1 on the rest, 2048 tokens."""
-    L = synth.layer_inputs(0, "cfg5", 0, p=0.1, p_shared=0.1, dead_frac=0.3, device="cuda")
-    X, LG = synth.tokens(0, "cfg5", 0, 2048)
+def prefill_2048():
+    """The full-size layer, 30% permanently dead, p = 0.1 on the rest, 2048 tokens."""
+    L = synth.layer_inputs(0, "prefill-2048", 0, p=0.1, p_shared=0.1, dead_frac=0.3, device="cuda")
+    X, LG = synth.tokens(0, "prefill-2048", 0, 2048)
     return L, make_layer(L, 6), X, LG
 
 
 @pytest.mark.parametrize("flags", GATHER, ids=["tiles", "gather"])
-def test_config5_sampled_parity(cfg5, flags):
+def test_prefill_2048_sampled_parity(prefill_2048, flags):
     """Full size, in the launch configuration the bench times; the oracle
     evaluates a sample of tokens one by one (each token's output depends on
     that token alone)."""
-    L, dl, X, LG = cfg5
+    L, dl, X, LG = prefill_2048
     y, yf, dbg = run_prefill(dl, X, LG, flags=flags)
     rng = np.random.default_rng(5)
     sample = np.sort(rng.choice(X.shape[0], size=16, replace=False))
     ref = oracle.moe_tokens(X[sample], LG[sample], L.routed_expert, L.shared, k=6)
     assert np.array_equal(dbg["topk_idx"].numpy()[sample], ref["idx"])
-    rel, mx = check_close(yf[sample], ref["out"], "config 5 sampled y_f32")
-    ulps = check_bf16_rounding(y[sample], yf[sample], ref["out"], "config 5 sampled")
+    rel, mx = check_close(yf[sample], ref["out"], "prefill 2048 sampled y_f32")
+    ulps = check_bf16_rounding(y[sample], yf[sample], ref["out"], "prefill 2048 sampled")
     words = dbg["live_mask"].numpy().view(np.uint64)
     flips = check_token_live_masks(words[sample], X[sample], ref, L.shared, L.routed_expert, synth.N_ROUTED, 6,
-                                   "fp16", "config 5 sampled")
-    print(f"config 5 sampled: rel-L2 {rel:.2e} max-abs/max {mx:.2e} bf16 max ulps {ulps:.0f} flips {flips}")
+                                   "fp16", "prefill 2048 sampled")
+    print(f"prefill 2048 sampled: rel-L2 {rel:.2e} max-abs/max {mx:.2e} bf16 max ulps {ulps:.0f} flips {flips}")
     assert flips <= 4 + len(sample) * (synth.N_SHARED + 6 * synth.N_ROUTED) // 2000
     gather = bool(flags & hs.HS_PREFILL_ROW_GATHER)
-    skipped = check_tiles_from_masks(dl, dbg, "config 5", gather=gather)
-    print(f"config 5 flags={flags}: skipped k-steps {skipped}")
+    skipped = check_tiles_from_masks(dl, dbg, "prefill 2048", gather=gather)
+    print(f"prefill 2048 flags={flags}: skipped k-steps {skipped}")
     if gather:   # the scattered 30% dead rows leave about a quarter of the k-steps out
         assert skipped > int(dbg["tiles"][1]) // 5
     # every (expert, token tile) pair is counted once: 58-tile shared expert + 29 tiles per routed tile
@@ -286,8 +286,8 @@ def test_config5_sampled_parity(cfg5, flags):
     assert np.isfinite(yf).all()
 
 
-def test_config5_dense_flag_equal(cfg5):
-    L, dl, X, LG = cfg5
+def test_prefill_2048_dense_flag_equal(prefill_2048):
+    L, dl, X, LG = prefill_2048
     y1, yf1, d1 = run_prefill(dl, X, LG, masks=False)
     yd, yfd, dd = run_prefill(dl, X, LG, flags=hs.HS_FORCE_DENSE, masks=False)
     assert np.array_equal(yf1, yfd) and torch.equal(y1, yd)
@@ -295,15 +295,15 @@ def test_config5_dense_flag_equal(cfg5):
 
 
 @pytest.mark.parametrize("flags", GATHER, ids=["tiles", "gather"])
-def test_config5_layer_at_max_tokens(cfg5, flags):
+def test_prefill_2048_layer_at_max_tokens(prefill_2048, flags):
     """The largest prompt chunk the library takes (4096 tokens: 24,576 routed
     pairs, 32 shared-expert tiles) on the full-size layer: sampled tokens
     (the first, the last and random ones; each routed expert's last tile is
     ragged) against the oracle, every (expert, token tile) pair counted once."""
-    L, dl, _, _ = cfg5
+    L, dl, _, _ = prefill_2048
     T = 4096
     assert dl.prefill_workspace_size(T) > 0 and dl.prefill_workspace_size(T + 1) == 0
-    X, LG = synth.tokens(0, "cfg5-max", 0, T)
+    X, LG = synth.tokens(0, "prefill-max", 0, T)
     y, yf, dbg = run_prefill(dl, X, LG, flags=flags)
     rng = np.random.default_rng(6)
     sample = np.unique(np.concatenate([[0, T - 1], rng.choice(T, size=10, replace=False)]))
@@ -323,11 +323,11 @@ def test_config5_layer_at_max_tokens(cfg5, flags):
 
 
 @pytest.mark.parametrize("flags", GATHER, ids=["tiles", "gather"])
-def test_config5_repeated_calls_bit_identical(cfg5, flags):
+def test_prefill_2048_repeated_calls_bit_identical(prefill_2048, flags):
     """Determinism under repetition: the full-size prefill called 16 times on
     the same inputs (fresh and reused workspaces alternating) gives the same
     bits every time."""
-    L, dl, X, LG = cfg5
+    L, dl, X, LG = prefill_2048
     T, H = X.shape
     Xc, LGc = X.cuda(), LG.cuda()
     ws_keep = torch.zeros(dl.prefill_workspace_size(T), dtype=torch.uint8, device="cuda")

@@ -98,8 +98,8 @@ def test_rowscale_full_layer_dense_flag_and_determinism():
     """Full-size layer at live fraction 0.1: parity, repeat and dense flag
     give the same bits, and the live counts equal those of the slab layout
     (the up projection is unchanged)."""
-    L = synth.layer_inputs(0, "cfg2", 0, device="cuda")
-    x, lg = synth.tokens(0, "cfg2", 0, 1)
+    L = synth.layer_inputs(0, "layer-p0.1", 0, device="cuda")
+    x, lg = synth.tokens(0, "layer-p0.1", 0, 1)
     dl, y1, yf1, d1 = check_rowscale_layer(L, 6, x, lg, "full")
     y2, yf2, _ = run_rowscale(dl, x, lg)
     yd, yfd, dd = run_rowscale(dl, x, lg, flags=hs.HS_FORCE_DENSE)

@@ -43,3 +43,4 @@ def test_two_cta_kernels_fit_their_register_budget(report):
             found += 1
             assert v["regs"] <= 128, (name, v)
     assert found >= 4
+

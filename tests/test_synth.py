@@ -53,9 +53,9 @@ def test_dead_neurons():
     assert m.sum() == 1114
 
 
-def test_config1_h():
-    h = synth.config1_h(0)
+def test_expert_down_h():
+    h = synth.expert_down_h(0)
     assert h.dtype == torch.float32 and h.shape == (1856,)
     frac = float((h > 0).float().mean())
     assert 0.08 < frac < 0.12
-    assert torch.equal(h, synth.config1_h(0))
+    assert torch.equal(h, synth.expert_down_h(0))

@@ -69,7 +69,7 @@ def _no_alloc(h, codes, sb, N, H):
 
 @pytest.mark.parametrize("H,N", [(synth.HIDDEN, synth.N_ROUTED), (3072, 4096), (256, 65536), (64, 64)])
 def test_no_alloc_matches_workspace_entry_point_twice(H, N):
-    """Configuration 1's shape (one pass, the scratch untouched), experts
+    """The single-expert shape (one pass, the scratch untouched), experts
     wider than one 32-group chunk that keep their partial sums and counters
     in the scratch (4096 neurons x 3072 outputs, and 65536 neurons, the
     largest the scratch holds: 32 chunks per band), and the smallest shape:
@@ -79,7 +79,7 @@ def test_no_alloc_matches_workspace_entry_point_twice(H, N):
     the oracle's live set."""
     if (H, N) == (synth.HIDDEN, synth.N_ROUTED):
         h1, down = synth.single_expert_down(0)
-        h2 = synth.config1_h(7)
+        h2 = synth.expert_down_h(7)
     else:
         down = synth.gen_proj(H, N, (4, "noalloc", H, N))
         rng = np.random.default_rng(H + N)
