@@ -73,6 +73,8 @@ struct BatchMeta {
     int live_grp[kMaxRouted + 1];   // groups with a union live row, same indexing
 };
 
+struct SmallPlan;
+
 struct BatchIO {
     const uint16_t* x;      // [B][H]
     const float* logits;    // [B][E]
@@ -84,7 +86,7 @@ struct BatchIO {
     int* pair_tok;          // [B*K] grouped by expert
     float* pair_w;
     int* pair_slot;         // 1..K
-    uint8_t* xt;            // [B][G][kXfStride] fixed-point x tables
+    uint8_t* xt;            // [B][G][kXfStride] fixed-point x tables ([B][G][128], packed, on the small-batch path)
     float* xsc;             // [B][G][2] (scale, sum) per group
     float* h_pair;          // [B*K][NR] by grouped pair index
     float* h_sh;            // [B][NS]
@@ -98,6 +100,7 @@ struct BatchIO {
     int* live_total;
     int* live_groups;
     uint64_t* dbg_live;     // [B][Ut] live mask (h > 0) per (token, slot group), or null
+    SmallPlan* small_plan;  // small-batch path: the batch's routed entries
     uint64_t* unit_live;    // small-batch path: live mask per unit (else null)
     int* unit_key;          // small-batch path: the unit's expert (n_routed = shared, -1 = none)
     int n_units;
@@ -1254,6 +1257,105 @@ __global__ void __launch_bounds__(256, 2) batch_fused_kernel(const __grid_consta
 // live-row counts (the union over an expert's units).
 constexpr int kSmallMaxBatch = 8;
 
+// One routed entry of the small-batch path: an expert and a group of up to
+// kFTok of its tokens (ascending), with their top-k slots and router weights.
+struct SmallEntry {
+    int e, T;
+    int tok[kFTok], slot[kFTok];
+    float w[kFTok];
+    int pad[2];
+};
+static_assert(sizeof(SmallEntry) == 64, "an entry is 16 words");
+struct SmallPlan {
+    int n_entries;
+    int pad[15];
+    SmallEntry ent[kSmallMaxBatch * kMaxTopK];
+};
+// The unit's per-group (scale, sum) words of its tokens' x tables, then its entry, in the tables region.
+constexpr int kSmallXscBytes = kFTok * (kMaxHidden / 64) * 8;
+static_assert(kSmallXscBytes + (int)sizeof(SmallEntry) <= FusedSmem::kTablesBytes, "small-batch tables exceed their region");
+
+__host__ __device__ inline int small_shared_units(int NGs, int B) { return NGs * ((B + kFTok - 1) / kFTok); }
+
+// The batch's routing, once: top-k and softmax of every token (warp per
+// token), the routed entries (experts ascending, ceil(pairs / kFTok) entries
+// each, an expert's tokens ascending in groups of kFTok), and every token's
+// fixed-point x table in the packed layout.  One CTA.
+__global__ void __launch_bounds__(256) batch_small_plan_kernel(const __grid_constant__ LayerParams P, const BatchIO io) {
+    __shared__ int topi[kSmallMaxBatch][kMaxTopK];
+    __shared__ float topw[kSmallMaxBatch][kMaxTopK];
+    __shared__ int cnt[kMaxRouted];
+    __shared__ int first[kMaxRouted + 1];
+    pdl_wait();
+    pdl_trigger();
+    const int t = threadIdx.x, lane = t & 31, warp = t >> 5;
+    const int B = io.batch, K = P.top_k, E = P.n_routed, H = P.hidden, G = H / 64;
+    SmallPlan* pl = io.small_plan;
+    if (t < kMaxRouted) cnt[t] = 0;
+    if (warp < B) {
+        const TopkPick pk = warp_topk_softmax(io.logits + (size_t)warp * E, E, K, topi[warp], topw[warp]);
+        if (lane < K) {
+            if (io.dbg_topk_idx) io.dbg_topk_idx[warp * K + lane] = pk.idx;
+            if (io.dbg_topk_w) io.dbg_topk_w[warp * K + lane] = pk.w;
+        }
+    }
+    __syncthreads();
+    if (t < B * K) atomicAdd(&cnt[topi[t / K][t % K]], 1);
+    __syncthreads();
+    if (warp == 0) {
+        // first entry of each expert
+        int n[kMaxRouted / 32], sum = 0;
+#pragma unroll
+        for (int i = 0; i < kMaxRouted / 32; ++i) {
+            const int e = (kMaxRouted / 32) * lane + i;
+            n[i] = e < E ? (cnt[e] + kFTok - 1) / kFTok : 0;
+            sum += n[i];
+        }
+        int incl = sum;
+#pragma unroll
+        for (int off = 1; off < 32; off <<= 1) {
+            const int o = __shfl_up_sync(0xffffffffu, incl, off);
+            if (lane >= off) incl += o;
+        }
+        int run = incl - sum;
+#pragma unroll
+        for (int i = 0; i < kMaxRouted / 32; ++i) {
+            const int e = (kMaxRouted / 32) * lane + i;
+            if (e < E) first[e] = run;
+            run += n[i];
+        }
+        if (lane == 31) pl->n_entries = incl;
+    } else {
+        for (int b = 0; b < B; ++b)
+            convert_x_fixed<true>(io.x + (size_t)b * H, G, io.xt + (size_t)b * G * 128, io.xsc + (size_t)b * G * 2, 32);
+    }
+    __syncthreads();
+    if (t < B * K) {
+        // pair (token b, slot s): its rank among its expert's pairs in token order
+        const int b = t / K, s = t % K, e = topi[b][s];
+        int rank = 0;
+        for (int q = 0; q < t; ++q) rank += topi[q / K][q % K] == e;
+        SmallEntry* en = &pl->ent[first[e] + rank / kFTok];
+        const int k = rank % kFTok;
+        en->tok[k] = b;
+        en->slot[k] = s;
+        en->w[k] = topw[b][s];
+        if (k == 0) {
+            en->e = e;
+            en->T = min(kFTok, cnt[e] - rank);
+        }
+    }
+}
+
+// The small-batch kernel's two ways to route a unit.  From kSmallPlanMinBatch
+// tokens a one-CTA kernel routes the batch first (top-k, entries, packed x
+// tables) and each routed unit reads its entry; below, every routed CTA
+// routes the batch itself and converts its x group from the bf16 x (no
+// kernel ahead of it on the dependency chain, which costs more than the
+// redundant routing saves for 2 tokens: 29.9 against 28.4 us per layer).
+constexpr int kSmallPlanMinBatch = 3;
+static_assert(kSmallPlanMinBatch - 1 <= kFTok, "the in-kernel routing takes one entry per distinct expert");
+
 // x_group_load with the group's eight 16-byte chunks read in an order rotated by the group
 // index: the threads of a warp read different groups 128 bytes apart, so in the natural order
 // every load of the warp falls on the same four banks.  The chunks are then rotated back into
@@ -1280,70 +1382,73 @@ __device__ __forceinline__ void x_group_load_staggered(const uint16_t* x_s, int 
     }
 }
 
-struct SmallTables {
-    int topi[kSmallMaxBatch][kMaxTopK];
-    float topw[kSmallMaxBatch][kMaxTopK];
-    int cnt[kMaxRouted];       // pairs per routed expert
-    int off[kMaxRouted + 1];   // first entry of each expert
+// Tables of the in-kernel routing (fewer than kSmallPlanMinBatch tokens).
+struct SmallRouteTables {
+    int topi[kFTok][kMaxTopK];
+    float topw[kFTok][kMaxTopK];
     int tok[kFTok], slot[kFTok];
     float w[kFTok];
     int T, e;
 };
-static_assert(sizeof(SmallTables) <= FusedSmem::kTablesBytes, "small-batch tables exceed their region");
+static_assert(sizeof(SmallRouteTables) <= FusedSmem::kTablesBytes, "small-batch tables exceed their region");
 
-__host__ __device__ inline int small_shared_units(int NGs, int B) { return NGs * ((B + kFTok - 1) / kFTok); }
-
+// One unit per CTA: the shared expert's (64-neuron group, group of up to
+// kFTok tokens), then room for every (routed entry, group).  Shared units
+// start their weight copies before the dependency wait; routed units past
+// the batch's entries leave at once.  The unit's x (packed tables, or the
+// bf16 x of the batch) is copied ahead of its weights into the space of the
+// last weight chunk, which is fetched once every thread holds its x group.
+template <bool kPlanned>
 __global__ void __launch_bounds__(256, 2) batch_small_kernel(const __grid_constant__ LayerParams P, const BatchIO io) {
     extern __shared__ __align__(128) uint8_t smem[];
-    const int H = P.hidden;
+    const int H = P.hidden, G = H / 64;
     const FusedBufs sm = fused_bufs(smem, H);
-    SmallTables* st = reinterpret_cast<SmallTables*>(sm.tables);
     const int t = threadIdx.x, lane = t & 31, warp = t >> 5, u = blockIdx.x;
     const int B = io.batch, K = P.top_k, E = P.n_routed;
     const int NGs = P.shared_neurons / 64, NGr = P.routed_neurons / 64;
     const int NSu = small_shared_units(NGs, B);
     const bool shared = u < NSu;
     uint64_t* xbar = &sm.bars[5];
-    const int nx = (B + kFTok - 1) / kFTok;  // chunks whose space holds x (1 or 2)
-    uint8_t* x_dst = sm.codes + (4 - nx) * 8 * H;
-    const uint16_t* x_s = reinterpret_cast<const uint16_t*>(x_dst);
+    uint8_t* x_dst = sm.codes + 3 * 8 * H;  // chunk 3's space: 4 tokens' packed tables (or bf16 x) fit in it
     if (t == 0) {
         for (int i = 0; i < 6; ++i) mbar_init(&sm.bars[i], 1);
         fence_mbar_init();
-        if (shared) fused_issue_up(sm, P.shared, u % NGs, H, policy_evict_first(), 0, 4 - nx);  // weights only
+        if (shared) fused_issue_up(sm, P.shared, u % NGs, H, policy_evict_first(), 0, 3);  // weights only
     }
     __syncthreads();
     pdl_wait();
     pdl_trigger();
-    if (t == 0) {
-        mbar_arrive_expect_tx(xbar, (uint32_t)(2 * B * H));
-        bulk_g2s(x_dst, io.x, (uint32_t)(2 * B * H), xbar, policy_evict_last());
-    }
-    const bool dbg_topk = io.dbg_topk_idx || io.dbg_topk_w;
-    if (!shared || (u == 0 && dbg_topk)) {
-        if (warp < B) warp_topk_softmax(io.logits + (size_t)warp * E, E, K, st->topi[warp], st->topw[warp]);
-        __syncthreads();
-        if (u == 0 && dbg_topk && t < B * K) {
-            if (io.dbg_topk_idx) io.dbg_topk_idx[t] = st->topi[t / K][t % K];
-            if (io.dbg_topk_w) io.dbg_topk_w[t] = st->topw[t / K][t % K];
-        }
-    }
     UnitTokens ut;
     ExpertPtrs ep;
-    int g, T;
-    if (shared) {
-        const int c = u / NGs;
-        g = u % NGs;
-        T = min(kFTok, B - kFTok * c);
-        ep = P.shared;
+    int g, T, key;
+    if constexpr (!kPlanned) {
+        // the batch's bf16 x, then the routing of every token by every routed CTA
+        SmallRouteTables* st = reinterpret_cast<SmallRouteTables*>(sm.tables);
+        if (t == 0) {
+            mbar_arrive_expect_tx(xbar, (uint32_t)(2 * B * H));
+            bulk_g2s(x_dst, io.x, (uint32_t)(2 * B * H), xbar, policy_evict_last());
+        }
+        const bool dbg_topk = io.dbg_topk_idx || io.dbg_topk_w;
+        if (!shared || (u == 0 && dbg_topk)) {
+            if (warp < B) warp_topk_softmax(io.logits + (size_t)warp * E, E, K, st->topi[warp], st->topw[warp]);
+            __syncthreads();
+            if (u == 0 && dbg_topk && t < B * K) {
+                if (io.dbg_topk_idx) io.dbg_topk_idx[t] = st->topi[t / K][t % K];
+                if (io.dbg_topk_w) io.dbg_topk_w[t] = st->topw[t / K][t % K];
+            }
+        }
+        if (shared) {
+            g = u % NGs;
+            T = B;
+            ep = P.shared;
+            key = E;
 #pragma unroll
-        for (int k = 0; k < kFTok; ++k) { ut.tok[k] = kFTok * c + (k < T ? k : 0); ut.ri[k] = g; ut.w[k] = 1.f; }
-    } else {
-        const int j = (u - NSu) / NGr;
-        g = (u - NSu) % NGr;
-        if (B <= kFTok) {
-            // one entry per distinct expert: the j-th member of the batch's 128-bit expert set
+            for (int k = 0; k < kFTok; ++k) { ut.tok[k] = k < T ? k : 0; ut.ri[k] = g; ut.w[k] = 1.f; }
+        } else {
+            const int j = (u - NSu) / NGr;
+            g = (u - NSu) % NGr;
             if (warp == 0) {
+                // one entry per distinct expert: the j-th member of the batch's expert set, its tokens ascending
                 const int ei = lane < B * K ? st->topi[lane / K][lane % K] : -1;
                 int e = -1, before = 0;
 #pragma unroll
@@ -1356,109 +1461,113 @@ __global__ void __launch_bounds__(256, 2) batch_small_kernel(const __grid_consta
                     }
                     before += c;
                 }
+                int slot = -1;
+                if (e >= 0 && lane < B)
+                    for (int s2 = 0; s2 < K; ++s2)
+                        if (st->topi[lane][s2] == e) slot = s2;
+                const unsigned has = __ballot_sync(0xffffffffu, slot >= 0);
+                const int k = __popc(has & ((1u << lane) - 1u));
+                if (slot >= 0) {
+                    st->tok[k] = lane;
+                    st->slot[k] = slot;
+                    st->w[k] = st->topw[lane][slot];
+                }
                 if (lane == 0) {
-                    st->off[0] = 0;  // the entry is the expert's first (token group 0)
                     st->e = e;
+                    st->T = e >= 0 ? __popc(has) : 0;
                 }
             }
+            __syncthreads();
+            T = st->T;
+            if (T == 0) {
+                if (t == 0) {
+                    io.unit_live[u] = 0;
+                    io.unit_key[u] = -1;
+                    mbar_wait(xbar, 0);  // no copy may be in flight into an exiting CTA
+                }
+                return;
+            }
+            key = st->e;
+            ep = routed_ptrs(P, key);
+#pragma unroll
+            for (int k = 0; k < kFTok; ++k) {
+                ut.tok[k] = k < T ? st->tok[k] : 0;
+                ut.ri[k] = k < T ? NGs + st->slot[k] * NGr + g : 0;
+                ut.w[k] = k < T ? st->w[k] : 0.f;
+            }
+            if (t == 0) fused_issue_up(sm, ep, g, H, policy_evict_first(), 0, 3);
+        }
+    } else {
+        float* xsc_s = reinterpret_cast<float*>(sm.tables);                   // [T][G][2]
+        int* ent_s = reinterpret_cast<int*>(sm.tables + kSmallXscBytes);      // the unit's entry, then n_entries
+        if (shared) {
+            const int c = u / NGs;
+            g = u % NGs;
+            T = min(kFTok, B - kFTok * c);
+            ep = P.shared;
+            key = E;
+#pragma unroll
+            for (int k = 0; k < kFTok; ++k) { ut.tok[k] = kFTok * c + (k < T ? k : 0); ut.ri[k] = g; ut.w[k] = 1.f; }
         } else {
-        // pairs per expert, then each expert's first entry (ceil(pairs / kFTok) entries each)
-        for (int e = t; e < E; e += blockDim.x) st->cnt[e] = 0;
-        __syncthreads();
-        if (t < B * K) atomicAdd(&st->cnt[st->topi[t / K][t % K]], 1);
-        __syncthreads();
-        if (warp == 0) {
-            int n[kMaxRouted / 32], sum = 0;
-#pragma unroll
-            for (int i = 0; i < kMaxRouted / 32; ++i) {
-                const int e = (kMaxRouted / 32) * lane + i;
-                n[i] = e < E ? (st->cnt[e] + kFTok - 1) / kFTok : 0;
-                sum += n[i];
+            const int j = (u - NSu) / NGr;  // < B * K: the plan holds room for every pair
+            g = (u - NSu) % NGr;
+            const SmallPlan* pl = io.small_plan;
+            if (t < 16) ent_s[t] = __ldcg(reinterpret_cast<const int*>(&pl->ent[j]) + t);
+            if (t == 16) ent_s[16] = __ldcg(&pl->n_entries);
+            __syncthreads();
+            const SmallEntry* en = reinterpret_cast<const SmallEntry*>(ent_s);
+            T = j < ent_s[16] ? en->T : 0;
+            if (T == 0) {  // no copy was issued
+                if (t == 0) {
+                    io.unit_live[u] = 0;
+                    io.unit_key[u] = -1;
+                }
+                return;
             }
-            int incl = sum;
+            key = en->e;
+            ep = routed_ptrs(P, key);
 #pragma unroll
-            for (int off = 1; off < 32; off <<= 1) {
-                const int o = __shfl_up_sync(0xffffffffu, incl, off);
-                if (lane >= off) incl += o;
-            }
-            int run = incl - sum;
-#pragma unroll
-            for (int i = 0; i < kMaxRouted / 32; ++i) {
-                const int e = (kMaxRouted / 32) * lane + i;
-                if (e < E) st->off[e] = run;
-                run += n[i];
-            }
-            if (lane == 31) st->off[E] = incl;
-        }
-        __syncthreads();
-        if (warp == 0) {
-            // this CTA's entry: the expert whose entries cover j, and its token group
-            int e = -1;
-#pragma unroll
-            for (int i = 0; i < kMaxRouted / 32; ++i) {
-                const int ee = (kMaxRouted / 32) * lane + i;
-                if (ee < E && st->off[ee] <= j && j < st->off[ee + 1]) e = ee;
-            }
-            e = warp_max_s32(e);
-            if (lane == 0) {
-                st->e = e;
-                st->off[0] = e >= 0 ? j - st->off[e] : 0;  // the token group within the expert
+            for (int k = 0; k < kFTok; ++k) {
+                ut.tok[k] = k < T ? en->tok[k] : 0;
+                ut.ri[k] = k < T ? NGs + en->slot[k] * NGr + g : 0;
+                ut.w[k] = k < T ? en->w[k] : 0.f;
             }
         }
-        }
-        __syncwarp();
-        if (warp == 0) {
-            // the expert's tokens in ascending order; the entry's group of up to kFTok of them
-            const int e = st->e, h = st->off[0];
-            int slot = -1;
-            if (e >= 0 && lane < B)
-                for (int s2 = 0; s2 < K; ++s2)
-                    if (st->topi[lane][s2] == e) slot = s2;
-            const unsigned has = __ballot_sync(0xffffffffu, slot >= 0);  // the expert's tokens, ascending
-            const int k = __popc(has & ((1u << lane) - 1u)) - kFTok * h;
-            if (slot >= 0 && k >= 0 && k < kFTok) {
-                st->tok[k] = lane;
-                st->slot[k] = slot;
-                st->w[k] = st->topw[lane][slot];
+        if (t == 0) {
+            // the unit's x tables first (they gate the dot products), then its weights
+            mbar_arrive_expect_tx(xbar, (uint32_t)(T * G * (128 + 8)));
+            for (int k = 0; k < T; ++k) {
+                const int b = ut.tok[k];
+                bulk_g2s(x_dst + (size_t)k * G * 128, io.xt + (size_t)b * G * 128, (uint32_t)G * 128, xbar,
+                         policy_evict_last());
+                bulk_g2s(xsc_s + (size_t)k * G * 2, io.xsc + (size_t)b * G * 2, (uint32_t)G * 8, xbar,
+                         policy_evict_last());
             }
-            if (lane == 0) st->T = e >= 0 ? min(kFTok, max(0, __popc(has) - kFTok * h)) : 0;
-        }
-        __syncthreads();
-        T = st->T;
-        if (T == 0) {
-            if (t == 0) {
-                io.unit_live[u] = 0;
-                io.unit_key[u] = -1;
-                mbar_wait(xbar, 0);  // no copy may be in flight into an exiting CTA
-            }
-            return;
-        }
-        ep = routed_ptrs(P, st->e);
-#pragma unroll
-        for (int k = 0; k < kFTok; ++k) {
-            ut.tok[k] = k < T ? st->tok[k] : 0;
-            ut.ri[k] = k < T ? NGs + st->slot[k] * NGr + g : 0;
-            ut.w[k] = k < T ? st->w[k] : 0.f;
+            if (!shared) fused_issue_up(sm, ep, g, H, policy_evict_first(), 0, 3);
         }
     }
-    if (!shared && t == 0) fused_issue_up(sm, ep, g, H, policy_evict_first(), 0, 4 - nx);
-    // each active thread's x group from shared memory, then the chunks whose space x took
-    const FusedRole role = fused_role(T, H / 64, false);
+    const FusedRole role = fused_role(T, G, false);
     const bool xok = mbar_wait(xbar, 0);
     XFixed xf = {};
     if (role.active && xok) {
-        uint32_t xw[4][8];
-        x_group_load_staggered(x_s + (size_t)pick(ut.tok, role.tk) * H, role.gc, xw);
-        x_group_fixed(xw, xf);
+        if constexpr (kPlanned) {
+            const float* xsc_s = reinterpret_cast<const float*>(sm.tables);
+            load_x_fixed_packed(x_dst + (size_t)role.tk * G * 128, xsc_s + (size_t)role.tk * G * 2, role.gc, xf);
+        } else {
+            uint32_t xw[4][8];
+            x_group_load_staggered(reinterpret_cast<const uint16_t*>(x_dst) + (size_t)pick(ut.tok, role.tk) * H,
+                                   role.gc, xw);
+            x_group_fixed(xw, xf);
+        }
     }
-    fence_proxy_async_smem();  // the reads of x come before the copies that overwrite them
+    fence_proxy_async_smem();  // the reads of x come before the copy that overwrites them
     if (!__syncthreads_and(xok)) {
         // a wait gave up (the error word is set): the chunks already requested land before the CTA leaves
         if (t == 0)
-            for (int i = 0; i < 4 - nx; ++i) mbar_wait(&sm.bars[i], 0);
+            for (int i = 0; i < 3; ++i) mbar_wait(&sm.bars[i], 0);
         return;
     }
-    if (t == 0) fused_issue_up(sm, ep, g, H, policy_evict_first(), 4 - nx, 4);
+    if (t == 0) fused_issue_up(sm, ep, g, H, policy_evict_first(), 3, 4);
     uint32_t dn_par = 0;
     uint64_t live = 0;
     const int fst = fused_unit<false>(P, io, sm, ep, g, T, ut, xf, xf, 0, dn_par, live);
@@ -1470,7 +1579,7 @@ __global__ void __launch_bounds__(256, 2) batch_small_kernel(const __grid_consta
         write_unit_live_masks(io.dbg_live, P.shared_neurons / 64 + P.top_k * (P.routed_neurons / 64), sm.h_s, T, ut);
     if (t == 0) {
         io.unit_live[u] = live;
-        io.unit_key[u] = shared ? E : st->e;
+        io.unit_key[u] = key;
     }
 }
 
@@ -1609,8 +1718,8 @@ using namespace hs_host;
 
 namespace {
 struct BatchLayout {
-    size_t meta, topk_idx, topk_w, pair_tok, pair_w, pair_slot, xt, xsc, h_pair, h_sh, mask_r, mask_s, unit_live, unit_key,
-        partial, total;
+    size_t meta, topk_idx, topk_w, pair_tok, pair_w, pair_slot, xt, xsc, h_pair, h_sh, mask_r, mask_s, small_plan,
+        unit_live, unit_key, partial, total;
 };
 
 // Grid of the small-batch kernel: the shared expert's units, then room for
@@ -1640,6 +1749,7 @@ BatchLayout batch_layout(const hs_moe_layer* L, int B) {
     l.mask_r = take((size_t)E * (NR / 32) * 4);
     l.mask_s = take((size_t)(NS ? NS / 32 : 1) * 4);
     const int Ut = (NS / 64) + K * (NR / 64);
+    l.small_plan = take(sizeof(hs::SmallPlan));
     l.unit_live = take((size_t)small_units(L, B) * 8);
     l.unit_key = take((size_t)small_units(L, B) * 4);
     // the fused path's partial rows (per token, slot and group) or the banded path's (per token and slot)
@@ -1713,15 +1823,22 @@ int hs_batch_decode(const hs_moe_layer* L, const uint16_t* x, const float* logit
     const int up_smem = hs::BatchUpSmem::total(L->hidden);
     const int dn_smem = hs::BatchDownSmem::total();
     if (batch <= hs::kSmallMaxBatch && !(flags & HS_BATCH_EXPERT_UNION)) {
-        // units numbered before routing: no route kernel, plan or meta block
+        // units are numbered before routing; from kSmallPlanMinBatch tokens one CTA routes the batch first
         const int f_smem = hs::FusedSmem::total(L->hidden);
         const int Ut = (L->shared ? L->shared->neurons / 64 : 0) + L->top_k * (L->routed[0].neurons / 64);
         io.unit_live = reinterpret_cast<uint64_t*>(w + l.unit_live);
         io.unit_key = reinterpret_cast<int*>(w + l.unit_key);
         io.n_units = small_units(L, batch);
-        if (set_smem_attr((const void*)hs::batch_small_kernel, f_smem) != HS_OK) return HS_ERR_CUDA;
+        io.small_plan = reinterpret_cast<hs::SmallPlan*>(w + l.small_plan);
+        const bool planned = batch >= hs::kSmallPlanMinBatch;
+        const void* small = planned ? (const void*)hs::batch_small_kernel<true> : (const void*)hs::batch_small_kernel<false>;
+        if (set_smem_attr(small, f_smem) != HS_OK) return HS_ERR_CUDA;
         if (set_smem_attr((const void*)hs::batch_fused_reduce_kernel, Ut * 128) != HS_OK) return HS_ERR_CUDA;
-        if (launch_pdl(hs::batch_small_kernel, dim3(io.n_units), dim3(256), f_smem, s, P, io) != cudaSuccess)
+        if (planned && launch_pdl(hs::batch_small_plan_kernel, dim3(1), dim3(256), 0, s, P, io) != cudaSuccess)
+            return HS_ERR_CUDA;
+        if ((planned ? launch_pdl(hs::batch_small_kernel<true>, dim3(io.n_units), dim3(256), f_smem, s, P, io)
+                     : launch_pdl(hs::batch_small_kernel<false>, dim3(io.n_units), dim3(256), f_smem, s, P, io)) !=
+            cudaSuccess)
             return HS_ERR_CUDA;
         if (launch_pdl(hs::batch_fused_reduce_kernel, dim3(L->hidden / 32, batch), dim3(256), (size_t)Ut * 128, s, P,
                        io) != cudaSuccess)

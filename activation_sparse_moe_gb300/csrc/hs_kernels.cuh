@@ -200,6 +200,12 @@ __device__ __forceinline__ float x_group_inv(int e) { return __int_as_float((127
 // group of 64, thread q covering quarter q.  The group maximum and sum
 // combine the 4 partials by a fixed 2-level tree (lanes q^1, then q^2).
 // Threads first..blockDim-1 (whole warps) take the work items round-robin.
+// Table layout: kXfStride bytes per group (hE, hO, lE, lO: 32 bytes each,
+// then padding), or with kPacked 128 bytes per group whose eight 16-byte
+// chunks sit rotated by the group index (chunk c of group g at slot
+// (c + g) % 8), so that lanes reading consecutive groups chunk by chunk hit
+// distinct banks without any shuffling of registers (load_x_fixed_packed).
+template <bool kPacked = false>
 __device__ __forceinline__ void convert_x_fixed(const uint16_t* x_s, int G, uint8_t* xf_s, float* xs_s, int first) {
     const int nthr = blockDim.x - first;
     for (int i0 = threadIdx.x - first; i0 - (int)(threadIdx.x & 31) < 4 * G; i0 += nthr) {
@@ -221,11 +227,16 @@ __device__ __forceinline__ void convert_x_fixed(const uint16_t* x_s, int G, uint
         uint32_t hE[2], hO[2], lE[2], lO[2];
         x_quarter_fixed(w, e, hE, hO, lE, lO);
         if (act) {
-            uint8_t* tb = xf_s + grp * kXfStride + 8 * q;
-            *reinterpret_cast<uint2*>(tb) = make_uint2(hE[0], hE[1]);
-            *reinterpret_cast<uint2*>(tb + 32) = make_uint2(hO[0], hO[1]);
-            *reinterpret_cast<uint2*>(tb + 64) = make_uint2(lE[0], lE[1]);
-            *reinterpret_cast<uint2*>(tb + 96) = make_uint2(lO[0], lO[1]);
+            // 8-byte piece at logical offset o = 32 * part + 8 * q of the group's table
+            auto at = [&](int part) -> uint2* {
+                const int o = 32 * part + 8 * q;
+                if (!kPacked) return reinterpret_cast<uint2*>(xf_s + grp * kXfStride + o);
+                return reinterpret_cast<uint2*>(xf_s + grp * 128 + 16 * (((o >> 4) + grp) & 7) + (o & 15));
+            };
+            *at(0) = make_uint2(hE[0], hE[1]);
+            *at(1) = make_uint2(hO[0], hO[1]);
+            *at(2) = make_uint2(lE[0], lE[1]);
+            *at(3) = make_uint2(lO[0], lO[1]);
             if (q == 0) {
                 xs_s[2 * grp] = x_group_inv(e);
                 xs_s[2 * grp + 1] = sm;
@@ -283,6 +294,25 @@ __device__ __forceinline__ void load_x_fixed(const uint8_t* xf_s, const float* x
     }
     xf.inv = xs_s[2 * gc];
     xf.xsum = xs_s[2 * gc + 1];
+}
+
+// Group gc of a packed table (convert_x_fixed<true>): step c reads slot
+// (c + gc) % 8, which holds chunk c, into the registers of chunk c.
+__device__ __forceinline__ void load_x_fixed_packed(const uint8_t* xf_s, const float* xs_s, int gc, XFixed& xf) {
+    const uint4* p = reinterpret_cast<const uint4*>(xf_s + gc * 128);
+    uint4 v[8];
+#pragma unroll
+    for (int c = 0; c < 8; ++c) v[c] = p[(c + gc) & 7];
+#pragma unroll
+    for (int i = 0; i < 2; ++i) {
+        xf.hE[4 * i] = (int)v[i].x; xf.hE[4 * i + 1] = (int)v[i].y; xf.hE[4 * i + 2] = (int)v[i].z; xf.hE[4 * i + 3] = (int)v[i].w;
+        xf.hO[4 * i] = (int)v[2 + i].x; xf.hO[4 * i + 1] = (int)v[2 + i].y; xf.hO[4 * i + 2] = (int)v[2 + i].z; xf.hO[4 * i + 3] = (int)v[2 + i].w;
+        xf.lE[4 * i] = v[4 + i].x; xf.lE[4 * i + 1] = v[4 + i].y; xf.lE[4 * i + 2] = v[4 + i].z; xf.lE[4 * i + 3] = v[4 + i].w;
+        xf.lO[4 * i] = v[6 + i].x; xf.lO[4 * i + 1] = v[6 + i].y; xf.lO[4 * i + 2] = v[6 + i].z; xf.lO[4 * i + 3] = v[6 + i].w;
+    }
+    const float2 sc = reinterpret_cast<const float2*>(xs_s)[gc];
+    xf.inv = sc.x;
+    xf.xsum = sc.y;
 }
 
 // Where the up phase leaves the partial dot product of (row r, group gc): the

@@ -152,7 +152,7 @@ def test_batch_rows_equal_single_token_decode(B, H, E, NR, NS, K):
         assert torch.equal(y[b], y1)
 
 
-@pytest.mark.parametrize("B", [4, 8])
+@pytest.mark.parametrize("B", [2, 4, 8])
 def test_small_path_every_token_on_the_same_experts(B):
     """All tokens route alike: with B = 4 each routed unit holds all 4 tokens;
     with B = 8 each expert's tokens fill two units (token groups of 4), whose

@@ -66,7 +66,7 @@ def _check_each_alone(run, B, K):
     assert int(full["topk_idx"].min()) >= 0 and float(full["topk_w"].min()) > 0.0
 
 
-@pytest.mark.parametrize("B", [1, 4, 16, 64])
+@pytest.mark.parametrize("B", [1, 2, 4, 16, 64])
 def test_decode_router_debug_outputs_each_alone(layer, B):
     X, LG = synth.tokens(7, "t-dbg", B, B, layer.hidden, layer.routed.E)
     _check_each_alone(lambda d: _decode(layer, X, LG, d), B, layer.top_k)
@@ -83,7 +83,7 @@ def _units(dl):
     return dl.shared.N // 64 + dl.top_k * (dl.routed.N // 64)
 
 
-@pytest.mark.parametrize("B", [1, 4, 16, 64])
+@pytest.mark.parametrize("B", [1, 2, 4, 16, 64])
 def test_live_mask_request_does_not_change_results(layer, B):
     """Asking for the live masks selects, on the 9..50-token path, the kernel
     instantiation that writes them; the results are the same bits."""
