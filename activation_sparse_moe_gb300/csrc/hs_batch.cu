@@ -1237,24 +1237,21 @@ __global__ void __launch_bounds__(256, 2) batch_fused_kernel(const __grid_consta
 
 // ------------------------------------------------------------------ small batch (B <= kSmallMaxBatch)
 // With at most 8 tokens the units can be numbered before routing.  A unit
-// holds at most kFTok of an expert's tokens: CTA u < NSu = NGs * ceil(B / 4)
-// is the shared expert's group u % NGs with token group u / NGs; CTA
-// NSu + j * NGr + g is group g of the j-th (routed expert, token group) entry
-// of the batch, experts ascending, each expert's tokens in order (an expert
-// with c tokens has ceil(c / 4) entries), and exits if the batch has fewer
-// entries.  Each routed CTA routes the B tokens itself (one warp per token)
-// and finds its entry (up to 4 tokens: the j-th distinct expert, from a
-// 128-bit set; 5 to 8: from per-expert pair counts and a scan, a step that
-// costs the smaller batches ~0.5 us), so there is no route kernel, plan,
-// ticket or zeroed meta block.  x of the B tokens (2BH bytes,
-// at most 16H) is bulk-copied once into the space of the last one or two
-// 16-row weight chunks right after the wait for the previous kernel and
-// before any routed weights are requested (x read by every thread from L2
-// instead waited behind the weight stream); each thread converts its group
-// from there, and those chunks are fetched after.  The shared expert's CTAs
-// issue their other weight copies before waiting for the previous kernel, as
-// in the batch-1 kernel.  Each unit leaves its live mask and expert for the
-// live-row counts (the union over an expert's units).
+// holds at most kFTok of an expert's tokens: CTA u < NSu is the shared
+// expert's group u % NGs with token group u / NGs (small_shared_tok(B)
+// tokens each); CTA NSu + j * NGr + g is group g of the j-th (routed expert,
+// token group) entry of the batch, experts ascending, each expert's tokens in
+// order (an expert with c tokens has ceil(c / 4) entries), and exits if the
+// batch has fewer entries.  From kSmallPlanMinBatch tokens the entries and
+// the packed fixed-point x tables come from batch_small_plan_kernel; with
+// fewer, each routed CTA routes the tokens itself (one warp per token) and
+// converts its x group from the bf16 x.  The unit's x is bulk-copied into the
+// space of the last 16-row weight chunk before its weights are requested (x
+// read by every thread from L2 instead waited behind the weight stream), and
+// that chunk is fetched once every thread holds its group.  The shared
+// expert's CTAs issue their other weight copies before waiting for the
+// previous kernel, as in the batch-1 kernel.  Each unit leaves its live mask
+// and expert for the live-row counts (the union over an expert's units).
 constexpr int kSmallMaxBatch = 8;
 
 // One routed entry of the small-batch path: an expert and a group of up to
@@ -1275,22 +1272,42 @@ struct SmallPlan {
 constexpr int kSmallXscBytes = kFTok * (kMaxHidden / 64) * 8;
 static_assert(kSmallXscBytes + (int)sizeof(SmallEntry) <= FusedSmem::kTablesBytes, "small-batch tables exceed their region");
 
-__host__ __device__ inline int small_shared_units(int NGs, int B) { return NGs * ((B + kFTok - 1) / kFTok); }
+// Tokens per shared-expert unit of the small-batch kernel: kFTok, except 2
+// for a batch of 3 (a 3-token unit leaves a quarter of its lanes idle: 34.5
+// against 35.5 us per layer; 2-token units measured equal or slower at 4, 5
+// and 8 tokens).
+__host__ __device__ inline int small_shared_tok(int B) { return B == 3 ? 2 : kFTok; }
+__host__ __device__ inline int small_shared_units(int NGs, int B) {
+    return NGs * ((B + small_shared_tok(B) - 1) / small_shared_tok(B));
+}
 
 // The batch's routing, once: top-k and softmax of every token (warp per
 // token), the routed entries (experts ascending, ceil(pairs / kFTok) entries
 // each, an expert's tokens ascending in groups of kFTok), and every token's
-// fixed-point x table in the packed layout.  One CTA.
+// fixed-point x table in the packed layout, converted from a copy of the
+// batch's x in shared memory (one bulk copy, in flight during the top-k).
+// One CTA; dynamic shared memory 2 * B * H bytes.
 __global__ void __launch_bounds__(256) batch_small_plan_kernel(const __grid_constant__ LayerParams P, const BatchIO io) {
+    extern __shared__ __align__(128) uint16_t x_s[];  // [B][H]
     __shared__ int topi[kSmallMaxBatch][kMaxTopK];
     __shared__ float topw[kSmallMaxBatch][kMaxTopK];
     __shared__ int cnt[kMaxRouted];
     __shared__ int first[kMaxRouted + 1];
-    pdl_wait();
-    pdl_trigger();
+    __shared__ __align__(8) uint64_t xbar;
     const int t = threadIdx.x, lane = t & 31, warp = t >> 5;
     const int B = io.batch, K = P.top_k, E = P.n_routed, H = P.hidden, G = H / 64;
     SmallPlan* pl = io.small_plan;
+    if (t == 0) {
+        mbar_init(&xbar, 1);
+        fence_mbar_init();
+    }
+    __syncthreads();
+    pdl_wait();
+    pdl_trigger();
+    if (t == 0) {
+        mbar_arrive_expect_tx(&xbar, (uint32_t)(2 * B * H));
+        bulk_g2s(x_s, io.x, (uint32_t)(2 * B * H), &xbar, policy_evict_last());
+    }
     if (t < kMaxRouted) cnt[t] = 0;
     if (warp < B) {
         const TopkPick pk = warp_topk_softmax(io.logits + (size_t)warp * E, E, K, topi[warp], topw[warp]);
@@ -1325,10 +1342,11 @@ __global__ void __launch_bounds__(256) batch_small_plan_kernel(const __grid_cons
             run += n[i];
         }
         if (lane == 31) pl->n_entries = incl;
-    } else {
+    } else if (mbar_wait(&xbar, 0)) {
         for (int b = 0; b < B; ++b)
-            convert_x_fixed<true>(io.x + (size_t)b * H, G, io.xt + (size_t)b * G * 128, io.xsc + (size_t)b * G * 2, 32);
+            convert_x_fixed<true>(x_s + (size_t)b * H, G, io.xt + (size_t)b * G * 128, io.xsc + (size_t)b * G * 2, 32);
     }
+    if (warp == 0 && lane == 0) mbar_wait(&xbar, 0);  // the copy has landed before the CTA leaves
     __syncthreads();
     if (t < B * K) {
         // pair (token b, slot s): its rank among its expert's pairs in token order
@@ -1393,7 +1411,7 @@ struct SmallRouteTables {
 static_assert(sizeof(SmallRouteTables) <= FusedSmem::kTablesBytes, "small-batch tables exceed their region");
 
 // One unit per CTA: the shared expert's (64-neuron group, group of up to
-// kFTok tokens), then room for every (routed entry, group).  Shared units
+// small_shared_tok(B) tokens), then room for every (routed entry, group).  Shared units
 // start their weight copies before the dependency wait; routed units past
 // the batch's entries leave at once.  The unit's x (packed tables, or the
 // bf16 x of the batch) is copied ahead of its weights into the space of the
@@ -1501,13 +1519,13 @@ __global__ void __launch_bounds__(256, 2) batch_small_kernel(const __grid_consta
         float* xsc_s = reinterpret_cast<float*>(sm.tables);                   // [T][G][2]
         int* ent_s = reinterpret_cast<int*>(sm.tables + kSmallXscBytes);      // the unit's entry, then n_entries
         if (shared) {
-            const int c = u / NGs;
+            const int c = u / NGs, st = small_shared_tok(B);
             g = u % NGs;
-            T = min(kFTok, B - kFTok * c);
+            T = min(st, B - st * c);
             ep = P.shared;
             key = E;
 #pragma unroll
-            for (int k = 0; k < kFTok; ++k) { ut.tok[k] = kFTok * c + (k < T ? k : 0); ut.ri[k] = g; ut.w[k] = 1.f; }
+            for (int k = 0; k < kFTok; ++k) { ut.tok[k] = st * c + (k < T ? k : 0); ut.ri[k] = g; ut.w[k] = 1.f; }
         } else {
             const int j = (u - NSu) / NGr;  // < B * K: the plan holds room for every pair
             g = (u - NSu) % NGr;
@@ -1834,7 +1852,9 @@ int hs_batch_decode(const hs_moe_layer* L, const uint16_t* x, const float* logit
         const void* small = planned ? (const void*)hs::batch_small_kernel<true> : (const void*)hs::batch_small_kernel<false>;
         if (set_smem_attr(small, f_smem) != HS_OK) return HS_ERR_CUDA;
         if (set_smem_attr((const void*)hs::batch_fused_reduce_kernel, Ut * 128) != HS_OK) return HS_ERR_CUDA;
-        if (planned && launch_pdl(hs::batch_small_plan_kernel, dim3(1), dim3(256), 0, s, P, io) != cudaSuccess)
+        const int plan_smem = 2 * batch * L->hidden;
+        if (planned && (set_smem_attr((const void*)hs::batch_small_plan_kernel, plan_smem) != HS_OK ||
+                        launch_pdl(hs::batch_small_plan_kernel, dim3(1), dim3(256), plan_smem, s, P, io) != cudaSuccess))
             return HS_ERR_CUDA;
         if ((planned ? launch_pdl(hs::batch_small_kernel<true>, dim3(io.n_units), dim3(256), f_smem, s, P, io)
                      : launch_pdl(hs::batch_small_kernel<false>, dim3(io.n_units), dim3(256), f_smem, s, P, io)) !=
