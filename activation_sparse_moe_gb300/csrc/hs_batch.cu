@@ -817,14 +817,16 @@ struct FusedOut {
     }
 };
 
-template <int OPT>
+// NT: token slots compiled in (the unit's T <= NT), so that a unit of one or
+// two tokens issues no multiply for the slots it does not have.
+template <int OPT, int NT>
 __device__ __forceinline__ void fused_down(const uint8_t* codes, const uint32_t* sb, const float* h_s, uint64_t live,
                                            const float (&Hsum)[kFTok], const float (&wgt)[kFTok],
                                            const int (&tok)[kFTok], const int (&ri)[kFTok], int T, int rowb, int j,
                                            const FusedOut& out) {
-    float acc[kFTok][OPT];
+    float acc[NT][OPT];
 #pragma unroll
-    for (int k = 0; k < kFTok; ++k)
+    for (int k = 0; k < NT; ++k)
 #pragma unroll
         for (int e = 0; e < OPT; ++e) acc[k][e] = 0.f;
     while (live) {
@@ -845,9 +847,9 @@ __device__ __forceinline__ void fused_down(const uint8_t* codes, const uint32_t*
             w[0] = *reinterpret_cast<const uint32_t*>(row + 6 * j);
             w[1] = *reinterpret_cast<const uint16_t*>(row + 6 * j + 4);
         }
-        float hs[kFTok][5];
+        float hs[NT][5];
 #pragma unroll
-        for (int k = 0; k < kFTok; ++k) {
+        for (int k = 0; k < NT; ++k) {
             const float hn = k < T ? h_s[k * 64 + n] : 0.f;
             hs[k][0] = hn; hs[k][1] = hn * 0.0625f; hs[k][2] = hn * 0.00390625f;
             hs[k][3] = hn * 0.000244140625f; hs[k][4] = hn * 1.52587890625e-05f;
@@ -862,7 +864,7 @@ __device__ __forceinline__ void fused_down(const uint8_t* codes, const uint32_t*
                 const int pos = i < 5 ? i : i - 3;
                 const float q = __uint_as_float((src & (15u << (4 * pos))) | 0x4B000000u) - 8388608.f;
 #pragma unroll
-                for (int k = 0; k < kFTok; ++k)
+                for (int k = 0; k < NT; ++k)
                     if (k < T) acc[k][8 * jj + i] = fmaf(hs[k][pos], q, acc[k][8 * jj + i]);
             }
         }
@@ -876,7 +878,7 @@ __device__ __forceinline__ void fused_down(const uint8_t* codes, const uint32_t*
 #pragma unroll
         for (int e = 0; e < 4; ++e) sbf[e] = half2_to_float2(sbw[e]);
 #pragma unroll
-        for (int k = 0; k < kFTok; ++k) {
+        for (int k = 0; k < NT; ++k) {
             if (k < T) {
                 float r[4];
 #pragma unroll
@@ -1115,10 +1117,15 @@ __device__ __forceinline__ int fused_unit(const LayerParams& P, const BatchIO& i
         } else {
             ok = mbar_wait(&sm.bars[4], dn_par);
             if (ok) {
-                if (H % 48 == 0)
-                    fused_down<12>(codes, sm.sbs, sm.h_s, live, hsum, ut.w, ut.tok, ut.ri, T, rowb, t, out);
-                else
-                    fused_down<16>(codes, sm.sbs, sm.h_s, live, hsum, ut.w, ut.tok, ut.ri, T, rowb, t, out);
+                if (H % 48 == 0) {
+                    if (T == 1) fused_down<12, 1>(codes, sm.sbs, sm.h_s, live, hsum, ut.w, ut.tok, ut.ri, T, rowb, t, out);
+                    else if (T == 2) fused_down<12, 2>(codes, sm.sbs, sm.h_s, live, hsum, ut.w, ut.tok, ut.ri, T, rowb, t, out);
+                    else fused_down<12, kFTok>(codes, sm.sbs, sm.h_s, live, hsum, ut.w, ut.tok, ut.ri, T, rowb, t, out);
+                } else {
+                    if (T == 1) fused_down<16, 1>(codes, sm.sbs, sm.h_s, live, hsum, ut.w, ut.tok, ut.ri, T, rowb, t, out);
+                    else if (T == 2) fused_down<16, 2>(codes, sm.sbs, sm.h_s, live, hsum, ut.w, ut.tok, ut.ri, T, rowb, t, out);
+                    else fused_down<16, kFTok>(codes, sm.sbs, sm.h_s, live, hsum, ut.w, ut.tok, ut.ri, T, rowb, t, out);
+                }
             }
         }
     } else if (any) {
