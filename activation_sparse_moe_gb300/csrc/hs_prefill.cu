@@ -543,7 +543,7 @@ prefill_up_kernel(const __grid_constant__ LayerParams P, const PrefillIO io, con
         const int r = 32 * (warp & 3) + lane;
         const uint32_t trow = tmem_a + ((uint32_t)(32 * (warp & 3)) << 16);
         uint32_t q = 0, nsb = 0;
-        const __half2 k1024 = __floats2half2_rn(1024.f, 1024.f);
+        const __half2 k1024 = __floats2half2_rn(1024.f, 1024.f), k1_16 = __floats2half2_rn(0.0625f, 0.0625f);
         // the next unit's descriptor is loaded one unit ahead (its loads overlap this unit's work)
         UpUnit dnext;
         if ((int)blockIdx.x < U) dnext = up_unit(P, io, ntr, mr, ms, blockIdx.x);
@@ -571,10 +571,10 @@ prefill_up_kernel(const __grid_constant__ LayerParams P, const PrefillIO io, con
                     const int sw = (r >> 1) & 3;
                     const uint4 c0 = *reinterpret_cast<const uint4*>(crow + (((2 * h) ^ sw) << 4));
                     const uint4 c1 = *reinterpret_cast<const uint4*>(crow + (((2 * h + 1) ^ sw) << 4));
-                    const float2 sbv = half2_to_float2(sbr[2 * k + h]);
-                    const __half2 s1 = __floats2half2_rn(sbv.x, sbv.x);
-                    const __half2 s16 = __floats2half2_rn(sbv.x * 0.0625f, sbv.x * 0.0625f);
-                    const __half2 b2 = __floats2half2_rn(sbv.y, sbv.y);
+                    // (scale, bias) in fp16 as stored; scale / 16 is exact (or rounds as an fp32 division would)
+                    const __half2 sbh = *reinterpret_cast<const __half2*>(&sbr[2 * k + h]);
+                    const __half2 s1 = __low2half2(sbh), b2 = __high2half2(sbh);
+                    const __half2 s16 = __hmul2(s1, k1_16);
                     const uint32_t w[8] = {c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w};
 #pragma unroll
                     for (int j = 0; j < 8; ++j) {
@@ -955,7 +955,7 @@ prefill_down_kernel(const __grid_constant__ LayerParams P, const PrefillIO io, c
                                        : r * (kDnBand / 2) + ((qd ^ ((r >> 1) & 3)) << 4) + 4 * (lane >> 3);
             }
         const NibTrLane trc = nib_tr_lane();
-        const __half2 k1024 = __floats2half2_rn(1024.f, 1024.f);
+        const __half2 k1024 = __floats2half2_rn(1024.f, 1024.f), k1_16 = __floats2half2_rn(0.0625f, 0.0625f);
         uint32_t q = 0;
         // the next unit's descriptor is loaded one unit ahead (its loads overlap this unit's work)
         DownUnit dnext;
@@ -973,15 +973,15 @@ prefill_down_kernel(const __grid_constant__ LayerParams P, const PrefillIO io, c
                 const uint8_t* cs = sW + s * Lay::kWSlot;
                 // (scale, bias) of groups A and B; 8-entry block kb takes A if kb < split8
                 const uint32_t* sbw = reinterpret_cast<const uint32_t*>(cs + (kGather ? DownLayoutG::kSlab : DownLayout::kCodes));
-                const float2 sa = half2_to_float2(sbw[32 * qd + lane]);
-                const float2 sbb = kGather ? half2_to_float2(sbw[kDnBand + 32 * qd + lane]) : sa;
+                // (scale, bias) in fp16 as stored; scale / 16 is exact (or rounds as an fp32 division would)
+                const __half2 sha = *reinterpret_cast<const __half2*>(&sbw[32 * qd + lane]);
+                const __half2 shb = kGather ? *reinterpret_cast<const __half2*>(&sbw[kDnBand + 32 * qd + lane]) : sha;
                 const int split8 =
                     kGather ? rowgather::ksd_split8(reinterpret_cast<const uint32_t*>(cs + DownLayoutG::kDesc)[kk & 3])
                             : 8;
-                const __half2 s1a = __floats2half2_rn(sa.x, sa.x), s1b = __floats2half2_rn(sbb.x, sbb.x);
-                const __half2 s16a = __floats2half2_rn(sa.x * 0.0625f, sa.x * 0.0625f);
-                const __half2 s16b = __floats2half2_rn(sbb.x * 0.0625f, sbb.x * 0.0625f);
-                const __half2 b2a = __floats2half2_rn(sa.y, sa.y), b2b = __floats2half2_rn(sbb.y, sbb.y);
+                const __half2 s1a = __low2half2(sha), s1b = __low2half2(shb);
+                const __half2 s16a = __hmul2(s1a, k1_16), s16b = __hmul2(s1b, k1_16);
+                const __half2 b2a = __high2half2(sha), b2b = __high2half2(shb);
                 uint32_t o[32];
 #pragma unroll
                 for (int hh = 0; hh < 2; ++hh) {

@@ -152,12 +152,13 @@ def test_batch_rows_equal_single_token_decode(B, H, E, NR, NS, K):
         assert torch.equal(y[b], y1)
 
 
-@pytest.mark.parametrize("B", [2, 4, 8])
+@pytest.mark.parametrize("B", [2, 3, 4, 5, 7, 8])
 def test_small_path_every_token_on_the_same_experts(B):
-    """All tokens route alike: with B = 4 each routed unit holds all 4 tokens;
-    with B = 8 each expert's tokens fill two units (token groups of 4), whose
-    live masks the counts must unite, and each row still equals its batch-1
-    decode."""
+    """All tokens route alike: with B <= 4 each routed unit holds all the
+    tokens (3 tokens: a unit with an idle token lane, and the shared expert in
+    units of 2 and 1); with 5, 7 and 8 each expert's tokens fill two units
+    (token groups of 4 and the rest), whose live masks the counts must unite,
+    and each row still equals its batch-1 decode."""
     H, E, NR, NS, K = 512, 8, 128, 256, 3
     L = synth.layer_inputs(3, "t-batch-same", 0, E, NR, NS, H, p=0.2, p_shared=0.3)
     X, LG = synth.tokens(3, "t-batch-same", 0, B, H, E)
@@ -236,7 +237,7 @@ def test_batch_layer_small_path_dense_flag_and_determinism(batch_layer):
         assert np.array_equal(yf1[b], yfs) and torch.equal(y1[b], ys)
 
 
-@pytest.mark.parametrize("B,flags", [(1, 0), (3, 0), (8, 0), (16, 0), (8, hs.HS_BATCH_EXPERT_UNION), (56, 0)])
+@pytest.mark.parametrize("B,flags", [(1, 0), (2, 0), (3, 0), (8, 0), (16, 0), (8, hs.HS_BATCH_EXPERT_UNION), (56, 0)])
 def test_graph_capture_equals_eager(B, flags):
     """The layer decode captured in a CUDA graph (as a serving loop replays
     it) gives the eager call's bits, replay after replay, on every path:
