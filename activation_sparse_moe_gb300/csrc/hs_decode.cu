@@ -66,7 +66,7 @@ struct SmemLayout {
         return codes_bytes(hidden) + sb_bytes(hidden, row);
     }
     // misc: h[64] f32, off[64] f32, topk_i[8] i32, topk_w[8] f32, bars[8] u64, live mask (u64, or
-    //       8 bytes of per-warp row bits), hsum f32,
+    //       8 bytes of per-warp row bits), 24 bytes (the slab claim flag i32 at +8),
     // then x[hidden] bf16 (staging), the fixed-point x table [G][144 B] and its
     // per-group (2^(E-15), sum x) pairs [G][2] f32.
     static constexpr int kH = 0, kOff = 256, kTopI = 512, kTopW = kTopI + 32, kBarsOff = kTopW + 32,
@@ -222,9 +222,12 @@ moe_decode_b1_kernel(const __grid_constant__ LayerParams P, const DecodeIO io) {
     const bool dense = (io.flags & HS_FORCE_DENSE) != 0;
     const uint64_t pol = policy_evict_first();
 
+    // set by the first live row of the group, whose thread then requests the slab
+    int* slab_claim = reinterpret_cast<int*>(misc + SmemLayout::kHsum + 8);
     if (t == 0) {
         for (int i = 0; i < SmemLayout::kBars; ++i) mbar_init(&bars[i], 1);
         fence_mbar_init();
+        *slab_claim = 0;
     }
     __syncthreads();
 
@@ -375,6 +378,12 @@ moe_decode_b1_kernel(const __grid_constant__ LayerParams P, const DecodeIO io) {
                 if (kRow)
                     bulk_g2s(reinterpret_cast<uint8_t*>(sb_buf) + (size_t)r * rsb,
                              reinterpret_cast<const uint8_t*>(ep.dn_sb) + ((size_t)g * 64 + r) * rsb, rsb, &bars[4], pol);
+                // the group's slab, requested once, by the first live row's thread (the up scales it
+                // replaces were read before the barrier above)
+                if (!kRow && atomicExch(slab_claim, 1) == 0) {
+                    mbar_expect_tx(&bars[4], (uint32_t)hidden * 4);
+                    bulk_g2s(sb_buf, ep.dn_sb + (size_t)g * hidden, hidden * 4, &bars[4], pol);
+                }
             }
         }
         const unsigned b = __ballot_sync(0xffffffffu, lv);  // bits at lanes 4i
@@ -385,17 +394,10 @@ moe_decode_b1_kernel(const __grid_constant__ LayerParams P, const DecodeIO io) {
             live8[t >> 5] = (uint8_t)m8;
         }
     }
-    // the group's slab is fetched if any neuron fired; the single arrival on
-    // the down barrier comes after every row's expected bytes were added
+    // the single arrival on the down barrier comes after every copy's expected
+    // bytes (rows, and the slab if any neuron fired) were added
     const bool any = __syncthreads_or(lv) != 0;
-    if (t == 0 && any) {
-        if (kRow) {
-            mbar_arrive(&bars[4]);  // the rows' scales came with the rows
-        } else {
-            mbar_arrive_expect_tx(&bars[4], (uint32_t)hidden * 4);
-            bulk_g2s(sb_buf, ep.dn_sb + (size_t)g * hidden, hidden * 4, &bars[4], pol);
-        }
-    }
+    if (t == 0 && any) mbar_arrive(&bars[4]);
     const uint64_t live = *reinterpret_cast<const uint64_t*>(live8);
     const PartialOut out_row{io.partial, io.units, u};
     if (t == 0) io.live_counts[u] = __popcll(live);
