@@ -9,10 +9,12 @@
 // live rows once (the verify step of section "Speculative decoding." reads
 // three rows' activations through the same weights this way).
 //
-// B <= 8 (batch_small_kernel + batch_fused_reduce_kernel): one CTA per
-// (expert, 64-neuron group, up to 4 of the expert's tokens) unit, numbered
-// before routing; every CTA routes the batch itself.  Two kernels, no meta
-// block, programmatic dependent launch in between.
+// B <= 8 (batch_small_kernel + batch_fused_reduce_kernel, from 3 tokens
+// after batch_small_plan_kernel): one CTA per (expert, 64-neuron group, up to
+// 4 of the expert's tokens) unit, numbered before routing; the plan kernel
+// routes the batch once and packs every token's fixed-point x table, and with
+// 2 tokens every CTA routes the batch itself.  No meta block; programmatic
+// dependent launch between the kernels.
 //
 // B <= 64 (batch_route_kernel, batch_fused_kernel, batch_fused_reduce_kernel):
 // routing and planning first, then persistent CTAs take (expert, group, up to
